@@ -1,0 +1,149 @@
+"""Oracle request flow over the radix cache.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+The flow follows "SGLang: Structured LLM Programs for Efficient Inference",
+section "How RadixAttention reuses past work": (1) match the longest prefix,
+(2) lock the matched nodes, (3) prefill only the rest, (4) decode and insert
+(the prompt suffix and the output tokens become nodes), (5) on finish unlock.
+Batching of extends follows the in-batch prefix rule of "SGLang: the tree, and
+the language nobody remembers", section "The scheduler is where the cache is
+won or lost": a request that shares more with a request already queued in the
+batch than with the tree waits, so that its sibling populates the tree first.
+
+Readings (listed in the design doc):
+
+* a wave of requests is processed as: extend batches -> ``decode_steps`` decode
+  steps over the whole wave -> finish of every request in order;
+* requests are taken in order; request ``j`` joins the open batch unless its
+  common prefix with some member exceeds its (side-effect free) tree match, in
+  which case the open batch runs first;
+* a batch runs as: for each member in order ``match_prefix`` on its prompt
+  minus the last token (the last prompt token is always recomputed, so every
+  request has at least one query) and ``inc_lock_ref``; then one allocation of
+  all new tokens, handed out in member order; then extend; then for each member
+  ``insert(prompt)``, lock the prompt's node and unlock the matched node;
+* a decode step allocates one slot per request (in order), stores the token's
+  K/V there and attends over the request's context including that token; decode
+  tokens stay outside the tree until finish;
+* finish is ``insert(prompt + outputs)`` then unlock of the prompt's node; slots
+  of any part that another request had already inserted are freed.
+
+Parity: pinned by ``tests/test_oracle_pins.py`` (12,960 / 6,660 / 3,060 prefill
+counts of the nested example; 2,800 of 3,000 reused at agent step 5).
+"""
+
+from .radix_cache import RadixCache, common_prefix_length
+
+
+class Trace:
+    """Everything the bookkeeping decides, for bit-exact comparison."""
+
+    def __init__(self):
+        self.batches = []        # per extend batch: list of (rid, prefix_len, row)
+        self.decode_steps = []   # per decode step: list of (rid, slot)
+        self.finishes = []       # per finish: (rid, already_cached)
+        self.prefilled = 0
+        self.eviction_log = []
+        self.stats = {}
+
+    def as_tuple(self):
+        return (
+            [[(rid, m, tuple(row)) for rid, m, row in b] for b in self.batches],
+            [list(s) for s in self.decode_steps],
+            list(self.finishes),
+            self.prefilled,
+            list(self.eviction_log),
+        )
+
+
+def plan_batches(cache, wave_prompts):
+    """Yield lists of positions into ``wave_prompts`` forming extend batches.
+
+    Lazily: a batch is yielded when it closes, so that the caller runs and
+    inserts it before the next request's tree match is taken.
+    """
+    batch = []
+    for j, prompt in enumerate(wave_prompts):
+        m = cache.match_length(prompt[:len(prompt) - 1])
+        if batch and any(common_prefix_length(prompt, wave_prompts[i]) > m
+                         for i in batch):
+            yield batch
+            batch = []
+        batch.append(j)
+    if batch:
+        yield batch
+
+
+def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
+                    on_decode=None):
+    """Run the request flow over a fresh oracle cache.
+
+    waves: list of waves; a wave is a list of ``(rid, prompt, outputs)`` with
+    ``outputs`` holding ``decode_steps`` token ids (may be empty when
+    ``decode_steps == 0``).  ``on_extend(batch_records)`` and
+    ``on_decode(step, rows)`` are optional callbacks for attention checks.
+    Returns ``(trace, cache)``.
+    """
+    cache = RadixCache(num_slots)
+    trace = Trace()
+    for wave in waves:
+        prompts = [list(p) for _, p, _ in wave]
+        rows = {}
+        prompt_nodes = {}
+        batches = plan_batches(cache, prompts)
+        for batch in batches:
+            matched = []
+            for j in batch:
+                rid, prompt, _ = wave[j]
+                slots, node = cache.match_prefix(prompts[j][:len(prompts[j]) - 1])
+                cache.inc_lock_ref(node)
+                matched.append((j, slots, node))
+            total_new = sum(len(prompts[j]) - len(s) for j, s, _ in matched)
+            new_slots = cache.alloc(total_new)
+            records = []
+            pos = 0
+            for j, slots, node in matched:
+                rid = wave[j][0]
+                n_new = len(prompts[j]) - len(slots)
+                row = list(slots) + new_slots[pos:pos + n_new]
+                pos += n_new
+                rows[rid] = row
+                records.append((rid, len(slots), row))
+                trace.prefilled += n_new
+            trace.batches.append(records)
+            if on_extend is not None:
+                on_extend(records)
+            for (j, slots, node), (rid, m, row) in zip(matched, records):
+                already, node2 = cache.insert(prompts[j], row)
+                if already != m:
+                    raise AssertionError(
+                        "in-batch duplicate prefill: rule violated")
+                cache.inc_lock_ref(node2)
+                cache.dec_lock_ref(node)
+                prompt_nodes[rid] = node2
+        for step in range(decode_steps):
+            slots = cache.alloc(len(wave))
+            step_rec = []
+            for (rid, _, _), s in zip(wave, slots):
+                rows[rid].append(s)
+                step_rec.append((rid, s))
+            trace.decode_steps.append(step_rec)
+            if on_decode is not None:
+                on_decode(step, {rid: list(rows[rid]) for rid, _, _ in wave})
+        for rid, prompt, outputs in wave:
+            full = list(prompt) + list(outputs[:decode_steps])
+            already, _ = cache.insert(full, rows[rid])
+            if already > len(prompt):
+                cache.free(rows[rid][len(prompt):already])
+            trace.finishes.append((rid, already))
+            cache.dec_lock_ref(prompt_nodes[rid])
+    trace.eviction_log = list(cache.eviction_log)
+    trace.stats = {
+        "cached": cache.cached_size(),
+        "evictable": cache.evictable_size_,
+        "protected": cache.protected_size_,
+        "free": len(cache.free_slots),
+        "num_nodes": cache.num_nodes(),
+    }
+    return trace, cache

@@ -1,0 +1,409 @@
+"""Pins of the oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: numbers the
+pages print (fixtures under tests/golden/, each citing its page and section),
+closed forms, brute force on tiny inputs, and structural invariants.
+"""
+
+import math
+import random
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+from oracle import attention as oatt
+from oracle.harness import run_bookkeeping
+from oracle.radix_cache import NoSpace, RadixCache, StateError
+from radix_tree_prefix_gb300 import workloads
+
+
+# ----------------------------------------------------------------- golden
+def _toy_fixture():
+    lines = read_golden("toy_trie_reuse.txt")
+    reqs, exp, total = [], [], None
+    mode = None
+    for ln in lines:
+        if ln == "requests:":
+            mode = "r"
+        elif ln == "expected:":
+            mode = "e"
+        elif ln.startswith("total:"):
+            total = ln.split()[1]
+        elif mode == "r":
+            reqs.append(ln.split(" "))
+        elif mode == "e":
+            exp.append(tuple(int(x) for x in ln.split()))
+    return reqs, exp, total
+
+
+def test_toy_trie_reuse_counts():
+    """Per-request reuse printed by the toy prefix tree listing."""
+    reqs, expected, total = _toy_fixture()
+    vocab = {}
+    cache = RadixCache(1000)
+    got = []
+    for words in reqs:
+        toks = [vocab.setdefault(w, len(vocab)) for w in words]
+        slots, node = cache.match_prefix(toks)
+        new = cache.alloc(len(toks) - len(slots))
+        cache.insert(toks, slots + new)
+        got.append((len(toks), len(slots)))
+    assert got == expected
+    cached = sum(h for _, h in got)
+    n = sum(t for t, _ in got)
+    assert f"{cached}/{n}" == total
+
+
+def _golden_kv(name):
+    out = {}
+    for ln in read_golden(name):
+        parts = ln.split()
+        if parts[0] != "case":
+            out[parts[0]] = int(parts[1])
+    return out
+
+
+def test_nested_example_prefill_counts():
+    """12,960 / 6,660 / 3,060 prompt tokens prefilled."""
+    g = _golden_kv("nested_prefill_counts.txt")
+    wl = workloads.nested_share()
+    waves = wl.oracle_waves()
+    prompts = [p for _, p, _ in waves[0]]
+    # no sharing: every prompt prefilled in full
+    assert sum(len(p) for p in prompts) == g["no_sharing"]
+    # instruction block only: the block is prefilled once, then every request
+    # reuses it and nothing else (inserts disabled)
+    cache = RadixCache(wl.num_slots)
+    instr = prompts[0][:900]
+    cache.insert(instr, cache.alloc(900))
+    pre = 900
+    for p in prompts:
+        slots, _ = cache.match_prefix(p[:-1])
+        pre += len(p) - len(slots)
+    assert pre == g["instruction_only"]
+    # the radix tree at all levels, with the in-batch rule
+    trace, _ = run_bookkeeping(waves, wl.num_slots, 0)
+    assert trace.prefilled == g["radix_tree"]
+    assert [[rid for rid, _, _ in b] for b in trace.batches] == \
+        [[0], [1, 2, 3, 4], [5, 6, 7]]
+
+
+def test_agent_step5_reuse():
+    """2,800 of 3,000 tokens reused at agent step 5."""
+    g = _golden_kv("agent_step_reuse.txt")
+    rng = random.Random(5)
+    instr = [rng.randrange(32000) for _ in range(g["instructions"])]
+    steps = [[rng.randrange(32000) for _ in range(g["per_step"])]
+             for _ in range(g["step"])]
+    waves = []
+    for k in range(1, g["step"] + 1):
+        prompt = instr + sum(steps[:k], [])
+        waves.append([(k, prompt, [])])
+    trace, _ = run_bookkeeping(waves, 10000, 0)
+    rid, m, row = trace.batches[g["step"] - 1][0]
+    assert len(row) == g["prompt_tokens"]
+    assert m == g["reused"]
+
+
+def _worked_cache(locked):
+    g = _golden_kv("worked_eviction.txt")
+    cache = RadixCache(g["capacity"] + 1)
+    rng = random.Random(7)
+    seq = lambda n: [rng.randrange(32000) for _ in range(n)]
+    s = seq(g["S"])
+    branches = {b: seq(g[b]) for b in "ABC"}
+    nodes = {}
+    for b in "ABC":      # A used longest ago, then B, then C
+        toks = s + branches[b]
+        slots, _ = cache.match_prefix(toks)
+        new = cache.alloc(len(toks) - len(slots))
+        _, nodes[b] = cache.insert(toks, slots + new)
+    assert cache.cached_size() == g["S"] + g["A"] + g["B"] + g["C"]
+    for b in locked:
+        cache.inc_lock_ref(nodes[b])
+    d = s + seq(g["D_new"])
+    slots, dnode = cache.match_prefix(d[:-1])
+    assert len(slots) == g["S"]
+    cache.inc_lock_ref(dnode)
+    return cache, nodes, d, slots, g
+
+
+@pytest.mark.parametrize("locked,victim,held", [
+    ("C", "A", 3500), ("AC", "B", 3800), ("ABC", None, None)])
+def test_worked_eviction_example(locked, victim, held):
+    cache, nodes, d, slots, g = _worked_cache(locked)
+    if victim is None:
+        with pytest.raises(NoSpace):
+            cache.alloc(g["D_new"])
+        assert cache.eviction_log == []
+        return
+    new = cache.alloc(g["D_new"])
+    assert cache.eviction_log == [(nodes[victim].id, g[victim])]
+    cache.insert(d, slots + new)
+    assert cache.cached_size() == held
+
+
+# ------------------------------------------------------------ brute force
+def test_match_against_prefix_dictionary():
+    """Match length and slots equal a naive dict-of-prefixes trie."""
+    rng = random.Random(11)
+    for trial in range(300):
+        alpha = rng.randint(1, 4)
+        cache = RadixCache(2000)
+        first_slot = {}          # prefix tuple -> slot of its last token
+        for _ in range(rng.randint(1, 8)):
+            seq = [rng.randrange(alpha) for _ in range(rng.randint(1, 12))]
+            # brute force: longest prefix present in the dictionary
+            n = 0
+            while n < len(seq) and tuple(seq[:n + 1]) in first_slot:
+                n += 1
+            want = [first_slot[tuple(seq[:p + 1])] for p in range(n)]
+            assert cache.match_length(seq) == n
+            slots, node = cache.match_prefix(seq)
+            assert slots == want
+            new = cache.alloc(len(seq) - n)
+            row = slots + new
+            already, _ = cache.insert(seq, row)
+            assert already == n
+            for p in range(len(seq)):
+                first_slot.setdefault(tuple(seq[:p + 1]), row[p])
+        assert cache.cached_size() == len(first_slot)
+
+
+def test_split_at_divergence():
+    """Second session sharing the system prompt splits the first node."""
+    cache = RadixCache(100)
+    sys_p = [1, 2, 3, 4]
+    a = sys_p + [10, 11]
+    b = sys_p + [20, 21, 22]
+    cache.insert(a, cache.alloc(len(a)))
+    assert cache.num_nodes() == 1
+    slots, node = cache.match_prefix(b)
+    assert len(slots) == 4 and node.key == sys_p   # split during the match
+    assert cache.num_nodes() == 2
+    cache.insert(b, slots + cache.alloc(3))
+    assert cache.num_nodes() == 3
+    keys = sorted(tuple(c.key) for c in node.children.values())
+    assert keys == [(10, 11), (20, 21, 22)]
+
+
+# -------------------------------------------------------------- invariants
+def test_lock_and_eviction_invariants():
+    """Random operations: accounting, locks and leaf-inward LRU eviction."""
+    rng = random.Random(3)
+    for trial in range(40):
+        n_slots = rng.randint(20, 60)
+        cache = RadixCache(n_slots)
+        held = {}                  # handle -> (node, slots it owns privately)
+        private = 0
+        locks = []
+        for step in range(80):
+            op = rng.random()
+            seq = [rng.randrange(3) for _ in range(rng.randint(1, 10))]
+            if op < 0.5:
+                slots, node = cache.match_prefix(seq[:-1])
+                cache.inc_lock_ref(node)
+                # snapshot before allocation
+                before = {}
+                stack = [cache.root]
+                while stack:
+                    x = stack.pop()
+                    before[x.id] = (x.lock_ref, [c.id for c in x.children.values()],
+                                    x.last_access_time)
+                    stack.extend(x.children.values())
+                log0 = len(cache.eviction_log)
+                try:
+                    new = cache.alloc(len(seq) - len(slots))
+                except NoSpace:
+                    cache.dec_lock_ref(node)
+                    new = None
+                evicted = [nid for nid, _ in cache.eviction_log[log0:]]
+                for pos, nid in enumerate(evicted):
+                    lock, kids, _ = before[nid]
+                    assert lock == 0, "locked node evicted"
+                    # every child was evicted before its parent
+                    for c in kids:
+                        assert c in evicted[:pos], "parent evicted before child"
+                if evicted:
+                    leaves = [(before[i][2], i) for i in before
+                              if i != 0 and not before[i][1] and before[i][0] == 0]
+                    assert evicted[0] == min(leaves)[1], "not least recent leaf"
+                if new is None:
+                    continue
+                row = slots + new
+                already, node2 = cache.insert(seq, row)
+                cache.free(row[len(slots):already])
+                cache.inc_lock_ref(node2)
+                cache.dec_lock_ref(node)
+                locks.append(node2)
+            elif locks:
+                node = locks.pop(rng.randrange(len(locks)))
+                cache.dec_lock_ref(node)
+            cached = cache.cached_size()
+            assert cache.evictable_size_ + cache.protected_size_ == cached
+            assert len(cache.free_slots) + cached + private == n_slots - 1
+        for node in locks:
+            cache.dec_lock_ref(node)
+        assert cache.protected_size_ == 0
+        with pytest.raises(StateError):
+            leaf = next(iter(cache.root.children.values()), None)
+            if leaf is None:
+                raise StateError("empty")
+            cache.dec_lock_ref(leaf)
+
+
+# --------------------------------------------------------------- attention
+def test_single_key_returns_its_value():
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((1, 2, 8))
+    k = rng.standard_normal((1, 1, 8))
+    v = rng.standard_normal((1, 1, 8))
+    o, lse = oatt.softmax_attention(q, k, v, [1])
+    assert np.array_equal(o[0, 0], v[0, 0]) and np.array_equal(o[0, 1], v[0, 0])
+    assert lse[0, 0] == pytest.approx(q[0, 0] @ k[0, 0] / math.sqrt(8), abs=1e-15)
+
+
+def test_two_keys_closed_form():
+    """Score gap ln 3 with scale 1/sqrt(d) gives weights 1/4 and 3/4."""
+    d = 4
+    q = np.zeros((1, 1, d)); q[0, 0, 0] = 1.0
+    k = np.zeros((2, 1, d)); k[1, 0, 0] = 2.0 * math.log(3.0)   # sqrt(4) = 2
+    v = np.zeros((2, 1, d)); v[0, 0, :] = 1.0; v[1, 0, :] = 5.0
+    o, lse = oatt.softmax_attention(q, k, v, [2])
+    assert o[0, 0] == pytest.approx(np.full(d, 0.25 * 1 + 0.75 * 5), abs=1e-14)
+    assert lse[0, 0] == pytest.approx(math.log(4.0), abs=1e-14)
+
+
+def test_equal_keys_average_visible_values():
+    """Causal boundary: query at position p+i averages values 0..p+i."""
+    n, p, d = 9, 4, 3
+    k = np.ones((n, 1, d))
+    v = np.arange(n, dtype=np.float64)[:, None, None] * np.ones((n, 1, d))
+    q = np.ones((n - p, 2, d))
+    o, _ = oatt.extend_attention(q, k, v, p)
+    for i in range(n - p):
+        assert o[i, 0] == pytest.approx(np.full(d, (p + i) / 2.0), abs=1e-13)
+
+
+def test_gqa_head_mapping():
+    """Query head h reads KV head h // G."""
+    hq, hkv, d, n = 8, 2, 4, 5
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((n, hq, d))
+    k = rng.standard_normal((n, hkv, d))
+    v = np.zeros((n, hkv, d))
+    for j in range(hkv):
+        v[:, j, :] = j + 1
+    o, _ = oatt.softmax_attention(q, k, v, list(range(1, n + 1)))
+    for h in range(hq):
+        assert np.allclose(o[:, h, :], h // (hq // hkv) + 1, atol=1e-14)
+
+
+def test_lse_merge_equals_unsplit():
+    rng = np.random.default_rng(2)
+    n, hq, hkv, d = 37, 4, 2, 16
+    q = rng.standard_normal((1, hq, d))
+    k = rng.standard_normal((n, hkv, d))
+    v = rng.standard_normal((n, hkv, d))
+    full_o, full_l = oatt.softmax_attention(q, k, v, [n])
+    parts = []
+    for lo, hi in [(0, 5), (5, 6), (6, 30), (30, 37)]:
+        o, l = oatt.softmax_attention(q, k[lo:hi], v[lo:hi], [hi - lo])
+        parts.append((o, l))
+    mo, ml = oatt.lse_merge(parts)
+    assert np.allclose(mo, full_o, atol=1e-12)
+    assert np.allclose(ml, full_l, atol=1e-12)
+    # a single part merges to itself
+    so, sl = oatt.lse_merge([(full_o, full_l)])
+    assert np.allclose(so, full_o, atol=1e-15) and np.allclose(sl, full_l, atol=1e-15)
+
+
+def test_cached_prefix_equals_full_recompute():
+    """Suffix rows with a cached prefix equal rows of the whole prompt."""
+    rng = np.random.default_rng(4)
+    n, p, hq, hkv, d = 23, 15, 4, 1, 8
+    q = rng.standard_normal((n, hq, d))
+    k = rng.standard_normal((n, hkv, d))
+    v = rng.standard_normal((n, hkv, d))
+    full_o, full_l = oatt.softmax_attention(q, k, v, list(range(1, n + 1)))
+    o, l = oatt.extend_attention(q[p:], k, v, p)
+    assert np.array_equal(o, full_o[p:]) and np.array_equal(l, full_l[p:])
+    do, dl = oatt.decode_attention(q[-1], k, v)
+    assert np.array_equal(do, full_o[-1]) and np.array_equal(dl, full_l[-1])
+
+
+def test_lock_protects_whole_path():
+    """inc_lock_ref moves every node from the node up to the root."""
+    cache = RadixCache(100)
+    a = [1, 2, 3, 4, 10, 11]
+    b = [1, 2, 3, 4, 20, 21, 22]
+    cache.insert(a, cache.alloc(len(a)))
+    slots, _ = cache.match_prefix(b)
+    _, leaf_b = cache.insert(b, slots + cache.alloc(3))
+    assert (cache.evictable_size_, cache.protected_size_) == (9, 0)
+    cache.inc_lock_ref(leaf_b)
+    assert (cache.evictable_size_, cache.protected_size_) == (2, 7)
+    cache.inc_lock_ref(leaf_b)
+    assert (cache.evictable_size_, cache.protected_size_) == (2, 7)
+    cache.dec_lock_ref(leaf_b)
+    cache.dec_lock_ref(leaf_b)
+    assert (cache.evictable_size_, cache.protected_size_) == (9, 0)
+    with pytest.raises(StateError):
+        cache.dec_lock_ref(leaf_b)
+
+
+def test_touch_makes_node_recent():
+    """A reused branch becomes recent: the least recently used leaf goes.
+
+    "Eviction on a tree" (bibekananda.in): a node touched by requests stays
+    warm; the worked example evicts the branch used longest ago.
+    """
+    cache = RadixCache(100)
+    s = [1, 2, 3]
+    nodes = {}
+    for name, tail in (("A", [10, 11]), ("B", [20, 21]), ("C", [30, 31])):
+        toks = s + tail
+        slots, _ = cache.match_prefix(toks)
+        _, nodes[name] = cache.insert(toks, slots + cache.alloc(len(toks) - len(slots)))
+    cache.match_prefix(s + [10, 11])          # user A comes back
+    assert cache.evict(1) == 2
+    assert cache.eviction_log == [(nodes["B"].id, 2)]
+    assert cache.evict(1) == 2
+    assert cache.eviction_log[-1] == (nodes["C"].id, 2)
+
+
+def test_cascade_reaches_parent_after_children():
+    """A parent becomes a candidate only once its last child is gone."""
+    cache = RadixCache(100)
+    a, b = [1, 2, 3, 4], [1, 2, 5, 6]
+    cache.insert(a, cache.alloc(4))
+    slots, _ = cache.match_prefix(b)
+    _, nb = cache.insert(b, slots + cache.alloc(2))
+    parent = nb.parent
+    assert cache.evict(100) == 6
+    ids = [i for i, _ in cache.eviction_log]
+    assert ids[-1] == parent.id and len(ids) == 3
+    assert cache.cached_size() == 0 and cache.num_nodes() == 0
+
+
+def test_allocator_fifo_reading():
+    """Reading (pages silent): FIFO free list 1..N-1, freed slots at the tail."""
+    cache = RadixCache(8)
+    assert cache.alloc(3) == [1, 2, 3]
+    cache.free([2])
+    assert cache.alloc(4) == [4, 5, 6, 7]
+    assert cache.alloc(1) == [2]
+    with pytest.raises(NoSpace):
+        cache.alloc(1)
+
+
+def test_evicted_slots_return_in_stored_order():
+    """Reading (pages silent): an evicted node's slots join the free list tail
+    in the order the node stores them."""
+    cache = RadixCache(6)
+    slots = cache.alloc(5)                     # [1, 2, 3, 4, 5]
+    order = [3, 1, 5, 2, 4]
+    cache.free([s for s in slots if s not in order])
+    cache.insert([7, 8, 9, 10, 11], order)
+    assert cache.alloc(5) == order             # forces eviction of the node
