@@ -1,0 +1,385 @@
+/*
+ * rx.h -- C ABI of librx: the RadixAttention hot path on one GB300 (sm_103a).
+ *
+ * A host radix cache over a token-granular KV pool decides which KV slots
+ * every request reads; CUDA kernels store new K/V into the pool and compute
+ * extend (suffix prefill) and decode attention over the slots the cache hands
+ * out.  Sources, by page title and section:
+ *
+ *   [T]  "SGLang: the tree, and the language nobody remembers"
+ *        - "A tree, not a map": TreeNode fields, lock_ref accounting, heap
+ *          eviction cascading to childless unlocked parents, node split at
+ *          divergence, children keyed on the first token at page_size 1.
+ *        - "What the C++ tree is actually for": match_prefix returns the
+ *          matched KV indices and a node handle.
+ *        - "Speculative decoding puts a tree inside the tree": a tree node
+ *          maps a token run to a vector of KV indices in the pool.
+ *   [B]  "SGLang" (bibekananda.in) - "One tree for everybody" (walk from the
+ *          root as far as tokens match; matched state is pointed at, not
+ *          recomputed; the divergent part becomes a new branch), "Eviction on
+ *          a tree" (leaves first, a parent only after its children).
+ *   [L]  "SGLang: Structured LLM Programs for Efficient Inference"
+ *        - "A quick recap of how an LLM generates text": decode attends over
+ *          the KV cache and appends its own keys and values.
+ *        - "How RadixAttention reuses past work": match, lock, prefill only
+ *          the rest attending to the reused KV as if just computed, decode and
+ *          insert, release.
+ *        - "Worked example, step by step": a node is evicted whole; locked
+ *          nodes are never evicted; with nothing evictable the request waits.
+ *
+ * Conventions
+ *   - Every call returns an rx_status; nothing throws across the ABI.  On an
+ *     error rx_last_error() returns a text for the calling thread.
+ *   - The library owns the tree (opaque rx_cache).  The caller owns every host
+ *     array and every device buffer (raw pointers, e.g. from torch tensors)
+ *     and the CUDA stream.  The library never allocates device memory.
+ *   - Host calls are synchronous and not thread-safe for one cache.  Device
+ *     calls only enqueue work on the given stream (cudaStream_t passed as
+ *     rx_stream_t; NULL is the legacy default stream) and return RX_ERR_CUDA
+ *     if the launch itself fails.
+ *   - Token ids and slots are int32.  Slot 0 is a pad slot that the allocator
+ *     never hands out; kernels read it for out-of-range keys only as a
+ *     harmless address and mask the value.
+ *   - KV pool layout (device, bf16): K and V each [num_layers][num_kv_heads]
+ *     [num_slots][head_dim], row-major; one slot row of one head is head_dim
+ *     contiguous bf16 (256 B at d=128, 512 B at d=256).  Pool base pointers
+ *     must be 16-byte aligned.  head_dim must be 128 or 256.
+ */
+#ifndef RX_H
+#define RX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rx_status {
+  RX_OK = 0,
+  RX_ERR_INVALID = 1,  /* bad argument, shape, alignment or unknown node   */
+  RX_ERR_NO_SPACE = 2, /* allocation impossible even after eviction        */
+  RX_ERR_STATE = 3,    /* lock misuse or a rule the caller had to keep     */
+  RX_ERR_CUDA = 4      /* a CUDA launch or copy returned an error          */
+} rx_status;
+
+typedef struct CUstream_st* rx_stream_t; /* identical to cudaStream_t */
+
+/* A node handle is the node's id: 0 is the root, every created node (new
+ * leaf, or the upper half of a split) takes the next id.  A handle stays valid
+ * while its node is in the tree; a split keeps the lower half's id, so a held
+ * handle keeps naming exactly the prefix it was returned for. */
+typedef int64_t rx_node;
+
+typedef struct rx_cache rx_cache;
+
+typedef struct rx_config {
+  int64_t num_slots; /* pool slots including pad slot 0; >= 1            */
+  int32_t page_size; /* must be 1 (token granularity)                    */
+  int32_t reserved;  /* must be 0                                         */
+} rx_config;
+
+typedef struct rx_stats_t {
+  int64_t cached_tokens;    /* tokens held by tree nodes                   */
+  int64_t evictable_tokens; /* cached tokens with lock_ref == 0            */
+  int64_t protected_tokens; /* cached tokens with lock_ref > 0             */
+  int64_t free_slots;       /* slots on the free list                      */
+  int64_t num_nodes;        /* nodes excluding the root                    */
+  int64_t evicted_nodes;    /* since creation                              */
+  int64_t evicted_tokens;   /* since creation                              */
+  int64_t clock;            /* logical access clock                        */
+} rx_stats_t;
+
+typedef struct rx_evict_rec {
+  int64_t node_id;
+  int64_t num_tokens;
+} rx_evict_rec;
+
+/* ------------------------------------------------------------------------
+ * Cache lifecycle
+ * ---------------------------------------------------------------------- */
+
+/* Create an empty tree and a FIFO free list holding slots 1 .. num_slots-1
+ * (reading: the pages do not fix the allocator order).
+ * Errors: RX_ERR_INVALID if num_slots < 1, page_size != 1 or out == NULL. */
+rx_status rx_cache_create(const rx_config* cfg, rx_cache** out);
+rx_status rx_cache_destroy(rx_cache* cache);
+
+/* Copy the calling thread's last error text (NUL-terminated, truncated to
+ * cap).  Returns the full length of the text. */
+size_t rx_last_error(char* buf, size_t cap);
+
+/* ------------------------------------------------------------------------
+ * S1 match  ([T] "A tree, not a map", [B] "One tree for everybody")
+ * ---------------------------------------------------------------------- */
+
+/* Longest cached prefix of tokens[0..n) without side effects (no split, no
+ * access-time update).  Used by the in-batch prefix rule. */
+rx_status rx_match_length(const rx_cache* cache, const int32_t* tokens,
+                          int64_t n, int64_t* out_len);
+
+/* Walk from the root as far as tokens[0..n) match.  Writes the matched
+ * prefix's slots to out_slots (caller capacity >= n), its length to *out_len
+ * and the node whose root path is exactly that prefix to *out_node (0 when
+ * nothing matched).  A match ending inside an edge splits the edge there
+ * (reading: so the returned node covers exactly the matched prefix).  The
+ * access clock advances by one and every node on the matched path takes it.
+ * Errors: RX_ERR_INVALID on NULL pointers or n < 0. */
+rx_status rx_match_prefix(rx_cache* cache, const int32_t* tokens, int64_t n,
+                          int32_t* out_slots, int64_t* out_len,
+                          rx_node* out_node);
+
+/* ------------------------------------------------------------------------
+ * S2 lock  ([T] inc_lock_ref / dec_lock_ref, [L] step 2 and step 5)
+ * ---------------------------------------------------------------------- */
+
+/* lock_ref += 1 on the node and every ancestor (root excluded); a node whose
+ * lock_ref goes 0 -> 1 moves its length from the evictable to the protected
+ * count.  Locking the root is a no-op.
+ * Errors: RX_ERR_INVALID for an unknown or evicted node. */
+rx_status rx_lock(rx_cache* cache, rx_node node);
+
+/* lock_ref -= 1 along the same path; 1 -> 0 moves the length back.
+ * Errors: RX_ERR_INVALID unknown node; RX_ERR_STATE if any lock_ref on the
+ * path is already 0 (nothing is changed then). */
+rx_status rx_unlock(rx_cache* cache, rx_node node);
+
+/* ------------------------------------------------------------------------
+ * S3 allocate / evict  ([T] heap eviction, [L] "Worked example")
+ * ---------------------------------------------------------------------- */
+
+/* Take k slots from the head of the free list into out_slots[0..k).  If
+ * fewer than k are free, first evict (rx_evict) the shortfall.  If still
+ * short: RX_ERR_NO_SPACE, nothing is allocated, and nodes evicted during the
+ * attempt stay evicted ("D would have to wait"). */
+rx_status rx_alloc(rx_cache* cache, int64_t k, int32_t* out_slots);
+
+/* Evict unlocked leaves, least recent first (key: priority 0,
+ * last_access_time, node id), each node whole; its slots join the free-list
+ * tail in stored order; a parent that becomes childless and unlocked joins
+ * the candidates.  Stops once >= k slots were freed or no candidate is left.
+ * *out_freed = slots freed (may exceed k). */
+rx_status rx_evict(rx_cache* cache, int64_t k, int64_t* out_freed);
+
+/* Return slots to the free-list tail, in the given order.  The caller must
+ * own them (allocated and not held by the tree). */
+rx_status rx_free(rx_cache* cache, const int32_t* slots, int64_t k);
+
+/* ------------------------------------------------------------------------
+ * S10 insert  ([B] "the divergent part becomes a new branch", [L] step 4)
+ * ---------------------------------------------------------------------- */
+
+/* Insert tokens[0..n) with their slots.  Walks and splits as rx_match_prefix;
+ * the uncached remainder becomes one new leaf holding slots of that part.
+ * *out_already = tokens that were already cached (the caller still owns its
+ * own slots for that part and frees those beyond what it had locked);
+ * *out_node = node ending exactly at n.  The access clock advances by one and
+ * the whole path takes it. */
+rx_status rx_insert(rx_cache* cache, const int32_t* tokens,
+                    const int32_t* slots, int64_t n, int64_t* out_already,
+                    rx_node* out_node);
+
+/* ------------------------------------------------------------------------
+ * Introspection
+ * ---------------------------------------------------------------------- */
+rx_status rx_stats(const rx_cache* cache, rx_stats_t* out);
+
+/* Copy eviction records [start, start+cap) (in eviction order) to out;
+ * *out_total = number of records since creation. */
+rx_status rx_eviction_log(const rx_cache* cache, int64_t start,
+                          rx_evict_rec* out, int64_t cap, int64_t* out_total);
+
+/* Number of tokens on the root path of a node (its depth in tokens). */
+rx_status rx_node_depth(const rx_cache* cache, rx_node node,
+                        int64_t* out_depth);
+
+/* ------------------------------------------------------------------------
+ * Batch steps of the request flow ([L] "How RadixAttention reuses past
+ * work"), composed from the calls above so one batch costs one call.
+ * ---------------------------------------------------------------------- */
+
+/* S1+S2+S3+S4 for an extend batch of R requests.  tokens holds the prompts
+ * back to back, request r at [tok_indptr[r], tok_indptr[r+1]).  In request
+ * order: rx_match_prefix on the prompt without its last token (the last prompt
+ * token is always recomputed) and rx_lock of the matched node; then ONE
+ * rx_alloc of all new tokens, handed out in request order.  Writes
+ *   req_to_token[r*row_stride + 0 .. n_r)  = matched slots ++ new slots,
+ *   out_prefix_len[r], out_match_node[r],
+ *   out_new_slots[0 .. total_new) = the new slots in request order (the K/V
+ *   of the batch's new tokens are stored there), *out_total_new.
+ * On RX_ERR_NO_SPACE every lock taken is released again (evictions stay).
+ * Errors: RX_ERR_INVALID if a prompt is empty or longer than row_stride. */
+rx_status rx_extend_begin(rx_cache* cache, int32_t R, const int32_t* tokens,
+                          const int64_t* tok_indptr, int32_t* req_to_token,
+                          int64_t row_stride, int32_t* out_prefix_len,
+                          rx_node* out_match_node, int32_t* out_new_slots,
+                          int64_t* out_total_new);
+
+/* S10 after an extend batch: for each request in order rx_insert(prompt,
+ * row), rx_lock(prompt node), rx_unlock(matched node).  Writes
+ * out_prompt_node[r].  RX_ERR_STATE if a prompt finds more of itself cached
+ * than its match (two requests of one batch shared more than their match:
+ * the caller's batching must prevent that). */
+rx_status rx_extend_end(rx_cache* cache, int32_t R, const int32_t* tokens,
+                        const int64_t* tok_indptr,
+                        const int32_t* req_to_token, int64_t row_stride,
+                        const int32_t* prefix_len,
+                        const rx_node* match_node, rx_node* out_prompt_node);
+
+/* Finish (S10): for each request, rx_insert(prompt ++ outputs, row) where
+ * tokens/tok_indptr hold prompt ++ outputs and the row holds their slots;
+ * slots of any part beyond prompt_len[r] that was already cached are freed;
+ * then rx_unlock(prompt_node[r]).  out_already[r] may be NULL. */
+rx_status rx_finish(rx_cache* cache, int32_t R, const int32_t* tokens,
+                    const int64_t* tok_indptr, const int32_t* req_to_token,
+                    int64_t row_stride, const int64_t* prompt_len,
+                    const rx_node* prompt_node, int64_t* out_already);
+
+/* In-batch prefix rule ([T] "The scheduler is where the cache is won or
+ * lost"): *out_conflict = 1 if the common prefix of tokens[0..n) with any of
+ * the R member prompts (concatenated as in rx_extend_begin) is longer than
+ * match_len, else 0. */
+rx_status rx_batch_conflict(const int32_t* tokens, int64_t n,
+                            int64_t match_len, int32_t R,
+                            const int32_t* member_tokens,
+                            const int64_t* member_indptr,
+                            int32_t* out_conflict);
+
+/* ------------------------------------------------------------------------
+ * Decode plan (S7/S8 split; host)
+ * ---------------------------------------------------------------------- */
+
+/* Layout of the int32 plan written by rx_plan_decode (all offsets in int32
+ * words from the start of the plan):
+ *   work[n_work][RX_WORK_WORDS]: {req_to_token row, kv_begin, kv_end,
+ *       member_off, n_members, part_base, n_rows (= n_members*G), 0}
+ *       -- one CTA per work item and KV head attends the member requests'
+ *       query heads of that KV head over keys row[kv_begin .. kv_end);
+ *   members[n_member_entries]: decode batch index of each member;
+ *   req_part_indptr[B+1], req_parts[n_parts]: partial results of request b
+ *       are entries req_parts[req_part_indptr[b] .. req_part_indptr[b+1]).
+ * Partial entry p of work item w's member i is part_base(w) + i. */
+#define RX_WORK_WORDS 8
+typedef struct rx_decode_plan_info {
+  int64_t plan_words;     /* int32 words used                             */
+  int64_t n_work;         /* work items (grid = n_work x num_kv_heads)    */
+  int64_t n_parts;        /* partial (o, lse) entries                     */
+  int64_t n_member_entries;
+  int64_t off_work, off_members, off_req_part_indptr, off_req_parts;
+  int64_t n_shared_segments; /* tree segments read by >= 2 requests       */
+  int64_t workspace_bytes;   /* device scratch rx_decode_attention needs  */
+  int64_t distinct_kv_tokens;/* distinct context tokens of the batch      */
+} rx_decode_plan_info;
+
+/* Plan one decode step for a batch of B requests.  prompt_node[b] is the
+ * locked node ending at request b's cached path; ctx_len[b] is the request's
+ * whole context length this step (cached path + decode tokens, the current
+ * token included); req_rows[b] is its row in the device req_to_token table,
+ * whose first ctx_len[b] entries must hold the context's slots.
+ * A tree node on the path of >= 2 requests becomes a shared segment read once
+ * for all of them as a multi-query tile; the rest of each context is that
+ * request's private segment.  Any partition of a context into segments gives
+ * the same attention after the log-sum-exp merge, so the plan affects speed
+ * only.  Errors: RX_ERR_INVALID (unknown node, ctx_len shorter than the node
+ * depth, plan_cap too small -- *out_info still reports plan_words). */
+rx_status rx_plan_decode(const rx_cache* cache, int32_t B,
+                         const rx_node* prompt_node, const int32_t* ctx_len,
+                         const int32_t* req_rows, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim,
+                         int32_t* plan, int64_t plan_cap,
+                         rx_decode_plan_info* out_info);
+
+/* ------------------------------------------------------------------------
+ * Device calls
+ * ---------------------------------------------------------------------- */
+
+typedef struct rx_pool_desc {
+  void* k_pool;          /* device bf16 [L][Hkv][num_slots][head_dim]      */
+  void* v_pool;          /* same layout                                    */
+  int64_t num_slots;
+  int32_t num_layers;
+  int32_t num_kv_heads;
+  int32_t head_dim;      /* 128 or 256                                     */
+  int32_t reserved;
+} rx_pool_desc;
+
+/* S5 ([L] "A quick recap": a token's keys and values are stored in the
+ * cache): K_pool[layer][h][d_slots[i]][:] = d_k[i][h][:], same for V, for
+ * i < T.  d_k, d_v: device bf16 [T][Hkv][head_dim], 16-byte aligned.
+ * Slots must be distinct and in [1, num_slots) (not checked on the device). */
+rx_status rx_kv_store(const rx_pool_desc* pool, int32_t layer,
+                      const int32_t* d_slots, const void* d_k,
+                      const void* d_v, int64_t T, rx_stream_t stream);
+
+/* Device req_to_token append: d_table[d_rows[i]*row_stride + d_pos[i]] =
+ * d_slots[i] for i < n (used to add decode tokens to device rows). */
+rx_status rx_req_to_token_write(int32_t* d_table, int64_t row_stride,
+                                const int32_t* d_rows, const int32_t* d_pos,
+                                const int32_t* d_slots, int64_t n,
+                                rx_stream_t stream);
+
+/* Host tile schedule for rx_extend_attention: tile_indptr[R+1] = prefix sums
+ * of the query-row tiles of each request (request r has
+ * (qo_indptr[r+1]-qo_indptr[r]) * Hq/Hkv rows per KV head). */
+rx_status rx_extend_plan(const int32_t* qo_indptr, int32_t R,
+                         int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t* tile_indptr,
+                         int64_t* out_num_tiles);
+
+/* S6 extend attention ([L] step 3: only the unmatched suffix is prefilled,
+ * attending to the reused KV as if it had just been computed).
+ * For request r (r < R) with prefix p = d_prefix_len[r] and suffix queries
+ * i in [0, s_r), s_r = qo_indptr[r+1]-qo_indptr[r], query head h:
+ *   o = softmax(scale * q . K[j]) V over keys j = 0 .. p+i of the request,
+ * key j's K/V read from pool slot d_req_to_token[d_req_rows[r]*row_stride+j],
+ * KV head h / (Hq/Hkv).  Inputs: d_q bf16 [total_q][Hq][head_dim] (request
+ * r's queries at rows qo_indptr[r] ..), d_qo_indptr/d_tile_indptr [R+1],
+ * d_prefix_len/d_req_rows [R] (all device int32), num_tiles from
+ * rx_extend_plan.  Outputs: d_out fp32 [total_q][Hq][head_dim], d_lse fp32
+ * [total_q][Hq] (natural log of the sum of exp of scaled scores).
+ * Errors: RX_ERR_INVALID for head_dim not in {128, 256}, Hq % Hkv != 0,
+ * layer out of range, misaligned pointers. */
+rx_status rx_extend_attention(const rx_pool_desc* pool, int32_t layer,
+                              const void* d_q, int32_t num_q_heads,
+                              const int32_t* d_req_to_token,
+                              int64_t row_stride, const int32_t* d_req_rows,
+                              const int32_t* d_prefix_len,
+                              const int32_t* d_qo_indptr,
+                              const int32_t* d_tile_indptr, int32_t R,
+                              int64_t num_tiles, float scale, float* d_out,
+                              float* d_lse, rx_stream_t stream);
+
+/* S7+S8+S9 decode attention ([L] "A quick recap": each new token attends
+ * over the KV cache, its own K/V already stored).  For request b < B, query
+ * head h: o = softmax(scale * q . K) V over its whole context, computed per
+ * plan segment into partial (o, lse) entries of d_workspace and merged by
+ * log-sum-exp: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+ * d_q bf16 [B][Hq][head_dim]; d_plan = device copy of the rx_plan_decode
+ * plan; info = its host info.  d_workspace: caller-owned device scratch of at
+ * least info->workspace_bytes, 16-byte aligned.  Outputs d_out fp32
+ * [B][Hq][head_dim], d_lse fp32 [B][Hq]. */
+rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
+                              const void* d_q, int32_t num_q_heads,
+                              const int32_t* d_req_to_token,
+                              int64_t row_stride, const int32_t* d_plan,
+                              const rx_decode_plan_info* info, int32_t B,
+                              float scale, float* d_out, float* d_lse,
+                              void* d_workspace, size_t workspace_bytes,
+                              rx_stream_t stream);
+
+/* Synchronise the current device and read the kernels' error words (then
+ * clear them).  *out_flags (may be NULL): bit 0 = rx_kv_store met a slot
+ * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel
+ * read a slot outside [0, num_slots) from req_to_token and used slot 0
+ * instead.  Returns RX_ERR_CUDA if a flag was set or the device reported an
+ * error. */
+rx_status rx_device_check(int32_t* out_flags);
+
+/* Library build information (kernel variant names, compiled arch). */
+const char* rx_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RX_H */

@@ -109,7 +109,7 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
                 row = list(slots) + new_slots[pos:pos + n_new]
                 pos += n_new
                 rows[rid] = row
-                records.append((rid, len(slots), row))
+                records.append((rid, len(slots), list(row)))
                 trace.prefilled += n_new
             trace.batches.append(records)
             if on_extend is not None:

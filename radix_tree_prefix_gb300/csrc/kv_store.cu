@@ -1,0 +1,169 @@
+// S5: scatter new K/V rows into their pool slots, and the device
+// req_to_token append.
+//
+// "SGLang: Structured LLM Programs for Efficient Inference", section "A quick
+// recap of how an LLM generates text": every computed token's keys and values
+// are stored in the KV cache; in decode each new token's own keys and values
+// are appended.  "SGLang: the tree, and the language nobody remembers",
+// section "Speculative decoding puts a tree inside the tree": the pool is
+// addressed by KV indices (slots) that tree nodes hold.
+//
+// HBM-bound copy: each 16-byte chunk of a source row is read once
+// (coalesced, contiguous) and written once to its slot's row (256 B or 512 B
+// contiguous per (slot, head)).
+
+#include <cuda_runtime.h>
+#include <stdio.h>
+
+#include "rx.h"
+#include "rx_internal.h"
+
+// Set (bit 0) when a kernel of this file met a slot outside [1, num_slots);
+// the offending write is skipped.  Read by rx_device_check().
+static __device__ int32_t g_kv_store_error;
+
+namespace {
+
+__global__ void __launch_bounds__(256) kv_store_kernel(uint4* __restrict__ kdst,
+                                                       uint4* __restrict__ vdst,
+                                                       const int32_t* __restrict__ slots,
+                                                       const uint4* __restrict__ ksrc,
+                                                       const uint4* __restrict__ vsrc,
+                                                       int64_t total_chunks, int hkv,
+                                                       int chunks_per_row, int64_t head_stride,
+                                                       int64_t num_slots) {
+  const int64_t per_token = int64_t(hkv) * chunks_per_row;
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < total_chunks;
+       c += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t t = c / per_token;
+    const int64_t rem = c - t * per_token;
+    const int h = int(rem / chunks_per_row);
+    const int j = int(rem - int64_t(h) * chunks_per_row);
+    const int32_t slot = __ldg(slots + t);
+    if (slot < 1 || slot >= num_slots) {  // never write outside the pool
+      atomicOr(&g_kv_store_error, 1);
+      continue;
+    }
+    const int64_t dst = h * head_stride + int64_t(slot) * chunks_per_row + j;
+    const uint4 kv = __ldg(ksrc + c);
+    const uint4 vv = __ldg(vsrc + c);
+    kdst[dst] = kv;
+    vdst[dst] = vv;
+  }
+}
+
+__global__ void r2t_write_kernel(int32_t* __restrict__ table, int64_t stride,
+                                 const int32_t* __restrict__ rows,
+                                 const int32_t* __restrict__ pos,
+                                 const int32_t* __restrict__ slots, int64_t n) {
+  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) table[int64_t(rows[i]) * stride + pos[i]] = slots[i];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+namespace rx_internal {
+
+rx_status check_pool(const rx_pool_desc* pool, int32_t layer) {
+  if (!pool || !pool->k_pool || !pool->v_pool)
+    return set_error(RX_ERR_INVALID, "pool descriptor or pool pointer is NULL");
+  if (pool->head_dim != 128 && pool->head_dim != 256)
+    return set_error(RX_ERR_INVALID, "head_dim must be 128 or 256");
+  if (pool->num_kv_heads <= 0 || pool->num_layers <= 0 || pool->num_slots < 2)
+    return set_error(RX_ERR_INVALID, "pool shape invalid");
+  if (layer < 0 || layer >= pool->num_layers)
+    return set_error(RX_ERR_INVALID, "layer out of range");
+  if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool))
+    return set_error(RX_ERR_INVALID, "pool pointers must be 16-byte aligned");
+  return RX_OK;
+}
+
+rx_status launch_status(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    static thread_local char buf[256];
+    snprintf(buf, sizeof(buf), "%s: %s", what, cudaGetErrorString(e));
+    return set_error(RX_ERR_CUDA, buf);
+  }
+  return RX_OK;
+}
+
+int32_t kv_store_error_flags(bool clear) {
+  int32_t v = 0;
+  cudaMemcpyFromSymbol(&v, g_kv_store_error, sizeof(v));
+  if (clear && v) {
+    int32_t z = 0;
+    cudaMemcpyToSymbol(g_kv_store_error, &z, sizeof(z));
+  }
+  return v;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 152;
+  }
+  return n;
+}
+
+}  // namespace rx_internal
+
+extern "C" rx_status rx_kv_store(const rx_pool_desc* pool, int32_t layer, const int32_t* d_slots,
+                                 const void* d_k, const void* d_v, int64_t T,
+                                 rx_stream_t stream) {
+  rx_status st = rx_internal::check_pool(pool, layer);
+  if (st != RX_OK) return st;
+  if (T < 0) return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_store: T < 0");
+  if (T == 0) return RX_OK;
+  if (!d_slots || !d_k || !d_v || !aligned16(d_k) || !aligned16(d_v))
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_store: NULL or misaligned input");
+  const int cpr = pool->head_dim / 8;
+  const int64_t head_stride = pool->num_slots * cpr;  // in 16-byte chunks
+  const int64_t layer_off = int64_t(layer) * pool->num_kv_heads * head_stride;
+  const int64_t total = T * pool->num_kv_heads * cpr;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = int64_t(rx_internal::sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  kv_store_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<uint4*>(pool->k_pool) + layer_off,
+      reinterpret_cast<uint4*>(pool->v_pool) + layer_off, d_slots,
+      reinterpret_cast<const uint4*>(d_k), reinterpret_cast<const uint4*>(d_v), total,
+      pool->num_kv_heads, cpr, head_stride, pool->num_slots);
+  return rx_internal::launch_status("rx_kv_store");
+}
+
+extern "C" rx_status rx_req_to_token_write(int32_t* d_table, int64_t row_stride,
+                                           const int32_t* d_rows, const int32_t* d_pos,
+                                           const int32_t* d_slots, int64_t n,
+                                           rx_stream_t stream) {
+  if (n < 0 || (n && (!d_table || !d_rows || !d_pos || !d_slots)) || row_stride <= 0)
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_req_to_token_write: bad argument");
+  if (n == 0) return RX_OK;
+  r2t_write_kernel<<<unsigned((n + 255) / 256), 256, 0,
+                     reinterpret_cast<cudaStream_t>(stream)>>>(d_table, row_stride, d_rows,
+                                                                d_pos, d_slots, n);
+  return rx_internal::launch_status("rx_req_to_token_write");
+}
+
+extern "C" rx_status rx_device_check(int32_t* out_flags) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    static thread_local char buf[256];
+    snprintf(buf, sizeof(buf), "rx_device_check: %s", cudaGetErrorString(e));
+    return rx_internal::set_error(RX_ERR_CUDA, buf);
+  }
+  int32_t f = rx_internal::kv_store_error_flags(true) | (rx_internal::attention_error_flags(true) << 1);
+  if (out_flags) *out_flags = f;
+  if (f)
+    return rx_internal::set_error(RX_ERR_CUDA, "rx_device_check: a kernel met a slot outside the pool");
+  return RX_OK;
+}
+
+extern "C" const char* rx_build_info(void) {
+  return "librx: host radix cache; kernels kv_store, extend/decode attention (sm_103a)";
+}

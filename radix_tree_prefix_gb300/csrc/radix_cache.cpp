@@ -1,0 +1,701 @@
+// Host radix cache over a token-granular KV slot pool (the rx_* host calls
+// of include/rx.h).
+//
+// Sources, by page title and section:
+//  - "SGLang: the tree, and the language nobody remembers", "A tree, not a
+//    map": TreeNode{key, value, children, parent, lock_ref, last_access_time,
+//    priority}; inc_lock_ref moves a node between the evictable and protected
+//    counts; eviction pops a heap of candidates and pushes a parent once it is
+//    childless and unlocked; a node splits at the divergence point; children
+//    are keyed on the first token at page_size 1; the match inside an edge is
+//    a galloping search (doubling windows, one block compare each, then a
+//    binary search of the window holding the divergence).
+//  - "SGLang" (bibekananda.in), "One tree for everybody" / "Eviction on a
+//    tree": walk as far as the tokens match; the divergent part becomes a new
+//    branch; leaves go first.
+//  - "SGLang: Structured LLM Programs for Efficient Inference", "How
+//    RadixAttention reuses past work" and "Worked example, step by step".
+//
+// Readings where the pages are silent: a logical access clock advanced once
+// per match/insert and written on the whole touched path; heap key
+// (priority = 0, last_access_time, node id); a FIFO free list 1..N-1; a
+// match ending inside an edge splits it; the split's upper half takes a fresh
+// id and the lower half's lock_ref and access time.
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <memory>
+#include <queue>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "rx.h"
+#include "rx_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+rx_status fail(rx_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+struct Node {
+  int64_t id = 0;
+  std::vector<int32_t> key;
+  std::vector<int32_t> value;
+  std::unordered_map<int32_t, Node*> children;
+  Node* parent = nullptr;
+  int64_t lock_ref = 0;
+  int64_t last_access_time = 0;
+  int32_t priority = 0;
+};
+
+// Length of the common prefix of a[0..n) and b[0..n): gallop over windows
+// of doubling size with one memcmp each, then bisect the window that holds
+// the first difference.
+int64_t common_prefix(const int32_t* a, const int32_t* b, int64_t n) {
+  int64_t i = 0, w = 16;
+  while (i < n) {
+    int64_t len = std::min(w, n - i);
+    if (std::memcmp(a + i, b + i, size_t(len) * sizeof(int32_t)) != 0) {
+      int64_t lo = i, hi = i + len;  // first difference lies in [lo, hi)
+      while (hi - lo > 16) {
+        int64_t mid = lo + (hi - lo) / 2;
+        if (std::memcmp(a + lo, b + lo, size_t(mid - lo) * sizeof(int32_t)) == 0)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      while (lo < hi && a[lo] == b[lo]) ++lo;
+      return lo;
+    }
+    i += len;
+    w *= 2;
+  }
+  return n;
+}
+
+}  // namespace
+
+struct rx_cache {
+  int64_t num_slots = 0;
+  std::unordered_map<int64_t, std::unique_ptr<Node>> nodes;
+  Node* root = nullptr;
+  std::deque<int32_t> free_list;
+  int64_t next_id = 1;
+  int64_t clock = 0;
+  int64_t evictable = 0;
+  int64_t protected_ = 0;
+  int64_t cached = 0;
+  int64_t evicted_tokens = 0;
+  std::vector<rx_evict_rec> evict_log;
+
+  Node* new_node(const int32_t* k, const int32_t* v, int64_t n, Node* parent) {
+    auto up = std::make_unique<Node>();
+    Node* x = up.get();
+    x->id = next_id++;
+    x->key.assign(k, k + n);
+    x->value.assign(v, v + n);
+    x->parent = parent;
+    nodes.emplace(x->id, std::move(up));
+    return x;
+  }
+
+  Node* find(rx_node id) const {
+    auto it = nodes.find(id);
+    return it == nodes.end() ? nullptr : it->second.get();
+  }
+
+  // Split `node` after its first k tokens; returns the new upper node.
+  Node* split(Node* node, int64_t k) {
+    Node* parent = node->parent;
+    Node* upper = new_node(node->key.data(), node->value.data(), k, parent);
+    upper->lock_ref = node->lock_ref;
+    upper->last_access_time = node->last_access_time;
+    parent->children[node->key[0]] = upper;
+    node->key.erase(node->key.begin(), node->key.begin() + k);
+    node->value.erase(node->value.begin(), node->value.begin() + k);
+    node->parent = upper;
+    upper->children[node->key[0]] = node;
+    return upper;
+  }
+
+  int64_t match_length(const int32_t* t, int64_t n) const {
+    const Node* node = root;
+    int64_t pos = 0;
+    while (pos < n) {
+      auto it = node->children.find(t[pos]);
+      if (it == node->children.end()) break;
+      const Node* c = it->second;
+      int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
+      int64_t k = common_prefix(c->key.data(), t + pos, lim);
+      pos += k;
+      if (k < int64_t(c->key.size())) break;
+      node = c;
+    }
+    return pos;
+  }
+
+  // Walk (splitting at the end of the match); returns the deepest node and
+  // the matched length; appends matched slots to `slots` if non-null.
+  Node* walk(const int32_t* t, int64_t n, int64_t* matched,
+             std::vector<Node*>* path, int32_t* slots) {
+    Node* node = root;
+    int64_t pos = 0;
+    while (pos < n) {
+      auto it = node->children.find(t[pos]);
+      if (it == node->children.end()) break;
+      Node* c = it->second;
+      int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
+      int64_t k = common_prefix(c->key.data(), t + pos, lim);
+      if (k < int64_t(c->key.size())) c = split(c, k);
+      if (slots) std::memcpy(slots + pos, c->value.data(), size_t(k) * sizeof(int32_t));
+      pos += k;
+      path->push_back(c);
+      node = c;
+    }
+    *matched = pos;
+    return node;
+  }
+
+  Node* match_prefix(const int32_t* t, int64_t n, int32_t* slots,
+                     int64_t* len) {
+    clock += 1;
+    std::vector<Node*> path;
+    Node* node = walk(t, n, len, &path, slots);
+    for (Node* x : path) x->last_access_time = clock;
+    return node;
+  }
+
+  Node* insert(const int32_t* t, const int32_t* s, int64_t n,
+               int64_t* already) {
+    clock += 1;
+    std::vector<Node*> path;
+    int64_t pos = 0;
+    Node* node = walk(t, n, &pos, &path, nullptr);
+    *already = pos;
+    if (pos < n) {
+      Node* leaf = new_node(t + pos, s + pos, n - pos, node);
+      node->children[t[pos]] = leaf;
+      evictable += n - pos;
+      cached += n - pos;
+      path.push_back(leaf);
+      node = leaf;
+    }
+    for (Node* x : path) x->last_access_time = clock;
+    return node;
+  }
+
+  void lock(Node* node) {
+    for (; node != root; node = node->parent) {
+      if (node->lock_ref == 0) {
+        evictable -= int64_t(node->key.size());
+        protected_ += int64_t(node->key.size());
+      }
+      node->lock_ref += 1;
+    }
+  }
+
+  bool unlock(Node* node) {
+    for (Node* w = node; w != root; w = w->parent)
+      if (w->lock_ref <= 0) return false;
+    for (; node != root; node = node->parent) {
+      if (node->lock_ref == 1) {
+        evictable += int64_t(node->key.size());
+        protected_ -= int64_t(node->key.size());
+      }
+      node->lock_ref -= 1;
+    }
+    return true;
+  }
+
+  int64_t evict(int64_t k) {
+    struct Cand {
+      int32_t priority;
+      int64_t time, id;
+      Node* node;
+      bool operator>(const Cand& o) const {
+        if (priority != o.priority) return priority > o.priority;
+        if (time != o.time) return time > o.time;
+        return id > o.id;
+      }
+    };
+    std::priority_queue<Cand, std::vector<Cand>, std::greater<Cand>> heap;
+    std::vector<Node*> stack{root};
+    while (!stack.empty()) {
+      Node* x = stack.back();
+      stack.pop_back();
+      if (x != root && x->children.empty() && x->lock_ref == 0)
+        heap.push({x->priority, x->last_access_time, x->id, x});
+      for (auto& kv : x->children) stack.push_back(kv.second);
+    }
+    int64_t freed = 0;
+    while (freed < k && !heap.empty()) {
+      Node* v = heap.top().node;
+      heap.pop();
+      Node* parent = v->parent;
+      parent->children.erase(v->key[0]);
+      for (int32_t s : v->value) free_list.push_back(s);
+      int64_t len = int64_t(v->key.size());
+      freed += len;
+      evictable -= len;
+      cached -= len;
+      evicted_tokens += len;
+      evict_log.push_back({v->id, len});
+      nodes.erase(v->id);
+      if (parent != root && parent->children.empty() && parent->lock_ref == 0)
+        heap.push({parent->priority, parent->last_access_time, parent->id,
+                   parent});
+    }
+    return freed;
+  }
+
+  bool alloc(int64_t k, int32_t* out) {
+    if (int64_t(free_list.size()) < k) evict(k - int64_t(free_list.size()));
+    if (int64_t(free_list.size()) < k) return false;
+    for (int64_t i = 0; i < k; ++i) {
+      out[i] = free_list.front();
+      free_list.pop_front();
+    }
+    return true;
+  }
+
+  int64_t depth(const Node* x) const {
+    int64_t d = 0;
+    for (; x != root; x = x->parent) d += int64_t(x->key.size());
+    return d;
+  }
+};
+
+// ---------------------------------------------------------------- C ABI
+extern "C" {
+
+size_t rx_last_error(char* buf, size_t cap) {
+  if (buf && cap) {
+    size_t n = std::min(cap - 1, g_err.size());
+    std::memcpy(buf, g_err.data(), n);
+    buf[n] = 0;
+  }
+  return g_err.size();
+}
+
+rx_status rx_cache_create(const rx_config* cfg, rx_cache** out) {
+  if (!cfg || !out) return fail(RX_ERR_INVALID, "rx_cache_create: NULL argument");
+  if (cfg->num_slots < 1 || cfg->num_slots > (int64_t(1) << 31))
+    return fail(RX_ERR_INVALID, "rx_cache_create: num_slots %lld out of range",
+                (long long)cfg->num_slots);
+  if (cfg->page_size != 1)
+    return fail(RX_ERR_INVALID, "rx_cache_create: page_size must be 1");
+  auto* c = new rx_cache();
+  c->num_slots = cfg->num_slots;
+  auto root = std::make_unique<Node>();
+  root->id = 0;
+  c->root = root.get();
+  c->nodes.emplace(0, std::move(root));
+  for (int64_t s = 1; s < cfg->num_slots; ++s) c->free_list.push_back(int32_t(s));
+  *out = c;
+  return RX_OK;
+}
+
+rx_status rx_cache_destroy(rx_cache* cache) {
+  delete cache;
+  return RX_OK;
+}
+
+rx_status rx_match_length(const rx_cache* c, const int32_t* tokens, int64_t n,
+                          int64_t* out_len) {
+  if (!c || (!tokens && n) || n < 0 || !out_len)
+    return fail(RX_ERR_INVALID, "rx_match_length: bad argument");
+  *out_len = c->match_length(tokens, n);
+  return RX_OK;
+}
+
+rx_status rx_match_prefix(rx_cache* c, const int32_t* tokens, int64_t n,
+                          int32_t* out_slots, int64_t* out_len,
+                          rx_node* out_node) {
+  if (!c || (!tokens && n) || n < 0 || (!out_slots && n) || !out_len || !out_node)
+    return fail(RX_ERR_INVALID, "rx_match_prefix: bad argument");
+  Node* x = c->match_prefix(tokens, n, out_slots, out_len);
+  *out_node = x->id;
+  return RX_OK;
+}
+
+rx_status rx_lock(rx_cache* c, rx_node node) {
+  Node* x = c ? c->find(node) : nullptr;
+  if (!x) return fail(RX_ERR_INVALID, "rx_lock: unknown node %lld", (long long)node);
+  c->lock(x);
+  return RX_OK;
+}
+
+rx_status rx_unlock(rx_cache* c, rx_node node) {
+  Node* x = c ? c->find(node) : nullptr;
+  if (!x) return fail(RX_ERR_INVALID, "rx_unlock: unknown node %lld", (long long)node);
+  if (!c->unlock(x))
+    return fail(RX_ERR_STATE, "rx_unlock: lock_ref of node %lld would go below 0",
+                (long long)node);
+  return RX_OK;
+}
+
+rx_status rx_alloc(rx_cache* c, int64_t k, int32_t* out_slots) {
+  if (!c || k < 0 || (!out_slots && k)) return fail(RX_ERR_INVALID, "rx_alloc: bad argument");
+  if (!c->alloc(k, out_slots))
+    return fail(RX_ERR_NO_SPACE, "rx_alloc: %lld slots requested, %lld free after eviction",
+                (long long)k, (long long)c->free_list.size());
+  return RX_OK;
+}
+
+rx_status rx_evict(rx_cache* c, int64_t k, int64_t* out_freed) {
+  if (!c || k < 0) return fail(RX_ERR_INVALID, "rx_evict: bad argument");
+  int64_t f = c->evict(k);
+  if (out_freed) *out_freed = f;
+  return RX_OK;
+}
+
+rx_status rx_free(rx_cache* c, const int32_t* slots, int64_t k) {
+  if (!c || k < 0 || (!slots && k)) return fail(RX_ERR_INVALID, "rx_free: bad argument");
+  for (int64_t i = 0; i < k; ++i) {
+    if (slots[i] < 1 || slots[i] >= c->num_slots)
+      return fail(RX_ERR_INVALID, "rx_free: slot %d out of range", slots[i]);
+  }
+  for (int64_t i = 0; i < k; ++i) c->free_list.push_back(slots[i]);
+  return RX_OK;
+}
+
+rx_status rx_insert(rx_cache* c, const int32_t* tokens, const int32_t* slots,
+                    int64_t n, int64_t* out_already, rx_node* out_node) {
+  if (!c || n < 0 || (n && (!tokens || !slots)) || !out_already)
+    return fail(RX_ERR_INVALID, "rx_insert: bad argument");
+  Node* x = c->insert(tokens, slots, n, out_already);
+  if (out_node) *out_node = x->id;
+  return RX_OK;
+}
+
+rx_status rx_stats(const rx_cache* c, rx_stats_t* out) {
+  if (!c || !out) return fail(RX_ERR_INVALID, "rx_stats: bad argument");
+  out->cached_tokens = c->cached;
+  out->evictable_tokens = c->evictable;
+  out->protected_tokens = c->protected_;
+  out->free_slots = int64_t(c->free_list.size());
+  out->num_nodes = int64_t(c->nodes.size()) - 1;
+  out->evicted_nodes = int64_t(c->evict_log.size());
+  out->evicted_tokens = c->evicted_tokens;
+  out->clock = c->clock;
+  return RX_OK;
+}
+
+rx_status rx_eviction_log(const rx_cache* c, int64_t start, rx_evict_rec* out,
+                          int64_t cap, int64_t* out_total) {
+  if (!c || start < 0 || cap < 0 || (cap && !out))
+    return fail(RX_ERR_INVALID, "rx_eviction_log: bad argument");
+  int64_t total = int64_t(c->evict_log.size());
+  for (int64_t i = 0; i < cap && start + i < total; ++i) out[i] = c->evict_log[start + i];
+  if (out_total) *out_total = total;
+  return RX_OK;
+}
+
+rx_status rx_node_depth(const rx_cache* c, rx_node node, int64_t* out_depth) {
+  const Node* x = c ? c->find(node) : nullptr;
+  if (!x || !out_depth) return fail(RX_ERR_INVALID, "rx_node_depth: unknown node");
+  *out_depth = c->depth(x);
+  return RX_OK;
+}
+
+// ------------------------------------------------------- batch helpers
+rx_status rx_extend_begin(rx_cache* c, int32_t R, const int32_t* tokens,
+                          const int64_t* tok_indptr, int32_t* req_to_token,
+                          int64_t row_stride, int32_t* out_prefix_len,
+                          rx_node* out_match_node, int32_t* out_new_slots,
+                          int64_t* out_total_new) {
+  if (!c || R < 0 || !tok_indptr || (R && (!tokens || !req_to_token || !out_prefix_len ||
+                                          !out_match_node || !out_new_slots)) ||
+      !out_total_new)
+    return fail(RX_ERR_INVALID, "rx_extend_begin: bad argument");
+  for (int32_t r = 0; r < R; ++r) {
+    int64_t n = tok_indptr[r + 1] - tok_indptr[r];
+    if (n < 1 || n > row_stride)
+      return fail(RX_ERR_INVALID, "rx_extend_begin: prompt %d has length %lld (row %lld)", r,
+                  (long long)n, (long long)row_stride);
+  }
+  int64_t total_new = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    const int32_t* t = tokens + tok_indptr[r];
+    int64_t n = tok_indptr[r + 1] - tok_indptr[r];
+    int64_t m = 0;
+    Node* x = c->match_prefix(t, n - 1, req_to_token + r * row_stride, &m);
+    c->lock(x);
+    out_prefix_len[r] = int32_t(m);
+    out_match_node[r] = x->id;
+    total_new += n - m;
+  }
+  if (!c->alloc(total_new, out_new_slots)) {
+    for (int32_t r = 0; r < R; ++r) c->unlock(c->find(out_match_node[r]));
+    return fail(RX_ERR_NO_SPACE, "rx_extend_begin: %lld new slots needed, %lld free after eviction",
+                (long long)total_new, (long long)c->free_list.size());
+  }
+  int64_t pos = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    int64_t n = tok_indptr[r + 1] - tok_indptr[r];
+    int64_t m = out_prefix_len[r];
+    std::memcpy(req_to_token + r * row_stride + m, out_new_slots + pos,
+                size_t(n - m) * sizeof(int32_t));
+    pos += n - m;
+  }
+  *out_total_new = total_new;
+  return RX_OK;
+}
+
+rx_status rx_extend_end(rx_cache* c, int32_t R, const int32_t* tokens,
+                        const int64_t* tok_indptr, const int32_t* req_to_token,
+                        int64_t row_stride, const int32_t* prefix_len,
+                        const rx_node* match_node, rx_node* out_prompt_node) {
+  if (!c || R < 0 || !tok_indptr || (R && (!tokens || !req_to_token || !prefix_len ||
+                                          !match_node || !out_prompt_node)))
+    return fail(RX_ERR_INVALID, "rx_extend_end: bad argument");
+  for (int32_t r = 0; r < R; ++r) {
+    if (!c->find(match_node[r]))
+      return fail(RX_ERR_INVALID, "rx_extend_end: unknown node %lld", (long long)match_node[r]);
+  }
+  for (int32_t r = 0; r < R; ++r) {
+    const int32_t* t = tokens + tok_indptr[r];
+    int64_t n = tok_indptr[r + 1] - tok_indptr[r];
+    int64_t already = 0;
+    Node* x = c->insert(t, req_to_token + r * row_stride, n, &already);
+    if (already != prefix_len[r])
+      return fail(RX_ERR_STATE,
+                  "rx_extend_end: request %d found %lld tokens cached but matched %d; "
+                  "two requests of one batch shared more than their match",
+                  r, (long long)already, prefix_len[r]);
+    c->lock(x);
+    c->unlock(c->find(match_node[r]));
+    out_prompt_node[r] = x->id;
+  }
+  return RX_OK;
+}
+
+rx_status rx_finish(rx_cache* c, int32_t R, const int32_t* tokens,
+                    const int64_t* tok_indptr, const int32_t* req_to_token,
+                    int64_t row_stride, const int64_t* prompt_len,
+                    const rx_node* prompt_node, int64_t* out_already) {
+  if (!c || R < 0 || !tok_indptr || (R && (!tokens || !req_to_token || !prompt_len ||
+                                          !prompt_node)))
+    return fail(RX_ERR_INVALID, "rx_finish: bad argument");
+  for (int32_t r = 0; r < R; ++r) {
+    if (!c->find(prompt_node[r]))
+      return fail(RX_ERR_INVALID, "rx_finish: unknown node %lld", (long long)prompt_node[r]);
+    if (tok_indptr[r + 1] - tok_indptr[r] > row_stride)
+      return fail(RX_ERR_INVALID, "rx_finish: sequence %d longer than the row", r);
+  }
+  for (int32_t r = 0; r < R; ++r) {
+    const int32_t* t = tokens + tok_indptr[r];
+    int64_t n = tok_indptr[r + 1] - tok_indptr[r];
+    const int32_t* row = req_to_token + r * row_stride;
+    int64_t already = 0;
+    c->insert(t, row, n, &already);
+    for (int64_t i = prompt_len[r]; i < already; ++i) c->free_list.push_back(row[i]);
+    if (out_already) out_already[r] = already;
+    if (!c->unlock(c->find(prompt_node[r])))
+      return fail(RX_ERR_STATE, "rx_finish: request %d was not locked", r);
+  }
+  return RX_OK;
+}
+
+rx_status rx_batch_conflict(const int32_t* tokens, int64_t n, int64_t match_len,
+                            int32_t R, const int32_t* member_tokens,
+                            const int64_t* member_indptr, int32_t* out_conflict) {
+  if ((!tokens && n) || n < 0 || R < 0 || (R && (!member_tokens || !member_indptr)) ||
+      !out_conflict)
+    return fail(RX_ERR_INVALID, "rx_batch_conflict: bad argument");
+  *out_conflict = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    const int32_t* m = member_tokens + member_indptr[r];
+    int64_t len = std::min<int64_t>(n, member_indptr[r + 1] - member_indptr[r]);
+    if (common_prefix(tokens, m, len) > match_len) {
+      *out_conflict = 1;
+      break;
+    }
+  }
+  return RX_OK;
+}
+
+}  // extern "C"
+
+// -------------------------------------------------------- decode plan
+// A tree node on the root path of >= 2 requests of the decode batch is read
+// once for all of them (a multi-query tile); each request's remaining context
+// is private.  Runs of consecutive nodes visited by the same requests are one
+// segment (a child's visitors are a subset of its parent's, so equal counts
+// mean equal sets).  Segments are cut into key chunks and member blocks, one
+// CTA per (chunk, block, KV head); every (chunk, member) yields a partial
+// (o, lse) entry that the merge combines per request.
+extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
+                                    const rx_node* prompt_node,
+                                    const int32_t* ctx_len,
+                                    const int32_t* req_rows, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t* plan, int64_t plan_cap,
+                                    rx_decode_plan_info* info) {
+  if (!c || B < 0 || !info || (B && (!prompt_node || !ctx_len || !req_rows)))
+    return fail(RX_ERR_INVALID, "rx_plan_decode: bad argument");
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(RX_ERR_INVALID, "rx_plan_decode: Hq %d not a multiple of Hkv %d", num_q_heads,
+                num_kv_heads);
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (G > rx_internal::kDecodeRowsPerCta)
+    return fail(RX_ERR_INVALID, "rx_plan_decode: group size %d above %d", G,
+                rx_internal::kDecodeRowsPerCta);
+  std::vector<std::vector<const Node*>> paths(static_cast<size_t>(B));
+  std::unordered_map<const Node*, int32_t> visits;
+  for (int32_t b = 0; b < B; ++b) {
+    const Node* x = c->find(prompt_node[b]);
+    if (!x)
+      return fail(RX_ERR_INVALID, "rx_plan_decode: unknown node %lld", (long long)prompt_node[b]);
+    if (c->depth(x) > ctx_len[b] || ctx_len[b] < 1)
+      return fail(RX_ERR_INVALID, "rx_plan_decode: ctx_len %d shorter than node depth",
+                  ctx_len[b]);
+    for (; x != c->root; x = x->parent) paths[b].push_back(x);
+    std::reverse(paths[b].begin(), paths[b].end());
+    for (const Node* n : paths[b]) visits[n] += 1;
+  }
+  struct Seg {
+    int32_t row;
+    int64_t kb, ke;
+    std::vector<int32_t> members;
+  };
+  std::vector<Seg> segs;
+  std::unordered_map<const Node*, size_t> seg_of;
+  int64_t n_shared = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const auto& path = paths[b];
+    int64_t pos = 0;
+    size_t i = 0;
+    while (i < path.size() && visits[path[i]] >= 2) {
+      int32_t cnt = visits[path[i]];
+      const Node* first = path[i];
+      int64_t start = pos;
+      while (i < path.size() && visits[path[i]] == cnt) {
+        pos += int64_t(path[i]->key.size());
+        ++i;
+      }
+      auto it = seg_of.find(first);
+      if (it == seg_of.end()) {
+        seg_of.emplace(first, segs.size());
+        segs.push_back(Seg{req_rows[b], start, pos, {b}});
+        ++n_shared;
+      } else {
+        segs[it->second].members.push_back(b);
+      }
+    }
+    if (ctx_len[b] > pos) segs.push_back(Seg{req_rows[b], pos, int64_t(ctx_len[b]), {b}});
+  }
+  // work items
+  struct Work {
+    int32_t row, kb, ke, member_off, n_members;
+  };
+  std::vector<Work> work;
+  std::vector<int32_t> members;
+  const int32_t per_block = rx_internal::kDecodeRowsPerCta / G;
+  const int64_t tile = rx_internal::kKeyTile;
+  int64_t distinct = 0;
+  for (const Seg& s : segs) {
+    int64_t n = s.ke - s.kb;
+    distinct += n;
+    int32_t k = int32_t(s.members.size());
+    int64_t chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, int64_t(8) * k * G);
+    int64_t n_chunks = (n + chunk - 1) / chunk;
+    int64_t len = (n + n_chunks - 1) / n_chunks;
+    len = (len + tile - 1) / tile * tile;
+    int32_t moff = int32_t(members.size());
+    members.insert(members.end(), s.members.begin(), s.members.end());
+    for (int64_t kb = s.kb; kb < s.ke; kb += len) {
+      int64_t ke = std::min(s.ke, kb + len);
+      for (int32_t m0 = 0; m0 < k; m0 += per_block) {
+        work.push_back(Work{s.row, int32_t(kb), int32_t(ke), moff + m0,
+                            std::min(per_block, k - m0)});
+      }
+    }
+  }
+  std::stable_sort(work.begin(), work.end(), [](const Work& a, const Work& b) {
+    return int64_t(a.ke - a.kb) * a.n_members > int64_t(b.ke - b.kb) * b.n_members;
+  });
+  std::vector<std::vector<int32_t>> parts_of(static_cast<size_t>(B));
+  int64_t n_parts = 0;
+  for (const Work& w : work) {
+    for (int32_t i = 0; i < w.n_members; ++i)
+      parts_of[size_t(members[size_t(w.member_off + i)])].push_back(int32_t(n_parts + i));
+    n_parts += w.n_members;
+  }
+  info->n_work = int64_t(work.size());
+  info->n_parts = n_parts;
+  info->n_member_entries = int64_t(members.size());
+  info->off_work = 0;
+  info->off_members = info->off_work + info->n_work * RX_WORK_WORDS;
+  info->off_req_part_indptr = info->off_members + info->n_member_entries;
+  info->off_req_parts = info->off_req_part_indptr + B + 1;
+  info->plan_words = info->off_req_parts + n_parts;
+  info->n_shared_segments = n_shared;
+  int64_t o_bytes = n_parts * num_q_heads * int64_t(head_dim) * 4;
+  int64_t l_bytes = n_parts * num_q_heads * 4;
+  info->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
+  info->distinct_kv_tokens = distinct;
+  if (!plan || plan_cap < info->plan_words)
+    return fail(RX_ERR_INVALID, "rx_plan_decode: plan needs %lld words, capacity %lld",
+                (long long)info->plan_words, (long long)plan_cap);
+  int64_t part = 0;
+  for (size_t w = 0; w < work.size(); ++w) {
+    int32_t* o = plan + info->off_work + int64_t(w) * RX_WORK_WORDS;
+    o[0] = work[w].row;
+    o[1] = work[w].kb;
+    o[2] = work[w].ke;
+    o[3] = work[w].member_off;
+    o[4] = work[w].n_members;
+    o[5] = int32_t(part);
+    o[6] = work[w].n_members * G;
+    o[7] = 0;
+    part += work[w].n_members;
+  }
+  std::memcpy(plan + info->off_members, members.data(), members.size() * sizeof(int32_t));
+  int32_t* indptr = plan + info->off_req_part_indptr;
+  int32_t* rp = plan + info->off_req_parts;
+  indptr[0] = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    std::memcpy(rp + indptr[b], parts_of[size_t(b)].data(),
+                parts_of[size_t(b)].size() * sizeof(int32_t));
+    indptr[b + 1] = indptr[b] + int32_t(parts_of[size_t(b)].size());
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_extend_plan(const int32_t* qo_indptr, int32_t R, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t* tile_indptr, int64_t* out_num_tiles) {
+  if (R < 0 || !qo_indptr || !tile_indptr || !out_num_tiles || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || (head_dim != 128 && head_dim != 256))
+    return fail(RX_ERR_INVALID, "rx_extend_plan: bad argument");
+  const int64_t G = num_q_heads / num_kv_heads;
+  const int64_t rows_per_tile = rx_internal::extend_rows_per_tile(head_dim);
+  tile_indptr[0] = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    int64_t s = qo_indptr[r + 1] - qo_indptr[r];
+    if (s < 0) return fail(RX_ERR_INVALID, "rx_extend_plan: qo_indptr not monotone");
+    int64_t t = (s * G + rows_per_tile - 1) / rows_per_tile;
+    if (tile_indptr[r] + t > INT32_MAX) return fail(RX_ERR_INVALID, "rx_extend_plan: too many tiles");
+    tile_indptr[r + 1] = int32_t(tile_indptr[r] + t);
+  }
+  *out_num_tiles = tile_indptr[R];
+  return RX_OK;
+}
+
+namespace rx_internal {
+rx_status set_error(rx_status s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace rx_internal

@@ -1,0 +1,261 @@
+"""Request flow over librx: extend batches, decode steps and finish.
+
+This drives the native calls in the order the pages give ("SGLang: Structured
+LLM Programs for Efficient Inference", section "How RadixAttention reuses past
+work": match the longest prefix, lock it, prefill only the rest, decode and
+insert, release) with the in-batch prefix rule of "SGLang: the tree, and the
+language nobody remembers", section "The scheduler is where the cache is won
+or lost" (a request sharing more with a queued batch member than with the
+tree waits for that member to populate the tree).
+
+Every cache decision is taken by the C++ library and every tensor operation
+of the method by the CUDA kernels; this module only moves arrays between
+them.  Per wave of requests:
+
+* extend batches: consecutive requests join the open batch until one shares
+  more with a member than its own tree match; ``rx_extend_begin`` (match +
+  lock + one allocation) -> upload of the batch's req_to_token rows ->
+  ``rx_kv_store`` + ``rx_extend_attention`` per layer -> ``rx_extend_end``
+  (insert the prompt, move the lock to the prompt's node);
+* ``decode_steps`` decode steps over the whole wave: ``rx_alloc`` one slot per
+  request -> device row append -> ``rx_kv_store`` -> ``rx_plan_decode`` ->
+  ``rx_decode_attention`` per layer;
+* finish: ``rx_finish`` (insert prompt + outputs, unlock).
+"""
+
+import math
+
+import numpy as np
+
+from . import rx
+
+
+class Trace:
+    """The bookkeeping decisions, in the same form as the oracle's trace."""
+
+    def __init__(self):
+        self.batches = []
+        self.decode_steps = []
+        self.finishes = []
+        self.prefilled = 0
+        self.eviction_log = []
+        self.stats = {}
+
+    def as_tuple(self):
+        return (
+            [[(rid, m, tuple(row)) for rid, m, row in b] for b in self.batches],
+            [list(s) for s in self.decode_steps],
+            list(self.finishes),
+            self.prefilled,
+            list(self.eviction_log),
+        )
+
+
+class GatherInputs:
+    """Q/K/V of the tokens a batch computes, gathered from seeded stores."""
+
+    def __init__(self, wl, values, layers):
+        import torch
+        self.torch = torch
+        self.wl = wl
+        self.values = values
+        self.layers = list(layers)
+        dev = next(iter(values["k"].values())).device
+        self.device = dev
+
+    def _idx(self, idx):
+        return self.torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int64)).to(self.device)
+
+    def extend(self, batch_no, reqs, prefix):
+        idx = np.concatenate([self.wl.prompt_store_index(r)[int(m):]
+                              for r, m in zip(reqs, prefix)])
+        ti = self._idx(idx)
+        return {layer: (self.values["q"][layer].index_select(0, ti),
+                        self.values["k"][layer].index_select(0, ti),
+                        self.values["v"][layer].index_select(0, ti)) for layer in self.layers}
+
+    def decode(self, step_no, reqs, t):
+        idx = np.array([self.wl.output_store_index(r)[t] for r in reqs], dtype=np.int64)
+        ti = self._idx(idx)
+        return {layer: (self.values["q"][layer].index_select(0, ti),
+                        self.values["k"][layer].index_select(0, ti),
+                        self.values["v"][layer].index_select(0, ti)) for layer in self.layers}
+
+
+class Engine:
+    """Runs a workload through librx.
+
+    ``device=None`` runs the host bookkeeping only (no CUDA).  With a device,
+    ``inputs`` supplies the Q/K/V of computed tokens and ``on_extend`` /
+    ``on_decode`` receive the attention outputs per layer.
+    """
+
+    def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
+                 on_decode=None, stream=None):
+        self.wl = wl
+        self.device = device
+        self.inputs = inputs
+        self.layers = list(range(wl.num_layers)) if layers is None else list(layers)
+        self.on_extend = on_extend
+        self.on_decode = on_decode
+        self.stream = stream
+        self.scale = 1.0 / math.sqrt(wl.head_dim)
+        self.max_ctx = max(len(wl.prompt_tokens(r)) for r in wl.requests.values()) + \
+            wl.decode_steps
+        self.max_wave = max(len(w) for w in wl.waves)
+        self.gpu_launches = 0
+        if device is not None:
+            import torch
+            self.torch = torch
+            L, hkv, d = wl.num_layers, wl.num_kv_heads, wl.head_dim
+            self.k_pool = torch.empty((L, hkv, wl.num_slots, d), dtype=torch.bfloat16,
+                                      device=device)
+            self.v_pool = torch.empty_like(self.k_pool)
+            self.pool = rx.pool_desc(self.k_pool, self.v_pool)
+            self.d_table = torch.zeros((self.max_wave, self.max_ctx), dtype=torch.int32,
+                                       device=device)
+            self.d_ws = torch.empty(0, dtype=torch.uint8, device=device)
+        # host staging
+        self.h_table = np.zeros((self.max_wave, self.max_ctx), dtype=np.int32)
+        self.plan_buf = np.empty(1 << 16, dtype=np.int32)
+
+    # ------------------------------------------------------------------ run
+    def run(self):
+        self.cache = rx.RadixCache(self.wl.num_slots)
+        self.trace = Trace()
+        self.batch_no = 0
+        self.step_no = 0
+        for wave in self.wl.waves:
+            self._run_wave(wave)
+        self.trace.eviction_log = self.cache.eviction_log()
+        st = self.cache.stats()
+        self.trace.stats = {
+            "cached": st["cached_tokens"], "evictable": st["evictable_tokens"],
+            "protected": st["protected_tokens"], "free": st["free_slots"],
+            "num_nodes": st["num_nodes"]}
+        return self.trace
+
+    def _run_wave(self, wave):
+        wl = self.wl
+        prompts = [wl.prompt_tokens(r).astype(np.int32) for r in wave]
+        lens = np.array([len(p) for p in prompts], dtype=np.int64)
+        indptr = np.zeros(len(wave) + 1, dtype=np.int64)
+        np.cumsum(lens, out=indptr[1:])
+        tokens = np.concatenate(prompts).astype(np.int32)
+        self.h_table[:len(wave)] = 0
+        prompt_nodes = np.zeros(len(wave), dtype=np.int64)
+        start = 0
+        for j in range(len(wave)):
+            if j > start:
+                m = self.cache.match_length(prompts[j][:-1])
+                seg = tokens[indptr[start]:indptr[j]]
+                sub = indptr[start:j + 1] - indptr[start]
+                if rx.batch_conflict(prompts[j], m, seg, sub):
+                    self._extend_batch(wave, start, j, tokens, indptr, prompt_nodes)
+                    start = j
+        self._extend_batch(wave, start, len(wave), tokens, indptr, prompt_nodes)
+        ctx = lens.astype(np.int32).copy()
+        for t in range(wl.decode_steps):
+            self._decode_step(wave, t, ctx, prompt_nodes)
+            ctx += 1
+        # finish: insert prompt ++ outputs, unlock
+        outs = [wl.output_tokens(r)[:wl.decode_steps].astype(np.int32) for r in wave]
+        full = np.concatenate([np.concatenate([p, o]) for p, o in zip(prompts, outs)])
+        findptr = np.zeros(len(wave) + 1, dtype=np.int64)
+        np.cumsum(lens + wl.decode_steps, out=findptr[1:])
+        already = self.cache.finish(full, findptr, self.h_table[:len(wave)], lens, prompt_nodes)
+        for r, a in zip(wave, already):
+            self.trace.finishes.append((r.rid, int(a)))
+
+    def _extend_batch(self, wave, j0, j1, tokens, indptr, prompt_nodes):
+        reqs = wave[j0:j1]
+        tok = tokens[indptr[j0]:indptr[j1]]
+        ind = indptr[j0:j1 + 1] - indptr[j0]
+        table = self.h_table[j0:j1]
+        prefix, match_nodes, new_slots = self.cache.extend_begin(tok, ind, table)
+        recs = []
+        for i, r in enumerate(reqs):
+            n = int(ind[i + 1] - ind[i])
+            recs.append((r.rid, int(prefix[i]), table[i, :n].copy()))
+            self.trace.prefilled += n - int(prefix[i])
+        self.trace.batches.append(recs)
+        if self.device is not None:
+            self._extend_device(reqs, j0, j1, prefix, ind, new_slots)
+        prompt_nodes[j0:j1] = self.cache.extend_end(tok, ind, table, prefix, match_nodes)
+        self.batch_no += 1
+
+    def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):
+        torch = self.torch
+        wl = self.wl
+        R = j1 - j0
+        qo = np.zeros(R + 1, dtype=np.int32)
+        np.cumsum((ind[1:] - ind[:-1]) - prefix, out=qo[1:])
+        tiles, n_tiles = rx.extend_plan(qo, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+        meta = np.concatenate([np.arange(j0, j1, dtype=np.int32), prefix.astype(np.int32), qo,
+                               tiles]).astype(np.int32)
+        d_meta = torch.from_numpy(meta).to(self.device, non_blocking=False)
+        d_rows, d_prefix = d_meta[:R], d_meta[R:2 * R]
+        d_qo, d_tiles = d_meta[2 * R:3 * R + 1], d_meta[3 * R + 1:]
+        width = int(max(ind[1:] - ind[:-1]))
+        self.d_table[j0:j1, :width].copy_(torch.from_numpy(self.h_table[j0:j1, :width]))
+        d_slots = torch.from_numpy(np.ascontiguousarray(new_slots)).to(self.device)
+        inputs = self.inputs.extend(self.batch_no, reqs, prefix)
+        total_q = int(qo[-1])
+        outs = {}
+        for layer in self.layers:
+            q, k, v = inputs[layer]
+            rx.kv_store(self.pool, layer, d_slots, k, v, self.stream)
+            out = torch.empty((total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
+                              device=self.device)
+            lse = torch.empty((total_q, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            rx.extend_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_rows,
+                                d_prefix, d_qo, d_tiles, R, n_tiles, self.scale, out, lse,
+                                self.stream)
+            self.gpu_launches += 2
+            outs[layer] = (out, lse)
+        if self.on_extend is not None:
+            self.on_extend(self.batch_no, [r.rid for r in reqs], prefix.copy(), qo, outs)
+
+    def _decode_step(self, wave, t, ctx, prompt_nodes):
+        B = len(wave)
+        slots = self.cache.alloc(B)
+        self.h_table[np.arange(B), ctx] = slots
+        self.trace.decode_steps.append([(r.rid, int(s)) for r, s in zip(wave, slots)])
+        if self.device is not None:
+            self._decode_device(wave, t, ctx, prompt_nodes, slots)
+        self.step_no += 1
+
+    def _decode_device(self, wave, t, ctx, prompt_nodes, slots):
+        torch = self.torch
+        wl = self.wl
+        B = len(wave)
+        rows = np.arange(B, dtype=np.int32)
+        ctx_now = (ctx + 1).astype(np.int32)
+        self.plan_buf, info = self.cache.plan_decode(
+            prompt_nodes, ctx_now, rows, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+            self.plan_buf)
+        pw = int(info.plan_words)
+        host = np.concatenate([rows, ctx.astype(np.int32), slots.astype(np.int32),
+                               self.plan_buf[:pw]])
+        d_host = torch.from_numpy(host).to(self.device)
+        d_rows, d_pos, d_slots = d_host[:B], d_host[B:2 * B], d_host[2 * B:3 * B]
+        d_plan = d_host[3 * B:]
+        rx.req_to_token_write(self.d_table, d_rows, d_pos, d_slots, self.stream)
+        if self.d_ws.numel() < info.workspace_bytes:
+            self.d_ws = torch.empty(int(info.workspace_bytes * 1.5) + 256, dtype=torch.uint8,
+                                    device=self.device)
+        inputs = self.inputs.decode(self.step_no, wave, t)
+        outs = {}
+        for layer in self.layers:
+            q, k, v = inputs[layer]
+            rx.kv_store(self.pool, layer, d_slots, k, v, self.stream)
+            out = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
+                              device=self.device)
+            lse = torch.empty((B, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            rx.decode_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_plan, info,
+                                B, self.scale, out, lse, self.d_ws, self.stream)
+            self.gpu_launches += 3
+            outs[layer] = (out, lse)
+        self.gpu_launches += 1
+        if self.on_decode is not None:
+            self.on_decode(self.step_no, t, [r.rid for r in wave], ctx_now, outs, info)

@@ -1,0 +1,342 @@
+"""ctypes binding of librx (include/rx.h): argument marshalling only.
+
+Every computation happens in the native library: the radix cache in C++, the
+attention and KV stores in sm_103a CUDA kernels.  Host arrays are numpy
+arrays (int32 tokens/slots, int64 indptrs); device buffers are torch tensors
+whose ``data_ptr()`` is passed through.  Importing this module loads
+``lib/librx.so`` and raises ``ImportError`` if it has not been built: there is
+no fallback path.
+"""
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "librx.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"librx.so not found at {LIB_PATH}; build it first with "
+        "`python -c 'import __graft_entry__ as g; g.build()'`")
+_lib = C.CDLL(LIB_PATH)
+
+RX_OK, RX_ERR_INVALID, RX_ERR_NO_SPACE, RX_ERR_STATE, RX_ERR_CUDA = range(5)
+RX_WORK_WORDS = 8
+
+
+class RxError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"rx status {status}: {msg}")
+        self.status = status
+
+
+class NoSpace(RxError):
+    pass
+
+
+class StateError(RxError):
+    pass
+
+
+class rx_config(C.Structure):
+    _fields_ = [("num_slots", C.c_int64), ("page_size", C.c_int32), ("reserved", C.c_int32)]
+
+
+class rx_stats_t(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in (
+        "cached_tokens", "evictable_tokens", "protected_tokens", "free_slots",
+        "num_nodes", "evicted_nodes", "evicted_tokens", "clock")]
+
+
+class rx_evict_rec(C.Structure):
+    _fields_ = [("node_id", C.c_int64), ("num_tokens", C.c_int64)]
+
+
+class rx_decode_plan_info(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in (
+        "plan_words", "n_work", "n_parts", "n_member_entries", "off_work",
+        "off_members", "off_req_part_indptr", "off_req_parts",
+        "n_shared_segments", "workspace_bytes", "distinct_kv_tokens")]
+
+
+class rx_pool_desc(C.Structure):
+    _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("num_slots", C.c_int64),
+                ("num_layers", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("reserved", C.c_int32)]
+
+
+P = C.c_void_p
+I32, I64, F32, SZ = C.c_int32, C.c_int64, C.c_float, C.c_size_t
+_SIGS = {
+    "rx_cache_create": [P, P],
+    "rx_cache_destroy": [P],
+    "rx_match_length": [P, P, I64, P],
+    "rx_match_prefix": [P, P, I64, P, P, P],
+    "rx_lock": [P, I64],
+    "rx_unlock": [P, I64],
+    "rx_alloc": [P, I64, P],
+    "rx_evict": [P, I64, P],
+    "rx_free": [P, P, I64],
+    "rx_insert": [P, P, P, I64, P, P],
+    "rx_stats": [P, P],
+    "rx_eviction_log": [P, I64, P, I64, P],
+    "rx_node_depth": [P, I64, P],
+    "rx_extend_begin": [P, I32, P, P, P, I64, P, P, P, P],
+    "rx_extend_end": [P, I32, P, P, P, I64, P, P, P],
+    "rx_finish": [P, I32, P, P, P, I64, P, P, P],
+    "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
+    "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
+    "rx_kv_store": [P, I32, P, P, P, I64, P],
+    "rx_req_to_token_write": [P, I64, P, P, P, I64, P],
+    "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
+    "rx_extend_attention": [P, I32, P, I32, P, I64, P, P, P, P, I32, I64, F32, P, P, P],
+    "rx_decode_attention": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P, SZ, P],
+    "rx_device_check": [P],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = C.c_int
+_lib.rx_last_error.argtypes = [C.c_char_p, C.c_size_t]
+_lib.rx_last_error.restype = C.c_size_t
+_lib.rx_build_info.argtypes = []
+_lib.rx_build_info.restype = C.c_char_p
+
+EXPORTED = sorted(list(_SIGS) + ["rx_last_error", "rx_build_info"])
+
+
+def last_error():
+    buf = C.create_string_buffer(1024)
+    _lib.rx_last_error(buf, 1024)
+    return buf.value.decode()
+
+
+def _check(st):
+    if st == RX_OK:
+        return
+    msg = last_error()
+    if st == RX_ERR_NO_SPACE:
+        raise NoSpace(st, msg)
+    if st == RX_ERR_STATE:
+        raise StateError(st, msg)
+    raise RxError(st, msg)
+
+
+def _p(a):
+    """Pointer of a contiguous numpy array (or None)."""
+    if a is None:
+        return None
+    return a.ctypes.data
+
+
+def _i32(x):
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _i64(x):
+    return np.ascontiguousarray(x, dtype=np.int64)
+
+
+def build_info():
+    return _lib.rx_build_info().decode()
+
+
+# -------------------------------------------------------------- host cache
+class RadixCache:
+    """Owner of one native rx_cache."""
+
+    def __init__(self, num_slots):
+        cfg = rx_config(int(num_slots), 1, 0)
+        h = C.c_void_p()
+        _check(_lib.rx_cache_create(C.byref(cfg), C.byref(h)))
+        self._h = h
+        self.num_slots = int(num_slots)
+
+    def close(self):
+        if self._h:
+            _lib.rx_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # S1
+    def match_length(self, tokens):
+        t = _i32(tokens)
+        out = C.c_int64()
+        _check(_lib.rx_match_length(self._h, _p(t), len(t), C.byref(out)))
+        return out.value
+
+    def match_prefix(self, tokens):
+        t = _i32(tokens)
+        slots = np.empty(max(1, len(t)), dtype=np.int32)
+        n = C.c_int64()
+        node = C.c_int64()
+        _check(_lib.rx_match_prefix(self._h, _p(t), len(t), _p(slots), C.byref(n),
+                                    C.byref(node)))
+        return slots[:n.value].copy(), node.value
+
+    # S2
+    def lock(self, node):
+        _check(_lib.rx_lock(self._h, int(node)))
+
+    def unlock(self, node):
+        _check(_lib.rx_unlock(self._h, int(node)))
+
+    # S3
+    def alloc(self, k, out=None):
+        if out is None:
+            out = np.empty(max(1, k), dtype=np.int32)
+        _check(_lib.rx_alloc(self._h, int(k), _p(out)))
+        return out[:k]
+
+    def evict(self, k):
+        f = C.c_int64()
+        _check(_lib.rx_evict(self._h, int(k), C.byref(f)))
+        return f.value
+
+    def free(self, slots):
+        s = _i32(slots)
+        _check(_lib.rx_free(self._h, _p(s), len(s)))
+
+    # S10
+    def insert(self, tokens, slots):
+        t, s = _i32(tokens), _i32(slots)
+        already = C.c_int64()
+        node = C.c_int64()
+        _check(_lib.rx_insert(self._h, _p(t), _p(s), len(t), C.byref(already), C.byref(node)))
+        return already.value, node.value
+
+    def stats(self):
+        st = rx_stats_t()
+        _check(_lib.rx_stats(self._h, C.byref(st)))
+        return {n: getattr(st, n) for n, _ in rx_stats_t._fields_}
+
+    def eviction_log(self):
+        total = C.c_int64()
+        _check(_lib.rx_eviction_log(self._h, 0, None, 0, C.byref(total)))
+        n = total.value
+        recs = (rx_evict_rec * max(1, n))()
+        _check(_lib.rx_eviction_log(self._h, 0, recs, n, C.byref(total)))
+        return [(recs[i].node_id, recs[i].num_tokens) for i in range(n)]
+
+    def node_depth(self, node):
+        d = C.c_int64()
+        _check(_lib.rx_node_depth(self._h, int(node), C.byref(d)))
+        return d.value
+
+    # batch steps
+    def extend_begin(self, tokens, tok_indptr, req_to_token):
+        """req_to_token: int32 [R, row_stride] host array written in place."""
+        R = len(tok_indptr) - 1
+        prefix = np.empty(max(1, R), dtype=np.int32)
+        nodes = np.empty(max(1, R), dtype=np.int64)
+        new = np.empty(max(1, int(tok_indptr[-1])), dtype=np.int32)
+        total = C.c_int64()
+        _check(_lib.rx_extend_begin(self._h, R, _p(tokens), _p(tok_indptr), _p(req_to_token),
+                                    req_to_token.shape[1], _p(prefix), _p(nodes), _p(new),
+                                    C.byref(total)))
+        return prefix[:R], nodes[:R], new[:total.value]
+
+    def extend_end(self, tokens, tok_indptr, req_to_token, prefix, match_nodes):
+        R = len(tok_indptr) - 1
+        out = np.empty(max(1, R), dtype=np.int64)
+        _check(_lib.rx_extend_end(self._h, R, _p(tokens), _p(tok_indptr), _p(req_to_token),
+                                  req_to_token.shape[1], _p(prefix), _p(match_nodes), _p(out)))
+        return out[:R]
+
+    def finish(self, tokens, tok_indptr, req_to_token, prompt_len, prompt_nodes):
+        R = len(tok_indptr) - 1
+        already = np.empty(max(1, R), dtype=np.int64)
+        _check(_lib.rx_finish(self._h, R, _p(tokens), _p(tok_indptr), _p(req_to_token),
+                              req_to_token.shape[1], _p(prompt_len), _p(prompt_nodes),
+                              _p(already)))
+        return already[:R]
+
+    def plan_decode(self, prompt_nodes, ctx_len, req_rows, hq, hkv, d, plan=None):
+        B = len(prompt_nodes)
+        info = rx_decode_plan_info()
+        pn, cl, rr = _i64(prompt_nodes), _i32(ctx_len), _i32(req_rows)
+        cap = 0 if plan is None else len(plan)
+        st = _lib.rx_plan_decode(self._h, B, _p(pn), _p(cl), _p(rr), hq, hkv, d,
+                                 _p(plan) if plan is not None else None, cap, C.byref(info))
+        if st != RX_OK and (plan is None or len(plan) < info.plan_words) and info.plan_words > 0:
+            plan = np.empty(int(info.plan_words) * 2, dtype=np.int32)
+            st = _lib.rx_plan_decode(self._h, B, _p(pn), _p(cl), _p(rr), hq, hkv, d, _p(plan),
+                                     len(plan), C.byref(info))
+        _check(st)
+        return plan, info
+
+
+def batch_conflict(tokens, match_len, member_tokens, member_indptr):
+    out = C.c_int32()
+    t = _i32(tokens)
+    R = len(member_indptr) - 1
+    _check(_lib.rx_batch_conflict(_p(t), len(t), int(match_len), R, _p(member_tokens),
+                                  _p(member_indptr), C.byref(out)))
+    return bool(out.value)
+
+
+def extend_plan(qo_indptr, hq, hkv, d):
+    qo = _i32(qo_indptr)
+    R = len(qo) - 1
+    tiles = np.empty(R + 1, dtype=np.int32)
+    n = C.c_int64()
+    _check(_lib.rx_extend_plan(_p(qo), R, hq, hkv, d, _p(tiles), C.byref(n)))
+    return tiles, n.value
+
+
+# ------------------------------------------------------------- device ops
+def pool_desc(k_pool, v_pool):
+    """Descriptor of torch bf16 pools shaped [L, Hkv, N, d]."""
+    L, hkv, n, d = k_pool.shape
+    return rx_pool_desc(k_pool.data_ptr(), v_pool.data_ptr(), n, L, hkv, d, 0)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def kv_store(pool, layer, d_slots, d_k, d_v, stream=None):
+    _check(_lib.rx_kv_store(C.byref(pool), layer, d_slots.data_ptr(), d_k.data_ptr(),
+                            d_v.data_ptr(), d_slots.numel(), _stream(stream)))
+
+
+def req_to_token_write(d_table, d_rows, d_pos, d_slots, stream=None):
+    _check(_lib.rx_req_to_token_write(d_table.data_ptr(), d_table.shape[1], d_rows.data_ptr(),
+                                      d_pos.data_ptr(), d_slots.data_ptr(), d_slots.numel(),
+                                      _stream(stream)))
+
+
+def extend_attention(pool, layer, d_q, hq, d_table, d_req_rows, d_prefix_len, d_qo_indptr,
+                     d_tile_indptr, R, num_tiles, scale, d_out, d_lse, stream=None):
+    _check(_lib.rx_extend_attention(C.byref(pool), layer, d_q.data_ptr(), hq,
+                                    d_table.data_ptr(), d_table.shape[1], d_req_rows.data_ptr(),
+                                    d_prefix_len.data_ptr(), d_qo_indptr.data_ptr(),
+                                    d_tile_indptr.data_ptr(), R, num_tiles, scale,
+                                    d_out.data_ptr(), d_lse.data_ptr(), _stream(stream)))
+
+
+def decode_attention(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_out, d_lse,
+                     d_workspace, stream=None):
+    _check(_lib.rx_decode_attention(C.byref(pool), layer, d_q.data_ptr(), hq, d_table.data_ptr(),
+                                    d_table.shape[1], d_plan.data_ptr(), C.byref(info), B, scale,
+                                    d_out.data_ptr(), d_lse.data_ptr(), d_workspace.data_ptr(),
+                                    d_workspace.numel() * d_workspace.element_size(),
+                                    _stream(stream)))
+
+
+def device_check():
+    flags = C.c_int32()
+    st = _lib.rx_device_check(C.byref(flags))
+    if st != RX_OK:
+        raise RxError(st, last_error() + f" (flags {flags.value})")
+    return flags.value

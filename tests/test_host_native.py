@@ -1,0 +1,226 @@
+"""librx host side on CPU: exported symbols, argument checks, and bit-exact
+agreement of the native radix cache with the oracle (slot tables, match
+lengths, prefilled counts, eviction order)."""
+
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, read_golden
+
+rx = pytest.importorskip("radix_tree_prefix_gb300.rx",
+                         reason="librx.so not built (run __graft_entry__.build())")
+from oracle.harness import run_bookkeeping  # noqa: E402
+from oracle.radix_cache import NoSpace as ONoSpace  # noqa: E402
+from oracle.radix_cache import RadixCache as ORadix  # noqa: E402
+from radix_tree_prefix_gb300 import workloads  # noqa: E402
+from radix_tree_prefix_gb300.engine import Engine  # noqa: E402
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "rx.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rx_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(rx._lib, n), f"{n} declared in rx.h but not exported"
+    assert set(names) <= set(rx.EXPORTED), "binding lacks a declared entry point"
+
+
+def test_argument_errors_need_no_gpu():
+    c = rx.RadixCache(16)
+    _, node = c.insert([1, 2], c.alloc(2))
+    with pytest.raises(rx.StateError):
+        c.unlock(node)
+    with pytest.raises(rx.RxError) as e:
+        c.lock(12345)
+    assert e.value.status == rx.RX_ERR_INVALID
+    with pytest.raises(rx.NoSpace):
+        c.alloc(100)
+    # device entry points validate before touching CUDA
+    bad = rx.rx_pool_desc(16, 16, 8, 1, 1, 64, 0)     # head_dim 64 unsupported
+    import ctypes as C
+    st = rx._lib.rx_kv_store(C.byref(bad), 0, None, None, None, 1, None)
+    assert st == rx.RX_ERR_INVALID and "head_dim" in rx.last_error()
+    bad = rx.rx_pool_desc(16, 16, 8, 1, 2, 128, 0)
+    st = rx._lib.rx_extend_attention(C.byref(bad), 3, None, 4, None, 0, None, None, None,
+                                     None, 1, 1, 1.0, None, None, None)
+    assert st == rx.RX_ERR_INVALID and "layer" in rx.last_error()
+    cfg = rx.rx_config(8, 2, 0)
+    h = C.c_void_p()
+    assert rx._lib.rx_cache_create(C.byref(cfg), C.byref(h)) == rx.RX_ERR_INVALID
+
+
+def test_worked_eviction_example_native():
+    """The worked example's victims and occupancy on the native cache."""
+    g = {}
+    for ln in read_golden("worked_eviction.txt"):
+        p = ln.split()
+        if p[0] != "case":
+            g[p[0]] = int(p[1])
+    for locked, victim, held in (("C", "A", 3500), ("AC", "B", 3800), ("ABC", None, None)):
+        c = rx.RadixCache(g["capacity"] + 1)
+        rng = random.Random(7)
+        seq = lambda n: [rng.randrange(32000) for _ in range(n)]
+        s = seq(g["S"])
+        nodes = {}
+        for b in "ABC":
+            toks = s + seq(g[b])
+            slots, _ = c.match_prefix(toks)
+            new = c.alloc(len(toks) - len(slots))
+            _, nodes[b] = c.insert(toks, np.concatenate([slots, new]))
+        for b in locked:
+            c.lock(nodes[b])
+        d = s + seq(g["D_new"])
+        slots, dn = c.match_prefix(d[:-1])
+        c.lock(dn)
+        if victim is None:
+            with pytest.raises(rx.NoSpace):
+                c.alloc(g["D_new"])
+            assert c.eviction_log() == []
+            continue
+        new = c.alloc(g["D_new"])
+        assert c.eviction_log() == [(nodes[victim], g[victim])]
+        c.insert(d, np.concatenate([slots, new]))
+        assert c.stats()["cached_tokens"] == held
+
+
+def test_random_ops_match_oracle():
+    """Same random operation sequence on both caches: identical results."""
+    rng = random.Random(21)
+    for trial in range(60):
+        n_slots = rng.randint(16, 80)
+        o, n = ORadix(n_slots), rx.RadixCache(n_slots)
+        onodes, nnodes = [], []
+        for step in range(120):
+            r = rng.random()
+            seq = [rng.randrange(rng.choice([2, 3, 5])) for _ in range(rng.randint(1, 14))]
+            if r < 0.2:
+                assert o.match_length(seq) == n.match_length(seq)
+                os_, on = o.match_prefix(seq)
+                ns_, nn = n.match_prefix(seq)
+                assert list(os_) == ns_.tolist() and on.id == nn
+            elif r < 0.55:
+                os_, on = o.match_prefix(seq[:-1])
+                ns_, nn = n.match_prefix(seq[:-1])
+                assert on.id == nn
+                k = len(seq) - len(os_)
+                try:
+                    onew = o.alloc(k)
+                except ONoSpace:
+                    onew = None
+                try:
+                    nnew = n.alloc(k).tolist()
+                except rx.NoSpace:
+                    nnew = None
+                assert onew == nnew
+                if onew is None:
+                    continue
+                oa, on2 = o.insert(seq, list(os_) + onew)
+                na, nn2 = n.insert(seq, ns_.tolist() + nnew)
+                assert (oa, on2.id) == (na, nn2)
+                o.free((list(os_) + onew)[len(os_):oa])
+                n.free((ns_.tolist() + nnew)[len(ns_):na])
+                o.inc_lock_ref(on2)
+                n.lock(nn2)
+                onodes.append(on2)
+                nnodes.append(nn2)
+            elif r < 0.8 and onodes:
+                i = rng.randrange(len(onodes))
+                o.dec_lock_ref(onodes.pop(i))
+                n.unlock(nnodes.pop(i))
+            else:
+                k = rng.randint(1, 10)
+                assert o.evict(k) == n.evict(k)
+            st = n.stats()
+            assert st["cached_tokens"] == o.cached_size()
+            assert st["evictable_tokens"] == o.evictable_size_
+            assert st["protected_tokens"] == o.protected_size_
+            assert st["free_slots"] == len(o.free_slots)
+            assert st["num_nodes"] == o.num_nodes()
+            assert n.eviction_log() == o.eviction_log
+
+
+SCALED = {
+    "nested_share": lambda: workloads.nested_share(),
+    "agent_loop": lambda: workloads.agent_loop(),
+    "fork_tree_small": lambda: workloads.fork_tree(branching=4, depth=3, level_tokens=40,
+                                                   decode_steps=5),
+    "multi_turn_small": lambda: workloads.multi_turn_chat(sessions=12, turns=4, system=300,
+                                                         user=30, decode_steps=6, layers=1),
+    "long_shared_small": lambda: workloads.long_shared(batch=8, prefix=2048, unique=128,
+                                                       decode_steps=8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCALED))
+def test_request_flow_matches_oracle(name):
+    wl = SCALED[name]()
+    got = Engine(wl).run()
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+    assert got.prefilled == want.prefilled
+    assert got.as_tuple() == want.as_tuple()
+    assert got.stats == want.stats
+    if name == "nested_share":
+        assert got.prefilled == 3060
+    if name.startswith("fork_tree"):
+        assert len(got.eviction_log) > 0
+
+
+def test_fork_tree_full_size_bookkeeping():
+    """Workload 4 at full size: eviction order and slot tables bit-exact."""
+    wl = workloads.fork_tree()
+    got = Engine(wl).run()
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+    assert got.as_tuple() == want.as_tuple()
+    assert len(got.eviction_log) > 100
+
+
+def test_decode_plan_covers_every_context_once():
+    """Shared segments are read once; each request's keys are covered once."""
+    wl = workloads.fork_tree(branching=3, depth=3, level_tokens=10, decode_steps=0)
+    c = rx.RadixCache(wl.num_slots + 1000)
+    wave = wl.waves[0]
+    nodes, lens = [], []
+    for r in wave:
+        toks = wl.prompt_tokens(r)
+        slots, _ = c.match_prefix(toks)
+        new = c.alloc(len(toks) - len(slots))
+        _, node = c.insert(toks, np.concatenate([slots, new]))
+        c.lock(node)
+        nodes.append(node)
+        lens.append(len(toks) + 2)             # two decode tokens beyond the tree
+    hq, hkv, d = 32, 8, 128
+    G = hq // hkv
+    plan, info = c.plan_decode(nodes, lens, list(range(len(wave))), hq, hkv, d)
+    W = rx.RX_WORK_WORDS
+    work = plan[info.off_work:info.off_work + info.n_work * W].reshape(-1, W)
+    members = plan[info.off_members:info.off_members + info.n_member_entries]
+    covered = {b: [] for b in range(len(wave))}
+    for row, kb, ke, moff, nm, pbase, nrows, _ in work:
+        assert nrows == nm * G and nm * G <= 64
+        for i in range(nm):
+            b = int(members[moff + i])
+            covered[b].append((int(kb), int(ke)))
+            if nm > 1 or ke <= 30:   # shared chunks read a member's own row range
+                assert kb < ke
+    for b, rngs in covered.items():
+        rngs.sort()
+        pos = 0
+        for kb, ke in rngs:
+            assert kb == pos
+            pos = ke
+        assert pos == lens[b]
+    # level-1 node (10 tokens) is shared by all 9 leaves, level-2 by 3 each
+    assert info.n_shared_segments == 1 + 3
+    assert info.distinct_kv_tokens == 10 + 3 * 10 + 9 * 10 + 9 * 2
+    indptr = plan[info.off_req_part_indptr:info.off_req_part_indptr + len(wave) + 1]
+    assert indptr[-1] == info.n_parts

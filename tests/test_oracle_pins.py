@@ -407,3 +407,16 @@ def test_evicted_slots_return_in_stored_order():
     cache.free([s for s in slots if s not in order])
     cache.insert([7, 8, 9, 10, 11], order)
     assert cache.alloc(5) == order             # forces eviction of the node
+
+
+def test_pool_store_writes_only_its_slots():
+    from oracle import pool as opool
+    rng = np.random.default_rng(9)
+    base = rng.standard_normal((2, 3, 10, 4))
+    kv = rng.standard_normal((3, 3, 4))
+    out = opool.store(base, 1, [7, 2, 5], kv)
+    for i, s in enumerate([7, 2, 5]):
+        assert np.array_equal(out[1, :, s, :], kv[i])
+    untouched = [s for s in range(10) if s not in (7, 2, 5)]
+    assert np.array_equal(out[1, :, untouched, :], base[1, :, untouched, :])
+    assert np.array_equal(out[0], base[0])
