@@ -217,14 +217,17 @@ rx_status rx_extend_begin(rx_cache* cache, int32_t R, const int32_t* tokens,
 
 /* S10 after an extend batch: for each request in order rx_insert(prompt,
  * row), rx_lock(prompt node), rx_unlock(matched node).  Writes
- * out_prompt_node[r].  RX_ERR_STATE if a prompt finds more of itself cached
- * than its match (two requests of one batch shared more than their match:
- * the caller's batching must prevent that). */
+ * out_prompt_node[r].  If a prompt finds more of itself cached than its
+ * match (an identical prompt was inserted by an earlier batch), the
+ * request's own slots for that part go back to the free list and its row is
+ * rewritten in place with the tree's slots (same tokens after the same
+ * predecessors, so the same K/V); *out_rewritten (may be NULL) counts the
+ * requests whose row changed, so the caller can refresh device rows. */
 rx_status rx_extend_end(rx_cache* cache, int32_t R, const int32_t* tokens,
-                        const int64_t* tok_indptr,
-                        const int32_t* req_to_token, int64_t row_stride,
-                        const int32_t* prefix_len,
-                        const rx_node* match_node, rx_node* out_prompt_node);
+                        const int64_t* tok_indptr, int32_t* req_to_token,
+                        int64_t row_stride, const int32_t* prefix_len,
+                        const rx_node* match_node, rx_node* out_prompt_node,
+                        int64_t* out_rewritten);
 
 /* Finish (S10): for each request, rx_insert(prompt ++ outputs, row) where
  * tokens/tok_indptr hold prompt ++ outputs and the row holds their slots;

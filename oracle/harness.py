@@ -26,6 +26,9 @@ Readings (listed in DESIGN.md):
 * a decode step allocates one slot per request (in order), stores the token's
   K/V there and attends over the request's context including that token; decode
   tokens stay outside the tree until finish;
+* when a prompt's insert finds more of it cached than its match (identical
+  prompts in consecutive batches), the request's own slots for that part are
+  freed and its row takes the tree's slots, which hold the same K/V;
 * finish is ``insert(prompt + outputs)`` then unlock of the prompt's node; slots
   of any part that another request had already inserted are freed.
 
@@ -115,10 +118,11 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
             if on_extend is not None:
                 on_extend(records)
             for (j, slots, node), (rid, m, row) in zip(matched, records):
-                already, node2 = cache.insert(prompts[j], row)
-                if already != m:
-                    raise AssertionError(
-                        "in-batch duplicate prefill: rule violated")
+                already, node2 = cache.insert(prompts[j], rows[rid])
+                if already > m:
+                    tree = cache.lookup_slots(prompts[j])[m:already]
+                    cache.free(rows[rid][m:already])
+                    rows[rid][m:already] = tree
                 cache.inc_lock_ref(node2)
                 cache.dec_lock_ref(node)
                 prompt_nodes[rid] = node2

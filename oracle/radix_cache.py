@@ -132,6 +132,23 @@ class RadixCache:
             node = child
         return pos
 
+    def lookup_slots(self, tokens):
+        """Slots of the longest cached prefix of ``tokens``, no side effects."""
+        node = self.root
+        pos = 0
+        out = []
+        while pos < len(tokens):
+            child = node.children.get(tokens[pos])
+            if child is None:
+                break
+            k = common_prefix_length(child.key, tokens[pos:])
+            out.extend(child.value[:k])
+            pos += k
+            if k < len(child.key):
+                break
+            node = child
+        return out
+
     def match_prefix(self, tokens):
         """Walk from the root as far as ``tokens`` match.
 

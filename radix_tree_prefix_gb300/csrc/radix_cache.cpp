@@ -147,6 +147,25 @@ struct rx_cache {
     return pos;
   }
 
+  // Slots of the longest cached prefix of t[0..n) (no split, no touch);
+  // writes them to out and returns the matched length.
+  int64_t lookup_slots(const int32_t* t, int64_t n, int32_t* out) const {
+    const Node* node = root;
+    int64_t pos = 0;
+    while (pos < n) {
+      auto it = node->children.find(t[pos]);
+      if (it == node->children.end()) break;
+      const Node* c = it->second;
+      int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
+      int64_t k = common_prefix(c->key.data(), t + pos, lim);
+      std::memcpy(out + pos, c->value.data(), size_t(k) * sizeof(int32_t));
+      pos += k;
+      if (k < int64_t(c->key.size())) break;
+      node = c;
+    }
+    return pos;
+  }
+
   // Walk (splitting at the end of the match); returns the deepest node and
   // the matched length; appends matched slots to `slots` if non-null.
   Node* walk(const int32_t* t, int64_t n, int64_t* matched,
@@ -456,9 +475,10 @@ rx_status rx_extend_begin(rx_cache* c, int32_t R, const int32_t* tokens,
 }
 
 rx_status rx_extend_end(rx_cache* c, int32_t R, const int32_t* tokens,
-                        const int64_t* tok_indptr, const int32_t* req_to_token,
+                        const int64_t* tok_indptr, int32_t* req_to_token,
                         int64_t row_stride, const int32_t* prefix_len,
-                        const rx_node* match_node, rx_node* out_prompt_node) {
+                        const rx_node* match_node, rx_node* out_prompt_node,
+                        int64_t* out_rewritten) {
   if (!c || R < 0 || !tok_indptr || (R && (!tokens || !req_to_token || !prefix_len ||
                                           !match_node || !out_prompt_node)))
     return fail(RX_ERR_INVALID, "rx_extend_end: bad argument");
@@ -466,20 +486,30 @@ rx_status rx_extend_end(rx_cache* c, int32_t R, const int32_t* tokens,
     if (!c->find(match_node[r]))
       return fail(RX_ERR_INVALID, "rx_extend_end: unknown node %lld", (long long)match_node[r]);
   }
+  int64_t rewritten = 0;
+  std::vector<int32_t> tree;
   for (int32_t r = 0; r < R; ++r) {
     const int32_t* t = tokens + tok_indptr[r];
     int64_t n = tok_indptr[r + 1] - tok_indptr[r];
+    int32_t* row = req_to_token + r * row_stride;
     int64_t already = 0;
-    Node* x = c->insert(t, req_to_token + r * row_stride, n, &already);
-    if (already != prefix_len[r])
-      return fail(RX_ERR_STATE,
-                  "rx_extend_end: request %d found %lld tokens cached but matched %d; "
-                  "two requests of one batch shared more than their match",
-                  r, (long long)already, prefix_len[r]);
+    Node* x = c->insert(t, row, n, &already);
+    if (already > prefix_len[r]) {
+      // Identical prompt inserted by an earlier batch: adopt the tree's slots
+      // (same tokens, same predecessors, same K/V) and free this request's.
+      tree.resize(size_t(n));
+      c->lookup_slots(t, already, tree.data());
+      for (int64_t i = prefix_len[r]; i < already; ++i) {
+        c->free_list.push_back(row[i]);
+        row[i] = tree[size_t(i)];
+      }
+      ++rewritten;
+    }
     c->lock(x);
     c->unlock(c->find(match_node[r]));
     out_prompt_node[r] = x->id;
   }
+  if (out_rewritten) *out_rewritten = rewritten;
   return RX_OK;
 }
 

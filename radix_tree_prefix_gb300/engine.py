@@ -82,6 +82,50 @@ class GatherInputs:
                         self.values["v"][layer].index_select(0, ti)) for layer in self.layers}
 
 
+class PreparedInputs:
+    """Inputs gathered once (by a recording run) and replayed in order.
+
+    ``source`` is any provider; the first pass records what it returns per
+    extend batch and decode step, later passes replay it.  ``host=True`` keeps
+    the recorded tensors in pinned host memory and copies each batch to the
+    device when it is used (the end-to-end path)."""
+
+    def __init__(self, source, host=False):
+        self.source = source
+        self.host = host
+        self.ext = {}
+        self.dec = {}
+        self.recording = True
+        self.h2d_bytes = 0
+
+    def freeze(self):
+        self.recording = False
+        if self.host:
+            for store in (self.ext, self.dec):
+                for key, per_layer in store.items():
+                    store[key] = {l: tuple(t.cpu().pin_memory() for t in qkv)
+                                  for l, qkv in per_layer.items()}
+
+    def _get(self, store, key, make):
+        if self.recording:
+            store[key] = make()
+            return store[key]
+        per_layer = store[key]
+        if not self.host:
+            return per_layer
+        out = {}
+        for l, qkv in per_layer.items():
+            out[l] = tuple(t.to(self.source.device, non_blocking=True) for t in qkv)
+            self.h2d_bytes += sum(t.numel() * t.element_size() for t in qkv)
+        return out
+
+    def extend(self, batch_no, reqs, prefix):
+        return self._get(self.ext, batch_no, lambda: self.source.extend(batch_no, reqs, prefix))
+
+    def decode(self, step_no, reqs, t):
+        return self._get(self.dec, step_no, lambda: self.source.decode(step_no, reqs, t))
+
+
 class Engine:
     """Runs a workload through librx.
 
@@ -91,7 +135,7 @@ class Engine:
     """
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
-                 on_decode=None, stream=None):
+                 on_decode=None, stream=None, timing=False):
         self.wl = wl
         self.device = device
         self.inputs = inputs
@@ -104,6 +148,8 @@ class Engine:
             wl.decode_steps
         self.max_wave = max(len(w) for w in wl.waves)
         self.gpu_launches = 0
+        self.timing = timing
+        self.kernel_events = []   # (kind, start event, end event, algorithmic work)
         if device is not None:
             import torch
             self.torch = torch
@@ -181,7 +227,11 @@ class Engine:
         self.trace.batches.append(recs)
         if self.device is not None:
             self._extend_device(reqs, j0, j1, prefix, ind, new_slots)
-        prompt_nodes[j0:j1] = self.cache.extend_end(tok, ind, table, prefix, match_nodes)
+        nodes, rewritten = self.cache.extend_end(tok, ind, table, prefix, match_nodes)
+        prompt_nodes[j0:j1] = nodes
+        if rewritten and self.device is not None:
+            width = int(max(ind[1:] - ind[:-1]))
+            self.d_table[j0:j1, :width].copy_(self.torch.from_numpy(self.h_table[j0:j1, :width]))
         self.batch_no += 1
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):
@@ -208,9 +258,11 @@ class Engine:
             out = torch.empty((total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
                               device=self.device)
             lse = torch.empty((total_q, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            ev = self._event_start()
             rx.extend_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_rows,
                                 d_prefix, d_qo, d_tiles, R, n_tiles, self.scale, out, lse,
                                 self.stream)
+            self._event_end(ev, "extend", self._extend_flops(prefix, qo))
             self.gpu_launches += 2
             outs[layer] = (out, lse)
         if self.on_extend is not None:
@@ -252,10 +304,46 @@ class Engine:
             out = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
                               device=self.device)
             lse = torch.empty((B, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            ev = self._event_start()
             rx.decode_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_plan, info,
                                 B, self.scale, out, lse, self.d_ws, self.stream)
+            self._event_end(ev, "decode", self.decode_bytes(info, B))
             self.gpu_launches += 3
             outs[layer] = (out, lse)
         self.gpu_launches += 1
         if self.on_decode is not None:
             self.on_decode(self.step_no, t, [r.rid for r in wave], ctx_now, outs, info)
+
+    # ------------------------------------------------------------ timing
+    def _event_start(self):
+        if not self.timing:
+            return None
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record(self.stream if self.stream is not None else self.torch.cuda.current_stream())
+        return e
+
+    def _event_end(self, start, kind, work):
+        if start is None:
+            return
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record(self.stream if self.stream is not None else self.torch.cuda.current_stream())
+        self.kernel_events.append((kind, start, e, work))
+
+    def _extend_flops(self, prefix, qo):
+        """Algorithmic FLOPs of one extend launch: 4 * d * Hq per visible
+        (query, key) pair; query i of a suffix of s over a prefix p sees
+        p + i + 1 keys."""
+        s = (qo[1:] - qo[:-1]).astype(np.int64)
+        p = np.asarray(prefix, dtype=np.int64)
+        pairs = int(np.sum(s * p + s * (s + 1) // 2))
+        return 4.0 * self.wl.head_dim * self.wl.num_q_heads * pairs
+
+    def decode_bytes(self, info, B):
+        """Algorithmic bytes of one decode launch: the distinct KV of the
+        batch read once (K and V, bf16), its slot indices, Q (bf16) and the
+        fp32 output and lse."""
+        wl = self.wl
+        kv = info.distinct_kv_tokens * (2 * wl.num_kv_heads * wl.head_dim * 2 + 4)
+        q = B * wl.num_q_heads * wl.head_dim * 2
+        o = B * wl.num_q_heads * (wl.head_dim + 1) * 4
+        return float(kv + q + o)

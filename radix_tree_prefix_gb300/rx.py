@@ -84,7 +84,7 @@ _SIGS = {
     "rx_eviction_log": [P, I64, P, I64, P],
     "rx_node_depth": [P, I64, P],
     "rx_extend_begin": [P, I32, P, P, P, I64, P, P, P, P],
-    "rx_extend_end": [P, I32, P, P, P, I64, P, P, P],
+    "rx_extend_end": [P, I32, P, P, P, I64, P, P, P, P],
     "rx_finish": [P, I32, P, P, P, I64, P, P, P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
@@ -244,11 +244,14 @@ class RadixCache:
         return prefix[:R], nodes[:R], new[:total.value]
 
     def extend_end(self, tokens, tok_indptr, req_to_token, prefix, match_nodes):
+        """Returns (prompt nodes, number of rows rewritten with tree slots)."""
         R = len(tok_indptr) - 1
         out = np.empty(max(1, R), dtype=np.int64)
+        rew = C.c_int64()
         _check(_lib.rx_extend_end(self._h, R, _p(tokens), _p(tok_indptr), _p(req_to_token),
-                                  req_to_token.shape[1], _p(prefix), _p(match_nodes), _p(out)))
-        return out[:R]
+                                  req_to_token.shape[1], _p(prefix), _p(match_nodes), _p(out),
+                                  C.byref(rew)))
+        return out[:R], rew.value
 
     def finish(self, tokens, tok_indptr, req_to_token, prompt_len, prompt_nodes):
         R = len(tok_indptr) - 1

@@ -1,0 +1,120 @@
+"""GPU parity of the librx kernels against the fp64 oracle.
+
+Every case runs the whole request flow through the C ABI (native cache +
+CUDA kernels); bookkeeping must equal the oracle's bit for bit and attention
+must be within max-abs 1e-2 / mean-abs 1e-3 of fp64 attention computed from
+the token streams (as if every prompt were recomputed).
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU machines, skipped there
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from oracle import pool as opool  # noqa: E402
+from parity_util import GpuRun  # noqa: E402
+from radix_tree_prefix_gb300 import rx, workloads  # noqa: E402
+from radix_tree_prefix_gb300.workloads import Request, Workload  # noqa: E402
+
+
+@pytest.mark.parametrize("d,hkv,T", [(128, 2, 1), (128, 8, 777), (256, 4, 300), (128, 1, 4096)])
+def test_kv_store_bit_exact(d, hkv, T):
+    dev = torch.device("cuda:0")
+    L, N = 2, 5000
+    g = torch.Generator(device=dev).manual_seed(T)
+    kp = torch.randn((L, hkv, N, d), generator=g, device=dev).to(torch.bfloat16)
+    vp = torch.randn((L, hkv, N, d), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    slots = (torch.randperm(N - 1, generator=g, device=dev)[:T] + 1).to(torch.int32)
+    want_k = opool.store(kp.float().cpu().numpy(), 1, slots.cpu().numpy(), k.float().cpu().numpy())
+    want_v = opool.store(vp.float().cpu().numpy(), 1, slots.cpu().numpy(), v.float().cpu().numpy())
+    rx.kv_store(rx.pool_desc(kp, vp), 1, slots, k, v)
+    torch.cuda.synchronize()
+    assert rx.device_check() == 0
+    assert np.array_equal(kp.float().cpu().numpy(), want_k)
+    assert np.array_equal(vp.float().cpu().numpy(), want_v)
+
+
+def test_empty_calls_launch_nothing():
+    dev = torch.device("cuda:0")
+    kp = torch.zeros((1, 1, 8, 128), dtype=torch.bfloat16, device=dev)
+    e = torch.zeros(0, dtype=torch.int32, device=dev)
+    rx.kv_store(rx.pool_desc(kp, kp), 0, e, kp, kp)
+    torch.cuda.synchronize()
+
+
+SMALL = {
+    # the nested example at full size: 3 batches, 3,060 prefilled tokens
+    "nested_share": (lambda: workloads.nested_share(), None),
+    # shared preamble + ragged suffixes + decode (G = 4)
+    "agent_small": (lambda: workloads.agent_loop(calls=6, preamble=300, lo=20, hi=60,
+                                                 decode_steps=5), None),
+    # G = 1 and G = 8
+    "agent_g1": (lambda: workloads.agent_loop(calls=5, preamble=200, lo=1, hi=70, decode_steps=3,
+                                              q_heads=4, kv_heads=4), None),
+    "agent_g8": (lambda: workloads.agent_loop(calls=5, preamble=150, lo=30, hi=90,
+                                              decode_steps=3, q_heads=64, kv_heads=8), None),
+    # head_dim 256, two layers, multi-turn waves (history reuse)
+    "chat_d256": (lambda: workloads.multi_turn_chat(sessions=4, turns=3, system=100, user=40,
+                                                    decode_steps=4, layers=2), None),
+    # branching tree with a small pool: eviction, slot reuse, nested shared segments
+    "fork_evict": (lambda: workloads.fork_tree(branching=3, depth=3, level_tokens=48,
+                                               decode_steps=4), None),
+    # many members on one shared segment: several member blocks of a chunk
+    "long_shared_small": (lambda: workloads.long_shared(batch=20, prefix=700, unique=50,
+                                                        decode_steps=3), None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_workload_parity(name):
+    wl = SMALL[name][0]()
+    run = GpuRun(wl)
+    mx, mean, n = run.assert_close()
+    if name == "nested_share":
+        assert run.trace.prefilled == 3060
+    if name == "fork_evict":
+        assert len(run.trace.eviction_log) > 0
+
+
+def test_single_token_suffixes_and_duplicates():
+    """Prompts that extend the previous one by one token (a 1-query extend
+    over a long prefix) and an identical prompt (rows adopt tree slots)."""
+    s = workloads._Segments(77)
+    base = s.new(300)
+    ones = [s.new(1) for _ in range(4)]
+    outs = [s.new(3) for _ in range(6)]
+    waves = []
+    for k in range(4):
+        waves.append([Request(k, (base,) + tuple(ones[:k + 1]), outs[k])])
+    waves.append([Request(4, (base, ones[0]), outs[4]), Request(5, (base, ones[0]), outs[5])])
+    wl = Workload("one_token", 1, 16, 4, 128, 2000, 3, s.tokens, waves, 77)
+    run = GpuRun(wl)
+    run.assert_close()
+    assert [len(b) for b in run.trace.batches] == [1, 1, 1, 1, 1, 1]
+
+
+def test_agent_loop_full_size_sampled():
+    """The benchmark workload at full size: bookkeeping bit-exact, sampled
+    extend rows of 6 requests and decode rows at 3 steps."""
+    wl = workloads.agent_loop()
+    run = GpuRun(wl, sample={0, 1, 7, 20, 38, 39}, extend_tokens=48, decode_steps={0, 31, 63})
+    run.assert_close()
+
+
+def test_long_shared_full_size_sampled():
+    wl = workloads.long_shared()
+    run = GpuRun(wl, sample={0, 1, 63}, extend_tokens=24, decode_steps={0, 127})
+    run.assert_close()
+
+
+def test_fork_tree_full_size_sampled():
+    wl = workloads.fork_tree()
+    run = GpuRun(wl, sample={0, 3, 130, 377, 624}, extend_tokens=16, decode_steps={0, 15})
+    run.assert_close()
+    assert len(run.trace.eviction_log) > 100

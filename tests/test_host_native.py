@@ -224,3 +224,17 @@ def test_decode_plan_covers_every_context_once():
     assert info.distinct_kv_tokens == 10 + 3 * 10 + 9 * 10 + 9 * 2
     indptr = plan[info.off_req_part_indptr:info.off_req_part_indptr + len(wave) + 1]
     assert indptr[-1] == info.n_parts
+
+
+def test_identical_prompts_share_slots():
+    """Several samples from one prompt: later copies adopt the tree's slots."""
+    base = workloads.nested_share()
+    seg = base.seg_tokens
+    waves = [[workloads.Request(0, (0, 1, 3)), workloads.Request(1, (0, 1, 3)),
+              workloads.Request(2, (0, 1, 3)), workloads.Request(3, (0, 2, 4))]]
+    wl = workloads.Workload("dup", 1, 8, 2, 128, 5000, 0, seg, waves)
+    got = Engine(wl).run()
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, 0)
+    assert got.as_tuple() == want.as_tuple()
+    assert [[r for r, _, _ in b] for b in got.batches] == [[0], [1], [2, 3]]
+    assert got.stats == want.stats
