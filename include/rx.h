@@ -374,8 +374,9 @@ rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
  * clear them).  *out_flags (may be NULL): bit 0 = rx_kv_store met a slot
  * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel
  * read a slot outside [0, num_slots) from req_to_token and used slot 0
- * instead.  Returns RX_ERR_CUDA if a flag was set or the device reported an
- * error. */
+ * instead; bit 2 = a tensor-core kernel gave up a barrier wait after its
+ * time limit (about 2 s) and returned without results.  Returns RX_ERR_CUDA
+ * if a flag was set or the device reported an error. */
 rx_status rx_device_check(int32_t* out_flags);
 
 /* Library build information (kernel variant names, compiled arch). */

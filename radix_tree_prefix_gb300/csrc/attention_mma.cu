@@ -402,6 +402,212 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restric
   if (lane == 0) lse_out[int64_t(b) * hq + h] = m + logf(sum);
 }
 
+// ---------------------------------------------------------------------------
+// Decode over one work item of <= 16 query rows (a request's private tail, or
+// a shared segment chunk with few rows), head_dim 128.  No shared-memory
+// staging of K/V: every thread loads 16-byte pieces of K and V rows straight
+// from the pool into mma.sync fragments.  This works because the head
+// dimension may be permuted consistently in Q and K (the dot product does not
+// care), and the output columns may be permuted when they are written back:
+//   QK^T: thread (g = lane/4, c = lane%4) holds d in [32j+8c, 32j+8c+8) of
+//         its K row (key 8nt+g) and of Q rows g, g+8; logical k-steps 2j and
+//         2j+1 consume elements {0,1|2,3} and {4,5|6,7} of that piece;
+//   PV:   output column n of n-tile t is d = 64(t/8) + 8n + t%8, so thread
+//         (g, c) reads d in [64h+8g, 64h+8g+8) of V rows 2c, 2c+1, 8+2c, 9+2c
+//         and writes 8 contiguous outputs per (row, h, e).
+// NW warps split the item's 16-key steps round-robin; their (m, l, O) are
+// merged through shared memory at the end into one partial per row.
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) decode_warp_kernel(const TileArgs a) {
+  constexpr int D = 128;
+  constexpr int NJ = D / 32;    // 16-byte pieces of a K row per thread
+  constexpr int NH = D / 64;    // 16-byte pieces of a V row per thread
+  constexpr int NT = D / 8;     // output n-tiles
+  extern __shared__ __align__(16) float dsm[];
+  float (*s_o)[16][D + 4] = reinterpret_cast<float (*)[16][D + 4]>(dsm);
+  float (*s_m)[16] = reinterpret_cast<float (*)[16]>(dsm + NW * 16 * (D + 4));
+  float (*s_l)[16] = reinterpret_cast<float (*)[16]>(dsm + NW * 16 * (D + 4) + NW * 16);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int kvh = blockIdx.y;
+  const int G = a.group;
+  const int32_t* w = a.work + int64_t(blockIdx.x) * RX_WORK_WORDS;
+  const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
+  const int kb = w[1], ke = w[2], member_off = w[3], part_base = w[5], n_rows = w[6];
+  const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
+  const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
+
+  // Q pieces of rows g and g+8 (zero for rows past n_rows)
+  uint4 qlo[NJ], qhi[NJ];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = g + 8 * e;
+    const bool ok = r < n_rows;
+    const bf16* qrow = a.q;
+    if (ok) {
+      const int unit = r / G;
+      const int64_t b = a.members[member_off + unit];
+      qrow = a.q + (b * a.hq + kvh * G + (r - unit * G)) * D;
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ok) v = __ldg(reinterpret_cast<const uint4*>(qrow + 32 * j + 8 * c));
+      if (e == 0) qlo[j] = v; else qhi[j] = v;
+    }
+  }
+
+  float o[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+
+  const int n_steps = (ke - kb + 15) >> 4;
+  for (int st = warp; st < n_steps; st += NW) {
+    const int k0 = kb + st * 16;
+    // slots: K rows k0+g, k0+8+g; V rows k0+2c, k0+2c+1, k0+8+2c, k0+9+2c
+    int64_t sk[2], sv[4];
+    bool vk[2], vv[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int key = k0 + 8 * i + g;
+      vk[i] = key < ke;
+      int64_t sl = vk[i] ? __ldg(trow + key) : 0;
+      if (sl < 0 || sl >= a.num_slots) { atomicOr(&g_attention_error, 1); sl = 0; }
+      sk[i] = sl;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int key = k0 + 2 * c + (i & 1) + 8 * (i >> 1);
+      vv[i] = key < ke;
+      int64_t sl = vv[i] ? __ldg(trow + key) : 0;
+      if (sl < 0 || sl >= a.num_slots) { atomicOr(&g_attention_error, 1); sl = 0; }
+      sv[i] = sl;
+    }
+    uint4 kf[2][NJ], vf[4][NH];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        kf[i][j] = __ldg(reinterpret_cast<const uint4*>(kbase + sk[i] * D + 32 * j + 8 * c));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        uint4 x = __ldg(reinterpret_cast<const uint4*>(vbase + sv[i] * D + 64 * h + 8 * g));
+        if (!vv[i]) x = make_uint4(0, 0, 0, 0);
+        vf[i][h] = x;
+      }
+    // S = Q K^T (16 rows x 16 keys)
+    float s[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        rxk::mma_bf16(s[i], qlo[j].x, qhi[j].x, qlo[j].y, qhi[j].y, kf[i][j].x, kf[i][j].y);
+        rxk::mma_bf16(s[i], qlo[j].z, qhi[j].z, qlo[j].w, qhi[j].w, kf[i][j].z, kf[i][j].w);
+      }
+    }
+    // scale, mask keys past the chunk, online softmax (log2 domain)
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = k0 + 8 * i + 2 * c + (e & 1);
+        const float v = key < ke ? s[i][e] * a.scale_log2 : -INFINITY;
+        s[i][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+    float alpha[2], m_use[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
+      const float m_new = fmaxf(m_run[e], mx[e]);
+      m_use[e] = (m_new == -INFINITY) ? 0.f : m_new;
+      alpha[e] = rxk::fast_exp2(m_run[e] - m_use[e]);
+      m_run[e] = m_new;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = rxk::fast_exp2(s[i][e] - m_use[e >> 1]);
+        s[i][e] = p;
+        rs[e >> 1] += p;
+      }
+    l_run[0] = l_run[0] * alpha[0] + rs[0];
+    l_run[1] = l_run[1] * alpha[1] + rs[1];
+    const uint32_t a0 = rxk::pack_bf16(s[0][0], s[0][1]);
+    const uint32_t a1 = rxk::pack_bf16(s[0][2], s[0][3]);
+    const uint32_t a2 = rxk::pack_bf16(s[1][0], s[1][1]);
+    const uint32_t a3 = rxk::pack_bf16(s[1][2], s[1][3]);
+    // O += P V
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int h = t >> 3, i = t & 7;
+      const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+      const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vf[0][h])[i >> 1];
+      const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vf[1][h])[i >> 1];
+      const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vf[2][h])[i >> 1];
+      const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vf[3][h])[i >> 1];
+      const uint32_t b0 = __byte_perm(w0, w1, sel);
+      const uint32_t b1 = __byte_perm(w2, w3, sel);
+      o[t][0] *= alpha[0];
+      o[t][1] *= alpha[0];
+      o[t][2] *= alpha[1];
+      o[t][3] *= alpha[1];
+      rxk::mma_bf16(o[t], a0, a1, a2, a3, b0, b1);
+    }
+  }
+
+  // merge the NW warps' partial softmax states through shared memory
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float l = l_run[e];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const int r = g + 8 * e;
+    if (c == 0) {
+      s_m[warp][r] = m_run[e];
+      s_l[warp][r] = l;
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int d0 = 64 * (t >> 3) + 8 * (2 * c) + (t & 7);
+      s_o[warp][r][d0] = o[t][2 * e];
+      s_o[warp][r][d0 + 8] = o[t][2 * e + 1];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 16 * D; idx += NW * 32) {
+    const int r = idx / D;
+    const int d = idx - r * D;
+    if (r >= n_rows) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < NW; ++x) M = fmaxf(M, s_m[x][r]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int x = 0; x < NW; ++x) {
+      const float f = (s_m[x][r] == -INFINITY) ? 0.f : rxk::fast_exp2(s_m[x][r] - M);
+      L += s_l[x][r] * f;
+      acc += s_o[x][r][d] * f;
+    }
+    const int unit = r / G;
+    const int head = kvh * G + (r - unit * G);
+    const int64_t part = int64_t(part_base) + unit;
+    a.ws_o[(part * a.hq + head) * D + d] = acc / L;
+    if (d == 0) a.ws_lse[part * a.hq + head] = M * kLn2 + logf(L);
+  }
+}
+
 template <int D, int NW, bool DECODE>
 constexpr int smem_bytes() {
   return (NW * 16 * D + 4 * BN * D) * 2;
@@ -454,30 +660,10 @@ extern "C" rx_status rx_extend_attention(const rx_pool_desc* pool, int32_t layer
   if (!d_q || !d_req_to_token || !d_req_rows || !d_prefix_len || !d_qo_indptr ||
       !d_tile_indptr || !d_out || !d_lse || !aligned16(d_q) || !aligned16(d_out))
     return rx_internal::set_error(RX_ERR_INVALID, "rx_extend_attention: NULL or misaligned");
-  const int D = pool->head_dim;
-  TileArgs a{};
-  a.q = static_cast<const bf16*>(d_q);
-  const int64_t layer_off = int64_t(layer) * pool->num_kv_heads * pool->num_slots * D;
-  a.kpool = static_cast<const bf16*>(pool->k_pool) + layer_off;
-  a.vpool = static_cast<const bf16*>(pool->v_pool) + layer_off;
-  a.head_stride = pool->num_slots * D;
-  a.num_slots = pool->num_slots;
-  a.table = d_req_to_token;
-  a.row_stride = row_stride;
-  a.hq = num_q_heads;
-  a.group = num_q_heads / pool->num_kv_heads;
-  a.scale_log2 = scale * kLog2e;
-  a.req_rows = d_req_rows;
-  a.prefix_len = d_prefix_len;
-  a.qo_indptr = d_qo_indptr;
-  a.tile_indptr = d_tile_indptr;
-  a.num_req = R;
-  a.num_tiles = int(num_tiles);
-  a.out = d_out;
-  a.lse = d_lse;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 128) return launch_tiles<128, 8, false>(a, unsigned(num_tiles), pool->num_kv_heads, s);
-  return launch_tiles<256, 4, false>(a, unsigned(num_tiles), pool->num_kv_heads, s);
+  return rx_internal::extend_attention_tc(pool, layer, d_q, num_q_heads, d_req_to_token,
+                                         row_stride, d_req_rows, d_prefix_len, d_qo_indptr,
+                                         d_tile_indptr, R, num_tiles, scale, d_out, d_lse,
+                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
@@ -519,8 +705,21 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
   a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + ((o_bytes + 255) / 256) * 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (info->n_work > 0) {
-    st = (D == 128) ? launch_tiles<128, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s)
-                    : launch_tiles<256, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s);
+    if (D == 128) {
+      constexpr int kNW = 8;
+      constexpr int bytes = (kNW * 16 * (128 + 4) + 2 * kNW * 16) * 4;
+      static bool configured = false;
+      if (!configured) {
+        cudaFuncSetAttribute(decode_warp_kernel<kNW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+        configured = true;
+      }
+      decode_warp_kernel<kNW><<<dim3(unsigned(info->n_work), pool->num_kv_heads), kNW * 32,
+                                bytes, s>>>(a);
+      st = rx_internal::launch_status("decode attention");
+    } else {
+      st = launch_tiles<256, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s);
+    }
     if (st != RX_OK) return st;
   }
   const unsigned blocks = unsigned((int64_t(B) * num_q_heads + 7) / 8);

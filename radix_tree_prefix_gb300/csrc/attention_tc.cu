@@ -1,0 +1,530 @@
+// S6 (and the dense multi-query tiles of S7): attention of 128 query rows
+// over gathered pool KV on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// What is computed ("SGLang: Structured LLM Programs for Efficient
+// Inference", sections "A quick recap of how an LLM generates text" and "How
+// RadixAttention reuses past work"): every suffix query attends with softmax
+// over its request's keys up to and including itself; reused prefix keys are
+// read from the slots the radix cache handed out, as if just computed.
+//
+// One CTA = 128 query rows that read one KV head over one key range:
+//   extend: rows = (suffix token, head in group) of one request, token-major,
+//           causal limit per row = prefix + token + 1;
+//   decode: rows = (member request, head in group) of a tree segment chunk
+//           shared by the members; writes partial (o, lse) per row.
+// Warp roles (288 threads):
+//   warps 0-3  softmax: thread i owns query row i = TMEM lane i; reads S from
+//              TMEM, keeps the running max / sum, writes P (bf16) to shared
+//              memory, rescales O in TMEM when the max grows by more than 2^8
+//              (rare after the first tile), and writes the output;
+//   warp 4     allocates TMEM and issues tcgen05.mma from one thread:
+//              S_j = Q K_j^T (double-buffered in TMEM), O += P_j V_j (O stays
+//              in TMEM for the whole key loop);
+//   warps 5-8  gather K/V rows by slot with 16-byte cp.async into 128-byte
+//              swizzled tiles (two stages), plus the Q tile.
+// Every mbarrier wait is bounded (about 2 s); on a timeout the CTA sets an
+// error bit, drains its tensor-core work and frees TMEM before returning.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+
+#include "ptx_util.cuh"
+#include "rx.h"
+#include "rx_internal.h"
+#include "tc_util.cuh"
+
+// Bit 0: a slot outside [0, num_slots) was read (slot 0 used instead);
+// bit 1: a barrier wait timed out.  Read by rx_device_check().
+static __device__ int32_t g_tc_error;
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
+constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr int BM = 128;
+constexpr int kThreads = 288;
+
+struct TcArgs {
+  const bf16* q;
+  const bf16* kpool;  // layer base, [Hkv][num_slots][D]
+  const bf16* vpool;
+  int64_t head_stride;
+  int64_t num_slots;
+  const int32_t* table;
+  int64_t row_stride;
+  int hq;
+  int group;
+  float scale_log2;
+  // extend
+  const int32_t* req_rows;
+  const int32_t* prefix_len;
+  const int32_t* qo_indptr;
+  const int32_t* tile_indptr;
+  int num_req;
+  int num_tiles;
+  float* out;
+  float* lse;
+  // decode
+  const int32_t* work;
+  const int32_t* members;
+  float* ws_o;
+  float* ws_lse;
+};
+
+struct TileDesc {
+  const int32_t* trow;
+  int key_begin, key_end, nomask_end, n_rows;
+  int gr0, q_base, prefix;
+  int member_off, part_base;
+};
+
+template <bool DECODE>
+__device__ __forceinline__ TileDesc describe(const TcArgs& a) {
+  TileDesc t;
+  if constexpr (DECODE) {
+    const int32_t* w = a.work + int64_t(blockIdx.x) * RX_WORK_WORDS;
+    t.trow = a.table + int64_t(w[0]) * a.row_stride;
+    t.key_begin = w[1];
+    t.key_end = w[2];
+    t.member_off = w[3];
+    t.part_base = w[5];
+    t.n_rows = w[6];
+    t.nomask_end = t.key_end;
+    t.gr0 = t.q_base = t.prefix = 0;
+  } else {
+    const int tile = a.num_tiles - 1 - int(blockIdx.x);  // heaviest first
+    int lo = 0, hi = a.num_req;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.tile_indptr[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int G = a.group;
+    t.q_base = a.qo_indptr[lo];
+    const int s_r = a.qo_indptr[lo + 1] - t.q_base;
+    t.prefix = a.prefix_len[lo];
+    t.trow = a.table + int64_t(a.req_rows[lo]) * a.row_stride;
+    t.gr0 = (tile - a.tile_indptr[lo]) * BM;
+    t.n_rows = min(BM, s_r * G - t.gr0);
+    t.key_begin = 0;
+    t.key_end = t.prefix + (t.gr0 + t.n_rows - 1) / G + 1;
+    t.nomask_end = t.prefix + t.gr0 / G + 1;
+    t.member_off = t.part_base = 0;
+  }
+  return t;
+}
+
+// row i -> (query index, head, part index for decode, causal limit)
+template <bool DECODE>
+__device__ __forceinline__ void row_info(const TcArgs& a, const TileDesc& t, int kvh, int i,
+                                         int64_t& qi, int& head, int64_t& part, int& lim) {
+  const int G = a.group;
+  if constexpr (DECODE) {
+    const int unit = i / G;
+    qi = a.members[t.member_off + unit];
+    head = kvh * G + (i - unit * G);
+    part = int64_t(t.part_base) + unit;
+    lim = t.key_end;
+  } else {
+    const int gr = t.gr0 + i;
+    const int tok = gr / G;
+    qi = int64_t(t.q_base) + tok;
+    head = kvh * G + (gr - tok * G);
+    part = 0;
+    lim = t.prefix + tok + 1;
+  }
+}
+
+// 128-byte-swizzled tile of `rows` rows, stored as column blocks of 64 bf16:
+// byte address of 16-byte chunk `ch` (of the full row) of row r.
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int rows, int r, int ch) {
+  return base + uint32_t((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+template <int D, int BN>
+struct Layout {
+  static constexpr int Q = 0;
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int K0 = Q + Q_BYTES;
+  static constexpr int V0 = K0 + 2 * KV_BYTES;
+  static constexpr int P0 = V0 + 2 * KV_BYTES;
+  static constexpr int BAR = P0 + 2 * P_BYTES;
+  // barriers: q, kfull[2], vfull[2], empty[2], s[2], p[2], o, final
+  static constexpr int NBAR = 13;
+  static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
+  static constexpr int BYTES = MISC + 16 + 1024;  // + alignment slack
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int O_COL = 2 * BN;
+};
+
+template <int D, int BN, bool DECODE>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
+  using Lo = Layout<D, BN>;
+  static_assert(2 * BN + D <= Lo::TMEM_COLS, "TMEM budget");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment of the swizzled tiles
+  const uint32_t raw = rxk::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + Lo::Q;
+  const uint32_t bar = base + Lo::BAR;
+  auto BAR_Q = [&]() { return bar; };
+  auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
+  auto BAR_VF = [&](int s) { return bar + 8u * (3 + s); };
+  auto BAR_EMPTY = [&](int s) { return bar + 8u * (5 + s); };
+  auto BAR_S = [&](int s) { return bar + 8u * (7 + s); };
+  auto BAR_P = [&](int s) { return bar + 8u * (9 + s); };
+  const uint32_t BAR_O = bar + 8u * 11;
+  const uint32_t BAR_FIN = bar + 8u * 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int kvh = blockIdx.y;
+  const TileDesc t = describe<DECODE>(a);
+  const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
+
+  if (tid == 0) {
+    tc::mbar_init(BAR_Q(), 128);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(BAR_KF(s), 128);
+      tc::mbar_init(BAR_VF(s), 128);
+      tc::mbar_init(BAR_EMPTY(s), 1);
+      tc::mbar_init(BAR_S(s), 1);
+      tc::mbar_init(BAR_P(s), 128);
+    }
+    tc::mbar_init(BAR_O, 1);
+    tc::mbar_init(BAR_FIN, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 4) {
+    tc::tmem_alloc(rxk::smem_addr(tmem_slot), Lo::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 5) {
+    // ------------------------------------------------------------ loaders
+    const int tl = tid - 160;
+    constexpr int CPR = D / 8;
+    for (int idx = tl; idx < BM * CPR; idx += 128) {
+      const int r = idx / CPR;
+      const int ch = idx - r * CPR;
+      const bool ok = r < t.n_rows;
+      const bf16* src = a.q;
+      if (ok) {
+        int64_t qi, part;
+        int head, lim;
+        row_info<DECODE>(a, t, kvh, r, qi, head, part, lim);
+        src = a.q + (qi * a.hq + head) * D + ch * 8;
+      }
+      rxk::cp_async_16(sw128(sQ, BM, r, ch), src, ok);
+    }
+    rxk::cp_async_commit();
+    rxk::cp_async_wait<0>();
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive(BAR_Q());
+    const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
+    const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j & 1;
+      if (j >= 2 && !tc::mbar_wait(BAR_EMPTY(s), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit))
+        break;
+      const int k0 = t.key_begin + j * BN;
+      const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
+      const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
+      for (int idx = tl; idx < BN * CPR; idx += 128) {
+        const int r = idx / CPR;
+        const int ch = idx - r * CPR;
+        const int key = k0 + r;
+        const bool ok = key < t.key_end;
+        int64_t slot = 0;
+        if (ok) {
+          slot = __ldg(t.trow + key);
+          if (slot < 0 || slot >= a.num_slots) {
+            atomicOr(&g_tc_error, 1);
+            slot = 0;
+          }
+        }
+        rxk::cp_async_16(sw128(sk, BN, r, ch), kb + slot * D + ch * 8, ok);
+      }
+      rxk::cp_async_commit();
+      for (int idx = tl; idx < BN * CPR; idx += 128) {
+        const int r = idx / CPR;
+        const int ch = idx - r * CPR;
+        const int key = k0 + r;
+        const bool ok = key < t.key_end;
+        int64_t slot = 0;
+        if (ok) {
+          slot = __ldg(t.trow + key);
+          if (slot < 0 || slot >= a.num_slots) slot = 0;
+        }
+        rxk::cp_async_16(sw128(sv, BN, r, ch), vb + slot * D + ch * 8, ok);
+      }
+      rxk::cp_async_commit();
+      rxk::cp_async_wait<1>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(BAR_KF(s));
+      rxk::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(BAR_VF(s));
+    }
+    rxk::cp_async_wait<0>();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
+      constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
+      bool ok = tc::mbar_wait(BAR_Q(), 0, abort_flag, kWaitLimit);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = uint32_t((ks & 3) * 32);
+          const uint64_t ad = tc::sdesc_sw128(sQ + (ks >> 2) * (BM * 128) + koff, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(sk + (ks >> 2) * (BN * 128) + koff, 16, 1024);
+          tc::mma_bf16_ss(tmem + uint32_t(s * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(BAR_S(s));
+      };
+      if (ok && n_tiles > 0) {
+        ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_s(0);
+        }
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j & 1;
+        if (j + 1 < n_tiles) {
+          if (!tc::mbar_wait(BAR_KF((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimit)) break;
+          tc::tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!tc::mbar_wait(BAR_P(s), (j >> 1) & 1, abort_flag, kWaitLimit)) break;
+        if (!tc::mbar_wait(BAR_VF(s), (j >> 1) & 1, abort_flag, kWaitLimit)) break;
+        tc::tc_fence_after();
+        const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
+        const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t ad =
+              tc::sdesc_sw128(sp + (ks >> 2) * (BM * 128) + uint32_t((ks & 3) * 32), 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(sv + uint32_t(ks * 2048), BN * 128, 1024);
+          tc::mma_bf16_ss(tmem + uint32_t(Lo::O_COL), ad, bd, IDESC_PV,
+                          (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(BAR_O);
+        tc::mma_commit(BAR_EMPTY(s));
+      }
+      // drain: every MMA issued above has completed once this arrives
+      tc::mma_commit(BAR_FIN);
+      tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int i = warp * 32 + lane;
+    int64_t qi = 0, part = 0;
+    int head = 0, lim = t.key_end;
+    const bool valid = i < t.n_rows;
+    if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
+    const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j & 1;
+      // waits are made warp-uniform before any warp-collective tcgen05 op
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR_S(s), (j >> 1) & 1, abort_flag, kWaitLimit))) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const int k0 = t.key_begin + j * BN;
+      const bool need_mask = k0 + BN > t.nomask_end;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        tc::tmem_ld32(tl + uint32_t(s * BN + cc * 32), r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(r[e]) * a.scale_log2;
+          if (need_mask && k0 + cc * 32 + e >= lim) x = -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      if (j == 0) {
+        m_ref = m_new;
+      } else {
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!__all_sync(0xffffffffu,
+                          tc::mbar_wait(BAR_O, (j - 1) & 1, abort_flag, kWaitLimit))) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const float alpha = need ? rxk::fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tc::tmem_ld32(tl + uint32_t(Lo::O_COL + cc * 32), r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tc::tmem_st32(tl + uint32_t(Lo::O_COL + cc * 32), r);
+          }
+          tc::tmem_st_wait();
+          if (need) {
+            l *= alpha;
+            m_ref = m_new;
+          }
+        }
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        tc::tmem_ld32(tl + uint32_t(s * BN + cc * 32), r);
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = __uint_as_float(r[e]) * a.scale_log2;
+          float x1 = __uint_as_float(r[e + 1]) * a.scale_log2;
+          if (need_mask && k0 + cc * 32 + e >= lim) x0 = -INFINITY;
+          if (need_mask && k0 + cc * 32 + e + 1 >= lim) x1 = -INFINITY;
+          const float p0 = rxk::fast_exp2(x0 - m_use);
+          const float p1 = rxk::fast_exp2(x1 - m_use);
+          l += p0 + p1;
+          pk[e >> 1] = rxk::pack_bf16(p0, p1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = sw128(sp, BM, i, cc * 4 + q);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(pk[4 * q]),
+                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                       : "memory");
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR_P(s));
+    }
+    if (ok && n_tiles > 0 &&
+        __all_sync(0xffffffffu,
+                   tc::mbar_wait(BAR_O, (n_tiles - 1) & 1, abort_flag, kWaitLimit))) {
+      tc::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* dst;
+      float* lse_dst;
+      if constexpr (DECODE) {
+        dst = a.ws_o + (part * a.hq + head) * D;
+        lse_dst = a.ws_lse + part * a.hq + head;
+      } else {
+        dst = a.out + (qi * a.hq + head) * D;
+        lse_dst = a.lse + qi * a.hq + head;
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tc::tmem_ld32(tl + uint32_t(Lo::O_COL + cc * 32), r);
+        tc::tmem_ld_wait();
+        if (valid) {
+          float4* o4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o4[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                __uint_as_float(r[4 * e + 2]) * inv,
+                                __uint_as_float(r[4 * e + 3]) * inv);
+        }
+      }
+      if (valid) *lse_dst = m_ref * kLn2 + logf(l);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) atomicOr(&g_tc_error, 2);
+  if (warp == 4) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, Lo::TMEM_COLS);
+  }
+}
+
+template <int D, int BN, bool DECODE>
+rx_status launch(const TcArgs& a, unsigned gx, unsigned gy, cudaStream_t s) {
+  constexpr int bytes = Layout<D, BN>::BYTES;
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(attn_tc_kernel<D, BN, DECODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         bytes);
+    configured = true;
+  }
+  attn_tc_kernel<D, BN, DECODE><<<dim3(gx, gy), kThreads, bytes, s>>>(a);
+  return rx_internal::launch_status(DECODE ? "shared decode attention (tcgen05)"
+                                           : "extend attention (tcgen05)");
+}
+
+}  // namespace
+
+namespace rx_internal {
+
+int32_t tc_error_flags(bool clear) {
+  int32_t v = 0;
+  cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v));
+  if (clear && v) {
+    int32_t z = 0;
+    cudaMemcpyToSymbol(g_tc_error, &z, sizeof(z));
+  }
+  return v;
+}
+
+rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                              int32_t num_q_heads, const int32_t* d_req_to_token,
+                              int64_t row_stride, const int32_t* d_req_rows,
+                              const int32_t* d_prefix_len, const int32_t* d_qo_indptr,
+                              const int32_t* d_tile_indptr, int32_t R, int64_t num_tiles,
+                              float scale, float* d_out, float* d_lse, cudaStream_t stream) {
+  const int D = pool->head_dim;
+  TcArgs a{};
+  a.q = static_cast<const bf16*>(d_q);
+  const int64_t layer_off = int64_t(layer) * pool->num_kv_heads * pool->num_slots * D;
+  a.kpool = static_cast<const bf16*>(pool->k_pool) + layer_off;
+  a.vpool = static_cast<const bf16*>(pool->v_pool) + layer_off;
+  a.head_stride = pool->num_slots * D;
+  a.num_slots = pool->num_slots;
+  a.table = d_req_to_token;
+  a.row_stride = row_stride;
+  a.hq = num_q_heads;
+  a.group = num_q_heads / pool->num_kv_heads;
+  a.scale_log2 = scale * kLog2e;
+  a.req_rows = d_req_rows;
+  a.prefix_len = d_prefix_len;
+  a.qo_indptr = d_qo_indptr;
+  a.tile_indptr = d_tile_indptr;
+  a.num_req = R;
+  a.num_tiles = int(num_tiles);
+  a.out = d_out;
+  a.lse = d_lse;
+  if (D == 128) return launch<128, 128, false>(a, unsigned(num_tiles), pool->num_kv_heads, stream);
+  return launch<256, 64, false>(a, unsigned(num_tiles), pool->num_kv_heads, stream);
+}
+
+}  // namespace rx_internal

@@ -157,10 +157,16 @@ extern "C" rx_status rx_device_check(int32_t* out_flags) {
     snprintf(buf, sizeof(buf), "rx_device_check: %s", cudaGetErrorString(e));
     return rx_internal::set_error(RX_ERR_CUDA, buf);
   }
-  int32_t f = rx_internal::kv_store_error_flags(true) | (rx_internal::attention_error_flags(true) << 1);
+  const int32_t tcf = rx_internal::tc_error_flags(true);
+  int32_t f = rx_internal::kv_store_error_flags(true) |
+              (rx_internal::attention_error_flags(true) << 1) | ((tcf & 1) << 1) |
+              ((tcf & 2) << 1);
   if (out_flags) *out_flags = f;
   if (f)
-    return rx_internal::set_error(RX_ERR_CUDA, "rx_device_check: a kernel met a slot outside the pool");
+    return rx_internal::set_error(RX_ERR_CUDA,
+                                  (f & 4) ? "rx_device_check: a tensor-core kernel timed out "
+                                            "waiting on a barrier"
+                                          : "rx_device_check: a kernel met a slot outside the pool");
   return RX_OK;
 }
 

@@ -581,9 +581,11 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     return fail(RX_ERR_INVALID, "rx_plan_decode: Hq %d not a multiple of Hkv %d", num_q_heads,
                 num_kv_heads);
   const int32_t G = num_q_heads / num_kv_heads;
-  if (G > rx_internal::kDecodeRowsPerCta)
+  if (head_dim != 128 && head_dim != 256)
+    return fail(RX_ERR_INVALID, "rx_plan_decode: head_dim must be 128 or 256");
+  if (G > rx_internal::decode_rows_per_item(head_dim))
     return fail(RX_ERR_INVALID, "rx_plan_decode: group size %d above %d", G,
-                rx_internal::kDecodeRowsPerCta);
+                rx_internal::decode_rows_per_item(head_dim));
   std::vector<std::vector<const Node*>> paths(static_cast<size_t>(B));
   std::unordered_map<const Node*, int32_t> visits;
   for (int32_t b = 0; b < B; ++b) {
@@ -634,14 +636,15 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
   };
   std::vector<Work> work;
   std::vector<int32_t> members;
-  const int32_t per_block = rx_internal::kDecodeRowsPerCta / G;
-  const int64_t tile = rx_internal::kKeyTile;
+  const int32_t rows_per_item = rx_internal::decode_rows_per_item(head_dim);
+  const int32_t per_block = rows_per_item / G;
+  const int64_t tile = rx_internal::kDecodeKeyStep;
   int64_t distinct = 0;
   for (const Seg& s : segs) {
     int64_t n = s.ke - s.kb;
     distinct += n;
     int32_t k = int32_t(s.members.size());
-    int64_t chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, int64_t(8) * k * G);
+    int64_t chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, int64_t(2) * k * G);
     int64_t n_chunks = (n + chunk - 1) / chunk;
     int64_t len = (n + n_chunks - 1) / n_chunks;
     len = (len + tile - 1) / tile * tile;

@@ -2,20 +2,27 @@
 #pragma once
 #include <stdint.h>
 
+#include <cuda_runtime.h>
+
 #include "rx.h"
 
 namespace rx_internal {
 
-// Decode: query rows (member requests x group heads) handled by one CTA.
-constexpr int kDecodeRowsPerCta = 64;
-// Decode: a segment chunk is at least this many keys (and at least 8 keys per
+// Decode: query rows (member requests x group heads) of one work item: 16
+// for the register-fragment kernel (head_dim 128), 64 for the shared-memory
+// tile kernel (head_dim 256).
+inline int decode_rows_per_item(int head_dim) { return head_dim == 128 ? 16 : 64; }
+// Decode: a segment chunk is at least this many keys (and at least 2 keys per
 // query row, so partial results stay small next to the KV they summarise).
 constexpr int kDecodeMinChunk = 512;
+// Decode chunks are cut at multiples of this many keys.
+constexpr int kDecodeKeyStep = 64;
 // Key tile of the attention kernels.
 constexpr int kKeyTile = 64;
 
-// Extend: query rows (query tokens x group heads) per CTA tile.
-inline int extend_rows_per_tile(int head_dim) { return head_dim == 256 ? 64 : 128; }
+// Extend: query rows (query tokens x group heads) per CTA tile (the tcgen05
+// tile kernel owns 128 TMEM lanes = 128 rows).
+inline int extend_rows_per_tile(int /*head_dim*/) { return 128; }
 
 rx_status set_error(rx_status s, const char* msg);
 
@@ -26,5 +33,12 @@ int sm_count();
 // Error words of the kernels of each file: bit 0 = slot out of range.
 int32_t kv_store_error_flags(bool clear);
 int32_t attention_error_flags(bool clear);
+int32_t tc_error_flags(bool clear);
+rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                              int32_t num_q_heads, const int32_t* d_req_to_token,
+                              int64_t row_stride, const int32_t* d_req_rows,
+                              const int32_t* d_prefix_len, const int32_t* d_qo_indptr,
+                              const int32_t* d_tile_indptr, int32_t R, int64_t num_tiles,
+                              float scale, float* d_out, float* d_lse, cudaStream_t stream);
 
 }  // namespace rx_internal

@@ -126,6 +126,50 @@ class PreparedInputs:
         return self._get(self.dec, step_no, lambda: self.source.decode(step_no, reqs, t))
 
 
+class _Staging:
+    """Host->device uploads through a ring of pinned buffers.
+
+    Each upload packs int32 arrays into one pinned buffer and issues a single
+    asynchronous copy on the engine's stream; a ring slot is reused only after
+    its previous copy has completed (event), so the host never blocks on the
+    GPU in the common case."""
+
+    def __init__(self, torch, device, stream, n=4):
+        self.torch, self.device, self.stream = torch, device, stream
+        self.host = [None] * n
+        self.dev = [None] * n
+        self.events = [None] * n
+        self.i = 0
+
+    def upload(self, arrays):
+        torch = self.torch
+        n = sum(len(a) for a in arrays)
+        i = self.i
+        self.i = (i + 1) % len(self.host)
+        if self.events[i] is not None:
+            self.events[i].synchronize()
+        if self.host[i] is None or self.host[i].numel() < n:
+            cap = max(n, 1 << 16) * 2
+            self.host[i] = torch.empty(cap, dtype=torch.int32, pin_memory=True)
+            self.dev[i] = torch.empty(cap, dtype=torch.int32, device=self.device)
+        h = self.host[i].numpy()
+        off = 0
+        spans = []
+        for a in arrays:
+            k = len(a)
+            h[off:off + k] = a
+            spans.append((off, k))
+            off += k
+        stream = self.stream if self.stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(stream):
+            self.dev[i][:n].copy_(self.host[i][:n], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self.events[i] = ev
+        d = self.dev[i]
+        return [d[o:o + k] for o, k in spans]
+
+
 class Engine:
     """Runs a workload through librx.
 
@@ -161,6 +205,7 @@ class Engine:
             self.d_table = torch.zeros((self.max_wave, self.max_ctx), dtype=torch.int32,
                                        device=device)
             self.d_ws = torch.empty(0, dtype=torch.uint8, device=device)
+            self.staging = _Staging(torch, device, stream)
         # host staging
         self.h_table = np.zeros((self.max_wave, self.max_ctx), dtype=np.int32)
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
@@ -200,10 +245,8 @@ class Engine:
                     self._extend_batch(wave, start, j, tokens, indptr, prompt_nodes)
                     start = j
         self._extend_batch(wave, start, len(wave), tokens, indptr, prompt_nodes)
-        ctx = lens.astype(np.int32).copy()
-        for t in range(wl.decode_steps):
-            self._decode_step(wave, t, ctx, prompt_nodes)
-            ctx += 1
+        if wl.decode_steps:
+            self._decode_phase(wave, lens.astype(np.int32), prompt_nodes)
         # finish: insert prompt ++ outputs, unlock
         outs = [wl.output_tokens(r)[:wl.decode_steps].astype(np.int32) for r in wave]
         full = np.concatenate([np.concatenate([p, o]) for p, o in zip(prompts, outs)])
@@ -231,7 +274,8 @@ class Engine:
         prompt_nodes[j0:j1] = nodes
         if rewritten and self.device is not None:
             width = int(max(ind[1:] - ind[:-1]))
-            self.d_table[j0:j1, :width].copy_(self.torch.from_numpy(self.h_table[j0:j1, :width]))
+            (blk,) = self.staging.upload([self.h_table[j0:j1, :width].ravel()])
+            self.d_table[j0:j1, :width].copy_(blk.view(j1 - j0, width))
         self.batch_no += 1
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):
@@ -241,16 +285,14 @@ class Engine:
         qo = np.zeros(R + 1, dtype=np.int32)
         np.cumsum((ind[1:] - ind[:-1]) - prefix, out=qo[1:])
         tiles, n_tiles = rx.extend_plan(qo, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
-        meta = np.concatenate([np.arange(j0, j1, dtype=np.int32), prefix.astype(np.int32), qo,
-                               tiles]).astype(np.int32)
-        d_meta = torch.from_numpy(meta).to(self.device, non_blocking=False)
-        d_rows, d_prefix = d_meta[:R], d_meta[R:2 * R]
-        d_qo, d_tiles = d_meta[2 * R:3 * R + 1], d_meta[3 * R + 1:]
         width = int(max(ind[1:] - ind[:-1]))
-        self.d_table[j0:j1, :width].copy_(torch.from_numpy(self.h_table[j0:j1, :width]))
-        d_slots = torch.from_numpy(np.ascontiguousarray(new_slots)).to(self.device)
+        d_rows, d_prefix, d_qo, d_tiles, d_slots, blk = self.staging.upload([
+            np.arange(j0, j1, dtype=np.int32), prefix, qo, tiles, new_slots,
+            self.h_table[j0:j1, :width].ravel()])
+        self.d_table[j0:j1, :width].copy_(blk.view(R, width))
         inputs = self.inputs.extend(self.batch_no, reqs, prefix)
         total_q = int(qo[-1])
+        flops = self._extend_flops(prefix, qo) if self.timing else 0.0
         outs = {}
         for layer in self.layers:
             q, k, v = inputs[layer]
@@ -262,57 +304,72 @@ class Engine:
             rx.extend_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_rows,
                                 d_prefix, d_qo, d_tiles, R, n_tiles, self.scale, out, lse,
                                 self.stream)
-            self._event_end(ev, "extend", self._extend_flops(prefix, qo))
+            self._event_end(ev, "extend", flops)
             self.gpu_launches += 2
             outs[layer] = (out, lse)
         if self.on_extend is not None:
             self.on_extend(self.batch_no, [r.rid for r in reqs], prefix.copy(), qo, outs)
 
-    def _decode_step(self, wave, t, ctx, prompt_nodes):
-        B = len(wave)
-        slots = self.cache.alloc(B)
-        self.h_table[np.arange(B), ctx] = slots
-        self.trace.decode_steps.append([(r.rid, int(s)) for r, s in zip(wave, slots)])
-        if self.device is not None:
-            self._decode_device(wave, t, ctx, prompt_nodes, slots)
-        self.step_no += 1
-
-    def _decode_device(self, wave, t, ctx, prompt_nodes, slots):
-        torch = self.torch
+    def _decode_phase(self, wave, ctx0, prompt_nodes):
+        """All decode steps of a wave.  Slot allocation and the decode plan of
+        every step depend only on the cache, not on kernel results, so the
+        host plans all steps first and uploads them with one copy; the GPU then
+        runs the steps back to back."""
         wl = self.wl
-        B = len(wave)
+        B, T = len(wave), wl.decode_steps
         rows = np.arange(B, dtype=np.int32)
-        ctx_now = (ctx + 1).astype(np.int32)
-        self.plan_buf, info = self.cache.plan_decode(
-            prompt_nodes, ctx_now, rows, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-            self.plan_buf)
-        pw = int(info.plan_words)
-        host = np.concatenate([rows, ctx.astype(np.int32), slots.astype(np.int32),
-                               self.plan_buf[:pw]])
-        d_host = torch.from_numpy(host).to(self.device)
-        d_rows, d_pos, d_slots = d_host[:B], d_host[B:2 * B], d_host[2 * B:3 * B]
-        d_plan = d_host[3 * B:]
+        all_slots = np.empty((T, B), dtype=np.int32)
+        all_pos = np.empty((T, B), dtype=np.int32)
+        plans, infos = [], []
+        ctx = ctx0.copy()
+        for t in range(T):
+            slots = self.cache.alloc(B)
+            all_slots[t] = slots
+            all_pos[t] = ctx
+            self.h_table[rows, ctx] = slots
+            self.trace.decode_steps.append([(r.rid, int(s)) for r, s in zip(wave, slots)])
+            if self.device is not None:
+                self.plan_buf, info = self.cache.plan_decode(
+                    prompt_nodes, ctx + 1, rows, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                    self.plan_buf)
+                plans.append(self.plan_buf[:int(info.plan_words)].copy())
+                infos.append(info)
+            ctx += 1
+        if self.device is None:
+            self.step_no += T
+            return
+        torch = self.torch
+        views = self.staging.upload([np.tile(rows, T), all_pos.ravel(), all_slots.ravel()] + plans)
+        d_rows, d_pos, d_slots = views[0], views[1], views[2]
+        d_plans = views[3:]
         rx.req_to_token_write(self.d_table, d_rows, d_pos, d_slots, self.stream)
-        if self.d_ws.numel() < info.workspace_bytes:
-            self.d_ws = torch.empty(int(info.workspace_bytes * 1.5) + 256, dtype=torch.uint8,
-                                    device=self.device)
-        inputs = self.inputs.decode(self.step_no, wave, t)
-        outs = {}
-        for layer in self.layers:
-            q, k, v = inputs[layer]
-            rx.kv_store(self.pool, layer, d_slots, k, v, self.stream)
-            out = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
-                              device=self.device)
-            lse = torch.empty((B, wl.num_q_heads), dtype=torch.float32, device=self.device)
-            ev = self._event_start()
-            rx.decode_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_plan, info,
-                                B, self.scale, out, lse, self.d_ws, self.stream)
-            self._event_end(ev, "decode", self.decode_bytes(info, B))
-            self.gpu_launches += 3
-            outs[layer] = (out, lse)
         self.gpu_launches += 1
-        if self.on_decode is not None:
-            self.on_decode(self.step_no, t, [r.rid for r in wave], ctx_now, outs, info)
+        need = max(int(i.workspace_bytes) for i in infos)
+        if self.d_ws.numel() < need:
+            self.d_ws = torch.empty(int(need * 1.25) + 256, dtype=torch.uint8, device=self.device)
+        ctx = ctx0.copy()
+        for t in range(T):
+            info = infos[t]
+            step_slots = d_slots[t * B:(t + 1) * B]
+            inputs = self.inputs.decode(self.step_no, wave, t)
+            nbytes = self.decode_bytes(info, B) if self.timing else 0.0
+            outs = {}
+            for layer in self.layers:
+                q, k, v = inputs[layer]
+                rx.kv_store(self.pool, layer, step_slots, k, v, self.stream)
+                out = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
+                                  device=self.device)
+                lse = torch.empty((B, wl.num_q_heads), dtype=torch.float32, device=self.device)
+                ev = self._event_start()
+                rx.decode_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_plans[t],
+                                    info, B, self.scale, out, lse, self.d_ws, self.stream)
+                self._event_end(ev, "decode", nbytes)
+                self.gpu_launches += 3
+                outs[layer] = (out, lse)
+            if self.on_decode is not None:
+                self.on_decode(self.step_no, t, [r.rid for r in wave], ctx + 1, outs, info)
+            ctx += 1
+            self.step_no += 1
 
     # ------------------------------------------------------------ timing
     def _event_start(self):
