@@ -370,6 +370,31 @@ rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
                               void* d_workspace, size_t workspace_bytes,
                               rx_stream_t stream);
 
+/* Decode attention that allocates nothing and takes no scratch buffer.  The
+ * pages have no counterpart of this call; it exists for callers that cannot
+ * supply device memory -- e.g. a host whose device memory is all reserved up
+ * front by its own pool, or a plugin handed a stream and tensors but no
+ * allocator.  Arguments and results are those of rx_decode_attention without
+ * d_workspace / workspace_bytes; the partial results go to a fixed array of
+ * RX_DECODE_STATIC_SCRATCH_BYTES inside the library's device image, which
+ * every GPU that loads the library holds until the process exits.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - A plan whose info->workspace_bytes exceeds the limit is rejected with
+ *     RX_ERR_INVALID and a message; nothing is launched.
+ *   - Every call shares the one array.  Calls that overlap on the GPU (other
+ *     streams, or other threads) race on it; serialise them.  Nothing in the
+ *     array needs to start at zero: each partial result is written before the
+ *     merge reads it. */
+#define RX_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_t layer,
+                                     const void* d_q, int32_t num_q_heads,
+                                     const int32_t* d_req_to_token,
+                                     int64_t row_stride, const int32_t* d_plan,
+                                     const rx_decode_plan_info* info, int32_t B,
+                                     float scale, float* d_out, float* d_lse,
+                                     rx_stream_t stream);
+
 /* Synchronise the current device and read the kernels' error words (then
  * clear them).  *out_flags (may be NULL): bit 0 = rx_kv_store met a slot
  * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel

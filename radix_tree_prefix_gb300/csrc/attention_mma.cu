@@ -28,6 +28,8 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <mutex>
+
 #include "ptx_util.cuh"
 #include "rx.h"
 #include "rx_internal.h"
@@ -732,4 +734,65 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
                                                  d_plan + info->off_req_parts, a.ws_o, a.ws_lse,
                                                  num_q_heads, B, d_out, d_lse);
   return rx_internal::launch_status("decode merge");
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot provide device memory.
+//
+// rx_decode_attention needs a caller-owned scratch buffer for its partial
+// results.  Some callers have no way to get one: a host process whose device
+// memory is entirely reserved up front by its own pool, or a plugin that is
+// handed a stream and pointers but no allocator.  This entry point keeps the
+// scratch in a fixed array that lives in the library's device image instead:
+// it exists on every GPU that loads the library, for as long as the process
+// runs, and is RX_DECODE_STATIC_SCRATCH_BYTES long.  It runs exactly the same
+// kernels as rx_decode_attention.
+static __device__ __align__(256) unsigned char g_decode_static_scratch[RX_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_scratch_ptr[kStaticMaxDevices];
+}  // namespace
+
+extern "C" rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_t layer,
+                                                const void* d_q, int32_t num_q_heads,
+                                                const int32_t* d_req_to_token, int64_t row_stride,
+                                                const int32_t* d_plan,
+                                                const rx_decode_plan_info* info, int32_t B,
+                                                float scale, float* d_out, float* d_lse,
+                                                rx_stream_t stream) {
+  if (!info) return rx_internal::set_error(RX_ERR_INVALID, "rx_decode_attention_static: no plan info");
+  if (info->workspace_bytes > int64_t(RX_DECODE_STATIC_SCRATCH_BYTES)) {
+    static thread_local char buf[256];
+    snprintf(buf, sizeof(buf),
+             "rx_decode_attention_static: the plan needs %lld bytes of scratch, the static "
+             "scratch holds %lld; use rx_decode_attention with a larger buffer",
+             (long long)info->workspace_bytes, (long long)RX_DECODE_STATIC_SCRATCH_BYTES);
+    return rx_internal::set_error(RX_ERR_INVALID, buf);
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices)
+    return rx_internal::set_error(RX_ERR_CUDA, "rx_decode_attention_static: no usable current device");
+  void* scratch = nullptr;
+  {
+    // First call on this device: look up the device address of the array
+    // (a host-side reference to it is not a device pointer).
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_scratch_ptr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_static_scratch);
+      if (e != cudaSuccess || !p) {
+        static thread_local char buf[256];
+        snprintf(buf, sizeof(buf), "rx_decode_attention_static: cudaGetSymbolAddress: %s",
+                 cudaGetErrorString(e));
+        return rx_internal::set_error(RX_ERR_CUDA, buf);
+      }
+      g_static_scratch_ptr[dev] = p;
+    }
+    scratch = g_static_scratch_ptr[dev];
+  }
+  return rx_decode_attention(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
+                             info, B, scale, d_out, d_lse, scratch,
+                             size_t(RX_DECODE_STATIC_SCRATCH_BYTES), stream);
 }

@@ -24,6 +24,7 @@ _lib = C.CDLL(LIB_PATH)
 
 RX_OK, RX_ERR_INVALID, RX_ERR_NO_SPACE, RX_ERR_STATE, RX_ERR_CUDA = range(5)
 RX_WORK_WORDS = 8
+RX_DECODE_STATIC_SCRATCH_BYTES = 16 << 20   # fixed scratch of rx_decode_attention_static
 
 
 class RxError(RuntimeError):
@@ -93,6 +94,7 @@ _SIGS = {
     "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
     "rx_extend_attention": [P, I32, P, I32, P, I64, P, P, P, P, I32, I64, F32, P, P, P],
     "rx_decode_attention": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P, SZ, P],
+    "rx_decode_attention_static": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P],
     "rx_device_check": [P],
 }
 for _name, _args in _SIGS.items():
@@ -335,6 +337,15 @@ def decode_attention(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_ou
                                     d_out.data_ptr(), d_lse.data_ptr(), d_workspace.data_ptr(),
                                     d_workspace.numel() * d_workspace.element_size(),
                                     _stream(stream)))
+
+
+def decode_attention_static(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_out, d_lse,
+                            stream=None):
+    """rx_decode_attention_static: decode with the library's own fixed scratch."""
+    _check(_lib.rx_decode_attention_static(C.byref(pool), layer, d_q.data_ptr(), hq,
+                                           d_table.data_ptr(), d_table.shape[1], d_plan.data_ptr(),
+                                           C.byref(info), B, scale, d_out.data_ptr(),
+                                           d_lse.data_ptr(), _stream(stream)))
 
 
 def device_check():
