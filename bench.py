@@ -62,7 +62,7 @@ def peaks():
 class Clocks:
     """nvidia-smi sampling of SM clock and throttle reasons in the background."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -75,10 +75,14 @@ class Clocks:
                  "-lms", "100", "-i", str(index)], stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        self.marks = []
+        self.t0 = None
+        self.t1 = None
 
-    def mark(self):
-        self.marks.append(time.time())
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -92,24 +96,34 @@ class Clocks:
         with open(self.file.name) as f:
             lines = [ln.strip() for ln in f if ln.strip()]
         os.unlink(self.file.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        rows = []
         for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+        # samples inside the timed region (all samples if the region was too short)
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 - 0.15 <= r[0] <= self.t1 + 0.15]
+        use = inside if inside else rows
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, clk, cmax, flags in use:
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names, flags):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_in_timed_region": len(inside)}
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -246,12 +260,13 @@ def main():
     n_dec = sum(len(w) for w in wl.waves) * wl.decode_steps
     q_per_step = n_ext + n_dec
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clocks = Clocks(local)          # started before warm-up: its start-up is not timed
     for _ in range(args.warmup):
         eng.run()
     torch.cuda.synchronize()
+    time.sleep(0.3)
 
     # ---------------- timed: inputs resident in HBM
-    clocks = Clocks(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -260,6 +275,7 @@ def main():
     launches0 = eng.gpu_launches
     step_ev = []
     stream = torch.cuda.current_stream()
+    clocks.begin()
     wall0 = time.perf_counter()
     for _ in range(args.steps):
         flush.zero_()                                   # L2 flushed between steps
@@ -271,6 +287,7 @@ def main():
         step_ev.append((e0, e1))
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    clocks.end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()

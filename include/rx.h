@@ -272,6 +272,8 @@ typedef struct rx_decode_plan_info {
   int64_t n_shared_segments; /* tree segments read by >= 2 requests       */
   int64_t workspace_bytes;   /* device scratch rx_decode_attention needs  */
   int64_t distinct_kv_tokens;/* distinct context tokens of the batch      */
+  int64_t n_work_tc;      /* the last n_work_tc items have more than 16 rows
+                             and run on the tensor-core tile kernel       */
 } rx_decode_plan_info;
 
 /* Plan one decode step for a batch of B requests.  prompt_node[b] is the

@@ -405,43 +405,45 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restric
 }
 
 // ---------------------------------------------------------------------------
-// Decode over one work item of <= 16 query rows (a request's private tail, or
-// a shared segment chunk with few rows), head_dim 128.  No shared-memory
-// staging of K/V: every thread loads 16-byte pieces of K and V rows straight
-// from the pool into mma.sync fragments.  This works because the head
-// dimension may be permuted consistently in Q and K (the dot product does not
-// care), and the output columns may be permuted when they are written back:
-//   QK^T: thread (g = lane/4, c = lane%4) holds d in [32j+8c, 32j+8c+8) of
-//         its K row (key 8nt+g) and of Q rows g, g+8; logical k-steps 2j and
-//         2j+1 consume elements {0,1|2,3} and {4,5|6,7} of that piece;
+// Decode over work items of <= 16 query rows (a request's private tail, or a
+// shared segment chunk with few rows), head_dim 128.  One warp owns one
+// (item, KV head) unit and streams its keys in steps of 16 through a private
+// S-stage cp.async ring in shared memory, so S-1 steps of K/V (8 KB each) are
+// in flight per warp while it computes; slot indices are fetched one step
+// ahead.  The head dimension is permuted consistently in Q and K (the dot
+// product does not care) and output columns are permuted on write-back, so
+// every fragment is one 16-byte shared-memory load:
+//   QK^T: thread (g = lane/4, c = lane%4) holds d in [32j+8c, 32j+8c+8) of K
+//         row 8nt+g and of Q rows g, g+8; k-steps 2j and 2j+1 use elements
+//         {0,1|2,3} and {4,5|6,7} of that piece;
 //   PV:   output column n of n-tile t is d = 64(t/8) + 8n + t%8, so thread
-//         (g, c) reads d in [64h+8g, 64h+8g+8) of V rows 2c, 2c+1, 8+2c, 9+2c
-//         and writes 8 contiguous outputs per (row, h, e).
-// NW warps split the item's 16-key steps round-robin; their (m, l, O) are
-// merged through shared memory at the end into one partial per row.
-template <int NW>
-__global__ void __launch_bounds__(NW * 32) decode_warp_kernel(const TileArgs a) {
+//         (g, c) reads d in [64h+8g, 64h+8g+8) of V rows 2c, 2c+1, 8+2c, 9+2c.
+// Shared rows are 256 B; 16-byte chunk ch of row r sits at ch ^ ((r & 3) << 2).
+template <int NW, int S>
+__global__ void __launch_bounds__(NW * 32, 1) decode_pipe_kernel(const TileArgs a, int n_units) {
   constexpr int D = 128;
-  constexpr int NJ = D / 32;    // 16-byte pieces of a K row per thread
-  constexpr int NH = D / 64;    // 16-byte pieces of a V row per thread
-  constexpr int NT = D / 8;     // output n-tiles
-  extern __shared__ __align__(16) float dsm[];
-  float (*s_o)[16][D + 4] = reinterpret_cast<float (*)[16][D + 4]>(dsm);
-  float (*s_m)[16] = reinterpret_cast<float (*)[16]>(dsm + NW * 16 * (D + 4));
-  float (*s_l)[16] = reinterpret_cast<float (*)[16]>(dsm + NW * 16 * (D + 4) + NW * 16);
-
+  constexpr int NJ = D / 32;
+  constexpr int NH = D / 64;
+  constexpr int NT = D / 8;
+  constexpr int ROWB = D * 2;                  // bytes per key row
+  constexpr int STAGE = 2 * 16 * ROWB;         // K and V of one 16-key step
+  extern __shared__ __align__(128) uint8_t dsm_pipe[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * NW + warp;
+  if (unit >= n_units) return;                 // no block-wide barriers below
+  const int n_heads_kv = a.hq / a.group;
+  const int item = unit / n_heads_kv;
+  const int kvh = unit - item * n_heads_kv;
   const int g = lane >> 2, c = lane & 3;
-  const int kvh = blockIdx.y;
   const int G = a.group;
-  const int32_t* w = a.work + int64_t(blockIdx.x) * RX_WORK_WORDS;
+  const int32_t* w = a.work + int64_t(item) * RX_WORK_WORDS;
   const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
   const int kb = w[1], ke = w[2], member_off = w[3], part_base = w[5], n_rows = w[6];
   const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
   const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
+  const uint32_t ring = rxk::smem_addr(dsm_pipe) + uint32_t(warp * S * STAGE);
 
-  // Q pieces of rows g and g+8 (zero for rows past n_rows)
   uint4 qlo[NJ], qhi[NJ];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
@@ -449,9 +451,9 @@ __global__ void __launch_bounds__(NW * 32) decode_warp_kernel(const TileArgs a) 
     const bool ok = r < n_rows;
     const bf16* qrow = a.q;
     if (ok) {
-      const int unit = r / G;
-      const int64_t b = a.members[member_off + unit];
-      qrow = a.q + (b * a.hq + kvh * G + (r - unit * G)) * D;
+      const int u = r / G;
+      const int64_t b = a.members[member_off + u];
+      qrow = a.q + (b * a.hq + kvh * G + (r - u * G)) * D;
     }
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
@@ -461,60 +463,70 @@ __global__ void __launch_bounds__(NW * 32) decode_warp_kernel(const TileArgs a) 
     }
   }
 
+  const int n_steps = (ke - kb + 15) >> 4;
+  // lane l < 16 holds the slot of key l of the next step to issue
+  int next_slot = -1;
+  auto fetch_slot = [&](int st) {
+    const int key = kb + st * 16 + (lane & 15);
+    next_slot = (st < n_steps && key < ke) ? __ldg(trow + key) : -1;
+  };
+  auto issue = [&](int st) {
+    // 16 rows x 16 chunks for K and for V: lane covers chunk (lane & 15) of
+    // rows (lane >> 4) + 2i
+    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
+    const uint32_t vst = kst + 16 * ROWB;
+    const int ch = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = (lane >> 4) + 2 * i;
+      int64_t sl = __shfl_sync(0xffffffffu, next_slot, row);
+      const bool ok = sl >= 0;
+      if (sl >= a.num_slots) {
+        atomicOr(&g_attention_error, 1);
+        sl = 0;
+      }
+      if (!ok) sl = 0;
+      const uint32_t off = uint32_t(row * ROWB + ((ch ^ ((row & 3) << 2)) << 4));
+      rxk::cp_async_16(kst + off, kbase + sl * D + ch * 8, ok);
+      rxk::cp_async_16(vst + off, vbase + sl * D + ch * 8, ok);
+    }
+  };
+  fetch_slot(0);
+#pragma unroll
+  for (int p = 0; p < S - 1; ++p) {
+    if (p < n_steps) issue(p);
+    rxk::cp_async_commit();
+    fetch_slot(p + 1);
+  }
+
   float o[NT][4];
 #pragma unroll
   for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
 
-  const int n_steps = (ke - kb + 15) >> 4;
-  for (int st = warp; st < n_steps; st += NW) {
+  for (int st = 0; st < n_steps; ++st) {
+    rxk::cp_async_wait<S - 2>();
+    __syncwarp();
     const int k0 = kb + st * 16;
-    // slots: K rows k0+g, k0+8+g; V rows k0+2c, k0+2c+1, k0+8+2c, k0+9+2c
-    int64_t sk[2], sv[4];
-    bool vk[2], vv[4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int key = k0 + 8 * i + g;
-      vk[i] = key < ke;
-      int64_t sl = vk[i] ? __ldg(trow + key) : 0;
-      if (sl < 0 || sl >= a.num_slots) { atomicOr(&g_attention_error, 1); sl = 0; }
-      sk[i] = sl;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int key = k0 + 2 * c + (i & 1) + 8 * (i >> 1);
-      vv[i] = key < ke;
-      int64_t sl = vv[i] ? __ldg(trow + key) : 0;
-      if (sl < 0 || sl >= a.num_slots) { atomicOr(&g_attention_error, 1); sl = 0; }
-      sv[i] = sl;
-    }
-    uint4 kf[2][NJ], vf[4][NH];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        kf[i][j] = __ldg(reinterpret_cast<const uint4*>(kbase + sk[i] * D + 32 * j + 8 * c));
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        uint4 x = __ldg(reinterpret_cast<const uint4*>(vbase + sv[i] * D + 64 * h + 8 * g));
-        if (!vv[i]) x = make_uint4(0, 0, 0, 0);
-        vf[i][h] = x;
-      }
-    // S = Q K^T (16 rows x 16 keys)
+    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
+    const uint32_t vst = kst + 16 * ROWB;
     float s[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+      const int row = 8 * i + g;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
-        rxk::mma_bf16(s[i], qlo[j].x, qhi[j].x, qlo[j].y, qhi[j].y, kf[i][j].x, kf[i][j].y);
-        rxk::mma_bf16(s[i], qlo[j].z, qhi[j].z, qlo[j].w, qhi[j].w, kf[i][j].z, kf[i][j].w);
+        uint4 kf;
+        const uint32_t addr = kst + uint32_t(row * ROWB + (((4 * j + c) ^ ((row & 3) << 2)) << 4));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(kf.x), "=r"(kf.y), "=r"(kf.z), "=r"(kf.w)
+                     : "r"(addr));
+        rxk::mma_bf16(s[i], qlo[j].x, qhi[j].x, qlo[j].y, qhi[j].y, kf.x, kf.y);
+        rxk::mma_bf16(s[i], qlo[j].z, qhi[j].z, qlo[j].w, qhi[j].w, kf.z, kf.w);
       }
     }
-    // scale, mask keys past the chunk, online softmax (log2 domain)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -550,63 +562,68 @@ __global__ void __launch_bounds__(NW * 32) decode_warp_kernel(const TileArgs a) 
     const uint32_t a1 = rxk::pack_bf16(s[0][2], s[0][3]);
     const uint32_t a2 = rxk::pack_bf16(s[1][0], s[1][1]);
     const uint32_t a3 = rxk::pack_bf16(s[1][2], s[1][3]);
-    // O += P V
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const int h = t >> 3, i = t & 7;
-      const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-      const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vf[0][h])[i >> 1];
-      const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vf[1][h])[i >> 1];
-      const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vf[2][h])[i >> 1];
-      const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vf[3][h])[i >> 1];
-      const uint32_t b0 = __byte_perm(w0, w1, sel);
-      const uint32_t b1 = __byte_perm(w2, w3, sel);
       o[t][0] *= alpha[0];
       o[t][1] *= alpha[0];
       o[t][2] *= alpha[1];
       o[t][3] *= alpha[1];
-      rxk::mma_bf16(o[t], a0, a1, a2, a3, b0, b1);
     }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      uint4 vf[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = 2 * c + (q & 1) + 8 * (q >> 1);
+        const uint32_t addr = vst + uint32_t(row * ROWB + (((8 * h + g) ^ ((row & 3) << 2)) << 4));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(vf[q].x), "=r"(vf[q].y), "=r"(vf[q].z), "=r"(vf[q].w)
+                     : "r"(addr));
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+        const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vf[0])[i >> 1];
+        const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vf[1])[i >> 1];
+        const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vf[2])[i >> 1];
+        const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vf[3])[i >> 1];
+        rxk::mma_bf16(o[8 * h + i], a0, a1, a2, a3, __byte_perm(w0, w1, sel),
+                      __byte_perm(w2, w3, sel));
+      }
+    }
+    __syncwarp();  // every lane is done with this stage before it is refilled
+    if (st + S - 1 < n_steps) issue(st + S - 1);
+    rxk::cp_async_commit();
+    fetch_slot(st + S);
   }
+  rxk::cp_async_wait<0>();
 
-  // merge the NW warps' partial softmax states through shared memory
+  // write the partial (o, lse) of rows g and g+8
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     float l = l_run[e];
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     const int r = g + 8 * e;
-    if (c == 0) {
-      s_m[warp][r] = m_run[e];
-      s_l[warp][r] = l;
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int d0 = 64 * (t >> 3) + 8 * (2 * c) + (t & 7);
-      s_o[warp][r][d0] = o[t][2 * e];
-      s_o[warp][r][d0 + 8] = o[t][2 * e + 1];
-    }
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < 16 * D; idx += NW * 32) {
-    const int r = idx / D;
-    const int d = idx - r * D;
     if (r >= n_rows) continue;
-    float M = -INFINITY;
+    const int u = r / G;
+    const int head = kvh * G + (r - u * G);
+    const int64_t part = int64_t(part_base) + u;
+    float* dst = a.ws_o + (part * a.hq + head) * D;
+    const float inv = 1.f / l;
 #pragma unroll
-    for (int x = 0; x < NW; ++x) M = fmaxf(M, s_m[x][r]);
-    float L = 0.f, acc = 0.f;
+    for (int h = 0; h < NH; ++h)
 #pragma unroll
-    for (int x = 0; x < NW; ++x) {
-      const float f = (s_m[x][r] == -INFINITY) ? 0.f : rxk::fast_exp2(s_m[x][r] - M);
-      L += s_l[x][r] * f;
-      acc += s_o[x][r][d] * f;
-    }
-    const int unit = r / G;
-    const int head = kvh * G + (r - unit * G);
-    const int64_t part = int64_t(part_base) + unit;
-    a.ws_o[(part * a.hq + head) * D + d] = acc / L;
-    if (d == 0) a.ws_lse[part * a.hq + head] = M * kLn2 + logf(L);
+      for (int e2 = 0; e2 < 2; ++e2) {
+        float* d0 = dst + 64 * h + 8 * (2 * c + e2);
+        reinterpret_cast<float4*>(d0)[0] =
+            make_float4(o[8 * h + 0][2 * e + e2] * inv, o[8 * h + 1][2 * e + e2] * inv,
+                        o[8 * h + 2][2 * e + e2] * inv, o[8 * h + 3][2 * e + e2] * inv);
+        reinterpret_cast<float4*>(d0)[1] =
+            make_float4(o[8 * h + 4][2 * e + e2] * inv, o[8 * h + 5][2 * e + e2] * inv,
+                        o[8 * h + 6][2 * e + e2] * inv, o[8 * h + 7][2 * e + e2] * inv);
+      }
+    if (c == 0) a.ws_lse[part * a.hq + head] = m_run[e] * kLn2 + logf(l);
   }
 }
 
@@ -707,22 +724,34 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
   a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + ((o_bytes + 255) / 256) * 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (info->n_work > 0) {
+    const int64_t n_small = info->n_work - info->n_work_tc;
     if (D == 128) {
-      constexpr int kNW = 8;
-      constexpr int bytes = (kNW * 16 * (128 + 4) + 2 * kNW * 16) * 4;
+      constexpr int kNW = 8, kS = 3;
+      constexpr int bytes = kNW * kS * 2 * 16 * 128 * 2;
       static bool configured = false;
       if (!configured) {
-        cudaFuncSetAttribute(decode_warp_kernel<kNW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes);
+        cudaFuncSetAttribute(decode_pipe_kernel<kNW, kS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         configured = true;
       }
-      decode_warp_kernel<kNW><<<dim3(unsigned(info->n_work), pool->num_kv_heads), kNW * 32,
-                                bytes, s>>>(a);
-      st = rx_internal::launch_status("decode attention");
+      const int64_t units = n_small * pool->num_kv_heads;
+      if (units > 0) {
+        decode_pipe_kernel<kNW, kS><<<unsigned((units + kNW - 1) / kNW), kNW * 32, bytes, s>>>(
+            a, int(units));
+        st = rx_internal::launch_status("decode attention");
+        if (st != RX_OK) return st;
+      }
+      if (info->n_work_tc > 0) {
+        st = rx_internal::decode_shared_tc(
+            pool, layer, d_q, num_q_heads, d_req_to_token, row_stride,
+            d_plan + info->off_work + n_small * RX_WORK_WORDS, d_plan + info->off_members,
+            info->n_work_tc, scale, a.ws_o, a.ws_lse, s);
+        if (st != RX_OK) return st;
+      }
     } else {
       st = launch_tiles<256, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s);
+      if (st != RX_OK) return st;
     }
-    if (st != RX_OK) return st;
   }
   const unsigned blocks = unsigned((int64_t(B) * num_q_heads + 7) / 8);
   if (D == 128)

@@ -12,7 +12,8 @@
 //           causal limit per row = prefix + token + 1;
 //   decode: rows = (member request, head in group) of a tree segment chunk
 //           shared by the members; writes partial (o, lse) per row.
-// Warp roles (288 threads):
+// Warp roles (256 threads; two warps per SM sub-partition leaves up to 255
+// registers per thread for the softmax warps):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i; reads S from
 //              TMEM, keeps the running max / sum, writes P (bf16) to shared
 //              memory, rescales O in TMEM when the max grows by more than 2^8
@@ -20,7 +21,7 @@
 //   warp 4     allocates TMEM and issues tcgen05.mma from one thread:
 //              S_j = Q K_j^T (double-buffered in TMEM), O += P_j V_j (O stays
 //              in TMEM for the whole key loop);
-//   warps 5-8  gather K/V rows by slot with 16-byte cp.async into 128-byte
+//   warps 5-7  gather K/V rows by slot with 16-byte cp.async into 128-byte
 //              swizzled tiles (two stages), plus the Q tile.
 // Every mbarrier wait is bounded (about 2 s); on a timeout the CTA sets an
 // error bit, drains its tensor-core work and frees TMEM before returning.
@@ -47,7 +48,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 constexpr int BM = 128;
-constexpr int kThreads = 288;
+constexpr int kThreads = 256;
+constexpr int kLoaders = 96;  // warps 5-7
 
 struct TcArgs {
   const bf16* q;
@@ -155,8 +157,8 @@ struct Layout {
   static constexpr int V0 = K0 + 2 * KV_BYTES;
   static constexpr int P0 = V0 + 2 * KV_BYTES;
   static constexpr int BAR = P0 + 2 * P_BYTES;
-  // barriers: q, kfull[2], vfull[2], empty[2], s[2], p[2], o, final
-  static constexpr int NBAR = 13;
+  // barriers: q, kfull[2], vfull[2], emptyk[2], emptyv[2], s[2], p[2], o, final
+  static constexpr int NBAR = 15;
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int BYTES = MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = 512;
@@ -177,11 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
   auto BAR_Q = [&]() { return bar; };
   auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
   auto BAR_VF = [&](int s) { return bar + 8u * (3 + s); };
-  auto BAR_EMPTY = [&](int s) { return bar + 8u * (5 + s); };
-  auto BAR_S = [&](int s) { return bar + 8u * (7 + s); };
-  auto BAR_P = [&](int s) { return bar + 8u * (9 + s); };
-  const uint32_t BAR_O = bar + 8u * 11;
-  const uint32_t BAR_FIN = bar + 8u * 12;
+  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (5 + s); };
+  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (7 + s); };
+  auto BAR_S = [&](int s) { return bar + 8u * (9 + s); };
+  auto BAR_P = [&](int s) { return bar + 8u * (11 + s); };
+  const uint32_t BAR_O = bar + 8u * 13;
+  const uint32_t BAR_FIN = bar + 8u * 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
 
@@ -193,11 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
 
   if (tid == 0) {
-    tc::mbar_init(BAR_Q(), 128);
+    tc::mbar_init(BAR_Q(), kLoaders);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(BAR_KF(s), 128);
-      tc::mbar_init(BAR_VF(s), 128);
-      tc::mbar_init(BAR_EMPTY(s), 1);
+      tc::mbar_init(BAR_KF(s), kLoaders);
+      tc::mbar_init(BAR_VF(s), kLoaders);
+      tc::mbar_init(BAR_EMPTY_K(s), 1);
+      tc::mbar_init(BAR_EMPTY_V(s), 1);
       tc::mbar_init(BAR_S(s), 1);
       tc::mbar_init(BAR_P(s), 128);
     }
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
     // ------------------------------------------------------------ loaders
     const int tl = tid - 160;
     constexpr int CPR = D / 8;
-    for (int idx = tl; idx < BM * CPR; idx += 128) {
+    for (int idx = tl; idx < BM * CPR; idx += kLoaders) {
       const int r = idx / CPR;
       const int ch = idx - r * CPR;
       const bool ok = r < t.n_rows;
@@ -238,48 +242,72 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
     tc::mbar_arrive(BAR_Q());
     const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
     const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !tc::mbar_wait(BAR_EMPTY(s), ((j - 2) >> 1) & 1, abort_flag, kWaitLimit))
-        break;
+    // Thread tl copies 16-byte chunk (tl % CPR) of key rows tl / CPR + r * RSTEP.
+    static_assert(kLoaders % CPR == 0, "loader threads cover whole rows");
+    constexpr int RSTEP = kLoaders / CPR;
+    constexpr int NR = (BN + RSTEP - 1) / RSTEP;  // rows per thread per tile (last may be out)
+    const int ch = tl % CPR;
+    const int r0 = tl / CPR;
+    int32_t slot[NR];  // slots of the next tile to issue, loaded one tile ahead
+    auto load_slots = [&](int j) {
       const int k0 = t.key_begin + j * BN;
-      const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
-      const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
-      for (int idx = tl; idx < BN * CPR; idx += 128) {
-        const int r = idx / CPR;
-        const int ch = idx - r * CPR;
-        const int key = k0 + r;
-        const bool ok = key < t.key_end;
-        int64_t slot = 0;
-        if (ok) {
-          slot = __ldg(t.trow + key);
-          if (slot < 0 || slot >= a.num_slots) {
-            atomicOr(&g_tc_error, 1);
-            slot = 0;
-          }
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const int row = r0 + r * RSTEP;
+        const int key = k0 + row;
+        slot[r] = (row < BN && key < t.key_end) ? __ldg(t.trow + key) : -1;
+      }
+    };
+    auto issue = [&](const bf16* src_base, uint32_t dst) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const int row = r0 + r * RSTEP;
+        if (row >= BN) break;
+        int64_t sl = slot[r];
+        const bool ok = sl >= 0;
+        if (sl >= a.num_slots) {
+          atomicOr(&g_tc_error, 1);
+          sl = 0;
         }
-        rxk::cp_async_16(sw128(sk, BN, r, ch), kb + slot * D + ch * 8, ok);
+        if (!ok) sl = 0;
+        rxk::cp_async_16(sw128(dst, BN, row, ch), src_base + sl * D + ch * 8, ok);
+      }
+    };
+    auto k_stage = [&](int j) { return base + Lo::K0 + (j & 1) * Lo::KV_BYTES; };
+    auto v_stage = [&](int j) { return base + Lo::V0 + (j & 1) * Lo::KV_BYTES; };
+    if (n_tiles > 0) {
+      load_slots(0);
+      issue(kb, k_stage(0));
+      rxk::cp_async_commit();
+      issue(vb, v_stage(0));
+      rxk::cp_async_commit();
+      if (n_tiles > 1) load_slots(1);
+    }
+    // Up to two tiles in flight: K_{j+1} is issued before K_j is awaited; a K
+    // stage is free once S of its previous tile completed, a V stage once PV
+    // of its previous tile completed.
+    for (int j = 0; j < n_tiles; ++j) {
+      if (j + 1 < n_tiles) {
+        if (j + 1 >= 2 &&
+            !tc::mbar_wait(BAR_EMPTY_K((j + 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitLimit))
+          break;
+        issue(kb, k_stage(j + 1));
       }
       rxk::cp_async_commit();
-      for (int idx = tl; idx < BN * CPR; idx += 128) {
-        const int r = idx / CPR;
-        const int ch = idx - r * CPR;
-        const int key = k0 + r;
-        const bool ok = key < t.key_end;
-        int64_t slot = 0;
-        if (ok) {
-          slot = __ldg(t.trow + key);
-          if (slot < 0 || slot >= a.num_slots) slot = 0;
-        }
-        rxk::cp_async_16(sw128(sv, BN, r, ch), vb + slot * D + ch * 8, ok);
+      rxk::cp_async_wait<2>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(BAR_KF(j & 1));
+      if (j + 1 < n_tiles) {
+        if (j + 1 >= 2 &&
+            !tc::mbar_wait(BAR_EMPTY_V((j + 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitLimit))
+          break;
+        issue(vb, v_stage(j + 1));
+        if (j + 2 < n_tiles) load_slots(j + 2);
       }
       rxk::cp_async_commit();
-      rxk::cp_async_wait<1>();
+      rxk::cp_async_wait<2>();
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_KF(s));
-      rxk::cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_VF(s));
+      tc::mbar_arrive(BAR_VF(j & 1));
     }
     rxk::cp_async_wait<0>();
   } else if (warp == 4) {
@@ -299,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
           tc::mma_bf16_ss(tmem + uint32_t(s * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(BAR_S(s));
+        tc::mma_commit(BAR_EMPTY_K(s));
       };
       if (ok && n_tiles > 0) {
         ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit);
@@ -328,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
                           (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(BAR_O);
-        tc::mma_commit(BAR_EMPTY(s));
+        tc::mma_commit(BAR_EMPTY_V(s));
       }
       // drain: every MMA issued above has completed once this arrives
       tc::mma_commit(BAR_FIN);
@@ -355,18 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
       tc::tc_fence_after();
       const int k0 = t.key_begin + j * BN;
       const bool need_mask = k0 + BN > t.nomask_end;
+      // the whole S row of this thread, one TMEM round trip
+      uint32_t sr[BN];
+      tc::tmem_ld_row<BN>(tl + uint32_t(s * BN), sr);
+      tc::tmem_ld_wait();
       float mx = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        uint32_t r[32];
-        tc::tmem_ld32(tl + uint32_t(s * BN + cc * 32), r);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(r[e]) * a.scale_log2;
-          if (need_mask && k0 + cc * 32 + e >= lim) x = -INFINITY;
-          mx = fmaxf(mx, x);
-        }
+      for (int e = 0; e < BN; ++e) {
+        float x = __uint_as_float(sr[e]) * a.scale_log2;
+        if (need_mask && k0 + e >= lim) x = -INFINITY;
+        sr[e] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
       }
       const float m_new = fmaxf(m_ref, mx);
       if (j == 0) {
@@ -401,18 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
       const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
 #pragma unroll
       for (int cc = 0; cc < BN / 32; ++cc) {
-        uint32_t r[32];
-        tc::tmem_ld32(tl + uint32_t(s * BN + cc * 32), r);
-        tc::tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float x0 = __uint_as_float(r[e]) * a.scale_log2;
-          float x1 = __uint_as_float(r[e + 1]) * a.scale_log2;
-          if (need_mask && k0 + cc * 32 + e >= lim) x0 = -INFINITY;
-          if (need_mask && k0 + cc * 32 + e + 1 >= lim) x1 = -INFINITY;
-          const float p0 = rxk::fast_exp2(x0 - m_use);
-          const float p1 = rxk::fast_exp2(x1 - m_use);
+          const float p0 = rxk::fast_exp2(__uint_as_float(sr[cc * 32 + e]) - m_use);
+          const float p1 = rxk::fast_exp2(__uint_as_float(sr[cc * 32 + e + 1]) - m_use);
           l += p0 + p1;
           pk[e >> 1] = rxk::pack_bf16(p0, p1);
         }
@@ -428,9 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
       tc::tc_fence_before();
       tc::mbar_arrive(BAR_P(s));
     }
+    // The epilogue waits on BAR_FIN, which completes exactly once, after every
+    // MMA of the CTA.  Waiting on BAR_O's parity here would be ambiguous: when
+    // this warp finishes its last tile, PV of the tile before may still run, and
+    // the last completed phase of BAR_O then has the parity of the last PV.
     if (ok && n_tiles > 0 &&
-        __all_sync(0xffffffffu,
-                   tc::mbar_wait(BAR_O, (n_tiles - 1) & 1, abort_flag, kWaitLimit))) {
+        __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit))) {
       tc::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float* dst;
@@ -494,6 +518,32 @@ int32_t tc_error_flags(bool clear) {
     cudaMemcpyToSymbol(g_tc_error, &z, sizeof(z));
   }
   return v;
+}
+
+rx_status decode_shared_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                           int32_t num_q_heads, const int32_t* d_req_to_token,
+                           int64_t row_stride, const int32_t* d_work, const int32_t* d_members,
+                           int64_t n_work, float scale, float* ws_o, float* ws_lse,
+                           cudaStream_t stream) {
+  const int D = pool->head_dim;
+  TcArgs a{};
+  a.q = static_cast<const bf16*>(d_q);
+  const int64_t layer_off = int64_t(layer) * pool->num_kv_heads * pool->num_slots * D;
+  a.kpool = static_cast<const bf16*>(pool->k_pool) + layer_off;
+  a.vpool = static_cast<const bf16*>(pool->v_pool) + layer_off;
+  a.head_stride = pool->num_slots * D;
+  a.num_slots = pool->num_slots;
+  a.table = d_req_to_token;
+  a.row_stride = row_stride;
+  a.hq = num_q_heads;
+  a.group = num_q_heads / pool->num_kv_heads;
+  a.scale_log2 = scale * kLog2e;
+  a.work = d_work;
+  a.members = d_members;
+  a.ws_o = ws_o;
+  a.ws_lse = ws_lse;
+  if (D != 128) return set_error(RX_ERR_INVALID, "tensor-core decode tiles need head_dim 128");
+  return launch<128, 128, true>(a, unsigned(n_work), pool->num_kv_heads, stream);
 }
 
 rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,

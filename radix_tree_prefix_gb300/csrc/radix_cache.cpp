@@ -583,7 +583,7 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
   const int32_t G = num_q_heads / num_kv_heads;
   if (head_dim != 128 && head_dim != 256)
     return fail(RX_ERR_INVALID, "rx_plan_decode: head_dim must be 128 or 256");
-  if (G > rx_internal::decode_rows_per_item(head_dim))
+  if (G > rx_internal::decode_rows_per_item(head_dim) || (head_dim == 256 && G > 64))
     return fail(RX_ERR_INVALID, "rx_plan_decode: group size %d above %d", G,
                 rx_internal::decode_rows_per_item(head_dim));
   std::vector<std::vector<const Node*>> paths(static_cast<size_t>(B));
@@ -630,37 +630,66 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     }
     if (ctx_len[b] > pos) segs.push_back(Seg{req_rows[b], pos, int64_t(ctx_len[b]), {b}});
   }
-  // work items
+  // work items: (key chunk, member block) of each segment.  head_dim 128:
+  // segments with <= kDecodeSmallRows rows go to the warp-pipelined kernel
+  // (listed first), larger ones to the tensor-core tile kernel in member blocks
+  // of <= kDecodeTcRows rows (listed last); head_dim 256: 64-row items.
   struct Work {
     int32_t row, kb, ke, member_off, n_members;
   };
-  std::vector<Work> work;
+  std::vector<Work> small, large;
   std::vector<int32_t> members;
-  const int32_t rows_per_item = rx_internal::decode_rows_per_item(head_dim);
-  const int32_t per_block = rows_per_item / G;
-  const int64_t tile = rx_internal::kDecodeKeyStep;
   int64_t distinct = 0;
   for (const Seg& s : segs) {
-    int64_t n = s.ke - s.kb;
+    const int64_t n = s.ke - s.kb;
     distinct += n;
-    int32_t k = int32_t(s.members.size());
-    int64_t chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, int64_t(2) * k * G);
-    int64_t n_chunks = (n + chunk - 1) / chunk;
+    const int32_t k = int32_t(s.members.size());
+    const int64_t rows = int64_t(k) * G;
+    bool is_small;
+    int32_t per_block;
+    int64_t chunk, step;
+    if (head_dim == 128 && rows <= rx_internal::kDecodeSmallRows) {
+      is_small = true;
+      per_block = k;
+      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 2 * rows);
+      step = 16;
+    } else if (head_dim == 128) {
+      is_small = false;
+      per_block = rx_internal::kDecodeTcRows / G;
+      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 4 * rows);
+      step = 128;
+    } else {
+      is_small = false;
+      per_block = 64 / G;
+      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 2 * rows);
+      step = 64;
+    }
+    const int64_t n_chunks = (n + chunk - 1) / chunk;
     int64_t len = (n + n_chunks - 1) / n_chunks;
-    len = (len + tile - 1) / tile * tile;
-    int32_t moff = int32_t(members.size());
+    len = (len + step - 1) / step * step;
+    const int32_t moff = int32_t(members.size());
     members.insert(members.end(), s.members.begin(), s.members.end());
     for (int64_t kb = s.kb; kb < s.ke; kb += len) {
-      int64_t ke = std::min(s.ke, kb + len);
+      const int64_t ke = std::min(s.ke, kb + len);
       for (int32_t m0 = 0; m0 < k; m0 += per_block) {
-        work.push_back(Work{s.row, int32_t(kb), int32_t(ke), moff + m0,
-                            std::min(per_block, k - m0)});
+        Work w{s.row, int32_t(kb), int32_t(ke), moff + m0, std::min(per_block, k - m0)};
+        (is_small ? small : large).push_back(w);
       }
     }
   }
-  std::stable_sort(work.begin(), work.end(), [](const Work& a, const Work& b) {
+  auto heavier = [](const Work& a, const Work& b) {
     return int64_t(a.ke - a.kb) * a.n_members > int64_t(b.ke - b.kb) * b.n_members;
-  });
+  };
+  std::stable_sort(small.begin(), small.end(), heavier);
+  std::stable_sort(large.begin(), large.end(), heavier);
+  std::vector<Work> work = small;
+  if (head_dim == 128) {
+    work.insert(work.end(), large.begin(), large.end());
+    info->n_work_tc = int64_t(large.size());
+  } else {
+    work.insert(work.end(), large.begin(), large.end());
+    info->n_work_tc = 0;
+  }
   std::vector<std::vector<int32_t>> parts_of(static_cast<size_t>(B));
   int64_t n_parts = 0;
   for (const Work& w : work) {

@@ -8,10 +8,14 @@
 
 namespace rx_internal {
 
-// Decode: query rows (member requests x group heads) of one work item: 16
-// for the register-fragment kernel (head_dim 128), 64 for the shared-memory
-// tile kernel (head_dim 256).
-inline int decode_rows_per_item(int head_dim) { return head_dim == 128 ? 16 : 64; }
+// Decode work items (head_dim 128): segments with at most kDecodeSmallRows
+// query rows (members x group heads) go to the warp-pipelined kernel; larger
+// ones are cut into member blocks of at most kDecodeTcRows rows for the
+// tensor-core tile kernel.  head_dim 256 uses 64-row items of the shared-
+// memory tile kernel.
+constexpr int kDecodeSmallRows = 16;
+constexpr int kDecodeTcRows = 128;
+inline int decode_rows_per_item(int head_dim) { return head_dim == 128 ? kDecodeTcRows : 64; }
 // Decode: a segment chunk is at least this many keys (and at least 2 keys per
 // query row, so partial results stay small next to the KV they summarise).
 constexpr int kDecodeMinChunk = 512;
@@ -34,6 +38,11 @@ int sm_count();
 int32_t kv_store_error_flags(bool clear);
 int32_t attention_error_flags(bool clear);
 int32_t tc_error_flags(bool clear);
+rx_status decode_shared_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                           int32_t num_q_heads, const int32_t* d_req_to_token,
+                           int64_t row_stride, const int32_t* d_work, const int32_t* d_members,
+                           int64_t n_work, float scale, float* ws_o, float* ws_lse,
+                           cudaStream_t stream);
 rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                               int32_t num_q_heads, const int32_t* d_req_to_token,
                               int64_t row_stride, const int32_t* d_req_rows,

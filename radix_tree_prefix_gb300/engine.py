@@ -149,7 +149,7 @@ class _Staging:
         if self.events[i] is not None:
             self.events[i].synchronize()
         if self.host[i] is None or self.host[i].numel() < n:
-            cap = max(n, 1 << 16) * 2
+            cap = max(2 * n, 1 << 21)
             self.host[i] = torch.empty(cap, dtype=torch.int32, pin_memory=True)
             self.dev[i] = torch.empty(cap, dtype=torch.int32, device=self.device)
         h = self.host[i].numpy()

@@ -79,6 +79,7 @@ class GpuRun:
         wl = self.wl
         errs = []
         n = 0
+        self.worst = {}
         for (rid, layer), (m, sel, o, lse) in self.ext.items():
             r = wl.requests[rid]
             pidx = wl.prompt_store_index(r)
@@ -88,6 +89,7 @@ class GpuRun:
             want_o, want_l = oatt.softmax_attention(q, k, v, m + sel + 1)
             errs.append(np.abs(o - want_o).ravel())
             errs.append(np.abs(lse - want_l).ravel())
+            self.worst[("extend", rid, layer)] = float(max(errs[-1].max(), errs[-2].max()))
             n += len(sel)
         for (rid, t, layer), (o, lse) in self.dec.items():
             r = wl.requests[rid]
@@ -99,6 +101,7 @@ class GpuRun:
                                                    self._rows("v", layer, ctx))
             errs.append(np.abs(o - want_o).ravel())
             errs.append(np.abs(lse - want_l).ravel())
+            self.worst[("decode", rid, t, layer)] = float(max(errs[-1].max(), errs[-2].max()))
             n += 1
         e = np.concatenate(errs)
         return float(e.max()), float(e.mean()), n
@@ -107,6 +110,7 @@ class GpuRun:
         mx, mean, n = self.compare()
         assert n > 0
         assert self.flags == 0
-        assert mx <= MAX_ABS, f"max abs error {mx} over {n} rows"
+        bad = sorted(((v, k) for k, v in self.worst.items() if v > MAX_ABS), reverse=True)
+        assert mx <= MAX_ABS, f"max abs error {mx} over {n} rows; worst: {bad[:6]}"
         assert mean <= MEAN_ABS, f"mean abs error {mean} over {n} rows"
         return mx, mean, n

@@ -206,7 +206,7 @@ def test_decode_plan_covers_every_context_once():
     members = plan[info.off_members:info.off_members + info.n_member_entries]
     covered = {b: [] for b in range(len(wave))}
     for row, kb, ke, moff, nm, pbase, nrows, _ in work:
-        assert nrows == nm * G and nm * G <= 64
+        assert nrows == nm * G and nm * G <= 128
         for i in range(nm):
             b = int(members[moff + i])
             covered[b].append((int(kb), int(ke)))
