@@ -372,6 +372,33 @@ rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
                               void* d_workspace, size_t workspace_bytes,
                               rx_stream_t stream);
 
+/* A run of decode steps planned ahead ([T] "The overlap that pays for
+ * itself": the next batch is built from slot numbers, never from sampled
+ * values, so allocation and planning run ahead of the GPU).  For each step
+ * s < n_steps, in order on the stream: rx_kv_store of that step's new tokens
+ * (steps[s].d_k / d_v at steps[s].d_slots, B tokens), then
+ * rx_decode_attention with steps[s]'s plan, queries and outputs.  The
+ * req_to_token rows must already hold every step's slots (a token's position
+ * beyond a step's context is never read by that step).  d_workspace must hold
+ * the largest steps[s].info->workspace_bytes.  Stops at the first error. */
+typedef struct rx_decode_step {
+  const void* d_q;          /* bf16 [B][Hq][head_dim]                     */
+  const void* d_k;          /* bf16 [B][Hkv][head_dim] new tokens' K      */
+  const void* d_v;          /* bf16 [B][Hkv][head_dim] new tokens' V      */
+  const int32_t* d_slots;   /* device int32 [B] new tokens' slots         */
+  const int32_t* d_plan;    /* device copy of this step's plan            */
+  const rx_decode_plan_info* info; /* host info of that plan             */
+  float* d_out;             /* fp32 [B][Hq][head_dim]                     */
+  float* d_lse;             /* fp32 [B][Hq]                               */
+} rx_decode_step;
+
+rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer,
+                          int32_t num_q_heads, const int32_t* d_req_to_token,
+                          int64_t row_stride, const rx_decode_step* steps,
+                          int32_t n_steps, int32_t B, float scale,
+                          void* d_workspace, size_t workspace_bytes,
+                          rx_stream_t stream);
+
 /* Decode attention that allocates nothing and takes no scratch buffer.  The
  * pages have no counterpart of this call; it exists for callers that cannot
  * supply device memory -- e.g. a host whose device memory is all reserved up

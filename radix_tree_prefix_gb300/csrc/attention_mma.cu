@@ -726,7 +726,7 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
   if (info->n_work > 0) {
     const int64_t n_small = info->n_work - info->n_work_tc;
     if (D == 128) {
-      constexpr int kNW = 8, kS = 3;
+      constexpr int kNW = 2, kS = 3;  // 48 KB per CTA: four CTAs per SM
       constexpr int bytes = kNW * kS * 2 * 16 * 128 * 2;
       static bool configured = false;
       if (!configured) {
@@ -763,6 +763,25 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
                                                  d_plan + info->off_req_parts, a.ws_o, a.ws_lse,
                                                  num_q_heads, B, d_out, d_lse);
   return rx_internal::launch_status("decode merge");
+}
+
+extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, int32_t num_q_heads,
+                                     const int32_t* d_req_to_token, int64_t row_stride,
+                                     const rx_decode_step* steps, int32_t n_steps, int32_t B,
+                                     float scale, void* d_workspace, size_t workspace_bytes,
+                                     rx_stream_t stream) {
+  if (n_steps < 0 || (n_steps && !steps))
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_decode_steps: bad step list");
+  for (int32_t i = 0; i < n_steps; ++i) {
+    const rx_decode_step& st = steps[i];
+    rx_status r = rx_kv_store(pool, layer, st.d_slots, st.d_k, st.d_v, B, stream);
+    if (r != RX_OK) return r;
+    r = rx_decode_attention(pool, layer, st.d_q, num_q_heads, d_req_to_token, row_stride, st.d_plan,
+                            st.info, B, scale, st.d_out, st.d_lse, d_workspace, workspace_bytes,
+                            stream);
+    if (r != RX_OK) return r;
+  }
+  return RX_OK;
 }
 
 // ---------------------------------------------------------------------------

@@ -12,8 +12,8 @@
 //           causal limit per row = prefix + token + 1;
 //   decode: rows = (member request, head in group) of a tree segment chunk
 //           shared by the members; writes partial (o, lse) per row.
-// Warp roles (256 threads; two warps per SM sub-partition leaves up to 255
-// registers per thread for the softmax warps):
+// Warp roles (192 threads; at most two warps per SM sub-partition, so the
+// softmax warps may use up to 255 registers):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i; reads S from
 //              TMEM, keeps the running max / sum, writes P (bf16) to shared
 //              memory, rescales O in TMEM when the max grows by more than 2^8
@@ -21,11 +21,16 @@
 //   warp 4     allocates TMEM and issues tcgen05.mma from one thread:
 //              S_j = Q K_j^T (double-buffered in TMEM), O += P_j V_j (O stays
 //              in TMEM for the whole key loop);
-//   warps 5-7  gather K/V rows by slot with 16-byte cp.async into 128-byte
-//              swizzled tiles (two stages), plus the Q tile.
+//   warp 5     loads K/V tiles into 128-byte swizzled shared memory (two
+//              stages): a tile whose slots form one contiguous run (the
+//              allocator hands out runs, so this is the common case) is one TMA
+//              box load per 64 columns; any other tile, and the ragged last tile,
+//              is gathered slot by slot with 16-byte cp.async (rows past the key
+//              range are zero-filled).  Also loads the Q tile.
 // Every mbarrier wait is bounded (about 2 s); on a timeout the CTA sets an
 // error bit, drains its tensor-core work and frees TMEM before returning.
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -40,6 +45,25 @@
 // bit 1: a barrier wait timed out.  Read by rx_device_check().
 static __device__ int32_t g_tc_error;
 
+#ifdef RX_TC_TRACE
+// Development timeline of CTA (0, 0): globaltimer stamps per tile and role.
+// Compiled only with -DRX_TC_TRACE (never in the library build).
+static __device__ unsigned long long g_tc_trace[16][256];
+__device__ __forceinline__ unsigned long long tc_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define TC_TRACE(ev, j)                                                          \
+  do {                                                                           \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < 256) g_tc_trace[ev][j] = tc_now(); \
+  } while (0)
+#else
+#define TC_TRACE(ev, j) \
+  do {                  \
+  } while (0)
+#endif
+
 namespace {
 
 using bf16 = __nv_bfloat16;
@@ -47,9 +71,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr uint32_t kSleepNs = 20000;            // MMA / loader waits sleep instead of spinning
+constexpr float kMasked = -1.0e30f;             // raw score of a masked key
 constexpr int BM = 128;
-constexpr int kThreads = 256;
-constexpr int kLoaders = 96;  // warps 5-7
+constexpr int kThreads = 192;
 
 struct TcArgs {
   const bf16* q;
@@ -71,6 +96,8 @@ struct TcArgs {
   int num_tiles;
   float* out;
   float* lse;
+  int64_t tma_row_base;  // row of (layer, KV head 0, slot 0) in the tensor maps
+  int64_t tma_head_rows; // rows per KV head (num_slots)
   // decode
   const int32_t* work;
   const int32_t* members;
@@ -166,7 +193,9 @@ struct Layout {
 };
 
 template <int D, int BN, bool DECODE>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
   using Lo = Layout<D, BN>;
   static_assert(2 * BN + D <= Lo::TMEM_COLS, "TMEM budget");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -196,10 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
 
   if (tid == 0) {
-    tc::mbar_init(BAR_Q(), kLoaders);
+    tc::mbar_init(BAR_Q(), 1);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(BAR_KF(s), kLoaders);
-      tc::mbar_init(BAR_VF(s), kLoaders);
+      tc::mbar_init(BAR_KF(s), 1);
+      tc::mbar_init(BAR_VF(s), 1);
       tc::mbar_init(BAR_EMPTY_K(s), 1);
       tc::mbar_init(BAR_EMPTY_V(s), 1);
       tc::mbar_init(BAR_S(s), 1);
@@ -219,11 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 5) {
-    // ------------------------------------------------------------ loaders
-    const int tl = tid - 160;
+  if (warp == 5) {
+    // ------------------------------------------------------------- loader
     constexpr int CPR = D / 8;
-    for (int idx = tl; idx < BM * CPR; idx += kLoaders) {
+    constexpr int SPL = BN / 32;  // slots per lane: rows lane + 32 i
+    for (int idx = lane; idx < BM * CPR; idx += 32) {
       const int r = idx / CPR;
       const int ch = idx - r * CPR;
       const bool ok = r < t.n_rows;
@@ -239,83 +268,97 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
     rxk::cp_async_commit();
     rxk::cp_async_wait<0>();
     tc::fence_proxy_async_smem();
-    tc::mbar_arrive(BAR_Q());
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(BAR_Q());
     const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
     const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
-    // Thread tl copies 16-byte chunk (tl % CPR) of key rows tl / CPR + r * RSTEP.
-    static_assert(kLoaders % CPR == 0, "loader threads cover whole rows");
-    constexpr int RSTEP = kLoaders / CPR;
-    constexpr int NR = (BN + RSTEP - 1) / RSTEP;  // rows per thread per tile (last may be out)
-    const int ch = tl % CPR;
-    const int r0 = tl / CPR;
-    int32_t slot[NR];  // slots of the next tile to issue, loaded one tile ahead
-    auto load_slots = [&](int j) {
+    const int64_t row0 = a.tma_row_base + int64_t(kvh) * a.tma_head_rows;
+    int32_t slot[SPL];  // slots of the tile being loaded
+    int32_t nxt[SPL];   // slots of the following tile, in flight meanwhile
+    auto load_slots = [&](int j, int32_t (&dst)[SPL]) {
       const int k0 = t.key_begin + j * BN;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const int row = r0 + r * RSTEP;
-        const int key = k0 + row;
-        slot[r] = (row < BN && key < t.key_end) ? __ldg(t.trow + key) : -1;
+      for (int i = 0; i < SPL; ++i) {
+        const int key = k0 + lane + 32 * i;
+        dst[i] = (j < n_tiles && key < t.key_end) ? __ldg(t.trow + key) : -1;
       }
     };
-    auto issue = [&](const bf16* src_base, uint32_t dst) {
+    auto check_slots = [&]() {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const int row = r0 + r * RSTEP;
-        if (row >= BN) break;
-        int64_t sl = slot[r];
-        const bool ok = sl >= 0;
-        if (sl >= a.num_slots) {
+      for (int i = 0; i < SPL; ++i) {
+        if (slot[i] >= a.num_slots || slot[i] < -1) {
           atomicOr(&g_tc_error, 1);
-          sl = 0;
+          slot[i] = 0;
         }
-        if (!ok) sl = 0;
-        rxk::cp_async_16(sw128(dst, BN, row, ch), src_base + sl * D + ch * 8, ok);
       }
     };
-    auto k_stage = [&](int j) { return base + Lo::K0 + (j & 1) * Lo::KV_BYTES; };
-    auto v_stage = [&](int j) { return base + Lo::V0 + (j & 1) * Lo::KV_BYTES; };
-    if (n_tiles > 0) {
-      load_slots(0);
-      issue(kb, k_stage(0));
-      rxk::cp_async_commit();
-      issue(vb, v_stage(0));
-      rxk::cp_async_commit();
-      if (n_tiles > 1) load_slots(1);
-    }
-    // Up to two tiles in flight: K_{j+1} is issued before K_j is awaited; a K
-    // stage is free once S of its previous tile completed, a V stage once PV
-    // of its previous tile completed.
+    // one K or V tile: TMA box loads if the slots are one contiguous run of
+    // BN valid slots, else a zero-filling cp.async gather
+    auto load_tile = [&](const CUtensorMap* tm, const bf16* src_base, uint32_t dst, uint32_t full_bar) {
+      const int32_t first = __shfl_sync(0xffffffffu, slot[0], 0);
+      bool run = first >= 0 && int64_t(first) + BN <= a.num_slots;
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) run = run && (slot[i] == first + lane + 32 * i);
+      run = __all_sync(0xffffffffu, run);
+      if (run) {
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(full_bar, uint32_t(BN * D * 2));
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            tc::tma_load_2d(dst + uint32_t(cb * BN * 128), tm, cb * 64, int(row0 + first),
+                            full_bar);
+        }
+      } else {
+        // lanes 0-15 and 16-31 copy chunks (lane % 16) + 16 h of rows 2k, 2k+1
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+#pragma unroll 4
+          for (int k = 0; k < 16; ++k) {
+            const int row = 32 * i + 2 * k + (lane >> 4);
+            const int32_t sl = __shfl_sync(0xffffffffu, slot[i], row & 31);
+            const bool ok = sl >= 0;
+            const int64_t s64 = ok ? int64_t(sl) : 0;
+#pragma unroll
+            for (int h = 0; h < CPR / 16; ++h) {
+              const int ch = (lane & 15) + 16 * h;
+              rxk::cp_async_16(sw128(dst, BN, row, ch), src_base + s64 * D + ch * 8, ok);
+            }
+          }
+        }
+        rxk::cp_async_commit();
+        rxk::cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(full_bar);
+      }
+    };
+    load_slots(0, slot);
+    load_slots(1, nxt);
     for (int j = 0; j < n_tiles; ++j) {
-      if (j + 1 < n_tiles) {
-        if (j + 1 >= 2 &&
-            !tc::mbar_wait(BAR_EMPTY_K((j + 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitLimit))
-          break;
-        issue(kb, k_stage(j + 1));
-      }
-      rxk::cp_async_commit();
-      rxk::cp_async_wait<2>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_KF(j & 1));
-      if (j + 1 < n_tiles) {
-        if (j + 1 >= 2 &&
-            !tc::mbar_wait(BAR_EMPTY_V((j + 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitLimit))
-          break;
-        issue(vb, v_stage(j + 1));
-        if (j + 2 < n_tiles) load_slots(j + 2);
-      }
-      rxk::cp_async_commit();
-      rxk::cp_async_wait<2>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_VF(j & 1));
+      const int s = j & 1;
+      check_slots();
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(s), ((j - 2) >> 1) & 1, abort_flag,
+                                                  kWaitLimit, kSleepNs)))
+        break;
+      load_tile(&tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
+      if (lane == 0) TC_TRACE(0, j);
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(s), ((j - 2) >> 1) & 1, abort_flag,
+                                                  kWaitLimit, kSleepNs)))
+        break;
+      load_tile(&tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
+      if (lane == 0) TC_TRACE(2, j);
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) slot[i] = nxt[i];
+      load_slots(j + 2, nxt);
     }
-    rxk::cp_async_wait<0>();
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
       constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
-      bool ok = tc::mbar_wait(BAR_Q(), 0, abort_flag, kWaitLimit);
+      bool ok = tc::mbar_wait(BAR_Q(), 0, abort_flag, kWaitLimit, kSleepNs);
       auto issue_s = [&](int j) {
         const int s = j & 1;
         const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
@@ -328,9 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
         }
         tc::mma_commit(BAR_S(s));
         tc::mma_commit(BAR_EMPTY_K(s));
+        TC_TRACE(4, j);
       };
       if (ok && n_tiles > 0) {
-        ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit);
+        ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit, kSleepNs);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0);
@@ -339,12 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int s = j & 1;
         if (j + 1 < n_tiles) {
-          if (!tc::mbar_wait(BAR_KF((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimit)) break;
+          if (!tc::mbar_wait(BAR_KF((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimit,
+                             kSleepNs))
+            break;
           tc::tc_fence_after();
           issue_s(j + 1);
         }
-        if (!tc::mbar_wait(BAR_P(s), (j >> 1) & 1, abort_flag, kWaitLimit)) break;
-        if (!tc::mbar_wait(BAR_VF(s), (j >> 1) & 1, abort_flag, kWaitLimit)) break;
+        if (!tc::mbar_wait(BAR_P(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
+        if (!tc::mbar_wait(BAR_VF(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
         tc::tc_fence_after();
         const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
         const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
@@ -358,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
         }
         tc::mma_commit(BAR_O);
         tc::mma_commit(BAR_EMPTY_V(s));
+        TC_TRACE(5, j);
       }
       // drain: every MMA issued above has completed once this arrives
       tc::mma_commit(BAR_FIN);
@@ -382,20 +429,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
         break;
       }
       tc::tc_fence_after();
+      if (i == 0) TC_TRACE(6, j);
       const int k0 = t.key_begin + j * BN;
       const bool need_mask = k0 + BN > t.nomask_end;
       // the whole S row of this thread, one TMEM round trip
       uint32_t sr[BN];
       tc::tmem_ld_row<BN>(tl + uint32_t(s * BN), sr);
       tc::tmem_ld_wait();
-      float mx = -INFINITY;
+      if (i == 0) TC_TRACE(8, j);
+      // row max of the raw scores (masked keys get a large negative finite
+      // score, so the packed exponent below never sees an infinity); eight
+      // independent partial maxima keep the dependency chains short
+      float mx8[8];
 #pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        float x = __uint_as_float(sr[e]) * a.scale_log2;
-        if (need_mask && k0 + e >= lim) x = -INFINITY;
-        sr[e] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+      for (int u = 0; u < 8; ++u) mx8[u] = kMasked;
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          if (k0 + e >= lim) sr[e] = __float_as_uint(kMasked);
+          mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
       }
+      const float mx = a.scale_log2 *
+                       fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_ref, mx);
       if (j == 0) {
         m_ref = m_new;
@@ -427,15 +487,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
+      float l8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) l8[u] = 0.f;
 #pragma unroll
       for (int cc = 0; cc < BN / 32; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = rxk::fast_exp2(__uint_as_float(sr[cc * 32 + e]) - m_use);
-          const float p1 = rxk::fast_exp2(__uint_as_float(sr[cc * 32 + e + 1]) - m_use);
-          l += p0 + p1;
-          pk[e >> 1] = rxk::pack_bf16(p0, p1);
+          // p = 2^(scale*s - m) for two keys at once: the exponents are rounded
+          // to bf16 with integer ops (add half an ulp, keep the high half) and
+          // one packed SFU op gives both p in bf16 (the precision P has in the
+          // PV product); the row sum adds exactly those values in fp32, in
+          // eight independent partial sums.
+          const float x0 = fmaf(__uint_as_float(sr[cc * 32 + e]), a.scale_log2, -m_use);
+          const float x1 = fmaf(__uint_as_float(sr[cc * 32 + e + 1]), a.scale_log2, -m_use);
+          const uint32_t h = rxk::exp2_bf16x2_bits(__float_as_uint(x0) + 0x8000u,
+                                                   __float_as_uint(x1) + 0x8000u);
+          l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
+          pk[e >> 1] = h;
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -445,9 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
                        : "memory");
         }
       }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      if (i == 0) TC_TRACE(10, j);
       tc::fence_proxy_async_smem();
+      if (i == 0) TC_TRACE(11, j);
       tc::tc_fence_before();
       tc::mbar_arrive(BAR_P(s));
+      if (i == 0) TC_TRACE(7, j);
     }
     // The epilogue waits on BAR_FIN, which completes exactly once, after every
     // MMA of the CTA.  Waiting on BAR_O's parity here would be ambiguous: when
@@ -492,8 +566,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcArgs a) {
   }
 }
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// Tensor map over a whole pool [L * Hkv * num_slots rows][D] of bf16, box of
+// 64 columns x BN rows, 128-byte swizzle (the shared-memory tile layout).
+bool make_pool_map(CUtensorMap* m, const void* pool, const rx_pool_desc* d, int BN) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(d->head_dim),
+                              cuuint64_t(d->num_layers) * d->num_kv_heads * d->num_slots};
+  const cuuint64_t strides[1] = {cuuint64_t(d->head_dim) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(BN)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int BN, bool DECODE>
-rx_status launch(const TcArgs& a, unsigned gx, unsigned gy, cudaStream_t s) {
+rx_status launch(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx, unsigned gy,
+                 cudaStream_t s) {
   constexpr int bytes = Layout<D, BN>::BYTES;
   static bool configured = false;
   if (!configured) {
@@ -501,7 +609,12 @@ rx_status launch(const TcArgs& a, unsigned gx, unsigned gy, cudaStream_t s) {
                          bytes);
     configured = true;
   }
-  attn_tc_kernel<D, BN, DECODE><<<dim3(gx, gy), kThreads, bytes, s>>>(a);
+  CUtensorMap tmk, tmv;
+  if (!make_pool_map(&tmk, pool->k_pool, pool, BN) || !make_pool_map(&tmv, pool->v_pool, pool, BN))
+    return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
+  a.tma_row_base = int64_t(layer) * pool->num_kv_heads * pool->num_slots;
+  a.tma_head_rows = pool->num_slots;
+  attn_tc_kernel<D, BN, DECODE><<<dim3(gx, gy), kThreads, bytes, s>>>(a, tmk, tmv);
   return rx_internal::launch_status(DECODE ? "shared decode attention (tcgen05)"
                                            : "extend attention (tcgen05)");
 }
@@ -509,6 +622,12 @@ rx_status launch(const TcArgs& a, unsigned gx, unsigned gy, cudaStream_t s) {
 }  // namespace
 
 namespace rx_internal {
+
+#ifdef RX_TC_TRACE
+void tc_trace_read(unsigned long long* out) {
+  cudaMemcpyFromSymbol(out, g_tc_trace, sizeof(g_tc_trace));
+}
+#endif
 
 int32_t tc_error_flags(bool clear) {
   int32_t v = 0;
@@ -543,7 +662,7 @@ rx_status decode_shared_tc(const rx_pool_desc* pool, int32_t layer, const void* 
   a.ws_o = ws_o;
   a.ws_lse = ws_lse;
   if (D != 128) return set_error(RX_ERR_INVALID, "tensor-core decode tiles need head_dim 128");
-  return launch<128, 128, true>(a, unsigned(n_work), pool->num_kv_heads, stream);
+  return launch<128, 128, true>(a, pool, layer, unsigned(n_work), pool->num_kv_heads, stream);
 }
 
 rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
@@ -573,8 +692,9 @@ rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const voi
   a.num_tiles = int(num_tiles);
   a.out = d_out;
   a.lse = d_lse;
-  if (D == 128) return launch<128, 128, false>(a, unsigned(num_tiles), pool->num_kv_heads, stream);
-  return launch<256, 64, false>(a, unsigned(num_tiles), pool->num_kv_heads, stream);
+  if (D == 128)
+    return launch<128, 128, false>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
+  return launch<256, 64, false>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
 }
 
 }  // namespace rx_internal

@@ -59,4 +59,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// (2^lo, 2^hi) rounded to bf16 and packed (lo in the low half), computed
+// as one packed SFU operation: the inputs are rounded to bf16 first.
+__device__ __forceinline__ uint32_t exp2_bf16x2(float lo, float hi) {
+  uint32_t x, y;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(x) : "f"(hi), "f"(lo));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Same from fp32 bit patterns already rounded at bit 16: the high halves are
+// packed with a byte permute (lo in the low half) and exponentiated as bf16x2.
+__device__ __forceinline__ uint32_t exp2_bf16x2_bits(uint32_t lo_bits, uint32_t hi_bits) {
+  const uint32_t x = __byte_perm(lo_bits, hi_bits, 0x7632);
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
 }  // namespace rxk

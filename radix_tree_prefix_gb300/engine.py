@@ -23,6 +23,7 @@ them.  Per wave of requests:
 * finish: ``rx_finish`` (insert prompt + outputs, unlock).
 """
 
+import ctypes
 import math
 
 import numpy as np
@@ -347,29 +348,44 @@ class Engine:
         need = max(int(i.workspace_bytes) for i in infos)
         if self.d_ws.numel() < need:
             self.d_ws = torch.empty(int(need * 1.25) + 256, dtype=torch.uint8, device=self.device)
-        ctx = ctx0.copy()
-        for t in range(T):
-            info = infos[t]
-            step_slots = d_slots[t * B:(t + 1) * B]
-            inputs = self.inputs.decode(self.step_no, wave, t)
-            nbytes = self.decode_bytes(info, B) if self.timing else 0.0
-            outs = {}
-            for layer in self.layers:
-                q, k, v = inputs[layer]
-                rx.kv_store(self.pool, layer, step_slots, k, v, self.stream)
-                out = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
-                                  device=self.device)
-                lse = torch.empty((B, wl.num_q_heads), dtype=torch.float32, device=self.device)
-                ev = self._event_start()
-                rx.decode_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_plans[t],
-                                    info, B, self.scale, out, lse, self.d_ws, self.stream)
-                self._event_end(ev, "decode", nbytes)
-                self.gpu_launches += 3
-                outs[layer] = (out, lse)
-            if self.on_decode is not None:
-                self.on_decode(self.step_no, t, [r.rid for r in wave], ctx + 1, outs, info)
-            ctx += 1
-            self.step_no += 1
+        # every step's inputs and outputs, then one native call per layer
+        inputs = [self.inputs.decode(self.step_no + t, wave, t) for t in range(T)]
+        outs = {}
+        for layer in self.layers:
+            o = torch.empty((T, B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
+                            device=self.device)
+            l = torch.empty((T, B, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            steps = (rx.rx_decode_step * T)()
+            for t in range(T):
+                q, k, v = inputs[t][layer]
+                st = steps[t]
+                st.d_q, st.d_k, st.d_v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+                st.d_slots = d_slots[t * B:(t + 1) * B].data_ptr()
+                st.d_plan = d_plans[t].data_ptr()
+                st.info = ctypes.addressof(infos[t])
+                st.d_out, st.d_lse = o[t].data_ptr(), l[t].data_ptr()
+            ev = self._event_start()
+            rx.decode_steps(self.pool, layer, wl.num_q_heads, self.d_table, steps, B, self.scale,
+                            self.d_ws, self.stream)
+            self._event_end(ev, "decode", sum(self.decode_bytes(i, B) for i in infos)
+                            if self.timing else 0.0)
+            self.gpu_launches += T * self._launches_per_decode(infos)
+            outs[layer] = (o, l)
+        if self.on_decode is not None:
+            ctx = ctx0.copy()
+            for t in range(T):
+                self.on_decode(self.step_no + t, t, [r.rid for r in wave], ctx + 1,
+                               {ly: (outs[ly][0][t], outs[ly][1][t]) for ly in self.layers},
+                               infos[t])
+                ctx += 1
+        self.step_no += T
+
+    def _launches_per_decode(self, infos):
+        """Kernels per decode step: kv_store, warp-pipelined decode (if any
+        small items), tensor-core tiles (if any large items), merge."""
+        i = infos[0]
+        small = int(i.n_work - i.n_work_tc) > 0
+        return 1 + int(small) + int(int(i.n_work_tc) > 0) + 1
 
     # ------------------------------------------------------------ timing
     def _event_start(self):

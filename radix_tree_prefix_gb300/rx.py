@@ -62,6 +62,12 @@ class rx_decode_plan_info(C.Structure):
         "n_shared_segments", "workspace_bytes", "distinct_kv_tokens", "n_work_tc")]
 
 
+class rx_decode_step(C.Structure):
+    _fields_ = [("d_q", C.c_void_p), ("d_k", C.c_void_p), ("d_v", C.c_void_p),
+                ("d_slots", C.c_void_p), ("d_plan", C.c_void_p), ("info", C.c_void_p),
+                ("d_out", C.c_void_p), ("d_lse", C.c_void_p)]
+
+
 class rx_pool_desc(C.Structure):
     _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("num_slots", C.c_int64),
                 ("num_layers", C.c_int32), ("num_kv_heads", C.c_int32),
@@ -95,6 +101,7 @@ _SIGS = {
     "rx_extend_attention": [P, I32, P, I32, P, I64, P, P, P, P, I32, I64, F32, P, P, P],
     "rx_decode_attention": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P, SZ, P],
     "rx_decode_attention_static": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P],
+    "rx_decode_steps": [P, I32, I32, P, I64, P, I32, I32, F32, P, SZ, P],
     "rx_device_check": [P],
 }
 for _name, _args in _SIGS.items():
@@ -337,6 +344,13 @@ def decode_attention(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_ou
                                     d_out.data_ptr(), d_lse.data_ptr(), d_workspace.data_ptr(),
                                     d_workspace.numel() * d_workspace.element_size(),
                                     _stream(stream)))
+
+
+def decode_steps(pool, layer, hq, d_table, steps, B, scale, d_workspace, stream=None):
+    """rx_decode_steps over a ctypes array of rx_decode_step."""
+    _check(_lib.rx_decode_steps(C.byref(pool), layer, hq, d_table.data_ptr(), d_table.shape[1],
+                                steps, len(steps), B, scale, d_workspace.data_ptr(),
+                                d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
 
 
 def decode_attention_static(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_out, d_lse,
