@@ -32,7 +32,11 @@
  *     error rx_last_error() returns a text for the calling thread.
  *   - The library owns the tree (opaque rx_cache).  The caller owns every host
  *     array and every device buffer (raw pointers, e.g. from torch tensors)
- *     and the CUDA stream.  The library never allocates device memory.
+ *     and the CUDA stream.  The library never allocates device memory; on its
+ *     first decode call on a device it creates one non-blocking side stream
+ *     and two events there, which rx_decode_attention uses to run its
+ *     independent kernels concurrently (forked from and joined back into the
+ *     caller's stream, so stream order is kept).
  *   - Host calls are synchronous and not thread-safe for one cache.  Device
  *     calls only enqueue work on the given stream (cudaStream_t passed as
  *     rx_stream_t; NULL is the legacy default stream) and return RX_ERR_CUDA
@@ -261,7 +265,11 @@ rx_status rx_batch_conflict(const int32_t* tokens, int64_t n,
  *   members[n_member_entries]: decode batch index of each member;
  *   req_part_indptr[B+1], req_parts[n_parts]: partial results of request b
  *       are entries req_parts[req_part_indptr[b] .. req_part_indptr[b+1]).
- * Partial entry p of work item w's member i is part_base(w) + i. */
+ * Partial entry p of work item w's member i is part_base(w) + i.  Word 7 of a
+ * work item is 0, or for a request's private tail the end of that tail at
+ * step 0 of a multi-step plan: at step t the item's keys end at
+ * min(kv_end, word7 + t) (an item left empty writes a zero partial with
+ * lse = -inf, which the merge weighs 0). */
 #define RX_WORK_WORDS 8
 typedef struct rx_decode_plan_info {
   int64_t plan_words;     /* int32 words used                             */
@@ -293,6 +301,27 @@ rx_status rx_plan_decode(const rx_cache* cache, int32_t B,
                          int32_t num_kv_heads, int32_t head_dim,
                          int32_t* plan, int64_t plan_cap,
                          rx_decode_plan_info* out_info);
+
+/* One plan for n_steps consecutive decode steps of the same batch: the tree
+ * does not change while the batch decodes (decode tokens stay outside it
+ * until finish), so the shared segments stay the same and only each private
+ * tail grows by one token per step.  ctx_len[b] is request b's context at
+ * the first step (its token included); at step t it is ctx_len[b] + t, and
+ * req_to_token rows must hold the slots of all n_steps tokens before the last
+ * step runs.  distinct_kv_tokens counts step 0.  The kernels take the step
+ * index through rx_decode_step.step. */
+rx_status rx_plan_decode_steps(const rx_cache* cache, int32_t B, int32_t n_steps,
+                               const rx_node* prompt_node, const int32_t* ctx_len,
+                               const int32_t* req_rows, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t* plan, int64_t plan_cap,
+                               rx_decode_plan_info* out_info);
+
+/* n_steps consecutive rx_alloc(k) calls (one decode slot per request and
+ * step), written to out_slots[t*k .. t*k+k).  RX_ERR_NO_SPACE at the first
+ * step that cannot be served (earlier steps stay allocated). */
+rx_status rx_alloc_steps(rx_cache* cache, int64_t k, int32_t n_steps,
+                         int32_t* out_slots);
 
 /* ------------------------------------------------------------------------
  * Device calls
@@ -390,6 +419,8 @@ typedef struct rx_decode_step {
   const rx_decode_plan_info* info; /* host info of that plan             */
   float* d_out;             /* fp32 [B][Hq][head_dim]                     */
   float* d_lse;             /* fp32 [B][Hq]                               */
+  int32_t step;             /* step index within a multi-step plan        */
+  int32_t reserved;
 } rx_decode_step;
 
 rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer,

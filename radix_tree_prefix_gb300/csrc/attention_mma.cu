@@ -70,6 +70,7 @@ struct TileArgs {
   const int32_t* members;
   float* ws_o;
   float* ws_lse;
+  int step;  // step index within a multi-step decode plan
 };
 
 // Shared-memory byte address of 16-byte chunk `chunk` of row `row` in a tile
@@ -98,7 +99,7 @@ __device__ __forceinline__ Tile describe_tile(const TileArgs& a) {
     const int32_t* w = a.work + int64_t(blockIdx.x) * RX_WORK_WORDS;
     t.trow = a.table + int64_t(w[0]) * a.row_stride;
     t.key_begin = w[1];
-    t.key_end = w[2];
+    t.key_end = w[7] > 0 ? min(w[2], w[7] + a.step) : w[2];  // growing private tail
     t.member_off = w[3];
     t.part_base = w[5];
     t.n_rows = w[6];
@@ -439,7 +440,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_pipe_kernel(const TileArgs 
   const int G = a.group;
   const int32_t* w = a.work + int64_t(item) * RX_WORK_WORDS;
   const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
-  const int kb = w[1], ke = w[2], member_off = w[3], part_base = w[5], n_rows = w[6];
+  const int kb = w[1], member_off = w[3], part_base = w[5], n_rows = w[6];
+  // a private tail of a multi-step plan ends at its step-0 end + step
+  const int ke = w[7] > 0 ? min(w[2], w[7] + a.step) : w[2];
   const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
   const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
   const uint32_t ring = rxk::smem_addr(dsm_pipe) + uint32_t(warp * S * STAGE);
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_pipe_kernel(const TileArgs 
     }
   }
 
-  const int n_steps = (ke - kb + 15) >> 4;
+  const int n_steps = ke > kb ? (ke - kb + 15) >> 4 : 0;
   // lane l < 16 holds the slot of key l of the next step to issue
   int next_slot = -1;
   auto fetch_slot = [&](int st) {
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_pipe_kernel(const TileArgs 
     const int head = kvh * G + (r - u * G);
     const int64_t part = int64_t(part_base) + u;
     float* dst = a.ws_o + (part * a.hq + head) * D;
-    const float inv = 1.f / l;
+    const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty chunk: zero partial, lse -inf
 #pragma unroll
     for (int h = 0; h < NH; ++h)
 #pragma unroll
@@ -623,7 +626,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_pipe_kernel(const TileArgs 
             make_float4(o[8 * h + 4][2 * e + e2] * inv, o[8 * h + 5][2 * e + e2] * inv,
                         o[8 * h + 6][2 * e + e2] * inv, o[8 * h + 7][2 * e + e2] * inv);
       }
-    if (c == 0) a.ws_lse[part * a.hq + head] = m_run[e] * kLn2 + logf(l);
+    if (c == 0) a.ws_lse[part * a.hq + head] = l > 0.f ? m_run[e] * kLn2 + logf(l) : -INFINITY;
   }
 }
 
@@ -685,13 +688,15 @@ extern "C" rx_status rx_extend_attention(const rx_pool_desc* pool, int32_t layer
                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
-                                         const void* d_q, int32_t num_q_heads,
-                                         const int32_t* d_req_to_token, int64_t row_stride,
-                                         const int32_t* d_plan, const rx_decode_plan_info* info,
-                                         int32_t B, float scale, float* d_out, float* d_lse,
-                                         void* d_workspace, size_t workspace_bytes,
-                                         rx_stream_t stream) {
+namespace {
+
+rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                                int32_t num_q_heads, const int32_t* d_req_to_token,
+                                int64_t row_stride, const int32_t* d_plan,
+                                const rx_decode_plan_info* info, int32_t B, float scale,
+                                float* d_out, float* d_lse, void* d_workspace,
+                                size_t workspace_bytes, cudaStream_t s, bool concurrent,
+                                int step) {
   rx_status st = rx_internal::check_pool(pool, layer);
   if (st != RX_OK) return st;
   if (!info || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0 || B < 0)
@@ -719,13 +724,27 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
   a.scale_log2 = scale * kLog2e;
   a.work = d_plan + info->off_work;
   a.members = d_plan + info->off_members;
+  a.step = step;
   const int64_t o_bytes = info->n_parts * num_q_heads * int64_t(D) * 4;
   a.ws_o = static_cast<float*>(d_workspace);
   a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + ((o_bytes + 255) / 256) * 256);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (info->n_work > 0) {
     const int64_t n_small = info->n_work - info->n_work_tc;
     if (D == 128) {
+      // The warp-pipelined items (private tails) and the tensor-core items
+      // (shared prefixes) are independent: with both present they run
+      // concurrently, the former on a side stream forked from and joined back
+      // into the caller's stream.
+      cudaStream_t side = s, small_stream = s;
+      cudaEvent_t fork = nullptr, join = nullptr;
+      const bool both = n_small > 0 && info->n_work_tc > 0;
+      if (both && concurrent && rx_internal::side_stream(&side, &fork, &join)) {
+        small_stream = side;
+        if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+          return rx_internal::launch_status("decode attention fork");
+      } else {
+        fork = join = nullptr;
+      }
       constexpr int kNW = 2, kS = 3;  // 48 KB per CTA: four CTAs per SM
       constexpr int bytes = kNW * kS * 2 * 16 * 128 * 2;
       static bool configured = false;
@@ -736,8 +755,8 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
       }
       const int64_t units = n_small * pool->num_kv_heads;
       if (units > 0) {
-        decode_pipe_kernel<kNW, kS><<<unsigned((units + kNW - 1) / kNW), kNW * 32, bytes, s>>>(
-            a, int(units));
+        decode_pipe_kernel<kNW, kS><<<unsigned((units + kNW - 1) / kNW), kNW * 32, bytes,
+                                      small_stream>>>(a, int(units));
         st = rx_internal::launch_status("decode attention");
         if (st != RX_OK) return st;
       }
@@ -747,6 +766,10 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
             d_plan + info->off_work + n_small * RX_WORK_WORDS, d_plan + info->off_members,
             info->n_work_tc, scale, a.ws_o, a.ws_lse, s);
         if (st != RX_OK) return st;
+      }
+      if (join) {
+        if (cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+          return rx_internal::launch_status("decode attention join");
       }
     } else {
       st = launch_tiles<256, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s);
@@ -765,6 +788,20 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
   return rx_internal::launch_status("decode merge");
 }
 
+}  // namespace
+
+extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
+                                         const void* d_q, int32_t num_q_heads,
+                                         const int32_t* d_req_to_token, int64_t row_stride,
+                                         const int32_t* d_plan, const rx_decode_plan_info* info,
+                                         int32_t B, float scale, float* d_out, float* d_lse,
+                                         void* d_workspace, size_t workspace_bytes,
+                                         rx_stream_t stream) {
+  return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
+                               info, B, scale, d_out, d_lse, d_workspace, workspace_bytes,
+                               reinterpret_cast<cudaStream_t>(stream), true, 0);
+}
+
 extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, int32_t num_q_heads,
                                      const int32_t* d_req_to_token, int64_t row_stride,
                                      const rx_decode_step* steps, int32_t n_steps, int32_t B,
@@ -776,9 +813,10 @@ extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, in
     const rx_decode_step& st = steps[i];
     rx_status r = rx_kv_store(pool, layer, st.d_slots, st.d_k, st.d_v, B, stream);
     if (r != RX_OK) return r;
-    r = rx_decode_attention(pool, layer, st.d_q, num_q_heads, d_req_to_token, row_stride, st.d_plan,
-                            st.info, B, scale, st.d_out, st.d_lse, d_workspace, workspace_bytes,
-                            stream);
+    r = decode_attention_impl(pool, layer, st.d_q, num_q_heads, d_req_to_token, row_stride,
+                              st.d_plan, st.info, B, scale, st.d_out, st.d_lse, d_workspace,
+                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true,
+                              st.step);
     if (r != RX_OK) return r;
   }
   return RX_OK;
@@ -840,7 +878,8 @@ extern "C" rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_
     }
     scratch = g_static_scratch_ptr[dev];
   }
-  return rx_decode_attention(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
-                             info, B, scale, d_out, d_lse, scratch,
-                             size_t(RX_DECODE_STATIC_SCRATCH_BYTES), stream);
+  return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
+                               info, B, scale, d_out, d_lse, scratch,
+                               size_t(RX_DECODE_STATIC_SCRATCH_BYTES),
+                               reinterpret_cast<cudaStream_t>(stream), false, 0);
 }

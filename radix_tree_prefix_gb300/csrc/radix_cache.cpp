@@ -568,13 +568,12 @@ rx_status rx_batch_conflict(const int32_t* tokens, int64_t n, int64_t match_len,
 // mean equal sets).  Segments are cut into key chunks and member blocks, one
 // CTA per (chunk, block, KV head); every (chunk, member) yields a partial
 // (o, lse) entry that the merge combines per request.
-extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
-                                    const rx_node* prompt_node,
-                                    const int32_t* ctx_len,
-                                    const int32_t* req_rows, int32_t num_q_heads,
-                                    int32_t num_kv_heads, int32_t head_dim,
-                                    int32_t* plan, int64_t plan_cap,
-                                    rx_decode_plan_info* info) {
+static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
+                                  const rx_node* prompt_node, const int32_t* ctx_len,
+                                  const int32_t* req_rows, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t* plan,
+                                  int64_t plan_cap, rx_decode_plan_info* info) {
+  if (n_steps < 1) return fail(RX_ERR_INVALID, "rx_plan_decode: n_steps < 1");
   if (!c || B < 0 || !info || (B && (!prompt_node || !ctx_len || !req_rows)))
     return fail(RX_ERR_INVALID, "rx_plan_decode: bad argument");
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -603,6 +602,7 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     int32_t row;
     int64_t kb, ke;
     std::vector<int32_t> members;
+    int64_t grow = 0;  // private tail: its end at step t is min(ke, grow + t)
   };
   std::vector<Seg> segs;
   std::unordered_map<const Node*, size_t> seg_of;
@@ -628,21 +628,24 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
         segs[it->second].members.push_back(b);
       }
     }
-    if (ctx_len[b] > pos) segs.push_back(Seg{req_rows[b], pos, int64_t(ctx_len[b]), {b}});
+    // private tail: covers the context of the last step; at step t it ends at
+    // ctx_len[b] + t
+    const int64_t last = int64_t(ctx_len[b]) + n_steps - 1;
+    if (last > pos) segs.push_back(Seg{req_rows[b], pos, last, {b}, int64_t(ctx_len[b])});
   }
   // work items: (key chunk, member block) of each segment.  head_dim 128:
   // segments with <= kDecodeSmallRows rows go to the warp-pipelined kernel
   // (listed first), larger ones to the tensor-core tile kernel in member blocks
   // of <= kDecodeTcRows rows (listed last); head_dim 256: 64-row items.
   struct Work {
-    int32_t row, kb, ke, member_off, n_members;
+    int32_t row, kb, ke, member_off, n_members, grow;
   };
   std::vector<Work> small, large;
   std::vector<int32_t> members;
   int64_t distinct = 0;
   for (const Seg& s : segs) {
     const int64_t n = s.ke - s.kb;
-    distinct += n;
+    distinct += s.grow ? std::max<int64_t>(0, s.grow - s.kb) : n;
     const int32_t k = int32_t(s.members.size());
     const int64_t rows = int64_t(k) * G;
     bool is_small;
@@ -651,7 +654,7 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     if (head_dim == 128 && rows <= rx_internal::kDecodeSmallRows) {
       is_small = true;
       per_block = k;
-      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 2 * rows);
+      chunk = std::max<int64_t>(rx_internal::kDecodeSmallChunk, 2 * rows);
       step = 16;
     } else if (head_dim == 128) {
       is_small = false;
@@ -672,7 +675,8 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     for (int64_t kb = s.kb; kb < s.ke; kb += len) {
       const int64_t ke = std::min(s.ke, kb + len);
       for (int32_t m0 = 0; m0 < k; m0 += per_block) {
-        Work w{s.row, int32_t(kb), int32_t(ke), moff + m0, std::min(per_block, k - m0)};
+        Work w{s.row, int32_t(kb), int32_t(ke), moff + m0, std::min(per_block, k - m0),
+               int32_t(s.grow)};
         (is_small ? small : large).push_back(w);
       }
     }
@@ -723,7 +727,7 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     o[4] = work[w].n_members;
     o[5] = int32_t(part);
     o[6] = work[w].n_members * G;
-    o[7] = 0;
+    o[7] = work[w].grow;
     part += work[w].n_members;
   }
   std::memcpy(plan + info->off_members, members.data(), members.size() * sizeof(int32_t));
@@ -734,6 +738,34 @@ extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B,
     std::memcpy(rp + indptr[b], parts_of[size_t(b)].data(),
                 parts_of[size_t(b)].size() * sizeof(int32_t));
     indptr[b + 1] = indptr[b] + int32_t(parts_of[size_t(b)].size());
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_plan_decode(const rx_cache* c, int32_t B, const rx_node* prompt_node,
+                                    const int32_t* ctx_len, const int32_t* req_rows,
+                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t* plan, int64_t plan_cap, rx_decode_plan_info* info) {
+  return plan_decode_impl(c, B, 1, prompt_node, ctx_len, req_rows, num_q_heads, num_kv_heads,
+                          head_dim, plan, plan_cap, info);
+}
+
+extern "C" rx_status rx_plan_decode_steps(const rx_cache* c, int32_t B, int32_t n_steps,
+                                          const rx_node* prompt_node, const int32_t* ctx_len,
+                                          const int32_t* req_rows, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t* plan,
+                                          int64_t plan_cap, rx_decode_plan_info* info) {
+  return plan_decode_impl(c, B, n_steps, prompt_node, ctx_len, req_rows, num_q_heads,
+                          num_kv_heads, head_dim, plan, plan_cap, info);
+}
+
+extern "C" rx_status rx_alloc_steps(rx_cache* c, int64_t k, int32_t n_steps, int32_t* out_slots) {
+  if (!c || k < 0 || n_steps < 0 || (!out_slots && k * n_steps))
+    return fail(RX_ERR_INVALID, "rx_alloc_steps: bad argument");
+  for (int32_t t = 0; t < n_steps; ++t) {
+    if (!c->alloc(k, out_slots + int64_t(t) * k))
+      return fail(RX_ERR_NO_SPACE, "rx_alloc_steps: step %d: %lld slots requested, %lld free after eviction",
+                  t, (long long)k, (long long)c->free_list.size());
   }
   return RX_OK;
 }

@@ -19,6 +19,9 @@ inline int decode_rows_per_item(int head_dim) { return head_dim == 128 ? kDecode
 // Decode: a segment chunk is at least this many keys (and at least 2 keys per
 // query row, so partial results stay small next to the KV they summarise).
 constexpr int kDecodeMinChunk = 512;
+// Decode: chunk of a <= 16-row item (one warp streams it, so shorter chunks
+// mean more warps in flight; the partial results stay small at <= 16 rows).
+constexpr int kDecodeSmallChunk = 128;
 // Decode chunks are cut at multiples of this many keys.
 constexpr int kDecodeKeyStep = 64;
 // Key tile of the attention kernels.
@@ -32,6 +35,9 @@ rx_status set_error(rx_status s, const char* msg);
 
 // Device-side helpers (kv_store.cu).
 rx_status check_pool(const rx_pool_desc* pool, int32_t layer);
+// A non-blocking side stream and two events of the current device, created
+// on first use, for running independent kernels of one call concurrently.
+bool side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join);
 rx_status launch_status(const char* what);
 int sm_count();
 // Error words of the kernels of each file: bit 0 = slot out of range.

@@ -43,13 +43,27 @@ class Trace:
         self.stats = {}
 
     def as_tuple(self):
+        steps = []
+        for rec in self.decode_steps:
+            steps.extend(rec.steps())
         return (
-            [[(rid, m, tuple(row)) for rid, m, row in b] for b in self.batches],
-            [list(s) for s in self.decode_steps],
+            [[(rid, m, tuple(int(x) for x in row)) for rid, m, row in b] for b in self.batches],
+            steps,
             list(self.finishes),
             self.prefilled,
             list(self.eviction_log),
         )
+
+
+class _DecodeRecord:
+    """Slots of every decode step of a wave, kept as arrays until compared."""
+
+    def __init__(self, rids, slots):
+        self.rids = rids
+        self.slots = slots
+
+    def steps(self):
+        return [[(int(r), int(x)) for r, x in zip(self.rids, row)] for row in self.slots]
 
 
 class GatherInputs:
@@ -312,40 +326,32 @@ class Engine:
             self.on_extend(self.batch_no, [r.rid for r in reqs], prefix.copy(), qo, outs)
 
     def _decode_phase(self, wave, ctx0, prompt_nodes):
-        """All decode steps of a wave.  Slot allocation and the decode plan of
-        every step depend only on the cache, not on kernel results, so the
-        host plans all steps first and uploads them with one copy; the GPU then
-        runs the steps back to back."""
+        """All decode steps of a wave.  Slot allocation and the decode plan
+        depend only on the cache, not on kernel results, and the tree does not
+        change while the wave decodes, so the host allocates every step's slots
+        (one call), builds one plan valid for every step, uploads both with one
+        copy, and the GPU then runs the steps back to back."""
         wl = self.wl
         B, T = len(wave), wl.decode_steps
         rows = np.arange(B, dtype=np.int32)
-        all_slots = np.empty((T, B), dtype=np.int32)
-        all_pos = np.empty((T, B), dtype=np.int32)
-        plans, infos = [], []
-        ctx = ctx0.copy()
-        for t in range(T):
-            slots = self.cache.alloc(B)
-            all_slots[t] = slots
-            all_pos[t] = ctx
-            self.h_table[rows, ctx] = slots
-            self.trace.decode_steps.append([(r.rid, int(s)) for r, s in zip(wave, slots)])
-            if self.device is not None:
-                self.plan_buf, info = self.cache.plan_decode(
-                    prompt_nodes, ctx + 1, rows, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                    self.plan_buf)
-                plans.append(self.plan_buf[:int(info.plan_words)].copy())
-                infos.append(info)
-            ctx += 1
+        all_slots = self.cache.alloc_steps(B, T)                    # [T, B]
+        all_pos = ctx0[None, :] + np.arange(T, dtype=np.int32)[:, None]
+        self.h_table[rows[None, :], all_pos] = all_slots
+        rids = np.array([r.rid for r in wave])
+        self.trace.decode_steps.append(_DecodeRecord(rids, all_slots))
         if self.device is None:
             self.step_no += T
             return
         torch = self.torch
-        views = self.staging.upload([np.tile(rows, T), all_pos.ravel(), all_slots.ravel()] + plans)
-        d_rows, d_pos, d_slots = views[0], views[1], views[2]
-        d_plans = views[3:]
+        self.plan_buf, info = self.cache.plan_decode(
+            prompt_nodes, ctx0 + 1, rows, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+            self.plan_buf, n_steps=T)
+        plan = self.plan_buf[:int(info.plan_words)]
+        d_rows, d_pos, d_slots, d_plan = self.staging.upload(
+            [np.tile(rows, T), all_pos.ravel().astype(np.int32), all_slots.ravel(), plan])
         rx.req_to_token_write(self.d_table, d_rows, d_pos, d_slots, self.stream)
         self.gpu_launches += 1
-        need = max(int(i.workspace_bytes) for i in infos)
+        need = int(info.workspace_bytes)
         if self.d_ws.numel() < need:
             self.d_ws = torch.empty(int(need * 1.25) + 256, dtype=torch.uint8, device=self.device)
         # every step's inputs and outputs, then one native call per layer
@@ -361,23 +367,22 @@ class Engine:
                 st = steps[t]
                 st.d_q, st.d_k, st.d_v = q.data_ptr(), k.data_ptr(), v.data_ptr()
                 st.d_slots = d_slots[t * B:(t + 1) * B].data_ptr()
-                st.d_plan = d_plans[t].data_ptr()
-                st.info = ctypes.addressof(infos[t])
+                st.d_plan = d_plan.data_ptr()
+                st.info = ctypes.addressof(info)
                 st.d_out, st.d_lse = o[t].data_ptr(), l[t].data_ptr()
+                st.step = t
             ev = self._event_start()
             rx.decode_steps(self.pool, layer, wl.num_q_heads, self.d_table, steps, B, self.scale,
                             self.d_ws, self.stream)
-            self._event_end(ev, "decode", sum(self.decode_bytes(i, B) for i in infos)
-                            if self.timing else 0.0)
-            self.gpu_launches += T * self._launches_per_decode(infos)
+            self._event_end(ev, "decode", sum(self.decode_bytes(info, B, t * B)
+                                              for t in range(T)) if self.timing else 0.0)
+            self.gpu_launches += T * self._launches_per_decode([info])
             outs[layer] = (o, l)
         if self.on_decode is not None:
-            ctx = ctx0.copy()
             for t in range(T):
-                self.on_decode(self.step_no + t, t, [r.rid for r in wave], ctx + 1,
+                self.on_decode(self.step_no + t, t, list(rids), ctx0 + 1 + t,
                                {ly: (outs[ly][0][t], outs[ly][1][t]) for ly in self.layers},
-                               infos[t])
-                ctx += 1
+                               info)
         self.step_no += T
 
     def _launches_per_decode(self, infos):
@@ -411,12 +416,13 @@ class Engine:
         pairs = int(np.sum(s * p + s * (s + 1) // 2))
         return 4.0 * self.wl.head_dim * self.wl.num_q_heads * pairs
 
-    def decode_bytes(self, info, B):
+    def decode_bytes(self, info, B, extra_tokens=0):
         """Algorithmic bytes of one decode launch: the distinct KV of the
         batch read once (K and V, bf16), its slot indices, Q (bf16) and the
-        fp32 output and lse."""
+        fp32 output and lse.  ``extra_tokens`` adds tokens beyond the plan's
+        step-0 count (later steps of a multi-step plan)."""
         wl = self.wl
-        kv = info.distinct_kv_tokens * (2 * wl.num_kv_heads * wl.head_dim * 2 + 4)
+        kv = (info.distinct_kv_tokens + extra_tokens) * (2 * wl.num_kv_heads * wl.head_dim * 2 + 4)
         q = B * wl.num_q_heads * wl.head_dim * 2
         o = B * wl.num_q_heads * (wl.head_dim + 1) * 4
         return float(kv + q + o)

@@ -65,7 +65,8 @@ class rx_decode_plan_info(C.Structure):
 class rx_decode_step(C.Structure):
     _fields_ = [("d_q", C.c_void_p), ("d_k", C.c_void_p), ("d_v", C.c_void_p),
                 ("d_slots", C.c_void_p), ("d_plan", C.c_void_p), ("info", C.c_void_p),
-                ("d_out", C.c_void_p), ("d_lse", C.c_void_p)]
+                ("d_out", C.c_void_p), ("d_lse", C.c_void_p), ("step", C.c_int32),
+                ("reserved", C.c_int32)]
 
 
 class rx_pool_desc(C.Structure):
@@ -95,6 +96,8 @@ _SIGS = {
     "rx_finish": [P, I32, P, P, P, I64, P, P, P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
+    "rx_plan_decode_steps": [P, I32, I32, P, P, P, I32, I32, I32, P, I64, P],
+    "rx_alloc_steps": [P, I64, I32, P],
     "rx_kv_store": [P, I32, P, P, P, I64, P],
     "rx_req_to_token_write": [P, I64, P, P, P, I64, P],
     "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
@@ -204,6 +207,12 @@ class RadixCache:
         _check(_lib.rx_alloc(self._h, int(k), _p(out)))
         return out[:k]
 
+    def alloc_steps(self, k, n_steps):
+        """n_steps consecutive alloc(k); returns int32 [n_steps, k]."""
+        out = np.empty((max(1, n_steps), max(1, k)), dtype=np.int32)
+        _check(_lib.rx_alloc_steps(self._h, int(k), int(n_steps), _p(out)))
+        return out[:n_steps, :k]
+
     def evict(self, k):
         f = C.c_int64()
         _check(_lib.rx_evict(self._h, int(k), C.byref(f)))
@@ -270,17 +279,24 @@ class RadixCache:
                               _p(already)))
         return already[:R]
 
-    def plan_decode(self, prompt_nodes, ctx_len, req_rows, hq, hkv, d, plan=None):
+    def plan_decode(self, prompt_nodes, ctx_len, req_rows, hq, hkv, d, plan=None, n_steps=None):
+        """rx_plan_decode, or rx_plan_decode_steps when n_steps is given."""
         B = len(prompt_nodes)
         info = rx_decode_plan_info()
         pn, cl, rr = _i64(prompt_nodes), _i32(ctx_len), _i32(req_rows)
-        cap = 0 if plan is None else len(plan)
-        st = _lib.rx_plan_decode(self._h, B, _p(pn), _p(cl), _p(rr), hq, hkv, d,
-                                 _p(plan) if plan is not None else None, cap, C.byref(info))
+
+        def call(buf):
+            cap = 0 if buf is None else len(buf)
+            ptr = _p(buf) if buf is not None else None
+            if n_steps is None:
+                return _lib.rx_plan_decode(self._h, B, _p(pn), _p(cl), _p(rr), hq, hkv, d, ptr,
+                                           cap, C.byref(info))
+            return _lib.rx_plan_decode_steps(self._h, B, int(n_steps), _p(pn), _p(cl), _p(rr),
+                                             hq, hkv, d, ptr, cap, C.byref(info))
+        st = call(plan)
         if st != RX_OK and (plan is None or len(plan) < info.plan_words) and info.plan_words > 0:
             plan = np.empty(int(info.plan_words) * 2, dtype=np.int32)
-            st = _lib.rx_plan_decode(self._h, B, _p(pn), _p(cl), _p(rr), hq, hkv, d, _p(plan),
-                                     len(plan), C.byref(info))
+            st = call(plan)
         _check(st)
         return plan, info
 

@@ -238,3 +238,38 @@ def test_identical_prompts_share_slots():
     assert got.as_tuple() == want.as_tuple()
     assert [[r for r, _, _ in b] for b in got.batches] == [[0], [1], [2, 3]]
     assert got.stats == want.stats
+
+
+def test_multi_step_plan_covers_each_step_once():
+    """A plan for T steps, clamped at step t, covers every context once."""
+    wl = workloads.agent_loop(calls=7, preamble=300, lo=50, hi=400, decode_steps=0)
+    c = rx.RadixCache(wl.num_slots + 1000)
+    nodes, ctx0 = [], []
+    for r in wl.waves[0]:
+        toks = wl.prompt_tokens(r)
+        slots, _ = c.match_prefix(toks)
+        new = c.alloc(len(toks) - len(slots))
+        _, node = c.insert(toks, np.concatenate([slots, new]))
+        c.lock(node)
+        nodes.append(node)
+        ctx0.append(len(toks) + 1)
+    T = 200
+    plan, info = c.plan_decode(nodes, ctx0, list(range(len(nodes))), 32, 8, 128, n_steps=T)
+    W = rx.RX_WORK_WORDS
+    work = plan[info.off_work:info.off_work + info.n_work * W].reshape(-1, W)
+    members = plan[info.off_members:info.off_members + info.n_member_entries]
+    for t in (0, 1, 77, T - 1):
+        covered = {b: [] for b in range(len(nodes))}
+        for row, kb, ke, moff, nm, pbase, nrows, grow in work:
+            end = min(ke, grow + t) if grow > 0 else ke
+            if end <= kb:
+                continue
+            for i in range(nm):
+                covered[int(members[moff + i])].append((int(kb), int(end)))
+        for b, rngs in covered.items():
+            rngs.sort()
+            pos = 0
+            for kb, ke in rngs:
+                assert kb == pos
+                pos = ke
+            assert pos == ctx0[b] + t
