@@ -282,6 +282,10 @@ typedef struct rx_decode_plan_info {
   int64_t distinct_kv_tokens;/* distinct context tokens of the batch      */
   int64_t n_work_tc;      /* the last n_work_tc items have more than 16 rows
                              and run on the tensor-core tile kernel       */
+  int64_t tails_private;  /* 1: at every step of the plan each request's
+                             newest token lies in a private tail run by the
+                             warp kernel (head_dim 128, group <= 16), so
+                             rx_decode_steps stores it inside that kernel */
 } rx_decode_plan_info;
 
 /* Plan one decode step for a batch of B requests.  prompt_node[b] is the
@@ -406,7 +410,11 @@ rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
  * values, so allocation and planning run ahead of the GPU).  For each step
  * s < n_steps, in order on the stream: rx_kv_store of that step's new tokens
  * (steps[s].d_k / d_v at steps[s].d_slots, B tokens), then
- * rx_decode_attention with steps[s]'s plan, queries and outputs.  The
+ * rx_decode_attention with steps[s]'s plan, queries and outputs.  When the
+ * plan's tails_private is 1 the store is not a launch of its own: the warp
+ * that reads the chunk holding request b's newest token (position
+ * ctx_len[b] + step - 1) first writes that token's K/V row to
+ * steps[s].d_slots[b], then reads the chunk; the result is the same.  The
  * req_to_token rows must already hold every step's slots (a token's position
  * beyond a step's context is never read by that step).  d_workspace must hold
  * the largest steps[s].info->workspace_bytes.  Stops at the first error. */

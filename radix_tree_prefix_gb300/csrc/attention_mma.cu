@@ -1,5 +1,8 @@
-// S6-S9: extend and decode attention over the radix KV pool, warp-level
-// tensor-core kernels (mma.sync m16n8k16 bf16, fp32 accumulate).
+// S6-S9: the C entry points of extend and decode attention over the radix KV
+// pool, the log-sum-exp merge of decode partials, and the head_dim 256 decode
+// tile kernel on warp-level tensor cores (mma.sync m16n8k16 bf16, fp32
+// accumulate).  Extend attention and head_dim 128 decode run on the tcgen05
+// kernels of attention_tc.cu.
 //
 // What is computed ("SGLang: Structured LLM Programs for Efficient
 // Inference", sections "A quick recap of how an LLM generates text" and "How
@@ -8,9 +11,9 @@
 // are read from the pool slots the radix cache handed out, exactly as if they
 // had just been computed.  Query head h reads KV head h / (Hq/Hkv).
 //
-// One CTA owns a tile of query rows that all read the same KV head over the
-// same key range, so every K/V tile staged in shared memory serves all of
-// them:
+// In the mma.sync tile kernel one CTA owns a tile of query rows that all read
+// the same KV head over the same key range, so every K/V tile staged in
+// shared memory serves all of them:
 //   extend: rows = (query token, head in group) of one request, token-major;
 //           causal limit per row = prefix + token + 1;
 //   decode: rows = (member request, head in group) of one plan work item: a
@@ -362,7 +365,10 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_tile_kernel(const TileArgs a)
 }
 
 // One warp per (request, query head): lse = log sum_s exp(lse_s),
-// o = sum_s exp(lse_s - lse) o_s over the request's partial entries.
+// o = sum_s exp(lse_s - lse) o_s over the request's partial entries.  Lane i
+// reads part i's lse (so every part's lse arrives in one round trip), the
+// warp reduces max and sum with shuffles, then the partial rows are summed
+// with independent loads in flight.
 template <int D>
 __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restrict__ indptr,
                                                         const int32_t* __restrict__ parts,
@@ -371,263 +377,58 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restric
                                                         int hq, int B, float* __restrict__ out,
                                                         float* __restrict__ lse_out) {
   constexpr int V = D / 128;  // float4 per lane
+  // launched after the decode kernels with programmatic stream serialization:
+  // let the next step's kernel start launching, then wait for the partials
+  rxk::griddep_launch_dependents();
+  rxk::griddep_wait();
   const int gw = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= B * hq) return;
   const int b = gw / hq;
   const int h = gw - b * hq;
-  const int p0 = indptr[b], p1 = indptr[b + 1];
+  const int p0 = indptr[b], n = indptr[b + 1] - p0;
   float m = -INFINITY;
-  for (int p = p0; p < p1; ++p) m = fmaxf(m, ws_lse[int64_t(parts[p]) * hq + h]);
+  for (int i = lane; i < n; i += 32) m = fmaxf(m, __ldcg(ws_lse + int64_t(parts[p0 + i]) * hq + h));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float4 acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   float sum = 0.f;
-  for (int p = p0; p < p1; ++p) {
-    const int64_t e = int64_t(parts[p]) * hq + h;
-    const float w = rxk::fast_exp2((ws_lse[e] - m) * kLog2e);
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    int64_t e = 0;
+    float w = 0.f;
+    if (i < n) {
+      e = int64_t(parts[p0 + i]) * hq + h;
+      const float li = __ldcg(ws_lse + e);
+      w = li == -INFINITY ? 0.f : rxk::fast_exp2((li - m) * kLog2e);
+    }
     sum += w;
-    const float4* src = reinterpret_cast<const float4*>(ws_o + e * D);
+    const int cnt = min(32, n - base);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const int64_t ej = __shfl_sync(0xffffffffu, e, j);
+      const float4* src = reinterpret_cast<const float4*>(ws_o + ej * D);
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const float4 x = src[v * 32 + lane];
-      acc[v].x += w * x.x;
-      acc[v].y += w * x.y;
-      acc[v].z += w * x.z;
-      acc[v].w += w * x.w;
+      for (int v = 0; v < V; ++v) {
+        const float4 x = __ldcg(src + v * 32 + lane);
+        acc[v].x += wj * x.x;
+        acc[v].y += wj * x.y;
+        acc[v].z += wj * x.z;
+        acc[v].w += wj * x.w;
+      }
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float inv = 1.f / sum;
   float4* dst = reinterpret_cast<float4*>(out + (int64_t(b) * hq + h) * D);
 #pragma unroll
   for (int v = 0; v < V; ++v)
     dst[v * 32 + lane] = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
   if (lane == 0) lse_out[int64_t(b) * hq + h] = m + logf(sum);
-}
-
-// ---------------------------------------------------------------------------
-// Decode over work items of <= 16 query rows (a request's private tail, or a
-// shared segment chunk with few rows), head_dim 128.  One warp owns one
-// (item, KV head) unit and streams its keys in steps of 16 through a private
-// S-stage cp.async ring in shared memory, so S-1 steps of K/V (8 KB each) are
-// in flight per warp while it computes; slot indices are fetched one step
-// ahead.  The head dimension is permuted consistently in Q and K (the dot
-// product does not care) and output columns are permuted on write-back, so
-// every fragment is one 16-byte shared-memory load:
-//   QK^T: thread (g = lane/4, c = lane%4) holds d in [32j+8c, 32j+8c+8) of K
-//         row 8nt+g and of Q rows g, g+8; k-steps 2j and 2j+1 use elements
-//         {0,1|2,3} and {4,5|6,7} of that piece;
-//   PV:   output column n of n-tile t is d = 64(t/8) + 8n + t%8, so thread
-//         (g, c) reads d in [64h+8g, 64h+8g+8) of V rows 2c, 2c+1, 8+2c, 9+2c.
-// Shared rows are 256 B; 16-byte chunk ch of row r sits at ch ^ ((r & 3) << 2).
-template <int NW, int S>
-__global__ void __launch_bounds__(NW * 32, 1) decode_pipe_kernel(const TileArgs a, int n_units) {
-  constexpr int D = 128;
-  constexpr int NJ = D / 32;
-  constexpr int NH = D / 64;
-  constexpr int NT = D / 8;
-  constexpr int ROWB = D * 2;                  // bytes per key row
-  constexpr int STAGE = 2 * 16 * ROWB;         // K and V of one 16-key step
-  extern __shared__ __align__(128) uint8_t dsm_pipe[];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int unit = blockIdx.x * NW + warp;
-  if (unit >= n_units) return;                 // no block-wide barriers below
-  const int n_heads_kv = a.hq / a.group;
-  const int item = unit / n_heads_kv;
-  const int kvh = unit - item * n_heads_kv;
-  const int g = lane >> 2, c = lane & 3;
-  const int G = a.group;
-  const int32_t* w = a.work + int64_t(item) * RX_WORK_WORDS;
-  const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
-  const int kb = w[1], member_off = w[3], part_base = w[5], n_rows = w[6];
-  // a private tail of a multi-step plan ends at its step-0 end + step
-  const int ke = w[7] > 0 ? min(w[2], w[7] + a.step) : w[2];
-  const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
-  const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
-  const uint32_t ring = rxk::smem_addr(dsm_pipe) + uint32_t(warp * S * STAGE);
-
-  uint4 qlo[NJ], qhi[NJ];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = g + 8 * e;
-    const bool ok = r < n_rows;
-    const bf16* qrow = a.q;
-    if (ok) {
-      const int u = r / G;
-      const int64_t b = a.members[member_off + u];
-      qrow = a.q + (b * a.hq + kvh * G + (r - u * G)) * D;
-    }
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (ok) v = __ldg(reinterpret_cast<const uint4*>(qrow + 32 * j + 8 * c));
-      if (e == 0) qlo[j] = v; else qhi[j] = v;
-    }
-  }
-
-  const int n_steps = ke > kb ? (ke - kb + 15) >> 4 : 0;
-  // lane l < 16 holds the slot of key l of the next step to issue
-  int next_slot = -1;
-  auto fetch_slot = [&](int st) {
-    const int key = kb + st * 16 + (lane & 15);
-    next_slot = (st < n_steps && key < ke) ? __ldg(trow + key) : -1;
-  };
-  auto issue = [&](int st) {
-    // 16 rows x 16 chunks for K and for V: lane covers chunk (lane & 15) of
-    // rows (lane >> 4) + 2i
-    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
-    const uint32_t vst = kst + 16 * ROWB;
-    const int ch = lane & 15;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = (lane >> 4) + 2 * i;
-      int64_t sl = __shfl_sync(0xffffffffu, next_slot, row);
-      const bool ok = sl >= 0;
-      if (sl >= a.num_slots) {
-        atomicOr(&g_attention_error, 1);
-        sl = 0;
-      }
-      if (!ok) sl = 0;
-      const uint32_t off = uint32_t(row * ROWB + ((ch ^ ((row & 3) << 2)) << 4));
-      rxk::cp_async_16(kst + off, kbase + sl * D + ch * 8, ok);
-      rxk::cp_async_16(vst + off, vbase + sl * D + ch * 8, ok);
-    }
-  };
-  fetch_slot(0);
-#pragma unroll
-  for (int p = 0; p < S - 1; ++p) {
-    if (p < n_steps) issue(p);
-    rxk::cp_async_commit();
-    fetch_slot(p + 1);
-  }
-
-  float o[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-
-  for (int st = 0; st < n_steps; ++st) {
-    rxk::cp_async_wait<S - 2>();
-    __syncwarp();
-    const int k0 = kb + st * 16;
-    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
-    const uint32_t vst = kst + 16 * ROWB;
-    float s[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-      const int row = 8 * i + g;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        uint4 kf;
-        const uint32_t addr = kst + uint32_t(row * ROWB + (((4 * j + c) ^ ((row & 3) << 2)) << 4));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(kf.x), "=r"(kf.y), "=r"(kf.z), "=r"(kf.w)
-                     : "r"(addr));
-        rxk::mma_bf16(s[i], qlo[j].x, qhi[j].x, qlo[j].y, qhi[j].y, kf.x, kf.y);
-        rxk::mma_bf16(s[i], qlo[j].z, qhi[j].z, qlo[j].w, qhi[j].w, kf.z, kf.w);
-      }
-    }
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = k0 + 8 * i + 2 * c + (e & 1);
-        const float v = key < ke ? s[i][e] * a.scale_log2 : -INFINITY;
-        s[i][e] = v;
-        mx[e >> 1] = fmaxf(mx[e >> 1], v);
-      }
-    float alpha[2], m_use[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
-      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
-      const float m_new = fmaxf(m_run[e], mx[e]);
-      m_use[e] = (m_new == -INFINITY) ? 0.f : m_new;
-      alpha[e] = rxk::fast_exp2(m_run[e] - m_use[e]);
-      m_run[e] = m_new;
-    }
-    float rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = rxk::fast_exp2(s[i][e] - m_use[e >> 1]);
-        s[i][e] = p;
-        rs[e >> 1] += p;
-      }
-    l_run[0] = l_run[0] * alpha[0] + rs[0];
-    l_run[1] = l_run[1] * alpha[1] + rs[1];
-    const uint32_t a0 = rxk::pack_bf16(s[0][0], s[0][1]);
-    const uint32_t a1 = rxk::pack_bf16(s[0][2], s[0][3]);
-    const uint32_t a2 = rxk::pack_bf16(s[1][0], s[1][1]);
-    const uint32_t a3 = rxk::pack_bf16(s[1][2], s[1][3]);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      o[t][0] *= alpha[0];
-      o[t][1] *= alpha[0];
-      o[t][2] *= alpha[1];
-      o[t][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      uint4 vf[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = 2 * c + (q & 1) + 8 * (q >> 1);
-        const uint32_t addr = vst + uint32_t(row * ROWB + (((8 * h + g) ^ ((row & 3) << 2)) << 4));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(vf[q].x), "=r"(vf[q].y), "=r"(vf[q].z), "=r"(vf[q].w)
-                     : "r"(addr));
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-        const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vf[0])[i >> 1];
-        const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vf[1])[i >> 1];
-        const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vf[2])[i >> 1];
-        const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vf[3])[i >> 1];
-        rxk::mma_bf16(o[8 * h + i], a0, a1, a2, a3, __byte_perm(w0, w1, sel),
-                      __byte_perm(w2, w3, sel));
-      }
-    }
-    __syncwarp();  // every lane is done with this stage before it is refilled
-    if (st + S - 1 < n_steps) issue(st + S - 1);
-    rxk::cp_async_commit();
-    fetch_slot(st + S);
-  }
-  rxk::cp_async_wait<0>();
-
-  // write the partial (o, lse) of rows g and g+8
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    float l = l_run[e];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const int r = g + 8 * e;
-    if (r >= n_rows) continue;
-    const int u = r / G;
-    const int head = kvh * G + (r - u * G);
-    const int64_t part = int64_t(part_base) + u;
-    float* dst = a.ws_o + (part * a.hq + head) * D;
-    const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty chunk: zero partial, lse -inf
-#pragma unroll
-    for (int h = 0; h < NH; ++h)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        float* d0 = dst + 64 * h + 8 * (2 * c + e2);
-        reinterpret_cast<float4*>(d0)[0] =
-            make_float4(o[8 * h + 0][2 * e + e2] * inv, o[8 * h + 1][2 * e + e2] * inv,
-                        o[8 * h + 2][2 * e + e2] * inv, o[8 * h + 3][2 * e + e2] * inv);
-        reinterpret_cast<float4*>(d0)[1] =
-            make_float4(o[8 * h + 4][2 * e + e2] * inv, o[8 * h + 5][2 * e + e2] * inv,
-                        o[8 * h + 6][2 * e + e2] * inv, o[8 * h + 7][2 * e + e2] * inv);
-      }
-    if (c == 0) a.ws_lse[part * a.hq + head] = l > 0.f ? m_run[e] * kLn2 + logf(l) : -INFINITY;
-  }
 }
 
 template <int D, int NW, bool DECODE>
@@ -695,8 +496,10 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
                                 int64_t row_stride, const int32_t* d_plan,
                                 const rx_decode_plan_info* info, int32_t B, float scale,
                                 float* d_out, float* d_lse, void* d_workspace,
-                                size_t workspace_bytes, cudaStream_t s, bool concurrent,
-                                int step) {
+                                size_t workspace_bytes, cudaStream_t s,
+                                int step, const void* k_new = nullptr,
+                                const void* v_new = nullptr,
+                                const int32_t* slots_new = nullptr) {
   rx_status st = rx_internal::check_pool(pool, layer);
   if (st != RX_OK) return st;
   if (!info || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0 || B < 0)
@@ -731,60 +534,38 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
   if (info->n_work > 0) {
     const int64_t n_small = info->n_work - info->n_work_tc;
     if (D == 128) {
-      // The warp-pipelined items (private tails) and the tensor-core items
-      // (shared prefixes) are independent: with both present they run
-      // concurrently, the former on a side stream forked from and joined back
-      // into the caller's stream.
-      cudaStream_t side = s, small_stream = s;
-      cudaEvent_t fork = nullptr, join = nullptr;
-      const bool both = n_small > 0 && info->n_work_tc > 0;
-      if (both && concurrent && rx_internal::side_stream(&side, &fork, &join)) {
-        small_stream = side;
-        if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
-          return rx_internal::launch_status("decode attention fork");
-      } else {
-        fork = join = nullptr;
-      }
-      constexpr int kNW = 2, kS = 3;  // 48 KB per CTA: four CTAs per SM
-      constexpr int bytes = kNW * kS * 2 * 16 * 128 * 2;
-      static bool configured = false;
-      if (!configured) {
-        cudaFuncSetAttribute(decode_pipe_kernel<kNW, kS>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        configured = true;
-      }
-      const int64_t units = n_small * pool->num_kv_heads;
-      if (units > 0) {
-        decode_pipe_kernel<kNW, kS><<<unsigned((units + kNW - 1) / kNW), kNW * 32, bytes,
-                                      small_stream>>>(a, int(units));
-        st = rx_internal::launch_status("decode attention");
-        if (st != RX_OK) return st;
-      }
-      if (info->n_work_tc > 0) {
-        st = rx_internal::decode_shared_tc(
-            pool, layer, d_q, num_q_heads, d_req_to_token, row_stride,
-            d_plan + info->off_work + n_small * RX_WORK_WORDS, d_plan + info->off_members,
-            info->n_work_tc, scale, a.ws_o, a.ws_lse, s);
-        if (st != RX_OK) return st;
-      }
-      if (join) {
-        if (cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
-          return rx_internal::launch_status("decode attention join");
-      }
+      st = rx_internal::decode_fused(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride,
+                                     a.work, n_small, a.work + n_small * RX_WORK_WORDS,
+                                     info->n_work_tc, a.members, scale, a.ws_o, a.ws_lse, step,
+                                     k_new, v_new, slots_new, s);
+      if (st != RX_OK) return st;
     } else {
       st = launch_tiles<256, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s);
       if (st != RX_OK) return st;
     }
   }
-  const unsigned blocks = unsigned((int64_t(B) * num_q_heads + 7) / 8);
+  // The merge may launch while the decode kernel before it still runs (it
+  // waits on the device for that kernel's results), so its launch latency is
+  // hidden.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned((int64_t(B) * num_q_heads + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int32_t* indptr = d_plan + info->off_req_part_indptr;
+  const int32_t* parts = d_plan + info->off_req_parts;
+  const float* wo = a.ws_o;
+  const float* wl = a.ws_lse;
   if (D == 128)
-    lse_merge_kernel<128><<<blocks, 256, 0, s>>>(d_plan + info->off_req_part_indptr,
-                                                 d_plan + info->off_req_parts, a.ws_o, a.ws_lse,
-                                                 num_q_heads, B, d_out, d_lse);
+    cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, indptr, parts, wo, wl, int(num_q_heads),
+                       int(B), d_out, d_lse);
   else
-    lse_merge_kernel<256><<<blocks, 256, 0, s>>>(d_plan + info->off_req_part_indptr,
-                                                 d_plan + info->off_req_parts, a.ws_o, a.ws_lse,
-                                                 num_q_heads, B, d_out, d_lse);
+    cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, indptr, parts, wo, wl, int(num_q_heads),
+                       int(B), d_out, d_lse);
   return rx_internal::launch_status("decode merge");
 }
 
@@ -799,7 +580,7 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
                                          rx_stream_t stream) {
   return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
                                info, B, scale, d_out, d_lse, d_workspace, workspace_bytes,
-                               reinterpret_cast<cudaStream_t>(stream), true, 0);
+                               reinterpret_cast<cudaStream_t>(stream), 0);
 }
 
 extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, int32_t num_q_heads,
@@ -809,14 +590,28 @@ extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, in
                                      rx_stream_t stream) {
   if (n_steps < 0 || (n_steps && !steps))
     return rx_internal::set_error(RX_ERR_INVALID, "rx_decode_steps: bad step list");
+  rx_status r = rx_internal::check_pool(pool, layer);
+  if (r != RX_OK) return r;
+  if (num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0)
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_decode_steps: Hq % Hkv != 0");
+  const int G = num_q_heads / pool->num_kv_heads;
   for (int32_t i = 0; i < n_steps; ++i) {
     const rx_decode_step& st = steps[i];
-    rx_status r = rx_kv_store(pool, layer, st.d_slots, st.d_k, st.d_v, B, stream);
-    if (r != RX_OK) return r;
+    // every step's new token is the end of a growing private tail: the warp
+    // kernel stores it itself
+    const bool fused = B > 0 && pool->head_dim == 128 && G <= rx_internal::kDecodeSmallRows &&
+                       st.info && st.info->tails_private == 1;
+    if (!fused) {
+      r = rx_kv_store(pool, layer, st.d_slots, st.d_k, st.d_v, B, stream);
+      if (r != RX_OK) return r;
+    } else if (!st.d_k || !st.d_v || !st.d_slots || (reinterpret_cast<uintptr_t>(st.d_k) & 15) ||
+               (reinterpret_cast<uintptr_t>(st.d_v) & 15)) {
+      return rx_internal::set_error(RX_ERR_INVALID, "rx_decode_steps: NULL or misaligned K/V");
+    }
     r = decode_attention_impl(pool, layer, st.d_q, num_q_heads, d_req_to_token, row_stride,
                               st.d_plan, st.info, B, scale, st.d_out, st.d_lse, d_workspace,
-                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true,
-                              st.step);
+                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream), st.step, fused ? st.d_k : nullptr, fused ? st.d_v : nullptr,
+                              fused ? st.d_slots : nullptr);
     if (r != RX_OK) return r;
   }
   return RX_OK;
@@ -881,5 +676,5 @@ extern "C" rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_
   return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
                                info, B, scale, d_out, d_lse, scratch,
                                size_t(RX_DECODE_STATIC_SCRATCH_BYTES),
-                               reinterpret_cast<cudaStream_t>(stream), false, 0);
+                               reinterpret_cast<cudaStream_t>(stream), 0);
 }

@@ -1,5 +1,7 @@
-// S6 (and the dense multi-query tiles of S7): attention of 128 query rows
-// over gathered pool KV on the 5th-generation tensor cores (tcgen05, TMEM).
+// S6-S8: extend attention and head_dim 128 decode attention.  The core is a
+// tile of 128 query rows over gathered pool KV on the 5th-generation tensor
+// cores (tcgen05, TMEM); decode adds a warp role for items of few rows, and
+// both run in one launch per decode step (decode_fused_kernel).
 //
 // What is computed ("SGLang: Structured LLM Programs for Efficient
 // Inference", sections "A quick recap of how an LLM generates text" and "How
@@ -14,7 +16,8 @@
 //           shared by the members; writes partial (o, lse) per row.
 // Warp roles (192 threads; at most two warps per SM sub-partition, so the
 // softmax warps may use up to 255 registers):
-//   warps 0-3  softmax: thread i owns query row i = TMEM lane i; reads S from
+//   warps 0-3  softmax: thread i owns query row i = TMEM lane i; gathers its
+//              Q row into shared memory first; then reads S from
 //              TMEM, keeps the running max / sum, writes P (bf16) to shared
 //              memory, rescales O in TMEM when the max grows by more than 2^8
 //              (rare after the first tile), and writes the output;
@@ -26,7 +29,7 @@
 //              allocator hands out runs, so this is the common case) is one TMA
 //              box load per 64 columns; any other tile, and the ragged last tile,
 //              is gathered slot by slot with 16-byte cp.async (rows past the key
-//              range are zero-filled).  Also loads the Q tile.
+//              range are zero-filled).
 // Every mbarrier wait is bounded (about 2 s); on a timeout the CTA sets an
 // error bit, drains its tensor-core work and frees TMEM before returning.
 
@@ -99,10 +102,18 @@ struct TcArgs {
   int64_t tma_row_base;  // row of (layer, KV head 0, slot 0) in the tensor maps
   int64_t tma_head_rows; // rows per KV head (num_slots)
   // decode
-  const int32_t* work;
+  const int32_t* work;     // tensor-core items
   const int32_t* members;
   float* ws_o;
   float* ws_lse;
+  // fused decode: warp-role items (<= 16 rows) and the step's new tokens
+  const int32_t* work_small;
+  int n_small_units;       // warp-role (item, KV head) units
+  int n_tc_ctas;           // tensor-core CTAs, listed first in the grid
+  int step;                // step index within a multi-step plan
+  const bf16* k_new;       // bf16 [B][Hkv][D] of the step's tokens, or NULL
+  const bf16* v_new;
+  const int32_t* slots_new;
 };
 
 struct TileDesc {
@@ -113,10 +124,10 @@ struct TileDesc {
 };
 
 template <bool DECODE>
-__device__ __forceinline__ TileDesc describe(const TcArgs& a) {
+__device__ __forceinline__ TileDesc describe(const TcArgs& a, int bx) {
   TileDesc t;
   if constexpr (DECODE) {
-    const int32_t* w = a.work + int64_t(blockIdx.x) * RX_WORK_WORDS;
+    const int32_t* w = a.work + int64_t(bx) * RX_WORK_WORDS;
     t.trow = a.table + int64_t(w[0]) * a.row_stride;
     t.key_begin = w[1];
     t.key_end = w[2];
@@ -126,7 +137,7 @@ __device__ __forceinline__ TileDesc describe(const TcArgs& a) {
     t.nomask_end = t.key_end;
     t.gr0 = t.q_base = t.prefix = 0;
   } else {
-    const int tile = a.num_tiles - 1 - int(blockIdx.x);  // heaviest first
+    const int tile = a.num_tiles - 1 - bx;  // heaviest first
     int lo = 0, hi = a.num_req;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -192,13 +203,13 @@ struct Layout {
   static constexpr int O_COL = 2 * BN;
 };
 
+// One 128-row tile (x = tile / work item, kvh = KV head) on 192 threads.
 template <int D, int BN, bool DECODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv) {
+__device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
+                                        const CUtensorMap* tmv, uint8_t* smem_raw, int bx,
+                                        int kvh) {
   using Lo = Layout<D, BN>;
   static_assert(2 * BN + D <= Lo::TMEM_COLS, "TMEM budget");
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the swizzled tiles
   const uint32_t raw = rxk::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -220,12 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int kvh = blockIdx.y;
-  const TileDesc t = describe<DECODE>(a);
+  const TileDesc t = describe<DECODE>(a, bx);
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
 
   if (tid == 0) {
-    tc::mbar_init(BAR_Q(), 1);
+    tc::mbar_init(BAR_Q(), 4 * 32);  // every softmax thread lands its Q row
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(BAR_KF(s), 1);
       tc::mbar_init(BAR_VF(s), 1);
@@ -250,26 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 5) {
     // ------------------------------------------------------------- loader
+    // keys written by earlier kernels on the stream are read from here on
+    rxk::griddep_wait();
     constexpr int CPR = D / 8;
     constexpr int SPL = BN / 32;  // slots per lane: rows lane + 32 i
-    for (int idx = lane; idx < BM * CPR; idx += 32) {
-      const int r = idx / CPR;
-      const int ch = idx - r * CPR;
-      const bool ok = r < t.n_rows;
-      const bf16* src = a.q;
-      if (ok) {
-        int64_t qi, part;
-        int head, lim;
-        row_info<DECODE>(a, t, kvh, r, qi, head, part, lim);
-        src = a.q + (qi * a.hq + head) * D + ch * 8;
-      }
-      rxk::cp_async_16(sw128(sQ, BM, r, ch), src, ok);
-    }
-    rxk::cp_async_commit();
-    rxk::cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(BAR_Q());
     const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
     const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
     const int64_t row0 = a.tma_row_base + int64_t(kvh) * a.tma_head_rows;
@@ -341,13 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(s), ((j - 2) >> 1) & 1, abort_flag,
                                                   kWaitLimit, kSleepNs)))
         break;
-      load_tile(&tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
+      load_tile(tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
       if (lane == 0) TC_TRACE(0, j);
       if (j >= 2 &&
           !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(s), ((j - 2) >> 1) & 1, abort_flag,
                                                   kWaitLimit, kSleepNs)))
         break;
-      load_tile(&tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
+      load_tile(tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
       if (lane == 0) TC_TRACE(2, j);
 #pragma unroll
       for (int i = 0; i < SPL; ++i) slot[i] = nxt[i];
@@ -418,6 +412,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     int head = 0, lim = t.key_end;
     const bool valid = i < t.n_rows;
     if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
+    // the queries and the outputs (decode: partial buffers the previous
+    // merge read) are touched only once earlier kernels on the stream are done
+    rxk::griddep_wait();
+    {
+      // thread i gathers Q row i (zeros past the tile's rows) while the
+      // loader warp already streams the first K/V tiles
+      constexpr int CPR = D / 8;
+      const bf16* src = a.q + (qi * a.hq + head) * D;
+#pragma unroll
+      for (int ch = 0; ch < CPR; ++ch) rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, valid);
+      rxk::cp_async_commit();
+      rxk::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(BAR_Q());
+    }
     const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
@@ -566,6 +575,290 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  tc_tile<D, BN, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
+}
+
+// ---------------------------------------------------------------------------
+// Decode over work items of <= 16 query rows (a request's private tail, or a
+// shared segment chunk with few rows), head_dim 128: the warp role of the
+// fused decode kernel below.  One warp owns one
+// (item, KV head) unit and streams its keys in steps of 16 through a private
+// S-stage cp.async ring in shared memory, so S-1 steps of K/V (8 KB each) are
+// in flight per warp while it computes; slot indices are fetched one step
+// ahead.  The head dimension is permuted consistently in Q and K (the dot
+// product does not care) and output columns are permuted on write-back, so
+// every fragment is one 16-byte shared-memory load:
+//   QK^T: thread (g = lane/4, c = lane%4) holds d in [32j+8c, 32j+8c+8) of K
+//         row 8nt+g and of Q rows g, g+8; k-steps 2j and 2j+1 use elements
+//         {0,1|2,3} and {4,5|6,7} of that piece;
+//   PV:   output column n of n-tile t is d = 64(t/8) + 8n + t%8, so thread
+//         (g, c) reads d in [64h+8g, 64h+8g+8) of V rows 2c, 2c+1, 8+2c, 9+2c.
+// Shared rows are 256 B; 16-byte chunk ch of row r sits at ch ^ ((r & 3) << 2).
+template <int NW, int S>
+__device__ __forceinline__ void pipe_units(const TcArgs& a, uint8_t* smem, int cta) {
+  constexpr int D = 128;
+  constexpr int NJ = D / 32;
+  constexpr int NH = D / 64;
+  constexpr int NT = D / 8;
+  constexpr int ROWB = D * 2;                  // bytes per key row
+  constexpr int STAGE = 2 * 16 * ROWB;         // K and V of one 16-key step
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int unit = cta * NW + warp;
+  if (unit >= a.n_small_units) return;        // no block-wide barriers below
+  const int n_heads_kv = a.hq / a.group;
+  const int item = unit / n_heads_kv;
+  const int kvh = unit - item * n_heads_kv;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = a.group;
+  const int32_t* w = a.work_small + int64_t(item) * RX_WORK_WORDS;
+  const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
+  const int kb = w[1], member_off = w[3], part_base = w[5], n_rows = w[6];
+  // a private tail of a multi-step plan ends at its step-0 end + step
+  const int ke = w[7] > 0 ? min(w[2], w[7] + a.step) : w[2];
+  const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
+  const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
+  const uint32_t ring = rxk::smem_addr(smem) + uint32_t(warp * S * STAGE);
+
+  // Earlier decode steps (the previous kernels on the stream) wrote keys this
+  // unit reads and read the partial buffers it writes.
+  rxk::griddep_wait();
+
+  // The unit whose chunk holds this step's newest token (the end of a growing
+  // private tail) stores that token's K/V row for its KV head first, so no
+  // separate store launch is needed; its own loads below then see the row.
+  if (a.k_new && w[7] > 0 && ke == w[7] + a.step && kb < ke) {
+    const int64_t b = a.members[member_off];
+    const int64_t sl = a.slots_new[b];
+    if (sl >= 1 && sl < a.num_slots) {
+      const int half = lane >> 4, ch = lane & 15;  // lanes 0-15: K, 16-31: V
+      const bf16* src = (half ? a.v_new : a.k_new) + (b * n_heads_kv + kvh) * D;
+      bf16* dst = const_cast<bf16*>(half ? vbase : kbase) + sl * D;
+      reinterpret_cast<uint4*>(dst)[ch] = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+    } else {
+      atomicOr(&g_tc_error, 1);
+    }
+    __threadfence();
+    __syncwarp();
+  }
+
+  uint4 qlo[NJ], qhi[NJ];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = g + 8 * e;
+    const bool ok = r < n_rows;
+    const bf16* qrow = a.q;
+    if (ok) {
+      const int u = r / G;
+      const int64_t b = a.members[member_off + u];
+      qrow = a.q + (b * a.hq + kvh * G + (r - u * G)) * D;
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ok) v = __ldg(reinterpret_cast<const uint4*>(qrow + 32 * j + 8 * c));
+      if (e == 0) qlo[j] = v; else qhi[j] = v;
+    }
+  }
+
+  const int n_steps = ke > kb ? (ke - kb + 15) >> 4 : 0;
+  // lane l < 16 holds the slot of key l of the next step to issue
+  int next_slot = -1;
+  auto fetch_slot = [&](int st) {
+    const int key = kb + st * 16 + (lane & 15);
+    next_slot = (st < n_steps && key < ke) ? __ldg(trow + key) : -1;
+  };
+  auto issue = [&](int st) {
+    // 16 rows x 16 chunks for K and for V: lane covers chunk (lane & 15) of
+    // rows (lane >> 4) + 2i
+    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
+    const uint32_t vst = kst + 16 * ROWB;
+    const int ch = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = (lane >> 4) + 2 * i;
+      int64_t sl = __shfl_sync(0xffffffffu, next_slot, row);
+      const bool ok = sl >= 0;
+      if (sl >= a.num_slots) {
+        atomicOr(&g_tc_error, 1);
+        sl = 0;
+      }
+      if (!ok) sl = 0;
+      const uint32_t off = uint32_t(row * ROWB + ((ch ^ ((row & 3) << 2)) << 4));
+      rxk::cp_async_16(kst + off, kbase + sl * D + ch * 8, ok);
+      rxk::cp_async_16(vst + off, vbase + sl * D + ch * 8, ok);
+    }
+  };
+  fetch_slot(0);
+#pragma unroll
+  for (int p = 0; p < S - 1; ++p) {
+    if (p < n_steps) issue(p);
+    rxk::cp_async_commit();
+    fetch_slot(p + 1);
+  }
+
+  float o[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+
+  for (int st = 0; st < n_steps; ++st) {
+    rxk::cp_async_wait<S - 2>();
+    __syncwarp();
+    const int k0 = kb + st * 16;
+    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
+    const uint32_t vst = kst + 16 * ROWB;
+    float s[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+      const int row = 8 * i + g;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        uint4 kf;
+        const uint32_t addr = kst + uint32_t(row * ROWB + (((4 * j + c) ^ ((row & 3) << 2)) << 4));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(kf.x), "=r"(kf.y), "=r"(kf.z), "=r"(kf.w)
+                     : "r"(addr));
+        rxk::mma_bf16(s[i], qlo[j].x, qhi[j].x, qlo[j].y, qhi[j].y, kf.x, kf.y);
+        rxk::mma_bf16(s[i], qlo[j].z, qhi[j].z, qlo[j].w, qhi[j].w, kf.z, kf.w);
+      }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = k0 + 8 * i + 2 * c + (e & 1);
+        const float v = key < ke ? s[i][e] * a.scale_log2 : -INFINITY;
+        s[i][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+    float alpha[2], m_use[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
+      const float m_new = fmaxf(m_run[e], mx[e]);
+      m_use[e] = (m_new == -INFINITY) ? 0.f : m_new;
+      alpha[e] = rxk::fast_exp2(m_run[e] - m_use[e]);
+      m_run[e] = m_new;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = rxk::fast_exp2(s[i][e] - m_use[e >> 1]);
+        s[i][e] = p;
+        rs[e >> 1] += p;
+      }
+    l_run[0] = l_run[0] * alpha[0] + rs[0];
+    l_run[1] = l_run[1] * alpha[1] + rs[1];
+    const uint32_t a0 = rxk::pack_bf16(s[0][0], s[0][1]);
+    const uint32_t a1 = rxk::pack_bf16(s[0][2], s[0][3]);
+    const uint32_t a2 = rxk::pack_bf16(s[1][0], s[1][1]);
+    const uint32_t a3 = rxk::pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      o[t][0] *= alpha[0];
+      o[t][1] *= alpha[0];
+      o[t][2] *= alpha[1];
+      o[t][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      uint4 vf[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = 2 * c + (q & 1) + 8 * (q >> 1);
+        const uint32_t addr = vst + uint32_t(row * ROWB + (((8 * h + g) ^ ((row & 3) << 2)) << 4));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(vf[q].x), "=r"(vf[q].y), "=r"(vf[q].z), "=r"(vf[q].w)
+                     : "r"(addr));
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+        const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vf[0])[i >> 1];
+        const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vf[1])[i >> 1];
+        const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vf[2])[i >> 1];
+        const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vf[3])[i >> 1];
+        rxk::mma_bf16(o[8 * h + i], a0, a1, a2, a3, __byte_perm(w0, w1, sel),
+                      __byte_perm(w2, w3, sel));
+      }
+    }
+    __syncwarp();  // every lane is done with this stage before it is refilled
+    if (st + S - 1 < n_steps) issue(st + S - 1);
+    rxk::cp_async_commit();
+    fetch_slot(st + S);
+  }
+  rxk::cp_async_wait<0>();
+
+  // write the partial (o, lse) of rows g and g+8
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float l = l_run[e];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const int r = g + 8 * e;
+    if (r >= n_rows) continue;
+    const int u = r / G;
+    const int head = kvh * G + (r - u * G);
+    const int64_t part = int64_t(part_base) + u;
+    float* dst = a.ws_o + (part * a.hq + head) * D;
+    const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty chunk: zero partial, lse -inf
+#pragma unroll
+    for (int h = 0; h < NH; ++h)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        float* d0 = dst + 64 * h + 8 * (2 * c + e2);
+        reinterpret_cast<float4*>(d0)[0] =
+            make_float4(o[8 * h + 0][2 * e + e2] * inv, o[8 * h + 1][2 * e + e2] * inv,
+                        o[8 * h + 2][2 * e + e2] * inv, o[8 * h + 3][2 * e + e2] * inv);
+        reinterpret_cast<float4*>(d0)[1] =
+            make_float4(o[8 * h + 4][2 * e + e2] * inv, o[8 * h + 5][2 * e + e2] * inv,
+                        o[8 * h + 6][2 * e + e2] * inv, o[8 * h + 7][2 * e + e2] * inv);
+      }
+    if (c == 0) a.ws_lse[part * a.hq + head] = l > 0.f ? m_run[e] * kLn2 + logf(l) : -INFINITY;
+  }
+}
+
+
+constexpr int kPipeWarps = kThreads / 32;  // warp-role units per CTA
+constexpr int kPipeStages = 4;             // 8 KB K/V steps per warp ring
+
+// One launch per decode step (head_dim 128).  CTAs [0, n_tc_ctas) run the
+// tensor-core tiles of segment chunks with more than 16 query rows (CTA c:
+// item c / Hkv, KV head c % Hkv); each later CTA runs six warp-role units.
+// Both kinds share the SMs in one grid instead of competing as two launches.
+// The kernel is launched with programmatic stream serialization: it lets the
+// merge that follows it launch early and waits (griddepcontrol.wait) for the
+// previous kernels on the stream before it touches what they wrote or read.
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_fused_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  rxk::griddep_launch_dependents();
+  const int cta = int(blockIdx.x);
+  if (cta < a.n_tc_ctas) {
+    const int hkv = a.hq / a.group;
+    tc_tile<128, 128, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
+  } else {
+    const uint32_t raw = rxk::smem_addr(smem_raw);
+    pipe_units<kPipeWarps, kPipeStages>(a, smem_raw + (((raw + 1023u) & ~1023u) - raw),
+                                        cta - a.n_tc_ctas);
+  }
+}
+static_assert(kPipeWarps * kPipeStages * 2 * 16 * 128 * 2 + 1024 <= Layout<128, 128>::BYTES,
+              "warp-role rings fit the tensor-core tile's shared memory");
+
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -599,24 +892,62 @@ bool make_pool_map(CUtensorMap* m, const void* pool, const rx_pool_desc* d, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BN, bool DECODE>
-rx_status launch(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx, unsigned gy,
-                 cudaStream_t s) {
+// Tensor maps of the pools last used on this thread (K and V of one pool
+// descriptor): encoding them is host work repeated on every launch otherwise.
+struct PoolMaps {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int64_t num_slots = 0;
+  int32_t layers = 0, heads = 0, dim = 0, box_rows = 0;
+  CUtensorMap mk, mv;
+};
+
+bool pool_maps(const rx_pool_desc* d, int BN, const CUtensorMap** mk, const CUtensorMap** mv) {
+  thread_local PoolMaps cache[4];
+  thread_local int next = 0;
+  for (PoolMaps& c : cache) {
+    if (c.k == d->k_pool && c.v == d->v_pool && c.num_slots == d->num_slots &&
+        c.layers == d->num_layers && c.heads == d->num_kv_heads && c.dim == d->head_dim &&
+        c.box_rows == BN) {
+      *mk = &c.mk;
+      *mv = &c.mv;
+      return true;
+    }
+  }
+  PoolMaps& c = cache[next];
+  next = (next + 1) & 3;
+  c.k = nullptr;
+  if (!make_pool_map(&c.mk, d->k_pool, d, BN) || !make_pool_map(&c.mv, d->v_pool, d, BN))
+    return false;
+  c.k = d->k_pool;
+  c.v = d->v_pool;
+  c.num_slots = d->num_slots;
+  c.layers = d->num_layers;
+  c.heads = d->num_kv_heads;
+  c.dim = d->head_dim;
+  c.box_rows = BN;
+  *mk = &c.mk;
+  *mv = &c.mv;
+  return true;
+}
+
+template <int D, int BN>
+rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx,
+                        unsigned gy, cudaStream_t s) {
   constexpr int bytes = Layout<D, BN>::BYTES;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(attn_tc_kernel<D, BN, DECODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(attn_tc_kernel<D, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          bytes);
     configured = true;
   }
-  CUtensorMap tmk, tmv;
-  if (!make_pool_map(&tmk, pool->k_pool, pool, BN) || !make_pool_map(&tmv, pool->v_pool, pool, BN))
+  const CUtensorMap *tmk, *tmv;
+  if (!pool_maps(pool, BN, &tmk, &tmv))
     return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   a.tma_row_base = int64_t(layer) * pool->num_kv_heads * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  attn_tc_kernel<D, BN, DECODE><<<dim3(gx, gy), kThreads, bytes, s>>>(a, tmk, tmv);
-  return rx_internal::launch_status(DECODE ? "shared decode attention (tcgen05)"
-                                           : "extend attention (tcgen05)");
+  attn_tc_kernel<D, BN><<<dim3(gx, gy), kThreads, bytes, s>>>(a, *tmk, *tmv);
+  return rx_internal::launch_status("extend attention (tcgen05)");
 }
 
 }  // namespace
@@ -639,15 +970,23 @@ int32_t tc_error_flags(bool clear) {
   return v;
 }
 
-rx_status decode_shared_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
-                           int32_t num_q_heads, const int32_t* d_req_to_token,
-                           int64_t row_stride, const int32_t* d_work, const int32_t* d_members,
-                           int64_t n_work, float scale, float* ws_o, float* ws_lse,
-                           cudaStream_t stream) {
+rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                       int32_t num_q_heads, const int32_t* d_req_to_token, int64_t row_stride,
+                       const int32_t* d_work_small, int64_t n_small, const int32_t* d_work_tc,
+                       int64_t n_tc, const int32_t* d_members, float scale, float* ws_o,
+                       float* ws_lse, int step, const void* k_new, const void* v_new,
+                       const int32_t* slots_new, cudaStream_t stream) {
   const int D = pool->head_dim;
+  if (D != 128) return set_error(RX_ERR_INVALID, "fused decode needs head_dim 128");
+  const int64_t hkv = pool->num_kv_heads;
+  const int64_t small_units = n_small * hkv;
+  const int64_t tc_ctas = n_tc * hkv;
+  const int64_t ctas = tc_ctas + (small_units + kPipeWarps - 1) / kPipeWarps;
+  if (ctas == 0) return RX_OK;
+  if (ctas > INT32_MAX) return set_error(RX_ERR_INVALID, "decode plan too large for one launch");
   TcArgs a{};
   a.q = static_cast<const bf16*>(d_q);
-  const int64_t layer_off = int64_t(layer) * pool->num_kv_heads * pool->num_slots * D;
+  const int64_t layer_off = int64_t(layer) * hkv * pool->num_slots * D;
   a.kpool = static_cast<const bf16*>(pool->k_pool) + layer_off;
   a.vpool = static_cast<const bf16*>(pool->v_pool) + layer_off;
   a.head_stride = pool->num_slots * D;
@@ -655,14 +994,42 @@ rx_status decode_shared_tc(const rx_pool_desc* pool, int32_t layer, const void* 
   a.table = d_req_to_token;
   a.row_stride = row_stride;
   a.hq = num_q_heads;
-  a.group = num_q_heads / pool->num_kv_heads;
+  a.group = num_q_heads / int(hkv);
   a.scale_log2 = scale * kLog2e;
-  a.work = d_work;
+  a.work = d_work_tc;
   a.members = d_members;
   a.ws_o = ws_o;
   a.ws_lse = ws_lse;
-  if (D != 128) return set_error(RX_ERR_INVALID, "tensor-core decode tiles need head_dim 128");
-  return launch<128, 128, true>(a, pool, layer, unsigned(n_work), pool->num_kv_heads, stream);
+  a.work_small = d_work_small;
+  a.n_small_units = int(small_units);
+  a.n_tc_ctas = int(tc_ctas);
+  a.step = step;
+  a.k_new = static_cast<const bf16*>(k_new);
+  a.v_new = static_cast<const bf16*>(v_new);
+  a.slots_new = slots_new;
+  a.tma_row_base = int64_t(layer) * hkv * pool->num_slots;
+  a.tma_head_rows = pool->num_slots;
+  constexpr int bytes = Layout<128, 128>::BYTES;
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    configured = true;
+  }
+  const CUtensorMap *tmk, *tmv;
+  if (!pool_maps(pool, 128, &tmk, &tmv))
+    return set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, *tmk, *tmv);
+  return launch_status("decode attention (fused)");
 }
 
 rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
@@ -693,8 +1060,9 @@ rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const voi
   a.out = d_out;
   a.lse = d_lse;
   if (D == 128)
-    return launch<128, 128, false>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
-  return launch<256, 64, false>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
+    return launch_extend<128, 128>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads,
+                                   stream);
+  return launch_extend<256, 64>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
 }
 
 }  // namespace rx_internal

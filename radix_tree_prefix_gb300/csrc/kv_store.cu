@@ -100,26 +100,6 @@ int32_t kv_store_error_flags(bool clear) {
   return v;
 }
 
-bool side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
-  constexpr int kMaxDev = 64;
-  static cudaStream_t streams[kMaxDev];
-  static cudaEvent_t forks[kMaxDev], joins[kMaxDev];
-  static bool ready[kMaxDev];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
-  if (!ready[dev]) {
-    if (cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&forks[dev], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&joins[dev], cudaEventDisableTiming) != cudaSuccess)
-      return false;
-    ready[dev] = true;
-  }
-  *side = streams[dev];
-  *fork = forks[dev];
-  *join = joins[dev];
-  return true;
-}
-
 int sm_count() {
   static int n = 0;
   if (n == 0) {

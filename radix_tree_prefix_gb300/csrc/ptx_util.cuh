@@ -77,4 +77,16 @@ __device__ __forceinline__ uint32_t exp2_bf16x2_bits(uint32_t lo_bits, uint32_t 
   return y;
 }
 
+// Programmatic dependent launch: wait until the kernels this grid depends on
+// (the previous ones on its stream) have completed and their writes are
+// visible; a no-op in a grid launched without that attribute.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+// Let the next kernel on the stream, if launched with programmatic stream
+// serialization, start launching before this grid completes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 }  // namespace rxk

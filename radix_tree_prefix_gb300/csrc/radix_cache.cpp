@@ -607,6 +607,9 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   std::vector<Seg> segs;
   std::unordered_map<const Node*, size_t> seg_of;
   int64_t n_shared = 0;
+  // every request's first-step token past its shared segments (the warp
+  // kernel then owns each step's newest token)
+  bool tails_private = head_dim == 128 && G <= rx_internal::kDecodeSmallRows;
   for (int32_t b = 0; b < B; ++b) {
     const auto& path = paths[b];
     int64_t pos = 0;
@@ -631,6 +634,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     // private tail: covers the context of the last step; at step t it ends at
     // ctx_len[b] + t
     const int64_t last = int64_t(ctx_len[b]) + n_steps - 1;
+    if (int64_t(ctx_len[b]) <= pos) tails_private = false;
     if (last > pos) segs.push_back(Seg{req_rows[b], pos, last, {b}, int64_t(ctx_len[b])});
   }
   // work items: (key chunk, member block) of each segment.  head_dim 128:
@@ -714,6 +718,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   int64_t l_bytes = n_parts * num_q_heads * 4;
   info->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
   info->distinct_kv_tokens = distinct;
+  info->tails_private = tails_private ? 1 : 0;
   if (!plan || plan_cap < info->plan_words)
     return fail(RX_ERR_INVALID, "rx_plan_decode: plan needs %lld words, capacity %lld",
                 (long long)info->plan_words, (long long)plan_cap);
@@ -760,7 +765,7 @@ extern "C" rx_status rx_plan_decode_steps(const rx_cache* c, int32_t B, int32_t 
 }
 
 extern "C" rx_status rx_alloc_steps(rx_cache* c, int64_t k, int32_t n_steps, int32_t* out_slots) {
-  if (!c || k < 0 || n_steps < 0 || (!out_slots && k * n_steps))
+  if (!c || k < 0 || n_steps < 0 || (!out_slots && k > 0 && n_steps > 0))
     return fail(RX_ERR_INVALID, "rx_alloc_steps: bad argument");
   for (int32_t t = 0; t < n_steps; ++t) {
     if (!c->alloc(k, out_slots + int64_t(t) * k))

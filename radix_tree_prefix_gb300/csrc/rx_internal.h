@@ -35,20 +35,23 @@ rx_status set_error(rx_status s, const char* msg);
 
 // Device-side helpers (kv_store.cu).
 rx_status check_pool(const rx_pool_desc* pool, int32_t layer);
-// A non-blocking side stream and two events of the current device, created
-// on first use, for running independent kernels of one call concurrently.
-bool side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join);
 rx_status launch_status(const char* what);
 int sm_count();
 // Error words of the kernels of each file: bit 0 = slot out of range.
 int32_t kv_store_error_flags(bool clear);
 int32_t attention_error_flags(bool clear);
 int32_t tc_error_flags(bool clear);
-rx_status decode_shared_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
-                           int32_t num_q_heads, const int32_t* d_req_to_token,
-                           int64_t row_stride, const int32_t* d_work, const int32_t* d_members,
-                           int64_t n_work, float scale, float* ws_o, float* ws_lse,
-                           cudaStream_t stream);
+// One decode step for head_dim 128 in a single launch: the tensor-core tiles
+// of the plan's large items and the warp-role units of its small items
+// (attention_tc.cu).  k_new / v_new / slots_new non-NULL: the warp owning a
+// request's newest token stores it first.  Launched with programmatic stream
+// serialization (the merge after it may launch early).
+rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
+                       int32_t num_q_heads, const int32_t* d_req_to_token, int64_t row_stride,
+                       const int32_t* d_work_small, int64_t n_small, const int32_t* d_work_tc,
+                       int64_t n_tc, const int32_t* d_members, float scale, float* ws_o,
+                       float* ws_lse, int step, const void* k_new, const void* v_new,
+                       const int32_t* slots_new, cudaStream_t stream);
 rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                               int32_t num_q_heads, const int32_t* d_req_to_token,
                               int64_t row_stride, const int32_t* d_req_rows,

@@ -386,11 +386,12 @@ class Engine:
         self.step_no += T
 
     def _launches_per_decode(self, infos):
-        """Kernels per decode step: kv_store, warp-pipelined decode (if any
-        small items), tensor-core tiles (if any large items), merge."""
+        """Kernels per decode step: kv_store (unless the decode kernel
+        stores the new tokens itself), the decode kernel (head_dim 128: one
+        fused launch for tensor-core and warp-role items), merge."""
         i = infos[0]
-        small = int(i.n_work - i.n_work_tc) > 0
-        return 1 + int(small) + int(int(i.n_work_tc) > 0) + 1
+        store = 0 if (int(i.tails_private) == 1 and self.wl.head_dim == 128) else 1
+        return store + int(int(i.n_work) > 0) + 1
 
     # ------------------------------------------------------------ timing
     def _event_start(self):

@@ -59,7 +59,7 @@ class rx_decode_plan_info(C.Structure):
     _fields_ = [(n, C.c_int64) for n in (
         "plan_words", "n_work", "n_parts", "n_member_entries", "off_work",
         "off_members", "off_req_part_indptr", "off_req_parts",
-        "n_shared_segments", "workspace_bytes", "distinct_kv_tokens", "n_work_tc")]
+        "n_shared_segments", "workspace_bytes", "distinct_kv_tokens", "n_work_tc", "tails_private")]
 
 
 class rx_decode_step(C.Structure):

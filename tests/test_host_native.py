@@ -273,3 +273,41 @@ def test_multi_step_plan_covers_each_step_once():
                 assert kb == pos
                 pos = ke
             assert pos == ctx0[b] + t
+    # the newest token of every step lies in exactly one growing private chunk
+    assert info.tails_private == 1
+    for t in (0, 1, T - 1):
+        owners = {b: 0 for b in range(len(nodes))}
+        for row, kb, ke, moff, nm, pbase, nrows, grow in work:
+            if grow > 0 and kb < grow + t <= ke:
+                assert nm == 1
+                owners[int(members[moff])] += 1
+        assert all(v == 1 for v in owners.values())
+
+
+def test_tails_private_flag():
+    """The in-kernel store of the newest token needs every request's newest
+    token in a private tail of the warp kernel; the plan says when it is."""
+    c = rx.RadixCache(4096)
+    toks = np.arange(1, 200, dtype=np.int32)
+    slots = c.alloc(len(toks))
+    _, node = c.insert(toks, slots)
+    c.lock(node)
+    other = np.concatenate([toks[:100], np.arange(500, 560, dtype=np.int32)])
+    s2 = c.alloc(60)
+    _, node2 = c.insert(other, np.concatenate([slots[:100], s2]))
+    c.lock(node2)
+    # contexts past the cached prompts: private tails hold the newest tokens
+    _, info = c.plan_decode([node, node2], [200, 161], [0, 1], 32, 8, 128, n_steps=4)
+    assert info.tails_private == 1
+    # head_dim 256 or a group above 16 rows: the store stays a launch of its own
+    _, info = c.plan_decode([node, node2], [200, 161], [0, 1], 32, 8, 256, n_steps=4)
+    assert info.tails_private == 0
+    _, info = c.plan_decode([node, node2], [200, 161], [0, 1], 32, 1, 128)
+    assert info.tails_private == 0
+    # a context that ends inside the shared segment (the caller passed the
+    # node of a token that is itself shared): no private tail at step 0
+    mid = c.match_prefix(toks[:100])[1]
+    c.lock(mid)
+    _, info = c.plan_decode([mid, node, node2], [100, 200, 161], [0, 1, 2], 32, 8, 128,
+                            n_steps=2)
+    assert info.tails_private == 0
