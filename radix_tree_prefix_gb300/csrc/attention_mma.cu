@@ -365,59 +365,89 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_tile_kernel(const TileArgs a)
 }
 
 // One warp per (request, query head): lse = log sum_s exp(lse_s),
-// o = sum_s exp(lse_s - lse) o_s over the request's partial entries.  Lane i
-// reads part i's lse (so every part's lse arrives in one round trip), the
-// warp reduces max and sum with shuffles, then the partial rows are summed
-// with independent loads in flight.
+// o = sum_s exp(lse_s - lse) o_s over the request's partial entries.  The
+// plan's part lists are read before the wait for the decode kernel; after it,
+// lane i reads part i's lse while the first eight parts' rows are already in
+// flight, so a request with up to eight parts costs one round trip to memory.
+// Partials are read through L2 (they were written by the previous kernel).
+// Block 0 also resets the decode kernel's work counter for the next step.
 template <int D>
 __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restrict__ indptr,
                                                         const int32_t* __restrict__ parts,
                                                         const float* __restrict__ ws_o,
                                                         const float* __restrict__ ws_lse,
                                                         int hq, int B, float* __restrict__ out,
-                                                        float* __restrict__ lse_out) {
+                                                        float* __restrict__ lse_out,
+                                                        int32_t* __restrict__ counter) {
   constexpr int V = D / 128;  // float4 per lane
-  // launched after the decode kernels with programmatic stream serialization:
+  constexpr int CH = 8;       // part rows loaded together
+  // launched after the decode kernel with programmatic stream serialization:
   // let the next step's kernel start launching, then wait for the partials
   rxk::griddep_launch_dependents();
-  rxk::griddep_wait();
   const int gw = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (gw >= B * hq) return;
-  const int b = gw / hq;
-  const int h = gw - b * hq;
-  const int p0 = indptr[b], n = indptr[b + 1] - p0;
-  float m = -INFINITY;
-  for (int i = lane; i < n; i += 32) m = fmaxf(m, __ldcg(ws_lse + int64_t(parts[p0 + i]) * hq + h));
+  const bool active = gw < B * hq;
+  const int b = active ? gw / hq : 0;
+  const int h = active ? gw - b * hq : 0;
+  const int p0 = active ? indptr[b] : 0;
+  const int n = active ? indptr[b + 1] - p0 : 0;
+  int64_t e = lane < n ? int64_t(parts[p0 + lane]) * hq + h : 0;
+  rxk::griddep_wait();
+  if (counter && blockIdx.x == 0 && threadIdx.x == 0) *counter = 0;
+  if (!active) return;
+  const float4* o4 = reinterpret_cast<const float4*>(ws_o);
+  float4 x[CH][V];
+#pragma unroll
+  for (int k = 0; k < CH; ++k) {
+    const int64_t ek = __shfl_sync(0xffffffffu, e, k);
+    if (k < n)
+#pragma unroll
+      for (int v = 0; v < V; ++v) x[k][v] = __ldcg(o4 + ek * (D / 4) + v * 32 + lane);
+  }
+  float li = lane < n ? __ldcg(ws_lse + e) : -INFINITY;
+  float m = li;
+  for (int i = lane + 32; i < n; i += 32)
+    m = fmaxf(m, __ldcg(ws_lse + int64_t(parts[p0 + i]) * hq + h));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float w = li == -INFINITY ? 0.f : rxk::fast_exp2((li - m) * kLog2e);
+  float sum = w;
   float4 acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float sum = 0.f;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    int64_t e = 0;
-    float w = 0.f;
-    if (i < n) {
-      e = int64_t(parts[p0 + i]) * hq + h;
-      const float li = __ldcg(ws_lse + e);
-      w = li == -INFINITY ? 0.f : rxk::fast_exp2((li - m) * kLog2e);
-    }
-    sum += w;
-    const int cnt = min(32, n - base);
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      const int64_t ej = __shfl_sync(0xffffffffu, e, j);
-      const float4* src = reinterpret_cast<const float4*>(ws_o + ej * D);
+#pragma unroll
+  for (int k = 0; k < CH; ++k) {
+    const float wk = __shfl_sync(0xffffffffu, w, k);
+    if (k < n)
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const float4 x = __ldcg(src + v * 32 + lane);
-        acc[v].x += wj * x.x;
-        acc[v].y += wj * x.y;
-        acc[v].z += wj * x.z;
-        acc[v].w += wj * x.w;
+        acc[v].x += wk * x[k][v].x;
+        acc[v].y += wk * x[k][v].y;
+        acc[v].z += wk * x[k][v].z;
+        acc[v].w += wk * x[k][v].w;
+      }
+  }
+  // parts beyond the first eight (long contexts split into many chunks)
+  for (int base = 0; base < n; base += 32) {
+    if (base > 0) {
+      const int i = base + lane;
+      e = i < n ? int64_t(parts[p0 + i]) * hq + h : 0;
+      const float lj = i < n ? __ldcg(ws_lse + e) : -INFINITY;
+      w = lj == -INFINITY ? 0.f : rxk::fast_exp2((lj - m) * kLog2e);
+      sum += w;
+    }
+    const int j0 = base == 0 ? CH : 0;
+    const int cnt = min(32, n - base);
+    for (int j = j0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const int64_t ej = __shfl_sync(0xffffffffu, e, j);
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const float4 y = __ldcg(o4 + ej * (D / 4) + v * 32 + lane);
+        acc[v].x += wj * y.x;
+        acc[v].y += wj * y.y;
+        acc[v].z += wj * y.z;
+        acc[v].w += wj * y.w;
       }
     }
   }
@@ -496,7 +526,7 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
                                 int64_t row_stride, const int32_t* d_plan,
                                 const rx_decode_plan_info* info, int32_t B, float scale,
                                 float* d_out, float* d_lse, void* d_workspace,
-                                size_t workspace_bytes, cudaStream_t s,
+                                size_t workspace_bytes, cudaStream_t s, bool first_call,
                                 int step, const void* k_new = nullptr,
                                 const void* v_new = nullptr,
                                 const int32_t* slots_new = nullptr) {
@@ -531,13 +561,20 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
   const int64_t o_bytes = info->n_parts * num_q_heads * int64_t(D) * 4;
   a.ws_o = static_cast<float*>(d_workspace);
   a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + ((o_bytes + 255) / 256) * 256);
+  const int64_t l_bytes = info->n_parts * num_q_heads * 4;
+  int32_t* counter = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(a.ws_lse) +
+                                                ((l_bytes + 255) / 256) * 256);
+  // the work counter of the decode kernel is 0 at every launch: zeroed here
+  // once per call, reset by each merge after that
+  if (D == 128 && first_call && cudaMemsetAsync(counter, 0, sizeof(int32_t), s) != cudaSuccess)
+    return rx_internal::launch_status("decode counter reset");
   if (info->n_work > 0) {
     const int64_t n_small = info->n_work - info->n_work_tc;
     if (D == 128) {
       st = rx_internal::decode_fused(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride,
                                      a.work, n_small, a.work + n_small * RX_WORK_WORDS,
-                                     info->n_work_tc, a.members, scale, a.ws_o, a.ws_lse, step,
-                                     k_new, v_new, slots_new, s);
+                                     info->n_work_tc, a.members, scale, a.ws_o, a.ws_lse,
+                                     counter, step, k_new, v_new, slots_new, s);
       if (st != RX_OK) return st;
     } else {
       st = launch_tiles<256, 4, true>(a, unsigned(info->n_work), pool->num_kv_heads, s);
@@ -562,10 +599,10 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
   const float* wl = a.ws_lse;
   if (D == 128)
     cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, indptr, parts, wo, wl, int(num_q_heads),
-                       int(B), d_out, d_lse);
+                       int(B), d_out, d_lse, counter);
   else
     cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, indptr, parts, wo, wl, int(num_q_heads),
-                       int(B), d_out, d_lse);
+                       int(B), d_out, d_lse, static_cast<int32_t*>(nullptr));
   return rx_internal::launch_status("decode merge");
 }
 
@@ -580,7 +617,7 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
                                          rx_stream_t stream) {
   return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
                                info, B, scale, d_out, d_lse, d_workspace, workspace_bytes,
-                               reinterpret_cast<cudaStream_t>(stream), 0);
+                               reinterpret_cast<cudaStream_t>(stream), true, 0);
 }
 
 extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, int32_t num_q_heads,
@@ -610,7 +647,8 @@ extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, in
     }
     r = decode_attention_impl(pool, layer, st.d_q, num_q_heads, d_req_to_token, row_stride,
                               st.d_plan, st.info, B, scale, st.d_out, st.d_lse, d_workspace,
-                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream), st.step, fused ? st.d_k : nullptr, fused ? st.d_v : nullptr,
+                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream), i == 0,
+                              st.step, fused ? st.d_k : nullptr, fused ? st.d_v : nullptr,
                               fused ? st.d_slots : nullptr);
     if (r != RX_OK) return r;
   }
@@ -676,5 +714,5 @@ extern "C" rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_
   return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
                                info, B, scale, d_out, d_lse, scratch,
                                size_t(RX_DECODE_STATIC_SCRATCH_BYTES),
-                               reinterpret_cast<cudaStream_t>(stream), 0);
+                               reinterpret_cast<cudaStream_t>(stream), true, 0);
 }

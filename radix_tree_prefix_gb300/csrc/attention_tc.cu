@@ -39,6 +39,8 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <algorithm>
+
 #include "ptx_util.cuh"
 #include "rx.h"
 #include "rx_internal.h"
@@ -110,6 +112,7 @@ struct TcArgs {
   const int32_t* work_small;
   int n_small_units;       // warp-role (item, KV head) units
   int n_tc_ctas;           // tensor-core CTAs, listed first in the grid
+  int* unit_counter;       // next warp-role unit to take (0 at launch)
   int step;                // step index within a multi-step plan
   const bf16* k_new;       // bf16 [B][Hkv][D] of the step's tokens, or NULL
   const bf16* v_new;
@@ -584,37 +587,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Decode over work items of <= 16 query rows (a request's private tail, or a
-// shared segment chunk with few rows), head_dim 128: the warp role of the
-// fused decode kernel below.  One warp owns one
-// (item, KV head) unit and streams its keys in steps of 16 through a private
-// S-stage cp.async ring in shared memory, so S-1 steps of K/V (8 KB each) are
-// in flight per warp while it computes; slot indices are fetched one step
-// ahead.  The head dimension is permuted consistently in Q and K (the dot
-// product does not care) and output columns are permuted on write-back, so
-// every fragment is one 16-byte shared-memory load:
-//   QK^T: thread (g = lane/4, c = lane%4) holds d in [32j+8c, 32j+8c+8) of K
-//         row 8nt+g and of Q rows g, g+8; k-steps 2j and 2j+1 use elements
-//         {0,1|2,3} and {4,5|6,7} of that piece;
-//   PV:   output column n of n-tile t is d = 64(t/8) + 8n + t%8, so thread
-//         (g, c) reads d in [64h+8g, 64h+8g+8) of V rows 2c, 2c+1, 8+2c, 9+2c.
-// Shared rows are 256 B; 16-byte chunk ch of row r sits at ch ^ ((r & 3) << 2).
-template <int NW, int S>
-__device__ __forceinline__ void pipe_units(const TcArgs& a, uint8_t* smem, int cta) {
+// Warp role of the fused decode kernel: work items of <= 16 query rows (a
+// request's private tail, or a shared segment chunk with few rows), head_dim
+// 128.  One warp owns one (item, KV head) unit and streams its keys in steps
+// of 16.  With few query rows per item the products are computed transposed,
+// keys in the M dimension of mma.sync m16n8k16 and query rows in N (8 or 16
+// rows, NR n-tiles), so no MMA row is wasted on keys:
+//   S^T (16 keys x 8 rows)  = K (16 x 128, ldmatrix)      . Q^T (registers)
+//   O^T (128 d x 8 rows)   += V^T (16 d x 16 keys per m-tile, ldmatrix.trans)
+//                             . P^T (the S^T accumulators, bf16, moved into
+//                               operand layout with four shuffles)
+// A thread of the S^T accumulators holds keys g, g+8 of rows 2c, 2c+1 (g =
+// lane/4, c = lane%4): the running max and sum of a row live in the 8 lanes
+// that share c.  K and V rows of a step are gathered by slot with 16-byte
+// cp.async into a ring of kPipeStages stages (kPipeStages - 1 steps in
+// flight) whose rows are padded to 272 B, so ldmatrix reads all 32 banks.
+// The max is rescaled lazily: O and the sum are rescaled only when a row's
+// max grows by more than 2^8.
+constexpr int kPipeWarps = kThreads / 32;        // warps of a CTA in the warp role
+constexpr int kPipeStages = 4;                   // ring stages per warp
+constexpr int kRowPitch = 272;                   // shared bytes per K/V row
+constexpr int kStageBytes = 32 * kRowPitch;      // 16 K rows, then 16 V rows
+constexpr int kSlotBuf = 128;                    // key slots staged per refill (x 16 B aligned)
+constexpr int kWarpBytes = kPipeStages * kStageBytes + kSlotBuf * 4;
+
+template <int NR>
+__device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_t* slot_buf,
+                                          int unit, uint32_t& gstep) {
   constexpr int D = 128;
-  constexpr int NJ = D / 32;
-  constexpr int NH = D / 64;
-  constexpr int NT = D / 8;
-  constexpr int ROWB = D * 2;                  // bytes per key row
-  constexpr int STAGE = 2 * 16 * ROWB;         // K and V of one 16-key step
-  const int warp = threadIdx.x >> 5;
+  constexpr int S = kPipeStages;
   const int lane = threadIdx.x & 31;
-  const int unit = cta * NW + warp;
-  if (unit >= a.n_small_units) return;        // no block-wide barriers below
+  const int g = lane >> 2, c = lane & 3;
   const int n_heads_kv = a.hq / a.group;
   const int item = unit / n_heads_kv;
   const int kvh = unit - item * n_heads_kv;
-  const int g = lane >> 2, c = lane & 3;
   const int G = a.group;
   const int32_t* w = a.work_small + int64_t(item) * RX_WORK_WORDS;
   const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
@@ -623,15 +629,10 @@ __device__ __forceinline__ void pipe_units(const TcArgs& a, uint8_t* smem, int c
   const int ke = w[7] > 0 ? min(w[2], w[7] + a.step) : w[2];
   const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
   const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
-  const uint32_t ring = rxk::smem_addr(smem) + uint32_t(warp * S * STAGE);
-
-  // Earlier decode steps (the previous kernels on the stream) wrote keys this
-  // unit reads and read the partial buffers it writes.
-  rxk::griddep_wait();
 
   // The unit whose chunk holds this step's newest token (the end of a growing
   // private tail) stores that token's K/V row for its KV head first, so no
-  // separate store launch is needed; its own loads below then see the row.
+  // separate store launch is needed; the bulk copies below then see the row.
   if (a.k_new && w[7] > 0 && ke == w[7] + a.step && kb < ke) {
     const int64_t b = a.members[member_off];
     const int64_t sl = a.slots_new[b];
@@ -647,200 +648,217 @@ __device__ __forceinline__ void pipe_units(const TcArgs& a, uint8_t* smem, int c
     __syncwarp();
   }
 
-  uint4 qlo[NJ], qhi[NJ];
+  // Q^T operand: n-tile nt, k-step kk: (d 16kk + 2c, +1 | 16kk + 2c + 8, +9) of row nt*8 + g
+  uint32_t qb[NR][8][2];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = g + 8 * e;
+  for (int nt = 0; nt < NR; ++nt) {
+    const int r = nt * 8 + g;
     const bool ok = r < n_rows;
-    const bf16* qrow = a.q;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q);
     if (ok) {
       const int u = r / G;
       const int64_t b = a.members[member_off + u];
-      qrow = a.q + (b * a.hq + kvh * G + (r - u * G)) * D;
+      qrow = reinterpret_cast<const uint32_t*>(a.q + (b * a.hq + kvh * G + (r - u * G)) * D);
     }
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (ok) v = __ldg(reinterpret_cast<const uint4*>(qrow + 32 * j + 8 * c));
-      if (e == 0) qlo[j] = v; else qhi[j] = v;
+    for (int kk = 0; kk < 8; ++kk) {
+      qb[nt][kk][0] = ok ? __ldg(qrow + 8 * kk + c) : 0u;
+      qb[nt][kk][1] = ok ? __ldg(qrow + 8 * kk + c + 4) : 0u;
     }
   }
 
   const int n_steps = ke > kb ? (ke - kb + 15) >> 4 : 0;
-  // lane l < 16 holds the slot of key l of the next step to issue
-  int next_slot = -1;
-  auto fetch_slot = [&](int st) {
-    const int key = kb + st * 16 + (lane & 15);
-    next_slot = (st < n_steps && key < ke) ? __ldg(trow + key) : -1;
-  };
-  auto issue = [&](int st) {
-    // 16 rows x 16 chunks for K and for V: lane covers chunk (lane & 15) of
-    // rows (lane >> 4) + 2i
-    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
-    const uint32_t vst = kst + 16 * ROWB;
-    const int ch = lane & 15;
+  int slot_base = 0;  // key offset (from kb) of slot_buf[0]
+  // slots of keys [kb + base, kb + base + kSlotBuf): -1 past the key range, a
+  // slot outside the pool is flagged and read as slot 0
+  auto fill_slots = [&](int base) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = (lane >> 4) + 2 * i;
-      int64_t sl = __shfl_sync(0xffffffffu, next_slot, row);
-      const bool ok = sl >= 0;
-      if (sl >= a.num_slots) {
+    for (int i = 0; i < kSlotBuf / 32; ++i) {
+      const int key = kb + base + lane + 32 * i;
+      int32_t sl = key < ke ? __ldg(trow + key) : -1;
+      if (key < ke && (sl < 0 || sl >= a.num_slots)) {
         atomicOr(&g_tc_error, 1);
         sl = 0;
       }
-      if (!ok) sl = 0;
-      const uint32_t off = uint32_t(row * ROWB + ((ch ^ ((row & 3) << 2)) << 4));
-      rxk::cp_async_16(kst + off, kbase + sl * D + ch * 8, ok);
-      rxk::cp_async_16(vst + off, vbase + sl * D + ch * 8, ok);
+      slot_buf[lane + 32 * i] = sl;
+    }
+    __syncwarp();
+  };
+  if (n_steps > 0) fill_slots(0);
+  // step st of this unit: 16 K rows and 16 V rows of 256 B, gathered by slot
+  // with 16-byte cp.async (lane: chunk lane % 16 of rows 8 (lane / 16) + i);
+  // rows past the key range are zero-filled (P is 0 there, and 0 * V must be 0)
+  const int r0 = (lane >> 4) * 8;
+  const char* ksrc = reinterpret_cast<const char*>(kbase) + (lane & 15) * 16;
+  const int64_t v_minus_k = reinterpret_cast<const char*>(vbase) - reinterpret_cast<const char*>(kbase);
+  auto issue = [&](int st) {
+    if (st * 16 >= slot_base + kSlotBuf) {
+      slot_base = st * 16;
+      fill_slots(slot_base);
+    }
+    const uint32_t dst = ring + ((gstep + uint32_t(st)) % S) * kStageBytes +
+                         uint32_t(r0 * kRowPitch + (lane & 15) * 16);
+    const int4* sp = reinterpret_cast<const int4*>(slot_buf + (st * 16 - slot_base + r0));
+    const int4 s0 = sp[0], s1 = sp[1];
+    const int32_t sl[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool ok = sl[i] >= 0;
+      const char* src = ksrc + int64_t(ok ? sl[i] : 0) * (D * 2);
+      rxk::cp_async_16(dst + uint32_t(i * kRowPitch), src, ok);
+      rxk::cp_async_16(dst + uint32_t((16 + i) * kRowPitch), src + v_minus_k, ok);
     }
   };
-  fetch_slot(0);
+
+  float o[NR][8][4];
 #pragma unroll
+  for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+  float m_ref[NR][2], l_run[NR][2];
+#pragma unroll
+  for (int nt = 0; nt < NR; ++nt) {
+    m_ref[nt][0] = m_ref[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+  }
+
+#pragma unroll 1
   for (int p = 0; p < S - 1; ++p) {
     if (p < n_steps) issue(p);
     rxk::cp_async_commit();
-    fetch_slot(p + 1);
   }
 
-  float o[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+  // ldmatrix lane addresses: K (A of S^T, keys x d) and V^T (A of O^T, d x keys)
+  const uint32_t k_lane = uint32_t(((lane & 7) + ((lane >> 3) & 1) * 8) * kRowPitch + (lane >> 4) * 16);
+  const uint32_t v_lane =
+      uint32_t((16 + (lane & 7) + (lane >> 4) * 8) * kRowPitch + ((lane >> 3) & 1) * 16);
 
+#pragma unroll 1
   for (int st = 0; st < n_steps; ++st) {
     rxk::cp_async_wait<S - 2>();
     __syncwarp();
-    const int k0 = kb + st * 16;
-    const uint32_t kst = ring + uint32_t((st % S) * STAGE);
-    const uint32_t vst = kst + 16 * ROWB;
-    float s[2][4];
+    const uint32_t stage = ring + ((gstep + uint32_t(st)) % S) * kStageBytes;
+    // S^T = K . Q^T, even and odd k-steps in two accumulator chains
+    float sacc[NR][4], sodd[NR][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-      const int row = 8 * i + g;
+    for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        uint4 kf;
-        const uint32_t addr = kst + uint32_t(row * ROWB + (((4 * j + c) ^ ((row & 3) << 2)) << 4));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(kf.x), "=r"(kf.y), "=r"(kf.z), "=r"(kf.w)
-                     : "r"(addr));
-        rxk::mma_bf16(s[i], qlo[j].x, qhi[j].x, qlo[j].y, qhi[j].y, kf.x, kf.y);
-        rxk::mma_bf16(s[i], qlo[j].z, qhi[j].z, qlo[j].w, qhi[j].w, kf.z, kf.w);
-      }
-    }
-    float mx[2] = {-INFINITY, -INFINITY};
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      rxk::ldsm_x4(stage + k_lane + uint32_t(kk * 32), a0, a1, a2, a3);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = k0 + 8 * i + 2 * c + (e & 1);
-        const float v = key < ke ? s[i][e] * a.scale_log2 : -INFINITY;
-        s[i][e] = v;
-        mx[e >> 1] = fmaxf(mx[e >> 1], v);
-      }
-    float alpha[2], m_use[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
-      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
-      const float m_new = fmaxf(m_run[e], mx[e]);
-      m_use[e] = (m_new == -INFINITY) ? 0.f : m_new;
-      alpha[e] = rxk::fast_exp2(m_run[e] - m_use[e]);
-      m_run[e] = m_new;
-    }
-    float rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = rxk::fast_exp2(s[i][e] - m_use[e >> 1]);
-        s[i][e] = p;
-        rs[e >> 1] += p;
-      }
-    l_run[0] = l_run[0] * alpha[0] + rs[0];
-    l_run[1] = l_run[1] * alpha[1] + rs[1];
-    const uint32_t a0 = rxk::pack_bf16(s[0][0], s[0][1]);
-    const uint32_t a1 = rxk::pack_bf16(s[0][2], s[0][3]);
-    const uint32_t a2 = rxk::pack_bf16(s[1][0], s[1][1]);
-    const uint32_t a3 = rxk::pack_bf16(s[1][2], s[1][3]);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      o[t][0] *= alpha[0];
-      o[t][1] *= alpha[0];
-      o[t][2] *= alpha[1];
-      o[t][3] *= alpha[1];
+      for (int nt = 0; nt < NR; ++nt)
+        rxk::mma_bf16((kk & 1) ? sodd[nt] : sacc[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
     }
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      uint4 vf[4];
+    for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = 2 * c + (q & 1) + 8 * (q >> 1);
-        const uint32_t addr = vst + uint32_t(row * ROWB + (((8 * h + g) ^ ((row & 3) << 2)) << 4));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(vf[q].x), "=r"(vf[q].y), "=r"(vf[q].z), "=r"(vf[q].w)
-                     : "r"(addr));
-      }
+      for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
+    // online softmax over the keys of this step (rows 2c, 2c+1 of each n-tile)
+    const int key0 = kb + st * 16 + g;
+    const bool in0 = key0 < ke, in1 = key0 + 8 < ke;
+    uint32_t pk[NR][2];  // (key g | key g+8) of rows 2c, 2c+1 as bf16x2
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-        const uint32_t w0 = reinterpret_cast<const uint32_t*>(&vf[0])[i >> 1];
-        const uint32_t w1 = reinterpret_cast<const uint32_t*>(&vf[1])[i >> 1];
-        const uint32_t w2 = reinterpret_cast<const uint32_t*>(&vf[2])[i >> 1];
-        const uint32_t w3 = reinterpret_cast<const uint32_t*>(&vf[3])[i >> 1];
-        rxk::mma_bf16(o[8 * h + i], a0, a1, a2, a3, __byte_perm(w0, w1, sel),
-                      __byte_perm(w2, w3, sel));
+    for (int nt = 0; nt < NR; ++nt) {
+      float x[4];
+      x[0] = in0 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
+      x[1] = in0 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
+      x[2] = in1 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
+      x[3] = in1 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = fmaxf(x[e], x[2 + e]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const bool need = mx > m_ref[nt][e] + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? rxk::fast_exp2(m_ref[nt][e] - mx) : 1.f;
+          if (need) m_ref[nt][e] = mx;
+          l_run[nt][e] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[nt][mt][e] *= alpha;
+            o[nt][mt][2 + e] *= alpha;
+          }
+        }
+        const float m_use = m_ref[nt][e] == -INFINITY ? 0.f : m_ref[nt][e];
+        uint32_t h;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n"
+            : "=r"(h)
+            : "f"(rxk::fast_exp2(x[2 + e] - m_use)), "f"(rxk::fast_exp2(x[e] - m_use)));
+        pk[nt][e] = h;  // low half: key g, high half: key g+8
+        l_run[nt][e] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
       }
+    }
+    // P^T operand for n-tile nt: b0 = (P[key 2c][row g], P[key 2c+1][row g]),
+    // b1 = keys 2c+8, 2c+9; key k of row r sits in lane 4k + r/2, half r%2
+    uint32_t pb[NR][2];
+    const int src1 = 8 * c + (g >> 1), src2 = src1 + 4;
+#pragma unroll
+    for (int nt = 0; nt < NR; ++nt) {
+      const uint32_t v0 = __shfl_sync(0xffffffffu, pk[nt][0], src1);
+      const uint32_t v1 = __shfl_sync(0xffffffffu, pk[nt][1], src1);
+      const uint32_t w0 = __shfl_sync(0xffffffffu, pk[nt][0], src2);
+      const uint32_t w1 = __shfl_sync(0xffffffffu, pk[nt][1], src2);
+      const uint32_t s1 = (g & 1) ? v1 : v0;
+      const uint32_t s2 = (g & 1) ? w1 : w0;
+      pb[nt][0] = __byte_perm(s1, s2, 0x5410);
+      pb[nt][1] = __byte_perm(s1, s2, 0x7632);
+    }
+    // O^T += V^T . P^T
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      rxk::ldsm_x4_t(stage + v_lane + uint32_t(mt * 32), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NR; ++nt) rxk::mma_bf16(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
     if (st + S - 1 < n_steps) issue(st + S - 1);
     rxk::cp_async_commit();
-    fetch_slot(st + S);
   }
   rxk::cp_async_wait<0>();
+  __syncwarp();
+  gstep += uint32_t(n_steps);
 
-  // write the partial (o, lse) of rows g and g+8
+  // write the partial (o, lse) of rows nt*8 + 2c + e
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    float l = l_run[e];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const int r = g + 8 * e;
-    if (r >= n_rows) continue;
-    const int u = r / G;
-    const int head = kvh * G + (r - u * G);
-    const int64_t part = int64_t(part_base) + u;
-    float* dst = a.ws_o + (part * a.hq + head) * D;
-    const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty chunk: zero partial, lse -inf
+  for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
-    for (int h = 0; h < NH; ++h)
+    for (int e = 0; e < 2; ++e) {
+      float l = l_run[nt][e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int r = nt * 8 + 2 * c + e;
+      if (r >= n_rows) continue;
+      const int uu = r / G;
+      const int head = kvh * G + (r - uu * G);
+      const int64_t part = int64_t(part_base) + uu;
+      float* dst = a.ws_o + (part * a.hq + head) * D;
+      const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty chunk: zero partial, lse -inf
 #pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        float* d0 = dst + 64 * h + 8 * (2 * c + e2);
-        reinterpret_cast<float4*>(d0)[0] =
-            make_float4(o[8 * h + 0][2 * e + e2] * inv, o[8 * h + 1][2 * e + e2] * inv,
-                        o[8 * h + 2][2 * e + e2] * inv, o[8 * h + 3][2 * e + e2] * inv);
-        reinterpret_cast<float4*>(d0)[1] =
-            make_float4(o[8 * h + 4][2 * e + e2] * inv, o[8 * h + 5][2 * e + e2] * inv,
-                        o[8 * h + 6][2 * e + e2] * inv, o[8 * h + 7][2 * e + e2] * inv);
+      for (int mt = 0; mt < 8; ++mt) {
+        dst[16 * mt + g] = o[nt][mt][e] * inv;
+        dst[16 * mt + g + 8] = o[nt][mt][2 + e] * inv;
       }
-    if (c == 0) a.ws_lse[part * a.hq + head] = l > 0.f ? m_run[e] * kLn2 + logf(l) : -INFINITY;
-  }
+      if (g == 0) a.ws_lse[part * a.hq + head] = l > 0.f ? m_ref[nt][e] * kLn2 + logf(l) : -INFINITY;
+    }
 }
 
-
-constexpr int kPipeWarps = kThreads / 32;  // warp-role units per CTA
-constexpr int kPipeStages = 4;             // 8 KB K/V steps per warp ring
-
-// One launch per decode step (head_dim 128).  CTAs [0, n_tc_ctas) run the
-// tensor-core tiles of segment chunks with more than 16 query rows (CTA c:
-// item c / Hkv, KV head c % Hkv); each later CTA runs six warp-role units.
-// Both kinds share the SMs in one grid instead of competing as two launches.
-// The kernel is launched with programmatic stream serialization: it lets the
-// merge that follows it launch early and waits (griddepcontrol.wait) for the
-// previous kernels on the stream before it touches what they wrote or read.
+// One launch per decode step (head_dim 128), at most one CTA per SM.  CTAs
+// [0, n_tc_ctas) first run the tensor-core tile of one segment chunk with
+// more than 16 query rows (CTA c: item c / Hkv, KV head c % Hkv).  Then every
+// warp of every CTA takes warp-role units (an item of <= 16 rows and one KV
+// head) from a shared counter, heaviest first, until none is left; so the
+// SMs of finished tiles join the warp-role work and no CTA waits for a second
+// wave.  The counter starts at 0 and the merge after this kernel resets it.
+// Launched with programmatic stream serialization: the merge that follows may
+// launch early, and this kernel waits (griddepcontrol.wait) for the previous
+// kernels on the stream before it touches what they wrote or read.
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
@@ -850,14 +868,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cta < a.n_tc_ctas) {
     const int hkv = a.hq / a.group;
     tc_tile<128, 128, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
-  } else {
-    const uint32_t raw = rxk::smem_addr(smem_raw);
-    pipe_units<kPipeWarps, kPipeStages>(a, smem_raw + (((raw + 1023u) & ~1023u) - raw),
-                                        cta - a.n_tc_ctas);
+  }
+  rxk::griddep_wait();
+  // warp role: this warp's ring, slot buffer and stage barriers
+  const uint32_t raw = rxk::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const int warp = int(threadIdx.x >> 5);
+  const int lane = int(threadIdx.x & 31);
+  const uint32_t ring = base + uint32_t(warp * kWarpBytes);
+  int32_t* slot_buf = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + warp * kWarpBytes +
+                                                 kPipeStages * kStageBytes);
+  const int hkv = a.hq / a.group;
+  uint32_t gstep = 0;
+  for (;;) {
+    int unit = 0;
+    if (lane == 0) unit = atomicAdd(a.unit_counter, 1);
+    unit = __shfl_sync(0xffffffffu, unit, 0);
+    if (unit >= a.n_small_units) break;
+    const int rows = a.work_small[int64_t(unit / hkv) * RX_WORK_WORDS + 6];
+    if (rows <= 8)
+      pipe_unit<1>(a, ring, slot_buf, unit, gstep);
+    else
+      pipe_unit<2>(a, ring, slot_buf, unit, gstep);
   }
 }
-static_assert(kPipeWarps * kPipeStages * 2 * 16 * 128 * 2 + 1024 <= Layout<128, 128>::BYTES,
+static_assert(kPipeWarps * kWarpBytes + 1024 <= Layout<128, 128>::BYTES,
               "warp-role rings fit the tensor-core tile's shared memory");
+static_assert(kRowPitch % 16 == 0 && kStageBytes % 16 == 0 && kWarpBytes % 16 == 0,
+              "cp.async destinations stay 16-byte aligned");
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -974,14 +1012,18 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                        int32_t num_q_heads, const int32_t* d_req_to_token, int64_t row_stride,
                        const int32_t* d_work_small, int64_t n_small, const int32_t* d_work_tc,
                        int64_t n_tc, const int32_t* d_members, float scale, float* ws_o,
-                       float* ws_lse, int step, const void* k_new, const void* v_new,
-                       const int32_t* slots_new, cudaStream_t stream) {
+                       float* ws_lse, int32_t* unit_counter, int step, const void* k_new,
+                       const void* v_new, const int32_t* slots_new, cudaStream_t stream) {
   const int D = pool->head_dim;
   if (D != 128) return set_error(RX_ERR_INVALID, "fused decode needs head_dim 128");
   const int64_t hkv = pool->num_kv_heads;
   const int64_t small_units = n_small * hkv;
   const int64_t tc_ctas = n_tc * hkv;
-  const int64_t ctas = tc_ctas + (small_units + kPipeWarps - 1) / kPipeWarps;
+  // one wave: the tiles plus enough CTAs for the warp-role units, at most one
+  // CTA per SM beyond the tiles
+  const int64_t ctas = std::max<int64_t>(
+      tc_ctas, std::min<int64_t>(tc_ctas + (small_units + kPipeWarps - 1) / kPipeWarps,
+                                 rx_internal::sm_count()));
   if (ctas == 0) return RX_OK;
   if (ctas > INT32_MAX) return set_error(RX_ERR_INVALID, "decode plan too large for one launch");
   TcArgs a{};
@@ -1003,6 +1045,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.work_small = d_work_small;
   a.n_small_units = int(small_units);
   a.n_tc_ctas = int(tc_ctas);
+  a.unit_counter = unit_counter;
   a.step = step;
   a.k_new = static_cast<const bf16*>(k_new);
   a.v_new = static_cast<const bf16*>(v_new);

@@ -716,7 +716,9 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   info->n_shared_segments = n_shared;
   int64_t o_bytes = n_parts * num_q_heads * int64_t(head_dim) * 4;
   int64_t l_bytes = n_parts * num_q_heads * 4;
-  info->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
+  // partial o, partial lse, and one 256-byte block for the decode kernel's
+  // work counter
+  info->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256 + 256;
   info->distinct_kv_tokens = distinct;
   info->tails_private = tails_private ? 1 : 0;
   if (!plan || plan_cap < info->plan_words)
