@@ -252,6 +252,17 @@ rx_status rx_batch_conflict(const int32_t* tokens, int64_t n,
                             const int64_t* member_indptr,
                             int32_t* out_conflict);
 
+/* The batch that starts at request `start` of a wave, under the same rule:
+ * requests start, start+1, ... join it while request j's prompt shares no
+ * more than m_j = rx_match_length(prompt_j minus its last token) tokens with
+ * every earlier member; *out_end = the first j that would share more (it
+ * starts the next batch), or R.  The cache is only read.  tokens/indptr hold
+ * the wave's R prompts concatenated.  Errors: RX_ERR_INVALID (start not in
+ * [0, R), an empty prompt). */
+rx_status rx_batch_end(const rx_cache* cache, const int32_t* tokens,
+                       const int64_t* indptr, int32_t start, int32_t R,
+                       int32_t* out_end);
+
 /* ------------------------------------------------------------------------
  * Decode plan (S7/S8 split; host)
  * ---------------------------------------------------------------------- */

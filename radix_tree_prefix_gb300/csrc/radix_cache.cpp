@@ -298,6 +298,16 @@ struct rx_cache {
 };
 
 // ---------------------------------------------------------------- C ABI
+// Whether two token sequences share more than `m` leading tokens: position m
+// is compared first (where prompts that match the tree to depth m usually
+// part), the m tokens before it only when that one agrees.
+static bool shares_more_than(const int32_t* a, int64_t na, const int32_t* b, int64_t nb,
+                             int64_t m) {
+  if (m < 0) return true;
+  if (na <= m || nb <= m || a[m] != b[m]) return false;
+  return common_prefix(a, b, m) == m;
+}
+
 extern "C" {
 
 size_t rx_last_error(char* buf, size_t cap) {
@@ -547,14 +557,31 @@ rx_status rx_batch_conflict(const int32_t* tokens, int64_t n, int64_t match_len,
       !out_conflict)
     return fail(RX_ERR_INVALID, "rx_batch_conflict: bad argument");
   *out_conflict = 0;
-  for (int32_t r = 0; r < R; ++r) {
-    const int32_t* m = member_tokens + member_indptr[r];
-    int64_t len = std::min<int64_t>(n, member_indptr[r + 1] - member_indptr[r]);
-    if (common_prefix(tokens, m, len) > match_len) {
+  for (int32_t r = 0; r < R; ++r)
+    if (shares_more_than(tokens, n, member_tokens + member_indptr[r],
+                         member_indptr[r + 1] - member_indptr[r], match_len)) {
       *out_conflict = 1;
       break;
     }
+  return RX_OK;
+}
+
+rx_status rx_batch_end(const rx_cache* c, const int32_t* tokens, const int64_t* indptr,
+                       int32_t start, int32_t R, int32_t* out_end) {
+  if (!c || !tokens || !indptr || start < 0 || start >= R || !out_end)
+    return fail(RX_ERR_INVALID, "rx_batch_end: bad argument");
+  for (int32_t j = start + 1; j < R; ++j) {
+    const int32_t* pj = tokens + indptr[j];
+    const int64_t nj = indptr[j + 1] - indptr[j];
+    if (nj < 1) return fail(RX_ERR_INVALID, "rx_batch_end: empty prompt %d", j);
+    const int64_t m = c->match_length(pj, nj - 1);
+    for (int32_t r = start; r < j; ++r)
+      if (shares_more_than(pj, nj, tokens + indptr[r], indptr[r + 1] - indptr[r], m)) {
+        *out_end = j;
+        return RX_OK;
+      }
   }
+  *out_end = R;
   return RX_OK;
 }
 

@@ -250,16 +250,13 @@ class Engine:
         tokens = np.concatenate(prompts).astype(np.int32)
         self.h_table[:len(wave)] = 0
         prompt_nodes = np.zeros(len(wave), dtype=np.int64)
+        # in-batch prefix rule: each batch runs to the first request that would
+        # share more with an earlier member than the tree gives it
         start = 0
-        for j in range(len(wave)):
-            if j > start:
-                m = self.cache.match_length(prompts[j][:-1])
-                seg = tokens[indptr[start]:indptr[j]]
-                sub = indptr[start:j + 1] - indptr[start]
-                if rx.batch_conflict(prompts[j], m, seg, sub):
-                    self._extend_batch(wave, start, j, tokens, indptr, prompt_nodes)
-                    start = j
-        self._extend_batch(wave, start, len(wave), tokens, indptr, prompt_nodes)
+        while start < len(wave):
+            end = self.cache.batch_end(tokens, indptr, start)
+            self._extend_batch(wave, start, end, tokens, indptr, prompt_nodes)
+            start = end
         if wl.decode_steps:
             self._decode_phase(wave, lens.astype(np.int32), prompt_nodes)
         # finish: insert prompt ++ outputs, unlock
@@ -357,20 +354,20 @@ class Engine:
         # every step's inputs and outputs, then one native call per layer
         inputs = [self.inputs.decode(self.step_no + t, wave, t) for t in range(T)]
         outs = {}
+        tt = np.arange(T, dtype=np.uint64)
         for layer in self.layers:
             o = torch.empty((T, B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
                             device=self.device)
             l = torch.empty((T, B, wl.num_q_heads), dtype=torch.float32, device=self.device)
-            steps = (rx.rx_decode_step * T)()
-            for t in range(T):
-                q, k, v = inputs[t][layer]
-                st = steps[t]
-                st.d_q, st.d_k, st.d_v = q.data_ptr(), k.data_ptr(), v.data_ptr()
-                st.d_slots = d_slots[t * B:(t + 1) * B].data_ptr()
-                st.d_plan = d_plan.data_ptr()
-                st.info = ctypes.addressof(info)
-                st.d_out, st.d_lse = o[t].data_ptr(), l[t].data_ptr()
-                st.step = t
+            steps = np.zeros(T, dtype=rx.DECODE_STEP_DTYPE)
+            for f, i in (("d_q", 0), ("d_k", 1), ("d_v", 2)):
+                steps[f] = [inputs[t][layer][i].data_ptr() for t in range(T)]
+            steps["d_slots"] = d_slots.data_ptr() + tt * np.uint64(4 * B)
+            steps["d_plan"] = d_plan.data_ptr()
+            steps["info"] = ctypes.addressof(info)
+            steps["d_out"] = o.data_ptr() + tt * np.uint64(o[0].numel() * 4)
+            steps["d_lse"] = l.data_ptr() + tt * np.uint64(l[0].numel() * 4)
+            steps["step"] = np.arange(T, dtype=np.int32)
             ev = self._event_start()
             rx.decode_steps(self.pool, layer, wl.num_q_heads, self.d_table, steps, B, self.scale,
                             self.d_ws, self.stream)

@@ -69,6 +69,14 @@ class rx_decode_step(C.Structure):
                 ("reserved", C.c_int32)]
 
 
+# the same layout as a numpy record, for filling many steps with array ops
+DECODE_STEP_DTYPE = np.dtype([("d_q", np.uint64), ("d_k", np.uint64), ("d_v", np.uint64),
+                              ("d_slots", np.uint64), ("d_plan", np.uint64),
+                              ("info", np.uint64), ("d_out", np.uint64), ("d_lse", np.uint64),
+                              ("step", np.int32), ("reserved", np.int32)])
+assert DECODE_STEP_DTYPE.itemsize == C.sizeof(rx_decode_step)
+
+
 class rx_pool_desc(C.Structure):
     _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("num_slots", C.c_int64),
                 ("num_layers", C.c_int32), ("num_kv_heads", C.c_int32),
@@ -95,6 +103,7 @@ _SIGS = {
     "rx_extend_end": [P, I32, P, P, P, I64, P, P, P, P],
     "rx_finish": [P, I32, P, P, P, I64, P, P, P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
+    "rx_batch_end": [P, P, P, I32, I32, P],
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
     "rx_plan_decode_steps": [P, I32, I32, P, P, P, I32, I32, I32, P, I64, P],
     "rx_alloc_steps": [P, I64, I32, P],
@@ -176,6 +185,14 @@ class RadixCache:
             self.close()
         except Exception:
             pass
+
+    def batch_end(self, tokens, indptr, start):
+        """End of the batch that starts at request `start` (rx_batch_end);
+        tokens int32 (the wave's prompts concatenated), indptr int64."""
+        out = C.c_int32()
+        _check(_lib.rx_batch_end(self._h, _p(tokens), _p(indptr), int(start), len(indptr) - 1,
+                                 C.byref(out)))
+        return out.value
 
     # S1
     def match_length(self, tokens):
@@ -363,9 +380,15 @@ def decode_attention(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_ou
 
 
 def decode_steps(pool, layer, hq, d_table, steps, B, scale, d_workspace, stream=None):
-    """rx_decode_steps over a ctypes array of rx_decode_step."""
+    """rx_decode_steps over a ctypes array of rx_decode_step or a numpy array
+    of DECODE_STEP_DTYPE records."""
+    if isinstance(steps, np.ndarray):
+        assert steps.dtype == DECODE_STEP_DTYPE and steps.flags.c_contiguous
+        ptr = steps.ctypes.data
+    else:
+        ptr = C.cast(steps, C.c_void_p)
     _check(_lib.rx_decode_steps(C.byref(pool), layer, hq, d_table.data_ptr(), d_table.shape[1],
-                                steps, len(steps), B, scale, d_workspace.data_ptr(),
+                                ptr, len(steps), B, scale, d_workspace.data_ptr(),
                                 d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
 
 

@@ -311,3 +311,42 @@ def test_tails_private_flag():
     _, info = c.plan_decode([mid, node, node2], [100, 200, 161], [0, 1, 2], 32, 8, 128,
                             n_steps=2)
     assert info.tails_private == 0
+
+
+def test_batch_end_follows_the_in_batch_rule():
+    """rx_batch_end equals the request-by-request rule: m_j from the tree,
+    conflict when a member shares more than m_j tokens (exactly m_j does not)."""
+    rng = np.random.default_rng(5)
+    c = rx.RadixCache(100000)
+    base = rng.integers(1, 50, size=300).astype(np.int32)
+    slots = c.alloc(200)
+    c.insert(base[:200], slots)
+    prompts = []
+    for i in range(30):
+        cut = int(rng.choice([0, 50, 199, 200, 201, 250, 300]))
+        tail = rng.integers(1, 50, size=int(rng.integers(1, 40))).astype(np.int32)
+        prompts.append(np.concatenate([base[:cut], tail]))
+    prompts.append(prompts[3].copy())   # an identical prompt
+    prompts.append(prompts[5][:1].copy())   # a one-token prompt
+    tokens = np.concatenate(prompts).astype(np.int32)
+    indptr = np.zeros(len(prompts) + 1, dtype=np.int64)
+    np.cumsum([len(p) for p in prompts], out=indptr[1:])
+    for start in range(len(prompts)):
+        want = len(prompts)
+        for j in range(start + 1, len(prompts)):
+            m = c.match_length(prompts[j][:-1])
+            if rx.batch_conflict(prompts[j], m, tokens[indptr[start]:indptr[j]],
+                                 indptr[start:j + 1] - indptr[start]):
+                want = j
+                break
+            # the rule itself, brute force
+            assert all(oracle_common(prompts[j], prompts[r]) <= m for r in range(start, j))
+        assert c.batch_end(tokens, indptr, start) == want
+
+
+def oracle_common(a, b):
+    n = min(len(a), len(b))
+    k = 0
+    while k < n and a[k] == b[k]:
+        k += 1
+    return k
