@@ -648,25 +648,6 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     __syncwarp();
   }
 
-  // Q^T operand: n-tile nt, k-step kk: (d 16kk + 2c, +1 | 16kk + 2c + 8, +9) of row nt*8 + g
-  uint32_t qb[NR][8][2];
-#pragma unroll
-  for (int nt = 0; nt < NR; ++nt) {
-    const int r = nt * 8 + g;
-    const bool ok = r < n_rows;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q);
-    if (ok) {
-      const int u = r / G;
-      const int64_t b = a.members[member_off + u];
-      qrow = reinterpret_cast<const uint32_t*>(a.q + (b * a.hq + kvh * G + (r - u * G)) * D);
-    }
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      qb[nt][kk][0] = ok ? __ldg(qrow + 8 * kk + c) : 0u;
-      qb[nt][kk][1] = ok ? __ldg(qrow + 8 * kk + c + 4) : 0u;
-    }
-  }
-
   const int n_steps = ke > kb ? (ke - kb + 15) >> 4 : 0;
   int slot_base = 0;  // key offset (from kb) of slot_buf[0]
   // slots of keys [kb + base, kb + base + kSlotBuf): -1 past the key range, a
@@ -728,6 +709,26 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     rxk::cp_async_commit();
   }
 
+  // Q^T operand, loaded while the first steps' keys are in flight: n-tile nt,
+  // k-step kk: (d 16kk + 2c, +1 | 16kk + 2c + 8, +9) of row nt*8 + g
+  uint32_t qb[NR][8][2];
+#pragma unroll
+  for (int nt = 0; nt < NR; ++nt) {
+    const int r = nt * 8 + g;
+    const bool ok = r < n_rows;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q);
+    if (ok) {
+      const int u = r / G;
+      const int64_t b = a.members[member_off + u];
+      qrow = reinterpret_cast<const uint32_t*>(a.q + (b * a.hq + kvh * G + (r - u * G)) * D);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      qb[nt][kk][0] = ok ? __ldg(qrow + 8 * kk + c) : 0u;
+      qb[nt][kk][1] = ok ? __ldg(qrow + 8 * kk + c + 4) : 0u;
+    }
+  }
+
   // ldmatrix lane addresses: K (A of S^T, keys x d) and V^T (A of O^T, d x keys)
   const uint32_t k_lane = uint32_t(((lane & 7) + ((lane >> 3) & 1) * 8) * kRowPitch + (lane >> 4) * 16);
   const uint32_t v_lane =
@@ -756,43 +757,67 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
-    // online softmax over the keys of this step (rows 2c, 2c+1 of each n-tile)
+    // online softmax over the keys of this step (rows 2c, 2c+1 of each n-tile).
+    // The row reference m_ref changes only when some key of the row exceeds it
+    // by more than 2^8: each lane tests its own keys, one vote per step, and
+    // only then are the row maxima reduced over the 8 lanes of a row and O and
+    // the sums rescaled (rare after the first step of a unit).
     const int key0 = kb + st * 16 + g;
     const bool in0 = key0 < ke, in1 = key0 + 8 < ke;
-    uint32_t pk[NR][2];  // (key g | key g+8) of rows 2c, 2c+1 as bf16x2
+    float x[NR][4];
+    bool grow = false;
 #pragma unroll
     for (int nt = 0; nt < NR; ++nt) {
-      float x[4];
-      x[0] = in0 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
-      x[1] = in0 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
-      x[2] = in1 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
-      x[3] = in1 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
+      x[nt][0] = in0 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
+      x[nt][1] = in0 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
+      x[nt][2] = in1 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
+      x[nt][3] = in1 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float mx = fmaxf(x[e], x[2 + e]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const bool need = mx > m_ref[nt][e] + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? rxk::fast_exp2(m_ref[nt][e] - mx) : 1.f;
-          if (need) m_ref[nt][e] = mx;
-          l_run[nt][e] *= alpha;
+      for (int e = 0; e < 2; ++e)
+        grow |= fmaxf(x[nt][e], x[nt][2 + e]) > m_ref[nt][e] + kRescaleThreshold;
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+      float mx[NR][2];
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            o[nt][mt][e] *= alpha;
-            o[nt][mt][2 + e] *= alpha;
+      for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mx[nt][e] = fmaxf(x[nt][e], x[nt][2 + e]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            mx[nt][e] = fmaxf(mx[nt][e], __shfl_xor_sync(0xffffffffu, mx[nt][e], off));
+#pragma unroll
+      for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (mx[nt][e] > m_ref[nt][e]) {
+            const float alpha = rxk::fast_exp2(m_ref[nt][e] - mx[nt][e]);  // 0 from -inf
+            m_ref[nt][e] = mx[nt][e];
+            l_run[nt][e] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[nt][mt][e] *= alpha;
+              o[nt][mt][2 + e] *= alpha;
+            }
           }
         }
+    }
+    uint32_t pk[NR][2];  // (key g | key g+8) of rows 2c, 2c+1 as bf16x2
+#pragma unroll
+    for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
         const float m_use = m_ref[nt][e] == -INFINITY ? 0.f : m_ref[nt][e];
         uint32_t h;
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n"
             : "=r"(h)
-            : "f"(rxk::fast_exp2(x[2 + e] - m_use)), "f"(rxk::fast_exp2(x[e] - m_use)));
+            : "f"(rxk::fast_exp2(x[nt][2 + e] - m_use)), "f"(rxk::fast_exp2(x[nt][e] - m_use)));
         pk[nt][e] = h;  // low half: key g, high half: key g+8
         l_run[nt][e] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
       }
-    }
     // P^T operand for n-tile nt: b0 = (P[key 2c][row g], P[key 2c+1][row g]),
     // b1 = keys 2c+8, 2c+9; key k of row r sits in lane 4k + r/2, half r%2
     uint32_t pb[NR][2];
