@@ -49,6 +49,18 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
+# captures summarised in profiles/ (cold L2, one launch): decode_fused_kernel
+# on an agent_loop decode step and on a long_shared decode step, and the
+# second agent_loop extend launch.  Bytes per launch, or None where no capture
+# of the current kernel exists.
+TRAFFIC = {
+    ("agent_loop", "rx_decode_attention"): 45.5e6 + 0.03e6,
+    ("long_shared", "rx_decode_attention"): 418.5e6 + 36.3e6,
+    ("agent_loop", "rx_extend_attention"): 104.7e6 + 73.8e6,
+}
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -327,11 +339,13 @@ def main():
     if ext["ms"] >= dec["ms"]:
         roof = {"kernel": "rx_extend_attention", "bound": "tensor", "achieved": ext_tflops,
                 "peak": bf16_peak, "unit": "TFLOP/s", "frac": ext_tflops / bf16_peak,
-                "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)"}
+                "traffic": TRAFFIC.get((args.workload, "rx_extend_attention")),
+                "peak_source": f"{peak_src} bf16_tflops (burst)"}
     else:
         roof = {"kernel": "rx_decode_attention", "bound": "hbm", "achieved": dec_gbs,
                 "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
-                "traffic": None, "peak_source": f"{peak_src} hbm_gbs"}
+                "traffic": TRAFFIC.get((args.workload, "rx_decode_attention")),
+                "peak_source": f"{peak_src} hbm_gbs"}
 
     # ---------------- e2e: host inputs copied in, outputs read back
     e2e = None
