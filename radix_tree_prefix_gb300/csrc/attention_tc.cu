@@ -76,10 +76,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
-constexpr uint32_t kSleepNs = 20000;            // MMA / loader waits sleep instead of spinning
+constexpr uint32_t kSleepNs = 0;                // MMA / loader waits: plain try_wait polling
 constexpr float kMasked = -1.0e30f;             // raw score of a masked key
 constexpr int BM = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;   // threads of a tensor-core tile (one softmax warpgroup)
+constexpr int kThreads2 = 320;  // threads of a split-softmax tile (two warpgroups)
+
+// CTA barrier of the 320 threads of a split-softmax tile (named barrier 1).
+__device__ __forceinline__ void tile2_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads2) : "memory");
+}
 
 struct TcArgs {
   const bf16* q;
@@ -198,8 +204,9 @@ struct Layout {
   static constexpr int V0 = K0 + 2 * KV_BYTES;
   static constexpr int P0 = V0 + 2 * KV_BYTES;
   static constexpr int BAR = P0 + 2 * P_BYTES;
-  // barriers: q, kfull[2], vfull[2], emptyk[2], emptyv[2], s[2], p[2], o, final
-  static constexpr int NBAR = 15;
+  // barriers: q, kfull[2], vfull[2], emptyk[2], emptyv[2], s[2], p[2], o, final,
+  // epilogue exchange (split-softmax tile)
+  static constexpr int NBAR = 16;
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int BYTES = MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = 512;
@@ -270,8 +277,10 @@ __device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
     const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
     const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
     const int64_t row0 = a.tma_row_base + int64_t(kvh) * a.tma_head_rows;
-    int32_t slot[SPL];  // slots of the tile being loaded
-    int32_t nxt[SPL];   // slots of the following tile, in flight meanwhile
+    // slots of four consecutive tiles (tile j in ring j % 4): a tile's table
+    // reads are issued four tiles ahead into registers that nothing touches
+    // until then, so their round trips to L2 overlap the loads before them
+    int32_t sa[SPL], sb[SPL], sc[SPL], sd[SPL];
     auto load_slots = [&](int j, int32_t (&dst)[SPL]) {
       const int k0 = t.key_begin + j * BN;
 #pragma unroll
@@ -280,7 +289,7 @@ __device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
         dst[i] = (j < n_tiles && key < t.key_end) ? __ldg(t.trow + key) : -1;
       }
     };
-    auto check_slots = [&]() {
+    auto check_slots = [&](int32_t (&slot)[SPL]) {
 #pragma unroll
       for (int i = 0; i < SPL; ++i) {
         if (slot[i] >= a.num_slots || slot[i] < -1) {
@@ -291,7 +300,8 @@ __device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
     };
     // one K or V tile: TMA box loads if the slots are one contiguous run of
     // BN valid slots, else a zero-filling cp.async gather
-    auto load_tile = [&](const CUtensorMap* tm, const bf16* src_base, uint32_t dst, uint32_t full_bar) {
+    auto load_tile = [&](int32_t (&slot)[SPL], const CUtensorMap* tm, const bf16* src_base,
+                         uint32_t dst, uint32_t full_bar) {
       const int32_t first = __shfl_sync(0xffffffffu, slot[0], 0);
       bool run = first >= 0 && int64_t(first) + BN <= a.num_slots;
 #pragma unroll
@@ -329,26 +339,35 @@ __device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
         if (lane == 0) tc::mbar_arrive(full_bar);
       }
     };
-    load_slots(0, slot);
-    load_slots(1, nxt);
-    for (int j = 0; j < n_tiles; ++j) {
+    load_slots(0, sa);
+    load_slots(1, sb);
+    load_slots(2, sc);
+    load_slots(3, sd);
+    // tile j: K and V with the slots in `slot`, then tile j + 4's table reads
+    // into the same registers
+    auto step = [&](int j, int32_t (&slot)[SPL]) -> bool {
       const int s = j & 1;
-      check_slots();
+      check_slots(slot);
       if (j >= 2 &&
           !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(s), ((j - 2) >> 1) & 1, abort_flag,
                                                   kWaitLimit, kSleepNs)))
-        break;
-      load_tile(tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
+        return false;
+      load_tile(slot, tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
       if (lane == 0) TC_TRACE(0, j);
       if (j >= 2 &&
           !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(s), ((j - 2) >> 1) & 1, abort_flag,
                                                   kWaitLimit, kSleepNs)))
-        break;
-      load_tile(tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
+        return false;
+      load_tile(slot, tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
       if (lane == 0) TC_TRACE(2, j);
-#pragma unroll
-      for (int i = 0; i < SPL; ++i) slot[i] = nxt[i];
-      load_slots(j + 2, nxt);
+      load_slots(j + 4, slot);
+      return true;
+    };
+    for (int j = 0; j < n_tiles; j += 4) {
+      if (!step(j, sa)) break;
+      if (j + 1 < n_tiles && !step(j + 1, sb)) break;
+      if (j + 2 < n_tiles && !step(j + 2, sc)) break;
+      if (j + 3 < n_tiles && !step(j + 3, sd)) break;
     }
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issue
@@ -578,12 +597,447 @@ __device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
   }
 }
 
+// One 128-row tile (x = tile / work item, kvh = KV head) on 320 threads with
+// the keys of every key tile split between two softmax warpgroups: warpgroup
+// w (warps 4w .. 4w+3) owns keys [w BN/2, (w+1) BN/2) of each tile and keeps
+// its own online softmax over them (row max m_w, sum l_w, and its own O_w
+// accumulator in TMEM: O_w += P[:, half w] V[half w, :]).  The two halves
+// need no exchange while the key loop runs; the epilogue merges them by
+// log-sum-exp (m = max(m_0, m_1), O = sum_w 2^(m_w - m) O_w, l likewise).
+// Two softmax warps per SM sub-partition hide each other's exp / TMEM /
+// shared-memory latencies.  Warp 8 issues the MMAs, warp 9 loads K/V.
+template <int D, int BN, bool DECODE>
+__device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk,
+                                         const CUtensorMap* tmv, uint8_t* smem_raw, int bx,
+                                         int kvh) {
+  using Lo = Layout<D, BN>;
+  constexpr int HALF = BN / 2;                 // keys per softmax warpgroup
+  constexpr int O0 = Lo::O_COL, O1 = Lo::O_COL + D;  // TMEM columns of O_0, O_1
+  static_assert(2 * BN + 2 * D <= Lo::TMEM_COLS, "TMEM budget");
+  // 1024-byte alignment of the swizzled tiles
+  const uint32_t raw = rxk::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + Lo::Q;
+  const uint32_t bar = base + Lo::BAR;
+  auto BAR_Q = [&]() { return bar; };
+  auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
+  auto BAR_VF = [&](int s) { return bar + 8u * (3 + s); };
+  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (5 + s); };
+  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (7 + s); };
+  auto BAR_S = [&](int s) { return bar + 8u * (9 + s); };
+  auto BAR_P = [&](int s) { return bar + 8u * (11 + s); };
+  const uint32_t BAR_O = bar + 8u * 13;
+  const uint32_t BAR_FIN = bar + 8u * 14;
+  const uint32_t BAR_XE = bar + 8u * 15;  // epilogue exchange of (m_w, l_w)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const TileDesc t = describe<DECODE>(a, bx);
+  const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
+
+  if (tid == 0) {
+    tc::mbar_init(BAR_Q(), 8 * 32);  // every softmax thread lands half a Q row
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(BAR_KF(s), 1);
+      tc::mbar_init(BAR_VF(s), 1);
+      tc::mbar_init(BAR_EMPTY_K(s), 1);
+      tc::mbar_init(BAR_EMPTY_V(s), 1);
+      tc::mbar_init(BAR_S(s), 1);
+      tc::mbar_init(BAR_P(s), 256);
+    }
+    tc::mbar_init(BAR_O, 1);
+    tc::mbar_init(BAR_FIN, 1);
+    tc::mbar_init(BAR_XE, 256);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(rxk::smem_addr(tmem_slot), Lo::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  tile2_sync();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 9) {
+    // ------------------------------------------------------------- loader
+    // keys written by earlier kernels on the stream are read from here on
+    rxk::griddep_wait();
+    constexpr int CPR = D / 8;
+    constexpr int SPL = BN / 32;  // slots per lane: rows lane + 32 i
+    const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
+    const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
+    const int64_t row0 = a.tma_row_base + int64_t(kvh) * a.tma_head_rows;
+    // slots of four consecutive tiles (tile j in ring j % 4): a tile's table
+    // reads are issued four tiles ahead into registers that nothing touches
+    // until then, so their round trips to L2 overlap the loads before them
+    int32_t sa[SPL], sb[SPL], sc[SPL], sd[SPL];
+    auto load_slots = [&](int j, int32_t (&dst)[SPL]) {
+      const int k0 = t.key_begin + j * BN;
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) {
+        const int key = k0 + lane + 32 * i;
+        dst[i] = (j < n_tiles && key < t.key_end) ? __ldg(t.trow + key) : -1;
+      }
+    };
+    auto check_slots = [&](int32_t (&slot)[SPL]) {
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) {
+        if (slot[i] >= a.num_slots || slot[i] < -1) {
+          atomicOr(&g_tc_error, 1);
+          slot[i] = 0;
+        }
+      }
+    };
+    // one K or V tile: TMA box loads if the slots are one contiguous run of
+    // BN valid slots, else a zero-filling cp.async gather
+    auto load_tile = [&](int32_t (&slot)[SPL], const CUtensorMap* tm, const bf16* src_base,
+                         uint32_t dst, uint32_t full_bar) {
+      const int32_t first = __shfl_sync(0xffffffffu, slot[0], 0);
+      bool run = first >= 0 && int64_t(first) + BN <= a.num_slots;
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) run = run && (slot[i] == first + lane + 32 * i);
+      run = __all_sync(0xffffffffu, run);
+      if (run) {
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(full_bar, uint32_t(BN * D * 2));
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            tc::tma_load_2d(dst + uint32_t(cb * BN * 128), tm, cb * 64, int(row0 + first),
+                            full_bar);
+        }
+      } else {
+        // lanes 0-15 and 16-31 copy chunks (lane % 16) + 16 h of rows 2k, 2k+1
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+#pragma unroll 4
+          for (int k = 0; k < 16; ++k) {
+            const int row = 32 * i + 2 * k + (lane >> 4);
+            const int32_t sl = __shfl_sync(0xffffffffu, slot[i], row & 31);
+            const bool ok = sl >= 0;
+            const int64_t s64 = ok ? int64_t(sl) : 0;
+#pragma unroll
+            for (int h = 0; h < CPR / 16; ++h) {
+              const int ch = (lane & 15) + 16 * h;
+              rxk::cp_async_16(sw128(dst, BN, row, ch), src_base + s64 * D + ch * 8, ok);
+            }
+          }
+        }
+        rxk::cp_async_commit();
+        rxk::cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(full_bar);
+      }
+    };
+    load_slots(0, sa);
+    load_slots(1, sb);
+    load_slots(2, sc);
+    load_slots(3, sd);
+    // tile j: K and V with the slots in `slot`, then tile j + 4's table reads
+    // into the same registers
+    auto step = [&](int j, int32_t (&slot)[SPL]) -> bool {
+      const int s = j & 1;
+      check_slots(slot);
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(s), ((j - 2) >> 1) & 1, abort_flag,
+                                                  kWaitLimit, kSleepNs)))
+        return false;
+      load_tile(slot, tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
+      if (lane == 0) TC_TRACE(0, j);
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(s), ((j - 2) >> 1) & 1, abort_flag,
+                                                  kWaitLimit, kSleepNs)))
+        return false;
+      load_tile(slot, tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
+      if (lane == 0) TC_TRACE(2, j);
+      load_slots(j + 4, slot);
+      return true;
+    };
+    for (int j = 0; j < n_tiles; j += 4) {
+      if (!step(j, sa)) break;
+      if (j + 1 < n_tiles && !step(j + 1, sb)) break;
+      if (j + 2 < n_tiles && !step(j + 2, sc)) break;
+      if (j + 3 < n_tiles && !step(j + 3, sd)) break;
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
+      constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
+      bool ok = tc::mbar_wait(BAR_Q(), 0, abort_flag, kWaitLimit, kSleepNs);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = uint32_t((ks & 3) * 32);
+          const uint64_t ad = tc::sdesc_sw128(sQ + (ks >> 2) * (BM * 128) + koff, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(sk + (ks >> 2) * (BN * 128) + koff, 16, 1024);
+          tc::mma_bf16_ss(tmem + uint32_t(s * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(BAR_S(s));
+        tc::mma_commit(BAR_EMPTY_K(s));
+        TC_TRACE(4, j);
+      };
+      if (ok && n_tiles > 0) {
+        ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit, kSleepNs);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_s(0);
+        }
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j & 1;
+        if (j + 1 < n_tiles) {
+          if (!tc::mbar_wait(BAR_KF((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimit,
+                             kSleepNs))
+            break;
+          TC_TRACE(1, j + 1);
+          tc::tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!tc::mbar_wait(BAR_P(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
+        if (!tc::mbar_wait(BAR_VF(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
+        TC_TRACE(3, j);
+        tc::tc_fence_after();
+        const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
+        const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
+        // O_0 += P[:, keys of warpgroup 0] V[those keys], O_1 likewise
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t ad =
+              tc::sdesc_sw128(sp + (ks >> 2) * (BM * 128) + uint32_t((ks & 3) * 32), 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(sv + uint32_t(ks * 2048), BN * 128, 1024);
+          const int half = ks / (HALF / 16);
+          tc::mma_bf16_ss(tmem + uint32_t(half ? O1 : O0), ad, bd, IDESC_PV,
+                          (j > 0 || ks != half * (HALF / 16)) ? 1u : 0u);
+        }
+        tc::mma_commit(BAR_O);
+        tc::mma_commit(BAR_EMPTY_V(s));
+        TC_TRACE(5, j);
+      }
+      // drain: every MMA issued above has completed once this arrives
+      tc::mma_commit(BAR_FIN);
+      tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int wg = warp >> 2;
+    const int i = (warp & 3) * 32 + lane;  // query row = TMEM lane
+    int64_t qi = 0, part = 0;
+    int head = 0, lim = t.key_end;
+    const bool valid = i < t.n_rows;
+    if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
+    // the queries and the outputs (decode: partial buffers the previous
+    // merge read) are touched only once earlier kernels on the stream are done
+    rxk::griddep_wait();
+    {
+      // warpgroup w gathers half w of Q row i (zeros past the tile's rows)
+      // while the loader warp already streams the first K/V tiles
+      constexpr int CPR = D / 8;
+      const bf16* src = a.q + (qi * a.hq + head) * D;
+#pragma unroll
+      for (int c = 0; c < CPR / 2; ++c) {
+        const int ch = wg * (CPR / 2) + c;
+        rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, valid);
+      }
+      rxk::cp_async_commit();
+      rxk::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(BAR_Q());
+    }
+    const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
+    const uint32_t o_col = uint32_t(wg ? O1 : O0);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j & 1;
+      // waits are made warp-uniform before any warp-collective tcgen05 op
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR_S(s), (j >> 1) & 1, abort_flag, kWaitLimit))) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      if (i == 0) TC_TRACE(wg ? 9 : 6, j);
+      const int k0 = t.key_begin + j * BN + wg * HALF;  // first key of this warpgroup's half
+      const bool need_mask = k0 + HALF > t.nomask_end;
+      uint32_t sr[HALF];
+      tc::tmem_ld_row<HALF>(tl + uint32_t(s * BN + wg * HALF), sr);
+      tc::tmem_ld_wait();
+      if (i == 0 && wg == 0) TC_TRACE(8, j);
+      // row max of the raw scores over this half (masked keys get a large
+      // negative finite score, so the packed exponent below never sees an
+      // infinity); eight independent partial maxima keep the chains short
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = kMasked;
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < HALF; ++e) {
+          if (k0 + e >= lim) sr[e] = __float_as_uint(kMasked);
+          mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < HALF; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
+      }
+      const float raw_mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // a half whose keys are all masked for this row (possible for one
+      // warpgroup) leaves m_ref where it is; its p are then 0
+      const float mx = raw_mx > 0.5f * kMasked ? a.scale_log2 * raw_mx : -INFINITY;
+      const float m_new = fmaxf(m_ref, mx);
+      if (j == 0) {
+        m_ref = m_new;
+      } else {
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!__all_sync(0xffffffffu,
+                          tc::mbar_wait(BAR_O, (j - 1) & 1, abort_flag, kWaitLimit))) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const float alpha = need ? rxk::fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tc::tmem_ld32(tl + o_col + uint32_t(cc * 32), r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tc::tmem_st32(tl + o_col + uint32_t(cc * 32), r);
+          }
+          tc::tmem_st_wait();
+          if (need) {
+            l *= alpha;
+            m_ref = m_new;
+          }
+        }
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
+      float l8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) l8[u] = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < HALF / 32; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          // p = 2^(scale*s - m) for two keys at once: the exponents are rounded
+          // to bf16 with integer ops (add half an ulp, keep the high half) and
+          // one packed SFU op gives both p in bf16 (the precision P has in the
+          // PV product); the row sum adds exactly those values in fp32, in
+          // eight independent partial sums.
+          const float x0 = fmaf(__uint_as_float(sr[cc * 32 + e]), a.scale_log2, -m_use);
+          const float x1 = fmaf(__uint_as_float(sr[cc * 32 + e + 1]), a.scale_log2, -m_use);
+          const uint32_t h = rxk::exp2_bf16x2_bits(__float_as_uint(x0) + 0x8000u,
+                                                   __float_as_uint(x1) + 0x8000u);
+          l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
+          pk[e >> 1] = h;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = sw128(sp, BM, i, wg * (HALF / 8) + cc * 4 + q);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(pk[4 * q]),
+                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                       : "memory");
+        }
+      }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      if (i == 0 && wg == 0) TC_TRACE(10, j);
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR_P(s));
+      if (i == 0) TC_TRACE(wg ? 11 : 7, j);
+    }
+    // The epilogue waits on BAR_FIN, which completes exactly once, after every
+    // MMA of the CTA (waiting on BAR_O's parity would be ambiguous).  Then the
+    // two warpgroups swap (m_w, l_w) of each row through shared memory (the P
+    // buffers are free by then) and warpgroup w writes output columns
+    // [w D/2, (w+1) D/2) of the merged row.
+    const bool fin = ok && n_tiles > 0 &&
+                     __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit));
+    float* xch = reinterpret_cast<float*>(gbase + Lo::P0);  // [2 warpgroups][m, l][BM]
+    if (fin) {
+      xch[(wg * 2 + 0) * BM + i] = m_ref;
+      xch[(wg * 2 + 1) * BM + i] = l;
+    }
+    tc::mbar_arrive(BAR_XE);  // every softmax thread arrives, so no waiter is left behind
+    const bool xok = __all_sync(0xffffffffu, tc::mbar_wait(BAR_XE, 0, abort_flag, kWaitLimit));
+    if (fin && xok) {
+      tc::tc_fence_after();
+      const float m_o = xch[((1 - wg) * 2 + 0) * BM + i];
+      const float l_o = xch[((1 - wg) * 2 + 1) * BM + i];
+      const float m_all = fmaxf(m_ref, m_o);
+      const float m_safe = m_all == -INFINITY ? 0.f : m_all;
+      const float c_me = m_ref == -INFINITY ? 0.f : rxk::fast_exp2(m_ref - m_safe);
+      const float c_ot = m_o == -INFINITY ? 0.f : rxk::fast_exp2(m_o - m_safe);
+      const float l_all = l * c_me + l_o * c_ot;
+      const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
+      const float c0 = (wg ? c_ot : c_me) * inv;  // weight of O_0
+      const float c1 = (wg ? c_me : c_ot) * inv;  // weight of O_1
+      float* dst;
+      float* lse_dst;
+      if constexpr (DECODE) {
+        dst = a.ws_o + (part * a.hq + head) * D;
+        lse_dst = a.ws_lse + part * a.hq + head;
+      } else {
+        dst = a.out + (qi * a.hq + head) * D;
+        lse_dst = a.lse + qi * a.hq + head;
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col = wg * (D / 2) + cc * 32;
+        uint32_t r0[32], r1[32];
+        tc::tmem_ld32(tl + uint32_t(O0 + col), r0);
+        tc::tmem_ld32(tl + uint32_t(O1 + col), r1);
+        tc::tmem_ld_wait();
+        if (valid) {
+          float4* o4 = reinterpret_cast<float4*>(dst + col);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o4[e] = make_float4(
+                __uint_as_float(r0[4 * e]) * c0 + __uint_as_float(r1[4 * e]) * c1,
+                __uint_as_float(r0[4 * e + 1]) * c0 + __uint_as_float(r1[4 * e + 1]) * c1,
+                __uint_as_float(r0[4 * e + 2]) * c0 + __uint_as_float(r1[4 * e + 2]) * c1,
+                __uint_as_float(r0[4 * e + 3]) * c0 + __uint_as_float(r1[4 * e + 3]) * c1);
+        }
+      }
+      if (valid && wg == 0) *lse_dst = m_safe * kLn2 + logf(l_all);
+    }
+  }
+  tc::tc_fence_before();
+  tile2_sync();
+  if (tid == 0 && *abort_flag) atomicOr(&g_tc_error, 2);
+  if (warp == 8) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, Lo::TMEM_COLS);
+  }
+}
+
 template <int D, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   tc_tile<D, BN, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
+}
+
+// Extend with the split-softmax tile (head_dim 128).
+__global__ void __launch_bounds__(kThreads2, 1)
+    attn_tc2_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  tc_tile2<128, 128, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
 }
 
 // ---------------------------------------------------------------------------
@@ -884,7 +1338,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
 // Launched with programmatic stream serialization: the merge that follows may
 // launch early, and this kernel waits (griddepcontrol.wait) for the previous
 // kernels on the stream before it touches what they wrote or read.
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads2, 1)
     decode_fused_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -892,8 +1346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cta = int(blockIdx.x);
   if (cta < a.n_tc_ctas) {
     const int hkv = a.hq / a.group;
-    tc_tile<128, 128, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
+    tc_tile2<128, 128, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
   }
+  if (threadIdx.x >= kPipeWarps * 32) return;  // the warp role uses the first six warps
   rxk::griddep_wait();
   // warp role: this warp's ring, slot buffer and stage barriers
   const uint32_t raw = rxk::smem_addr(smem_raw);
@@ -998,10 +1453,15 @@ template <int D, int BN>
 rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx,
                         unsigned gy, cudaStream_t s) {
   constexpr int bytes = Layout<D, BN>::BYTES;
+  // head_dim 128: the split-softmax tile; 256: O_0 and O_1 would not fit in TMEM
+  constexpr bool split = D == 128;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(attn_tc_kernel<D, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         bytes);
+    if constexpr (split)
+      cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    else
+      cudaFuncSetAttribute(attn_tc_kernel<D, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
     configured = true;
   }
   const CUtensorMap *tmk, *tmv;
@@ -1009,7 +1469,10 @@ rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsig
     return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   a.tma_row_base = int64_t(layer) * pool->num_kv_heads * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  attn_tc_kernel<D, BN><<<dim3(gx, gy), kThreads, bytes, s>>>(a, *tmk, *tmv);
+  if constexpr (split)
+    attn_tc2_kernel<<<dim3(gx, gy), kThreads2, bytes, s>>>(a, *tmk, *tmv);
+  else
+    attn_tc_kernel<D, BN><<<dim3(gx, gy), kThreads, bytes, s>>>(a, *tmk, *tmv);
   return rx_internal::launch_status("extend attention (tcgen05)");
 }
 
@@ -1088,7 +1551,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
     return set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(ctas));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kThreads2);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
