@@ -79,13 +79,7 @@ constexpr float kRescaleThreshold = 8.0f;       // log2 units
 constexpr uint32_t kSleepNs = 0;                // MMA / loader waits: plain try_wait polling
 constexpr float kMasked = -1.0e30f;             // raw score of a masked key
 constexpr int BM = 128;
-constexpr int kThreads = 192;   // threads of a tensor-core tile (one softmax warpgroup)
-constexpr int kThreads2 = 320;  // threads of a split-softmax tile (two warpgroups)
-
-// CTA barrier of the 320 threads of a split-softmax tile (named barrier 1).
-__device__ __forceinline__ void tile2_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads2) : "memory");
-}
+constexpr int kThreads = 192;   // threads of a tensor-core tile
 
 struct TcArgs {
   const bf16* q;
@@ -204,9 +198,8 @@ struct Layout {
   static constexpr int V0 = K0 + 2 * KV_BYTES;
   static constexpr int P0 = V0 + 2 * KV_BYTES;
   static constexpr int BAR = P0 + 2 * P_BYTES;
-  // barriers: q, kfull[2], vfull[2], emptyk[2], emptyv[2], s[2], p[2], o, final,
-  // epilogue exchange (split-softmax tile)
-  static constexpr int NBAR = 16;
+  // barriers: q, kfull[2], vfull[2], emptyk[2], emptyv[2], s[2], p[2], o, final
+  static constexpr int NBAR = 15;
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int BYTES = MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = 512;
@@ -597,39 +590,86 @@ __device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
   }
 }
 
-// One 128-row tile (x = tile / work item, kvh = KV head) on 320 threads with
-// the keys of every key tile split between two softmax warpgroups: warpgroup
-// w (warps 4w .. 4w+3) owns keys [w BN/2, (w+1) BN/2) of each tile and keeps
-// its own online softmax over them (row max m_w, sum l_w, and its own O_w
-// accumulator in TMEM: O_w += P[:, half w] V[half w, :]).  The two halves
-// need no exchange while the key loop runs; the epilogue merges them by
-// log-sum-exp (m = max(m_0, m_1), O = sum_w 2^(m_w - m) O_w, l likewise).
-// Two softmax warps per SM sub-partition hide each other's exp / TMEM /
-// shared-memory latencies.  Warp 8 issues the MMAs, warp 9 loads K/V.
-template <int D, int BN, bool DECODE>
-__device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk,
+// Tensor-core tile for head_dim 128 (128 query rows, 128 keys per key
+// tile) on 320 threads.  The MMA warp keeps two S tiles ahead of the softmax:
+// S_{j+2} = Q K_{j+2}^T is issued before PV_j, into a ring of three S
+// buffers in TMEM, so the softmax of tile j+1 never waits for an MMA.  P_j
+// (bf16) overwrites the first 64 columns of S_j's buffer once the softmax
+// has read S_j, and PV_j reads it from TMEM as its A operand; tcgen05.mma
+// operations from one thread run in issue order, so S_{j+3} (issued after
+// PV_j) reuses that buffer only after PV_j read P_j.
+// TMEM: S ring [0, 384), O [384, 512).  Shared memory: Q (128-byte
+// swizzled, the A operand of S), K in three stages, V in two.
+// Warps 0-7 softmax in two warpgroups that split each key tile's columns
+// (thread (w, i) of warpgroup w: row i = TMEM lane i, keys [64 w, 64 w + 64);
+// it also gathers chunks [8 w, 8 w + 8) of Q row i first), warp 8 issues
+// the MMAs, warp 9 loads K and warp 10 loads V (a V stage frees only when PV
+// of its previous tile completes, and K loads must not queue behind that).
+constexpr int kThreads3 = 352;
+
+struct Layout3 {
+  static constexpr int D = 128, BN = 128, KSTAGES = 3, VSTAGES = 2, SBUF = 3;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int Q = 0;
+  static constexpr int K0 = Q + BM * D * 2;
+  static constexpr int V0 = K0 + KSTAGES * KV_BYTES;
+  // exchange slots: per-tile half-row maxima (two parities) and the final
+  // row sums, [3][2 warpgroups][128 rows] floats
+  static constexpr int XCH = V0 + VSTAGES * KV_BYTES;
+  static constexpr int BAR = XCH + 3 * 2 * 128 * 4;
+  // barriers: q, kfull[3], vfull[2], emptyk[3], emptyv[2], s[3], p[3], o,
+  // final, max exchange[2], sum exchange
+  static constexpr int NBAR = 23;
+  static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
+  static constexpr int BYTES = MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int O_COL = SBUF * BN;
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+};
+
+// D(tmem) (+)= A(tmem) * B(smem); issued by a single thread.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit values from registers (thread t: lane t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+template <bool DECODE>
+__device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk,
                                          const CUtensorMap* tmv, uint8_t* smem_raw, int bx,
                                          int kvh) {
-  using Lo = Layout<D, BN>;
-  constexpr int HALF = BN / 2;                 // keys per softmax warpgroup
-  constexpr int O0 = Lo::O_COL, O1 = Lo::O_COL + D;  // TMEM columns of O_0, O_1
-  static_assert(2 * BN + 2 * D <= Lo::TMEM_COLS, "TMEM budget");
-  // 1024-byte alignment of the swizzled tiles
+  using Lo = Layout3;
+  constexpr int D = Lo::D, BN = Lo::BN, NK = Lo::KSTAGES, NV = Lo::VSTAGES, NB = Lo::SBUF;
   const uint32_t raw = rxk::smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte alignment of the swizzled tiles
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + Lo::Q;
   const uint32_t bar = base + Lo::BAR;
-  auto BAR_Q = [&]() { return bar; };
+  const uint32_t BAR_Q = bar;
   auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
-  auto BAR_VF = [&](int s) { return bar + 8u * (3 + s); };
-  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (5 + s); };
-  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (7 + s); };
-  auto BAR_S = [&](int s) { return bar + 8u * (9 + s); };
-  auto BAR_P = [&](int s) { return bar + 8u * (11 + s); };
-  const uint32_t BAR_O = bar + 8u * 13;
-  const uint32_t BAR_FIN = bar + 8u * 14;
-  const uint32_t BAR_XE = bar + 8u * 15;  // epilogue exchange of (m_w, l_w)
+  auto BAR_VF = [&](int s) { return bar + 8u * (4 + s); };
+  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (6 + s); };
+  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (9 + s); };
+  auto BAR_S = [&](int b) { return bar + 8u * (11 + b); };
+  auto BAR_P = [&](int b) { return bar + 8u * (14 + b); };
+  const uint32_t BAR_O = bar + 8u * 17;
+  const uint32_t BAR_FIN = bar + 8u * 18;
+  auto XB = [&](int p) { return bar + 8u * (19 + p); };
+  const uint32_t XE = bar + 8u * 21;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
 
@@ -640,18 +680,24 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
 
   if (tid == 0) {
-    tc::mbar_init(BAR_Q(), 8 * 32);  // every softmax thread lands half a Q row
-    for (int s = 0; s < 2; ++s) {
+    tc::mbar_init(BAR_Q, 8 * 32);  // every softmax thread lands half a Q row
+    for (int s = 0; s < NK; ++s) {
       tc::mbar_init(BAR_KF(s), 1);
-      tc::mbar_init(BAR_VF(s), 1);
       tc::mbar_init(BAR_EMPTY_K(s), 1);
-      tc::mbar_init(BAR_EMPTY_V(s), 1);
-      tc::mbar_init(BAR_S(s), 1);
-      tc::mbar_init(BAR_P(s), 256);
     }
+    for (int s = 0; s < NV; ++s) {
+      tc::mbar_init(BAR_VF(s), 1);
+      tc::mbar_init(BAR_EMPTY_V(s), 1);
+    }
+    for (int b = 0; b < NB; ++b) {
+      tc::mbar_init(BAR_S(b), 1);
+      tc::mbar_init(BAR_P(b), 8 * 32);
+    }
+    tc::mbar_init(XB(0), 8 * 32);
+    tc::mbar_init(XB(1), 8 * 32);
+    tc::mbar_init(XE, 8 * 32);
     tc::mbar_init(BAR_O, 1);
     tc::mbar_init(BAR_FIN, 1);
-    tc::mbar_init(BAR_XE, 256);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -660,12 +706,13 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
-  tile2_sync();
+  __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
-    // ------------------------------------------------------------- loader
+  if (warp >= 9) {
+    // ------------------------------------------------------------- loaders
+    const bool load_v = warp == 10;
     // keys written by earlier kernels on the stream are read from here on
     rxk::griddep_wait();
     constexpr int CPR = D / 8;
@@ -739,23 +786,27 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
     load_slots(1, sb);
     load_slots(2, sc);
     load_slots(3, sd);
-    // tile j: K and V with the slots in `slot`, then tile j + 4's table reads
-    // into the same registers
+    // tile j (K stage j % NK, V stage j % NV): K and V with the slots in
+    // `slot`, then tile j + 4's table reads into the same registers; a stage
+    // is refilled once the MMA that read its previous tile has completed
     auto step = [&](int j, int32_t (&slot)[SPL]) -> bool {
-      const int s = j & 1;
+      const int sk = j % NK, sv = j % NV;
       check_slots(slot);
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(s), ((j - 2) >> 1) & 1, abort_flag,
-                                                  kWaitLimit, kSleepNs)))
-        return false;
-      load_tile(slot, tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
-      if (lane == 0) TC_TRACE(0, j);
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(s), ((j - 2) >> 1) & 1, abort_flag,
-                                                  kWaitLimit, kSleepNs)))
-        return false;
-      load_tile(slot, tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
-      if (lane == 0) TC_TRACE(2, j);
+      if (!load_v) {
+        if (j >= NK &&
+            !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(sk), uint32_t(j / NK - 1) & 1u,
+                                                    abort_flag, kWaitLimit, kSleepNs)))
+          return false;
+        load_tile(slot, tmk, kb, base + Lo::K0 + sk * Lo::KV_BYTES, BAR_KF(sk));
+        if (lane == 0) TC_TRACE(0, j);
+      } else {
+        if (j >= NV &&
+            !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(sv), uint32_t(j / NV - 1) & 1u,
+                                                    abort_flag, kWaitLimit, kSleepNs)))
+          return false;
+        load_tile(slot, tmv, vb, base + Lo::V0 + sv * Lo::KV_BYTES, BAR_VF(sv));
+        if (lane == 0) TC_TRACE(2, j);
+      }
       load_slots(j + 4, slot);
       return true;
     };
@@ -767,59 +818,52 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue
+    // S_j = Q K_j^T into S buffer j % 3 (two tiles ahead of the softmax), then
+    // O += P_j V_j with P_j from TMEM.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
       constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
-      bool ok = tc::mbar_wait(BAR_Q(), 0, abort_flag, kWaitLimit, kSleepNs);
-      auto issue_s = [&](int j) {
-        const int s = j & 1;
-        const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
+      bool ok = tc::mbar_wait(BAR_Q, 0, abort_flag, kWaitLimit, kSleepNs);
+      auto issue_s = [&](int j) -> bool {
+        const int sk = j % NK;
+        if (!tc::mbar_wait(BAR_KF(sk), uint32_t(j / NK) & 1u, abort_flag, kWaitLimit, kSleepNs))
+          return false;
+        TC_TRACE(1, j);
+        tc::tc_fence_after();
+        const uint32_t kt = base + Lo::K0 + sk * Lo::KV_BYTES;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = uint32_t((ks & 3) * 32);
           const uint64_t ad = tc::sdesc_sw128(sQ + (ks >> 2) * (BM * 128) + koff, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sk + (ks >> 2) * (BN * 128) + koff, 16, 1024);
-          tc::mma_bf16_ss(tmem + uint32_t(s * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+          const uint64_t bd = tc::sdesc_sw128(kt + (ks >> 2) * (BN * 128) + koff, 16, 1024);
+          tc::mma_bf16_ss(tmem + uint32_t((j % NB) * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
         }
-        tc::mma_commit(BAR_S(s));
-        tc::mma_commit(BAR_EMPTY_K(s));
+        tc::mma_commit(BAR_S(j % NB));
+        tc::mma_commit(BAR_EMPTY_K(sk));
         TC_TRACE(4, j);
+        return true;
       };
-      if (ok && n_tiles > 0) {
-        ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit, kSleepNs);
-        if (ok) {
-          tc::tc_fence_after();
-          issue_s(0);
-        }
-      }
+      for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_s(j);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j & 1;
-        if (j + 1 < n_tiles) {
-          if (!tc::mbar_wait(BAR_KF((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimit,
-                             kSleepNs))
-            break;
-          TC_TRACE(1, j + 1);
-          tc::tc_fence_after();
-          issue_s(j + 1);
-        }
-        if (!tc::mbar_wait(BAR_P(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
-        if (!tc::mbar_wait(BAR_VF(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
+        if (j + 2 < n_tiles && !issue_s(j + 2)) break;
+        const int sv = j % NV;
+        TC_TRACE(15, j);
+        if (!tc::mbar_wait(BAR_P(j % NB), uint32_t(j / NB) & 1u, abort_flag, kWaitLimit,
+                           kSleepNs))
+          break;
+        if (!tc::mbar_wait(BAR_VF(sv), uint32_t(j / NV) & 1u, abort_flag, kWaitLimit, kSleepNs))
+          break;
         TC_TRACE(3, j);
         tc::tc_fence_after();
-        const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
-        const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
-        // O_0 += P[:, keys of warpgroup 0] V[those keys], O_1 likewise
+        const uint32_t vt = base + Lo::V0 + sv * Lo::KV_BYTES;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t ad =
-              tc::sdesc_sw128(sp + (ks >> 2) * (BM * 128) + uint32_t((ks & 3) * 32), 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sv + uint32_t(ks * 2048), BN * 128, 1024);
-          const int half = ks / (HALF / 16);
-          tc::mma_bf16_ss(tmem + uint32_t(half ? O1 : O0), ad, bd, IDESC_PV,
-                          (j > 0 || ks != half * (HALF / 16)) ? 1u : 0u);
+          const uint64_t bd = tc::sdesc_sw128(vt + uint32_t(ks * 2048), BN * 128, 1024);
+          mma_bf16_ts(tmem + uint32_t(Lo::O_COL), tmem + uint32_t((j % NB) * BN + ks * 8), bd,
+                      IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(BAR_O);
-        tc::mma_commit(BAR_EMPTY_V(s));
+        tc::mma_commit(BAR_EMPTY_V(sv));
         TC_TRACE(5, j);
       }
       // drain: every MMA issued above has completed once this arrives
@@ -829,44 +873,50 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // Two warpgroups: warpgroup w (warps 4w .. 4w+3) owns keys [64 w, 64 w +
+    // 64) of every key tile for the same 128 rows (warp 4w + q reaches TMEM
+    // lanes 32 q ..).  Per tile the two halves of a row agree on the row max
+    // through shared memory (one bounded mbarrier round), so both write P
+    // against the same reference and share one O accumulator.
     const int wg = warp >> 2;
-    const int i = (warp & 3) * 32 + lane;  // query row = TMEM lane
+    const int i = (warp & 3) * 32 + lane;
+    constexpr int HALF = BN / 2;
     int64_t qi = 0, part = 0;
     int head = 0, lim = t.key_end;
     const bool valid = i < t.n_rows;
     if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
+    const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
+    float* xch = reinterpret_cast<float*>(gbase + Lo::XCH);  // [3][2 warpgroups][BM]
     // the queries and the outputs (decode: partial buffers the previous
     // merge read) are touched only once earlier kernels on the stream are done
     rxk::griddep_wait();
     {
-      // warpgroup w gathers half w of Q row i (zeros past the tile's rows)
-      // while the loader warp already streams the first K/V tiles
-      constexpr int CPR = D / 8;
+      // chunks [8 w, 8 w + 8) of Q row i (zeros past the tile's rows) while
+      // the loader warp already streams the first K/V tiles
       const bf16* src = a.q + (qi * a.hq + head) * D;
 #pragma unroll
-      for (int c = 0; c < CPR / 2; ++c) {
-        const int ch = wg * (CPR / 2) + c;
+      for (int c = 0; c < D / 16; ++c) {
+        const int ch = wg * (D / 16) + c;
         rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, valid);
       }
       rxk::cp_async_commit();
       rxk::cp_async_wait<0>();
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_Q());
+      tc::mbar_arrive(BAR_Q);
     }
-    const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
-    const uint32_t o_col = uint32_t(wg ? O1 : O0);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & 1;
+      const int s = j % NB;  // S buffer
       // waits are made warp-uniform before any warp-collective tcgen05 op
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR_S(s), (j >> 1) & 1, abort_flag, kWaitLimit))) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR_S(s), uint32_t(j / NB) & 1u, abort_flag,
+                                                  kWaitLimit))) {
         ok = false;
         break;
       }
       tc::tc_fence_after();
-      if (i == 0) TC_TRACE(wg ? 9 : 6, j);
-      const int k0 = t.key_begin + j * BN + wg * HALF;  // first key of this warpgroup's half
+      if (i == 0 && wg == 0) TC_TRACE(6, j);
+      const int k0 = t.key_begin + j * BN + wg * HALF;  // first key of this half
       const bool need_mask = k0 + HALF > t.nomask_end;
       uint32_t sr[HALF];
       tc::tmem_ld_row<HALF>(tl + uint32_t(s * BN + wg * HALF), sr);
@@ -888,17 +938,29 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
 #pragma unroll
         for (int e = 0; e < HALF; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
       }
-      const float raw_mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // a half whose keys are all masked for this row (possible for one
-      // warpgroup) leaves m_ref where it is; its p are then 0
-      const float mx = raw_mx > 0.5f * kMasked ? a.scale_log2 * raw_mx : -INFINITY;
+      const float mx_half = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // the other half's max of this row (parity-double-buffered slot: a thread
+      // reaches tile j + 2's write only after every thread has passed tile
+      // j + 1's exchange, hence has read tile j's)
+      xch[((j & 1) * 2 + wg) * BM + i] = mx_half;
+      tc::mbar_arrive(XB(j & 1));
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(XB(j & 1), (j >> 1) & 1, abort_flag, kWaitLimit))) {
+        ok = false;
+        break;
+      }
+      const float mx_other = xch[((j & 1) * 2 + (1 - wg)) * BM + i];
+      if (i == 0 && wg == 0) TC_TRACE(9, j);
+      const float mx = a.scale_log2 * fmaxf(mx_half, mx_other);
       const float m_new = fmaxf(m_ref, mx);
       if (j == 0) {
         m_ref = m_new;
       } else {
         const bool need = m_new > m_ref + kRescaleThreshold;
+        // both warps of a row quadrant see the same rows, so they agree
         if (__any_sync(0xffffffffu, need)) {
+          // O is rescaled once PV_{j-1} has written it; each warpgroup takes
+          // half of its columns
           if (!__all_sync(0xffffffffu,
                           tc::mbar_wait(BAR_O, (j - 1) & 1, abort_flag, kWaitLimit))) {
             ok = false;
@@ -907,15 +969,15 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
           tc::tc_fence_after();
           const float alpha = need ? rxk::fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t r[32];
-            tc::tmem_ld32(tl + o_col + uint32_t(cc * 32), r);
+            const uint32_t col = uint32_t(Lo::O_COL + wg * (D / 2) + cc * 32);
+            tc::tmem_ld32(tl + col, r);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tc::tmem_st32(tl + o_col + uint32_t(cc * 32), r);
+            tc::tmem_st32(tl + col, r);
           }
-          tc::tmem_st_wait();
           if (need) {
             l *= alpha;
             m_ref = m_new;
@@ -923,7 +985,6 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
         }
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
       float l8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) l8[u] = 0.f;
@@ -944,47 +1005,33 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
           l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
           pk[e >> 1] = h;
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t addr = sw128(sp, BM, i, wg * (HALF / 8) + cc * 4 + q);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(pk[4 * q]),
-                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                       : "memory");
-        }
+        // keys of this half, two per column, over the first 64 columns of
+        // S_j's buffer (half w at columns 32 w ..)
+        if (cc == HALF / 32 - 1 && i == 0 && wg == 0) TC_TRACE(12, j);
+        tmem_st16(tl + uint32_t(s * BN + wg * (HALF / 2) + 16 * cc), pk);
       }
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      if (i == 0 && wg == 0) TC_TRACE(13, j);
+      tc::tmem_st_wait();
       if (i == 0 && wg == 0) TC_TRACE(10, j);
-      tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       tc::mbar_arrive(BAR_P(s));
       if (i == 0) TC_TRACE(wg ? 11 : 7, j);
     }
     // The epilogue waits on BAR_FIN, which completes exactly once, after every
-    // MMA of the CTA (waiting on BAR_O's parity would be ambiguous).  Then the
-    // two warpgroups swap (m_w, l_w) of each row through shared memory (the P
-    // buffers are free by then) and warpgroup w writes output columns
-    // [w D/2, (w+1) D/2) of the merged row.
+    // MMA of the CTA (BAR_O's parity would be ambiguous), then the halves add
+    // their row sums through shared memory and warpgroup w writes output
+    // columns [64 w, 64 w + 64).  Every softmax thread arrives on the
+    // exchange barrier, so no waiter is left behind when a wait gave up.
     const bool fin = ok && n_tiles > 0 &&
                      __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit));
-    float* xch = reinterpret_cast<float*>(gbase + Lo::P0);  // [2 warpgroups][m, l][BM]
-    if (fin) {
-      xch[(wg * 2 + 0) * BM + i] = m_ref;
-      xch[(wg * 2 + 1) * BM + i] = l;
-    }
-    tc::mbar_arrive(BAR_XE);  // every softmax thread arrives, so no waiter is left behind
-    const bool xok = __all_sync(0xffffffffu, tc::mbar_wait(BAR_XE, 0, abort_flag, kWaitLimit));
+    if (fin) xch[(2 * 2 + wg) * BM + i] = l;
+    tc::mbar_arrive(XE);
+    const bool xok = __all_sync(0xffffffffu, tc::mbar_wait(XE, 0, abort_flag, kWaitLimit));
     if (fin && xok) {
       tc::tc_fence_after();
-      const float m_o = xch[((1 - wg) * 2 + 0) * BM + i];
-      const float l_o = xch[((1 - wg) * 2 + 1) * BM + i];
-      const float m_all = fmaxf(m_ref, m_o);
-      const float m_safe = m_all == -INFINITY ? 0.f : m_all;
-      const float c_me = m_ref == -INFINITY ? 0.f : rxk::fast_exp2(m_ref - m_safe);
-      const float c_ot = m_o == -INFINITY ? 0.f : rxk::fast_exp2(m_o - m_safe);
-      const float l_all = l * c_me + l_o * c_ot;
+      const float l_all = l + xch[(2 * 2 + (1 - wg)) * BM + i];
       const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
-      const float c0 = (wg ? c_ot : c_me) * inv;  // weight of O_0
-      const float c1 = (wg ? c_me : c_ot) * inv;  // weight of O_1
       float* dst;
       float* lse_dst;
       if constexpr (DECODE) {
@@ -997,26 +1044,23 @@ __device__ __forceinline__ void tc_tile2(const TcArgs& a, const CUtensorMap* tmk
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int col = wg * (D / 2) + cc * 32;
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld32(tl + uint32_t(O0 + col), r0);
-        tc::tmem_ld32(tl + uint32_t(O1 + col), r1);
+        uint32_t r[32];
+        tc::tmem_ld32(tl + uint32_t(Lo::O_COL + col), r);
         tc::tmem_ld_wait();
         if (valid) {
           float4* o4 = reinterpret_cast<float4*>(dst + col);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            o4[e] = make_float4(
-                __uint_as_float(r0[4 * e]) * c0 + __uint_as_float(r1[4 * e]) * c1,
-                __uint_as_float(r0[4 * e + 1]) * c0 + __uint_as_float(r1[4 * e + 1]) * c1,
-                __uint_as_float(r0[4 * e + 2]) * c0 + __uint_as_float(r1[4 * e + 2]) * c1,
-                __uint_as_float(r0[4 * e + 3]) * c0 + __uint_as_float(r1[4 * e + 3]) * c1);
+            o4[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                __uint_as_float(r[4 * e + 2]) * inv,
+                                __uint_as_float(r[4 * e + 3]) * inv);
         }
       }
-      if (valid && wg == 0) *lse_dst = m_safe * kLn2 + logf(l_all);
+      if (valid && wg == 0) *lse_dst = m_ref * kLn2 + logf(l_all);
     }
   }
   tc::tc_fence_before();
-  tile2_sync();
+  __syncthreads();
   if (tid == 0 && *abort_flag) atomicOr(&g_tc_error, 2);
   if (warp == 8) {
     tc::tc_fence_after();
@@ -1032,12 +1076,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_tile<D, BN, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
 }
 
-// Extend with the split-softmax tile (head_dim 128).
-__global__ void __launch_bounds__(kThreads2, 1)
-    attn_tc2_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
+// Extend with the tensor-memory operand tile (head_dim 128).
+__global__ void __launch_bounds__(kThreads3, 1)
+    attn_tc3_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  tc_tile2<128, 128, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
+  tc_tile3<false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
 }
 
 // ---------------------------------------------------------------------------
@@ -1338,7 +1382,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
 // Launched with programmatic stream serialization: the merge that follows may
 // launch early, and this kernel waits (griddepcontrol.wait) for the previous
 // kernels on the stream before it touches what they wrote or read.
-__global__ void __launch_bounds__(kThreads2, 1)
+__global__ void __launch_bounds__(kThreads3, 1)
     decode_fused_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1346,7 +1390,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int cta = int(blockIdx.x);
   if (cta < a.n_tc_ctas) {
     const int hkv = a.hq / a.group;
-    tc_tile2<128, 128, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
+    tc_tile3<true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
   }
   if (threadIdx.x >= kPipeWarps * 32) return;  // the warp role uses the first six warps
   rxk::griddep_wait();
@@ -1372,8 +1416,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
       pipe_unit<2>(a, ring, slot_buf, unit, gstep);
   }
 }
-static_assert(kPipeWarps * kWarpBytes + 1024 <= Layout<128, 128>::BYTES,
-              "warp-role rings fit the tensor-core tile's shared memory");
+// shared memory of a fused-kernel CTA: the tile's, or the warp role's rings
+constexpr int kFusedSmem =
+    Layout3::BYTES > kPipeWarps * kWarpBytes + 1024 ? Layout3::BYTES : kPipeWarps * kWarpBytes + 1024;
+static_assert(kFusedSmem <= 227 * 1024, "fused decode CTA fits in shared memory");
 static_assert(kRowPitch % 16 == 0 && kStageBytes % 16 == 0 && kWarpBytes % 16 == 0,
               "cp.async destinations stay 16-byte aligned");
 
@@ -1452,13 +1498,16 @@ bool pool_maps(const rx_pool_desc* d, int BN, const CUtensorMap** mk, const CUte
 template <int D, int BN>
 rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx,
                         unsigned gy, cudaStream_t s) {
-  constexpr int bytes = Layout<D, BN>::BYTES;
-  // head_dim 128: the split-softmax tile; 256: O_0 and O_1 would not fit in TMEM
-  constexpr bool split = D == 128;
+  // head_dim 128: Q and P in TMEM; 256: the S, O, Q and P columns would not fit
+  constexpr bool tmem_ops = D == 128;
+  constexpr int bytes = [] {
+    if constexpr (tmem_ops) return Layout3::BYTES;
+    else return Layout<D, BN>::BYTES;
+  }();
   static bool configured = false;
   if (!configured) {
-    if constexpr (split)
-      cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if constexpr (tmem_ops)
+      cudaFuncSetAttribute(attn_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     else
       cudaFuncSetAttribute(attn_tc_kernel<D, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            bytes);
@@ -1469,8 +1518,8 @@ rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsig
     return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   a.tma_row_base = int64_t(layer) * pool->num_kv_heads * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  if constexpr (split)
-    attn_tc2_kernel<<<dim3(gx, gy), kThreads2, bytes, s>>>(a, *tmk, *tmv);
+  if constexpr (tmem_ops)
+    attn_tc3_kernel<<<dim3(gx, gy), kThreads3, bytes, s>>>(a, *tmk, *tmv);
   else
     attn_tc_kernel<D, BN><<<dim3(gx, gy), kThreads, bytes, s>>>(a, *tmk, *tmv);
   return rx_internal::launch_status("extend attention (tcgen05)");
@@ -1540,7 +1589,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.slots_new = slots_new;
   a.tma_row_base = int64_t(layer) * hkv * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  constexpr int bytes = Layout<128, 128>::BYTES;
+  constexpr int bytes = kFusedSmem;
   static bool configured = false;
   if (!configured) {
     cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1551,7 +1600,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
     return set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(ctas));
-  cfg.blockDim = dim3(kThreads2);
+  cfg.blockDim = dim3(kThreads3);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
