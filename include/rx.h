@@ -292,10 +292,10 @@ typedef struct rx_decode_plan_info {
   int64_t workspace_bytes;   /* device scratch rx_decode_attention needs  */
   int64_t distinct_kv_tokens;/* distinct context tokens of the batch      */
   int64_t n_work_tc;      /* the last n_work_tc items have more than 16 rows
-                             and run on the tensor-core tile kernel       */
+                             and run on the tensor-core tile role        */
   int64_t tails_private;  /* 1: at every step of the plan each request's
                              newest token lies in a private tail run by the
-                             warp kernel (head_dim 128, group <= 16), so
+                             warp role (group <= 16), so
                              rx_decode_steps stores it inside that kernel */
 } rx_decode_plan_info;
 

@@ -1087,33 +1087,39 @@ __global__ void __launch_bounds__(kThreads3, 1)
 // ---------------------------------------------------------------------------
 // Warp role of the fused decode kernel: work items of <= 16 query rows (a
 // request's private tail, or a shared segment chunk with few rows), head_dim
-// 128.  One warp owns one (item, KV head) unit and streams its keys in steps
-// of 16.  With few query rows per item the products are computed transposed,
+// D = 128 or 256.  One warp owns one (item, KV head) unit and streams its keys
+// in steps of 16.  With few query rows per item the products are computed transposed,
 // keys in the M dimension of mma.sync m16n8k16 and query rows in N (8 or 16
 // rows, NR n-tiles), so no MMA row is wasted on keys:
-//   S^T (16 keys x 8 rows)  = K (16 x 128, ldmatrix)      . Q^T (registers)
-//   O^T (128 d x 8 rows)   += V^T (16 d x 16 keys per m-tile, ldmatrix.trans)
+//   S^T (16 keys x 8 rows)  = K (16 x D, ldmatrix)        . Q^T (registers)
+//   O^T (D x 8 rows)       += V^T (16 d x 16 keys per m-tile, ldmatrix.trans)
 //                             . P^T (the S^T accumulators, bf16, moved into
 //                               operand layout with four shuffles)
 // A thread of the S^T accumulators holds keys g, g+8 of rows 2c, 2c+1 (g =
 // lane/4, c = lane%4): the running max and sum of a row live in the 8 lanes
 // that share c.  K and V rows of a step are gathered by slot with 16-byte
-// cp.async into a ring of kPipeStages stages (kPipeStages - 1 steps in
-// flight) whose rows are padded to 272 B, so ldmatrix reads all 32 banks.
+// cp.async into a ring of PipeCfg<D>::STAGES stages (one fewer steps in
+// flight) whose rows are padded by 16 B, so ldmatrix reads all 32 banks.
 // The max is rescaled lazily: O and the sum are rescaled only when a row's
 // max grows by more than 2^8.
 constexpr int kPipeWarps = kThreads / 32;        // warps of a CTA in the warp role
-constexpr int kPipeStages = 4;                   // ring stages per warp
-constexpr int kRowPitch = 272;                   // shared bytes per K/V row
-constexpr int kStageBytes = 32 * kRowPitch;      // 16 K rows, then 16 V rows
 constexpr int kSlotBuf = 128;                    // key slots staged per refill (x 16 B aligned)
-constexpr int kWarpBytes = kPipeStages * kStageBytes + kSlotBuf * 4;
+template <int D>
+struct PipeCfg {
+  static constexpr int STAGES = D == 128 ? 4 : 2;     // ring stages per warp
+  static constexpr int PITCH = 2 * D + 16;            // shared bytes per K/V row
+  static constexpr int STAGE_BYTES = 32 * PITCH;      // 16 K rows, then 16 V rows
+  static constexpr int WARP_BYTES = STAGES * STAGE_BYTES + kSlotBuf * 4;
+};
 
-template <int NR>
+template <int NR, int D>
 __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_t* slot_buf,
                                           int unit, uint32_t& gstep) {
-  constexpr int D = 128;
-  constexpr int S = kPipeStages;
+  using Cfg = PipeCfg<D>;
+  constexpr int S = Cfg::STAGES;
+  constexpr int kRowPitch = Cfg::PITCH;
+  constexpr int kStageBytes = Cfg::STAGE_BYTES;
+  constexpr int NK = D / 16;  // k-steps of S^T, m-tiles of O^T
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int n_heads_kv = a.hq / a.group;
@@ -1138,7 +1144,10 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
       const int half = lane >> 4, ch = lane & 15;  // lanes 0-15: K, 16-31: V
       const bf16* src = (half ? a.v_new : a.k_new) + (b * n_heads_kv + kvh) * D;
       bf16* dst = const_cast<bf16*>(half ? vbase : kbase) + sl * D;
-      reinterpret_cast<uint4*>(dst)[ch] = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+#pragma unroll
+      for (int h = 0; h < D / 128; ++h)
+        reinterpret_cast<uint4*>(dst)[ch + 16 * h] =
+            __ldg(reinterpret_cast<const uint4*>(src) + ch + 16 * h);
     } else {
       atomicOr(&g_tc_error, 1);
     }
@@ -1164,9 +1173,10 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     __syncwarp();
   };
   if (n_steps > 0) fill_slots(0);
-  // step st of this unit: 16 K rows and 16 V rows of 256 B, gathered by slot
-  // with 16-byte cp.async (lane: chunk lane % 16 of rows 8 (lane / 16) + i);
-  // rows past the key range are zero-filled (P is 0 there, and 0 * V must be 0)
+  // step st of this unit: 16 K rows and 16 V rows of 2D bytes, gathered by
+  // slot with 16-byte cp.async (lane: chunks lane % 16 (+ 16 h) of rows
+  // 8 (lane / 16) + i); rows past the key range are zero-filled (P is 0
+  // there, and 0 * V must be 0)
   const int r0 = (lane >> 4) * 8;
   const char* ksrc = reinterpret_cast<const char*>(kbase) + (lane & 15) * 16;
   const int64_t v_minus_k = reinterpret_cast<const char*>(vbase) - reinterpret_cast<const char*>(kbase);
@@ -1184,16 +1194,20 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     for (int i = 0; i < 8; ++i) {
       const bool ok = sl[i] >= 0;
       const char* src = ksrc + int64_t(ok ? sl[i] : 0) * (D * 2);
-      rxk::cp_async_16(dst + uint32_t(i * kRowPitch), src, ok);
-      rxk::cp_async_16(dst + uint32_t((16 + i) * kRowPitch), src + v_minus_k, ok);
+#pragma unroll
+      for (int h = 0; h < D / 128; ++h) {
+        rxk::cp_async_16(dst + uint32_t(i * kRowPitch + 256 * h), src + 256 * h, ok);
+        rxk::cp_async_16(dst + uint32_t((16 + i) * kRowPitch + 256 * h), src + 256 * h + v_minus_k,
+                         ok);
+      }
     }
   };
 
-  float o[NR][8][4];
+  float o[NR][NK][4];
 #pragma unroll
   for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    for (int mt = 0; mt < NK; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
   float m_ref[NR][2], l_run[NR][2];
 #pragma unroll
   for (int nt = 0; nt < NR; ++nt) {
@@ -1209,7 +1223,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
 
   // Q^T operand, loaded while the first steps' keys are in flight: n-tile nt,
   // k-step kk: (d 16kk + 2c, +1 | 16kk + 2c + 8, +9) of row nt*8 + g
-  uint32_t qb[NR][8][2];
+  uint32_t qb[NR][NK][2];
 #pragma unroll
   for (int nt = 0; nt < NR; ++nt) {
     const int r = nt * 8 + g;
@@ -1221,7 +1235,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
       qrow = reinterpret_cast<const uint32_t*>(a.q + (b * a.hq + kvh * G + (r - u * G)) * D);
     }
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < NK; ++kk) {
       qb[nt][kk][0] = ok ? __ldg(qrow + 8 * kk + c) : 0u;
       qb[nt][kk][1] = ok ? __ldg(qrow + 8 * kk + c + 4) : 0u;
     }
@@ -1244,7 +1258,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < NK; ++kk) {
       uint32_t a0, a1, a2, a3;
       rxk::ldsm_x4(stage + k_lane + uint32_t(kk * 32), a0, a1, a2, a3);
 #pragma unroll
@@ -1296,7 +1310,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
             m_ref[nt][e] = mx[nt][e];
             l_run[nt][e] *= alpha;
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
+            for (int mt = 0; mt < NK; ++mt) {
               o[nt][mt][e] *= alpha;
               o[nt][mt][2 + e] *= alpha;
             }
@@ -1333,7 +1347,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     }
     // O^T += V^T . P^T
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+    for (int mt = 0; mt < NK; ++mt) {
       uint32_t a0, a1, a2, a3;
       rxk::ldsm_x4_t(stage + v_lane + uint32_t(mt * 32), a0, a1, a2, a3);
 #pragma unroll
@@ -1364,7 +1378,7 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
       float* dst = a.ws_o + (part * a.hq + head) * D;
       const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty chunk: zero partial, lse -inf
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
+      for (int mt = 0; mt < NK; ++mt) {
         dst[16 * mt + g] = o[nt][mt][e] * inv;
         dst[16 * mt + g + 8] = o[nt][mt][2 + e] * inv;
       }
@@ -1372,36 +1386,52 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     }
 }
 
-// One launch per decode step (head_dim 128), at most one CTA per SM.  CTAs
-// [0, n_tc_ctas) first run the tensor-core tile of one segment chunk with
-// more than 16 query rows (CTA c: item c / Hkv, KV head c % Hkv).  Then every
-// warp of every CTA takes warp-role units (an item of <= 16 rows and one KV
-// head) from a shared counter, heaviest first, until none is left; so the
-// SMs of finished tiles join the warp-role work and no CTA waits for a second
-// wave.  The counter starts at 0 and the merge after this kernel resets it.
-// Launched with programmatic stream serialization: the merge that follows may
-// launch early, and this kernel waits (griddepcontrol.wait) for the previous
-// kernels on the stream before it touches what they wrote or read.
-__global__ void __launch_bounds__(kThreads3, 1)
+// One launch per decode step, at most one CTA per SM.  CTAs [0, n_tc_ctas)
+// first run the tensor-core tile of one segment chunk with more than 16 query
+// rows (CTA c: item c / Hkv, KV head c % Hkv): head_dim 128 the 352-thread
+// tile with TMEM operands, head_dim 256 the 192-thread tile with 64-key
+// tiles.  Then the first six warps of every CTA take warp-role units (an item
+// of <= 16 rows and one KV head) from a shared counter, heaviest first, until
+// none is left; so the SMs of finished tiles join the warp-role work and no
+// CTA waits for a second wave.  The counter starts at 0 and the merge after
+// this kernel resets it.  Launched with programmatic stream serialization:
+// the merge that follows may launch early, and this kernel waits
+// (griddepcontrol.wait) for the previous kernels on the stream before it
+// touches what they wrote or read.
+template <int D>
+struct Fused {
+  static constexpr int THREADS = D == 128 ? kThreads3 : kThreads;
+  static constexpr int TILE_BYTES = D == 128 ? Layout3::BYTES : Layout<256, 64>::BYTES;
+  static constexpr int PIPE_BYTES = kPipeWarps * PipeCfg<D>::WARP_BYTES + 1024;
+  static constexpr int SMEM = TILE_BYTES > PIPE_BYTES ? TILE_BYTES : PIPE_BYTES;
+  static_assert(SMEM <= 227 * 1024, "fused decode CTA fits in shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(Fused<D>::THREADS, 1)
     decode_fused_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
+  using Cfg = PipeCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   rxk::griddep_launch_dependents();
   const int cta = int(blockIdx.x);
   if (cta < a.n_tc_ctas) {
     const int hkv = a.hq / a.group;
-    tc_tile3<true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
+    if constexpr (D == 128)
+      tc_tile3<true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
+    else
+      tc_tile<256, 64, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
   }
   if (threadIdx.x >= kPipeWarps * 32) return;  // the warp role uses the first six warps
   rxk::griddep_wait();
-  // warp role: this warp's ring, slot buffer and stage barriers
+  // warp role: this warp's ring and slot buffer
   const uint32_t raw = rxk::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const int warp = int(threadIdx.x >> 5);
   const int lane = int(threadIdx.x & 31);
-  const uint32_t ring = base + uint32_t(warp * kWarpBytes);
-  int32_t* slot_buf = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + warp * kWarpBytes +
-                                                 kPipeStages * kStageBytes);
+  const uint32_t ring = base + uint32_t(warp * Cfg::WARP_BYTES);
+  int32_t* slot_buf = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + warp * Cfg::WARP_BYTES +
+                                                 Cfg::STAGES * Cfg::STAGE_BYTES);
   const int hkv = a.hq / a.group;
   uint32_t gstep = 0;
   for (;;) {
@@ -1411,17 +1441,11 @@ __global__ void __launch_bounds__(kThreads3, 1)
     if (unit >= a.n_small_units) break;
     const int rows = a.work_small[int64_t(unit / hkv) * RX_WORK_WORDS + 6];
     if (rows <= 8)
-      pipe_unit<1>(a, ring, slot_buf, unit, gstep);
+      pipe_unit<1, D>(a, ring, slot_buf, unit, gstep);
     else
-      pipe_unit<2>(a, ring, slot_buf, unit, gstep);
+      pipe_unit<2, D>(a, ring, slot_buf, unit, gstep);
   }
 }
-// shared memory of a fused-kernel CTA: the tile's, or the warp role's rings
-constexpr int kFusedSmem =
-    Layout3::BYTES > kPipeWarps * kWarpBytes + 1024 ? Layout3::BYTES : kPipeWarps * kWarpBytes + 1024;
-static_assert(kFusedSmem <= 227 * 1024, "fused decode CTA fits in shared memory");
-static_assert(kRowPitch % 16 == 0 && kStageBytes % 16 == 0 && kWarpBytes % 16 == 0,
-              "cp.async destinations stay 16-byte aligned");
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1552,7 +1576,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                        float* ws_lse, int32_t* unit_counter, int step, const void* k_new,
                        const void* v_new, const int32_t* slots_new, cudaStream_t stream) {
   const int D = pool->head_dim;
-  if (D != 128) return set_error(RX_ERR_INVALID, "fused decode needs head_dim 128");
+  if (D != 128 && D != 256) return set_error(RX_ERR_INVALID, "decode needs head_dim 128 or 256");
   const int64_t hkv = pool->num_kv_heads;
   const int64_t small_units = n_small * hkv;
   const int64_t tc_ctas = n_tc * hkv;
@@ -1589,26 +1613,33 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.slots_new = slots_new;
   a.tma_row_base = int64_t(layer) * hkv * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  constexpr int bytes = kFusedSmem;
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    configured = true;
+  static bool configured[2] = {false, false};
+  if (!configured[D == 256]) {
+    if (D == 128)
+      cudaFuncSetAttribute(decode_fused_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Fused<128>::SMEM);
+    else
+      cudaFuncSetAttribute(decode_fused_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Fused<256>::SMEM);
+    configured[D == 256] = true;
   }
   const CUtensorMap *tmk, *tmv;
-  if (!pool_maps(pool, 128, &tmk, &tmv))
+  if (!pool_maps(pool, D == 128 ? 128 : 64, &tmk, &tmv))
     return set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(ctas));
-  cfg.blockDim = dim3(kThreads3);
-  cfg.dynamicSmemBytes = bytes;
+  cfg.blockDim = dim3(unsigned(D == 128 ? Fused<128>::THREADS : Fused<256>::THREADS));
+  cfg.dynamicSmemBytes = D == 128 ? Fused<128>::SMEM : Fused<256>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, *tmk, *tmv);
+  if (D == 128)
+    cudaLaunchKernelEx(&cfg, decode_fused_kernel<128>, a, *tmk, *tmv);
+  else
+    cudaLaunchKernelEx(&cfg, decode_fused_kernel<256>, a, *tmk, *tmv);
   return launch_status("decode attention (fused)");
 }
 

@@ -609,7 +609,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   const int32_t G = num_q_heads / num_kv_heads;
   if (head_dim != 128 && head_dim != 256)
     return fail(RX_ERR_INVALID, "rx_plan_decode: head_dim must be 128 or 256");
-  if (G > rx_internal::decode_rows_per_item(head_dim) || (head_dim == 256 && G > 64))
+  if (G > rx_internal::decode_rows_per_item(head_dim))
     return fail(RX_ERR_INVALID, "rx_plan_decode: group size %d above %d", G,
                 rx_internal::decode_rows_per_item(head_dim));
   std::vector<std::vector<const Node*>> paths(static_cast<size_t>(B));
@@ -636,7 +636,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   int64_t n_shared = 0;
   // every request's first-step token past its shared segments (the warp
   // kernel then owns each step's newest token)
-  bool tails_private = head_dim == 128 && G <= rx_internal::kDecodeSmallRows;
+  bool tails_private = G <= rx_internal::kDecodeSmallRows;
   for (int32_t b = 0; b < B; ++b) {
     const auto& path = paths[b];
     int64_t pos = 0;
@@ -664,10 +664,11 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     if (int64_t(ctx_len[b]) <= pos) tails_private = false;
     if (last > pos) segs.push_back(Seg{req_rows[b], pos, last, {b}, int64_t(ctx_len[b])});
   }
-  // work items: (key chunk, member block) of each segment.  head_dim 128:
-  // segments with <= kDecodeSmallRows rows go to the warp-pipelined kernel
-  // (listed first), larger ones to the tensor-core tile kernel in member blocks
-  // of <= kDecodeTcRows rows (listed last); head_dim 256: 64-row items.
+  // work items: (key chunk, member block) of each segment.  Segments with <=
+  // kDecodeSmallRows rows go to the warp role of the decode kernel (listed
+  // first), larger ones to its tensor-core tiles in member blocks of <=
+  // kDecodeTcRows rows (listed last); chunks are cut at the tile's key step
+  // (128 keys at head_dim 128, 64 at 256).
   struct Work {
     int32_t row, kb, ke, member_off, n_members, grow;
   };
@@ -682,21 +683,16 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     bool is_small;
     int32_t per_block;
     int64_t chunk, step;
-    if (head_dim == 128 && rows <= rx_internal::kDecodeSmallRows) {
+    if (rows <= rx_internal::kDecodeSmallRows) {
       is_small = true;
       per_block = k;
       chunk = std::max<int64_t>(rx_internal::kDecodeSmallChunk, 2 * rows);
       step = 16;
-    } else if (head_dim == 128) {
+    } else {
       is_small = false;
       per_block = rx_internal::kDecodeTcRows / G;
       chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 4 * rows);
-      step = 128;
-    } else {
-      is_small = false;
-      per_block = 64 / G;
-      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 2 * rows);
-      step = 64;
+      step = head_dim == 128 ? 128 : 64;
     }
     const int64_t n_chunks = (n + chunk - 1) / chunk;
     int64_t len = (n + n_chunks - 1) / n_chunks;
@@ -718,13 +714,8 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   std::stable_sort(small.begin(), small.end(), heavier);
   std::stable_sort(large.begin(), large.end(), heavier);
   std::vector<Work> work = small;
-  if (head_dim == 128) {
-    work.insert(work.end(), large.begin(), large.end());
-    info->n_work_tc = int64_t(large.size());
-  } else {
-    work.insert(work.end(), large.begin(), large.end());
-    info->n_work_tc = 0;
-  }
+  work.insert(work.end(), large.begin(), large.end());
+  info->n_work_tc = int64_t(large.size());
   std::vector<std::vector<int32_t>> parts_of(static_cast<size_t>(B));
   int64_t n_parts = 0;
   for (const Work& w : work) {

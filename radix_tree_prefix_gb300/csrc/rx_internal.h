@@ -8,14 +8,13 @@
 
 namespace rx_internal {
 
-// Decode work items (head_dim 128): segments with at most kDecodeSmallRows
-// query rows (members x group heads) go to the warp-pipelined kernel; larger
-// ones are cut into member blocks of at most kDecodeTcRows rows for the
-// tensor-core tile kernel.  head_dim 256 uses 64-row items of the shared-
-// memory tile kernel.
+// Decode work items: segments with at most kDecodeSmallRows query rows
+// (members x group heads) go to the warp role of the fused decode kernel;
+// larger ones are cut into member blocks of at most kDecodeTcRows rows for
+// its tensor-core tiles (both head dims).
 constexpr int kDecodeSmallRows = 16;
 constexpr int kDecodeTcRows = 128;
-inline int decode_rows_per_item(int head_dim) { return head_dim == 128 ? kDecodeTcRows : 64; }
+inline int decode_rows_per_item(int /*head_dim*/) { return kDecodeTcRows; }
 // Decode: a segment chunk is at least this many keys (and at least 2 keys per
 // query row, so partial results stay small next to the KV they summarise).
 constexpr int kDecodeMinChunk = 512;
@@ -39,11 +38,9 @@ rx_status launch_status(const char* what);
 int sm_count();
 // Error words of the kernels of each file: bit 0 = slot out of range.
 int32_t kv_store_error_flags(bool clear);
-int32_t attention_error_flags(bool clear);
 int32_t tc_error_flags(bool clear);
-// One decode step for head_dim 128 in a single launch: the tensor-core tiles
-// of the plan's large items and the warp-role units of its small items
-// (attention_tc.cu).  *unit_counter must be 0; the merge resets it.  k_new / v_new / slots_new non-NULL: the warp owning a
+// One decode step in a single launch: the tensor-core tiles of the plan's
+// large items and the warp-role units of its small items (attention_tc.cu).  *unit_counter must be 0; the merge resets it.  k_new / v_new / slots_new non-NULL: the warp owning a
 // request's newest token stores it first.  Launched with programmatic stream
 // serialization (the merge after it may launch early).
 rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,

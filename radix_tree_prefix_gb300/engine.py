@@ -387,7 +387,7 @@ class Engine:
         stores the new tokens itself), the decode kernel (head_dim 128: one
         fused launch for tensor-core and warp-role items), merge."""
         i = infos[0]
-        store = 0 if (int(i.tails_private) == 1 and self.wl.head_dim == 128) else 1
+        store = 0 if int(i.tails_private) == 1 else 1
         return store + int(int(i.n_work) > 0) + 1
 
     # ------------------------------------------------------------ timing

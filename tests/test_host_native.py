@@ -286,7 +286,7 @@ def test_multi_step_plan_covers_each_step_once():
 
 def test_tails_private_flag():
     """The in-kernel store of the newest token needs every request's newest
-    token in a private tail of the warp kernel; the plan says when it is."""
+    token in a private tail of the warp role; the plan says when it is."""
     c = rx.RadixCache(4096)
     toks = np.arange(1, 200, dtype=np.int32)
     slots = c.alloc(len(toks))
@@ -299,9 +299,10 @@ def test_tails_private_flag():
     # contexts past the cached prompts: private tails hold the newest tokens
     _, info = c.plan_decode([node, node2], [200, 161], [0, 1], 32, 8, 128, n_steps=4)
     assert info.tails_private == 1
-    # head_dim 256 or a group above 16 rows: the store stays a launch of its own
+    # head_dim 256 takes the same warp role
     _, info = c.plan_decode([node, node2], [200, 161], [0, 1], 32, 8, 256, n_steps=4)
-    assert info.tails_private == 0
+    assert info.tails_private == 1
+    # a group above 16 rows: the store stays a launch of its own
     _, info = c.plan_decode([node, node2], [200, 161], [0, 1], 32, 1, 128)
     assert info.tails_private == 0
     # a context that ends inside the shared segment (the caller passed the
