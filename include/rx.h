@@ -479,7 +479,9 @@ rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_t layer,
  * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel
  * read a slot outside [0, num_slots) from req_to_token and used slot 0
  * instead; bit 2 = a tensor-core kernel gave up a barrier wait after its
- * time limit (about 2 s) and returned without results.  Returns RX_ERR_CUDA
+ * time limit (about 2 s) and returned without results; bit 3 = a
+ * tensor-core tile found its dynamic shared memory off a 1024-byte boundary
+ * and returned without results.  Returns RX_ERR_CUDA
  * if a flag was set or the device reported an error. */
 rx_status rx_device_check(int32_t* out_flags);
 

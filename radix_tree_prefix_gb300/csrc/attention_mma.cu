@@ -253,7 +253,7 @@ extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, in
     const rx_decode_step& st = steps[i];
     // every step's new token is the end of a growing private tail: the decode
     // kernel's warp role stores it itself
-    const bool fused = B > 0 && G <= rx_internal::kDecodeSmallRows && st.info &&
+    const bool fused = B > 0 && G <= rx_internal::decode_small_rows(pool->head_dim) && st.info &&
                        st.info->tails_private == 1;
     if (!fused) {
       r = rx_kv_store(pool, layer, st.d_slots, st.d_k, st.d_v, B, stream);

@@ -1,7 +1,6 @@
-// S6-S8: extend attention and head_dim 128 decode attention.  The core is a
-// tile of 128 query rows over gathered pool KV on the 5th-generation tensor
-// cores (tcgen05, TMEM); decode adds a warp role for items of few rows, and
-// both run in one launch per decode step (decode_fused_kernel).
+// S6-S8: extend and decode attention on the 5th-generation tensor cores
+// (tcgen05, TMEM), plus the warp role that decode adds for work items of few
+// query rows; decode runs both in one launch per step (decode_fused_kernel).
 //
 // What is computed ("SGLang: Structured LLM Programs for Efficient
 // Inference", sections "A quick recap of how an LLM generates text" and "How
@@ -9,27 +8,29 @@
 // over its request's keys up to and including itself; reused prefix keys are
 // read from the slots the radix cache handed out, as if just computed.
 //
-// One CTA = 128 query rows that read one KV head over one key range:
+// One tile = 128 query rows that read one KV head over one key range:
 //   extend: rows = (suffix token, head in group) of one request, token-major,
 //           causal limit per row = prefix + token + 1;
 //   decode: rows = (member request, head in group) of a tree segment chunk
 //           shared by the members; writes partial (o, lse) per row.
-// Warp roles (192 threads; at most two warps per SM sub-partition, so the
-// softmax warps may use up to 255 registers):
-//   warps 0-3  softmax: thread i owns query row i = TMEM lane i; gathers its
-//              Q row into shared memory first; then reads S from
-//              TMEM, keeps the running max / sum, writes P (bf16) to shared
-//              memory, rescales O in TMEM when the max grows by more than 2^8
-//              (rare after the first tile), and writes the output;
-//   warp 4     allocates TMEM and issues tcgen05.mma from one thread:
-//              S_j = Q K_j^T (double-buffered in TMEM), O += P_j V_j (O stays
+// The tile (tc_tile3, 352 threads) streams K and V tiles of 32 KB (128 keys
+// at head_dim 128, 64 at head_dim 256):
+//   warps 0-7  softmax in two warpgroups that split every key tile's keys;
+//              thread (w, i) owns query row i = TMEM lane i; the two halves
+//              of a row agree on its max through shared memory; P (bf16)
+//              goes into TMEM over the S tile it came from; O is rescaled in
+//              TMEM when the max grows by more than 2^8 (rare after the
+//              first tile); then the output is written;
+//   warp 8     allocates TMEM and issues tcgen05.mma from one thread: S_j =
+//              Q K_j^T into a ring of three TMEM buffers, two tiles ahead of
+//              the softmax, and O += P_j V_j with P_j read from TMEM (O stays
 //              in TMEM for the whole key loop);
-//   warp 5     loads K/V tiles into 128-byte swizzled shared memory (two
-//              stages): a tile whose slots form one contiguous run (the
-//              allocator hands out runs, so this is the common case) is one TMA
-//              box load per 64 columns; any other tile, and the ragged last tile,
-//              is gathered slot by slot with 16-byte cp.async (rows past the key
-//              range are zero-filled).
+//   warps 9-10 load K and V into 128-byte swizzled shared memory (three and
+//              two stages): a tile whose slots form one contiguous run (the
+//              allocator hands out runs, so this is the common case) is one
+//              TMA box load per 64 columns; any other tile, and the ragged
+//              last tile, is gathered slot by slot with 16-byte cp.async
+//              (rows past the key range are zero-filled).
 // Every mbarrier wait is bounded (about 2 s); on a timeout the CTA sets an
 // error bit, drains its tensor-core work and frees TMEM before returning.
 
@@ -47,7 +48,8 @@
 #include "tc_util.cuh"
 
 // Bit 0: a slot outside [0, num_slots) was read (slot 0 used instead);
-// bit 1: a barrier wait timed out.  Read by rx_device_check().
+// bit 1: a barrier wait timed out; bit 2: a tile found its dynamic shared
+// memory off a 1024-byte boundary and did nothing.  Read by rx_device_check().
 static __device__ int32_t g_tc_error;
 
 #ifdef RX_TC_TRACE
@@ -79,7 +81,6 @@ constexpr float kRescaleThreshold = 8.0f;       // log2 units
 constexpr uint32_t kSleepNs = 0;                // MMA / loader waits: plain try_wait polling
 constexpr float kMasked = -1.0e30f;             // raw score of a masked key
 constexpr int BM = 128;
-constexpr int kThreads = 192;   // threads of a tensor-core tile
 
 struct TcArgs {
   const bf16* q;
@@ -111,7 +112,8 @@ struct TcArgs {
   // fused decode: warp-role items (<= 16 rows) and the step's new tokens
   const int32_t* work_small;
   int n_small_units;       // warp-role (item, KV head) units
-  int n_tc_ctas;           // tensor-core CTAs, listed first in the grid
+  int n_tc_ctas;           // tensor-core CTAs
+  int n_warp_first;        // warp-role-only CTAs placed before them
   int* unit_counter;       // next warp-role unit to take (0 at launch)
   int step;                // step index within a multi-step plan
   const bf16* k_new;       // bf16 [B][Hkv][D] of the step's tokens, or NULL
@@ -188,443 +190,53 @@ __device__ __forceinline__ uint32_t sw128(uint32_t base, int rows, int r, int ch
   return base + uint32_t((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
-template <int D, int BN>
-struct Layout {
-  static constexpr int Q = 0;
-  static constexpr int Q_BYTES = BM * D * 2;
-  static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int K0 = Q + Q_BYTES;
-  static constexpr int V0 = K0 + 2 * KV_BYTES;
-  static constexpr int P0 = V0 + 2 * KV_BYTES;
-  static constexpr int BAR = P0 + 2 * P_BYTES;
-  // barriers: q, kfull[2], vfull[2], emptyk[2], emptyv[2], s[2], p[2], o, final
-  static constexpr int NBAR = 15;
-  static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
-  static constexpr int BYTES = MISC + 16 + 1024;  // + alignment slack
-  static constexpr int TMEM_COLS = 512;
-  static constexpr int O_COL = 2 * BN;
-};
-
-// One 128-row tile (x = tile / work item, kvh = KV head) on 192 threads.
-template <int D, int BN, bool DECODE>
-__device__ __forceinline__ void tc_tile(const TcArgs& a, const CUtensorMap* tmk,
-                                        const CUtensorMap* tmv, uint8_t* smem_raw, int bx,
-                                        int kvh) {
-  using Lo = Layout<D, BN>;
-  static_assert(2 * BN + D <= Lo::TMEM_COLS, "TMEM budget");
-  // 1024-byte alignment of the swizzled tiles
-  const uint32_t raw = rxk::smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + Lo::Q;
-  const uint32_t bar = base + Lo::BAR;
-  auto BAR_Q = [&]() { return bar; };
-  auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
-  auto BAR_VF = [&](int s) { return bar + 8u * (3 + s); };
-  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (5 + s); };
-  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (7 + s); };
-  auto BAR_S = [&](int s) { return bar + 8u * (9 + s); };
-  auto BAR_P = [&](int s) { return bar + 8u * (11 + s); };
-  const uint32_t BAR_O = bar + 8u * 13;
-  const uint32_t BAR_FIN = bar + 8u * 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const TileDesc t = describe<DECODE>(a, bx);
-  const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
-
-  if (tid == 0) {
-    tc::mbar_init(BAR_Q(), 4 * 32);  // every softmax thread lands its Q row
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(BAR_KF(s), 1);
-      tc::mbar_init(BAR_VF(s), 1);
-      tc::mbar_init(BAR_EMPTY_K(s), 1);
-      tc::mbar_init(BAR_EMPTY_V(s), 1);
-      tc::mbar_init(BAR_S(s), 1);
-      tc::mbar_init(BAR_P(s), 128);
-    }
-    tc::mbar_init(BAR_O, 1);
-    tc::mbar_init(BAR_FIN, 1);
-    *abort_flag = 0;
-    tc::fence_barrier_init();
-  }
-  if (warp == 4) {
-    tc::tmem_alloc(rxk::smem_addr(tmem_slot), Lo::TMEM_COLS);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 5) {
-    // ------------------------------------------------------------- loader
-    // keys written by earlier kernels on the stream are read from here on
-    rxk::griddep_wait();
-    constexpr int CPR = D / 8;
-    constexpr int SPL = BN / 32;  // slots per lane: rows lane + 32 i
-    const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
-    const bf16* vb = a.vpool + int64_t(kvh) * a.head_stride;
-    const int64_t row0 = a.tma_row_base + int64_t(kvh) * a.tma_head_rows;
-    // slots of four consecutive tiles (tile j in ring j % 4): a tile's table
-    // reads are issued four tiles ahead into registers that nothing touches
-    // until then, so their round trips to L2 overlap the loads before them
-    int32_t sa[SPL], sb[SPL], sc[SPL], sd[SPL];
-    auto load_slots = [&](int j, int32_t (&dst)[SPL]) {
-      const int k0 = t.key_begin + j * BN;
-#pragma unroll
-      for (int i = 0; i < SPL; ++i) {
-        const int key = k0 + lane + 32 * i;
-        dst[i] = (j < n_tiles && key < t.key_end) ? __ldg(t.trow + key) : -1;
-      }
-    };
-    auto check_slots = [&](int32_t (&slot)[SPL]) {
-#pragma unroll
-      for (int i = 0; i < SPL; ++i) {
-        if (slot[i] >= a.num_slots || slot[i] < -1) {
-          atomicOr(&g_tc_error, 1);
-          slot[i] = 0;
-        }
-      }
-    };
-    // one K or V tile: TMA box loads if the slots are one contiguous run of
-    // BN valid slots, else a zero-filling cp.async gather
-    auto load_tile = [&](int32_t (&slot)[SPL], const CUtensorMap* tm, const bf16* src_base,
-                         uint32_t dst, uint32_t full_bar) {
-      const int32_t first = __shfl_sync(0xffffffffu, slot[0], 0);
-      bool run = first >= 0 && int64_t(first) + BN <= a.num_slots;
-#pragma unroll
-      for (int i = 0; i < SPL; ++i) run = run && (slot[i] == first + lane + 32 * i);
-      run = __all_sync(0xffffffffu, run);
-      if (run) {
-        if (lane == 0) {
-          tc::mbar_arrive_expect_tx(full_bar, uint32_t(BN * D * 2));
-#pragma unroll
-          for (int cb = 0; cb < D / 64; ++cb)
-            tc::tma_load_2d(dst + uint32_t(cb * BN * 128), tm, cb * 64, int(row0 + first),
-                            full_bar);
-        }
-      } else {
-        // lanes 0-15 and 16-31 copy chunks (lane % 16) + 16 h of rows 2k, 2k+1
-#pragma unroll
-        for (int i = 0; i < SPL; ++i) {
-#pragma unroll 4
-          for (int k = 0; k < 16; ++k) {
-            const int row = 32 * i + 2 * k + (lane >> 4);
-            const int32_t sl = __shfl_sync(0xffffffffu, slot[i], row & 31);
-            const bool ok = sl >= 0;
-            const int64_t s64 = ok ? int64_t(sl) : 0;
-#pragma unroll
-            for (int h = 0; h < CPR / 16; ++h) {
-              const int ch = (lane & 15) + 16 * h;
-              rxk::cp_async_16(sw128(dst, BN, row, ch), src_base + s64 * D + ch * 8, ok);
-            }
-          }
-        }
-        rxk::cp_async_commit();
-        rxk::cp_async_wait<0>();
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(full_bar);
-      }
-    };
-    load_slots(0, sa);
-    load_slots(1, sb);
-    load_slots(2, sc);
-    load_slots(3, sd);
-    // tile j: K and V with the slots in `slot`, then tile j + 4's table reads
-    // into the same registers
-    auto step = [&](int j, int32_t (&slot)[SPL]) -> bool {
-      const int s = j & 1;
-      check_slots(slot);
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(s), ((j - 2) >> 1) & 1, abort_flag,
-                                                  kWaitLimit, kSleepNs)))
-        return false;
-      load_tile(slot, tmk, kb, base + Lo::K0 + s * Lo::KV_BYTES, BAR_KF(s));
-      if (lane == 0) TC_TRACE(0, j);
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(s), ((j - 2) >> 1) & 1, abort_flag,
-                                                  kWaitLimit, kSleepNs)))
-        return false;
-      load_tile(slot, tmv, vb, base + Lo::V0 + s * Lo::KV_BYTES, BAR_VF(s));
-      if (lane == 0) TC_TRACE(2, j);
-      load_slots(j + 4, slot);
-      return true;
-    };
-    for (int j = 0; j < n_tiles; j += 4) {
-      if (!step(j, sa)) break;
-      if (j + 1 < n_tiles && !step(j + 1, sb)) break;
-      if (j + 2 < n_tiles && !step(j + 2, sc)) break;
-      if (j + 3 < n_tiles && !step(j + 3, sd)) break;
-    }
-  } else if (warp == 4) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
-      constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
-      bool ok = tc::mbar_wait(BAR_Q(), 0, abort_flag, kWaitLimit, kSleepNs);
-      auto issue_s = [&](int j) {
-        const int s = j & 1;
-        const uint32_t sk = base + Lo::K0 + s * Lo::KV_BYTES;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = uint32_t((ks & 3) * 32);
-          const uint64_t ad = tc::sdesc_sw128(sQ + (ks >> 2) * (BM * 128) + koff, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sk + (ks >> 2) * (BN * 128) + koff, 16, 1024);
-          tc::mma_bf16_ss(tmem + uint32_t(s * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(BAR_S(s));
-        tc::mma_commit(BAR_EMPTY_K(s));
-        TC_TRACE(4, j);
-      };
-      if (ok && n_tiles > 0) {
-        ok = tc::mbar_wait(BAR_KF(0), 0, abort_flag, kWaitLimit, kSleepNs);
-        if (ok) {
-          tc::tc_fence_after();
-          issue_s(0);
-        }
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j & 1;
-        if (j + 1 < n_tiles) {
-          if (!tc::mbar_wait(BAR_KF((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimit,
-                             kSleepNs))
-            break;
-          tc::tc_fence_after();
-          issue_s(j + 1);
-        }
-        if (!tc::mbar_wait(BAR_P(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
-        if (!tc::mbar_wait(BAR_VF(s), (j >> 1) & 1, abort_flag, kWaitLimit, kSleepNs)) break;
-        tc::tc_fence_after();
-        const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
-        const uint32_t sv = base + Lo::V0 + s * Lo::KV_BYTES;
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t ad =
-              tc::sdesc_sw128(sp + (ks >> 2) * (BM * 128) + uint32_t((ks & 3) * 32), 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sv + uint32_t(ks * 2048), BN * 128, 1024);
-          tc::mma_bf16_ss(tmem + uint32_t(Lo::O_COL), ad, bd, IDESC_PV,
-                          (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(BAR_O);
-        tc::mma_commit(BAR_EMPTY_V(s));
-        TC_TRACE(5, j);
-      }
-      // drain: every MMA issued above has completed once this arrives
-      tc::mma_commit(BAR_FIN);
-      tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int i = warp * 32 + lane;
-    int64_t qi = 0, part = 0;
-    int head = 0, lim = t.key_end;
-    const bool valid = i < t.n_rows;
-    if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
-    // the queries and the outputs (decode: partial buffers the previous
-    // merge read) are touched only once earlier kernels on the stream are done
-    rxk::griddep_wait();
-    {
-      // thread i gathers Q row i (zeros past the tile's rows) while the
-      // loader warp already streams the first K/V tiles
-      constexpr int CPR = D / 8;
-      const bf16* src = a.q + (qi * a.hq + head) * D;
-#pragma unroll
-      for (int ch = 0; ch < CPR; ++ch) rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, valid);
-      rxk::cp_async_commit();
-      rxk::cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_Q());
-    }
-    const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & 1;
-      // waits are made warp-uniform before any warp-collective tcgen05 op
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR_S(s), (j >> 1) & 1, abort_flag, kWaitLimit))) {
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
-      if (i == 0) TC_TRACE(6, j);
-      const int k0 = t.key_begin + j * BN;
-      const bool need_mask = k0 + BN > t.nomask_end;
-      // the whole S row of this thread, one TMEM round trip
-      uint32_t sr[BN];
-      tc::tmem_ld_row<BN>(tl + uint32_t(s * BN), sr);
-      tc::tmem_ld_wait();
-      if (i == 0) TC_TRACE(8, j);
-      // row max of the raw scores (masked keys get a large negative finite
-      // score, so the packed exponent below never sees an infinity); eight
-      // independent partial maxima keep the dependency chains short
-      float mx8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = kMasked;
-      if (need_mask) {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          if (k0 + e >= lim) sr[e] = __float_as_uint(kMasked);
-          mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sr[e]));
-      }
-      const float mx = a.scale_log2 *
-                       fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_ref, mx);
-      if (j == 0) {
-        m_ref = m_new;
-      } else {
-        const bool need = m_new > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          if (!__all_sync(0xffffffffu,
-                          tc::mbar_wait(BAR_O, (j - 1) & 1, abort_flag, kWaitLimit))) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const float alpha = need ? rxk::fast_exp2(m_ref - m_new) : 1.f;
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t r[32];
-            tc::tmem_ld32(tl + uint32_t(Lo::O_COL + cc * 32), r);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tc::tmem_st32(tl + uint32_t(Lo::O_COL + cc * 32), r);
-          }
-          tc::tmem_st_wait();
-          if (need) {
-            l *= alpha;
-            m_ref = m_new;
-          }
-        }
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const uint32_t sp = base + Lo::P0 + s * Lo::P_BYTES;
-      float l8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) l8[u] = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          // p = 2^(scale*s - m) for two keys at once: the exponents are rounded
-          // to bf16 with integer ops (add half an ulp, keep the high half) and
-          // one packed SFU op gives both p in bf16 (the precision P has in the
-          // PV product); the row sum adds exactly those values in fp32, in
-          // eight independent partial sums.
-          const float x0 = fmaf(__uint_as_float(sr[cc * 32 + e]), a.scale_log2, -m_use);
-          const float x1 = fmaf(__uint_as_float(sr[cc * 32 + e + 1]), a.scale_log2, -m_use);
-          const uint32_t h = rxk::exp2_bf16x2_bits(__float_as_uint(x0) + 0x8000u,
-                                                   __float_as_uint(x1) + 0x8000u);
-          l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
-          pk[e >> 1] = h;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t addr = sw128(sp, BM, i, cc * 4 + q);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(pk[4 * q]),
-                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                       : "memory");
-        }
-      }
-      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      if (i == 0) TC_TRACE(10, j);
-      tc::fence_proxy_async_smem();
-      if (i == 0) TC_TRACE(11, j);
-      tc::tc_fence_before();
-      tc::mbar_arrive(BAR_P(s));
-      if (i == 0) TC_TRACE(7, j);
-    }
-    // The epilogue waits on BAR_FIN, which completes exactly once, after every
-    // MMA of the CTA.  Waiting on BAR_O's parity here would be ambiguous: when
-    // this warp finishes its last tile, PV of the tile before may still run, and
-    // the last completed phase of BAR_O then has the parity of the last PV.
-    if (ok && n_tiles > 0 &&
-        __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit))) {
-      tc::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* dst;
-      float* lse_dst;
-      if constexpr (DECODE) {
-        dst = a.ws_o + (part * a.hq + head) * D;
-        lse_dst = a.ws_lse + part * a.hq + head;
-      } else {
-        dst = a.out + (qi * a.hq + head) * D;
-        lse_dst = a.lse + qi * a.hq + head;
-      }
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tc::tmem_ld32(tl + uint32_t(Lo::O_COL + cc * 32), r);
-        tc::tmem_ld_wait();
-        if (valid) {
-          float4* o4 = reinterpret_cast<float4*>(dst + cc * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o4[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                __uint_as_float(r[4 * e + 2]) * inv,
-                                __uint_as_float(r[4 * e + 3]) * inv);
-        }
-      }
-      if (valid) *lse_dst = m_ref * kLn2 + logf(l);
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  if (tid == 0 && *abort_flag) atomicOr(&g_tc_error, 2);
-  if (warp == 4) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, Lo::TMEM_COLS);
-  }
-}
-
-// Tensor-core tile for head_dim 128 (128 query rows, 128 keys per key
-// tile) on 320 threads.  The MMA warp keeps two S tiles ahead of the softmax:
-// S_{j+2} = Q K_{j+2}^T is issued before PV_j, into a ring of three S
-// buffers in TMEM, so the softmax of tile j+1 never waits for an MMA.  P_j
-// (bf16) overwrites the first 64 columns of S_j's buffer once the softmax
+// Tensor-core tile: 128 query rows, key tiles of BN = 128 keys at head_dim
+// 128 and 64 at head_dim 256 (a K or V tile is 32 KB either way), 352
+// threads.  The MMA warp keeps two S tiles ahead of the softmax: S_{j+2} =
+// Q K_{j+2}^T is issued before PV_j, into a ring of three S buffers in TMEM,
+// so the softmax of tile j+1 never waits for an MMA.  P_j (bf16, two keys per
+// column) overwrites the first BN/2 columns of S_j's buffer once the softmax
 // has read S_j, and PV_j reads it from TMEM as its A operand; tcgen05.mma
 // operations from one thread run in issue order, so S_{j+3} (issued after
 // PV_j) reuses that buffer only after PV_j read P_j.
-// TMEM: S ring [0, 384), O [384, 512).  Shared memory: Q (128-byte
-// swizzled, the A operand of S), K in three stages, V in two.
+// TMEM: S ring [0, 3 BN), O from column O_COL (D columns).  Shared memory: Q
+// (128-byte swizzled, the A operand of S), K in three stages, V in two.
 // Warps 0-7 softmax in two warpgroups that split each key tile's columns
-// (thread (w, i) of warpgroup w: row i = TMEM lane i, keys [64 w, 64 w + 64);
-// it also gathers chunks [8 w, 8 w + 8) of Q row i first), warp 8 issues
-// the MMAs, warp 9 loads K and warp 10 loads V (a V stage frees only when PV
-// of its previous tile completes, and K loads must not queue behind that).
+// (thread (w, i) of warpgroup w: row i = TMEM lane i, keys [w BN/2, (w+1)
+// BN/2); it also gathers half of Q row i first), warp 8 issues the MMAs,
+// warp 9 loads K and warp 10 loads V (a V stage frees only when PV of its
+// previous tile completes, and K loads must not queue behind that).
 constexpr int kThreads3 = 352;
 
+template <int HEAD_DIM>
 struct Layout3 {
-  static constexpr int D = 128, BN = 128, KSTAGES = 3, VSTAGES = 2, SBUF = 3;
+  static constexpr int D = HEAD_DIM;
+  static constexpr int BN = D == 128 ? 128 : 64;
+  static constexpr int KSTAGES = 3, VSTAGES = 2, SBUF = 3;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int Q = 0;
   static constexpr int K0 = Q + BM * D * 2;
   static constexpr int V0 = K0 + KSTAGES * KV_BYTES;
-  // exchange slots: per-tile half-row maxima (two parities) and the final
-  // row sums, [3][2 warpgroups][128 rows] floats
+  // exchange slots: per-tile half-row maxima, two parities, [2][2
+  // warpgroups][128 rows] floats; the final row sums reuse the parity that
+  // follows the last tile
   static constexpr int XCH = V0 + VSTAGES * KV_BYTES;
-  static constexpr int BAR = XCH + 3 * 2 * 128 * 4;
+  static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
   // barriers: q, kfull[3], vfull[2], emptyk[3], emptyv[2], s[3], p[3], o,
   // final, max exchange[2], sum exchange
   static constexpr int NBAR = 23;
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
-  static constexpr int BYTES = MISC + 16 + 1024;
+  // At head_dim 128 the layout carries 1024 bytes of slack to align the
+  // swizzled tiles.  At head_dim 256 it leaves 824 of the 227 KB a CTA may
+  // have, so the tile requires dynamic shared memory that starts on a
+  // 1024-byte boundary: a CTA that finds otherwise sets an error bit and
+  // returns without touching anything.
+  static constexpr bool SLACK = D == 128;
+  static constexpr int BYTES = MISC + 16 + (SLACK ? 1024 : 0);
   static constexpr int TMEM_COLS = 512;
-  static constexpr int O_COL = SBUF * BN;
-  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  static constexpr int O_COL = D == 128 ? SBUF * BN : 256;
+  static_assert(SBUF * BN <= O_COL && O_COL + D <= TMEM_COLS, "TMEM budget");
+  static_assert(BYTES <= 227 * 1024, "shared memory budget");
 };
 
 // D(tmem) (+)= A(tmem) * B(smem); issued by a single thread.
@@ -648,14 +260,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-template <bool DECODE>
+template <int D, bool DECODE>
 __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk,
                                          const CUtensorMap* tmv, uint8_t* smem_raw, int bx,
                                          int kvh) {
-  using Lo = Layout3;
-  constexpr int D = Lo::D, BN = Lo::BN, NK = Lo::KSTAGES, NV = Lo::VSTAGES, NB = Lo::SBUF;
+  using Lo = Layout3<D>;
+  constexpr int BN = Lo::BN, NK = Lo::KSTAGES, NV = Lo::VSTAGES, NB = Lo::SBUF;
   const uint32_t raw = rxk::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte alignment of the swizzled tiles
+  if constexpr (!Lo::SLACK) {
+    if (base != raw) {  // uniform over the CTA: nothing initialised yet
+      if (threadIdx.x == 0) atomicOr(&g_tc_error, 4);
+      return;
+    }
+  }
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + Lo::Q;
   const uint32_t bar = base + Lo::BAR;
@@ -886,7 +504,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     const bool valid = i < t.n_rows;
     if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
     const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
-    float* xch = reinterpret_cast<float*>(gbase + Lo::XCH);  // [3][2 warpgroups][BM]
+    float* xch = reinterpret_cast<float*>(gbase + Lo::XCH);  // [2][2 warpgroups][BM]
     // the queries and the outputs (decode: partial buffers the previous
     // merge read) are touched only once earlier kernels on the stream are done
     rxk::griddep_wait();
@@ -1005,8 +623,8 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
           l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
           pk[e >> 1] = h;
         }
-        // keys of this half, two per column, over the first 64 columns of
-        // S_j's buffer (half w at columns 32 w ..)
+        // keys of this half, two per column, over the first BN/2 columns
+        // of S_j's buffer (half w at columns w BN/4 ..)
         if (cc == HALF / 32 - 1 && i == 0 && wg == 0) TC_TRACE(12, j);
         tmem_st16(tl + uint32_t(s * BN + wg * (HALF / 2) + 16 * cc), pk);
       }
@@ -1025,12 +643,14 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // exchange barrier, so no waiter is left behind when a wait gave up.
     const bool fin = ok && n_tiles > 0 &&
                      __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit));
-    if (fin) xch[(2 * 2 + wg) * BM + i] = l;
+    // (a thread got here after every thread passed the exchange of tile
+    // n_tiles - 1, hence had read the slot of tile n_tiles - 2)
+    if (fin) xch[((n_tiles & 1) * 2 + wg) * BM + i] = l;
     tc::mbar_arrive(XE);
     const bool xok = __all_sync(0xffffffffu, tc::mbar_wait(XE, 0, abort_flag, kWaitLimit));
     if (fin && xok) {
       tc::tc_fence_after();
-      const float l_all = l + xch[(2 * 2 + (1 - wg)) * BM + i];
+      const float l_all = l + xch[((n_tiles & 1) * 2 + (1 - wg)) * BM + i];
       const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
       float* dst;
       float* lse_dst;
@@ -1068,26 +688,19 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   }
 }
 
-template <int D, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  tc_tile<D, BN, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
-}
-
-// Extend with the tensor-memory operand tile (head_dim 128).
+// Extend: one tile per CTA (x = row tile, y = KV head).
+template <int D>
 __global__ void __launch_bounds__(kThreads3, 1)
     attn_tc3_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  tc_tile3<false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
+  tc_tile3<D, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
 }
 
 // ---------------------------------------------------------------------------
-// Warp role of the fused decode kernel: work items of <= 16 query rows (a
-// request's private tail, or a shared segment chunk with few rows), head_dim
-// D = 128 or 256.  One warp owns one (item, KV head) unit and streams its keys
+// Warp role of the fused decode kernel: work items of <= 16 query rows at
+// head_dim 128, <= 8 at 256 (a request's private tail, or a shared segment
+// chunk with few rows).  One warp owns one (item, KV head) unit and streams its keys
 // in steps of 16.  With few query rows per item the products are computed transposed,
 // keys in the M dimension of mma.sync m16n8k16 and query rows in N (8 or 16
 // rows, NR n-tiles), so no MMA row is wasted on keys:
@@ -1102,7 +715,7 @@ __global__ void __launch_bounds__(kThreads3, 1)
 // flight) whose rows are padded by 16 B, so ldmatrix reads all 32 banks.
 // The max is rescaled lazily: O and the sum are rescaled only when a row's
 // max grows by more than 2^8.
-constexpr int kPipeWarps = kThreads / 32;        // warps of a CTA in the warp role
+constexpr int kPipeWarps = 6;                    // warps of a CTA in the warp role
 constexpr int kSlotBuf = 128;                    // key slots staged per refill (x 16 B aligned)
 template <int D>
 struct PipeCfg {
@@ -1386,22 +999,24 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     }
 }
 
-// One launch per decode step, at most one CTA per SM.  CTAs [0, n_tc_ctas)
-// first run the tensor-core tile of one segment chunk with more than 16 query
-// rows (CTA c: item c / Hkv, KV head c % Hkv): head_dim 128 the 352-thread
-// tile with TMEM operands, head_dim 256 the 192-thread tile with 64-key
-// tiles.  Then the first six warps of every CTA take warp-role units (an item
-// of <= 16 rows and one KV head) from a shared counter, heaviest first, until
-// none is left; so the SMs of finished tiles join the warp-role work and no
-// CTA waits for a second wave.  The counter starts at 0 and the merge after
-// this kernel resets it.  Launched with programmatic stream serialization:
-// the merge that follows may launch early, and this kernel waits
+// One launch per decode step, at most one CTA per SM.  CTAs [w, w + n_tc_ctas)
+// (w = n_warp_first) first run the tensor-core tile of one segment chunk with
+// more than 16 query rows (CTA w + c: item c / Hkv, KV head c % Hkv).  Then
+// the first six warps of every CTA take warp-role units (an item of <= 16
+// rows and one KV head) from a shared counter, heaviest first, until none is
+// left; so the SMs of finished tiles join the warp-role work.  When the tiles
+// alone fill more than one wave, the w CTAs before them take warp-role units
+// from the start, so the streaming of private tails (bound by HBM) runs
+// beside the first wave of tiles (bound by the tensor core and the
+// exponentials) instead of after it.  The counter starts at 0 and the merge
+// after this kernel resets it.  Launched with programmatic stream
+// serialization: the merge that follows may launch early, and this kernel waits
 // (griddepcontrol.wait) for the previous kernels on the stream before it
 // touches what they wrote or read.
 template <int D>
 struct Fused {
-  static constexpr int THREADS = D == 128 ? kThreads3 : kThreads;
-  static constexpr int TILE_BYTES = D == 128 ? Layout3::BYTES : Layout<256, 64>::BYTES;
+  static constexpr int THREADS = kThreads3;
+  static constexpr int TILE_BYTES = Layout3<D>::BYTES;
   static constexpr int PIPE_BYTES = kPipeWarps * PipeCfg<D>::WARP_BYTES + 1024;
   static constexpr int SMEM = TILE_BYTES > PIPE_BYTES ? TILE_BYTES : PIPE_BYTES;
   static_assert(SMEM <= 227 * 1024, "fused decode CTA fits in shared memory");
@@ -1414,13 +1029,10 @@ __global__ void __launch_bounds__(Fused<D>::THREADS, 1)
   using Cfg = PipeCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   rxk::griddep_launch_dependents();
-  const int cta = int(blockIdx.x);
-  if (cta < a.n_tc_ctas) {
+  const int cta = int(blockIdx.x) - a.n_warp_first;
+  if (cta >= 0 && cta < a.n_tc_ctas) {
     const int hkv = a.hq / a.group;
-    if constexpr (D == 128)
-      tc_tile3<true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
-    else
-      tc_tile<256, 64, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
+    tc_tile3<D, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
   }
   if (threadIdx.x >= kPipeWarps * 32) return;  // the warp role uses the first six warps
   rxk::griddep_wait();
@@ -1440,10 +1052,13 @@ __global__ void __launch_bounds__(Fused<D>::THREADS, 1)
     unit = __shfl_sync(0xffffffffu, unit, 0);
     if (unit >= a.n_small_units) break;
     const int rows = a.work_small[int64_t(unit / hkv) * RX_WORK_WORDS + 6];
-    if (rows <= 8)
+    if (rows <= 8) {
       pipe_unit<1, D>(a, ring, slot_buf, unit, gstep);
-    else
+    } else if constexpr (D == 128) {
       pipe_unit<2, D>(a, ring, slot_buf, unit, gstep);
+    } else if (lane == 0) {
+      atomicOr(&g_tc_error, 1);  // the plan gives head_dim 256 no such item
+    }
   }
 }
 
@@ -1519,33 +1134,22 @@ bool pool_maps(const rx_pool_desc* d, int BN, const CUtensorMap** mk, const CUte
   return true;
 }
 
-template <int D, int BN>
+template <int D>
 rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx,
                         unsigned gy, cudaStream_t s) {
-  // head_dim 128: Q and P in TMEM; 256: the S, O, Q and P columns would not fit
-  constexpr bool tmem_ops = D == 128;
-  constexpr int bytes = [] {
-    if constexpr (tmem_ops) return Layout3::BYTES;
-    else return Layout<D, BN>::BYTES;
-  }();
+  using Lo = Layout3<D>;
   static bool configured = false;
   if (!configured) {
-    if constexpr (tmem_ops)
-      cudaFuncSetAttribute(attn_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    else
-      cudaFuncSetAttribute(attn_tc_kernel<D, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           bytes);
+    cudaFuncSetAttribute(attn_tc3_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Lo::BYTES);
     configured = true;
   }
   const CUtensorMap *tmk, *tmv;
-  if (!pool_maps(pool, BN, &tmk, &tmv))
+  if (!pool_maps(pool, Lo::BN, &tmk, &tmv))
     return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   a.tma_row_base = int64_t(layer) * pool->num_kv_heads * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  if constexpr (tmem_ops)
-    attn_tc3_kernel<<<dim3(gx, gy), kThreads3, bytes, s>>>(a, *tmk, *tmv);
-  else
-    attn_tc_kernel<D, BN><<<dim3(gx, gy), kThreads, bytes, s>>>(a, *tmk, *tmv);
+  attn_tc3_kernel<D><<<dim3(gx, gy), kThreads3, Lo::BYTES, s>>>(a, *tmk, *tmv);
   return rx_internal::launch_status("extend attention (tcgen05)");
 }
 
@@ -1580,11 +1184,19 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   const int64_t hkv = pool->num_kv_heads;
   const int64_t small_units = n_small * hkv;
   const int64_t tc_ctas = n_tc * hkv;
-  // one wave: the tiles plus enough CTAs for the warp-role units, at most one
-  // CTA per SM beyond the tiles
-  const int64_t ctas = std::max<int64_t>(
-      tc_ctas, std::min<int64_t>(tc_ctas + (small_units + kPipeWarps - 1) / kPipeWarps,
-                                 rx_internal::sm_count()));
+  // the tiles plus CTAs for the warp-role units: when everything fits in one
+  // wave, enough of them for every unit (after the tiles); otherwise up to a
+  // quarter of the SMs, placed before the tiles so that they start at once
+  const int64_t sms = rx_internal::sm_count();
+  const int64_t unit_ctas = (small_units + kPipeWarps - 1) / kPipeWarps;
+  int64_t warp_first = 0, ctas = tc_ctas;
+  if (tc_ctas + unit_ctas <= sms)
+    ctas = tc_ctas + unit_ctas;
+  else if (tc_ctas >= sms)
+    warp_first = std::min<int64_t>(unit_ctas, (sms + 3) / 4);
+  else
+    ctas = sms;
+  ctas += warp_first;
   if (ctas == 0) return RX_OK;
   if (ctas > INT32_MAX) return set_error(RX_ERR_INVALID, "decode plan too large for one launch");
   TcArgs a{};
@@ -1606,6 +1218,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.work_small = d_work_small;
   a.n_small_units = int(small_units);
   a.n_tc_ctas = int(tc_ctas);
+  a.n_warp_first = int(warp_first);
   a.unit_counter = unit_counter;
   a.step = step;
   a.k_new = static_cast<const bf16*>(k_new);
@@ -1671,9 +1284,8 @@ rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const voi
   a.out = d_out;
   a.lse = d_lse;
   if (D == 128)
-    return launch_extend<128, 128>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads,
-                                   stream);
-  return launch_extend<256, 64>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
+    return launch_extend<128>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
+  return launch_extend<256>(a, pool, layer, unsigned(num_tiles), pool->num_kv_heads, stream);
 }
 
 }  // namespace rx_internal

@@ -158,13 +158,15 @@ extern "C" rx_status rx_device_check(int32_t* out_flags) {
     return rx_internal::set_error(RX_ERR_CUDA, buf);
   }
   const int32_t tcf = rx_internal::tc_error_flags(true);
-  int32_t f = rx_internal::kv_store_error_flags(true) | ((tcf & 1) << 1) | ((tcf & 2) << 1);
+  int32_t f = rx_internal::kv_store_error_flags(true) | ((tcf & 7) << 1);
   if (out_flags) *out_flags = f;
   if (f)
     return rx_internal::set_error(RX_ERR_CUDA,
-                                  (f & 4) ? "rx_device_check: a tensor-core kernel timed out "
-                                            "waiting on a barrier"
-                                          : "rx_device_check: a kernel met a slot outside the pool");
+                                  (f & 8)   ? "rx_device_check: a tensor-core tile found its "
+                                              "shared memory misaligned"
+                                  : (f & 4) ? "rx_device_check: a tensor-core kernel timed out "
+                                              "waiting on a barrier"
+                                            : "rx_device_check: a kernel met a slot outside the pool");
   return RX_OK;
 }
 

@@ -636,7 +636,8 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   int64_t n_shared = 0;
   // every request's first-step token past its shared segments (the warp
   // kernel then owns each step's newest token)
-  bool tails_private = G <= rx_internal::kDecodeSmallRows;
+  const int64_t small_rows = rx_internal::decode_small_rows(head_dim);
+  bool tails_private = G <= small_rows;
   for (int32_t b = 0; b < B; ++b) {
     const auto& path = paths[b];
     int64_t pos = 0;
@@ -665,7 +666,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     if (last > pos) segs.push_back(Seg{req_rows[b], pos, last, {b}, int64_t(ctx_len[b])});
   }
   // work items: (key chunk, member block) of each segment.  Segments with <=
-  // kDecodeSmallRows rows go to the warp role of the decode kernel (listed
+  // small_rows rows go to the warp role of the decode kernel (listed
   // first), larger ones to its tensor-core tiles in member blocks of <=
   // kDecodeTcRows rows (listed last); chunks are cut at the tile's key step
   // (128 keys at head_dim 128, 64 at 256).
@@ -683,7 +684,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     bool is_small;
     int32_t per_block;
     int64_t chunk, step;
-    if (rows <= rx_internal::kDecodeSmallRows) {
+    if (rows <= small_rows) {
       is_small = true;
       per_block = k;
       chunk = std::max<int64_t>(rx_internal::kDecodeSmallChunk, 2 * rows);

@@ -8,23 +8,21 @@
 
 namespace rx_internal {
 
-// Decode work items: segments with at most kDecodeSmallRows query rows
-// (members x group heads) go to the warp role of the fused decode kernel;
-// larger ones are cut into member blocks of at most kDecodeTcRows rows for
-// its tensor-core tiles (both head dims).
-constexpr int kDecodeSmallRows = 16;
+// Decode work items: segments with at most decode_small_rows(head_dim) query
+// rows (members x group heads) go to the warp role of the fused decode
+// kernel (16 rows at head_dim 128; 8 at head_dim 256, where the O^T
+// accumulators of 16 rows would not fit in the registers a warp of the
+// 352-thread CTA has); larger ones are cut into member blocks of at most
+// kDecodeTcRows rows for its tensor-core tiles.
+inline int decode_small_rows(int head_dim) { return head_dim == 128 ? 16 : 8; }
 constexpr int kDecodeTcRows = 128;
 inline int decode_rows_per_item(int /*head_dim*/) { return kDecodeTcRows; }
 // Decode: a segment chunk is at least this many keys (and at least 2 keys per
 // query row, so partial results stay small next to the KV they summarise).
 constexpr int kDecodeMinChunk = 512;
-// Decode: chunk of a <= 16-row item (one warp streams it, so shorter chunks
+// Decode: chunk of a warp-role item (one warp streams it, so shorter chunks
 // mean more warps in flight; the partial results stay small at <= 16 rows).
 constexpr int kDecodeSmallChunk = 128;
-// Decode chunks are cut at multiples of this many keys.
-constexpr int kDecodeKeyStep = 64;
-// Key tile of the attention kernels.
-constexpr int kKeyTile = 64;
 
 // Extend: query rows (query tokens x group heads) per CTA tile (the tcgen05
 // tile kernel owns 128 TMEM lanes = 128 rows).
@@ -40,8 +38,9 @@ int sm_count();
 int32_t kv_store_error_flags(bool clear);
 int32_t tc_error_flags(bool clear);
 // One decode step in a single launch: the tensor-core tiles of the plan's
-// large items and the warp-role units of its small items (attention_tc.cu).  *unit_counter must be 0; the merge resets it.  k_new / v_new / slots_new non-NULL: the warp owning a
-// request's newest token stores it first.  Launched with programmatic stream
+// large items and the warp-role units of its small items (attention_tc.cu).
+// *unit_counter must be 0; the merge resets it.  k_new / v_new / slots_new
+// non-NULL: the warp owning a request's newest token stores it first.  Launched with programmatic stream
 // serialization (the merge after it may launch early).
 rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                        int32_t num_q_heads, const int32_t* d_req_to_token, int64_t row_stride,

@@ -149,8 +149,9 @@ class _Staging:
     its previous copy has completed (event), so the host never blocks on the
     GPU in the common case."""
 
-    def __init__(self, torch, device, stream, n=4):
+    def __init__(self, torch, device, stream, explicit, n=4):
         self.torch, self.device, self.stream = torch, device, stream
+        self.explicit = explicit    # False: ``stream`` is the current stream
         self.host = [None] * n
         self.dev = [None] * n
         self.events = [None] * n
@@ -175,8 +176,11 @@ class _Staging:
             h[off:off + k] = a
             spans.append((off, k))
             off += k
-        stream = self.stream if self.stream is not None else torch.cuda.current_stream()
-        with torch.cuda.stream(stream):
+        stream = self.stream
+        if self.explicit:
+            with torch.cuda.stream(stream):
+                self.dev[i][:n].copy_(self.host[i][:n], non_blocking=True)
+        else:
             self.dev[i][:n].copy_(self.host[i][:n], non_blocking=True)
         ev = torch.cuda.Event()
         ev.record(stream)
@@ -190,7 +194,9 @@ class Engine:
 
     ``device=None`` runs the host bookkeeping only (no CUDA).  With a device,
     ``inputs`` supplies the Q/K/V of computed tokens and ``on_extend`` /
-    ``on_decode`` receive the attention outputs per layer.
+    ``on_decode`` receive the attention outputs per layer.  Every copy and
+    launch goes to ``stream``; left as None it is the device's current stream
+    when the engine is made, which must then stay current while it runs.
     """
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
@@ -202,6 +208,10 @@ class Engine:
         self.on_extend = on_extend
         self.on_decode = on_decode
         self.stream = stream
+        # launches with no explicit stream go to the device's current stream
+        # as of construction, resolved once (a lookup per launch costs more
+        # host time than some of the kernels it launches)
+        self._explicit_stream = stream is not None
         self.scale = 1.0 / math.sqrt(wl.head_dim)
         self.max_ctx = max(len(wl.prompt_tokens(r)) for r in wl.requests.values()) + \
             wl.decode_steps
@@ -212,6 +222,8 @@ class Engine:
         if device is not None:
             import torch
             self.torch = torch
+            if self.stream is None:
+                self.stream = torch.cuda.current_stream(device)
             L, hkv, d = wl.num_layers, wl.num_kv_heads, wl.head_dim
             self.k_pool = torch.empty((L, hkv, wl.num_slots, d), dtype=torch.bfloat16,
                                       device=device)
@@ -220,7 +232,7 @@ class Engine:
             self.d_table = torch.zeros((self.max_wave, self.max_ctx), dtype=torch.int32,
                                        device=device)
             self.d_ws = torch.empty(0, dtype=torch.uint8, device=device)
-            self.staging = _Staging(torch, device, stream)
+            self.staging = _Staging(torch, device, self.stream, self._explicit_stream)
         # host staging
         self.h_table = np.zeros((self.max_wave, self.max_ctx), dtype=np.int32)
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
@@ -384,8 +396,8 @@ class Engine:
 
     def _launches_per_decode(self, infos):
         """Kernels per decode step: kv_store (unless the decode kernel
-        stores the new tokens itself), the decode kernel (head_dim 128: one
-        fused launch for tensor-core and warp-role items), merge."""
+        stores the new tokens itself), the decode kernel (one fused launch
+        for tensor-core and warp-role items), merge."""
         i = infos[0]
         store = 0 if int(i.tails_private) == 1 else 1
         return store + int(int(i.n_work) > 0) + 1
@@ -395,14 +407,14 @@ class Engine:
         if not self.timing:
             return None
         e = self.torch.cuda.Event(enable_timing=True)
-        e.record(self.stream if self.stream is not None else self.torch.cuda.current_stream())
+        e.record(self.stream)
         return e
 
     def _event_end(self, start, kind, work):
         if start is None:
             return
         e = self.torch.cuda.Event(enable_timing=True)
-        e.record(self.stream if self.stream is not None else self.torch.cuda.current_stream())
+        e.record(self.stream)
         self.kernel_events.append((kind, start, e, work))
 
     def _extend_flops(self, prefix, qo):
