@@ -222,13 +222,13 @@ struct Layout3 {
   // follows the last tile
   static constexpr int XCH = V0 + VSTAGES * KV_BYTES;
   static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
-  // barriers: q, kfull[3], vfull[2], emptyk[3], emptyv[2], s[3], p[3], o,
-  // final, max exchange[2], sum exchange
-  static constexpr int NBAR = 23;
+  // barriers: q, kfull, vfull, emptyk, emptyv (one per stage), s[3], p[3],
+  // o, final, max exchange[2], sum exchange
+  static constexpr int NBAR = 1 + 2 * KSTAGES + 2 * VSTAGES + 2 * SBUF + 5;
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   // At head_dim 128 the layout carries 1024 bytes of slack to align the
-  // swizzled tiles.  At head_dim 256 it leaves 824 of the 227 KB a CTA may
-  // have, so the tile requires dynamic shared memory that starts on a
+  // swizzled tiles.  At head_dim 256 it leaves under 1 KB of the 227 KB a CTA
+  // may have, so the tile requires dynamic shared memory that starts on a
   // 1024-byte boundary: a CTA that finds otherwise sets an error bit and
   // returns without touching anything.
   static constexpr bool SLACK = D == 128;
@@ -278,16 +278,20 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const uint32_t sQ = base + Lo::Q;
   const uint32_t bar = base + Lo::BAR;
   const uint32_t BAR_Q = bar;
+  // barrier indices: q, kfull[NK], vfull[NV], emptyk[NK], emptyv[NV], s[NB],
+  // p[NB], o, final, max exchange[2], sum exchange
   auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
-  auto BAR_VF = [&](int s) { return bar + 8u * (4 + s); };
-  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (6 + s); };
-  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (9 + s); };
-  auto BAR_S = [&](int b) { return bar + 8u * (11 + b); };
-  auto BAR_P = [&](int b) { return bar + 8u * (14 + b); };
-  const uint32_t BAR_O = bar + 8u * 17;
-  const uint32_t BAR_FIN = bar + 8u * 18;
-  auto XB = [&](int p) { return bar + 8u * (19 + p); };
-  const uint32_t XE = bar + 8u * 21;
+  auto BAR_VF = [&](int s) { return bar + 8u * (1 + NK + s); };
+  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (1 + NK + NV + s); };
+  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (1 + 2 * NK + NV + s); };
+  auto BAR_S = [&](int b) { return bar + 8u * (1 + 2 * NK + 2 * NV + b); };
+  auto BAR_P = [&](int b) { return bar + 8u * (1 + 2 * NK + 2 * NV + NB + b); };
+  constexpr uint32_t kAfterP = 1 + 2 * NK + 2 * NV + 2 * NB;
+  const uint32_t BAR_O = bar + 8u * kAfterP;
+  const uint32_t BAR_FIN = bar + 8u * (kAfterP + 1);
+  auto XB = [&](int p) { return bar + 8u * (kAfterP + 2 + p); };
+  const uint32_t XE = bar + 8u * (kAfterP + 4);
+  static_assert(kAfterP + 5 == Lo::NBAR, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
 
@@ -296,6 +300,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const int lane = tid & 31;
   const TileDesc t = describe<DECODE>(a, bx);
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
+  if (tid == 0) TC_TRACE(14, 0);
 
   if (tid == 0) {
     tc::mbar_init(BAR_Q, 8 * 32);  // every softmax thread lands half a Q row
@@ -643,6 +648,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // exchange barrier, so no waiter is left behind when a wait gave up.
     const bool fin = ok && n_tiles > 0 &&
                      __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit));
+    if (i == 0 && wg == 0) TC_TRACE(14, 1);
     // (a thread got here after every thread passed the exchange of tile
     // n_tiles - 1, hence had read the slot of tile n_tiles - 2)
     if (fin) xch[((n_tiles & 1) * 2 + wg) * BM + i] = l;
@@ -661,23 +667,43 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         dst = a.out + (qi * a.hq + head) * D;
         lse_dst = a.lse + qi * a.hq + head;
       }
+      // Warpgroup w owns output columns [w D/2, (w+1) D/2).  Its rows go
+      // through shared memory (the K stages, idle once every MMA completed
+      // and every load landed) so that each warp then writes the 32 rows of
+      // its TMEM lane quadrant as whole contiguous row segments: one thread
+      // per row would make every store instruction touch 32 rows.
+      constexpr int HC = D / 2;           // columns per warpgroup
+      constexpr int PITCH = HC * 4 + 16;  // staged row bytes (+16: conflict-free)
+      constexpr int LPR = HC / 4;         // float4 per staged row
+      static_assert(2 * BM * PITCH <= Lo::XCH - Lo::K0, "staging fits in the K/V stages");
+      uint8_t* stage = gbase + Lo::K0 + wg * (BM * PITCH);
 #pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int col = wg * (D / 2) + cc * 32;
+      for (int cc = 0; cc < HC / 32; ++cc) {
         uint32_t r[32];
-        tc::tmem_ld32(tl + uint32_t(Lo::O_COL + col), r);
+        tc::tmem_ld32(tl + uint32_t(Lo::O_COL + wg * HC + cc * 32), r);
         tc::tmem_ld_wait();
-        if (valid) {
-          float4* o4 = reinterpret_cast<float4*>(dst + col);
+        float4* s4 = reinterpret_cast<float4*>(stage + i * PITCH + cc * 128);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o4[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                __uint_as_float(r[4 * e + 2]) * inv,
-                                __uint_as_float(r[4 * e + 3]) * inv);
-        }
+        for (int e = 0; e < 8; ++e)
+          s4[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                              __uint_as_float(r[4 * e + 2]) * inv,
+                              __uint_as_float(r[4 * e + 3]) * inv);
+      }
+      __syncwarp();
+      const int qrow = (warp & 3) * 32;  // first row of this warp's quadrant
+      const unsigned long long my_dst =
+          valid ? reinterpret_cast<unsigned long long>(dst + wg * HC) : 0ull;
+#pragma unroll 4
+      for (int k = 0; k < LPR; ++k) {
+        const int idx = k * 32 + lane;
+        const int rr = idx / LPR, c4 = idx - rr * LPR;  // row within the quadrant, float4
+        const unsigned long long rd = __shfl_sync(0xffffffffu, my_dst, rr);
+        const float4 v = *reinterpret_cast<const float4*>(stage + (qrow + rr) * PITCH + c4 * 16);
+        if (rd) reinterpret_cast<float4*>(rd)[c4] = v;
       }
       if (valid && wg == 0) *lse_dst = m_ref * kLn2 + logf(l_all);
     }
+    if (i == 0 && wg == 0) TC_TRACE(14, 2);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -686,6 +712,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Lo::TMEM_COLS);
   }
+  if (tid == 0) TC_TRACE(14, 3);
 }
 
 // Extend: one tile per CTA (x = row tile, y = KV head).
@@ -1160,6 +1187,8 @@ namespace rx_internal {
 #ifdef RX_TC_TRACE
 void tc_trace_read(unsigned long long* out) {
   cudaMemcpyFromSymbol(out, g_tc_trace, sizeof(g_tc_trace));
+  static unsigned long long zero[16 * 256];
+  cudaMemcpyToSymbol(g_tc_trace, zero, sizeof(g_tc_trace));
 }
 #endif
 

@@ -324,10 +324,11 @@ class Engine:
             out = torch.empty((total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
                               device=self.device)
             lse = torch.empty((total_q, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            call = rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, self.d_table,
+                                            d_rows, d_prefix, d_qo, d_tiles, R, n_tiles,
+                                            self.scale, out, lse, self.stream)
             ev = self._event_start()
-            rx.extend_attention(self.pool, layer, q, wl.num_q_heads, self.d_table, d_rows,
-                                d_prefix, d_qo, d_tiles, R, n_tiles, self.scale, out, lse,
-                                self.stream)
+            call()
             self._event_end(ev, "extend", flops)
             self.gpu_launches += 2
             outs[layer] = (out, lse)
