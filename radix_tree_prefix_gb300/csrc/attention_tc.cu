@@ -239,13 +239,28 @@ struct Layout3 {
   static_assert(BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// D(tmem) (+)= A(tmem) * B(smem); issued by a single thread.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
+// D(tmem) (+)= A * B(smem), A from shared memory (ss) or TMEM (ts), issued
+// by a single thread, with the shared-memory descriptors passed as 32-bit
+// halves: the high half (stride between 8-row groups, version, swizzle) is
+// common to every operand of the tile, and the low half (start address >> 4
+// and leading-byte offset) moves by compile-time steps, so the issuing thread
+// spends one add per operand instead of rebuilding 64-bit descriptors.
+__device__ __forceinline__ void mma_ss_split(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 ad, {%1, %3};\n mov.b64 bd, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_split(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 bd, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -446,48 +461,72 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
       constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
+      // shared-memory descriptors (128-byte swizzle, 1024 bytes between
+      // 8-row groups): common high half; low halves of Q, K stage 0 (K-major,
+      // leading offset 16 B) and V stage 0 (MN-major, leading offset = one
+      // 64-column block of BN rows)
+      constexpr uint32_t DHI = (1024u >> 4) | (1u << 14) | (2u << 29);
+      constexpr uint32_t KV_STEP = uint32_t(Lo::KV_BYTES) >> 4;
+      const uint32_t q_lo = ((sQ & 0x3FFFFu) >> 4) | (1u << 16);
+      const uint32_t k_lo0 = (((base + Lo::K0) & 0x3FFFFu) >> 4) | (1u << 16);
+      const uint32_t v_lo0 = (((base + Lo::V0) & 0x3FFFFu) >> 4) | (uint32_t(BN * 128 / 16) << 16);
+      static_assert(Lo::V0 + NV * Lo::KV_BYTES < (1 << 18), "descriptor address field");
       bool ok = tc::mbar_wait(BAR_Q, 0, abort_flag, kWaitLimit, kSleepNs);
+      // running stage indices and barrier phases: S_j's K stage, S buffer
+      // of the next S to issue; PV's V stage and S buffer
+      int ks_stage = 0, s_buf = 0;
+      uint32_t k_phase = 0;
       auto issue_s = [&](int j) -> bool {
-        const int sk = j % NK;
-        if (!tc::mbar_wait(BAR_KF(sk), uint32_t(j / NK) & 1u, abort_flag, kWaitLimit, kSleepNs))
+        if (!tc::mbar_wait(BAR_KF(ks_stage), k_phase, abort_flag, kWaitLimit, kSleepNs))
           return false;
         TC_TRACE(1, j);
         tc::tc_fence_after();
-        const uint32_t kt = base + Lo::K0 + sk * Lo::KV_BYTES;
+        const uint32_t k_lo = k_lo0 + uint32_t(ks_stage) * KV_STEP;
+        const uint32_t d_s = tmem + uint32_t(s_buf * BN);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = uint32_t((ks & 3) * 32);
-          const uint64_t ad = tc::sdesc_sw128(sQ + (ks >> 2) * (BM * 128) + koff, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(kt + (ks >> 2) * (BN * 128) + koff, 16, 1024);
-          tc::mma_bf16_ss(tmem + uint32_t((j % NB) * BN), ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+          const uint32_t a_off = uint32_t(((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4);
+          const uint32_t b_off = uint32_t(((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4);
+          mma_ss_split(d_s, q_lo + a_off, k_lo + b_off, DHI, IDESC_S, ks > 0 ? 1u : 0u);
         }
-        tc::mma_commit(BAR_S(j % NB));
-        tc::mma_commit(BAR_EMPTY_K(sk));
+        tc::mma_commit(BAR_S(s_buf));
+        tc::mma_commit(BAR_EMPTY_K(ks_stage));
         TC_TRACE(4, j);
+        if (++ks_stage == NK) {
+          ks_stage = 0;
+          k_phase ^= 1u;
+        }
+        if (++s_buf == NB) s_buf = 0;
         return true;
       };
       for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_s(j);
+      int sv = 0, pb = 0;
+      uint32_t v_phase = 0, p_phase = 0;
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 2 < n_tiles && !issue_s(j + 2)) break;
-        const int sv = j % NV;
         TC_TRACE(15, j);
-        if (!tc::mbar_wait(BAR_P(j % NB), uint32_t(j / NB) & 1u, abort_flag, kWaitLimit,
-                           kSleepNs))
-          break;
-        if (!tc::mbar_wait(BAR_VF(sv), uint32_t(j / NV) & 1u, abort_flag, kWaitLimit, kSleepNs))
-          break;
+        if (!tc::mbar_wait(BAR_P(pb), p_phase, abort_flag, kWaitLimit, kSleepNs)) break;
+        if (!tc::mbar_wait(BAR_VF(sv), v_phase, abort_flag, kWaitLimit, kSleepNs)) break;
         TC_TRACE(3, j);
         tc::tc_fence_after();
-        const uint32_t vt = base + Lo::V0 + sv * Lo::KV_BYTES;
+        const uint32_t v_lo = v_lo0 + uint32_t(sv) * KV_STEP;
+        const uint32_t p_t = tmem + uint32_t(pb * BN);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bd = tc::sdesc_sw128(vt + uint32_t(ks * 2048), BN * 128, 1024);
-          mma_bf16_ts(tmem + uint32_t(Lo::O_COL), tmem + uint32_t((j % NB) * BN + ks * 8), bd,
-                      IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts_split(tmem + uint32_t(Lo::O_COL), p_t + uint32_t(ks * 8),
+                       v_lo + uint32_t(ks * 2048 / 16), DHI, IDESC_PV,
+                       (j > 0 || ks > 0) ? 1u : 0u);
         tc::mma_commit(BAR_O);
         tc::mma_commit(BAR_EMPTY_V(sv));
         TC_TRACE(5, j);
+        if (++sv == NV) {
+          sv = 0;
+          v_phase ^= 1u;
+        }
+        if (++pb == NB) {
+          pb = 0;
+          p_phase ^= 1u;
+        }
       }
       // drain: every MMA issued above has completed once this arrives
       tc::mma_commit(BAR_FIN);
