@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "extend query-tok/s and decode attn GB/s (% of GB300 HBM peak) on radix KV pool"
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 126 << 20            # GB300 L2 capacity
 
 
 def parse():
@@ -50,14 +51,13 @@ def parse():
 
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
-# captures summarised in profiles/ (cold L2, one launch): decode_fused_kernel
-# on an agent_loop decode step and on a long_shared decode step, and the
-# second agent_loop extend launch.  Bytes per launch, or None where no capture
-# of the current kernel exists.
+# captures summarised in profiles/ (cold L2, one launch of the current
+# kernels): decode_fused_kernel on an agent_loop decode step and on a
+# long_shared decode step.  None (absent) where no capture of that launch
+# exists.
 TRAFFIC = {
-    ("agent_loop", "rx_decode_attention"): 45.5e6 + 0.03e6,
-    ("long_shared", "rx_decode_attention"): 418.5e6 + 36.3e6,
-    ("agent_loop", "rx_extend_attention"): 104.7e6 + 73.8e6,
+    ("agent_loop", "rx_decode_attention"): 44.52e6 + 0.06e6,
+    ("long_shared", "rx_decode_attention"): 415.7e6 + 37.8e6,
 }
 
 
@@ -330,12 +330,14 @@ def main():
         "tflops": ext_tflops, "frac_of_bf16_peak": ext_tflops / bf16_peak,
         "ms_per_step": ext["ms"] / args.steps, "launches_per_step": ext["launches"] / args.steps,
         "flop_per_step": ext["work"] / args.steps}
+    n_dec_launches = args.steps * len(wl.waves) * wl.decode_steps * len(layers)
     decode_info = {
         "gbs": dec_gbs, "frac_of_hbm_peak": dec_gbs / hbm_peak,
         "ms_per_step": dec["ms"] / args.steps, "launches_per_step": dec["launches"] / args.steps,
         "bytes_per_step": dec["work"] / args.steps,
-        "note": "decode working set fits in L2; L2 is flushed between steps only, so "
-                "later decode steps of a step read KV that is partly L2-resident (effective GB/s)"}
+        "note": ("decode working set fits in L2; L2 is flushed between steps only, so "
+                 "later decode steps of a step read KV that is partly L2-resident (effective GB/s)")
+        if dec["launches"] and dec["work"] / max(1, n_dec_launches) < L2_BYTES else None}
     if ext["ms"] >= dec["ms"]:
         roof = {"kernel": "rx_extend_attention", "bound": "tensor", "achieved": ext_tflops,
                 "peak": bf16_peak, "unit": "TFLOP/s", "frac": ext_tflops / bf16_peak,

@@ -196,6 +196,15 @@ def multi_turn_chat(seed=BASE_SEED, sessions=256, turns=8, system=2000,
                     distinct + 1, decode_steps, s.tokens, waves, seed)
 
 
+def multi_turn_chat_small(seed=BASE_SEED):
+    """multi_turn_chat cut to 32 sessions x 2 turns: the same head_dim-256
+    kernel shapes per launch with a few GB on the device, for profiler
+    captures of single launches."""
+    wl = multi_turn_chat(seed, sessions=32, turns=2)
+    wl.name = "multi_turn_chat_small"
+    return wl
+
+
 def fork_tree(seed=BASE_SEED, branching=5, depth=4, level_tokens=512,
               decode_steps=16, pool_fraction=0.6, q_heads=32, kv_heads=8,
               head_dim=128):
@@ -246,6 +255,7 @@ WORKLOADS = {
     "nested_share": nested_share,
     "agent_loop": agent_loop,
     "multi_turn_chat": multi_turn_chat,
+    "multi_turn_chat_small": multi_turn_chat_small,
     "fork_tree": fork_tree,
     "long_shared": long_shared,
 }
