@@ -673,6 +673,19 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   struct Work {
     int32_t row, kb, ke, member_off, n_members, grow;
   };
+  // chunk of the warp-role items: the longest that keeps enough units
+  int64_t small_chunk = rx_internal::kDecodeSmallChunkMin;
+  for (int64_t c = rx_internal::kDecodeSmallChunkMax; c > rx_internal::kDecodeSmallChunkMin;
+       c /= 2) {
+    int64_t units = 0;
+    for (const Seg& s : segs)
+      if (int64_t(s.members.size()) * G <= small_rows)
+        units += (s.ke - s.kb + c - 1) / c * num_kv_heads;
+    if (units >= int64_t(rx_internal::kDecodeWarpSlots) * rx_internal::kDecodeUnitsPerWarp) {
+      small_chunk = c;
+      break;
+    }
+  }
   std::vector<Work> small, large;
   std::vector<int32_t> members;
   int64_t distinct = 0;
@@ -687,12 +700,13 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     if (rows <= small_rows) {
       is_small = true;
       per_block = k;
-      chunk = std::max<int64_t>(rx_internal::kDecodeSmallChunk, 2 * rows);
+      chunk = std::max<int64_t>(small_chunk, 2 * rows);
       step = 16;
     } else {
       is_small = false;
       per_block = rx_internal::kDecodeTcRows / G;
-      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk, 4 * rows);
+      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk,
+                                rx_internal::kDecodeKeysPerRow * rows);
       step = head_dim == 128 ? 128 : 64;
     }
     const int64_t n_chunks = (n + chunk - 1) / chunk;

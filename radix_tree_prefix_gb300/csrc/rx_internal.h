@@ -17,12 +17,20 @@ namespace rx_internal {
 inline int decode_small_rows(int head_dim) { return head_dim == 128 ? 16 : 8; }
 constexpr int kDecodeTcRows = 128;
 inline int decode_rows_per_item(int /*head_dim*/) { return kDecodeTcRows; }
-// Decode: a segment chunk is at least this many keys (and at least 2 keys per
-// query row, so partial results stay small next to the KV they summarise).
+// Decode: a tensor-core chunk is at least this many keys, and at least 8
+// keys per query row (fewer, longer tile CTAs: each pays about 4 us of
+// start-up and epilogue, and writes 128 rows of partial results).
 constexpr int kDecodeMinChunk = 512;
-// Decode: chunk of a warp-role item (one warp streams it, so shorter chunks
-// mean more warps in flight; the partial results stay small at <= 16 rows).
-constexpr int kDecodeSmallChunk = 128;
+constexpr int kDecodeKeysPerRow = 8;
+// Decode: a warp-role item's chunk is the largest of 128, 256, 512 and 1024
+// keys that still leaves at least kDecodeUnitsPerWarp units (item x KV head)
+// per warp-role warp of the GPU (152 SMs x 6 warps): long chunks spread a
+// unit's start-up (work item, slot table, first K/V round trips) over more
+// keys, short ones keep every warp busy when the batch has few private keys.
+constexpr int kDecodeSmallChunkMin = 128;
+constexpr int kDecodeSmallChunkMax = 1024;
+constexpr int kDecodeWarpSlots = 152 * 6;
+constexpr int kDecodeUnitsPerWarp = 2;
 
 // Extend: query rows (query tokens x group heads) per CTA tile (the tcgen05
 // tile kernel owns 128 TMEM lanes = 128 rows).
