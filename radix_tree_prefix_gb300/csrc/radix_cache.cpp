@@ -686,6 +686,25 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
       break;
     }
   }
+  // chunks of the tensor-core items: kDecodeKeysPerRow keys per row (at
+  // least kDecodeMinChunk), times the smallest power of two that keeps the
+  // tile CTAs at or below kDecodeTcCap
+  auto tc_base_chunk = [&](int64_t rows) {
+    return std::max<int64_t>(rx_internal::kDecodeMinChunk, rx_internal::kDecodeKeysPerRow * rows);
+  };
+  int64_t tc_scale = 1;
+  for (; tc_scale < 64; tc_scale *= 2) {
+    int64_t ctas = 0;
+    for (const Seg& s : segs) {
+      const int64_t rows = int64_t(s.members.size()) * G;
+      if (rows <= small_rows) continue;
+      const int64_t per_block = rx_internal::kDecodeTcRows / G;
+      const int64_t blocks = (int64_t(s.members.size()) + per_block - 1) / per_block;
+      const int64_t c = tc_base_chunk(rows) * tc_scale;
+      ctas += (s.ke - s.kb + c - 1) / c * blocks * num_kv_heads;
+    }
+    if (ctas <= rx_internal::kDecodeTcCap) break;
+  }
   std::vector<Work> small, large;
   std::vector<int32_t> members;
   int64_t distinct = 0;
@@ -705,8 +724,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     } else {
       is_small = false;
       per_block = rx_internal::kDecodeTcRows / G;
-      chunk = std::max<int64_t>(rx_internal::kDecodeMinChunk,
-                                rx_internal::kDecodeKeysPerRow * rows);
+      chunk = tc_base_chunk(rows) * tc_scale;
       step = head_dim == 128 ? 128 : 64;
     }
     const int64_t n_chunks = (n + chunk - 1) / chunk;

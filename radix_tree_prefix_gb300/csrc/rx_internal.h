@@ -17,11 +17,15 @@ namespace rx_internal {
 inline int decode_small_rows(int head_dim) { return head_dim == 128 ? 16 : 8; }
 constexpr int kDecodeTcRows = 128;
 inline int decode_rows_per_item(int /*head_dim*/) { return kDecodeTcRows; }
-// Decode: a tensor-core chunk is at least this many keys, and at least 8
-// keys per query row (fewer, longer tile CTAs: each pays about 4 us of
-// start-up and epilogue, and writes 128 rows of partial results).
+// Decode: a tensor-core chunk is at least kDecodeMinChunk keys and at least
+// kDecodeKeysPerRow keys per query row of its segment (each tile CTA pays
+// about 4 us of start-up and epilogue and writes 128 rows of partial
+// results, so chunks are long); when that still gives more than
+// kDecodeTcCap tile CTAs, every chunk is doubled until it does not (the
+// tiles then run in about one wave beside the warp-role CTAs placed first).
 constexpr int kDecodeMinChunk = 512;
 constexpr int kDecodeKeysPerRow = 8;
+constexpr int kDecodeTcCap = 128;
 // Decode: a warp-role item's chunk is the largest of 128, 256, 512 and 1024
 // keys that still leaves at least kDecodeUnitsPerWarp units (item x KV head)
 // per warp-role warp of the GPU (152 SMs x 6 warps): long chunks spread a
