@@ -40,17 +40,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// Contiguous (non-tensor) bulk copy of `bytes` (a multiple of 16, both
-// addresses 16-byte aligned) from global into this CTA's shared memory;
-// completion is signalled as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 // try_wait with a suspend-time hint: the thread may sleep (issuing nothing)
 // until the phase completes or about `ns` nanoseconds pass.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
@@ -106,11 +95,6 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------------ fences
-// Orders this thread's earlier generic-proxy global writes before later
-// async-proxy (bulk copy) reads of the same memory.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;\n" ::: "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
