@@ -782,18 +782,57 @@ __global__ void __launch_bounds__(kThreads3, 1)
 // The max is rescaled lazily: O and the sum are rescaled only when a row's
 // max grows by more than 2^8.
 constexpr int kPipeWarps = 6;                    // warps of a CTA in the warp role
-constexpr int kSlotBuf = 128;                    // key slots staged per refill (x 16 B aligned)
+constexpr int kSlotBuf = 128;                    // key slots per slot block (x 16 B aligned)
+constexpr int kSlotRegs = kSlotBuf / 32;         // slots of a block per lane
 template <int D>
 struct PipeCfg {
   static constexpr int STAGES = D == 128 ? 4 : 2;     // ring stages per warp
   static constexpr int PITCH = 2 * D + 16;            // shared bytes per K/V row
   static constexpr int STAGE_BYTES = 32 * PITCH;      // 16 K rows, then 16 V rows
-  static constexpr int WARP_BYTES = STAGES * STAGE_BYTES + kSlotBuf * 4;
+  // the ring, then two slot blocks (the one in use and the next)
+  static constexpr int WARP_BYTES = STAGES * STAGE_BYTES + 2 * kSlotBuf * 4;
 };
+
+// A warp's next warp-role unit, fetched in stages while the current one
+// streams, so that the counter, work-item and slot-table round trips are off
+// the path: stage 1 takes an index from the counter (lane 0), stage 2 loads
+// the item's work words (lane k < 8 holds word k), stage 3 its first block
+// of key slots (lane l holds keys l + 32 i).  idx >= n_small_units: none left.
+struct NextUnit {
+  int idx;  // lane 0 only until stage 2
+  int32_t wk;
+  int32_t s[kSlotRegs];
+  int stage;
+  __device__ __forceinline__ int32_t word(int k) const { return __shfl_sync(0xffffffffu, wk, k); }
+};
+
+__device__ __forceinline__ void next_unit_step(const TcArgs& a, NextUnit& n) {
+  const int lane = threadIdx.x & 31;
+  if (n.stage == 0) {
+    n.idx = lane == 0 ? atomicAdd(a.unit_counter, 1) : 0;
+  } else if (n.stage == 1) {
+    n.idx = __shfl_sync(0xffffffffu, n.idx, 0);
+    n.wk = 0;
+    if (n.idx < a.n_small_units && lane < RX_WORK_WORDS)
+      n.wk = __ldg(a.work_small + int64_t(n.idx / (a.hq / a.group)) * RX_WORK_WORDS + lane);
+  } else if (n.stage == 2) {
+    const int32_t row = n.word(0), kb = n.word(1), kend = n.word(2), grow = n.word(7);
+    if (n.idx < a.n_small_units) {
+      const int32_t* trow = a.table + int64_t(row) * a.row_stride;
+      const int ke = grow > 0 ? min(kend, grow + a.step) : kend;
+#pragma unroll
+      for (int i = 0; i < kSlotRegs; ++i) {
+        const int key = kb + lane + 32 * i;
+        n.s[i] = key < ke ? __ldg(trow + key) : -1;
+      }
+    }
+  }
+  if (n.stage < 3) ++n.stage;
+}
 
 template <int NR, int D>
 __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_t* slot_buf,
-                                          int unit, uint32_t& gstep) {
+                                          uint32_t& gstep, const NextUnit& cur, NextUnit& nxt) {
   using Cfg = PipeCfg<D>;
   constexpr int S = Cfg::STAGES;
   constexpr int kRowPitch = Cfg::PITCH;
@@ -802,21 +841,22 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int n_heads_kv = a.hq / a.group;
-  const int item = unit / n_heads_kv;
-  const int kvh = unit - item * n_heads_kv;
+  const int unit = cur.idx;
+  const int kvh = unit - (unit / n_heads_kv) * n_heads_kv;
   const int G = a.group;
-  const int32_t* w = a.work_small + int64_t(item) * RX_WORK_WORDS;
-  const int32_t* trow = a.table + int64_t(w[0]) * a.row_stride;
-  const int kb = w[1], member_off = w[3], part_base = w[5], n_rows = w[6];
+  const int32_t w_row = cur.word(0), w_kend = cur.word(2), w_grow = cur.word(7);
+  const int32_t* trow = a.table + int64_t(w_row) * a.row_stride;
+  const int kb = cur.word(1), member_off = cur.word(3), part_base = cur.word(5),
+            n_rows = cur.word(6);
   // a private tail of a multi-step plan ends at its step-0 end + step
-  const int ke = w[7] > 0 ? min(w[2], w[7] + a.step) : w[2];
+  const int ke = w_grow > 0 ? min(w_kend, w_grow + a.step) : w_kend;
   const bf16* kbase = a.kpool + int64_t(kvh) * a.head_stride;
   const bf16* vbase = a.vpool + int64_t(kvh) * a.head_stride;
 
   // The unit whose chunk holds this step's newest token (the end of a growing
   // private tail) stores that token's K/V row for its KV head first, so no
   // separate store launch is needed; the bulk copies below then see the row.
-  if (a.k_new && w[7] > 0 && ke == w[7] + a.step && kb < ke) {
+  if (a.k_new && w_grow > 0 && ke == w_grow + a.step && kb < ke) {
     const int64_t b = a.members[member_off];
     const int64_t sl = a.slots_new[b];
     if (sl >= 1 && sl < a.num_slots) {
@@ -830,28 +870,43 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
     } else {
       atomicOr(&g_tc_error, 1);
     }
-    __threadfence();
+    // only this warp reads the row back (cp.async below): order the lanes'
+    // stores before those reads within the CTA
+    __threadfence_block();
     __syncwarp();
   }
 
   const int n_steps = ke > kb ? (ke - kb + 15) >> 4 : 0;
-  int slot_base = 0;  // key offset (from kb) of slot_buf[0]
-  // slots of keys [kb + base, kb + base + kSlotBuf): -1 past the key range, a
-  // slot outside the pool is flagged and read as slot 0
-  auto fill_slots = [&](int base) {
+  // Key slots go through two shared blocks of kSlotBuf: block b (keys
+  // [kb + 128 b, ..)) sits in half b % 2.  Block 0 comes prefetched with the
+  // unit; block b + 1 is loaded into registers when block b is stored, and
+  // stored when the first step of block b + 1 is issued, so no table read
+  // waits.  -1 past the key range; a slot outside the pool is flagged and
+  // read as slot 0.
+  int32_t blk[kSlotRegs];
+  auto store_block = [&](const int32_t (&r)[kSlotRegs], int half) {
 #pragma unroll
-    for (int i = 0; i < kSlotBuf / 32; ++i) {
-      const int key = kb + base + lane + 32 * i;
-      int32_t sl = key < ke ? __ldg(trow + key) : -1;
-      if (key < ke && (sl < 0 || sl >= a.num_slots)) {
+    for (int i = 0; i < kSlotRegs; ++i) {
+      int32_t sl = r[i];
+      if (sl < -1 || sl >= a.num_slots) {
         atomicOr(&g_tc_error, 1);
         sl = 0;
       }
-      slot_buf[lane + 32 * i] = sl;
+      slot_buf[half * kSlotBuf + lane + 32 * i] = sl;
     }
     __syncwarp();
   };
-  if (n_steps > 0) fill_slots(0);
+  auto load_block = [&](int base) {
+#pragma unroll
+    for (int i = 0; i < kSlotRegs; ++i) {
+      const int key = kb + base + lane + 32 * i;
+      blk[i] = key < ke ? __ldg(trow + key) : -1;
+    }
+  };
+  if (n_steps > 0) {
+    store_block(cur.s, 0);
+    load_block(kSlotBuf);
+  }
   // step st of this unit: 16 K rows and 16 V rows of 2D bytes, gathered by
   // slot with 16-byte cp.async (lane: chunks lane % 16 (+ 16 h) of rows
   // 8 (lane / 16) + i); rows past the key range are zero-filled (P is 0
@@ -860,13 +915,15 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
   const char* ksrc = reinterpret_cast<const char*>(kbase) + (lane & 15) * 16;
   const int64_t v_minus_k = reinterpret_cast<const char*>(vbase) - reinterpret_cast<const char*>(kbase);
   auto issue = [&](int st) {
-    if (st * 16 >= slot_base + kSlotBuf) {
-      slot_base = st * 16;
-      fill_slots(slot_base);
+    const int block = (st * 16) / kSlotBuf;
+    if (block > 0 && st * 16 == block * kSlotBuf) {
+      store_block(blk, block & 1);
+      load_block((block + 1) * kSlotBuf);
     }
     const uint32_t dst = ring + ((gstep + uint32_t(st)) % S) * kStageBytes +
                          uint32_t(r0 * kRowPitch + (lane & 15) * 16);
-    const int4* sp = reinterpret_cast<const int4*>(slot_buf + (st * 16 - slot_base + r0));
+    const int4* sp = reinterpret_cast<const int4*>(
+        slot_buf + ((block & 1) * kSlotBuf + st * 16 - block * kSlotBuf + r0));
     const int4 s0 = sp[0], s1 = sp[1];
     const int32_t sl[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
@@ -927,6 +984,8 @@ __device__ __forceinline__ void pipe_unit(const TcArgs& a, uint32_t ring, int32_
 
 #pragma unroll 1
   for (int st = 0; st < n_steps; ++st) {
+    // the next unit: index at step 0, work words at step 2, slots at step 4
+    if (st == 0 || st == 2 || st == 4) next_unit_step(a, nxt);
     rxk::cp_async_wait<S - 2>();
     __syncwarp();
     const uint32_t stage = ring + ((gstep + uint32_t(st)) % S) * kStageBytes;
@@ -1109,22 +1168,23 @@ __global__ void __launch_bounds__(Fused<D>::THREADS, 1)
   const int lane = int(threadIdx.x & 31);
   const uint32_t ring = base + uint32_t(warp * Cfg::WARP_BYTES);
   int32_t* slot_buf = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + warp * Cfg::WARP_BYTES +
-                                                 Cfg::STAGES * Cfg::STAGE_BYTES);
-  const int hkv = a.hq / a.group;
+                                                 Cfg::STAGES * Cfg::STAGE_BYTES);  // [2][kSlotBuf]
   uint32_t gstep = 0;
-  for (;;) {
-    int unit = 0;
-    if (lane == 0) unit = atomicAdd(a.unit_counter, 1);
-    unit = __shfl_sync(0xffffffffu, unit, 0);
-    if (unit >= a.n_small_units) break;
-    const int rows = a.work_small[int64_t(unit / hkv) * RX_WORK_WORDS + 6];
+  NextUnit cur, nxt;
+  cur.stage = 0;
+  while (cur.stage < 3) next_unit_step(a, cur);
+  while (cur.idx < a.n_small_units) {
+    nxt.stage = 0;
+    const int rows = cur.word(6);
     if (rows <= 8) {
-      pipe_unit<1, D>(a, ring, slot_buf, unit, gstep);
+      pipe_unit<1, D>(a, ring, slot_buf, gstep, cur, nxt);
     } else if constexpr (D == 128) {
-      pipe_unit<2, D>(a, ring, slot_buf, unit, gstep);
+      pipe_unit<2, D>(a, ring, slot_buf, gstep, cur, nxt);
     } else if (lane == 0) {
       atomicOr(&g_tc_error, 1);  // the plan gives head_dim 256 no such item
     }
+    while (nxt.stage < 3) next_unit_step(a, nxt);  // short units: the rest now
+    cur = nxt;
   }
 }
 
