@@ -118,3 +118,14 @@ def test_fork_tree_full_size_sampled():
     run = GpuRun(wl, sample={0, 3, 130, 377, 624}, extend_tokens=16, decode_steps={0, 15})
     run.assert_close()
     assert len(run.trace.eviction_log) > 100
+
+
+def test_multi_turn_chat_full_size_sampled():
+    """head_dim 256 at full size (256 sessions x 8 turns over a 2,000-token
+    system prompt, 477,137 pool slots): bookkeeping bit-exact; the first and
+    the last of the 16 layers run the same launches as in the benchmark and
+    are sampled in five sessions' turns at the first and last decode step."""
+    wl = workloads.multi_turn_chat()
+    run = GpuRun(wl, layers=[0, 15], sample={0, 1, 255, 1024, 2047}, extend_tokens=16,
+                 decode_steps={0, 31})
+    run.assert_close()
