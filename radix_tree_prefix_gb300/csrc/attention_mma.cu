@@ -142,7 +142,7 @@ extern "C" rx_status rx_extend_attention(const rx_pool_desc* pool, int32_t layer
   if (st != RX_OK) return st;
   if (num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0)
     return rx_internal::set_error(RX_ERR_INVALID, "rx_extend_attention: Hq % Hkv != 0");
-  if (R < 0 || num_tiles < 0 || num_tiles > INT32_MAX)
+  if (R < 0 || num_tiles < 0 || num_tiles * pool->num_kv_heads > INT32_MAX)
     return rx_internal::set_error(RX_ERR_INVALID, "rx_extend_attention: bad R or num_tiles");
   if (R == 0 || num_tiles == 0) return RX_OK;
   if (!d_q || !d_req_to_token || !d_req_rows || !d_prefix_len || !d_qo_indptr ||

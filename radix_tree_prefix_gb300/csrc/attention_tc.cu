@@ -80,6 +80,7 @@ constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 constexpr uint32_t kSleepNs = 0;                // MMA / loader waits: plain try_wait polling
 constexpr float kMasked = -1.0e30f;             // raw score of a masked key
+constexpr int kExtendInterleaveWaves = 8;
 constexpr int BM = 128;
 
 struct TcArgs {
@@ -100,6 +101,7 @@ struct TcArgs {
   const int32_t* tile_indptr;
   int num_req;
   int num_tiles;
+  int heads_interleaved;   // extend CTA order: 1 = tile-major over heads, 0 = head-major
   float* out;
   float* lse;
   int64_t tma_row_base;  // row of (layer, KV head 0, slot 0) in the tensor maps
@@ -754,13 +756,23 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   if (tid == 0) TC_TRACE(14, 3);
 }
 
-// Extend: one tile per CTA (x = row tile, y = KV head).
+// Extend: one tile per CTA, heaviest row tile first.  With few waves of CTAs
+// (heads_interleaved) CTA c takes row tile c / Hkv of KV head c % Hkv, so the
+// heavy tiles of every head go out before the light ones and the last wave
+// is short; with many waves CTA c takes head c / tiles, so the CTAs resident
+// at one time read the keys of one head and those stay in L2.
 template <int D>
 __global__ void __launch_bounds__(kThreads3, 1)
     attn_tc3_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  tc_tile3<D, false>(a, &tmk, &tmv, smem_raw, int(blockIdx.x), int(blockIdx.y));
+  const int c = int(blockIdx.x);
+  if (a.heads_interleaved) {
+    const int hkv = a.hq / a.group;
+    tc_tile3<D, false>(a, &tmk, &tmv, smem_raw, c / hkv, c - (c / hkv) * hkv);
+  } else {
+    tc_tile3<D, false>(a, &tmk, &tmv, smem_raw, c % a.num_tiles, c / a.num_tiles);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1275,7 +1287,7 @@ rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsig
     return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
   a.tma_row_base = int64_t(layer) * pool->num_kv_heads * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  attn_tc3_kernel<D><<<dim3(gx, gy), kThreads3, Lo::BYTES, s>>>(a, *tmk, *tmv);
+  attn_tc3_kernel<D><<<dim3(gx * gy), kThreads3, Lo::BYTES, s>>>(a, *tmk, *tmv);
   return rx_internal::launch_status("extend attention (tcgen05)");
 }
 
@@ -1409,6 +1421,10 @@ rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const voi
   a.tile_indptr = d_tile_indptr;
   a.num_req = R;
   a.num_tiles = int(num_tiles);
+  // up to kExtendInterleaveWaves waves of CTAs: heads interleaved (short tail);
+  // more: head-major (L2 locality of long key ranges)
+  a.heads_interleaved =
+      num_tiles * pool->num_kv_heads <= int64_t(kExtendInterleaveWaves) * rx_internal::sm_count();
   a.out = d_out;
   a.lse = d_lse;
   if (D == 128)
