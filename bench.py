@@ -369,7 +369,7 @@ def main():
 
         eng2 = Engine(wl, device=dev, inputs=host_inputs, layers=layers,
                       on_extend=lambda b, r, p, q, outs: grab(outs),
-                      on_decode=lambda s, t, r, c, outs, i: grab(outs))
+                      on_decode_wave=lambda s, r, c, outs, i: grab(outs))
         eng2.run()
         torch.cuda.synchronize()
         sinks.clear()

@@ -89,12 +89,19 @@ class GatherInputs:
                         self.values["k"][layer].index_select(0, ti),
                         self.values["v"][layer].index_select(0, ti)) for layer in self.layers}
 
-    def decode(self, step_no, reqs, t):
-        idx = np.array([self.wl.output_store_index(r)[t] for r in reqs], dtype=np.int64)
+    def decode_wave(self, step0, reqs, T):
+        """Q/K/V of the new tokens of T decode steps of a wave, [T][B][heads][d]
+        per layer (step t, request b: the token at output position t)."""
+        idx = np.array([[self.wl.output_store_index(r)[t] for r in reqs] for t in range(T)],
+                       dtype=np.int64).reshape(-1)
         ti = self._idx(idx)
-        return {layer: (self.values["q"][layer].index_select(0, ti),
-                        self.values["k"][layer].index_select(0, ti),
-                        self.values["v"][layer].index_select(0, ti)) for layer in self.layers}
+        B = len(reqs)
+
+        def rows(kind, layer):
+            x = self.values[kind][layer].index_select(0, ti)
+            return x.view(T, B, *x.shape[1:])
+        return {layer: (rows("q", layer), rows("k", layer), rows("v", layer))
+                for layer in self.layers}
 
 
 class PreparedInputs:
@@ -137,8 +144,8 @@ class PreparedInputs:
     def extend(self, batch_no, reqs, prefix):
         return self._get(self.ext, batch_no, lambda: self.source.extend(batch_no, reqs, prefix))
 
-    def decode(self, step_no, reqs, t):
-        return self._get(self.dec, step_no, lambda: self.source.decode(step_no, reqs, t))
+    def decode_wave(self, step0, reqs, T):
+        return self._get(self.dec, step0, lambda: self.source.decode_wave(step0, reqs, T))
 
 
 class _Staging:
@@ -193,20 +200,24 @@ class Engine:
     """Runs a workload through librx.
 
     ``device=None`` runs the host bookkeeping only (no CUDA).  With a device,
-    ``inputs`` supplies the Q/K/V of computed tokens and ``on_extend`` /
-    ``on_decode`` receive the attention outputs per layer.  Every copy and
+    ``inputs`` supplies the Q/K/V of computed tokens (``extend`` per batch,
+    ``decode_wave`` for all decode steps of a wave) and ``on_extend`` /
+    ``on_decode`` receive the attention outputs per layer, per batch and per
+    decode step; ``on_decode_wave`` receives a wave's decode outputs at once
+    ([T][B] tensors per layer).  Every copy and
     launch goes to ``stream``; left as None it is the device's current stream
     when the engine is made, which must then stay current while it runs.
     """
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
-                 on_decode=None, stream=None, timing=False):
+                 on_decode=None, stream=None, timing=False, on_decode_wave=None):
         self.wl = wl
         self.device = device
         self.inputs = inputs
         self.layers = list(range(wl.num_layers)) if layers is None else list(layers)
         self.on_extend = on_extend
         self.on_decode = on_decode
+        self.on_decode_wave = on_decode_wave
         self.stream = stream
         # launches with no explicit stream go to the device's current stream
         # as of construction, resolved once (a lookup per launch costs more
@@ -365,7 +376,7 @@ class Engine:
         if self.d_ws.numel() < need:
             self.d_ws = torch.empty(int(need * 1.25) + 256, dtype=torch.uint8, device=self.device)
         # every step's inputs and outputs, then one native call per layer
-        inputs = [self.inputs.decode(self.step_no + t, wave, t) for t in range(T)]
+        inputs = self.inputs.decode_wave(self.step_no, wave, T)
         outs = {}
         tt = np.arange(T, dtype=np.uint64)
         for layer in self.layers:
@@ -373,8 +384,8 @@ class Engine:
                             device=self.device)
             l = torch.empty((T, B, wl.num_q_heads), dtype=torch.float32, device=self.device)
             steps = np.zeros(T, dtype=rx.DECODE_STEP_DTYPE)
-            for f, i in (("d_q", 0), ("d_k", 1), ("d_v", 2)):
-                steps[f] = [inputs[t][layer][i].data_ptr() for t in range(T)]
+            for f, x in zip(("d_q", "d_k", "d_v"), inputs[layer]):
+                steps[f] = x.data_ptr() + tt * np.uint64(x[0].numel() * x.element_size())
             steps["d_slots"] = d_slots.data_ptr() + tt * np.uint64(4 * B)
             steps["d_plan"] = d_plan.data_ptr()
             steps["info"] = ctypes.addressof(info)
@@ -393,6 +404,8 @@ class Engine:
                 self.on_decode(self.step_no + t, t, list(rids), ctx0 + 1 + t,
                                {ly: (outs[ly][0][t], outs[ly][1][t]) for ly in self.layers},
                                info)
+        if self.on_decode_wave is not None:
+            self.on_decode_wave(self.step_no, list(rids), ctx0 + 1, outs, info)
         self.step_no += T
 
     def _launches_per_decode(self, infos):
