@@ -673,14 +673,27 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   struct Work {
     int32_t row, kb, ke, member_off, n_members, grow;
   };
+  // A segment goes to the warp role when its rows fit one warp-role item, or
+  // when it has at most kDecodeSplitRows rows: those are cut into member
+  // blocks of at most small_rows rows (each block re-reads the segment's
+  // keys, mostly from L2), which costs the GPU less than a 128-row tile
+  // that would be mostly empty.
+  const int64_t warp_block = std::max<int64_t>(1, small_rows / G);
+  auto is_warp_seg = [&](int64_t members_k) {
+    const int64_t rows = members_k * G;
+    return rows <= small_rows || (rows <= rx_internal::kDecodeSplitRows && G <= small_rows);
+  };
+  auto warp_blocks = [&](int64_t members_k) {
+    return members_k * G <= small_rows ? int64_t(1) : (members_k + warp_block - 1) / warp_block;
+  };
   // chunk of the warp-role items: the longest that keeps enough units
   int64_t small_chunk = rx_internal::kDecodeSmallChunkMin;
   for (int64_t c = rx_internal::kDecodeSmallChunkMax; c > rx_internal::kDecodeSmallChunkMin;
        c /= 2) {
     int64_t units = 0;
     for (const Seg& s : segs)
-      if (int64_t(s.members.size()) * G <= small_rows)
-        units += (s.ke - s.kb + c - 1) / c * num_kv_heads;
+      if (is_warp_seg(int64_t(s.members.size())))
+        units += (s.ke - s.kb + c - 1) / c * warp_blocks(int64_t(s.members.size())) * num_kv_heads;
     if (units >= int64_t(rx_internal::kDecodeWarpSlots) * rx_internal::kDecodeUnitsPerWarp) {
       small_chunk = c;
       break;
@@ -697,7 +710,7 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     int64_t ctas = 0;
     for (const Seg& s : segs) {
       const int64_t rows = int64_t(s.members.size()) * G;
-      if (rows <= small_rows) continue;
+      if (is_warp_seg(int64_t(s.members.size()))) continue;
       const int64_t per_block = rx_internal::kDecodeTcRows / G;
       const int64_t blocks = (int64_t(s.members.size()) + per_block - 1) / per_block;
       const int64_t c = tc_base_chunk(rows) * tc_scale;
@@ -716,10 +729,10 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
     bool is_small;
     int32_t per_block;
     int64_t chunk, step;
-    if (rows <= small_rows) {
+    if (is_warp_seg(k)) {
       is_small = true;
-      per_block = k;
-      chunk = std::max<int64_t>(small_chunk, 2 * rows);
+      per_block = rows <= small_rows ? k : int32_t(warp_block);
+      chunk = std::max<int64_t>(small_chunk, 2 * std::min<int64_t>(rows, small_rows));
       step = 16;
     } else {
       is_small = false;

@@ -16,6 +16,9 @@ namespace rx_internal {
 // kDecodeTcRows rows for its tensor-core tiles.
 inline int decode_small_rows(int head_dim) { return head_dim == 128 ? 16 : 8; }
 constexpr int kDecodeTcRows = 128;
+// Decode: segments of up to this many rows are split into warp-role items
+// (member blocks of <= decode_small_rows rows) instead of a tensor-core tile.
+constexpr int kDecodeSplitRows = 32;
 inline int decode_rows_per_item(int /*head_dim*/) { return kDecodeTcRows; }
 // Decode: a tensor-core chunk is at least kDecodeMinChunk keys and at least
 // kDecodeKeysPerRow keys per query row of its segment (each tile CTA pays
