@@ -18,6 +18,7 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ptx_util.cuh"
@@ -43,12 +44,15 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restric
                                                         const float* __restrict__ ws_lse,
                                                         int hq, int B, float* __restrict__ out,
                                                         float* __restrict__ lse_out,
-                                                        int32_t* __restrict__ counter) {
+                                                        int32_t* __restrict__ counter,
+                                                        int late_trigger) {
   constexpr int V = D / 128;  // float4 per lane
   constexpr int CH = 8;       // part rows loaded together
   // launched after the decode kernel with programmatic stream serialization:
-  // let the next step's kernel start launching, then wait for the partials
-  rxk::griddep_launch_dependents();
+  // let the next step's kernel start launching, then wait for the partials.
+  // late_trigger: the next kernel may launch only once this one has waited,
+  // i.e. once the decode kernel before it has completed.
+  if (!late_trigger) rxk::griddep_launch_dependents();
   const int gw = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const bool active = gw < B * hq;
@@ -58,6 +62,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const int32_t* __restric
   const int n = active ? indptr[b + 1] - p0 : 0;
   int64_t e = lane < n ? int64_t(parts[p0 + lane]) * hq + h : 0;
   rxk::griddep_wait();
+  if (late_trigger) rxk::griddep_launch_dependents();
   if (counter && blockIdx.x == 0 && threadIdx.x == 0) *counter = 0;
   if (!active) return;
   const float4* o4 = reinterpret_cast<const float4*>(ws_o);
@@ -164,7 +169,9 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
                                 size_t workspace_bytes, cudaStream_t s, bool first_call,
                                 int step, const void* k_new = nullptr,
                                 const void* v_new = nullptr,
-                                const int32_t* slots_new = nullptr) {
+                                const int32_t* slots_new = nullptr,
+                                int32_t* counter_at = nullptr, bool early_inputs = false,
+                                bool late_trigger = false) {
   rx_status st = rx_internal::check_pool(pool, layer);
   if (st != RX_OK) return st;
   if (!info || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0 || B < 0)
@@ -184,8 +191,9 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
   float* ws_o = static_cast<float*>(d_workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + ((o_bytes + 255) / 256) * 256);
   const int64_t l_bytes = info->n_parts * num_q_heads * 4;
-  int32_t* counter = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws_lse) +
-                                                ((l_bytes + 255) / 256) * 256);
+  int32_t* counter = counter_at ? counter_at
+                                : reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws_lse) +
+                                                             ((l_bytes + 255) / 256) * 256);
   // the work counter of the decode kernel is 0 at every launch: zeroed here
   // once per call, reset by each merge after that
   if (first_call && cudaMemsetAsync(counter, 0, sizeof(int32_t), s) != cudaSuccess)
@@ -195,7 +203,7 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
     st = rx_internal::decode_fused(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, work,
                                    n_small, work + n_small * RX_WORK_WORDS, info->n_work_tc,
                                    members, scale, ws_o, ws_lse, counter, step, k_new, v_new,
-                                   slots_new, s);
+                                   slots_new, s, early_inputs);
     if (st != RX_OK) return st;
   }
   // The merge may launch while the decode kernel before it still runs (it
@@ -216,10 +224,10 @@ rx_status decode_attention_impl(const rx_pool_desc* pool, int32_t layer, const v
   const float* wl = ws_lse;
   if (D == 128)
     cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, indptr, parts, wo, wl, int(num_q_heads),
-                       int(B), d_out, d_lse, counter);
+                       int(B), d_out, d_lse, counter, late_trigger ? 1 : 0);
   else
     cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, indptr, parts, wo, wl, int(num_q_heads),
-                       int(B), d_out, d_lse, counter);
+                       int(B), d_out, d_lse, counter, late_trigger ? 1 : 0);
   return rx_internal::launch_status("decode merge");
 }
 
@@ -249,6 +257,31 @@ extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, in
   if (num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0)
     return rx_internal::set_error(RX_ERR_INVALID, "rx_decode_steps: Hq % Hkv != 0");
   const int G = num_q_heads / pool->num_kv_heads;
+  // A run of steps whose new tokens all lie in private tails: every step has
+  // its own work counter (zeroed here at once, after the largest step's
+  // partial results), step 0's merge lets the next kernel launch only after
+  // step 0 has completed, and later steps' tiles then read their queries and
+  // the shared segments (no kernel of the run writes those) without waiting
+  // for the step before; only their partial writes wait for its merge.
+  bool early = n_steps >= 2 && B > 0 && G <= rx_internal::decode_small_rows(pool->head_dim);
+  int64_t region = 0;
+  for (int32_t i = 0; early && i < n_steps; ++i) {
+    const rx_decode_plan_info* inf = steps[i].info;
+    if (!inf || inf->tails_private != 1) {
+      early = false;
+      break;
+    }
+    const int64_t o = inf->n_parts * num_q_heads * int64_t(pool->head_dim) * 4;
+    const int64_t l = inf->n_parts * num_q_heads * 4;
+    region = std::max<int64_t>(region, (o + 255) / 256 * 256 + (l + 255) / 256 * 256);
+  }
+  if (early && (!d_workspace || int64_t(workspace_bytes) < region + 4 * int64_t(n_steps)))
+    early = false;
+  int32_t* counters =
+      early ? reinterpret_cast<int32_t*>(static_cast<char*>(d_workspace) + region) : nullptr;
+  if (early && cudaMemsetAsync(counters, 0, 4 * size_t(n_steps),
+                               reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return rx_internal::launch_status("decode counters reset");
   for (int32_t i = 0; i < n_steps; ++i) {
     const rx_decode_step& st = steps[i];
     // every step's new token is the end of a growing private tail: the decode
@@ -264,9 +297,10 @@ extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, in
     }
     r = decode_attention_impl(pool, layer, st.d_q, num_q_heads, d_req_to_token, row_stride,
                               st.d_plan, st.info, B, scale, st.d_out, st.d_lse, d_workspace,
-                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream), i == 0,
-                              st.step, fused ? st.d_k : nullptr, fused ? st.d_v : nullptr,
-                              fused ? st.d_slots : nullptr);
+                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                              i == 0 && !early, st.step, fused ? st.d_k : nullptr,
+                              fused ? st.d_v : nullptr, fused ? st.d_slots : nullptr,
+                              early ? counters + i : nullptr, early && i > 0, early && i == 0);
     if (r != RX_OK) return r;
   }
   return RX_OK;

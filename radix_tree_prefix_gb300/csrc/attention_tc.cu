@@ -117,6 +117,8 @@ struct TcArgs {
   int n_tc_ctas;           // tensor-core CTAs
   int n_warp_first;        // warp-role-only CTAs placed before them
   int* unit_counter;       // next warp-role unit to take (0 at launch)
+  int early_inputs;        // decode: the tiles may read Q and shared-segment keys
+                           // before griddepcontrol.wait (see decode_fused)
   int step;                // step index within a multi-step plan
   const bf16* k_new;       // bf16 [B][Hkv][D] of the step's tokens, or NULL
   const bf16* v_new;
@@ -354,7 +356,9 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // ------------------------------------------------------------- loaders
     const bool load_v = warp == 10;
     // keys written by earlier kernels on the stream are read from here on
-    rxk::griddep_wait();
+    // (a decode step after the first of a run reads shared segments that no
+    // kernel of the run writes: it need not wait)
+    if (!DECODE || !a.early_inputs) rxk::griddep_wait();
     constexpr int CPR = D / 8;
     constexpr int SPL = BN / 32;  // slots per lane: rows lane + 32 i
     const bf16* kb = a.kpool + int64_t(kvh) * a.head_stride;
@@ -552,8 +556,10 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
     float* xch = reinterpret_cast<float*>(gbase + Lo::XCH);  // [2][2 warpgroups][BM]
     // the queries and the outputs (decode: partial buffers the previous
-    // merge read) are touched only once earlier kernels on the stream are done
-    rxk::griddep_wait();
+    // merge read) are touched only once earlier kernels on the stream are
+    // done; with early inputs the queries are complete already and only the
+    // partial writes wait (below)
+    if (!DECODE || !a.early_inputs) rxk::griddep_wait();
     {
       // chunks [8 w, 8 w + 8) of Q row i (zeros past the tile's rows) while
       // the loader warp already streams the first K/V tiles
@@ -689,6 +695,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // exchange barrier, so no waiter is left behind when a wait gave up.
     const bool fin = ok && n_tiles > 0 &&
                      __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit));
+    if (DECODE && a.early_inputs) rxk::griddep_wait();  // the previous merge read ws
     if (i == 0 && wg == 0) TC_TRACE(14, 1);
     // (a thread got here after every thread passed the exchange of tile
     // n_tiles - 1, hence had read the slot of tile n_tiles - 2)
@@ -1318,7 +1325,8 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                        const int32_t* d_work_small, int64_t n_small, const int32_t* d_work_tc,
                        int64_t n_tc, const int32_t* d_members, float scale, float* ws_o,
                        float* ws_lse, int32_t* unit_counter, int step, const void* k_new,
-                       const void* v_new, const int32_t* slots_new, cudaStream_t stream) {
+                       const void* v_new, const int32_t* slots_new, cudaStream_t stream,
+                       bool early_inputs) {
   const int D = pool->head_dim;
   if (D != 128 && D != 256) return set_error(RX_ERR_INVALID, "decode needs head_dim 128 or 256");
   const int64_t hkv = pool->num_kv_heads;
@@ -1360,6 +1368,7 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.n_tc_ctas = int(tc_ctas);
   a.n_warp_first = int(warp_first);
   a.unit_counter = unit_counter;
+  a.early_inputs = early_inputs ? 1 : 0;
   a.step = step;
   a.k_new = static_cast<const bf16*>(k_new);
   a.v_new = static_cast<const bf16*>(v_new);

@@ -782,7 +782,9 @@ static rx_status plan_decode_impl(const rx_cache* c, int32_t B, int32_t n_steps,
   int64_t l_bytes = n_parts * num_q_heads * 4;
   // partial o, partial lse, and one 256-byte block for the decode kernel's
   // work counter
-  info->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256 + 256;
+  // partial results, then the work counters (one per step of the plan)
+  info->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256 +
+                          std::max<int64_t>(256, (4 * int64_t(n_steps) + 255) / 256 * 256);
   info->distinct_kv_tokens = distinct;
   info->tails_private = tails_private ? 1 : 0;
   if (!plan || plan_cap < info->plan_words)

@@ -54,15 +54,20 @@ int32_t kv_store_error_flags(bool clear);
 int32_t tc_error_flags(bool clear);
 // One decode step in a single launch: the tensor-core tiles of the plan's
 // large items and the warp-role units of its small items (attention_tc.cu).
-// *unit_counter must be 0; the merge resets it.  k_new / v_new / slots_new
-// non-NULL: the warp owning a request's newest token stores it first.  Launched with programmatic stream
-// serialization (the merge after it may launch early).
+// *unit_counter must be 0 at launch.  k_new / v_new / slots_new non-NULL:
+// the warp owning a request's newest token stores it first.  Launched with
+// programmatic stream serialization (the merge after it may launch early).
+// early_inputs: the run's first step has completed when this kernel starts,
+// so its tiles load queries and shared-segment keys (which no kernel of a
+// run of decode steps writes) without griddepcontrol.wait, and wait only
+// before writing partial results.
 rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                        int32_t num_q_heads, const int32_t* d_req_to_token, int64_t row_stride,
                        const int32_t* d_work_small, int64_t n_small, const int32_t* d_work_tc,
                        int64_t n_tc, const int32_t* d_members, float scale, float* ws_o,
                        float* ws_lse, int32_t* unit_counter, int step, const void* k_new,
-                       const void* v_new, const int32_t* slots_new, cudaStream_t stream);
+                       const void* v_new, const int32_t* slots_new, cudaStream_t stream,
+                       bool early_inputs);
 rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const void* d_q,
                               int32_t num_q_heads, const int32_t* d_req_to_token,
                               int64_t row_stride, const int32_t* d_req_rows,
