@@ -108,17 +108,23 @@ class PreparedInputs:
     """Inputs gathered once (by a recording run) and replayed in order.
 
     ``source`` is any provider; the first pass records what it returns per
-    extend batch and decode step, later passes replay it.  ``host=True`` keeps
-    the recorded tensors in pinned host memory and copies each batch to the
-    device when it is used (the end-to-end path)."""
+    extend batch and per decode wave, later passes replay it.  ``host=True``
+    keeps the recorded tensors in pinned host memory and copies them to the
+    device when they are used (the end-to-end path): when the engine asks for
+    one batch's inputs, the next batch's (in the recorded order) are already
+    being copied on a side stream, so the copies overlap the kernels."""
 
     def __init__(self, source, host=False):
         self.source = source
         self.host = host
         self.ext = {}
         self.dec = {}
+        self.order = []        # (store, key) in the order a run asks for them
         self.recording = True
         self.h2d_bytes = 0
+        self._pos = 0
+        self._ahead = None     # (position, device tensors per layer, event)
+        self._copy_stream = None
 
     def freeze(self):
         self.recording = False
@@ -128,24 +134,52 @@ class PreparedInputs:
                     store[key] = {l: tuple(t.cpu().pin_memory() for t in qkv)
                                   for l, qkv in per_layer.items()}
 
-    def _get(self, store, key, make):
-        if self.recording:
-            store[key] = make()
-            return store[key]
-        per_layer = store[key]
-        if not self.host:
-            return per_layer
+    def _copy(self, per_layer):
         out = {}
         for l, qkv in per_layer.items():
             out[l] = tuple(t.to(self.source.device, non_blocking=True) for t in qkv)
             self.h2d_bytes += sum(t.numel() * t.element_size() for t in qkv)
         return out
 
+    def _get(self, name, store, key, make):
+        if self.recording:
+            store[key] = make()
+            self.order.append((name, key))
+            return store[key]
+        if not self.host:
+            return store[key]
+        import torch
+        cur = torch.cuda.current_stream(self.source.device)
+        pos = self._pos
+        if self.order[pos] != (name, key):     # not the recorded order: start over
+            pos = self.order.index((name, key))
+            self._ahead = None
+        if self._ahead is not None and self._ahead[0] == pos:
+            _, out, ev = self._ahead
+            cur.wait_event(ev)
+            for qkv in out.values():
+                for t in qkv:
+                    t.record_stream(cur)
+        else:
+            out = self._copy(store[key])
+        self._pos = (pos + 1) % len(self.order)
+        nname, nkey = self.order[self._pos]
+        if self._copy_stream is None:
+            self._copy_stream = torch.cuda.Stream(self.source.device)
+        with torch.cuda.stream(self._copy_stream):
+            ahead = self._copy((self.ext if nname == "ext" else self.dec)[nkey])
+            ev = torch.cuda.Event()
+            ev.record(self._copy_stream)
+        self._ahead = (self._pos, ahead, ev)
+        return out
+
     def extend(self, batch_no, reqs, prefix):
-        return self._get(self.ext, batch_no, lambda: self.source.extend(batch_no, reqs, prefix))
+        return self._get("ext", self.ext, batch_no,
+                         lambda: self.source.extend(batch_no, reqs, prefix))
 
     def decode_wave(self, step0, reqs, T):
-        return self._get(self.dec, step0, lambda: self.source.decode_wave(step0, reqs, T))
+        return self._get("dec", self.dec, step0,
+                         lambda: self.source.decode_wave(step0, reqs, T))
 
 
 class _Staging:
