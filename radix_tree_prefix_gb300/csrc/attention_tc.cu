@@ -117,6 +117,7 @@ struct TcArgs {
   int n_tc_ctas;           // tensor-core CTAs
   int n_warp_first;        // warp-role-only CTAs placed before them
   int* unit_counter;       // next warp-role unit to take (0 at launch)
+  int tiles_leave;         // decode: tile CTAs exit after their tile
   int early_inputs;        // decode: the tiles may read Q and shared-segment keys
                            // before griddepcontrol.wait (see decode_fused)
   int step;                // step index within a multi-step plan
@@ -1179,6 +1180,10 @@ __global__ void __launch_bounds__(Fused<D>::THREADS, 1)
     tc_tile3<D, true>(a, &tmk, &tmv, smem_raw, cta / hkv, cta - (cta / hkv) * hkv);
   }
   if (threadIdx.x >= kPipeWarps * 32) return;  // the warp role uses the first six warps
+  // tiles_leave: in a run of steps a tile CTA leaves its SM to the next
+  // step's tiles, which start there at once (early inputs) while this step's
+  // warp-role units still stream on the other SMs
+  if (a.tiles_leave && cta >= 0 && cta < a.n_tc_ctas) return;
   rxk::griddep_wait();
   // warp role: this warp's ring and slot buffer
   const uint32_t raw = rxk::smem_addr(smem_raw);
@@ -1369,6 +1374,9 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.n_warp_first = int(warp_first);
   a.unit_counter = unit_counter;
   a.early_inputs = early_inputs ? 1 : 0;
+  // with three times as many warp-role CTAs as tile CTAs (few, long tiles
+  // beside many units), the tiles need not help with the units
+  a.tiles_leave = early_inputs && ctas - tc_ctas >= 3 * tc_ctas ? 1 : 0;
   a.step = step;
   a.k_new = static_cast<const bf16*>(k_new);
   a.v_new = static_cast<const bf16*>(v_new);
