@@ -11,7 +11,7 @@ the language nobody remembers", section "The scheduler is where the cache is
 won or lost": a request that shares more with a request already queued in the
 batch than with the tree waits, so that its sibling populates the tree first.
 
-Readings (listed in DESIGN.md):
+Readings of the pages where they leave a step open:
 
 * a wave of requests is processed as: extend batches -> ``decode_steps`` decode
   steps over the whole wave -> finish of every request in order;

@@ -21,7 +21,7 @@ Sources (page title, section):
   unlock) and "Worked example, step by step" (a node is evicted whole; locked
   nodes are never candidates; if nothing can be evicted the request waits).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * token granularity only (``page_size == 1``);
 * a match that ends inside an edge splits that edge so the returned node covers

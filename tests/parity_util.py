@@ -11,7 +11,7 @@ MAX_ABS = 1e-2    # attention tolerance vs fp64 (bf16 inputs, fp32 accumulation)
 MEAN_ABS = 1e-3
 
 
-class GpuRun:
+class DeviceRun:
     def __init__(self, wl, layers=None, sample=None, extend_tokens=None, decode_steps=None,
                  check_bookkeeping=True):
         import torch

@@ -16,7 +16,7 @@ if not torch.cuda.is_available():  # collected on CPU machines, skipped there
     pytest.skip("no CUDA device", allow_module_level=True)
 
 from oracle import pool as opool  # noqa: E402
-from parity_util import GpuRun  # noqa: E402
+from parity_util import DeviceRun  # noqa: E402
 from radix_tree_prefix_gb300 import rx, workloads  # noqa: E402
 from radix_tree_prefix_gb300.workloads import Request, Workload  # noqa: E402
 
@@ -74,7 +74,7 @@ SMALL = {
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_workload_parity(name):
     wl = SMALL[name][0]()
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     mx, mean, n = run.assert_close()
     if name == "nested_share":
         assert run.trace.prefilled == 3060
@@ -94,7 +94,7 @@ def test_single_token_suffixes_and_duplicates():
         waves.append([Request(k, (base,) + tuple(ones[:k + 1]), outs[k])])
     waves.append([Request(4, (base, ones[0]), outs[4]), Request(5, (base, ones[0]), outs[5])])
     wl = Workload("one_token", 1, 16, 4, 128, 2000, 3, s.tokens, waves, 77)
-    run = GpuRun(wl)
+    run = DeviceRun(wl)
     run.assert_close()
     assert [len(b) for b in run.trace.batches] == [1, 1, 1, 1, 1, 1]
 
@@ -103,19 +103,19 @@ def test_agent_loop_full_size_sampled():
     """The benchmark workload at full size: bookkeeping bit-exact, sampled
     extend rows of 6 requests and decode rows at 3 steps."""
     wl = workloads.agent_loop()
-    run = GpuRun(wl, sample={0, 1, 7, 20, 38, 39}, extend_tokens=48, decode_steps={0, 31, 63})
+    run = DeviceRun(wl, sample={0, 1, 7, 20, 38, 39}, extend_tokens=48, decode_steps={0, 31, 63})
     run.assert_close()
 
 
 def test_long_shared_full_size_sampled():
     wl = workloads.long_shared()
-    run = GpuRun(wl, sample={0, 1, 63}, extend_tokens=24, decode_steps={0, 127})
+    run = DeviceRun(wl, sample={0, 1, 63}, extend_tokens=24, decode_steps={0, 127})
     run.assert_close()
 
 
 def test_fork_tree_full_size_sampled():
     wl = workloads.fork_tree()
-    run = GpuRun(wl, sample={0, 3, 130, 377, 624}, extend_tokens=16, decode_steps={0, 15})
+    run = DeviceRun(wl, sample={0, 3, 130, 377, 624}, extend_tokens=16, decode_steps={0, 15})
     run.assert_close()
     assert len(run.trace.eviction_log) > 100
 
@@ -126,6 +126,6 @@ def test_multi_turn_chat_full_size_sampled():
     the last of the 16 layers run the same launches as in the benchmark and
     are sampled in five sessions' turns at the first and last decode step."""
     wl = workloads.multi_turn_chat()
-    run = GpuRun(wl, layers=[0, 15], sample={0, 1, 255, 1024, 2047}, extend_tokens=16,
+    run = DeviceRun(wl, layers=[0, 15], sample={0, 1, 255, 1024, 2047}, extend_tokens=16,
                  decode_steps={0, 31})
     run.assert_close()
