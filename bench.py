@@ -61,6 +61,24 @@ TRAFFIC = {
 }
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (time of a step: the job is as slow as
+    its slowest replica); x itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, seconds, world):
+    """Whole-job throughput of `world` replicas that each process
+    units_per_rank units in the (max over ranks) time `seconds`."""
+    return world * units_per_rank / seconds
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -307,12 +325,8 @@ def main():
     assert t.as_tuple() == trace.as_tuple(), "timed steps made different cache decisions"
     rx.device_check()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * q_per_step / (ms / 1000.0)
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = job_rate(q_per_step, ms / 1000.0, world)
 
     kinds = {}
     for kind, a, b, work in eng.kernel_events:
@@ -404,12 +418,8 @@ def main():
             eng2.run()
             torch.cuda.synchronize()
             sink_i[0] = 0
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        if world > 1:
-            tt = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
-        e2e = {"value": world * q_per_step / e2e_s, "unit": "query-tok/s",
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
+        e2e = {"value": job_rate(q_per_step, e2e_s, world), "unit": "query-tok/s",
                "h2d_bytes_per_step": host_inputs.h2d_bytes // args.steps,
                "d2h_bytes_per_step": d2h["bytes"] // args.steps,
                "ms_per_step": e2e_s * 1e3}
