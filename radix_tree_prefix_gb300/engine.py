@@ -182,34 +182,57 @@ class PreparedInputs:
                          lambda: self.source.decode_wave(step0, reqs, T))
 
 
+class _DevSpan:
+    """A span of int32 values in a staging buffer on the device: the part of a
+    tensor the librx binding reads (data_ptr, numel, shape), without the cost
+    of making a tensor view per array."""
+
+    __slots__ = ("ptr", "n", "shape")
+
+    def __init__(self, ptr, n, shape=None):
+        self.ptr, self.n = ptr, n
+        self.shape = (n,) if shape is None else shape
+
+    def data_ptr(self):
+        return self.ptr
+
+    def numel(self):
+        return self.n
+
+
 class _Staging:
     """Host->device uploads through a ring of pinned buffers.
 
     Each upload packs int32 arrays into one pinned buffer and issues a single
-    asynchronous copy on the engine's stream; a ring slot is reused only after
-    its previous copy has completed (event), so the host never blocks on the
-    GPU in the common case."""
+    asynchronous copy on the engine's stream; a ring slot's pinned buffer is
+    refilled only after its previous copy has completed (event), so the host
+    never blocks on the GPU in the common case.  Device-side reuse of a slot
+    is ordered by the stream itself."""
 
     def __init__(self, torch, device, stream, explicit, n=4):
         self.torch, self.device, self.stream = torch, device, stream
         self.explicit = explicit    # False: ``stream`` is the current stream
         self.host = [None] * n
+        self.host_np = [None] * n
         self.dev = [None] * n
-        self.events = [None] * n
+        self.events = [torch.cuda.Event() for _ in range(n)]
+        self.used = [False] * n
         self.i = 0
 
-    def upload(self, arrays):
+    def upload(self, arrays, as_tensors=False):
+        """Device spans (or, with as_tensors, tensor views) of the arrays."""
         torch = self.torch
         n = sum(len(a) for a in arrays)
         i = self.i
         self.i = (i + 1) % len(self.host)
-        if self.events[i] is not None:
+        if self.used[i]:
             self.events[i].synchronize()
         if self.host[i] is None or self.host[i].numel() < n:
             cap = max(2 * n, 1 << 21)
             self.host[i] = torch.empty(cap, dtype=torch.int32, pin_memory=True)
+            self.host_np[i] = self.host[i].numpy()
             self.dev[i] = torch.empty(cap, dtype=torch.int32, device=self.device)
-        h = self.host[i].numpy()
+        h = self.host_np[i]
         off = 0
         spans = []
         for a in arrays:
@@ -223,11 +246,13 @@ class _Staging:
                 self.dev[i][:n].copy_(self.host[i][:n], non_blocking=True)
         else:
             self.dev[i][:n].copy_(self.host[i][:n], non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(stream)
-        self.events[i] = ev
+        self.events[i].record(stream)
+        self.used[i] = True
         d = self.dev[i]
-        return [d[o:o + k] for o, k in spans]
+        if as_tensors:
+            return [d[o:o + k] for o, k in spans]
+        base = d.data_ptr()
+        return [_DevSpan(base + 4 * o, k) for o, k in spans]
 
 
 class Engine:
@@ -339,12 +364,8 @@ class Engine:
         self.trace.batches.append(recs)
         if self.device is not None:
             self._extend_device(reqs, j0, j1, prefix, ind, new_slots)
-        nodes, rewritten = self.cache.extend_end(tok, ind, table, prefix, match_nodes)
+        nodes, _ = self.cache.extend_end(tok, ind, table, prefix, match_nodes)
         prompt_nodes[j0:j1] = nodes
-        if rewritten and self.device is not None:
-            width = int(max(ind[1:] - ind[:-1]))
-            (blk,) = self.staging.upload([self.h_table[j0:j1, :width].ravel()])
-            self.d_table[j0:j1, :width].copy_(blk.view(j1 - j0, width))
         self.batch_no += 1
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):
@@ -354,11 +375,14 @@ class Engine:
         qo = np.zeros(R + 1, dtype=np.int32)
         np.cumsum((ind[1:] - ind[:-1]) - prefix, out=qo[1:])
         tiles, n_tiles = rx.extend_plan(qo, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+        # the kernels read the batch's rows of the slot table from the staged
+        # copy (rows 0 .. R-1); the engine's device table gets the wave's rows
+        # once, before its decode steps
         width = int(max(ind[1:] - ind[:-1]))
-        d_rows, d_prefix, d_qo, d_tiles, d_slots, blk = self.staging.upload([
-            np.arange(j0, j1, dtype=np.int32), prefix, qo, tiles, new_slots,
+        d_rows, d_prefix, d_qo, d_tiles, d_slots, d_tab = self.staging.upload([
+            np.arange(R, dtype=np.int32), prefix, qo, tiles, new_slots,
             self.h_table[j0:j1, :width].ravel()])
-        self.d_table[j0:j1, :width].copy_(blk.view(R, width))
+        d_tab.shape = (R, width)
         inputs = self.inputs.extend(self.batch_no, reqs, prefix)
         total_q = int(qo[-1])
         flops = self._extend_flops(prefix, qo) if self.timing else 0.0
@@ -369,7 +393,7 @@ class Engine:
             out = torch.empty((total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
                               device=self.device)
             lse = torch.empty((total_q, wl.num_q_heads), dtype=torch.float32, device=self.device)
-            call = rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, self.d_table,
+            call = rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, d_tab,
                                             d_rows, d_prefix, d_qo, d_tiles, R, n_tiles,
                                             self.scale, out, lse, self.stream)
             ev = self._event_start()
@@ -402,6 +426,11 @@ class Engine:
             prompt_nodes, ctx0 + 1, rows, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
             self.plan_buf, n_steps=T)
         plan = self.plan_buf[:int(info.plan_words)]
+        # the wave's prompt rows of the slot table (the extend kernels read
+        # per-batch staged copies), then every step's decode slots
+        width = int(ctx0.max())
+        (tab,) = self.staging.upload([self.h_table[:B, :width].ravel()], as_tensors=True)
+        self.d_table[:B, :width].copy_(tab.view(B, width))
         d_rows, d_pos, d_slots, d_plan = self.staging.upload(
             [np.tile(rows, T), all_pos.ravel().astype(np.int32), all_slots.ravel(), plan])
         rx.req_to_token_write(self.d_table, d_rows, d_pos, d_slots, self.stream)
