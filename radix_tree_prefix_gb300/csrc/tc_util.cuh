@@ -75,25 +75,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Like mbar_wait, but a thread that finds the phase incomplete sleeps about
-// `backoff_ns` between polls, leaving issue slots and shared-memory
-// bandwidth to the warps on the critical path (for waits with slack).
-__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, long long limit,
-                                                  uint32_t backoff_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    __nanosleep(backoff_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > limit) {
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
