@@ -228,8 +228,8 @@ struct Layout3 {
   static constexpr int XCH = V0 + VSTAGES * KV_BYTES;
   static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
   // barriers: q, kfull, vfull, emptyk, emptyv (one per stage), s[3], p[3],
-  // o, final, max exchange[2], sum exchange
-  static constexpr int NBAR = 1 + 2 * KSTAGES + 2 * VSTAGES + 2 * SBUF + 5;
+  // o[2] (PV of even / odd tiles), final, max exchange[2], sum exchange
+  static constexpr int NBAR = 1 + 2 * KSTAGES + 2 * VSTAGES + 2 * SBUF + 6;
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   // At head_dim 128 the layout carries 1024 bytes of slack to align the
   // swizzled tiles.  At head_dim 256 it leaves under 1 KB of the 227 KB a CTA
@@ -299,7 +299,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const uint32_t bar = base + Lo::BAR;
   const uint32_t BAR_Q = bar;
   // barrier indices: q, kfull[NK], vfull[NV], emptyk[NK], emptyv[NV], s[NB],
-  // p[NB], o, final, max exchange[2], sum exchange
+  // p[NB], o[2], final, max exchange[2], sum exchange
   auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
   auto BAR_VF = [&](int s) { return bar + 8u * (1 + NK + s); };
   auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (1 + NK + NV + s); };
@@ -307,11 +307,17 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   auto BAR_S = [&](int b) { return bar + 8u * (1 + 2 * NK + 2 * NV + b); };
   auto BAR_P = [&](int b) { return bar + 8u * (1 + 2 * NK + 2 * NV + NB + b); };
   constexpr uint32_t kAfterP = 1 + 2 * NK + 2 * NV + 2 * NB;
-  const uint32_t BAR_O = bar + 8u * kAfterP;
-  const uint32_t BAR_FIN = bar + 8u * (kAfterP + 1);
-  auto XB = [&](int p) { return bar + 8u * (kAfterP + 2 + p); };
-  const uint32_t XE = bar + 8u * (kAfterP + 4);
-  static_assert(kAfterP + 5 == Lo::NBAR, "barrier count");
+  // PV_j completes phase j / 2 of BAR_O(j % 2).  One barrier per parity of
+  // j: when the softmax of tile j waits for PV_{j-1}, PV_{j-3} has completed
+  // (it was issued before S_j, whose completion the softmax waited for), so the
+  // phase parity it waits on cannot be mistaken for an older phase; with a
+  // single barrier PV_{j-2} may still be in flight and the parity would be
+  // ambiguous.
+  auto BAR_O = [&](int p) { return bar + 8u * (kAfterP + p); };
+  const uint32_t BAR_FIN = bar + 8u * (kAfterP + 2);
+  auto XB = [&](int p) { return bar + 8u * (kAfterP + 3 + p); };
+  const uint32_t XE = bar + 8u * (kAfterP + 5);
+  static_assert(kAfterP + 6 == Lo::NBAR, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
 
@@ -339,7 +345,8 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     tc::mbar_init(XB(0), 8 * 32);
     tc::mbar_init(XB(1), 8 * 32);
     tc::mbar_init(XE, 8 * 32);
-    tc::mbar_init(BAR_O, 1);
+    tc::mbar_init(BAR_O(0), 1);
+    tc::mbar_init(BAR_O(1), 1);
     tc::mbar_init(BAR_FIN, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -523,7 +530,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
           mma_ts_split(tmem + uint32_t(Lo::O_COL), p_t + uint32_t(ks * 8),
                        v_lo + uint32_t(ks * 2048 / 16), DHI, IDESC_PV,
                        (j > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(BAR_O);
+        tc::mma_commit(BAR_O(j & 1));
         tc::mma_commit(BAR_EMPTY_V(sv));
         TC_TRACE(5, j);
         if (++sv == NV) {
@@ -632,8 +639,8 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         if (__any_sync(0xffffffffu, need)) {
           // O is rescaled once PV_{j-1} has written it; each warpgroup takes
           // half of its columns
-          if (!__all_sync(0xffffffffu,
-                          tc::mbar_wait(BAR_O, (j - 1) & 1, abort_flag, kWaitLimit))) {
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR_O((j - 1) & 1), ((j - 1) >> 1) & 1,
+                                                      abort_flag, kWaitLimit))) {
             ok = false;
             break;
           }
@@ -664,15 +671,16 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          // p = 2^(scale*s - m) for two keys at once: the exponents are rounded
-          // to bf16 with integer ops (add half an ulp, keep the high half) and
-          // one packed SFU op gives both p in bf16 (the precision P has in the
-          // PV product); the row sum adds exactly those values in fp32, in
-          // eight independent partial sums.
+          // p = 2^(scale*s - m) for two keys: exp2 in fp32 on the SFU, then
+          // both rounded to nearest into one bf16x2 word (the precision P has
+          // in the PV product).  With the lazy max the dominant keys'
+          // exponents reach +8, where a bf16 exponent or a bf16 exp2 result
+          // would cost up to 1% per weight on peaked rows.  The row sum adds
+          // exactly the rounded values in fp32, in eight independent partial
+          // sums.
           const float x0 = fmaf(__uint_as_float(sr[cc * 32 + e]), a.scale_log2, -m_use);
           const float x1 = fmaf(__uint_as_float(sr[cc * 32 + e + 1]), a.scale_log2, -m_use);
-          const uint32_t h = rxk::exp2_bf16x2_bits(__float_as_uint(x0) + 0x8000u,
-                                                   __float_as_uint(x1) + 0x8000u);
+          const uint32_t h = rxk::pack_bf16(rxk::fast_exp2(x0), rxk::fast_exp2(x1));
           l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
           pk[e >> 1] = h;
         }
@@ -690,7 +698,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       if (i == 0) TC_TRACE(wg ? 11 : 7, j);
     }
     // The epilogue waits on BAR_FIN, which completes exactly once, after every
-    // MMA of the CTA (BAR_O's parity would be ambiguous), then the halves add
+    // MMA of the CTA, then the halves add
     // their row sums through shared memory and warpgroup w writes output
     // columns [64 w, 64 w + 64).  Every softmax thread arrives on the
     // exchange barrier, so no waiter is left behind when a wait gave up.

@@ -47,6 +47,7 @@ __device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// (lo, hi) rounded to nearest bf16 and packed, lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -56,24 +57,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// (2^lo, 2^hi) rounded to bf16 and packed (lo in the low half), computed
-// as one packed SFU operation: the inputs are rounded to bf16 first.
-__device__ __forceinline__ uint32_t exp2_bf16x2(float lo, float hi) {
-  uint32_t x, y;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(x) : "f"(hi), "f"(lo));
-  asm("ex2.approx.ftz.bf16x2 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
-
-// Same from fp32 bit patterns already rounded at bit 16: the high halves are
-// packed with a byte permute (lo in the low half) and exponentiated as bf16x2.
-__device__ __forceinline__ uint32_t exp2_bf16x2_bits(uint32_t lo_bits, uint32_t hi_bits) {
-  const uint32_t x = __byte_perm(lo_bits, hi_bits, 0x7632);
-  uint32_t y;
-  asm("ex2.approx.ftz.bf16x2 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
 

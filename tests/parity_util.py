@@ -13,7 +13,7 @@ MEAN_ABS = 1e-3
 
 class DeviceRun:
     def __init__(self, wl, layers=None, sample=None, extend_tokens=None, decode_steps=None,
-                 check_bookkeeping=True):
+                 check_bookkeeping=True, values_fn=None):
         import torch
 
         from radix_tree_prefix_gb300 import rx, workloads
@@ -27,6 +27,8 @@ class DeviceRun:
         self.decode_sel = None if decode_steps is None else set(decode_steps)
         self.dev = torch.device("cuda:0")
         self.vals = workloads.make_values(wl, self.dev, self.layers)
+        if values_fn is not None:  # reshape the inputs (both sides read self.vals)
+            values_fn(self.vals)
         self.ext = {}
         self.dec = {}
         self.rng = np.random.default_rng(123)

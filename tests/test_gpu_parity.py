@@ -129,3 +129,31 @@ def test_multi_turn_chat_full_size_sampled():
     run = DeviceRun(wl, layers=[0, 15], sample={0, 1, 255, 1024, 2047}, extend_tokens=16,
                  decode_steps={0, 31})
     run.assert_close()
+
+
+@pytest.mark.parametrize("head_dim", [128, 256])
+@pytest.mark.parametrize("doubling", [128, 192])
+def test_running_max_grows_over_key_tiles(head_dim, doubling):
+    """Keys of the shared preamble grow in norm along the sequence (x2 every
+    `doubling` positions), so rows are peaked and their running max rises from
+    key tile to key tile: by more than 8 (log2 units) at many tiles, where the
+    tile rescales O in TMEM after waiting for the previous tile's PV product,
+    and by up to 8 at others, where the dominant keys' exponents are positive
+    (relative to the stale max).  A few keys carry each row here, so the
+    rounding of each weight shows in the output instead of averaging out; the
+    tile is held to the same tolerances."""
+    # 12 calls x 4 query heads per KV head: the preamble's decode chunks have
+    # 48 rows and go to the tensor-core tile as well
+    wl = workloads.agent_loop(calls=12, preamble=700, lo=20, hi=60, decode_steps=3,
+                              head_dim=head_dim)
+
+    def ramp(vals):
+        for layer, k in vals["k"].items():
+            n = min(700, k.shape[0])
+            f = torch.exp2(torch.arange(n, device=k.device, dtype=torch.float32) / doubling)
+            k[:n] = (k[:n].float() * f[:, None, None]).to(torch.bfloat16)
+
+    run = DeviceRun(wl, values_fn=ramp)
+    mx, mean, n = run.assert_close()
+    print(f"peaked rows, head_dim {head_dim}, doubling {doubling}: max abs {mx:.2e}, "
+          f"mean abs {mean:.2e} over {n} rows")
