@@ -227,9 +227,13 @@ struct Layout3 {
   // follows the last tile
   static constexpr int XCH = V0 + VSTAGES * KV_BYTES;
   static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
-  // barriers: q, kfull, vfull, emptyk, emptyv (one per stage), s[3], p[3],
-  // o[2] (PV of even / odd tiles), final, max exchange[2], sum exchange
-  static constexpr int NBAR = 1 + 2 * KSTAGES + 2 * VSTAGES + 2 * SBUF + 6;
+  // barriers: q, kfull, vfull (one per stage), s[3], p[3], o[2] (PV of even
+  // / odd tiles), final, max exchange[2], sum exchange.  A K stage is free
+  // again when the S product that read it completes (s[] of the same index:
+  // both rings have three entries) and a V stage when its PV product does
+  // (o[] of the same parity: two V stages).
+  static constexpr int NBAR = 1 + KSTAGES + VSTAGES + 2 * SBUF + 6;
+  static_assert(KSTAGES == SBUF && VSTAGES == 2, "stage rings share the MMA barriers");
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   // At head_dim 128 the layout carries 1024 bytes of slack to align the
   // swizzled tiles.  At head_dim 256 it leaves under 1 KB of the 227 KB a CTA
@@ -298,15 +302,13 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const uint32_t sQ = base + Lo::Q;
   const uint32_t bar = base + Lo::BAR;
   const uint32_t BAR_Q = bar;
-  // barrier indices: q, kfull[NK], vfull[NV], emptyk[NK], emptyv[NV], s[NB],
-  // p[NB], o[2], final, max exchange[2], sum exchange
+  // barrier indices: q, kfull[NK], vfull[NV], s[NB], p[NB], o[2], final,
+  // max exchange[2], sum exchange
   auto BAR_KF = [&](int s) { return bar + 8u * (1 + s); };
   auto BAR_VF = [&](int s) { return bar + 8u * (1 + NK + s); };
-  auto BAR_EMPTY_K = [&](int s) { return bar + 8u * (1 + NK + NV + s); };
-  auto BAR_EMPTY_V = [&](int s) { return bar + 8u * (1 + 2 * NK + NV + s); };
-  auto BAR_S = [&](int b) { return bar + 8u * (1 + 2 * NK + 2 * NV + b); };
-  auto BAR_P = [&](int b) { return bar + 8u * (1 + 2 * NK + 2 * NV + NB + b); };
-  constexpr uint32_t kAfterP = 1 + 2 * NK + 2 * NV + 2 * NB;
+  auto BAR_S = [&](int b) { return bar + 8u * (1 + NK + NV + b); };
+  auto BAR_P = [&](int b) { return bar + 8u * (1 + NK + NV + NB + b); };
+  constexpr uint32_t kAfterP = 1 + NK + NV + 2 * NB;
   // PV_j completes phase j / 2 of BAR_O(j % 2).  One barrier per parity of
   // j: when the softmax of tile j waits for PV_{j-1}, PV_{j-3} has completed
   // (it was issued before S_j, whose completion the softmax waited for), so the
@@ -330,14 +332,8 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
 
   if (tid == 0) {
     tc::mbar_init(BAR_Q, 8 * 32);  // every softmax thread lands half a Q row
-    for (int s = 0; s < NK; ++s) {
-      tc::mbar_init(BAR_KF(s), 1);
-      tc::mbar_init(BAR_EMPTY_K(s), 1);
-    }
-    for (int s = 0; s < NV; ++s) {
-      tc::mbar_init(BAR_VF(s), 1);
-      tc::mbar_init(BAR_EMPTY_V(s), 1);
-    }
+    for (int s = 0; s < NK; ++s) tc::mbar_init(BAR_KF(s), 1);
+    for (int s = 0; s < NV; ++s) tc::mbar_init(BAR_VF(s), 1);
     for (int b = 0; b < NB; ++b) {
       tc::mbar_init(BAR_S(b), 1);
       tc::mbar_init(BAR_P(b), 8 * 32);
@@ -440,20 +436,21 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     load_slots(3, sd);
     // tile j (K stage j % NK, V stage j % NV): K and V with the slots in
     // `slot`, then tile j + 4's table reads into the same registers; a stage
-    // is refilled once the MMA that read its previous tile has completed
+    // is refilled once the MMA that read its previous tile has completed:
+    // S_{j-NK} (barrier s[j % NK]) for K, PV_{j-2} (barrier o[j % 2]) for V
     auto step = [&](int j, int32_t (&slot)[SPL]) -> bool {
       const int sk = j % NK, sv = j % NV;
       check_slots(slot);
       if (!load_v) {
         if (j >= NK &&
-            !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_K(sk), uint32_t(j / NK - 1) & 1u,
+            !__all_sync(0xffffffffu, tc::mbar_wait(BAR_S(sk), uint32_t(j / NK - 1) & 1u,
                                                     abort_flag, kWaitLimit, kSleepNs)))
           return false;
         load_tile(slot, tmk, kb, base + Lo::K0 + sk * Lo::KV_BYTES, BAR_KF(sk));
         if (lane == 0) TC_TRACE(0, j);
       } else {
         if (j >= NV &&
-            !__all_sync(0xffffffffu, tc::mbar_wait(BAR_EMPTY_V(sv), uint32_t(j / NV - 1) & 1u,
+            !__all_sync(0xffffffffu, tc::mbar_wait(BAR_O(sv), uint32_t(j / NV - 1) & 1u,
                                                     abort_flag, kWaitLimit, kSleepNs)))
           return false;
         load_tile(slot, tmv, vb, base + Lo::V0 + sv * Lo::KV_BYTES, BAR_VF(sv));
@@ -503,8 +500,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
           const uint32_t b_off = uint32_t(((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4);
           mma_ss_split(d_s, q_lo + a_off, k_lo + b_off, DHI, IDESC_S, ks > 0 ? 1u : 0u);
         }
-        tc::mma_commit(BAR_S(s_buf));
-        tc::mma_commit(BAR_EMPTY_K(ks_stage));
+        tc::mma_commit(BAR_S(s_buf));  // also frees K stage ks_stage (== s_buf)
         TC_TRACE(4, j);
         if (++ks_stage == NK) {
           ks_stage = 0;
@@ -530,8 +526,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
           mma_ts_split(tmem + uint32_t(Lo::O_COL), p_t + uint32_t(ks * 8),
                        v_lo + uint32_t(ks * 2048 / 16), DHI, IDESC_PV,
                        (j > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(BAR_O(j & 1));
-        tc::mma_commit(BAR_EMPTY_V(sv));
+        tc::mma_commit(BAR_O(j & 1));  // also frees V stage sv (== j & 1)
         TC_TRACE(5, j);
         if (++sv == NV) {
           sv = 0;
