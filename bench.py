@@ -50,14 +50,17 @@ def parse():
     return ap.parse_args()
 
 
-# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
-# captures summarised in profiles/ (cold L2, one launch of the current
-# kernels): decode_fused_kernel on an agent_loop decode step and on a
-# long_shared decode step.  None (absent) where no capture of that launch
-# exists.
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# captures summarised in profiles/ (cold L2, the current kernels):
+# decode_fused_kernel on one agent_loop and one long_shared decode step; the
+# extend kernel averaged over the launches of one step (long_shared: 2,
+# fork_tree: 130), as `achieved` averages over them.  None (absent) where no
+# capture of that launch exists.
 TRAFFIC = {
-    ("agent_loop", "rx_decode_attention"): 44.53e6 + 0.01e6,
-    ("long_shared", "rx_decode_attention"): 406.3e6 + 16.2e6,
+    ("agent_loop", "rx_decode_attention"): 44.534e6 + 0.006e6,
+    ("long_shared", "rx_decode_attention"): 406.35e6 + 16.01e6,
+    ("long_shared", "rx_extend_attention"): (2230.64e6 + 3158.90e6) / 2,
+    ("fork_tree", "rx_extend_attention"): (5711.18e6 + 887.04e6) / 130,
 }
 
 

@@ -596,8 +596,9 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       tc::tmem_ld_wait();
       if (i == 0 && wg == 0) TC_TRACE(8, j);
       // row max of the raw scores over this half (masked keys get a large
-      // negative finite score, so the packed exponent below never sees an
-      // infinity); eight independent partial maxima keep the chains short
+      // negative finite score, so no exponent below is an infinity or a NaN,
+      // even for a row whose keys are all masked); eight independent partial
+      // maxima keep the chains short
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = kMasked;
