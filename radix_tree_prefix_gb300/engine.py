@@ -305,6 +305,7 @@ class Engine:
             self.staging = _Staging(torch, device, self.stream, self._explicit_stream)
         # host staging
         self.h_table = np.zeros((self.max_wave, self.max_ctx), dtype=np.int32)
+        self._wave_arrays = {}
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
 
     # ------------------------------------------------------------------ run
@@ -313,8 +314,8 @@ class Engine:
         self.trace = Trace()
         self.batch_no = 0
         self.step_no = 0
-        for wave in self.wl.waves:
-            self._run_wave(wave)
+        for wi, wave in enumerate(self.wl.waves):
+            self._run_wave(wi, wave)
         self.trace.eviction_log = self.cache.eviction_log()
         st = self.cache.stats()
         self.trace.stats = {
@@ -323,13 +324,34 @@ class Engine:
             "num_nodes": st["num_nodes"]}
         return self.trace
 
-    def _run_wave(self, wave):
+    def _wave_host(self, wi, wave):
+        """The token arrays of a wave's requests, as they arrive: prompt
+        lengths, the prompts concatenated (int32) with their int64 offsets, and
+        each prompt followed by its decode outputs, with offsets.  They depend
+        only on the requests, so they are built on the first run and reused."""
+        h = self._wave_arrays.get(wi)
+        if h is None:
+            wl = self.wl
+            prompts = [np.asarray(wl.prompt_tokens(r), dtype=np.int32) for r in wave]
+            lens = np.array([len(p) for p in prompts], dtype=np.int64)
+            indptr = np.zeros(len(wave) + 1, dtype=np.int64)
+            np.cumsum(lens, out=indptr[1:])
+            tokens = np.concatenate(prompts).astype(np.int32, copy=False)
+            outs = [np.asarray(wl.output_tokens(r)[:wl.decode_steps], dtype=np.int32)
+                    for r in wave]
+            full = np.concatenate([np.concatenate([p, o]) for p, o in zip(prompts, outs)])
+            full = full.astype(np.int32, copy=False)
+            findptr = np.zeros(len(wave) + 1, dtype=np.int64)
+            np.cumsum(lens + wl.decode_steps, out=findptr[1:])
+            h = (lens, indptr, tokens, full, findptr)
+            for arr in h:
+                arr.setflags(write=False)
+            self._wave_arrays[wi] = h
+        return h
+
+    def _run_wave(self, wi, wave):
         wl = self.wl
-        prompts = [wl.prompt_tokens(r).astype(np.int32) for r in wave]
-        lens = np.array([len(p) for p in prompts], dtype=np.int64)
-        indptr = np.zeros(len(wave) + 1, dtype=np.int64)
-        np.cumsum(lens, out=indptr[1:])
-        tokens = np.concatenate(prompts).astype(np.int32)
+        lens, indptr, tokens, full, findptr = self._wave_host(wi, wave)
         self.h_table[:len(wave)] = 0
         prompt_nodes = np.zeros(len(wave), dtype=np.int64)
         # in-batch prefix rule: each batch runs to the first request that would
@@ -342,10 +364,6 @@ class Engine:
         if wl.decode_steps:
             self._decode_phase(wave, lens.astype(np.int32), prompt_nodes)
         # finish: insert prompt ++ outputs, unlock
-        outs = [wl.output_tokens(r)[:wl.decode_steps].astype(np.int32) for r in wave]
-        full = np.concatenate([np.concatenate([p, o]) for p, o in zip(prompts, outs)])
-        findptr = np.zeros(len(wave) + 1, dtype=np.int64)
-        np.cumsum(lens + wl.decode_steps, out=findptr[1:])
         already = self.cache.finish(full, findptr, self.h_table[:len(wave)], lens, prompt_nodes)
         for r, a in zip(wave, already):
             self.trace.finishes.append((r.rid, int(a)))
