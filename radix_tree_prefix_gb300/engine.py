@@ -112,7 +112,11 @@ class PreparedInputs:
     keeps the recorded tensors in pinned host memory and copies them to the
     device when they are used (the end-to-end path): when the engine asks for
     one batch's inputs, the next batch's (in the recorded order) are already
-    being copied on a side stream, so the copies overlap the kernels."""
+    being copied on a side stream, so the copies overlap the kernels.  Each
+    recorded position has device buffers of its own, allocated on the first
+    pass and refilled on every later one once the work that read them on the
+    consumer's stream (everything it had enqueued when it asked for the next
+    position) has completed."""
 
     def __init__(self, source, host=False):
         self.source = source
@@ -123,8 +127,11 @@ class PreparedInputs:
         self.recording = True
         self.h2d_bytes = 0
         self._pos = 0
-        self._ahead = None     # (position, device tensors per layer, event)
+        self._ahead = None     # (position, event: its copy has landed)
         self._copy_stream = None
+        self._dev = {}         # position -> {layer: (q, k, v) device buffers}
+        self._last_use = {}    # position -> event after its last reader
+        self._handed = None    # position handed out last
 
     def freeze(self):
         self.recording = False
@@ -134,12 +141,26 @@ class PreparedInputs:
                     store[key] = {l: tuple(t.cpu().pin_memory() for t in qkv)
                                   for l, qkv in per_layer.items()}
 
-    def _copy(self, per_layer):
-        out = {}
-        for l, qkv in per_layer.items():
-            out[l] = tuple(t.to(self.source.device, non_blocking=True) for t in qkv)
-            self.h2d_bytes += sum(t.numel() * t.element_size() for t in qkv)
-        return out
+    def _fill(self, pos, stream):
+        """Copies position pos's recorded inputs into its device buffers on
+        `stream`, after their previous readers."""
+        import torch
+        name, key = self.order[pos]
+        src = (self.ext if name == "ext" else self.dec)[key]
+        dev = self._dev.get(pos)
+        if dev is None:
+            dev = {l: tuple(torch.empty_like(t, device=self.source.device) for t in qkv)
+                   for l, qkv in src.items()}
+            self._dev[pos] = dev
+        ev = self._last_use.get(pos)
+        if ev is not None:
+            stream.wait_event(ev)
+        with torch.cuda.stream(stream):
+            for l, qkv in src.items():
+                for d, h in zip(dev[l], qkv):
+                    d.copy_(h, non_blocking=True)
+                    self.h2d_bytes += h.numel() * h.element_size()
+        return dev
 
     def _get(self, name, store, key, make):
         if self.recording:
@@ -150,27 +171,31 @@ class PreparedInputs:
             return store[key]
         import torch
         cur = torch.cuda.current_stream(self.source.device)
+        if self._handed is not None:
+            # the consumer has enqueued all its work on the previous position
+            ev = self._last_use.get(self._handed)
+            if ev is None:
+                ev = self._last_use[self._handed] = torch.cuda.Event()
+            ev.record(cur)
         pos = self._pos
         if self.order[pos] != (name, key):     # not the recorded order: start over
             pos = self.order.index((name, key))
             self._ahead = None
         if self._ahead is not None and self._ahead[0] == pos:
-            _, out, ev = self._ahead
-            cur.wait_event(ev)
-            for qkv in out.values():
-                for t in qkv:
-                    t.record_stream(cur)
+            cur.wait_event(self._ahead[1])
+            out = self._dev[pos]
         else:
-            out = self._copy(store[key])
+            out = self._fill(pos, cur)
+        self._handed = pos
         self._pos = (pos + 1) % len(self.order)
-        nname, nkey = self.order[self._pos]
-        if self._copy_stream is None:
-            self._copy_stream = torch.cuda.Stream(self.source.device)
-        with torch.cuda.stream(self._copy_stream):
-            ahead = self._copy((self.ext if nname == "ext" else self.dec)[nkey])
-            ev = torch.cuda.Event()
-            ev.record(self._copy_stream)
-        self._ahead = (self._pos, ahead, ev)
+        self._ahead = None
+        if self._pos != pos:
+            if self._copy_stream is None:
+                self._copy_stream = torch.cuda.Stream(self.source.device)
+            self._fill(self._pos, self._copy_stream)
+            ready = torch.cuda.Event()
+            ready.record(self._copy_stream)
+            self._ahead = (self._pos, ready)
         return out
 
     def extend(self, batch_no, reqs, prefix):
@@ -266,10 +291,15 @@ class Engine:
     ([T][B] tensors per layer).  Every copy and
     launch goes to ``stream``; left as None it is the device's current stream
     when the engine is made, which must then stay current while it runs.
+    With ``reuse_outputs`` the output tensors of each extend batch and decode
+    wave (per layer) are allocated on the first run and written again by
+    every later run: they stay valid until the next run starts, and whoever
+    reads them on another stream must be done (e.g. synchronized) by then.
     """
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
-                 on_decode=None, stream=None, timing=False, on_decode_wave=None):
+                 on_decode=None, stream=None, timing=False, on_decode_wave=None,
+                 reuse_outputs=False):
         self.wl = wl
         self.device = device
         self.inputs = inputs
@@ -288,6 +318,8 @@ class Engine:
         self.max_wave = max(len(w) for w in wl.waves)
         self.gpu_launches = 0
         self.timing = timing
+        self.reuse_outputs = reuse_outputs
+        self._out_bufs = {}
         self.kernel_events = []   # (kind, start event, end event, algorithmic work)
         if device is not None:
             import torch
@@ -408,9 +440,8 @@ class Engine:
         for layer in self.layers:
             q, k, v = inputs[layer]
             rx.kv_store(self.pool, layer, d_slots, k, v, self.stream)
-            out = torch.empty((total_q, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
-                              device=self.device)
-            lse = torch.empty((total_q, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            out, lse = self._outputs(("ext", self.batch_no, layer),
+                                     (total_q, wl.num_q_heads, wl.head_dim))
             call = rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, d_tab,
                                             d_rows, d_prefix, d_qo, d_tiles, R, n_tiles,
                                             self.scale, out, lse, self.stream)
@@ -461,9 +492,8 @@ class Engine:
         outs = {}
         tt = np.arange(T, dtype=np.uint64)
         for layer in self.layers:
-            o = torch.empty((T, B, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
-                            device=self.device)
-            l = torch.empty((T, B, wl.num_q_heads), dtype=torch.float32, device=self.device)
+            o, l = self._outputs(("dec", self.step_no, layer),
+                                 (T, B, wl.num_q_heads, wl.head_dim))
             steps = np.zeros(T, dtype=rx.DECODE_STEP_DTYPE)
             for f, x in zip(("d_q", "d_k", "d_v"), inputs[layer]):
                 steps[f] = x.data_ptr() + tt * np.uint64(x[0].numel() * x.element_size())
@@ -488,6 +518,21 @@ class Engine:
         if self.on_decode_wave is not None:
             self.on_decode_wave(self.step_no, list(rids), ctx0 + 1, outs, info)
         self.step_no += T
+
+    def _outputs(self, key, shape):
+        """fp32 output [..., Hq, d] and lse [..., Hq] tensors for one launch:
+        fresh ones, or with reuse_outputs the ones this key got on an earlier
+        run (same shapes every run)."""
+        torch = self.torch
+        if self.reuse_outputs:
+            bufs = self._out_bufs.get(key)
+            if bufs is not None and tuple(bufs[0].shape) == tuple(shape):
+                return bufs
+        bufs = (torch.empty(shape, dtype=torch.float32, device=self.device),
+                torch.empty(shape[:-1], dtype=torch.float32, device=self.device))
+        if self.reuse_outputs:
+            self._out_bufs[key] = bufs
+        return bufs
 
     def _launches_per_decode(self, infos):
         """Kernels per decode step: kv_store (unless the decode kernel
