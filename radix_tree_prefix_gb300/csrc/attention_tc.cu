@@ -475,7 +475,11 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       // shared-memory descriptors (128-byte swizzle, 1024 bytes between
       // 8-row groups): common high half; low halves of Q, K stage 0 (K-major,
       // leading offset 16 B) and V stage 0 (MN-major, leading offset = one
-      // 64-column block of BN rows)
+      // 64-column block of BN rows).  Fields of the 64-bit descriptor: start
+      // address >> 4 in bits 0-13, leading byte offset >> 4 in bits 16-29,
+      // stride byte offset >> 4 in bits 32-45, version 1 at bit 46, layout
+      // (2 = 128-byte swizzle) in bits 61-63; swizzle atoms (8 rows x 128 B)
+      // start on 1024-byte boundaries
       constexpr uint32_t DHI = (1024u >> 4) | (1u << 14) | (2u << 29);
       constexpr uint32_t KV_STEP = uint32_t(Lo::KV_BYTES) >> 4;
       const uint32_t q_lo = ((sQ & 0x3FFFFu) >> 4) | (1u << 16);

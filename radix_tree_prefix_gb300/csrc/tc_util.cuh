@@ -166,34 +166,11 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ------------------------------------------------------------------- MMA
-// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
-// and stride byte offsets (16-byte units), descriptor version 1, layout
-// SWIZZLE_128B.  Swizzle atoms (8 rows x 128 B) must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
-  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-  d |= uint64_t(1) << 46;
-  d |= uint64_t(2) << 61;
-  return d;
-}
-
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
 // A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn) << 16) |
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-// D(tmem) (+)= A(smem) * B(smem); issued by a single thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
