@@ -264,6 +264,40 @@ def test_single_key_returns_its_value():
     assert lse[0, 0] == pytest.approx(q[0, 0] @ k[0, 0] / math.sqrt(8), abs=1e-15)
 
 
+def test_brute_force_in_exact_and_high_precision_arithmetic():
+    """Tiny inputs (n <= 8 keys, d = 4) with dyadic entries: q.k is formed
+    exactly with fractions, the exponentials and the normalisation at 50
+    digits (mpmath), each query seeing a causal prefix; the fp64 oracle must
+    agree to 1e-13 in the output and the log-sum-exp."""
+    from fractions import Fraction
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    rng = random.Random(7)
+    for trial in range(25):
+        n = rng.randint(1, 8)
+        hq, hkv, d = 2, 1, 4
+        dy = lambda: Fraction(rng.randint(-16, 16), 8)   # exact in binary
+        q = [[[dy() for _ in range(d)] for _ in range(hq)] for _ in range(n)]
+        k = [[[dy() for _ in range(d)] for _ in range(hkv)] for _ in range(n)]
+        v = [[[dy() for _ in range(d)] for _ in range(hkv)] for _ in range(n)]
+        visible = [i + 1 for i in range(n)]
+        o, lse = oatt.softmax_attention(np.array(q, dtype=np.float64),
+                                        np.array(k, dtype=np.float64),
+                                        np.array(v, dtype=np.float64), visible)
+        scale = 1 / mpmath.sqrt(d)            # 1/2 exactly for d = 4
+        for i in range(n):
+            for h in range(hq):
+                dots = [sum(q[i][h][c] * k[j][0][c] for c in range(d)) for j in range(visible[i])]
+                s = [mpmath.mpf(x.numerator) / x.denominator * scale for x in dots]
+                m = max(s)
+                w = [mpmath.exp(x - m) for x in s]
+                z = mpmath.fsum(w)
+                for c in range(d):
+                    want = mpmath.fsum(w[j] * v[j][0][c] for j in range(len(w))) / z
+                    assert abs(o[i, h, c] - float(want)) < 1e-13, (trial, i, h, c)
+                assert abs(lse[i, h] - float(m + mpmath.log(z))) < 1e-13, (trial, i, h)
+
+
 def test_two_keys_closed_form():
     """Score gap ln 3 with scale 1/sqrt(d) gives weights 1/4 and 3/4."""
     d = 4
