@@ -337,7 +337,16 @@ class Engine:
             self.staging = _Staging(torch, device, self.stream, self._explicit_stream)
         # host staging
         self.h_table = np.zeros((self.max_wave, self.max_ctx), dtype=np.int32)
+        self._h_table_p = self.h_table.ctypes.data
         self._wave_arrays = {}
+        # one extend batch's outputs of rx_extend_begin, reused batch to batch
+        # (what outlives the batch is copied out of them)
+        max_wave_tokens = max(sum(len(wl.prompt_tokens(r)) for r in w) for w in wl.waves)
+        self._b_prefix = np.zeros(self.max_wave, dtype=np.int32)
+        self._b_nodes = np.zeros(self.max_wave, dtype=np.int64)
+        self._b_new = np.zeros(max(1, max_wave_tokens), dtype=np.int32)
+        self._b_ptrs = (self._b_prefix.ctypes.data, self._b_nodes.ctypes.data,
+                        self._b_new.ctypes.data)
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
 
     # ------------------------------------------------------------------ run
@@ -375,23 +384,24 @@ class Engine:
             full = full.astype(np.int32, copy=False)
             findptr = np.zeros(len(wave) + 1, dtype=np.int64)
             np.cumsum(lens + wl.decode_steps, out=findptr[1:])
-            h = (lens, indptr, tokens, full, findptr)
-            for arr in h:
+            for arr in (lens, indptr, tokens, full, findptr):
                 arr.setflags(write=False)
+            h = (lens, indptr, tokens, full, findptr, tokens.ctypes.data, indptr.ctypes.data)
             self._wave_arrays[wi] = h
         return h
 
     def _run_wave(self, wi, wave):
         wl = self.wl
-        lens, indptr, tokens, full, findptr = self._wave_host(wi, wave)
+        lens, indptr, tokens, full, findptr, tokens_p, indptr_p = self._wave_host(wi, wave)
         self.h_table[:len(wave)] = 0
         prompt_nodes = np.zeros(len(wave), dtype=np.int64)
+        ptrs = (tokens_p, indptr_p, prompt_nodes.ctypes.data)
         # in-batch prefix rule: each batch runs to the first request that would
         # share more with an earlier member than the tree gives it
         start = 0
         while start < len(wave):
-            end = self.cache.batch_end(tokens, indptr, start)
-            self._extend_batch(wave, start, end, tokens, indptr, prompt_nodes)
+            end = self.cache.batch_end_p(tokens_p, indptr_p, start, len(wave))
+            self._extend_batch(wave, start, end, indptr, ptrs)
             start = end
         if wl.decode_steps:
             self._decode_phase(wave, lens.astype(np.int32), prompt_nodes)
@@ -400,22 +410,33 @@ class Engine:
         for r, a in zip(wave, already):
             self.trace.finishes.append((r.rid, int(a)))
 
-    def _extend_batch(self, wave, j0, j1, tokens, indptr, prompt_nodes):
+    def _extend_batch(self, wave, j0, j1, indptr, ptrs):
+        """Requests j0 .. j1-1 of the wave as one extend batch.  ``indptr`` is
+        the wave's token offsets (this batch's slice of it is passed as is:
+        offsets are relative to the wave's tokens); ``ptrs`` = addresses of
+        the wave's tokens, its offsets and its prompt-node array."""
+        tokens_p, indptr_p, nodes_out_p = ptrs
         reqs = wave[j0:j1]
-        tok = tokens[indptr[j0]:indptr[j1]]
-        ind = indptr[j0:j1 + 1] - indptr[j0]
+        R = j1 - j0
+        ind = indptr[j0:j1 + 1]
+        ind_p = indptr_p + 8 * j0
         table = self.h_table[j0:j1]
-        prefix, match_nodes, new_slots = self.cache.extend_begin(tok, ind, table)
-        recs = []
-        for i, r in enumerate(reqs):
-            n = int(ind[i + 1] - ind[i])
-            recs.append((r.rid, int(prefix[i]), table[i, :n].copy()))
-            self.trace.prefilled += n - int(prefix[i])
-        self.trace.batches.append(recs)
+        table_p = self._h_table_p + 4 * self.max_ctx * j0
+        prefix_p, mnodes_p, new_p = self._b_ptrs
+        total = self.cache.extend_begin_p(R, tokens_p, ind_p, table_p, self.max_ctx, prefix_p,
+                                          mnodes_p, new_p)
+        prefix = self._b_prefix[:R]
+        new_slots = self._b_new[:total]
+        lens = ind[1:] - ind[:-1]
+        # the trace keeps each row as extend_begin wrote it (one copy per batch)
+        rows = table[:, :int(lens.max())].copy()
+        pre, ln = prefix.tolist(), lens.tolist()
+        self.trace.batches.append([(r.rid, pre[i], rows[i, :ln[i]]) for i, r in enumerate(reqs)])
+        self.trace.prefilled += int(lens.sum()) - sum(pre)
         if self.device is not None:
             self._extend_device(reqs, j0, j1, prefix, ind, new_slots)
-        nodes, _ = self.cache.extend_end(tok, ind, table, prefix, match_nodes)
-        prompt_nodes[j0:j1] = nodes
+        self.cache.extend_end_p(R, tokens_p, ind_p, table_p, self.max_ctx, prefix_p, mnodes_p,
+                                nodes_out_p + 8 * j0)
         self.batch_no += 1
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):

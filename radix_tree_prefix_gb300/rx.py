@@ -174,6 +174,8 @@ class RadixCache:
         _check(_lib.rx_cache_create(C.byref(cfg), C.byref(h)))
         self._h = h
         self.num_slots = int(num_slots)
+        self._i32 = C.c_int32()
+        self._i64 = C.c_int64()
 
     def close(self):
         if self._h:
@@ -193,6 +195,32 @@ class RadixCache:
         _check(_lib.rx_batch_end(self._h, _p(tokens), _p(indptr), int(start), len(indptr) - 1,
                                  C.byref(out)))
         return out.value
+
+    # Pointer forms of the batch steps, for a caller that keeps its arrays
+    # (the engine): every argument named *_p is the address of a contiguous
+    # array of the C type the header gives, owned by the caller.  They skip
+    # the per-call array handling of the forms above; offsets in an indptr
+    # are relative to the tokens pointer passed with it.
+    def batch_end_p(self, tokens_p, indptr_p, start, R):
+        _check(_lib.rx_batch_end(self._h, tokens_p, indptr_p, int(start), int(R),
+                                 C.byref(self._i32)))
+        return self._i32.value
+
+    def extend_begin_p(self, R, tokens_p, indptr_p, table_p, row_stride, prefix_p, nodes_p,
+                       new_p):
+        """rx_extend_begin; returns the number of new slots written at new_p."""
+        _check(_lib.rx_extend_begin(self._h, int(R), tokens_p, indptr_p, table_p,
+                                    int(row_stride), prefix_p, nodes_p, new_p,
+                                    C.byref(self._i64)))
+        return self._i64.value
+
+    def extend_end_p(self, R, tokens_p, indptr_p, table_p, row_stride, prefix_p, nodes_p,
+                     out_nodes_p):
+        """rx_extend_end; returns the number of rows rewritten with tree slots."""
+        _check(_lib.rx_extend_end(self._h, int(R), tokens_p, indptr_p, table_p,
+                                  int(row_stride), prefix_p, nodes_p, out_nodes_p,
+                                  C.byref(self._i64)))
+        return self._i64.value
 
     # S1
     def match_length(self, tokens):
