@@ -351,3 +351,51 @@ def oracle_common(a, b):
     while k < n and a[k] == b[k]:
         k += 1
     return k
+
+
+def test_pointer_forms_match_array_forms():
+    """The pointer forms of the batch steps, given a batch's slice of the
+    wave's offsets (offsets relative to the wave's tokens) and reused output
+    buffers, give the array forms' results: same batch ends, prefixes, new
+    slots, slot-table rows and prompt nodes, on twin caches."""
+    rng = np.random.default_rng(11)
+    base = rng.integers(1, 40, size=120).astype(np.int32)
+    prompts = []
+    for i in range(14):
+        cut = int(rng.choice([0, 30, 119, 120]))
+        tail = rng.integers(1, 40, size=int(rng.integers(1, 30))).astype(np.int32)
+        prompts.append(np.concatenate([base[:cut], tail]))
+    prompts.append(prompts[2].copy())
+    tokens = np.concatenate(prompts).astype(np.int32)
+    indptr = np.zeros(len(prompts) + 1, dtype=np.int64)
+    np.cumsum([len(p) for p in prompts], out=indptr[1:])
+    W, S = len(prompts), 200
+    ca, cp = rx.RadixCache(5000), rx.RadixCache(5000)
+    ta, tp = np.zeros((W, S), np.int32), np.zeros((W, S), np.int32)
+    na, npn = np.zeros(W, np.int64), np.zeros(W, np.int64)
+    b_prefix, b_nodes = np.zeros(W, np.int32), np.zeros(W, np.int64)
+    b_new = np.zeros(len(tokens), np.int32)
+    start = 0
+    while start < W:
+        end = ca.batch_end(tokens, indptr, start)
+        assert cp.batch_end_p(tokens.ctypes.data, indptr.ctypes.data, start, W) == end
+        R = end - start
+        tok = tokens[indptr[start]:indptr[end]]
+        ind = indptr[start:end + 1] - indptr[start]
+        prefix, mnodes, new = ca.extend_begin(tok, ind, ta[start:end])
+        ind_p = indptr.ctypes.data + 8 * start
+        row_p = tp.ctypes.data + 4 * S * start
+        total = cp.extend_begin_p(R, tokens.ctypes.data, ind_p, row_p, S, b_prefix.ctypes.data,
+                                  b_nodes.ctypes.data, b_new.ctypes.data)
+        assert total == len(new)
+        assert np.array_equal(b_prefix[:R], prefix) and np.array_equal(b_new[:total], new)
+        assert np.array_equal(tp[start:end], ta[start:end])
+        nodes, rew = ca.extend_end(tok, ind, ta[start:end], prefix, mnodes)
+        rew_p = cp.extend_end_p(R, tokens.ctypes.data, ind_p, row_p, S, b_prefix.ctypes.data,
+                                b_nodes.ctypes.data, npn.ctypes.data + 8 * start)
+        na[start:end] = nodes
+        assert rew_p == rew
+        assert np.array_equal(tp[start:end], ta[start:end])
+        start = end
+    assert np.array_equal(npn, na)
+    assert ca.stats() == cp.stats()
