@@ -203,7 +203,9 @@ rx_status rx_node_depth(const rx_cache* cache, rx_node node,
  * ---------------------------------------------------------------------- */
 
 /* S1+S2+S3+S4 for an extend batch of R requests.  tokens holds the prompts
- * back to back, request r at [tok_indptr[r], tok_indptr[r+1]).  In request
+ * back to back, request r at [tok_indptr[r], tok_indptr[r+1]) (offsets need
+ * not start at 0: a batch of a wave may pass the wave's tokens and its slice
+ * of the wave's offsets; the same holds for rx_extend_end).  In request
  * order: rx_match_prefix on the prompt without its last token (the last prompt
  * token is always recomputed) and rx_lock of the matched node; then ONE
  * rx_alloc of all new tokens, handed out in request order.  Writes
