@@ -454,3 +454,140 @@ def test_pool_store_writes_only_its_slots():
     untouched = [s for s in range(10) if s not in (7, 2, 5)]
     assert np.array_equal(out[1, :, untouched, :], base[1, :, untouched, :])
     assert np.array_equal(out[0], base[0])
+
+
+# ------------------------------------------------- decode, finish, adoption
+def _tree_slots(cache):
+    """Every slot the tree holds, node by node."""
+    out = []
+    stack = [cache.root]
+    while stack:
+        n = stack.pop()
+        out.extend(n.value)
+        stack.extend(n.children.values())
+    return out
+
+
+def _assert_slots_conserved(cache):
+    """Once every request has finished, each slot 1 .. N-1 is either held by
+    exactly one tree position or on the free list, never both and never
+    neither (no slot leaked, none handed out twice)."""
+    held = _tree_slots(cache) + list(cache.free_slots)
+    assert sorted(held) == list(range(1, cache.num_slots)), "slots leaked or duplicated"
+    assert len(set(_tree_slots(cache))) == cache.cached_size()
+
+
+def _agent_steps_with_actions(actions, seed=5):
+    """The agent example run through decode: a 2,000-token preamble and 200
+    new tokens per step, of which the first ``actions`` are the previous
+    step's decoded action (its outputs) and the rest fresh tool tokens (step
+    1's 200 tokens are all fresh).  Step k's prompt has 2,000 + 200 k tokens."""
+    g = _golden_kv("agent_step_reuse.txt")
+    rng = random.Random(seed)
+    fresh = lambda n: [rng.randrange(32000) for _ in range(n)]
+    prompt = fresh(g["instructions"]) + fresh(g["per_step"])
+    waves = []
+    for k in range(1, g["step"] + 1):
+        outs = fresh(actions)
+        waves.append([(k, list(prompt), outs)])
+        prompt = prompt + outs + fresh(g["per_step"] - actions)
+    return waves, g
+
+
+@pytest.mark.parametrize("actions", [0, 8, 32])
+def test_agent_steps_through_decode_reuse(actions):
+    """"The problem SGLang solves" ("Pause and think"): step 5's prompt of
+    3,000 tokens finds 2,800 of them already computed by steps 1-4.  With
+    step 4's action decoded before step 5 ("How RadixAttention reuses past
+    work", step 4: the output tokens become nodes of the tree at finish),
+    step 5 reuses step 4's whole prompt plus that action: 2,800 + D tokens
+    for an action of D tokens, and every earlier step k reuses 2,000 +
+    200 (k-1) + D.  A finish that drops the outputs reuses only 2,800."""
+    waves, g = _agent_steps_with_actions(actions)
+    trace, cache = run_bookkeeping(waves, 10000, actions)
+    for k in range(2, g["step"] + 1):
+        rid, m, row = trace.batches[k - 1][0]
+        assert len(row) == g["instructions"] + g["per_step"] * k
+        assert m == g["instructions"] + g["per_step"] * (k - 1) + actions
+    rid, m, row = trace.batches[g["step"] - 1][0]
+    assert len(row) == g["prompt_tokens"] and m == g["reused"] + actions
+    # each step's decoded action sits in the tree on the slots its decode
+    # steps allocated (one per step, in order)
+    last_rid, last_prompt, last_outs = waves[-1][0]
+    full = last_prompt + last_outs
+    assert cache.match_length(full) == len(full)
+    tree_row = cache.lookup_slots(full)
+    for k, wave in enumerate(waves):
+        _, prompt, outs = wave[0]
+        decoded = [trace.decode_steps[k * actions + t][0][1] for t in range(actions)]
+        assert tree_row[len(prompt):len(prompt) + actions] == decoded
+    # at finish only the prompt (inserted when its extend ended) is cached
+    assert [a for _, a in trace.finishes] == [len(w[0][1]) for w in waves]
+    _assert_slots_conserved(cache)
+
+
+def test_identical_samples_share_prompt_and_free_duplicate_outputs():
+    """Two samples of one prompt that decode the same tokens ("One tree for
+    everybody": matched state is pointed at, not stored twice).  The second
+    request waits for the first (the in-batch rule), recomputes only its last
+    prompt token and then points at the first one's slots for the whole
+    prompt; at finish the second finds the first's outputs cached and frees
+    its own copies.  Afterwards every slot is held exactly once."""
+    rng = random.Random(17)
+    prompt = [rng.randrange(32000) for _ in range(40)]
+    outs = [rng.randrange(32000) for _ in range(6)]
+    other = prompt[:10] + [rng.randrange(32000) for _ in range(7)]
+    waves = [[(0, prompt, outs), (1, list(prompt), list(outs)),
+              (2, other, [rng.randrange(32000) for _ in range(6)])]]
+    rows_seen = {}
+
+    def on_decode(step, rows):
+        rows_seen[step] = rows
+
+    trace, cache = run_bookkeeping(waves, 200, 6, on_decode=on_decode)
+    assert [[rid for rid, _, _ in b] for b in trace.batches] == [[0], [1, 2]]
+    _, m1, row1 = trace.batches[1][0]
+    assert m1 == len(prompt) - 1
+    # the second sample's prompt row is the first's, slot for slot
+    for step, rows in rows_seen.items():
+        assert rows[1][:len(prompt)] == rows[0][:len(prompt)]
+        assert rows[1][len(prompt):] != rows[0][len(prompt):]   # own decode slots
+    assert trace.finishes == [(0, len(prompt)), (1, len(prompt) + 6), (2, len(other))]
+    assert cache.cached_size() == len(prompt) + 6 + (len(other) - 10) + 6
+    _assert_slots_conserved(cache)
+
+
+def test_chat_turn_reuses_whole_history():
+    """Multi-turn chat: turn t+1 of a session is its history (system prompt,
+    earlier user turns and the replies decoded for them) plus a new user
+    turn, and with a pool that never evicts it reuses the whole history; at
+    the end every slot is held exactly once."""
+    wl = workloads.multi_turn_chat(sessions=5, turns=4, system=60, user=9, decode_steps=4,
+                                   layers=1)
+    waves = wl.oracle_waves()
+    trace, cache = run_bookkeeping(waves, wl.num_slots, wl.decode_steps)
+    hist = {}
+    batches = [rec for b in trace.batches for rec in b]
+    by_rid = {rid: (m, row) for rid, m, row in batches}
+    for wave in waves:
+        for rid, prompt, outs in wave:
+            m, row = by_rid[rid]
+            sess = rid % 5
+            want = hist.get(sess, 60 if rid else 0)   # the very first request finds nothing
+            assert m == want, (rid, m, want)
+            hist[sess] = len(prompt) + len(outs)
+    _assert_slots_conserved(cache)
+
+
+@pytest.mark.parametrize("make", [
+    lambda: workloads.agent_loop(calls=7, preamble=120, lo=5, hi=40, decode_steps=5),
+    lambda: workloads.fork_tree(branching=3, depth=3, level_tokens=12, decode_steps=3),
+    lambda: workloads.long_shared(batch=6, prefix=90, unique=11, decode_steps=4),
+])
+def test_request_flow_conserves_slots(make):
+    """Every slot is held exactly once after the flow ends, eviction and slot
+    reuse included (fork_tree's pool holds 60% of its distinct tokens)."""
+    wl = make()
+    trace, cache = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+    _assert_slots_conserved(cache)
+    assert trace.stats["protected"] == 0
