@@ -32,11 +32,9 @@
  *     error rx_last_error() returns a text for the calling thread.
  *   - The library owns the tree (opaque rx_cache).  The caller owns every host
  *     array and every device buffer (raw pointers, e.g. from torch tensors)
- *     and the CUDA stream.  The library never allocates device memory; on its
- *     first decode call on a device it creates one non-blocking side stream
- *     and two events there, which rx_decode_attention uses to run its
- *     independent kernels concurrently (forked from and joined back into the
- *     caller's stream, so stream order is kept).
+ *     and the CUDA stream.  The library never allocates device memory and
+ *     creates no streams or events: every kernel runs on the caller's
+ *     stream, in call order.
  *   - Host calls are synchronous and not thread-safe for one cache.  Device
  *     calls only enqueue work on the given stream (cudaStream_t passed as
  *     rx_stream_t; NULL is the legacy default stream) and return RX_ERR_CUDA
@@ -357,17 +355,22 @@ typedef struct rx_pool_desc {
 /* S5 ([L] "A quick recap": a token's keys and values are stored in the
  * cache): K_pool[layer][h][d_slots[i]][:] = d_k[i][h][:], same for V, for
  * i < T.  d_k, d_v: device bf16 [T][Hkv][head_dim], 16-byte aligned.
- * Slots must be distinct and in [1, num_slots) (not checked on the device). */
+ * Slots must be distinct.  A slot outside [1, num_slots) is skipped on the
+ * device and reported by rx_device_check (bit 0). */
 rx_status rx_kv_store(const rx_pool_desc* pool, int32_t layer,
                       const int32_t* d_slots, const void* d_k,
                       const void* d_v, int64_t T, rx_stream_t stream);
 
 /* Device req_to_token append: d_table[d_rows[i]*row_stride + d_pos[i]] =
- * d_slots[i] for i < n (used to add decode tokens to device rows). */
-rx_status rx_req_to_token_write(int32_t* d_table, int64_t row_stride,
-                                const int32_t* d_rows, const int32_t* d_pos,
-                                const int32_t* d_slots, int64_t n,
-                                rx_stream_t stream);
+ * d_slots[i] for i < n (used to add decode tokens to device rows).  d_table
+ * is device int32 [num_rows][row_stride]; d_rows, d_pos, d_slots device
+ * int32 [n].  An entry whose row is outside [0, num_rows) or whose position
+ * is outside [0, row_stride) is skipped on the device and reported by
+ * rx_device_check (bit 4). */
+rx_status rx_req_to_token_write(int32_t* d_table, int64_t num_rows,
+                                int64_t row_stride, const int32_t* d_rows,
+                                const int32_t* d_pos, const int32_t* d_slots,
+                                int64_t n, rx_stream_t stream);
 
 /* Host tile schedule for rx_extend_attention: tile_indptr[R+1] = prefix sums
  * of the query-row tiles of each request (request r has
@@ -481,9 +484,12 @@ rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_t layer,
  * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel
  * read a slot outside [0, num_slots) from req_to_token and used slot 0
  * instead; bit 2 = a tensor-core kernel gave up a barrier wait after its
- * time limit (about 2 s) and returned without results; bit 3 = a
+ * time limit (about 2 s) and returned without results (every output of
+ * that launch is void; its CTAs still wait, bounded, for the loads and
+ * tensor-core operations they had issued before they exit); bit 3 = a
  * tensor-core tile found its dynamic shared memory off a 1024-byte boundary
- * and returned without results.  Returns RX_ERR_CUDA
+ * and returned without results; bit 4 = rx_req_to_token_write met a row or
+ * position outside the table and skipped that entry.  Returns RX_ERR_CUDA
  * if a flag was set or the device reported an error. */
 rx_status rx_device_check(int32_t* out_flags);
 

@@ -52,24 +52,6 @@
 // memory off a 1024-byte boundary and did nothing.  Read by rx_device_check().
 static __device__ int32_t g_tc_error;
 
-#ifdef RX_TC_TRACE
-// Development timeline of CTA (0, 0): globaltimer stamps per tile and role.
-// Compiled only with -DRX_TC_TRACE (never in the library build).
-static __device__ unsigned long long g_tc_trace[16][256];
-__device__ __forceinline__ unsigned long long tc_now() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-#define TC_TRACE(ev, j)                                                          \
-  do {                                                                           \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < 256) g_tc_trace[ev][j] = tc_now(); \
-  } while (0)
-#else
-#define TC_TRACE(ev, j) \
-  do {                  \
-  } while (0)
-#endif
 
 namespace {
 
@@ -328,7 +310,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const int lane = tid & 31;
   const TileDesc t = describe<DECODE>(a, bx);
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
-  if (tid == 0) TC_TRACE(14, 0);
 
   if (tid == 0) {
     tc::mbar_init(BAR_Q, 8 * 32);  // every softmax thread lands half a Q row
@@ -438,6 +419,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // `slot`, then tile j + 4's table reads into the same registers; a stage
     // is refilled once the MMA that read its previous tile has completed:
     // S_{j-NK} (barrier s[j % NK]) for K, PV_{j-2} (barrier o[j % 2]) for V
+    int issued = 0;  // tiles whose K (or V) load has been issued
     auto step = [&](int j, int32_t (&slot)[SPL]) -> bool {
       const int sk = j % NK, sv = j % NV;
       check_slots(slot);
@@ -447,15 +429,14 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
                                                     abort_flag, kWaitLimit, kSleepNs)))
           return false;
         load_tile(slot, tmk, kb, base + Lo::K0 + sk * Lo::KV_BYTES, BAR_KF(sk));
-        if (lane == 0) TC_TRACE(0, j);
       } else {
         if (j >= NV &&
             !__all_sync(0xffffffffu, tc::mbar_wait(BAR_O(sv), uint32_t(j / NV - 1) & 1u,
                                                     abort_flag, kWaitLimit, kSleepNs)))
           return false;
         load_tile(slot, tmv, vb, base + Lo::V0 + sv * Lo::KV_BYTES, BAR_VF(sv));
-        if (lane == 0) TC_TRACE(2, j);
       }
+      issued = j + 1;
       load_slots(j + 4, slot);
       return true;
     };
@@ -465,6 +446,20 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       if (j + 2 < n_tiles && !step(j + 2, sc)) break;
       if (j + 3 < n_tiles && !step(j + 3, sd)) break;
     }
+    // Before the CTA gives up its shared memory, the last load of every
+    // stage has landed.  On the normal path the MMAs consumed them all and
+    // these waits return at once; after a wait of another warp timed out
+    // (abort), TMA box loads may still be in flight, so they get one more
+    // bounded wait that does not look at the abort flag.
+    if (lane == 0) {
+      const int NS = load_v ? NV : NK;
+      int drain_abort = 0;
+      for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
+        const uint32_t fb = load_v ? BAR_VF(j % NV) : BAR_KF(j % NK);
+        tc::mbar_wait(fb, uint32_t(j / NS) & 1u, &drain_abort, kWaitLimit);
+      }
+    }
+    __syncwarp();
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue
     // S_j = Q K_j^T into S buffer j % 3 (two tiles ahead of the softmax), then
@@ -494,7 +489,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       auto issue_s = [&](int j) -> bool {
         if (!tc::mbar_wait(BAR_KF(ks_stage), k_phase, abort_flag, kWaitLimit, kSleepNs))
           return false;
-        TC_TRACE(1, j);
         tc::tc_fence_after();
         const uint32_t k_lo = k_lo0 + uint32_t(ks_stage) * KV_STEP;
         const uint32_t d_s = tmem + uint32_t(s_buf * BN);
@@ -505,7 +499,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
           mma_ss_split(d_s, q_lo + a_off, k_lo + b_off, DHI, IDESC_S, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(BAR_S(s_buf));  // also frees K stage ks_stage (== s_buf)
-        TC_TRACE(4, j);
         if (++ks_stage == NK) {
           ks_stage = 0;
           k_phase ^= 1u;
@@ -518,10 +511,8 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       uint32_t v_phase = 0, p_phase = 0;
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 2 < n_tiles && !issue_s(j + 2)) break;
-        TC_TRACE(15, j);
         if (!tc::mbar_wait(BAR_P(pb), p_phase, abort_flag, kWaitLimit, kSleepNs)) break;
         if (!tc::mbar_wait(BAR_VF(sv), v_phase, abort_flag, kWaitLimit, kSleepNs)) break;
-        TC_TRACE(3, j);
         tc::tc_fence_after();
         const uint32_t v_lo = v_lo0 + uint32_t(sv) * KV_STEP;
         const uint32_t p_t = tmem + uint32_t(pb * BN);
@@ -531,7 +522,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
                        v_lo + uint32_t(ks * 2048 / 16), DHI, IDESC_PV,
                        (j > 0 || ks > 0) ? 1u : 0u);
         tc::mma_commit(BAR_O(j & 1));  // also frees V stage sv (== j & 1)
-        TC_TRACE(5, j);
         if (++sv == NV) {
           sv = 0;
           v_phase ^= 1u;
@@ -541,9 +531,13 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
           p_phase ^= 1u;
         }
       }
-      // drain: every MMA issued above has completed once this arrives
+      // drain: every MMA issued above has completed once this arrives.  The
+      // wait ignores the abort flag (bounded all the same): after another
+      // warp gave up, MMAs already issued must finish writing TMEM and
+      // reading shared memory before the CTA frees both.
       tc::mma_commit(BAR_FIN);
-      tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit);
+      int drain_abort = 0;
+      tc::mbar_wait(BAR_FIN, 0, &drain_abort, kWaitLimit);
     }
     __syncwarp();
   } else {
@@ -592,13 +586,11 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         break;
       }
       tc::tc_fence_after();
-      if (i == 0 && wg == 0) TC_TRACE(6, j);
       const int k0 = t.key_begin + j * BN + wg * HALF;  // first key of this half
       const bool need_mask = k0 + HALF > t.nomask_end;
       uint32_t sr[HALF];
       tc::tmem_ld_row<HALF>(tl + uint32_t(s * BN + wg * HALF), sr);
       tc::tmem_ld_wait();
-      if (i == 0 && wg == 0) TC_TRACE(8, j);
       // row max of the raw scores over this half (masked keys get a large
       // negative finite score, so no exponent below is an infinity or a NaN,
       // even for a row whose keys are all masked); eight independent partial
@@ -628,7 +620,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         break;
       }
       const float mx_other = xch[((j & 1) * 2 + (1 - wg)) * BM + i];
-      if (i == 0 && wg == 0) TC_TRACE(9, j);
       const float mx = a.scale_log2 * fmaxf(mx_half, mx_other);
       const float m_new = fmaxf(m_ref, mx);
       if (j == 0) {
@@ -686,16 +677,12 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         }
         // keys of this half, two per column, over the first BN/2 columns
         // of S_j's buffer (half w at columns w BN/4 ..)
-        if (cc == HALF / 32 - 1 && i == 0 && wg == 0) TC_TRACE(12, j);
         tmem_st16(tl + uint32_t(s * BN + wg * (HALF / 2) + 16 * cc), pk);
       }
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      if (i == 0 && wg == 0) TC_TRACE(13, j);
       tc::tmem_st_wait();
-      if (i == 0 && wg == 0) TC_TRACE(10, j);
       tc::tc_fence_before();
       tc::mbar_arrive(BAR_P(s));
-      if (i == 0) TC_TRACE(wg ? 11 : 7, j);
     }
     // The epilogue waits on BAR_FIN, which completes exactly once, after every
     // MMA of the CTA, then the halves add
@@ -705,7 +692,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     const bool fin = ok && n_tiles > 0 &&
                      __all_sync(0xffffffffu, tc::mbar_wait(BAR_FIN, 0, abort_flag, kWaitLimit));
     if (DECODE && a.early_inputs) rxk::griddep_wait();  // the previous merge read ws
-    if (i == 0 && wg == 0) TC_TRACE(14, 1);
     // (a thread got here after every thread passed the exchange of tile
     // n_tiles - 1, hence had read the slot of tile n_tiles - 2)
     if (fin) xch[((n_tiles & 1) * 2 + wg) * BM + i] = l;
@@ -760,7 +746,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       }
       if (valid && wg == 0) *lse_dst = m_ref * kLn2 + logf(l_all);
     }
-    if (i == 0 && wg == 0) TC_TRACE(14, 2);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -769,7 +754,6 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Lo::TMEM_COLS);
   }
-  if (tid == 0) TC_TRACE(14, 3);
 }
 
 // Extend: one tile per CTA, heaviest row tile first.  With few waves of CTAs
@@ -1314,14 +1298,6 @@ rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsig
 }  // namespace
 
 namespace rx_internal {
-
-#ifdef RX_TC_TRACE
-void tc_trace_read(unsigned long long* out) {
-  cudaMemcpyFromSymbol(out, g_tc_trace, sizeof(g_tc_trace));
-  static unsigned long long zero[16 * 256];
-  cudaMemcpyToSymbol(g_tc_trace, zero, sizeof(g_tc_trace));
-}
-#endif
 
 int32_t tc_error_flags(bool clear) {
   int32_t v = 0;

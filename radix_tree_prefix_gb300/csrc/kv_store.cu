@@ -18,8 +18,9 @@
 #include "rx.h"
 #include "rx_internal.h"
 
-// Set (bit 0) when a kernel of this file met a slot outside [1, num_slots);
-// the offending write is skipped.  Read by rx_device_check().
+// Bit 0: rx_kv_store met a slot outside [1, num_slots); bit 4:
+// rx_req_to_token_write met a row or position outside the table.  The
+// offending write is skipped either way.  Read by rx_device_check().
 static __device__ int32_t g_kv_store_error;
 
 namespace {
@@ -52,12 +53,21 @@ __global__ void __launch_bounds__(256) kv_store_kernel(uint4* __restrict__ kdst,
   }
 }
 
-__global__ void r2t_write_kernel(int32_t* __restrict__ table, int64_t stride,
+// table[rows[i]][pos[i]] = slots[i]; an entry whose row is outside
+// [0, num_rows) or whose position is outside [0, stride) is skipped and sets
+// bit 4 of the error word, so a bad index never writes outside the table.
+__global__ void r2t_write_kernel(int32_t* __restrict__ table, int64_t num_rows, int64_t stride,
                                  const int32_t* __restrict__ rows,
                                  const int32_t* __restrict__ pos,
                                  const int32_t* __restrict__ slots, int64_t n) {
   int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < n) table[int64_t(rows[i]) * stride + pos[i]] = slots[i];
+  if (i >= n) return;
+  const int32_t r = rows[i], p = pos[i];
+  if (r < 0 || r >= num_rows || p < 0 || p >= stride) {
+    atomicOr(&g_kv_store_error, 16);
+    return;
+  }
+  table[int64_t(r) * stride + p] = slots[i];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -137,16 +147,17 @@ extern "C" rx_status rx_kv_store(const rx_pool_desc* pool, int32_t layer, const 
   return rx_internal::launch_status("rx_kv_store");
 }
 
-extern "C" rx_status rx_req_to_token_write(int32_t* d_table, int64_t row_stride,
-                                           const int32_t* d_rows, const int32_t* d_pos,
-                                           const int32_t* d_slots, int64_t n,
-                                           rx_stream_t stream) {
-  if (n < 0 || (n && (!d_table || !d_rows || !d_pos || !d_slots)) || row_stride <= 0)
+extern "C" rx_status rx_req_to_token_write(int32_t* d_table, int64_t num_rows,
+                                           int64_t row_stride, const int32_t* d_rows,
+                                           const int32_t* d_pos, const int32_t* d_slots,
+                                           int64_t n, rx_stream_t stream) {
+  if (n < 0 || (n && (!d_table || !d_rows || !d_pos || !d_slots)) || row_stride <= 0 ||
+      num_rows < 0)
     return rx_internal::set_error(RX_ERR_INVALID, "rx_req_to_token_write: bad argument");
   if (n == 0) return RX_OK;
   r2t_write_kernel<<<unsigned((n + 255) / 256), 256, 0,
-                     reinterpret_cast<cudaStream_t>(stream)>>>(d_table, row_stride, d_rows,
-                                                                d_pos, d_slots, n);
+                     reinterpret_cast<cudaStream_t>(stream)>>>(d_table, num_rows, row_stride,
+                                                                d_rows, d_pos, d_slots, n);
   return rx_internal::launch_status("rx_req_to_token_write");
 }
 
@@ -162,11 +173,13 @@ extern "C" rx_status rx_device_check(int32_t* out_flags) {
   if (out_flags) *out_flags = f;
   if (f)
     return rx_internal::set_error(RX_ERR_CUDA,
-                                  (f & 8)   ? "rx_device_check: a tensor-core tile found its "
-                                              "shared memory misaligned"
-                                  : (f & 4) ? "rx_device_check: a tensor-core kernel timed out "
-                                              "waiting on a barrier"
-                                            : "rx_device_check: a kernel met a slot outside the pool");
+                                  (f & 8)    ? "rx_device_check: a tensor-core tile found its "
+                                               "shared memory misaligned"
+                                  : (f & 4)  ? "rx_device_check: a tensor-core kernel timed out "
+                                               "waiting on a barrier"
+                                  : (f & 16) ? "rx_device_check: a slot-table write met a row "
+                                               "or position outside the table"
+                                             : "rx_device_check: a kernel met a slot outside the pool");
   return RX_OK;
 }
 

@@ -108,7 +108,7 @@ _SIGS = {
     "rx_plan_decode_steps": [P, I32, I32, P, P, P, I32, I32, I32, P, I64, P],
     "rx_alloc_steps": [P, I64, I32, P],
     "rx_kv_store": [P, I32, P, P, P, I64, P],
-    "rx_req_to_token_write": [P, I64, P, P, P, I64, P],
+    "rx_req_to_token_write": [P, I64, I64, P, P, P, I64, P],
     "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
     "rx_extend_attention": [P, I32, P, I32, P, I64, P, P, P, P, I32, I64, F32, P, P, P],
     "rx_decode_attention": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P, SZ, P],
@@ -384,9 +384,9 @@ def kv_store(pool, layer, d_slots, d_k, d_v, stream=None):
 
 
 def req_to_token_write(d_table, d_rows, d_pos, d_slots, stream=None):
-    _check(_lib.rx_req_to_token_write(d_table.data_ptr(), d_table.shape[1], d_rows.data_ptr(),
-                                      d_pos.data_ptr(), d_slots.data_ptr(), d_slots.numel(),
-                                      _stream(stream)))
+    _check(_lib.rx_req_to_token_write(d_table.data_ptr(), d_table.shape[0], d_table.shape[1],
+                                      d_rows.data_ptr(), d_pos.data_ptr(), d_slots.data_ptr(),
+                                      d_slots.numel(), _stream(stream)))
 
 
 def extend_attention_call(pool, layer, d_q, hq, d_table, d_req_rows, d_prefix_len,

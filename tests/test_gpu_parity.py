@@ -40,6 +40,37 @@ def test_kv_store_bit_exact(d, hkv, T):
     assert np.array_equal(vp.float().cpu().numpy(), want_v)
 
 
+def test_out_of_range_indices_are_skipped_and_reported():
+    """A slot outside the pool (kv_store) or a row or position outside the
+    slot table (req_to_token write) is skipped on the device, leaves memory
+    untouched and is reported by rx_device_check (bits 0 and 4)."""
+    dev = torch.device("cuda:0")
+    kp = torch.zeros((1, 2, 64, 128), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    k = torch.ones((3, 2, 128), dtype=torch.bfloat16, device=dev)
+    slots = torch.tensor([5, 64, 7], dtype=torch.int32, device=dev)   # 64 is outside
+    rx.kv_store(rx.pool_desc(kp, vp), 0, slots, k, k)
+    torch.cuda.synchronize()
+    with pytest.raises(rx.RxError) as e:
+        rx.device_check()
+    assert "(flags 1)" in str(e.value)
+    assert int((kp[0, :, 5] != 0).sum()) == 256 and int((kp[0, :, 7] != 0).sum()) == 256
+    assert int((kp != 0).sum()) == 512
+    table = torch.zeros((4, 16), dtype=torch.int32, device=dev)
+    rows = torch.tensor([0, 4, 1, -1, 2], dtype=torch.int32, device=dev)
+    pos = torch.tensor([3, 0, 16, 0, 15], dtype=torch.int32, device=dev)
+    vals = torch.tensor([11, 12, 13, 14, 15], dtype=torch.int32, device=dev)
+    rx.req_to_token_write(table, rows, pos, vals)
+    torch.cuda.synchronize()
+    with pytest.raises(rx.RxError) as e:
+        rx.device_check()
+    assert "(flags 16)" in str(e.value)
+    want = torch.zeros_like(table)
+    want[0, 3], want[2, 15] = 11, 15
+    assert torch.equal(table, want)
+    assert rx.device_check() == 0      # flags were cleared
+
+
 def test_empty_calls_launch_nothing():
     dev = torch.device("cuda:0")
     kp = torch.zeros((1, 1, 8, 128), dtype=torch.bfloat16, device=dev)
