@@ -1,18 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the radix-cache attention hot path on one GB300 (or N replicas).
 
-One step = the whole agent-loop workload through librx: 40 calls sharing a
-3,000-token preamble with U[150, 250]-token suffixes, extend batches chosen by
-the in-batch prefix rule, 64 decode steps over all 40 calls, finish.  Every
-step starts from an empty cache, so it repeats the same cache decisions: match,
-lock, allocate, req_to_token upload, kv_store, extend attention, decode plan,
-shared-prefix + private decode attention with log-sum-exp merge, insert,
-unlock.  Q/K/V are seeded synthetic bf16 N(0, 1) values resident in HBM before
-the timed region (``value``); ``e2e`` repeats the step with the inputs in pinned
-host memory, copied to the device inside the timed region, and the attention
-outputs read back.
+One step = the whole multi-turn chat workload through librx: 256 sessions x 8
+turns over a shared 2,000-token system prompt, each turn 200 new user tokens
+and 32 decoded tokens, 16 full-attention layers, 16 query / 4 KV heads,
+head_dim 256 (64 KiB of KV per token).  Every step starts from an empty cache,
+so it repeats the same cache decisions: match, lock, allocate, req_to_token
+upload, kv_store, extend attention, decode plan, shared-prefix + private
+decode attention with log-sum-exp merge, insert, unlock.  Q/K/V are seeded
+synthetic bf16 N(0, 1) values resident in HBM before the timed region
+(``value``); ``e2e`` repeats the step with the inputs in page-locked host
+memory, copied to the device inside the timed region, and every attention
+output read back to the host through a bounded ring of buffers.  The same line
+carries, per other workload (agent loop, long shared prefix, fork tree), its
+step time and the extend, decode and kv_store rates (``configs``).
 
-Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead;
+``--only kv_store`` times the kv_store kernel alone at the shape of the
+workload's largest extend batch (a small case for profiler captures).
 """
 
 import os
@@ -36,32 +41,49 @@ sys.path.insert(0, ROOT)
 METRIC = "extend query-tok/s and decode attn GB/s (% of GB300 HBM peak) on radix KV pool"
 L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 126 << 20            # GB300 L2 capacity
+DEFAULT_WORKLOAD = "multi_turn_chat"
+# other workloads measured in the same run, each with its own object in the line
+SIDE_WORKLOADS = ("agent_loop", "long_shared", "fork_tree")
+SIDE_STEPS = 10                 # timed steps of each side workload (3 warm-up)
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="agent_loop")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave out the other workloads' objects")
+    ap.add_argument("--only", choices=["kv_store"], default=None)
+    return ap.parse_args(argv)
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
 # captures summarised in profiles/ (cold L2, the current kernels):
 # decode_fused_kernel on one agent_loop and one long_shared decode step; the
 # extend kernel averaged over the launches of one step (long_shared: 2,
-# fork_tree: 130), as `achieved` averages over them.  None (absent) where no
-# capture of that launch exists.
+# fork_tree: 130), as `achieved` averages over them; multi_turn_chat's decode
+# launch scaled from a capture of one multi_turn_chat_small decode launch by
+# the ratio of algorithmic bytes (the full workload's pool is beyond the
+# capture size rule).  None (absent) where no capture of that launch exists.
 TRAFFIC = {
     ("agent_loop", "rx_decode_attention"): 44.534e6 + 0.006e6,
     ("long_shared", "rx_decode_attention"): 406.35e6 + 16.01e6,
     ("long_shared", "rx_extend_attention"): (2230.64e6 + 3158.90e6) / 2,
     ("fork_tree", "rx_extend_attention"): (5711.18e6 + 887.04e6) / 130,
 }
+
+
+def config_of(wl, world):
+    """The workload's description as both arms print it (identical keys)."""
+    return {"workload": wl.name, **{k: v for k, v in wl.describe().items() if k != "workload"},
+            "l2": "inputs larger than L2, and L2 flushed between timed steps (256 MiB write, "
+                  "outside the step events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single"}
 
 
 def max_over_ranks(x, world, device):
@@ -159,88 +181,109 @@ class Clocks:
                 "samples_in_timed_region": len(inside)}
 
 
+
+
 # --------------------------------------------------------------- CPU oracle
-def oracle_rate(wl, rows_of, budget_s=12.0, seed=0):
-    """Oracle throughput (query tokens/s) on a bounded sample.
+def _pairs(trace, wl):
+    """Visible (query, key) pairs of one layer: extend query i of a prompt
+    sees keys 0..i; decode step t of a request sees its prompt and t + 1
+    decode tokens."""
+    ext = 0
+    for b in trace.batches:
+        for rid, m, row in b:
+            n = len(row)
+            ext += (n * (n + 1) - m * (m + 1)) // 2
+    dec = 0
+    T = wl.decode_steps
+    for w in wl.waves:
+        for r in w:
+            p = len(wl.prompt_tokens(r))
+            dec += T * p + T * (T + 1) // 2
+    return ext, dec
 
-    Bookkeeping of the whole workload is run in full; attention is computed
-    in fp64 for a random sample of the workload's queries (extend tokens and
-    decode tokens) until ``budget_s`` is spent, and the per-query cost is
-    scaled to the whole workload."""
-    from oracle import attention as oatt
+
+def oracle_bookkeeping(wl):
+    """The oracle's request flow over the whole workload, timed."""
     from oracle.harness import run_bookkeeping
-
     t0 = time.perf_counter()
     trace, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
-    t_book = time.perf_counter() - t0
+    return trace, time.perf_counter() - t0
+
+
+def oracle_rate(wl, budget_s=12.0, seed=0, booked=None, n_requests=8):
+    """Oracle throughput (query tokens/s) from a bounded sample.
+
+    The oracle's bookkeeping runs over the whole workload (or ``booked`` =
+    (trace, seconds) of such a run is reused).  Attention is computed in fp64
+    at one layer with all heads for the queries of ``n_requests`` seeded
+    requests (extend and decode queries, in random order) until ``budget_s``
+    is spent; its time per visible (query, key) pair is scaled to every pair
+    of every layer of the workload.  The oracle's time does not depend on the
+    values, so they are seeded normal draws made here."""
+    from oracle import attention as oatt
+
+    trace, t_book = booked if booked is not None else oracle_bookkeeping(wl)
     n_ext = trace.prefilled
     n_dec = sum(len(w) for w in wl.waves) * wl.decode_steps
+    ext_pairs, dec_pairs = _pairs(trace, wl)
+    rng = np.random.default_rng(seed)
+    rids = sorted(wl.requests)
+    pick = set(int(x) for x in rng.choice(rids, size=min(n_requests, len(rids)), replace=False))
     queries = []
     for b in trace.batches:
         for rid, m, row in b:
-            for i in range(m, len(row)):
-                queries.append(("e", rid, m, i))
-    rng = np.random.default_rng(seed)
-    order = rng.permutation(len(queries))
-    dec_q = [(r.rid, t) for w in wl.waves for r in w for t in range(wl.decode_steps)]
-    dorder = rng.permutation(len(dec_q))
-    done = 0
+            if rid in pick:
+                queries += [i + 1 for i in range(m, len(row))]
+    for rid in pick:
+        p = len(wl.prompt_tokens(wl.requests[rid]))
+        queries += [p + t + 1 for t in range(wl.decode_steps)]
+    queries = [queries[i] for i in rng.permutation(len(queries))]
+    ctx = max(queries)
+    k = rng.standard_normal((ctx, wl.num_kv_heads, wl.head_dim))
+    v = rng.standard_normal((ctx, wl.num_kv_heads, wl.head_dim))
+    q = rng.standard_normal((1, wl.num_q_heads, wl.head_dim))
+    done = pairs = 0
     t_att = 0.0
-    k = 0
-    while t_att < budget_s and k < len(order):
-        # alternate extend and decode queries in proportion to the workload
-        if dec_q and rng.random() < n_dec / (n_ext + n_dec):
-            rid, t = dec_q[dorder[k % len(dorder)]]
-            r = wl.requests[rid]
-            ctx = np.concatenate([wl.prompt_store_index(r), wl.output_store_index(r)[:t + 1]])
-            q, kk, vv = rows_of("q", [wl.output_store_index(r)[t]]), rows_of("k", ctx), rows_of("v", ctx)
-            s0 = time.perf_counter()
-            oatt.decode_attention(q[0], kk, vv)
-        else:
-            _, rid, m, i = queries[order[k]]
-            r = wl.requests[rid]
-            pidx = wl.prompt_store_index(r)
-            q, kk, vv = rows_of("q", [pidx[i]]), rows_of("k", pidx[:i + 1]), rows_of("v", pidx[:i + 1])
-            s0 = time.perf_counter()
-            oatt.softmax_attention(q, kk, vv, [i + 1])
+    for n in queries:
+        if t_att >= budget_s:
+            break
+        s0 = time.perf_counter()
+        oatt.softmax_attention(q, k[:n], v[:n], [n])
         t_att += time.perf_counter() - s0
         done += 1
-        k += 1
+        pairs += n
     total_q = n_ext + n_dec
-    est = t_book + t_att * total_q / max(1, done)
+    est = t_book + t_att / max(1, pairs) * (ext_pairs + dec_pairs) * wl.num_layers
     return {
         "value": total_q / est,
         "unit": "query-tok/s",
         "cores": 1,
         "kind": "oracle",
-        "sample": (f"bookkeeping of the whole workload ({t_book:.2f} s) + fp64 attention of "
-                   f"{done} randomly drawn queries of {total_q} ({t_att:.1f} s), scaled to all "
-                   "queries; numpy single-threaded"),
+        "sample": (f"bookkeeping of the whole workload ({t_book:.2f} s) + fp64 attention, layer "
+                   f"0, all {wl.num_q_heads} heads, of {done} queries drawn from {len(pick)} "
+                   f"seeded requests ({t_att:.1f} s, {pairs} of the layer's "
+                   f"{ext_pairs + dec_pairs} visible query-key pairs), scaled by pairs to all "
+                   f"{wl.num_layers} layers and {total_q} queries; numpy single-threaded"),
         "seconds": t_book + t_att,
     }
 
 
 def run_reference(args, rank, world):
+    """The oracle timed as it stands on one host core: its bookkeeping of the
+    whole workload once (before the warm-up steps), then per step a bounded
+    attention sample (oracle_rate); value = mean over the timed steps."""
     if rank != 0:
         return
     from radix_tree_prefix_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]()
-    import torch
-
-    def make_rows():
-        g = workloads.make_values(wl, "cpu")
-
-        def rows_of(kind, idx):
-            t = torch.from_numpy(np.asarray(idx, dtype=np.int64))
-            return g[kind][0].index_select(0, t).double().numpy()
-        return rows_of
-
-    rows_of = make_rows()
-    oracle_rate(wl, rows_of, budget_s=1.0)      # warm-up (imports, caches)
+    booked = oracle_bookkeeping(wl)
+    per_step = max(0.5, 60.0 / max(1, args.steps))
+    for s in range(args.warmup):
+        oracle_rate(wl, budget_s=min(1.0, per_step), seed=1000 + s, booked=booked)
     vals = []
     t0 = time.perf_counter()
     for s in range(args.steps):
-        r = oracle_rate(wl, rows_of, budget_s=max(1.0, 60.0 / max(1, args.steps)), seed=s)
+        r = oracle_rate(wl, budget_s=per_step, seed=s, booked=booked)
         vals.append(r["value"])
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
@@ -249,10 +292,9 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * wall / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items()
-                                            if k != "workload"}},
+        "config": config_of(wl, world),
         "cpu_baseline": {"value": value, "unit": "query-tok/s", "cores": 1, "kind": "oracle",
-                         "sample": r["sample"]},
+                         "sample": r["sample"] + f"; mean of {args.steps} steps"},
         "e2e": {"value": value, "unit": "query-tok/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -260,8 +302,202 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- GPU arm
-def main():
-    args = parse()
+def _kind_stats(events, steps):
+    kinds = {}
+    for kind, a, b, work in events:
+        d = kinds.setdefault(kind, {"ms": 0.0, "launches": 0, "work": 0.0})
+        d["ms"] += a.elapsed_time(b)
+        d["launches"] += 1
+        d["work"] += work
+    for d in kinds.values():
+        d["steps"] = steps
+    return kinds
+
+
+def _rates(kinds, n_ext, hbm_peak, bf16_peak, steps, n_dec_launch_bytes=None):
+    zero = {"ms": 0.0, "launches": 0, "work": 0.0}
+    ext, dec, st = (kinds.get(k, zero) for k in ("extend", "decode", "kv_store"))
+    ext_tflops = ext["work"] / (ext["ms"] / 1e3) / 1e12 if ext["ms"] else 0.0
+    dec_gbs = dec["work"] / (dec["ms"] / 1e3) / 1e9 if dec["ms"] else 0.0
+    st_gbs = st["work"] / (st["ms"] / 1e3) / 1e9 if st["ms"] else 0.0
+    extend = {"qtok_s": n_ext * steps / (ext["ms"] / 1e3) if ext["ms"] else None,
+              "tflops": ext_tflops, "frac_of_bf16_peak": ext_tflops / bf16_peak,
+              "ms_per_step": ext["ms"] / steps, "launches_per_step": ext["launches"] / steps,
+              "flop_per_step": ext["work"] / steps}
+    decode = {"gbs": dec_gbs, "frac_of_hbm_peak": dec_gbs / hbm_peak,
+              "ms_per_step": dec["ms"] / steps, "launches_per_step": dec["launches"] / steps,
+              "bytes_per_step": dec["work"] / steps}
+    if n_dec_launch_bytes is not None and dec["launches"] and n_dec_launch_bytes < L2_BYTES:
+        decode["note"] = ("decode working set fits in L2; L2 is flushed between steps only, so "
+                          "later decode steps of a step read KV that is partly L2-resident "
+                          "(effective GB/s)")
+    kv_store = {"gbs": st_gbs, "frac_of_hbm_peak": st_gbs / hbm_peak,
+                "ms_per_step": st["ms"] / steps, "launches_per_step": st["launches"] / steps,
+                "bytes_per_step": st["work"] / steps}
+    return extend, decode, kv_store
+
+
+def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
+    """Times `steps` runs of the whole workload (after `warmup` runs), inputs
+    resident in HBM, L2 flushed between runs; optionally the end-to-end leg."""
+    import torch
+    import torch.distributed as dist
+
+    from radix_tree_prefix_gb300 import rx, workloads
+    from radix_tree_prefix_gb300.engine import (Engine, GatherInputs, OutputRing,
+                                                PreparedInputs)
+
+    layers = list(range(wl.num_layers))
+    values = workloads.make_values(wl, dev, layers)
+    source = GatherInputs(wl, values, layers)
+    prepared = PreparedInputs(source)
+    eng = Engine(wl, device=dev, inputs=prepared, layers=layers)
+    trace = eng.run()                       # records the inputs of every batch/step
+    prepared.freeze()
+    torch.cuda.synchronize()
+    rx.device_check()
+    source.values = None                    # the stores are no longer needed
+    del values
+    n_ext = trace.prefilled
+    n_dec = sum(len(w) for w in wl.waves) * wl.decode_steps
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        eng.run()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    eng.timing = True
+    eng.kernel_events = []
+    launches0 = eng.gpu_launches
+    step_ev = []
+    stream = torch.cuda.current_stream()
+    if clocks is not None:
+        clocks.begin()
+    wall0 = time.perf_counter()
+    for _ in range(steps):
+        flush.zero_()                                   # L2 flushed between steps
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        t = eng.run()
+        e1.record(stream)
+        step_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if clocks is not None:
+        clocks.end()
+    if world > 1:
+        dist.barrier()
+    assert t.as_tuple() == trace.as_tuple(), "timed steps made different cache decisions"
+    rx.device_check()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    out = {"wl": wl, "trace": trace, "n_ext": n_ext, "n_dec": n_dec, "ms": ms,
+           "kinds": _kind_stats(eng.kernel_events, steps),
+           "launches": eng.gpu_launches - launches0, "wall": wall, "e2e": None}
+    if e2e:
+        # host copies of every recorded input, then the device copies go
+        host = PreparedInputs(source, host=True)
+        host.adopt(prepared)
+        host.freeze()
+        prepared.ext.clear()
+        prepared.dec.clear()
+        del eng
+        torch.cuda.empty_cache()
+        hq, d = wl.num_q_heads, wl.head_dim
+        most = max([sum(len(row) - m for _, m, row in b) for b in trace.batches] +
+                   [len(w) * wl.decode_steps for w in wl.waves])
+        ring = OutputRing(dev, most * hq * (d + 1), slots=4)
+        eng2 = Engine(wl, device=dev, inputs=host, layers=layers, out_ring=ring)
+        eng2.run()                                      # untimed first run
+        torch.cuda.synchronize()
+        host.h2d_bytes = 0
+        ring.d2h_bytes = 0
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            flush.zero_()
+            eng2.run()
+            torch.cuda.synchronize()
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
+        rx.device_check()
+        out["e2e"] = {"value": job_rate(n_ext + n_dec, e2e_s, world), "unit": "query-tok/s",
+                      "h2d_bytes_per_step": host.h2d_bytes // steps,
+                      "d2h_bytes_per_step": ring.d2h_bytes // steps,
+                      "ms_per_step": e2e_s * 1e3,
+                      "copies": "inputs from page-locked host memory one batch ahead on a side "
+                                "stream; every output (fp32 o and lse) read back through a "
+                                "ring of 4 device/host buffer pairs on another stream"}
+        del eng2
+        ring.close()
+        host.close()
+    return out
+
+
+def _summary(res, steps, hbm_peak, bf16_peak):
+    wl = res["wl"]
+    launch_bytes = None
+    kinds = res["kinds"]
+    if "decode" in kinds and kinds["decode"]["launches"]:
+        per_launch = kinds["decode"]["work"] / kinds["decode"]["launches"]
+        launch_bytes = per_launch / max(1, wl.decode_steps)
+    extend, decode, kv_store = _rates(kinds, res["n_ext"], hbm_peak, bf16_peak, steps,
+                                      launch_bytes)
+    return extend, decode, kv_store
+
+
+def only_kv_store(args, dev):
+    """kv_store alone at the shape of the workload's largest extend batch:
+    one layer's pool of the workload's slot count, the batch's new slots (from
+    the host bookkeeping), seeded K/V rows; W untimed and K timed launches,
+    L2 flushed before each."""
+    import torch
+
+    from radix_tree_prefix_gb300 import rx, workloads
+    from radix_tree_prefix_gb300.engine import Engine
+
+    wl = workloads.WORKLOADS[args.workload]()
+    trace = Engine(wl).run()
+    batch = max(trace.batches, key=lambda b: sum(len(r) - m for _, m, r in b))
+    slots = np.concatenate([np.asarray(r[m:], dtype=np.int32) for _, m, r in batch])
+    T, hkv, d = len(slots), wl.num_kv_heads, wl.head_dim
+    g = torch.Generator(device=dev).manual_seed(1)
+    kp = torch.zeros((1, hkv, wl.num_slots, d), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    k = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    d_slots = torch.from_numpy(slots).to(dev)
+    pool = rx.pool_desc(kp, vp)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rx.kv_store(pool, 0, d_slots, k, v, stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    rx.device_check()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in times[args.warmup:])
+    nbytes = 4 * T * hkv * d * 2 + 4 * T
+    hbm_peak, _, src = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"kernel": "kv_store_kernel", "workload": wl.name, "tokens": T,
+                      "bytes_per_launch": nbytes, "ms_per_launch": ms, "gbs": gbs,
+                      "frac_of_hbm_peak": gbs / hbm_peak, "peak_source": src,
+                      "launches_timed": args.steps}), flush=True)
+
+
+def main(argv=None):
+    args = parse(argv)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -277,181 +513,67 @@ def main():
     dev = torch.device("cuda", local)
     import __graft_entry__
     __graft_entry__.build()
-    from radix_tree_prefix_gb300 import rx, workloads
-    from radix_tree_prefix_gb300.engine import Engine, GatherInputs, PreparedInputs
+    from radix_tree_prefix_gb300 import workloads
 
-    wl = workloads.WORKLOADS[args.workload]()
-    layers = list(range(wl.num_layers))
-    values = workloads.make_values(wl, dev, layers)
-    prepared = PreparedInputs(GatherInputs(wl, values, layers))
-    eng = Engine(wl, device=dev, inputs=prepared, layers=layers)
-    trace = eng.run()                       # records the inputs of every batch/step
-    prepared.freeze()
-    torch.cuda.synchronize()
-    rx.device_check()
-    n_ext = trace.prefilled
-    n_dec = sum(len(w) for w in wl.waves) * wl.decode_steps
-    q_per_step = n_ext + n_dec
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    clocks = Clocks(local)          # started before warm-up: its start-up is not timed
-    for _ in range(args.warmup):
-        eng.run()
-    torch.cuda.synchronize()
-    time.sleep(0.3)
+    if args.only == "kv_store":
+        if rank == 0:
+            only_kv_store(args, dev)
+        return
 
-    # ---------------- timed: inputs resident in HBM
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    eng.timing = True
-    eng.kernel_events = []
-    launches0 = eng.gpu_launches
-    step_ev = []
-    stream = torch.cuda.current_stream()
-    clocks.begin()
-    wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        flush.zero_()                                   # L2 flushed between steps
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        t = eng.run()
-        e1.record(stream)
-        step_ev.append((e0, e1))
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    clocks.end()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    launches = eng.gpu_launches - launches0
-    assert t.as_tuple() == trace.as_tuple(), "timed steps made different cache decisions"
-    rx.device_check()
-    step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
-    value = job_rate(q_per_step, ms / 1000.0, world)
-
-    kinds = {}
-    for kind, a, b, work in eng.kernel_events:
-        d = kinds.setdefault(kind, {"ms": 0.0, "launches": 0, "work": 0.0})
-        d["ms"] += a.elapsed_time(b)
-        d["launches"] += 1
-        d["work"] += work
     hbm_peak, bf16_peak, peak_src = peaks()
-    ext = kinds.get("extend", {"ms": 0.0, "launches": 0, "work": 0.0})
-    dec = kinds.get("decode", {"ms": 0.0, "launches": 0, "work": 0.0})
-    ext_tflops = ext["work"] / (ext["ms"] / 1e3) / 1e12 if ext["ms"] else 0.0
-    dec_gbs = dec["work"] / (dec["ms"] / 1e3) / 1e9 if dec["ms"] else 0.0
-    extend_info = {
-        "qtok_s": n_ext * args.steps / (ext["ms"] / 1e3) if ext["ms"] else None,
-        "tflops": ext_tflops, "frac_of_bf16_peak": ext_tflops / bf16_peak,
-        "ms_per_step": ext["ms"] / args.steps, "launches_per_step": ext["launches"] / args.steps,
-        "flop_per_step": ext["work"] / args.steps}
-    n_dec_launches = args.steps * len(wl.waves) * wl.decode_steps * len(layers)
-    decode_info = {
-        "gbs": dec_gbs, "frac_of_hbm_peak": dec_gbs / hbm_peak,
-        "ms_per_step": dec["ms"] / args.steps, "launches_per_step": dec["launches"] / args.steps,
-        "bytes_per_step": dec["work"] / args.steps,
-        "note": ("decode working set fits in L2; L2 is flushed between steps only, so "
-                 "later decode steps of a step read KV that is partly L2-resident (effective GB/s)")
-        if dec["launches"] and dec["work"] / max(1, n_dec_launches) < L2_BYTES else None}
-    if ext["ms"] >= dec["ms"]:
-        roof = {"kernel": "rx_extend_attention", "bound": "tensor", "achieved": ext_tflops,
-                "peak": bf16_peak, "unit": "TFLOP/s", "frac": ext_tflops / bf16_peak,
-                "traffic": TRAFFIC.get((args.workload, "rx_extend_attention")),
+    wl = workloads.WORKLOADS[args.workload]()
+    clocks = Clocks(local)          # started before warm-up: its start-up is not timed
+    res = measure(wl, dev, args.steps, args.warmup, world, e2e=not args.no_e2e, clocks=clocks)
+    clk = clocks.stop()
+    torch.cuda.empty_cache()
+    n_ext, n_dec = res["n_ext"], res["n_dec"]
+    q_per_step = n_ext + n_dec
+    value = job_rate(q_per_step, res["ms"] / 1000.0, world)
+    extend, decode, kv_store = _summary(res, args.steps, hbm_peak, bf16_peak)
+    if extend["ms_per_step"] >= decode["ms_per_step"]:
+        roof = {"kernel": "rx_extend_attention", "bound": "tensor", "achieved": extend["tflops"],
+                "peak": bf16_peak, "unit": "TFLOP/s", "frac": extend["frac_of_bf16_peak"],
+                "traffic": TRAFFIC.get((wl.name, "rx_extend_attention")),
                 "peak_source": f"{peak_src} bf16_tflops (burst)"}
     else:
-        roof = {"kernel": "rx_decode_attention", "bound": "hbm", "achieved": dec_gbs,
-                "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
-                "traffic": TRAFFIC.get((args.workload, "rx_decode_attention")),
+        roof = {"kernel": "rx_decode_attention", "bound": "hbm", "achieved": decode["gbs"],
+                "peak": hbm_peak, "unit": "GB/s", "frac": decode["frac_of_hbm_peak"],
+                "traffic": TRAFFIC.get((wl.name, "rx_decode_attention")),
                 "peak_source": f"{peak_src} hbm_gbs"}
 
-    # ---------------- e2e: host inputs copied in, outputs read back
-    e2e = None
-    if not args.no_e2e:
-        host_inputs = PreparedInputs(prepared.source, host=True)
-        host_inputs.ext = dict(prepared.ext)
-        host_inputs.dec = dict(prepared.dec)
-        host_inputs.order = list(prepared.order)
-        host_inputs.freeze()
-        d2h = {"bytes": 0}
-        # pinned host buffers for the outputs, allocated in the untimed first
-        # run and reused in call order (each step ends with a synchronize)
-        sinks = []
-        sink_i = [0]
-
-        # outputs go back on a side stream once they are written, while the
-        # main stream runs on
-        out_stream = torch.cuda.Stream(dev)
-        main_stream = torch.cuda.current_stream(dev)
-
-        def grab(outs):
-            ready = torch.cuda.Event()
-            ready.record(main_stream)
-            out_stream.wait_event(ready)
-            for o, lse in outs.values():
-                for x in (o, lse):
-                    x.record_stream(out_stream)
-                    i = sink_i[0]
-                    if i == len(sinks) or sinks[i].shape != x.shape:
-                        h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-                        if i == len(sinks):
-                            sinks.append(h)
-                        else:
-                            sinks[i] = h
-                    with torch.cuda.stream(out_stream):
-                        sinks[i].copy_(x, non_blocking=True)
-                    sink_i[0] = i + 1
-                    d2h["bytes"] += x.numel() * x.element_size()
-
-        # output tensors reused run to run (each run ends with a synchronize,
-        # so the previous run's reads of them are done)
-        eng2 = Engine(wl, device=dev, inputs=host_inputs, layers=layers,
-                      on_extend=lambda b, r, p, q, outs: grab(outs),
-                      on_decode_wave=lambda s, r, c, outs, i: grab(outs), reuse_outputs=True)
-        eng2.run()
-        torch.cuda.synchronize()
-        sink_i[0] = 0
-        host_inputs.h2d_bytes = 0
-        d2h["bytes"] = 0
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            flush.zero_()
-            eng2.run()
-            torch.cuda.synchronize()
-            sink_i[0] = 0
-        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
-        e2e = {"value": job_rate(q_per_step, e2e_s, world), "unit": "query-tok/s",
-               "h2d_bytes_per_step": host_inputs.h2d_bytes // args.steps,
-               "d2h_bytes_per_step": d2h["bytes"] // args.steps,
-               "ms_per_step": e2e_s * 1e3}
+    configs = {}
+    if not args.no_configs and world == 1:
+        for name in SIDE_WORKLOADS:
+            if name == wl.name:
+                continue
+            side = measure(workloads.WORKLOADS[name](), dev, SIDE_STEPS, 3, 1)
+            e, dcd, st = _summary(side, SIDE_STEPS, hbm_peak, bf16_peak)
+            configs[name] = {"ms_per_step": side["ms"],
+                             "query_tokens_per_step": side["n_ext"] + side["n_dec"],
+                             "value": (side["n_ext"] + side["n_dec"]) / (side["ms"] / 1e3),
+                             "steps": SIDE_STEPS, "warmup": 3,
+                             "extend": e, "decode": dcd, "kv_store": st}
+            del side
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu and world == 1:
-        def rows_of(kind, idx):
-            t = torch.from_numpy(np.asarray(idx, dtype=np.int64)).to(dev)
-            return values[kind][0].index_select(0, t).double().cpu().numpy()
-        cpu = oracle_rate(wl, rows_of)
+        cpu = oracle_rate(wl)
         cpu.pop("seconds", None)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "query-tok/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items()
-                                                if k != "workload"},
-                       "query_tokens_per_step": q_per_step, "extend_query_tokens": n_ext,
+            "config": config_of(wl, world),
+            "detail": {"query_tokens_per_step": q_per_step, "extend_query_tokens": n_ext,
                        "decode_query_tokens": n_dec,
-                       "l2": "flushed between timed steps (256 MiB write, outside the step events)",
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "wall_s_timed_region_incl_flush": wall},
-            "extend": extend_info, "decode": decode_info, "roofline": roof,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+                       "wall_s_timed_region_incl_flush": res["wall"]},
+            "extend": extend, "decode": decode, "kv_store": kv_store, "roofline": roof,
+            "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["launches"],
+            "clocks": clk, "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

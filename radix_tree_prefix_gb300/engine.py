@@ -104,63 +104,167 @@ class GatherInputs:
                 for layer in self.layers}
 
 
+class HostBuffer:
+    """Page-locked host memory of an exact size: a numpy array registered
+    with CUDA (cudaHostRegister), so copies from and to it run
+    asynchronously, without the power-of-two rounding of the framework's
+    pinned-memory cache.  ``tensor`` views it; ``close`` unregisters it."""
+
+    def __init__(self, nbytes):
+        import torch
+        self.torch = torch
+        self.array = np.empty(max(1, int(nbytes)), dtype=np.uint8)
+        self.registered = False
+        rt = getattr(torch._C, "_cudart", None)
+        if rt is not None and hasattr(rt, "cudaHostRegister"):
+            err = rt.cudaHostRegister(self.array.ctypes.data, self.array.nbytes, 0)
+            self.registered = int(getattr(err, "value", err)) == 0
+        if self.registered:
+            self.tensor = torch.from_numpy(self.array)
+        else:   # registration unavailable: the framework's pinned allocator
+            self.tensor = torch.empty(self.array.nbytes, dtype=torch.uint8, pin_memory=True)
+            self.array = None
+
+    def view(self, offset, shape, dtype):
+        n = int(np.prod(shape)) * _itemsize(dtype)
+        return self.tensor[offset:offset + n].view(dtype).view(shape)
+
+    def close(self):
+        if self.registered:
+            self.torch._C._cudart.cudaHostUnregister(self.array.ctypes.data)
+            self.registered = False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _itemsize(dtype):
+    import torch
+    return torch.empty(0, dtype=dtype).element_size()
+
+
+def _layout(per_layer):
+    """Offsets (256-byte aligned) of a position's tensors packed in one flat
+    buffer: [(layer, [(offset, shape, dtype), ...]), ...] and the total."""
+    off = 0
+    out = []
+    for layer, qkv in per_layer.items():
+        ents = []
+        for t in qkv:
+            ents.append((off, tuple(t.shape), t.dtype))
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        out.append((layer, ents))
+    return out, off
+
+
 class PreparedInputs:
     """Inputs gathered once (by a recording run) and replayed in order.
 
     ``source`` is any provider; the first pass records what it returns per
     extend batch and per decode wave, later passes replay it.  ``host=True``
-    keeps the recorded tensors in pinned host memory and copies them to the
-    device when they are used (the end-to-end path): when the engine asks for
-    one batch's inputs, the next batch's (in the recorded order) are already
-    being copied on a side stream, so the copies overlap the kernels.  Each
-    recorded position has device buffers of its own, allocated on the first
-    pass and refilled on every later one once the work that read them on the
-    consumer's stream (everything it had enqueued when it asked for the next
-    position) has completed."""
+    keeps the recorded tensors in page-locked host memory and copies them to
+    the device when they are used (the end-to-end path): when the engine asks
+    for one batch's inputs, the next batch's (in the recorded order) are
+    already being copied on a side stream, so the copies overlap the kernels.
+    The device side is a ring of ``ring`` flat buffers, each as large as the
+    largest position, filled in turn: a buffer is refilled once the work that
+    read its previous occupant on the consumer's stream (everything the
+    consumer had enqueued when it asked for the position after that one) has
+    completed."""
 
-    def __init__(self, source, host=False):
+    def __init__(self, source, host=False, ring=3):
         self.source = source
         self.host = host
+        self.ring = max(2, int(ring))
         self.ext = {}
         self.dec = {}
         self.order = []        # (store, key) in the order a run asks for them
         self.recording = True
         self.h2d_bytes = 0
         self._pos = 0
-        self._ahead = None     # (position, event: its copy has landed)
+        self._ahead = None     # (position, event: its copy landed, views, buffer)
         self._copy_stream = None
-        self._dev = {}         # position -> {layer: (q, k, v) device buffers}
-        self._last_use = {}    # position -> event after its last reader
-        self._handed = None    # position handed out last
+        self._dev = {}         # ring slot -> flat device buffer
+        self._last_use = {}    # ring slot -> event after its last reader
+        self._handed = None    # ring buffer of the position handed out last
+        self._seq = 0          # ring buffers filled so far
+        self._host_bufs = []
+        self._lay = {}         # position -> (layout, bytes)
+
+    def adopt(self, other):
+        """Replay what `other` recorded (same order and tensors)."""
+        self.ext, self.dec, self.order = dict(other.ext), dict(other.dec), list(other.order)
 
     def freeze(self):
         self.recording = False
-        if self.host:
-            for store in (self.ext, self.dec):
-                for key, per_layer in store.items():
-                    store[key] = {l: tuple(t.cpu().pin_memory() for t in qkv)
-                                  for l, qkv in per_layer.items()}
+        if not self.host:
+            return
+        import torch
+        # one exact-size page-locked buffer per position, filled from the
+        # recorded tensors; the recorded device tensors are then dropped
+        for pos, (name, key) in enumerate(self.order):
+            if pos in self._lay:            # frozen before
+                continue
+            store = self.ext if name == "ext" else self.dec
+            per_layer = store[key]
+            lay, nbytes = _layout(per_layer)
+            hb = HostBuffer(nbytes)
+            self._host_bufs.append(hb)
+            host = {}
+            for layer, ents in lay:
+                views = []
+                for (off, shape, dtype), t in zip(ents, per_layer[layer]):
+                    h = hb.view(off, shape, dtype)
+                    h.copy_(t)
+                    views.append(h)
+                host[layer] = tuple(views)
+            store[key] = host
+            self._lay[pos] = (lay, nbytes)
+        torch.cuda.synchronize()
+        self._slot_bytes = max((b for _, b in self._lay.values()), default=0)
 
-    def _fill(self, pos, stream):
-        """Copies position pos's recorded inputs into its device buffers on
-        `stream`, after their previous readers."""
+    def close(self):
+        for hb in self._host_bufs:
+            hb.close()
+        self._host_bufs = []
+
+    def _fill(self, pos, slot, stream):
+        """Copies position pos's recorded inputs into ring buffer `slot` on
+        `stream`, after that buffer's previous readers."""
         import torch
         name, key = self.order[pos]
         src = (self.ext if name == "ext" else self.dec)[key]
-        dev = self._dev.get(pos)
-        if dev is None:
-            dev = {l: tuple(torch.empty_like(t, device=self.source.device) for t in qkv)
-                   for l, qkv in src.items()}
-            self._dev[pos] = dev
-        ev = self._last_use.get(pos)
+        buf = self._dev.get(slot)
+        if buf is None:
+            buf = torch.empty(max(1, self._slot_bytes), dtype=torch.uint8,
+                              device=self.source.device)
+            self._dev[slot] = buf
+        ev = self._last_use.get(slot)
         if ev is not None:
             stream.wait_event(ev)
+        lay, _ = self._lay[pos]
+        out = {}
         with torch.cuda.stream(stream):
-            for l, qkv in src.items():
-                for d, h in zip(dev[l], qkv):
+            for (layer, ents) in lay:
+                views = []
+                for (off, shape, dtype), h in zip(ents, src[layer]):
+                    n = h.numel() * h.element_size()
+                    d = buf[off:off + n].view(dtype).view(shape)
                     d.copy_(h, non_blocking=True)
-                    self.h2d_bytes += h.numel() * h.element_size()
-        return dev
+                    self.h2d_bytes += n
+                    views.append(d)
+                out[layer] = tuple(views)
+        return out
+
+    def _next_slot(self):
+        # consecutive fills take consecutive ring buffers, so a buffer is
+        # refilled only after `ring - 1` other positions were handed out
+        slot = self._seq % self.ring
+        self._seq += 1
+        return slot
 
     def _get(self, name, store, key, make):
         if self.recording:
@@ -182,20 +286,22 @@ class PreparedInputs:
             pos = self.order.index((name, key))
             self._ahead = None
         if self._ahead is not None and self._ahead[0] == pos:
-            cur.wait_event(self._ahead[1])
-            out = self._dev[pos]
+            _, ready, out, slot = self._ahead
+            cur.wait_event(ready)
         else:
-            out = self._fill(pos, cur)
-        self._handed = pos
+            slot = self._next_slot()
+            out = self._fill(pos, slot, cur)
+        self._handed = slot
         self._pos = (pos + 1) % len(self.order)
         self._ahead = None
         if self._pos != pos:
             if self._copy_stream is None:
                 self._copy_stream = torch.cuda.Stream(self.source.device)
-            self._fill(self._pos, self._copy_stream)
+            nslot = self._next_slot()
+            views = self._fill(self._pos, nslot, self._copy_stream)
             ready = torch.cuda.Event()
             ready.record(self._copy_stream)
-            self._ahead = (self._pos, ready)
+            self._ahead = (self._pos, ready, views, nslot)
         return out
 
     def extend(self, batch_no, reqs, prefix):
@@ -205,6 +311,76 @@ class PreparedInputs:
     def decode_wave(self, step0, reqs, T):
         return self._get("dec", self.dec, step0,
                          lambda: self.source.decode_wave(step0, reqs, T))
+
+
+class OutputRing:
+    """Attention outputs of the end-to-end path, read back to the host
+    through a bounded ring: ``slots`` device buffers paired with as many
+    page-locked host buffers, each as large as the largest launch's output
+    and lse.  ``take(shape)`` hands out the next pair's device tensors; the
+    one handed out before it is then complete on the consumer's stream, so
+    its device-to-host copy is issued on a side stream, and the kernel that
+    writes a buffer next waits for that copy.  ``flush()`` issues the last
+    copy.  The host buffers keep only the latest outputs of each slot: a
+    reader that wants every output consumes them as they land."""
+
+    def __init__(self, device, max_elems, slots=4):
+        import torch
+        self.torch = torch
+        self.device = device
+        self.slots = int(slots)
+        self.cap = int(max_elems)
+        self.dev = [torch.empty(self.cap, dtype=torch.float32, device=device)
+                    for _ in range(self.slots)]
+        self.host = [HostBuffer(self.cap * 4) for _ in range(self.slots)]
+        self.copied = [None] * self.slots     # event: slot's last copy done
+        self.stream = torch.cuda.Stream(device)
+        self.pending = None                   # (slot, o elems, lse elems)
+        self.i = 0
+        self.d2h_bytes = 0
+
+    def _retire(self, cur):
+        if self.pending is None:
+            return
+        slot, no, nl = self.pending
+        self.pending = None
+        written = self.torch.cuda.Event()
+        written.record(cur)
+        self.stream.wait_event(written)
+        n = no + nl
+        with self.torch.cuda.stream(self.stream):
+            self.host[slot].view(0, (n,), self.torch.float32).copy_(self.dev[slot][:n],
+                                                                    non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record(self.stream)
+        self.copied[slot] = ev
+        self.d2h_bytes += 4 * n
+
+    def take(self, shape, cur):
+        no = int(np.prod(shape))
+        nl = int(np.prod(shape[:-1]))
+        if no + nl > self.cap:
+            raise ValueError(f"output of {no + nl} values exceeds the ring's {self.cap}")
+        self._retire(cur)
+        slot = self.i
+        self.i = (self.i + 1) % self.slots
+        if self.copied[slot] is not None:
+            cur.wait_event(self.copied[slot])
+        buf = self.dev[slot]
+        self.pending = (slot, no, nl)
+        return buf[:no].view(shape), buf[no:no + nl].view(shape[:-1])
+
+    def flush(self, cur):
+        self._retire(cur)
+
+    def close(self):
+        for h in self.host:
+            h.close()
+
+
+def total_new_bytes(T, wl):
+    """Bytes of the K (or V) rows of T tokens of one layer (bf16)."""
+    return T * wl.num_kv_heads * wl.head_dim * 2
 
 
 class _DevSpan:
@@ -295,11 +471,15 @@ class Engine:
     wave (per layer) are allocated on the first run and written again by
     every later run: they stay valid until the next run starts, and whoever
     reads them on another stream must be done (e.g. synchronized) by then.
+    With ``out_ring`` (an ``OutputRing``) every launch writes into the ring's
+    next device buffer and the ring copies each buffer back to the host once
+    the next launch takes a buffer (and at the end of a run); the tensors the
+    callbacks receive are then overwritten when the ring comes round.
     """
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
                  on_decode=None, stream=None, timing=False, on_decode_wave=None,
-                 reuse_outputs=False):
+                 reuse_outputs=False, out_ring=None):
         self.wl = wl
         self.device = device
         self.inputs = inputs
@@ -319,6 +499,7 @@ class Engine:
         self.gpu_launches = 0
         self.timing = timing
         self.reuse_outputs = reuse_outputs
+        self.out_ring = out_ring
         self._out_bufs = {}
         self.kernel_events = []   # (kind, start event, end event, algorithmic work)
         if device is not None:
@@ -357,6 +538,8 @@ class Engine:
         self.step_no = 0
         for wi, wave in enumerate(self.wl.waves):
             self._run_wave(wi, wave)
+        if self.out_ring is not None and self.device is not None:
+            self.out_ring.flush(self.stream)
         self.trace.eviction_log = self.cache.eviction_log()
         st = self.cache.stats()
         self.trace.stats = {
@@ -458,9 +641,12 @@ class Engine:
         total_q = int(qo[-1])
         flops = self._extend_flops(prefix, qo) if self.timing else 0.0
         outs = {}
+        store_bytes = float(4 * total_new_bytes(len(new_slots), wl) + 4 * len(new_slots))
         for layer in self.layers:
             q, k, v = inputs[layer]
+            ev = self._event_start()
             rx.kv_store(self.pool, layer, d_slots, k, v, self.stream)
+            self._event_end(ev, "kv_store", store_bytes)
             out, lse = self._outputs(("ext", self.batch_no, layer),
                                      (total_q, wl.num_q_heads, wl.head_dim))
             call = rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, d_tab,
@@ -545,6 +731,8 @@ class Engine:
         fresh ones, or with reuse_outputs the ones this key got on an earlier
         run (same shapes every run)."""
         torch = self.torch
+        if self.out_ring is not None:
+            return self.out_ring.take(shape, self.stream)
         if self.reuse_outputs:
             bufs = self._out_bufs.get(key)
             if bufs is not None and tuple(bufs[0].shape) == tuple(shape):

@@ -217,7 +217,7 @@ def test_host_input_replay_with_reused_outputs_is_bit_identical():
     torch.cuda.synchronize()
 
     host = PreparedInputs(prepared.source, host=True)
-    host.ext, host.dec, host.order = dict(prepared.ext), dict(prepared.dec), list(prepared.order)
+    host.adopt(prepared)
     host.freeze()
     got = {}
     e, w = collect(got)
@@ -232,3 +232,44 @@ def test_host_input_replay_with_reused_outputs_is_bit_identical():
             for a, b in zip(got[k], want[k]):
                 assert torch.equal(a, b), k
     assert rx.device_check() == 0
+
+
+def test_output_ring_reads_back_every_output():
+    """End-to-end output path: with as many ring buffers as launches, the
+    host side of buffer i holds launch i's output (o then lse, fp32) exactly
+    as a run into fresh device tensors computes it, on each of two runs."""
+    from radix_tree_prefix_gb300.engine import Engine, GatherInputs, OutputRing, PreparedInputs
+
+    dev = torch.device("cuda:0")
+    wl = workloads.agent_loop(calls=6, preamble=300, lo=20, hi=60, decode_steps=4)
+    vals = workloads.make_values(wl, dev, [0])
+    want = []
+
+    def on_ext(b, rids, prefix, qo, outs):
+        want.append(torch.cat([x.reshape(-1) for x in outs[0]]).clone())
+
+    def on_wave(s, rids, ctx, outs, info):
+        want.append(torch.cat([x.reshape(-1) for x in outs[0]]).clone())
+
+    prepared = PreparedInputs(GatherInputs(wl, vals, [0]))
+    Engine(wl, device=dev, inputs=prepared, layers=[0], on_extend=on_ext,
+           on_decode_wave=on_wave).run()
+    prepared.freeze()
+    torch.cuda.synchronize()
+    host = PreparedInputs(prepared.source, host=True, ring=2)
+    host.adopt(prepared)
+    host.freeze()
+    n = max(w.numel() for w in want)
+    ring = OutputRing(dev, n, slots=len(want))
+    eng = Engine(wl, device=dev, inputs=host, layers=[0], out_ring=ring)
+    for _ in range(2):
+        ring.d2h_bytes = 0
+        eng.run()
+        torch.cuda.synchronize()
+        for i, w in enumerate(want):
+            got = ring.host[i].view(0, (w.numel(),), torch.float32)
+            assert torch.equal(got, w.cpu()), i
+        assert ring.d2h_bytes == 4 * sum(w.numel() for w in want)
+    assert rx.device_check() == 0
+    ring.close()
+    host.close()
