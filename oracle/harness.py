@@ -32,6 +32,24 @@ Readings of the pages where they leave a step open:
 * finish is ``insert(prompt + outputs)`` then unlock of the prompt's node; slots
   of any part that another request had already inserted are freed.
 
+With pages of more than one slot (keys page-aligned, "SGLang: the tree, and
+the language nobody remembers", section "A tree, not a map"), the readings
+are the same with every length counted in whole pages:
+
+* the in-batch rule compares the common prefix rounded down to whole pages
+  with the (page-aligned) tree match;
+* a batch takes, in member order, ``ceil(new tokens / page_size)`` pages per
+  member from one allocation, and a member's new tokens fill its pages in
+  order (a request never shares a page with another);
+* only the whole pages of a prompt are inserted; its last, partly filled page
+  stays private to the request;
+* a decode token whose position starts a page takes a new page (one
+  allocation per step for all requests that need one, in request order), any
+  other takes the next slot of the request's last page;
+* at finish the whole pages of prompt + outputs are inserted; the request
+  frees its pages that another request had already inserted and the partly
+  filled page past the last whole one.
+
 Parity: pinned by ``tests/test_oracle_pins.py`` (12,960 / 6,660 / 3,060 prefill
 counts of the nested example; 2,800 of 3,000 reused at agent step 5).
 """
@@ -69,7 +87,7 @@ def plan_batches(cache, wave_prompts):
     batch = []
     for j, prompt in enumerate(wave_prompts):
         m = cache.match_length(prompt[:len(prompt) - 1])
-        if batch and any(common_prefix_length(prompt, wave_prompts[i]) > m
+        if batch and any(cache.aligned(common_prefix_length(prompt, wave_prompts[i])) > m
                          for i in batch):
             yield batch
             batch = []
@@ -79,7 +97,7 @@ def plan_batches(cache, wave_prompts):
 
 
 def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
-                    on_decode=None):
+                    on_decode=None, page_size=1):
     """Run the request flow over a fresh oracle cache.
 
     waves: list of waves; a wave is a list of ``(rid, prompt, outputs)`` with
@@ -88,7 +106,8 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
     ``on_decode(step, rows)`` are optional callbacks for attention checks.
     Returns ``(trace, cache)``.
     """
-    cache = RadixCache(num_slots)
+    cache = RadixCache(num_slots, page_size)
+    ps = page_size
     trace = Trace()
     for wave in waves:
         prompts = [list(p) for _, p, _ in wave]
@@ -102,15 +121,15 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
                 slots, node = cache.match_prefix(prompts[j][:len(prompts[j]) - 1])
                 cache.inc_lock_ref(node)
                 matched.append((j, slots, node))
-            total_new = sum(len(prompts[j]) - len(s) for j, s, _ in matched)
-            new_slots = cache.alloc(total_new)
+            pages_of = [-(-(len(prompts[j]) - len(s)) // ps) for j, s, _ in matched]
+            new_pages = cache.alloc_pages(sum(pages_of))
             records = []
             pos = 0
-            for j, slots, node in matched:
+            for (j, slots, node), n_pages in zip(matched, pages_of):
                 rid = wave[j][0]
                 n_new = len(prompts[j]) - len(slots)
-                row = list(slots) + new_slots[pos:pos + n_new]
-                pos += n_new
+                row = list(slots) + cache.page_slots(new_pages[pos:pos + n_pages], n_new)
+                pos += n_pages
                 rows[rid] = row
                 records.append((rid, len(slots), list(row)))
                 trace.prefilled += n_new
@@ -127,7 +146,11 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
                 cache.dec_lock_ref(node)
                 prompt_nodes[rid] = node2
         for step in range(decode_steps):
-            slots = cache.alloc(len(wave))
+            need = [len(rows[rid]) % ps == 0 for rid, _, _ in wave]
+            pages = cache.alloc_pages(sum(need))
+            slots = []
+            for (rid, _, _), starts_page in zip(wave, need):
+                slots.append(pages.pop(0) * ps if starts_page else rows[rid][-1] + 1)
             step_rec = []
             for (rid, _, _), s in zip(wave, slots):
                 rows[rid].append(s)
@@ -138,8 +161,10 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
         for rid, prompt, outputs in wave:
             full = list(prompt) + list(outputs[:decode_steps])
             already, _ = cache.insert(full, rows[rid])
-            if already > len(prompt):
-                cache.free(rows[rid][len(prompt):already])
+            if already > cache.aligned(len(prompt)):
+                cache.free(rows[rid][cache.aligned(len(prompt)):already])
+            if cache.aligned(len(full)) < len(full):      # the partly filled last page
+                cache.free(rows[rid][cache.aligned(len(full)):])
             trace.finishes.append((rid, already))
             cache.dec_lock_ref(prompt_nodes[rid])
     trace.eviction_log = list(cache.eviction_log)

@@ -21,9 +21,18 @@ Sources (page title, section):
   unlock) and "Worked example, step by step" (a node is evicted whole; locked
   nodes are never candidates; if nothing can be evicted the request waits).
 
+* same page, same section: keys are page-aligned -- every key is truncated to
+  a multiple of ``page_size`` and a match is rounded down to one -- and a
+  node's children are keyed on the first token at ``page_size == 1`` and on
+  the tuple of the first ``page_size`` tokens otherwise.
+
 Readings where the pages are silent:
 
-* token granularity only (``page_size == 1``);
+* the pool is cut into pages of ``page_size`` consecutive slots; page 0 (slots
+  ``0 .. page_size-1``) is a pad page that is never handed out, and the
+  allocator hands out whole pages, so a request's positions ``[k*page_size,
+  (k+1)*page_size)`` always lie in one page, in slot order (at
+  ``page_size == 1`` a page is a slot);
 * a match that ends inside an edge splits that edge so the returned node covers
   exactly the matched prefix; the new upper node takes a fresh id and inherits
   the lower node's ``lock_ref`` and ``last_access_time``;
@@ -31,8 +40,9 @@ Readings where the pages are silent:
   or ``insert`` call and is written on every node of the touched path;
 * the eviction key is ``(priority, last_access_time, node id)`` with
   ``priority == 0`` everywhere, i.e. least recently used, ties by creation order;
-* the allocator is a FIFO free list initialised ``1 .. N-1`` (slot 0 is a pad
-  slot that is never handed out); freed slots join the tail in the order given;
+* the allocator is a FIFO free list of pages initialised ``1 .. N/page_size -
+  1``; freed pages join the tail in the order given (a page once, at the first
+  of its slots);
 * an allocation that cannot be met after evicting everything evictable fails
   with ``NoSpace``; nodes evicted during that attempt stay evicted.
 
@@ -77,13 +87,15 @@ def common_prefix_length(a, b):
 
 
 class RadixCache:
-    """Radix tree over token prefixes plus the FIFO slot allocator."""
+    """Radix tree over token prefixes plus the FIFO page allocator."""
 
-    def __init__(self, num_slots):
-        if num_slots < 1:
-            raise ValueError("num_slots must be >= 1")
+    def __init__(self, num_slots, page_size=1):
+        if page_size < 1 or num_slots < page_size or num_slots % page_size:
+            raise ValueError("num_slots must be a positive multiple of page_size")
         self.num_slots = num_slots
-        self.free_slots = deque(range(1, num_slots))   # slot 0 is the pad slot
+        self.page_size = page_size
+        # page 0 is the pad page
+        self.free_pages = deque(range(1, num_slots // page_size))
         self.root = TreeNode(0, [], [], None)
         self.next_id = 1
         self.clock = 0
@@ -91,6 +103,24 @@ class RadixCache:
         self.protected_size_ = 0
         self.nodes = {0: self.root}
         self.eviction_log = []        # (node id, number of tokens) in order
+
+    # ------------------------------------------------------------- pages
+    def aligned(self, n):
+        """``n`` rounded down to a whole number of pages."""
+        return n - n % self.page_size
+
+    def child_key(self, tokens, pos):
+        """Key of the child that starts at ``tokens[pos]``: the token itself at
+        page size 1, else the tuple of the page's tokens."""
+        if self.page_size == 1:
+            return tokens[pos]
+        return tuple(tokens[pos:pos + self.page_size])
+
+    @property
+    def free_slots(self):
+        """Slots of the free pages, in free-list order."""
+        ps = self.page_size
+        return [p * ps + j for p in self.free_pages for j in range(ps)]
 
     # ------------------------------------------------------------------ walk
     def _new_node(self, key, value, parent):
@@ -110,22 +140,23 @@ class RadixCache:
         upper = self._new_node(node.key[:k], node.value[:k], parent)
         upper.lock_ref = node.lock_ref
         upper.last_access_time = node.last_access_time
-        parent.children[node.key[0]] = upper
+        parent.children[self.child_key(node.key, 0)] = upper
         node.key = node.key[k:]
         node.value = node.value[k:]
         node.parent = upper
-        upper.children[node.key[0]] = node
+        upper.children[self.child_key(node.key, 0)] = node
         return upper
 
     def match_length(self, tokens):
-        """Longest cached prefix of ``tokens``, with no side effects."""
+        """Longest cached prefix of ``tokens`` (whole pages), no side effects."""
+        tokens = tokens[:self.aligned(len(tokens))]
         node = self.root
         pos = 0
         while pos < len(tokens):
-            child = node.children.get(tokens[pos])
+            child = node.children.get(self.child_key(tokens, pos))
             if child is None:
                 break
-            k = common_prefix_length(child.key, tokens[pos:])
+            k = self.aligned(common_prefix_length(child.key, tokens[pos:]))
             pos += k
             if k < len(child.key):
                 break
@@ -134,14 +165,15 @@ class RadixCache:
 
     def lookup_slots(self, tokens):
         """Slots of the longest cached prefix of ``tokens``, no side effects."""
+        tokens = tokens[:self.aligned(len(tokens))]
         node = self.root
         pos = 0
         out = []
         while pos < len(tokens):
-            child = node.children.get(tokens[pos])
+            child = node.children.get(self.child_key(tokens, pos))
             if child is None:
                 break
-            k = common_prefix_length(child.key, tokens[pos:])
+            k = self.aligned(common_prefix_length(child.key, tokens[pos:]))
             out.extend(child.value[:k])
             pos += k
             if k < len(child.key):
@@ -154,19 +186,22 @@ class RadixCache:
 
         Returns ``(slots, node)``: the KV slots of the matched prefix, in
         order, and the node whose path from the root is exactly that prefix
-        (the root when nothing matched).  A match ending inside an edge splits
-        that edge.  Every node on the matched path is touched.
+        (the root when nothing matched).  Only whole pages match: ``tokens``
+        is truncated to whole pages and the match inside an edge rounded down
+        to one.  A match ending inside an edge splits that edge.  Every node
+        on the matched path is touched.
         """
         self.clock += 1
+        tokens = tokens[:self.aligned(len(tokens))]
         node = self.root
         slots = []
         pos = 0
         path = []
         while pos < len(tokens):
-            child = node.children.get(tokens[pos])
+            child = node.children.get(self.child_key(tokens, pos))
             if child is None:
                 break
-            k = common_prefix_length(child.key, tokens[pos:])
+            k = self.aligned(common_prefix_length(child.key, tokens[pos:]))
             if k < len(child.key):
                 child = self._split(child, k)
             slots.extend(child.value)
@@ -180,23 +215,27 @@ class RadixCache:
     def insert(self, tokens, slots):
         """Insert ``tokens`` with their KV ``slots``.
 
-        Walks (and splits) as ``match_prefix`` does; the part of ``tokens``
-        not yet in the tree becomes one new leaf holding the matching part of
-        ``slots``.  Returns ``(already, node)``: how many leading tokens were
-        already cached (the caller frees its own slots for that part beyond
-        what it had locked) and the node that ends exactly at ``len(tokens)``.
+        Only the whole pages of ``tokens`` are inserted (the key is
+        truncated to a multiple of the page size).  Walks (and splits) as
+        ``match_prefix`` does; the part not yet in the tree becomes one new
+        leaf holding the matching part of ``slots``.  Returns ``(already,
+        node)``: how many leading tokens were already cached (the caller frees
+        its own slots for that part beyond what it had locked) and the node
+        that ends exactly at the truncated length.
         """
         if len(tokens) != len(slots):
             raise ValueError("tokens and slots differ in length")
+        n = self.aligned(len(tokens))
+        tokens, slots = list(tokens[:n]), list(slots[:n])
         self.clock += 1
         node = self.root
         pos = 0
         path = []
         while pos < len(tokens):
-            child = node.children.get(tokens[pos])
+            child = node.children.get(self.child_key(tokens, pos))
             if child is None:
                 break
-            k = common_prefix_length(child.key, tokens[pos:])
+            k = self.aligned(common_prefix_length(child.key, tokens[pos:]))
             if k < len(child.key):
                 child = self._split(child, k)
             pos += k
@@ -205,7 +244,7 @@ class RadixCache:
         already = pos
         if pos < len(tokens):
             leaf = self._new_node(tokens[pos:], slots[pos:], node)
-            node.children[tokens[pos]] = leaf
+            node.children[self.child_key(tokens, pos)] = leaf
             self.evictable_size_ += len(leaf.key)
             path.append(leaf)
             node = leaf
@@ -258,7 +297,7 @@ class RadixCache:
         """Free at least ``num_tokens`` slots by evicting unlocked leaves.
 
         Candidates are the unlocked leaves, ordered by ``(priority,
-        last_access_time, id)``.  The smallest is evicted whole, its slots go
+        last_access_time, id)``.  The smallest is evicted whole, its pages go
         to the tail of the free list in stored order, and its parent becomes a
         candidate once childless and unlocked.  Stops when enough is freed or
         no candidate is left; returns the number of slots freed.
@@ -270,8 +309,9 @@ class RadixCache:
         while freed < num_tokens and heap:
             _, _, _, victim = heapq.heappop(heap)
             parent = victim.parent
-            del parent.children[victim.key[0]]
-            self.free_slots.extend(victim.value)
+            del parent.children[self.child_key(victim.key, 0)]
+            self.free_pages.extend(s // self.page_size
+                                   for s in victim.value[::self.page_size])
             freed += len(victim.value)
             self.evictable_size_ -= len(victim.key)
             self.eviction_log.append((victim.id, len(victim.key)))
@@ -284,18 +324,37 @@ class RadixCache:
         return freed
 
     # ----------------------------------------------------------- allocator
-    def alloc(self, k):
-        """Take ``k`` slots from the head of the free list, evicting if short."""
-        if k < 0:
+    def alloc_pages(self, n):
+        """Take ``n`` pages from the head of the free list, evicting the
+        shortfall first (in slots) if too few are free."""
+        if n < 0:
             raise ValueError("negative allocation")
-        if len(self.free_slots) < k:
-            self.evict(k - len(self.free_slots))
-        if len(self.free_slots) < k:
-            raise NoSpace(k)
-        return [self.free_slots.popleft() for _ in range(k)]
+        if len(self.free_pages) < n:
+            self.evict((n - len(self.free_pages)) * self.page_size)
+        if len(self.free_pages) < n:
+            raise NoSpace(n)
+        return [self.free_pages.popleft() for _ in range(n)]
+
+    def page_slots(self, pages, k):
+        """The first ``k`` slots of ``pages``, page after page."""
+        ps = self.page_size
+        return [p * ps + j for p in pages for j in range(ps)][:k]
+
+    def alloc(self, k):
+        """``k`` slots: the first ``k`` slots of the ``ceil(k / page_size)``
+        pages taken from the head of the free list (evicting if short)."""
+        ps = self.page_size
+        return self.page_slots(self.alloc_pages(-(-k // ps)), k)
 
     def free(self, slots):
-        self.free_slots.extend(slots)
+        """Return the pages the given slots lie in (each once, in order)."""
+        seen, order = set(), []
+        for s in slots:
+            p = s // self.page_size
+            if p not in seen:
+                seen.add(p)
+                order.append(p)
+        self.free_pages.extend(order)
 
     # --------------------------------------------------------------- stats
     def cached_size(self):

@@ -8,7 +8,8 @@ pass.  Every substitution must match the oracle's source exactly once, so a
 change to the oracle that makes a mutation inapplicable fails here too.
 
 The mistakes cover the cache (heap order, split attributes, the cascade
-condition, allocator order, access times, lock paths, eviction candidates),
+condition, allocator order, access times, lock paths, eviction candidates,
+page alignment of keys, matches and child keys),
 the request flow (in-batch rule, what is matched, adoption of identical
 prompts, what finish inserts and frees, decode tokens kept out of the tree,
 lock release) and attention (scale, GQA head, causal boundary, log-sum-exp).
@@ -47,15 +48,18 @@ MUTANTS = {
          "                    and parent.lock_ref == 0):",
          "if False:")]),
     "allocator_lifo": ("radix_cache.py", [
-        ("return [self.free_slots.popleft() for _ in range(k)]",
-         "return [self.free_slots.pop() for _ in range(k)]")]),
+        ("return [self.free_pages.popleft() for _ in range(n)]",
+         "return [self.free_pages.pop() for _ in range(n)]")]),
     "match_does_not_touch": ("radix_cache.py", [
         ("        for n in path:\n            n.last_access_time = self.clock\n"
          "        return slots, node",
          "        return slots, node")]),
     "evicted_slots_reversed": ("radix_cache.py", [
-        ("self.free_slots.extend(victim.value)",
-         "self.free_slots.extend(reversed(victim.value))")]),
+        ("for s in victim.value[::self.page_size])",
+         "for s in victim.value[::-self.page_size])")]),
+    "evicted_pages_keep_only_first": ("radix_cache.py", [
+        ("for s in victim.value[::self.page_size])",
+         "for s in victim.value[:1])")]),
     "lock_only_the_node": ("radix_cache.py", [
         ("            node.lock_ref += 1\n            node = node.parent",
          "            node.lock_ref += 1\n            break")]),
@@ -92,8 +96,29 @@ MUTANTS = {
          "                rows[rid].append(s)\n"
          "                cache.insert(list(p_) + list(o_[:step + 1]), rows[rid])\n")]),
     "finish_keeps_duplicate_slots": ("harness.py", [
-        ("            if already > len(prompt):\n"
-         "                cache.free(rows[rid][len(prompt):already])\n", "")]),
+        ("            if already > cache.aligned(len(prompt)):\n"
+         "                cache.free(rows[rid][cache.aligned(len(prompt)):already])\n", "")]),
+    "finish_keeps_partial_page": ("harness.py", [
+        ("                cache.free(rows[rid][cache.aligned(len(full)):])\n",
+         "                pass\n")]),
+    "match_not_rounded_to_pages": ("radix_cache.py", [
+        ("            k = self.aligned(common_prefix_length(child.key, tokens[pos:]))\n"
+         "            if k < len(child.key):\n                child = self._split(child, k)\n"
+         "            slots.extend(child.value)",
+         "            k = common_prefix_length(child.key, tokens[pos:])\n"
+         "            if k < len(child.key):\n                child = self._split(child, k)\n"
+         "            slots.extend(child.value)")]),
+    "insert_keeps_partial_page": ("radix_cache.py", [
+        ("        n = self.aligned(len(tokens))\n", "        n = len(tokens)\n")]),
+    "children_keyed_on_first_token": ("radix_cache.py", [
+        ("        if self.page_size == 1:\n            return tokens[pos]\n",
+         "        if True:\n            return tokens[pos]\n")]),
+    "decode_page_not_started": ("harness.py", [
+        ("need = [len(rows[rid]) % ps == 0 for rid, _, _ in wave]",
+         "need = [len(rows[rid]) % ps == 1 % ps for rid, _, _ in wave]")]),
+    "in_batch_rule_unrounded": ("harness.py", [
+        ("if batch and any(cache.aligned(common_prefix_length(prompt, wave_prompts[i])) > m",
+         "if batch and any(common_prefix_length(prompt, wave_prompts[i]) > m")]),
     "no_adoption_of_identical_prompt": ("harness.py", [
         ("                if already > m:\n"
          "                    tree = cache.lookup_slots(prompts[j])[m:already]\n"

@@ -469,11 +469,13 @@ def _tree_slots(cache):
 
 
 def _assert_slots_conserved(cache):
-    """Once every request has finished, each slot 1 .. N-1 is either held by
-    exactly one tree position or on the free list, never both and never
-    neither (no slot leaked, none handed out twice)."""
+    """Once every request has finished, each slot outside the pad page is
+    either held by exactly one tree position or on the free list (a page is
+    free as a whole), never both and never neither (no slot leaked, none
+    handed out twice)."""
     held = _tree_slots(cache) + list(cache.free_slots)
-    assert sorted(held) == list(range(1, cache.num_slots)), "slots leaked or duplicated"
+    assert sorted(held) == list(range(cache.page_size, cache.num_slots)), \
+        "slots leaked or duplicated"
     assert len(set(_tree_slots(cache))) == cache.cached_size()
 
 
@@ -591,3 +593,184 @@ def test_request_flow_conserves_slots(make):
     trace, cache = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
     _assert_slots_conserved(cache)
     assert trace.stats["protected"] == 0
+
+
+# ------------------------------------------------------------------- pages
+def _toy_run(page_size):
+    reqs, _, _ = _toy_fixture()
+    vocab = {}
+    cache = RadixCache(4096, page_size)
+    got = []
+    for words in reqs:
+        toks = [vocab.setdefault(w, len(vocab)) for w in words]
+        slots, node = cache.match_prefix(toks)
+        new = cache.alloc(len(toks) - len(slots))
+        cache.insert(toks, slots + new)
+        got.append(len(slots))
+    return reqs, got
+
+
+@pytest.mark.parametrize("page_size", [2, 4, 8, 16])
+def test_toy_trie_reuse_counts_with_pages(page_size):
+    """The toy's requests with page-aligned keys: reuse per request as derived
+    by hand (fixture), and as brute force over the request strings."""
+    want = {}
+    for ln in read_golden("toy_trie_reuse_pages.txt"):
+        ps, rest = ln.split(":")
+        *counts, total = rest.split()
+        want[int(ps)] = ([int(c) for c in counts], total)
+    reqs, got = _toy_run(page_size)
+    counts, total = want[page_size]
+    assert got == counts
+    assert f"{sum(got)}/{sum(len(r) for r in reqs)}" == total
+    # brute force: longest whole-page prefix shared with an earlier request's
+    # whole pages
+    al = lambda n: n - n % page_size
+    brute = []
+    for i, r in enumerate(reqs):
+        best = 0
+        for j in range(i):
+            c = 0
+            while c < min(len(r), len(reqs[j])) and r[c] == reqs[j][c]:
+                c += 1
+            best = max(best, min(c, al(len(reqs[j]))))
+        brute.append(al(best))
+    assert brute == counts
+
+
+@pytest.mark.parametrize("page_size,want", [(4, 3060), (60, 3060), (16, 3136)])
+def test_nested_example_with_pages(page_size, want):
+    g = {ln.split()[2]: int(ln.split()[4]) for ln in read_golden("nested_prefill_counts.txt")
+         if ln.startswith("case page")}
+    assert g[str(page_size)] == want
+    wl = workloads.nested_share()
+    slots = (wl.num_slots // page_size + 40) * page_size
+    trace, cache = run_bookkeeping(wl.oracle_waves(), slots, 0, page_size=page_size)
+    assert trace.prefilled == want
+    assert [[rid for rid, _, _ in b] for b in trace.batches] == [[0], [1, 2, 3, 4], [5, 6, 7]]
+    _assert_slots_conserved(cache)
+
+
+@pytest.mark.parametrize("locked,victim,held", [
+    ("C", "A", 3500), ("AC", "B", 3800), ("ABC", None, None)])
+def test_worked_eviction_example_with_pages(locked, victim, held):
+    """Every size of the worked example is a multiple of 100: with pages of
+    100 slots (one pad page) the same node goes and the same occupancy
+    results."""
+    g = _golden_kv("worked_eviction.txt")
+    ps = 100
+    cache = RadixCache(g["capacity"] + ps, ps)
+    rng = random.Random(7)
+    seq = lambda n: [rng.randrange(32000) for _ in range(n)]
+    s = seq(g["S"])
+    nodes = {}
+    for b in "ABC":
+        toks = s + seq(g[b])
+        slots, _ = cache.match_prefix(toks)
+        _, nodes[b] = cache.insert(toks, slots + cache.alloc(len(toks) - len(slots)))
+    for b in locked:
+        cache.inc_lock_ref(nodes[b])
+    d = s + seq(g["D_new"])
+    slots, dnode = cache.match_prefix(d[:-1])
+    assert len(slots) == g["S"]
+    cache.inc_lock_ref(dnode)
+    if victim is None:
+        with pytest.raises(NoSpace):
+            cache.alloc(g["D_new"])
+        assert cache.eviction_log == []
+        return
+    new = cache.alloc(g["D_new"])
+    assert cache.eviction_log == [(nodes[victim].id, g[victim])]
+    cache.insert(d, slots + new)
+    assert cache.cached_size() == held
+
+
+@pytest.mark.parametrize("page_size", [2, 3])
+def test_match_against_page_prefix_dictionary(page_size):
+    """Match length and slots equal a naive dictionary of the whole-page
+    prefixes of every inserted sequence (tiny alphabets)."""
+    rng = random.Random(13 + page_size)
+    al = lambda n: n - n % page_size
+    for trial in range(200):
+        alpha = rng.randint(1, 3)
+        cache = RadixCache(3000 * page_size, page_size)
+        slot_at = {}             # whole-page prefix -> slots of its last page
+        for _ in range(rng.randint(1, 8)):
+            seq = [rng.randrange(alpha) for _ in range(rng.randint(1, 14))]
+            n = 0
+            while n + page_size <= len(seq) and tuple(seq[:n + page_size]) in slot_at:
+                n += page_size
+            want = []
+            for p in range(page_size, n + 1, page_size):
+                want += slot_at[tuple(seq[:p])]
+            assert cache.match_length(seq) == n
+            slots, node = cache.match_prefix(seq)
+            assert slots == want
+            new = cache.alloc(len(seq) - n)
+            row = slots + new
+            already, _ = cache.insert(seq, row)
+            assert already == n
+            for p in range(page_size, al(len(seq)) + 1, page_size):
+                slot_at.setdefault(tuple(seq[:p]), row[p - page_size:p])
+        assert cache.cached_size() == len(slot_at) * page_size
+
+
+def test_page_allocator_reading():
+    """Reading (pages silent on the order): a FIFO free list of pages 1 ..
+    N/page_size - 1 (page 0 is the pad page); a request's slots fill its
+    pages in order; freeing any slot of a page returns the whole page, once."""
+    cache = RadixCache(24, 4)
+    assert cache.alloc(5) == [4, 5, 6, 7, 8]
+    assert cache.alloc(4) == [12, 13, 14, 15]
+    cache.free([9, 8, 6])
+    assert list(cache.free_pages) == [4, 5, 2, 1]
+    assert cache.alloc(12) == [16, 17, 18, 19, 20, 21, 22, 23, 8, 9, 10, 11]
+    with pytest.raises(NoSpace):
+        cache.alloc(5)
+
+
+def _assert_rows_page_consistent(rows, ps):
+    """Positions [k ps, (k+1) ps) of a request lie in one page, in order."""
+    for row in rows.values():
+        for p, s in enumerate(row):
+            assert s % ps == p % ps and s // ps == row[p - p % ps] // ps
+
+
+@pytest.mark.parametrize("page_size", [4, 16])
+@pytest.mark.parametrize("make", [
+    lambda: workloads.agent_loop(calls=7, preamble=120, lo=5, hi=40, decode_steps=9),
+    lambda: workloads.fork_tree(branching=3, depth=3, level_tokens=24, decode_steps=5),
+    lambda: workloads.multi_turn_chat(sessions=4, turns=3, system=50, user=13, decode_steps=6,
+                                      layers=1),
+])
+def test_request_flow_with_pages_conserves_pages(make, page_size):
+    """With pages: every row keeps each page's positions together and in
+    order at every decode step, and after the flow every page is held by
+    exactly one tree position or the free list (fork_tree evicts)."""
+    wl = make()
+    seen = {}
+
+    def on_decode(step, rows):
+        seen[step] = True
+        _assert_rows_page_consistent(rows, page_size)
+
+    slots = -(-int(wl.num_slots * 1.3) // page_size) * page_size
+    trace, cache = run_bookkeeping(wl.oracle_waves(), slots, wl.decode_steps,
+                                   on_decode=on_decode, page_size=page_size)
+    assert seen
+    for b in trace.batches:
+        for rid, m, row in b:
+            assert m % page_size == 0
+    _assert_slots_conserved(cache)
+    assert trace.stats["protected"] == 0
+
+
+@pytest.mark.parametrize("actions", [8, 32])
+def test_agent_steps_through_decode_reuse_with_pages(actions):
+    """The agent example through decode with pages of 8 slots: every length
+    of the example is a multiple of 8, so step 5 again reuses 2,800 + D."""
+    waves, g = _agent_steps_with_actions(actions)
+    trace, cache = run_bookkeeping(waves, 16000, actions, page_size=8)
+    rid, m, row = trace.batches[g["step"] - 1][0]
+    assert len(row) == g["prompt_tokens"] and m == g["reused"] + actions
+    _assert_slots_conserved(cache)
