@@ -206,7 +206,8 @@ def oracle_bookkeeping(wl):
     """The oracle's request flow over the whole workload, timed."""
     from oracle.harness import run_bookkeeping
     t0 = time.perf_counter()
-    trace, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+    trace, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                                   page_size=wl.page_size)
     return trace, time.perf_counter() - t0
 
 

@@ -9,7 +9,9 @@
  *   [T]  "SGLang: the tree, and the language nobody remembers"
  *        - "A tree, not a map": TreeNode fields, lock_ref accounting, heap
  *          eviction cascading to childless unlocked parents, node split at
- *          divergence, children keyed on the first token at page_size 1.
+ *          divergence, children keyed on the first token at page_size 1 and
+ *          on the first page otherwise; keys truncated to whole pages and
+ *          matches rounded down to a page (page_aligned).
  *        - "What the C++ tree is actually for": match_prefix returns the
  *          matched KV indices and a node handle.
  *        - "Speculative decoding puts a tree inside the tree": a tree node
@@ -42,6 +44,13 @@
  *   - Token ids and slots are int32.  Slot 0 is a pad slot that the allocator
  *     never hands out; kernels read it for out-of-range keys only as a
  *     harmless address and mask the value.
+ *   - Pages: the pool is cut into pages of page_size consecutive slots (page
+ *     p = slots p*page_size .. p*page_size+page_size-1); page 0 is the pad
+ *     page.  The cache hands out and takes back whole pages, keys in the tree
+ *     are whole pages, and a request's positions [k*page_size,
+ *     (k+1)*page_size) always lie in one page, in slot order.  At page_size 1
+ *     a page is a slot and every rule below reduces to token granularity.
+ *     The kernels read slot tables and are the same at every page size.
  *   - KV pool layout (device, bf16): K and V each [num_layers][num_kv_heads]
  *     [num_slots][head_dim], row-major; one slot row of one head is head_dim
  *     contiguous bf16 (256 B at d=128, 512 B at d=256).  Pool base pointers
@@ -76,8 +85,9 @@ typedef int64_t rx_node;
 typedef struct rx_cache rx_cache;
 
 typedef struct rx_config {
-  int64_t num_slots; /* pool slots including pad slot 0; >= 1            */
-  int32_t page_size; /* must be 1 (token granularity)                    */
+  int64_t num_slots; /* pool slots including the pad page; a multiple of
+                        page_size                                        */
+  int32_t page_size; /* slots per page, >= 1 (1 = token granularity)     */
   int32_t reserved;  /* must be 0                                         */
 } rx_config;
 
@@ -101,9 +111,10 @@ typedef struct rx_evict_rec {
  * Cache lifecycle
  * ---------------------------------------------------------------------- */
 
-/* Create an empty tree and a FIFO free list holding slots 1 .. num_slots-1
- * (reading: the pages do not fix the allocator order).
- * Errors: RX_ERR_INVALID if num_slots < 1, page_size != 1 or out == NULL. */
+/* Create an empty tree and a FIFO free list holding pages 1 ..
+ * num_slots/page_size - 1 (reading: the pages do not fix the allocator
+ * order).  Errors: RX_ERR_INVALID if page_size < 1, num_slots is not a
+ * positive multiple of page_size, or out == NULL. */
 rx_status rx_cache_create(const rx_config* cfg, rx_cache** out);
 rx_status rx_cache_destroy(rx_cache* cache);
 
@@ -115,15 +126,18 @@ size_t rx_last_error(char* buf, size_t cap);
  * S1 match  ([T] "A tree, not a map", [B] "One tree for everybody")
  * ---------------------------------------------------------------------- */
 
-/* Longest cached prefix of tokens[0..n) without side effects (no split, no
- * access-time update).  Used by the in-batch prefix rule. */
+/* Longest cached prefix of tokens[0..n) in whole pages, without side
+ * effects (no split, no access-time update).  Used by the in-batch prefix
+ * rule. */
 rx_status rx_match_length(const rx_cache* cache, const int32_t* tokens,
                           int64_t n, int64_t* out_len);
 
-/* Walk from the root as far as tokens[0..n) match.  Writes the matched
- * prefix's slots to out_slots (caller capacity >= n), its length to *out_len
- * and the node whose root path is exactly that prefix to *out_node (0 when
- * nothing matched).  A match ending inside an edge splits the edge there
+/* Walk from the root as far as tokens[0..n) match, in whole pages (n is
+ * truncated to whole pages, a match inside an edge rounded down to one).
+ * Writes the matched prefix's slots to out_slots (caller capacity >= n), its
+ * length to *out_len and the node whose root path is exactly that prefix to
+ * *out_node (0 when nothing matched).  A match ending inside an edge splits
+ * the edge there
  * (reading: so the returned node covers exactly the matched prefix).  The
  * access clock advances by one and every node on the matched path takes it.
  * Errors: RX_ERR_INVALID on NULL pointers or n < 0. */
@@ -150,29 +164,34 @@ rx_status rx_unlock(rx_cache* cache, rx_node node);
  * S3 allocate / evict  ([T] heap eviction, [L] "Worked example")
  * ---------------------------------------------------------------------- */
 
-/* Take k slots from the head of the free list into out_slots[0..k).  If
- * fewer than k are free, first evict (rx_evict) the shortfall.  If still
- * short: RX_ERR_NO_SPACE, nothing is allocated, and nodes evicted during the
- * attempt stay evicted ("D would have to wait"). */
+/* Take ceil(k / page_size) pages from the head of the free list and write
+ * their first k slots, page after page, to out_slots[0..k) (the rest of the
+ * last page belongs to the caller too).  If too few pages are free, first
+ * evict (rx_evict) the shortfall.  If still short: RX_ERR_NO_SPACE, nothing
+ * is allocated, and nodes evicted during the attempt stay evicted ("D would
+ * have to wait"). */
 rx_status rx_alloc(rx_cache* cache, int64_t k, int32_t* out_slots);
 
 /* Evict unlocked leaves, least recent first (key: priority 0,
- * last_access_time, node id), each node whole; its slots join the free-list
+ * last_access_time, node id), each node whole; its pages join the free-list
  * tail in stored order; a parent that becomes childless and unlocked joins
  * the candidates.  Stops once >= k slots were freed or no candidate is left.
  * *out_freed = slots freed (may exceed k). */
 rx_status rx_evict(rx_cache* cache, int64_t k, int64_t* out_freed);
 
-/* Return slots to the free-list tail, in the given order.  The caller must
- * own them (allocated and not held by the tree). */
+/* Return the pages of the given slots to the free-list tail, each page once,
+ * in the order of its first slot.  The caller must own those whole pages
+ * (allocated and not held by the tree).  Errors: RX_ERR_INVALID for a slot in
+ * the pad page or beyond the pool. */
 rx_status rx_free(rx_cache* cache, const int32_t* slots, int64_t k);
 
 /* ------------------------------------------------------------------------
  * S10 insert  ([B] "the divergent part becomes a new branch", [L] step 4)
  * ---------------------------------------------------------------------- */
 
-/* Insert tokens[0..n) with their slots.  Walks and splits as rx_match_prefix;
- * the uncached remainder becomes one new leaf holding slots of that part.
+/* Insert the whole pages of tokens[0..n) with their slots (n truncated to
+ * whole pages).  Walks and splits as rx_match_prefix; the uncached remainder
+ * becomes one new leaf holding slots of that part.
  * *out_already = tokens that were already cached (the caller still owns its
  * own slots for that part and frees those beyond what it had locked);
  * *out_node = node ending exactly at n.  The access clock advances by one and
@@ -206,7 +225,8 @@ rx_status rx_node_depth(const rx_cache* cache, rx_node node,
  * of the wave's offsets; the same holds for rx_extend_end).  In request
  * order: rx_match_prefix on the prompt without its last token (the last prompt
  * token is always recomputed) and rx_lock of the matched node; then ONE
- * rx_alloc of all new tokens, handed out in request order.  Writes
+ * allocation of every request's ceil(new tokens / page_size) pages, handed
+ * out in request order (a request's new tokens fill its own pages).  Writes
  *   req_to_token[r*row_stride + 0 .. n_r)  = matched slots ++ new slots,
  *   out_prefix_len[r], out_match_node[r],
  *   out_new_slots[0 .. total_new) = the new slots in request order (the K/V
@@ -220,10 +240,11 @@ rx_status rx_extend_begin(rx_cache* cache, int32_t R, const int32_t* tokens,
                           int64_t* out_total_new);
 
 /* S10 after an extend batch: for each request in order rx_insert(prompt,
- * row), rx_lock(prompt node), rx_unlock(matched node).  Writes
+ * row) (its whole pages; a partly filled last page stays the request's),
+ * rx_lock(prompt node), rx_unlock(matched node).  Writes
  * out_prompt_node[r].  If a prompt finds more of itself cached than its
  * match (an identical prompt was inserted by an earlier batch), the
- * request's own slots for that part go back to the free list and its row is
+ * request's own pages for that part go back to the free list and its row is
  * rewritten in place with the tree's slots (same tokens after the same
  * predecessors, so the same K/V); *out_rewritten (may be NULL) counts the
  * requests whose row changed, so the caller can refresh device rows. */
@@ -235,17 +256,19 @@ rx_status rx_extend_end(rx_cache* cache, int32_t R, const int32_t* tokens,
 
 /* Finish (S10): for each request, rx_insert(prompt ++ outputs, row) where
  * tokens/tok_indptr hold prompt ++ outputs and the row holds their slots;
- * slots of any part beyond prompt_len[r] that was already cached are freed;
- * then rx_unlock(prompt_node[r]).  out_already[r] may be NULL. */
+ * the request's pages past the prompt's whole pages that another request
+ * had already inserted, and its partly filled last page, are freed; then
+ * rx_unlock(prompt_node[r]).  out_already[r] may be NULL. */
 rx_status rx_finish(rx_cache* cache, int32_t R, const int32_t* tokens,
                     const int64_t* tok_indptr, const int32_t* req_to_token,
                     int64_t row_stride, const int64_t* prompt_len,
                     const rx_node* prompt_node, int64_t* out_already);
 
 /* In-batch prefix rule ([T] "The scheduler is where the cache is won or
- * lost"): *out_conflict = 1 if the common prefix of tokens[0..n) with any of
- * the R member prompts (concatenated as in rx_extend_begin) is longer than
- * match_len, else 0. */
+ * lost") at token granularity: *out_conflict = 1 if the common prefix of
+ * tokens[0..n) with any of the R member prompts (concatenated as in
+ * rx_extend_begin) is longer than match_len, else 0.  (rx_batch_end applies
+ * the rule in whole pages of its cache.) */
 rx_status rx_batch_conflict(const int32_t* tokens, int64_t n,
                             int64_t match_len, int32_t R,
                             const int32_t* member_tokens,
@@ -254,8 +277,9 @@ rx_status rx_batch_conflict(const int32_t* tokens, int64_t n,
 
 /* The batch that starts at request `start` of a wave, under the same rule:
  * requests start, start+1, ... join it while request j's prompt shares no
- * more than m_j = rx_match_length(prompt_j minus its last token) tokens with
- * every earlier member; *out_end = the first j that would share more (it
+ * more than m_j = rx_match_length(prompt_j minus its last token) tokens,
+ * counted in whole pages, with every earlier member; *out_end = the first j
+ * that would share more (it
  * starts the next batch), or R.  The cache is only read.  tokens/indptr hold
  * the wave's R prompts concatenated.  Errors: RX_ERR_INVALID (start not in
  * [0, R), an empty prompt). */
@@ -334,9 +358,24 @@ rx_status rx_plan_decode_steps(const rx_cache* cache, int32_t B, int32_t n_steps
 
 /* n_steps consecutive rx_alloc(k) calls (one decode slot per request and
  * step), written to out_slots[t*k .. t*k+k).  RX_ERR_NO_SPACE at the first
- * step that cannot be served (earlier steps stay allocated). */
+ * step that cannot be served (earlier steps stay allocated).  Page size 1
+ * only (RX_ERR_INVALID otherwise; use rx_alloc_decode_steps). */
 rx_status rx_alloc_steps(rx_cache* cache, int64_t k, int32_t n_steps,
                          int32_t* out_slots);
+
+/* Decode slots of n_steps steps for B requests at any page size.  Request
+ * b's first decode token is at position pos0[b], right after the slot
+ * last_slot[b] (the slot of position pos0[b]-1).  At step t, in request
+ * order, a token whose position starts a page takes a new page (one
+ * allocation per step of the pages that step needs, handed out in request
+ * order, evicting as rx_alloc does) and gets its first slot; any other token
+ * gets the slot after the request's previous one.  Writes
+ * out_slots[t*B + b].  At page size 1 this equals rx_alloc_steps(B,
+ * n_steps).  RX_ERR_NO_SPACE at the first step that cannot be served
+ * (earlier steps stay allocated). */
+rx_status rx_alloc_decode_steps(rx_cache* cache, int32_t B, int32_t n_steps,
+                                const int32_t* pos0, const int32_t* last_slot,
+                                int32_t* out_slots);
 
 /* ------------------------------------------------------------------------
  * Device calls

@@ -6,10 +6,12 @@
 //    map": TreeNode{key, value, children, parent, lock_ref, last_access_time,
 //    priority}; inc_lock_ref moves a node between the evictable and protected
 //    counts; eviction pops a heap of candidates and pushes a parent once it is
-//    childless and unlocked; a node splits at the divergence point; children
-//    are keyed on the first token at page_size 1; the match inside an edge is
-//    a galloping search (doubling windows, one block compare each, then a
-//    binary search of the window holding the divergence).
+//    childless and unlocked; a node splits at the divergence point; keys are
+//    page-aligned (truncated to whole pages, matches rounded down to a page)
+//    and children are keyed on the first token at page_size 1, on the first
+//    page otherwise; the match inside an edge is a galloping search
+//    (doubling windows, one block compare each, then a binary search of the
+//    window holding the divergence).
 //  - "SGLang" (bibekananda.in), "One tree for everybody" / "Eviction on a
 //    tree": walk as far as the tokens match; the divergent part becomes a new
 //    branch; leaves go first.
@@ -18,9 +20,12 @@
 //
 // Readings where the pages are silent: a logical access clock advanced once
 // per match/insert and written on the whole touched path; heap key
-// (priority = 0, last_access_time, node id); a FIFO free list 1..N-1; a
-// match ending inside an edge splits it; the split's upper half takes a fresh
-// id and the lower half's lock_ref and access time.
+// (priority = 0, last_access_time, node id); the pool cut into pages of
+// page_size consecutive slots with page 0 a pad page, and a FIFO free list of
+// pages 1..N/page_size-1 handing out whole pages (a request's positions
+// [k*page_size, (k+1)*page_size) lie in one page, in slot order); a match
+// ending inside an edge splits it; the split's upper half takes a fresh id and
+// the lower half's lock_ref and access time.
 
 #include <algorithm>
 #include <cstdarg>
@@ -31,6 +36,7 @@
 #include <queue>
 #include <string>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "rx.h"
@@ -54,7 +60,8 @@ struct Node {
   int64_t id = 0;
   std::vector<int32_t> key;
   std::vector<int32_t> value;
-  std::unordered_map<int32_t, Node*> children;
+  std::unordered_map<int32_t, Node*> children;       // page_size 1: first token
+  std::unordered_map<std::string, Node*> pchildren;  // page_size > 1: first page
   Node* parent = nullptr;
   int64_t lock_ref = 0;
   int64_t last_access_time = 0;
@@ -90,9 +97,10 @@ int64_t common_prefix(const int32_t* a, const int32_t* b, int64_t n) {
 
 struct rx_cache {
   int64_t num_slots = 0;
+  int64_t ps = 1;  // page size in slots
   std::unordered_map<int64_t, std::unique_ptr<Node>> nodes;
   Node* root = nullptr;
-  std::deque<int32_t> free_list;
+  std::deque<int32_t> free_list;  // free pages (a page is a slot at page size 1)
   int64_t next_id = 1;
   int64_t clock = 0;
   int64_t evictable = 0;
@@ -100,6 +108,71 @@ struct rx_cache {
   int64_t cached = 0;
   int64_t evicted_tokens = 0;
   std::vector<rx_evict_rec> evict_log;
+
+  // ------------------------------------------------------------- pages
+  int64_t aligned(int64_t n) const { return n - n % ps; }
+  int64_t pages_for(int64_t tokens) const { return (tokens + ps - 1) / ps; }
+  std::string page_key(const int32_t* t) const {
+    return std::string(reinterpret_cast<const char*>(t), size_t(ps) * sizeof(int32_t));
+  }
+  Node* child_of(const Node* n, const int32_t* t) const {
+    if (ps == 1) {
+      auto it = n->children.find(t[0]);
+      return it == n->children.end() ? nullptr : it->second;
+    }
+    auto it = n->pchildren.find(page_key(t));
+    return it == n->pchildren.end() ? nullptr : it->second;
+  }
+  void set_child(Node* n, const int32_t* t, Node* c) {
+    if (ps == 1)
+      n->children[t[0]] = c;
+    else
+      n->pchildren[page_key(t)] = c;
+  }
+  void erase_child(Node* n, const int32_t* t) {
+    if (ps == 1)
+      n->children.erase(t[0]);
+    else
+      n->pchildren.erase(page_key(t));
+  }
+  bool childless(const Node* n) const {
+    return ps == 1 ? n->children.empty() : n->pchildren.empty();
+  }
+  template <class F>
+  void for_children(const Node* n, F f) const {
+    if (ps == 1)
+      for (const auto& kv : n->children) f(kv.second);
+    else
+      for (const auto& kv : n->pchildren) f(kv.second);
+  }
+  // Pages of slots[0..n), each once, in order of first appearance, to the
+  // free-list tail.
+  void free_slot_pages(const int32_t* slots, int64_t n) {
+    if (ps == 1) {
+      for (int64_t i = 0; i < n; ++i) free_list.push_back(slots[i]);
+      return;
+    }
+    std::unordered_set<int32_t> seen;
+    for (int64_t i = 0; i < n; ++i) {
+      const int32_t p = int32_t(slots[i] / ps);
+      if (seen.insert(p).second) free_list.push_back(p);
+    }
+  }
+  // Take n pages from the head of the free list, evicting the shortfall
+  // first; false (nothing taken) if still short.
+  bool alloc_pages(int64_t n, int32_t* out) {
+    if (int64_t(free_list.size()) < n) evict((n - int64_t(free_list.size())) * ps);
+    if (int64_t(free_list.size()) < n) return false;
+    for (int64_t i = 0; i < n; ++i) {
+      out[i] = free_list.front();
+      free_list.pop_front();
+    }
+    return true;
+  }
+  // The first k slots of pages[0..), page after page.
+  void page_slots(const int32_t* pages, int64_t k, int32_t* out) const {
+    for (int64_t i = 0; i < k; ++i) out[i] = int32_t(int64_t(pages[i / ps]) * ps + i % ps);
+  }
 
   Node* new_node(const int32_t* k, const int32_t* v, int64_t n, Node* parent) {
     auto up = std::make_unique<Node>();
@@ -123,23 +196,23 @@ struct rx_cache {
     Node* upper = new_node(node->key.data(), node->value.data(), k, parent);
     upper->lock_ref = node->lock_ref;
     upper->last_access_time = node->last_access_time;
-    parent->children[node->key[0]] = upper;
+    set_child(parent, node->key.data(), upper);
     node->key.erase(node->key.begin(), node->key.begin() + k);
     node->value.erase(node->value.begin(), node->value.begin() + k);
     node->parent = upper;
-    upper->children[node->key[0]] = node;
+    set_child(upper, node->key.data(), node);
     return upper;
   }
 
   int64_t match_length(const int32_t* t, int64_t n) const {
+    n = aligned(n);
     const Node* node = root;
     int64_t pos = 0;
     while (pos < n) {
-      auto it = node->children.find(t[pos]);
-      if (it == node->children.end()) break;
-      const Node* c = it->second;
+      const Node* c = child_of(node, t + pos);
+      if (!c) break;
       int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
-      int64_t k = common_prefix(c->key.data(), t + pos, lim);
+      int64_t k = aligned(common_prefix(c->key.data(), t + pos, lim));
       pos += k;
       if (k < int64_t(c->key.size())) break;
       node = c;
@@ -150,14 +223,14 @@ struct rx_cache {
   // Slots of the longest cached prefix of t[0..n) (no split, no touch);
   // writes them to out and returns the matched length.
   int64_t lookup_slots(const int32_t* t, int64_t n, int32_t* out) const {
+    n = aligned(n);
     const Node* node = root;
     int64_t pos = 0;
     while (pos < n) {
-      auto it = node->children.find(t[pos]);
-      if (it == node->children.end()) break;
-      const Node* c = it->second;
+      const Node* c = child_of(node, t + pos);
+      if (!c) break;
       int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
-      int64_t k = common_prefix(c->key.data(), t + pos, lim);
+      int64_t k = aligned(common_prefix(c->key.data(), t + pos, lim));
       std::memcpy(out + pos, c->value.data(), size_t(k) * sizeof(int32_t));
       pos += k;
       if (k < int64_t(c->key.size())) break;
@@ -170,14 +243,14 @@ struct rx_cache {
   // the matched length; appends matched slots to `slots` if non-null.
   Node* walk(const int32_t* t, int64_t n, int64_t* matched,
              std::vector<Node*>* path, int32_t* slots) {
+    n = aligned(n);
     Node* node = root;
     int64_t pos = 0;
     while (pos < n) {
-      auto it = node->children.find(t[pos]);
-      if (it == node->children.end()) break;
-      Node* c = it->second;
+      Node* c = child_of(node, t + pos);
+      if (!c) break;
       int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
-      int64_t k = common_prefix(c->key.data(), t + pos, lim);
+      int64_t k = aligned(common_prefix(c->key.data(), t + pos, lim));
       if (k < int64_t(c->key.size())) c = split(c, k);
       if (slots) std::memcpy(slots + pos, c->value.data(), size_t(k) * sizeof(int32_t));
       pos += k;
@@ -197,8 +270,11 @@ struct rx_cache {
     return node;
   }
 
+  // Inserts the whole pages of t[0..n) (the key truncated to a multiple of
+  // the page size).
   Node* insert(const int32_t* t, const int32_t* s, int64_t n,
                int64_t* already) {
+    n = aligned(n);
     clock += 1;
     std::vector<Node*> path;
     int64_t pos = 0;
@@ -206,7 +282,7 @@ struct rx_cache {
     *already = pos;
     if (pos < n) {
       Node* leaf = new_node(t + pos, s + pos, n - pos, node);
-      node->children[t[pos]] = leaf;
+      set_child(node, t + pos, leaf);
       evictable += n - pos;
       cached += n - pos;
       path.push_back(leaf);
@@ -255,17 +331,18 @@ struct rx_cache {
     while (!stack.empty()) {
       Node* x = stack.back();
       stack.pop_back();
-      if (x != root && x->children.empty() && x->lock_ref == 0)
+      if (x != root && childless(x) && x->lock_ref == 0)
         heap.push({x->priority, x->last_access_time, x->id, x});
-      for (auto& kv : x->children) stack.push_back(kv.second);
+      for_children(x, [&](Node* c) { stack.push_back(c); });
     }
     int64_t freed = 0;
     while (freed < k && !heap.empty()) {
       Node* v = heap.top().node;
       heap.pop();
       Node* parent = v->parent;
-      parent->children.erase(v->key[0]);
-      for (int32_t s : v->value) free_list.push_back(s);
+      erase_child(parent, v->key.data());
+      for (size_t i = 0; i < v->value.size(); i += size_t(ps))
+        free_list.push_back(int32_t(v->value[i] / ps));
       int64_t len = int64_t(v->key.size());
       freed += len;
       evictable -= len;
@@ -273,20 +350,20 @@ struct rx_cache {
       evicted_tokens += len;
       evict_log.push_back({v->id, len});
       nodes.erase(v->id);
-      if (parent != root && parent->children.empty() && parent->lock_ref == 0)
+      if (parent != root && childless(parent) && parent->lock_ref == 0)
         heap.push({parent->priority, parent->last_access_time, parent->id,
                    parent});
     }
     return freed;
   }
 
+  // k slots: the first k slots of ceil(k / page size) pages (all of them at
+  // page size 1).
   bool alloc(int64_t k, int32_t* out) {
-    if (int64_t(free_list.size()) < k) evict(k - int64_t(free_list.size()));
-    if (int64_t(free_list.size()) < k) return false;
-    for (int64_t i = 0; i < k; ++i) {
-      out[i] = free_list.front();
-      free_list.pop_front();
-    }
+    if (ps == 1) return alloc_pages(k, out);
+    std::vector<int32_t> pages(size_t(pages_for(k)));
+    if (!alloc_pages(int64_t(pages.size()), pages.data())) return false;
+    page_slots(pages.data(), k, out);
     return true;
   }
 
@@ -298,13 +375,17 @@ struct rx_cache {
 };
 
 // ---------------------------------------------------------------- C ABI
-// Whether two token sequences share more than `m` leading tokens: position m
-// is compared first (where prompts that match the tree to depth m usually
-// part), the m tokens before it only when that one agrees.
+// Whether two token sequences share more than `m` leading tokens counted in
+// whole pages of `ps` tokens (m itself a multiple of ps), i.e. their first
+// m + ps tokens agree: the page after position m is compared first (where
+// prompts that match the tree to depth m usually part), the m tokens before
+// it only when that one agrees.
 static bool shares_more_than(const int32_t* a, int64_t na, const int32_t* b, int64_t nb,
-                             int64_t m) {
+                             int64_t m, int64_t ps = 1) {
   if (m < 0) return true;
-  if (na <= m || nb <= m || a[m] != b[m]) return false;
+  const int64_t need = m + ps;
+  if (na < need || nb < need || a[m] != b[m]) return false;
+  if (std::memcmp(a + m, b + m, size_t(ps) * sizeof(int32_t)) != 0) return false;
   return common_prefix(a, b, m) == m;
 }
 
@@ -324,15 +405,20 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache** out) {
   if (cfg->num_slots < 1 || cfg->num_slots > (int64_t(1) << 31))
     return fail(RX_ERR_INVALID, "rx_cache_create: num_slots %lld out of range",
                 (long long)cfg->num_slots);
-  if (cfg->page_size != 1)
-    return fail(RX_ERR_INVALID, "rx_cache_create: page_size must be 1");
+  if (cfg->page_size < 1 || cfg->num_slots < cfg->page_size ||
+      cfg->num_slots % cfg->page_size != 0)
+    return fail(RX_ERR_INVALID,
+                "rx_cache_create: page_size %d must be >= 1 and divide num_slots %lld",
+                cfg->page_size, (long long)cfg->num_slots);
   auto* c = new rx_cache();
   c->num_slots = cfg->num_slots;
+  c->ps = cfg->page_size;
   auto root = std::make_unique<Node>();
   root->id = 0;
   c->root = root.get();
   c->nodes.emplace(0, std::move(root));
-  for (int64_t s = 1; s < cfg->num_slots; ++s) c->free_list.push_back(int32_t(s));
+  for (int64_t p = 1; p < cfg->num_slots / cfg->page_size; ++p)
+    c->free_list.push_back(int32_t(p));
   *out = c;
   return RX_OK;
 }
@@ -380,7 +466,7 @@ rx_status rx_alloc(rx_cache* c, int64_t k, int32_t* out_slots) {
   if (!c || k < 0 || (!out_slots && k)) return fail(RX_ERR_INVALID, "rx_alloc: bad argument");
   if (!c->alloc(k, out_slots))
     return fail(RX_ERR_NO_SPACE, "rx_alloc: %lld slots requested, %lld free after eviction",
-                (long long)k, (long long)c->free_list.size());
+                (long long)k, (long long)(int64_t(c->free_list.size()) * c->ps));
   return RX_OK;
 }
 
@@ -394,10 +480,10 @@ rx_status rx_evict(rx_cache* c, int64_t k, int64_t* out_freed) {
 rx_status rx_free(rx_cache* c, const int32_t* slots, int64_t k) {
   if (!c || k < 0 || (!slots && k)) return fail(RX_ERR_INVALID, "rx_free: bad argument");
   for (int64_t i = 0; i < k; ++i) {
-    if (slots[i] < 1 || slots[i] >= c->num_slots)
+    if (slots[i] < c->ps || slots[i] >= c->num_slots)
       return fail(RX_ERR_INVALID, "rx_free: slot %d out of range", slots[i]);
   }
-  for (int64_t i = 0; i < k; ++i) c->free_list.push_back(slots[i]);
+  c->free_slot_pages(slots, k);
   return RX_OK;
 }
 
@@ -415,7 +501,7 @@ rx_status rx_stats(const rx_cache* c, rx_stats_t* out) {
   out->cached_tokens = c->cached;
   out->evictable_tokens = c->evictable;
   out->protected_tokens = c->protected_;
-  out->free_slots = int64_t(c->free_list.size());
+  out->free_slots = int64_t(c->free_list.size()) * c->ps;
   out->num_nodes = int64_t(c->nodes.size()) - 1;
   out->evicted_nodes = int64_t(c->evict_log.size());
   out->evicted_tokens = c->evicted_tokens;
@@ -456,7 +542,7 @@ rx_status rx_extend_begin(rx_cache* c, int32_t R, const int32_t* tokens,
       return fail(RX_ERR_INVALID, "rx_extend_begin: prompt %d has length %lld (row %lld)", r,
                   (long long)n, (long long)row_stride);
   }
-  int64_t total_new = 0;
+  int64_t total_new = 0, total_pages = 0;
   for (int32_t r = 0; r < R; ++r) {
     const int32_t* t = tokens + tok_indptr[r];
     int64_t n = tok_indptr[r + 1] - tok_indptr[r];
@@ -466,16 +552,29 @@ rx_status rx_extend_begin(rx_cache* c, int32_t R, const int32_t* tokens,
     out_prefix_len[r] = int32_t(m);
     out_match_node[r] = x->id;
     total_new += n - m;
+    total_pages += c->pages_for(n - m);
   }
-  if (!c->alloc(total_new, out_new_slots)) {
+  // one allocation of every member's pages, handed out in member order; a
+  // member's new tokens fill its own pages in order
+  std::vector<int32_t> pages;
+  int32_t* page_out = out_new_slots;
+  if (c->ps > 1) {
+    pages.resize(size_t(total_pages));
+    page_out = pages.data();
+  }
+  if (!c->alloc_pages(total_pages, page_out)) {
     for (int32_t r = 0; r < R; ++r) c->unlock(c->find(out_match_node[r]));
     return fail(RX_ERR_NO_SPACE, "rx_extend_begin: %lld new slots needed, %lld free after eviction",
-                (long long)total_new, (long long)c->free_list.size());
+                (long long)total_new, (long long)(int64_t(c->free_list.size()) * c->ps));
   }
-  int64_t pos = 0;
+  int64_t pos = 0, pg = 0;
   for (int32_t r = 0; r < R; ++r) {
     int64_t n = tok_indptr[r + 1] - tok_indptr[r];
     int64_t m = out_prefix_len[r];
+    if (c->ps > 1) {
+      c->page_slots(pages.data() + pg, n - m, out_new_slots + pos);
+      pg += c->pages_for(n - m);
+    }
     std::memcpy(req_to_token + r * row_stride + m, out_new_slots + pos,
                 size_t(n - m) * sizeof(int32_t));
     pos += n - m;
@@ -509,10 +608,8 @@ rx_status rx_extend_end(rx_cache* c, int32_t R, const int32_t* tokens,
       // (same tokens, same predecessors, same K/V) and free this request's.
       tree.resize(size_t(n));
       c->lookup_slots(t, already, tree.data());
-      for (int64_t i = prefix_len[r]; i < already; ++i) {
-        c->free_list.push_back(row[i]);
-        row[i] = tree[size_t(i)];
-      }
+      c->free_slot_pages(row + prefix_len[r], already - prefix_len[r]);
+      for (int64_t i = prefix_len[r]; i < already; ++i) row[i] = tree[size_t(i)];
       ++rewritten;
     }
     c->lock(x);
@@ -542,7 +639,11 @@ rx_status rx_finish(rx_cache* c, int32_t R, const int32_t* tokens,
     const int32_t* row = req_to_token + r * row_stride;
     int64_t already = 0;
     c->insert(t, row, n, &already);
-    for (int64_t i = prompt_len[r]; i < already; ++i) c->free_list.push_back(row[i]);
+    // the request's own pages another request had already inserted, and the
+    // partly filled page past the last whole one
+    const int64_t p_al = c->aligned(prompt_len[r]);
+    if (already > p_al) c->free_slot_pages(row + p_al, already - p_al);
+    if (c->aligned(n) < n) c->free_slot_pages(row + c->aligned(n), 1);
     if (out_already) out_already[r] = already;
     if (!c->unlock(c->find(prompt_node[r])))
       return fail(RX_ERR_STATE, "rx_finish: request %d was not locked", r);
@@ -576,7 +677,7 @@ rx_status rx_batch_end(const rx_cache* c, const int32_t* tokens, const int64_t* 
     if (nj < 1) return fail(RX_ERR_INVALID, "rx_batch_end: empty prompt %d", j);
     const int64_t m = c->match_length(pj, nj - 1);
     for (int32_t r = start; r < j; ++r)
-      if (shares_more_than(pj, nj, tokens + indptr[r], indptr[r + 1] - indptr[r], m)) {
+      if (shares_more_than(pj, nj, tokens + indptr[r], indptr[r + 1] - indptr[r], m, c->ps)) {
         *out_end = j;
         return RX_OK;
       }
@@ -835,10 +936,36 @@ extern "C" rx_status rx_plan_decode_steps(const rx_cache* c, int32_t B, int32_t 
 extern "C" rx_status rx_alloc_steps(rx_cache* c, int64_t k, int32_t n_steps, int32_t* out_slots) {
   if (!c || k < 0 || n_steps < 0 || (!out_slots && k > 0 && n_steps > 0))
     return fail(RX_ERR_INVALID, "rx_alloc_steps: bad argument");
+  if (c->ps != 1)
+    return fail(RX_ERR_INVALID, "rx_alloc_steps: page_size %lld > 1; use rx_alloc_decode_steps",
+                (long long)c->ps);
   for (int32_t t = 0; t < n_steps; ++t) {
     if (!c->alloc(k, out_slots + int64_t(t) * k))
       return fail(RX_ERR_NO_SPACE, "rx_alloc_steps: step %d: %lld slots requested, %lld free after eviction",
                   t, (long long)k, (long long)c->free_list.size());
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_alloc_decode_steps(rx_cache* c, int32_t B, int32_t n_steps,
+                                          const int32_t* pos0, const int32_t* last_slot,
+                                          int32_t* out_slots) {
+  if (!c || B < 0 || n_steps < 0 || (B && n_steps && (!pos0 || !last_slot || !out_slots)))
+    return fail(RX_ERR_INVALID, "rx_alloc_decode_steps: bad argument");
+  std::vector<int32_t> pages(static_cast<size_t>(B));
+  for (int32_t t = 0; t < n_steps; ++t) {
+    int32_t* out = out_slots + int64_t(t) * B;
+    const int32_t* prev = t ? out - B : last_slot;
+    int64_t need = 0;
+    for (int32_t b = 0; b < B; ++b) need += (int64_t(pos0[b]) + t) % c->ps == 0;
+    if (!c->alloc_pages(need, pages.data()))
+      return fail(RX_ERR_NO_SPACE,
+                  "rx_alloc_decode_steps: step %d: %lld pages requested, %lld free after eviction",
+                  t, (long long)need, (long long)c->free_list.size());
+    int64_t k = 0;
+    for (int32_t b = 0; b < B; ++b)
+      out[b] = (int64_t(pos0[b]) + t) % c->ps == 0 ? int32_t(int64_t(pages[size_t(k++)]) * c->ps)
+                                                   : prev[b] + 1;
   }
   return RX_OK;
 }

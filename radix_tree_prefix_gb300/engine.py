@@ -532,7 +532,7 @@ class Engine:
 
     # ------------------------------------------------------------------ run
     def run(self):
-        self.cache = rx.RadixCache(self.wl.num_slots)
+        self.cache = rx.RadixCache(self.wl.num_slots, self.wl.page_size)
         self.trace = Trace()
         self.batch_no = 0
         self.step_no = 0
@@ -669,7 +669,11 @@ class Engine:
         wl = self.wl
         B, T = len(wave), wl.decode_steps
         rows = np.arange(B, dtype=np.int32)
-        all_slots = self.cache.alloc_steps(B, T)                    # [T, B]
+        if wl.page_size == 1:
+            all_slots = self.cache.alloc_steps(B, T)                # [T, B]
+        else:   # a token that starts a page takes a new one, others follow
+            all_slots = self.cache.alloc_decode_steps(
+                ctx0, self.h_table[np.arange(B), ctx0 - 1], T)
         all_pos = ctx0[None, :] + np.arange(T, dtype=np.int32)[:, None]
         self.h_table[rows[None, :], all_pos] = all_slots
         rids = np.array([r.rid for r in wave])

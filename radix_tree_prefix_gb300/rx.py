@@ -107,6 +107,7 @@ _SIGS = {
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
     "rx_plan_decode_steps": [P, I32, I32, P, P, P, I32, I32, I32, P, I64, P],
     "rx_alloc_steps": [P, I64, I32, P],
+    "rx_alloc_decode_steps": [P, I32, I32, P, P, P],
     "rx_kv_store": [P, I32, P, P, P, I64, P],
     "rx_req_to_token_write": [P, I64, I64, P, P, P, I64, P],
     "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
@@ -166,14 +167,15 @@ def build_info():
 
 # -------------------------------------------------------------- host cache
 class RadixCache:
-    """Owner of one native rx_cache."""
+    """Owner of one native rx_cache (pages of `page_size` slots)."""
 
-    def __init__(self, num_slots):
-        cfg = rx_config(int(num_slots), 1, 0)
+    def __init__(self, num_slots, page_size=1):
+        cfg = rx_config(int(num_slots), int(page_size), 0)
         h = C.c_void_p()
         _check(_lib.rx_cache_create(C.byref(cfg), C.byref(h)))
         self._h = h
         self.num_slots = int(num_slots)
+        self.page_size = int(page_size)
         self._i32 = C.c_int32()
         self._i64 = C.c_int64()
 
@@ -257,6 +259,15 @@ class RadixCache:
         out = np.empty((max(1, n_steps), max(1, k)), dtype=np.int32)
         _check(_lib.rx_alloc_steps(self._h, int(k), int(n_steps), _p(out)))
         return out[:n_steps, :k]
+
+    def alloc_decode_steps(self, pos0, last_slot, n_steps):
+        """Decode slots of n_steps steps for requests whose first decode
+        token is at position pos0[b] after slot last_slot[b]; int32 [n_steps, B]."""
+        p0, ls = _i32(pos0), _i32(last_slot)
+        B = len(p0)
+        out = np.empty((max(1, n_steps), max(1, B)), dtype=np.int32)
+        _check(_lib.rx_alloc_decode_steps(self._h, B, int(n_steps), _p(p0), _p(ls), _p(out)))
+        return out[:n_steps, :B]
 
     def evict(self, k):
         f = C.c_int64()

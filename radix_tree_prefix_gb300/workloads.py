@@ -65,6 +65,7 @@ class Workload:
     seg_tokens: list = field(default_factory=list)
     waves: list = field(default_factory=list)
     seed: int = BASE_SEED
+    page_size: int = 1
 
     def __post_init__(self):
         self._finalise()
@@ -121,6 +122,7 @@ class Workload:
             "decode_steps": self.decode_steps,
             "pool_slots": self.num_slots,
             "distinct_tokens": self.n_store,
+            "page_size": self.page_size,
         }
 
 
@@ -249,6 +251,18 @@ def long_shared(seed=BASE_SEED, batch=64, prefix=32768, unique=1024,
     distinct = prefix + batch * (unique + decode_steps)
     return Workload("long_shared", 1, q_heads, kv_heads, head_dim, distinct + 1,
                     decode_steps, s.tokens, [wave], seed)
+
+
+def with_pages(wl, page_size):
+    """The same workload over a pool cut into pages of `page_size` slots:
+    every request may leave part of a page unused (its last prompt page and
+    its last decode page), so the pool grows by two pages per request of the
+    largest wave and rounds up to whole pages."""
+    extra = 2 * max(len(w) for w in wl.waves) * page_size
+    wl.num_slots = -(-(wl.num_slots + extra) // page_size) * page_size
+    wl.page_size = page_size
+    wl.name = f"{wl.name}_p{page_size}"
+    return wl
 
 
 WORKLOADS = {

@@ -39,7 +39,8 @@ class DeviceRun:
         self.flags = rx.device_check()
         self.engine = eng
         if check_bookkeeping:
-            want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+            want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                                   page_size=wl.page_size)
             assert self.trace.as_tuple() == want.as_tuple(), "bookkeeping differs from oracle"
 
     def _pick_tokens(self, s):

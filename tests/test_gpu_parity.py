@@ -99,6 +99,15 @@ SMALL = {
     # many members on one shared segment: several member blocks of a chunk
     "long_shared_small": (lambda: workloads.long_shared(batch=20, prefix=700, unique=50,
                                                         decode_steps=3), None),
+    # paged pools: whole-page keys and allocation, partly filled last pages,
+    # decode tokens continuing a request's page
+    "agent_p16": (lambda: workloads.with_pages(
+        workloads.agent_loop(calls=6, preamble=300, lo=20, hi=60, decode_steps=21), 16), None),
+    "fork_evict_p4": (lambda: workloads.with_pages(
+        workloads.fork_tree(branching=3, depth=3, level_tokens=48, decode_steps=4), 4), None),
+    "chat_d256_p16": (lambda: workloads.with_pages(
+        workloads.multi_turn_chat(sessions=4, turns=3, system=100, user=40, decode_steps=4,
+                                  layers=2), 16), None),
 }
 
 
@@ -109,7 +118,7 @@ def test_small_workload_parity(name):
     mx, mean, n = run.assert_close()
     if name == "nested_share":
         assert run.trace.prefilled == 3060
-    if name == "fork_evict":
+    if name.startswith("fork_evict"):
         assert len(run.trace.eviction_log) > 0
 
 

@@ -54,9 +54,10 @@ def test_argument_errors_need_no_gpu():
     st = rx._lib.rx_extend_attention(C.byref(bad), 3, None, 4, None, 0, None, None, None,
                                      None, 1, 1, 1.0, None, None, None)
     assert st == rx.RX_ERR_INVALID and "layer" in rx.last_error()
-    cfg = rx.rx_config(8, 2, 0)
     h = C.c_void_p()
-    assert rx._lib.rx_cache_create(C.byref(cfg), C.byref(h)) == rx.RX_ERR_INVALID
+    for slots, ps in ((9, 2), (8, 0), (3, 4)):    # page size must divide the slot count
+        cfg = rx.rx_config(slots, ps, 0)
+        assert rx._lib.rx_cache_create(C.byref(cfg), C.byref(h)) == rx.RX_ERR_INVALID
 
 
 def test_worked_eviction_example_native():
@@ -165,7 +166,8 @@ SCALED = {
 def test_request_flow_matches_oracle(name):
     wl = SCALED[name]()
     got = Engine(wl).run()
-    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                                   page_size=wl.page_size)
     assert got.prefilled == want.prefilled
     assert got.as_tuple() == want.as_tuple()
     assert got.stats == want.stats
@@ -179,7 +181,8 @@ def test_fork_tree_full_size_bookkeeping():
     """Workload 4 at full size: eviction order and slot tables bit-exact."""
     wl = workloads.fork_tree()
     got = Engine(wl).run()
-    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps)
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                                   page_size=wl.page_size)
     assert got.as_tuple() == want.as_tuple()
     assert len(got.eviction_log) > 100
 
@@ -234,7 +237,7 @@ def test_identical_prompts_share_slots():
               workloads.Request(2, (0, 1, 3)), workloads.Request(3, (0, 2, 4))]]
     wl = workloads.Workload("dup", 1, 8, 2, 128, 5000, 0, seg, waves)
     got = Engine(wl).run()
-    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, 0)
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, 0, page_size=wl.page_size)
     assert got.as_tuple() == want.as_tuple()
     assert [[r for r, _, _ in b] for b in got.batches] == [[0], [1], [2, 3]]
     assert got.stats == want.stats
@@ -399,3 +402,105 @@ def test_pointer_forms_match_array_forms():
         start = end
     assert np.array_equal(npn, na)
     assert ca.stats() == cp.stats()
+
+
+# ------------------------------------------------------------------- pages
+@pytest.mark.parametrize("page_size", [1, 4, 16])
+def test_random_ops_match_oracle_with_pages(page_size):
+    """The random operation sequence of the token-level test, on caches cut
+    into pages: identical slots, nodes, eviction order and counts."""
+    rng = random.Random(31 + page_size)
+    for trial in range(40):
+        n_slots = rng.randint(6, 20) * page_size
+        o, n = ORadix(n_slots, page_size), rx.RadixCache(n_slots, page_size)
+        onodes, nnodes = [], []
+        for step in range(100):
+            r = rng.random()
+            seq = [rng.randrange(rng.choice([2, 3])) for _ in range(rng.randint(1, 5 * page_size))]
+            if r < 0.2:
+                assert o.match_length(seq) == n.match_length(seq)
+                os_, on = o.match_prefix(seq)
+                ns_, nn = n.match_prefix(seq)
+                assert list(os_) == ns_.tolist() and on.id == nn
+            elif r < 0.55:
+                os_, on = o.match_prefix(seq[:-1])
+                ns_, nn = n.match_prefix(seq[:-1])
+                assert on.id == nn
+                k = len(seq) - len(os_)
+                try:
+                    onew = o.alloc(k)
+                except ONoSpace:
+                    onew = None
+                try:
+                    nnew = n.alloc(k).tolist()
+                except rx.NoSpace:
+                    nnew = None
+                assert onew == nnew
+                if onew is None:
+                    continue
+                oa, on2 = o.insert(seq, list(os_) + onew)
+                na, nn2 = n.insert(seq, ns_.tolist() + nnew)
+                assert (oa, on2.id) == (na, nn2)
+                orow = list(os_) + onew
+                o.free(orow[len(os_):oa] + orow[o.aligned(len(seq)):])
+                n.free(np.array(orow[len(os_):oa] + orow[o.aligned(len(seq)):], dtype=np.int32))
+                o.inc_lock_ref(on2)
+                n.lock(nn2)
+                onodes.append(on2)
+                nnodes.append(nn2)
+            elif r < 0.8 and onodes:
+                i = rng.randrange(len(onodes))
+                o.dec_lock_ref(onodes.pop(i))
+                n.unlock(nnodes.pop(i))
+            else:
+                k = rng.randint(1, 3 * page_size)
+                assert o.evict(k) == n.evict(k)
+            st = n.stats()
+            assert st["cached_tokens"] == o.cached_size()
+            assert st["evictable_tokens"] == o.evictable_size_
+            assert st["protected_tokens"] == o.protected_size_
+            assert st["free_slots"] == len(o.free_slots)
+            assert st["num_nodes"] == o.num_nodes()
+            assert n.eviction_log() == o.eviction_log
+
+
+PAGED = {
+    "nested_share": lambda: workloads.nested_share(),
+    "agent_small": lambda: workloads.agent_loop(calls=9, preamble=130, lo=3, hi=50,
+                                                decode_steps=21),
+    "fork_tree_small": lambda: workloads.fork_tree(branching=4, depth=3, level_tokens=40,
+                                                   decode_steps=5),
+    "multi_turn_small": lambda: workloads.multi_turn_chat(sessions=12, turns=4, system=300,
+                                                         user=30, decode_steps=6, layers=1),
+    "long_shared_small": lambda: workloads.long_shared(batch=8, prefix=2048, unique=128,
+                                                       decode_steps=8),
+}
+
+
+@pytest.mark.parametrize("page_size", [4, 16])
+@pytest.mark.parametrize("name", sorted(PAGED))
+def test_request_flow_with_pages_matches_oracle(name, page_size):
+    """The whole request flow on a paged pool: slot tables, prefixes,
+    decode slots, finishes and eviction order equal the oracle's."""
+    wl = workloads.with_pages(PAGED[name](), page_size)
+    got = Engine(wl).run()
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                              page_size=page_size)
+    assert got.as_tuple() == want.as_tuple()
+    assert got.stats == want.stats
+    if name.startswith("fork_tree"):
+        assert len(got.eviction_log) > 0
+
+
+def test_alloc_decode_steps_follows_pages():
+    """A decode token that starts a page takes a new page (one allocation per
+    step, in request order), any other the next slot of the request's page."""
+    c = rx.RadixCache(64, 4)
+    first = c.alloc(7)                    # pages 1, 2: slots 4 .. 10
+    assert first.tolist() == [4, 5, 6, 7, 8, 9, 10]
+    out = c.alloc_decode_steps([7, 8], [10, 99], 3)
+    # step 0: request 1 (position 8) starts a page -> page 3 (slots 12..15);
+    # request 0 (position 7) takes slot 11.  Step 1: request 0 (position 8)
+    # starts a page -> page 4 (16..19); request 1 takes 13.  Step 2: 17, 14.
+    assert out[:, 0].tolist() == [11, 16, 17]
+    assert out[:, 1].tolist() == [12, 13, 14]
