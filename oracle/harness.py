@@ -14,10 +14,13 @@ batch than with the tree waits, so that its sibling populates the tree first.
 Readings of the pages where they leave a step open:
 
 * a wave of requests is processed as: extend batches -> ``decode_steps`` decode
-  steps over the whole wave -> finish of every request in order;
-* requests are taken in order; request ``j`` joins the open batch unless its
-  common prefix with some member exceeds its (side-effect free) tree match, in
-  which case the open batch runs first;
+  steps over the whole wave -> finish of every request, decode and finish in
+  the order the requests were served;
+* before every extend batch the requests still waiting are ordered by the
+  scheduling policy (``oracle/scheduler.py``; first come, first served keeps
+  arrival order); taking them in that order, request ``j`` joins the batch
+  unless its common prefix with some member exceeds its (side-effect free)
+  tree match, and the batch then runs;
 * a batch runs as: for each member in order ``match_prefix`` on its prompt
   minus the last token (the last prompt token is always recomputed, so every
   request has at least one query) and ``inc_lock_ref``; then one allocation of
@@ -54,6 +57,7 @@ Parity: pinned by ``tests/test_oracle_pins.py`` (12,960 / 6,660 / 3,060 prefill
 counts of the nested example; 2,800 of 3,000 reused at agent step 5).
 """
 
+from . import scheduler
 from .radix_cache import RadixCache, common_prefix_length
 
 
@@ -78,26 +82,39 @@ class Trace:
         )
 
 
-def plan_batches(cache, wave_prompts):
-    """Yield lists of positions into ``wave_prompts`` forming extend batches.
-
-    Lazily: a batch is yielded when it closes, so that the caller runs and
-    inserts it before the next request's tree match is taken.
-    """
+def next_batch(cache, wave_prompts, ordered):
+    """The extend batch at the head of ``ordered`` (positions into
+    ``wave_prompts``): requests join in order until one shares more (in whole
+    pages) with a member than its own tree match."""
     batch = []
-    for j, prompt in enumerate(wave_prompts):
+    for j in ordered:
+        prompt = wave_prompts[j]
         m = cache.match_length(prompt[:len(prompt) - 1])
         if batch and any(cache.aligned(common_prefix_length(prompt, wave_prompts[i])) > m
                          for i in batch):
-            yield batch
-            batch = []
+            break
         batch.append(j)
-    if batch:
+    return batch
+
+
+def plan_batches(cache, wave_prompts, policy="fcfs"):
+    """Yield lists of positions into ``wave_prompts`` forming extend batches.
+
+    Lazily: a batch is yielded when it is formed, and the caller runs and
+    inserts it before the waiting requests are ordered again and the next
+    batch is formed.
+    """
+    pending = list(range(len(wave_prompts)))
+    while pending:
+        pos = scheduler.order(cache, [wave_prompts[j] for j in pending], policy)
+        batch = next_batch(cache, wave_prompts, [pending[k] for k in pos])
         yield batch
+        taken = set(batch)
+        pending = [j for j in pending if j not in taken]
 
 
 def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
-                    on_decode=None, page_size=1):
+                    on_decode=None, page_size=1, policy="fcfs"):
     """Run the request flow over a fresh oracle cache.
 
     waves: list of waves; a wave is a list of ``(rid, prompt, outputs)`` with
@@ -113,8 +130,9 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
         prompts = [list(p) for _, p, _ in wave]
         rows = {}
         prompt_nodes = {}
-        batches = plan_batches(cache, prompts)
-        for batch in batches:
+        served = []
+        for batch in plan_batches(cache, prompts, policy):
+            served += batch
             matched = []
             for j in batch:
                 rid, prompt, _ = wave[j]
@@ -145,6 +163,7 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
                 cache.inc_lock_ref(node2)
                 cache.dec_lock_ref(node)
                 prompt_nodes[rid] = node2
+        wave = [wave[j] for j in served]
         for step in range(decode_steps):
             need = [len(rows[rid]) % ps == 0 for rid, _, _ in wave]
             pages = cache.alloc_pages(sum(need))

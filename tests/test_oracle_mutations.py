@@ -12,7 +12,9 @@ condition, allocator order, access times, lock paths, eviction candidates,
 page alignment of keys, matches and child keys),
 the request flow (in-batch rule, what is matched, adoption of identical
 prompts, what finish inserts and frees, decode tokens kept out of the tree,
-lock release) and attention (scale, GQA head, causal boundary, log-sum-exp).
+lock release), the scheduler (LPM direction, the in-batch thresholds, the
+queue-length switch, the depth-first weights and order) and attention (scale,
+GQA head, causal boundary, log-sum-exp).
 
 Not planted: a split that does not copy the lower node's access time to the
 upper one.  Splits happen only inside a match or an insert, and both write
@@ -126,6 +128,25 @@ MUTANTS = {
          "                    rows[rid][m:already] = tree\n", "")]),
     "no_in_batch_rule": ("harness.py", [
         ("        if batch and any(", "        if False and any(")]),
+    "lpm_shortest_prefix_first": ("scheduler.py", [
+        ("keys.append((float(\"inf\") if deprioritised else -m, i))",
+         "keys.append((float(\"inf\") if deprioritised else m, i))")]),
+    "in_batch_deprioritise_strictly_above": ("scheduler.py", [
+        (">= IN_BATCH_DEPRIORITIZE_THRESHOLD:", "> IN_BATCH_DEPRIORITIZE_THRESHOLD:")]),
+    "in_batch_check_strictly_below": ("scheduler.py", [
+        ("if m <= IN_BATCH_CHECK_THRESHOLD:", "if m < IN_BATCH_CHECK_THRESHOLD:")]),
+    "in_batch_queue_never_filled": ("scheduler.py", [
+        ("                queued.append(list(p))\n", "                pass\n")]),
+    "lpm_limit_inclusive": ("scheduler.py", [
+        ("if n > LPM_QUEUE_LIMIT:", "if n >= LPM_QUEUE_LIMIT:")]),
+    "dfs_lighter_children_first": ("scheduler.py", [
+        ("kids.sort(key=lambda c: (-weight[c.id], first[c.id]))",
+         "kids.sort(key=lambda c: (weight[c.id], first[c.id]))")]),
+    "dfs_own_requests_last": ("scheduler.py", [
+        ("        out.extend(at.get(node.id, []))\n        kids = [",
+         "        kids = [")]),
+    "dfs_weight_without_subtree": ("scheduler.py", [
+        ("            w += cw\n", "")]),
     "match_whole_prompt": ("harness.py", [
         ("slots, node = cache.match_prefix(prompts[j][:len(prompts[j]) - 1])",
          "slots, node = cache.match_prefix(prompts[j])")]),

@@ -13,6 +13,7 @@ import pytest
 
 from conftest import read_golden
 from oracle import attention as oatt
+from oracle import scheduler as oscheduler
 from oracle.harness import run_bookkeeping
 from oracle.radix_cache import NoSpace, RadixCache, StateError
 from radix_tree_prefix_gb300 import workloads
@@ -773,4 +774,126 @@ def test_agent_steps_through_decode_reuse_with_pages(actions):
     trace, cache = run_bookkeeping(waves, 16000, actions, page_size=8)
     rid, m, row = trace.batches[g["step"] - 1][0]
     assert len(row) == g["prompt_tokens"] and m == g["reused"] + actions
+    _assert_slots_conserved(cache)
+
+
+# -------------------------------------------------------------- scheduling
+def _lpm_toy(policy):
+    """The cache-aware scheduling toy served one request at a time through
+    the oracle's scheduler and radix cache (the last token of each request is
+    its own, so matching the prompt minus its last token matches what the toy
+    matches)."""
+    g = {}
+    for ln in read_golden("lpm_toy.txt"):
+        k, *v = ln.split()
+        g[k] = v
+    n = int(g["prompt_tokens"][0])
+    X = [f"x{i}" for i in range(n)]
+    Y = [f"y{i}" for i in range(n)]
+    queue = [("X1", X + ["a"]), ("Y1", Y + ["b"]), ("X2", X + ["c"]),
+             ("Y2", Y + ["d"]), ("X3", X + ["e"]), ("Y3", Y + ["f"])]
+    vocab = {}
+    pending = [(name, [vocab.setdefault(w, len(vocab)) for w in words]) for name, words in queue]
+    cache = RadixCache(int(g["capacity"][0]) + 1)
+    log, prefilled = [], 0
+    while pending:
+        k = oscheduler.order(cache, [t for _, t in pending], policy)[0]
+        name, toks = pending.pop(k)
+        slots, node = cache.match_prefix(toks[:-1])
+        cache.inc_lock_ref(node)
+        new = cache.alloc(len(toks) - len(slots))
+        cache.insert(toks, slots + new)
+        cache.dec_lock_ref(node)
+        prefilled += len(toks) - len(slots)
+        log.append(f"{name}:{len(slots)}")
+    return log, prefilled, g
+
+
+@pytest.mark.parametrize("policy", ["fcfs", "lpm"])
+def test_lpm_toy_served_order_and_prefill(policy):
+    """126 of 126 tokens prefilled in arrival order, 46 of 126 with the
+    longest prefix first, in the printed served order."""
+    log, prefilled, g = _lpm_toy(policy)
+    assert log == g[policy]
+    assert [prefilled, 126] == [int(x) for x in g[policy + "_prefilled"]]
+
+
+def test_lpm_queue_limit_falls_back_to_fcfs():
+    """More than 128 waiting requests: arrival order; 128: LPM."""
+    cache = RadixCache(5000)
+    base = list(range(1, 41))
+    cache.insert(base, cache.alloc(40))
+    prompts = [[1000 + i, 7] if i % 2 else base[:30] + [2000 + i, 7] for i in range(129)]
+    assert oscheduler.order(cache, prompts, "lpm") == list(range(129))
+    got = oscheduler.order(cache, prompts[:128], "lpm")
+    assert got[:64] == list(range(0, 128, 2))     # 30 tokens matched, first
+
+
+def test_in_batch_prefix_deprioritises_siblings():
+    """A request with a thin tree match (<= 32) that shares >= 32 tokens with
+    an earlier queued request goes to the back; 31 shared tokens do not
+    count; a request matching more than 32 tokens of the tree is not checked
+    against the queue."""
+    cache = RadixCache(5000)
+    S = list(range(100, 140))                     # 40 tokens, not in the tree
+    T31 = S[:31] + [900, 901, 902]                # shares 31 with S
+    cache.insert(list(range(500, 540)), cache.alloc(40))
+    R = list(range(500, 533)) + [7, 8]            # 33 tokens in the tree
+    prompts = [S + [1], S + [2], T31 + [3], S + [4], R, list(range(600, 640)) + [5]]
+    # keys: S+[1]: 0 (queued); S+[2]: back; T31: 0 (queued); S+[4]: back;
+    # R: -33; the last: 0 (queued)
+    assert oscheduler.order(cache, prompts, "lpm") == [4, 0, 2, 5, 1, 3]
+    # exactly 32 shared tokens deprioritise, 31 do not
+    Z = list(range(700, 710))
+    T32 = S[:32] + [903, 904]
+    assert oscheduler.order(cache, [S + [1], T32 + [5], Z], "lpm") == [0, 2, 1]
+    assert oscheduler.order(cache, [T32 + [5], S + [1], Z], "lpm") == [0, 2, 1]
+    assert oscheduler.order(cache, [S + [1], S[:31] + [5], Z], "lpm") == [0, 1, 2]
+    # a tree match of exactly 32 tokens is still checked against the queue,
+    # one of 33 is not
+    W = list(range(300, 360))
+    cache.insert(W[:32] + [999], cache.alloc(33))
+    assert oscheduler.order(cache, [W + [1], W + [2], Z], "lpm") == [0, 2, 1]
+    cache.insert(W[:33] + [998], cache.alloc(34))
+    assert oscheduler.order(cache, [W + [1], W + [2], Z], "lpm") == [0, 1, 2]
+
+
+def _dfs_tree():
+    cache = RadixCache(5000)
+    P = list(range(10, 20))
+    P1, P2 = list(range(20, 25)), list(range(30, 35))
+    Q = list(range(40, 50))
+    # two leaves below each of P1, P2 and Q make each a node of its own
+    for seq in (P + P1 + [0], P + P1 + [1], P + P2 + [0], P + P2 + [1], Q + [0], Q + [1]):
+        slots, _ = cache.match_prefix(seq)
+        cache.insert(seq, slots + cache.alloc(len(seq) - len(slots)))
+    return cache, P, P1, P2, Q
+
+
+def test_dfs_weight_order_by_hand():
+    """Weights: P1 2 (r1, r4), P2 1 (r3), P 1 + 3 = 4 (r5 hangs off P), Q 2
+    (r0, r6), root 1 (r2).  Depth first, a node's own requests first, heavier
+    children first: r2, then P's subtree (r5; P1: r1, r4; P2: r3), then Q
+    (r0, r6)."""
+    cache, P, P1, P2, Q = _dfs_tree()
+    prompts = [Q + [99, 98], P + P1 + [5, 6], [77, 78], P + P2 + [7, 8], P + P1 + [9, 9],
+               P + [50, 51, 52], Q + [66, 67]]
+    assert oscheduler.order(cache, prompts, "dfs-weight") == [2, 5, 1, 4, 3, 0, 6]
+    # equal weights: the subtree whose earliest waiting request came first
+    prompts = [Q + [7, 2], P + P2 + [3, 4], P + P1 + [5, 6], Q + [8, 8]]
+    # P (2: r1 via P2, r2 via P1) ties Q (2: r0, r3); Q's earliest is r0
+    assert oscheduler.order(cache, prompts, "dfs-weight") == [0, 3, 1, 2]
+
+
+@pytest.mark.parametrize("policy", ["lpm", "dfs-weight"])
+def test_scheduled_flow_conserves_slots_and_serves_everyone(policy):
+    """A shuffled fork tree under a small pool: every request is served once,
+    every slot is held exactly once after the flow."""
+    wl = workloads.fork_tree(branching=3, depth=3, level_tokens=12, decode_steps=3)
+    rng = random.Random(3)
+    waves = [rng.sample(w, len(w)) for w in wl.oracle_waves()]
+    trace, cache = run_bookkeeping(waves, wl.num_slots, wl.decode_steps, policy=policy)
+    served = [rid for b in trace.batches for rid, _, _ in b]
+    assert sorted(served) == sorted(r[0] for w in waves for r in w)
+    assert len(trace.eviction_log) > 0
     _assert_slots_conserved(cache)
