@@ -288,6 +288,36 @@ rx_status rx_batch_end(const rx_cache* cache, const int32_t* tokens,
                        int32_t* out_end);
 
 /* ------------------------------------------------------------------------
+ * Cache-aware scheduling ([T] "The scheduler is where the cache is won or
+ * lost"); host, reads the cache only.
+ * ---------------------------------------------------------------------- */
+
+#define RX_POLICY_FCFS 0       /* arrival order                              */
+#define RX_POLICY_LPM 1        /* longest prefix match first                 */
+#define RX_POLICY_DFS_WEIGHT 2 /* weighted depth-first order of the tree     */
+
+/* Order in which a waiting queue of R prompts (concatenated, request r at
+ * [indptr[r], indptr[r+1]), each non-empty) is served: out_order[k] = queue
+ * position of the k-th request to serve.  Each request's match, against the
+ * tree and against the queue tree below, is taken on its prompt without the
+ * last token, in whole pages; sorts are stable (equal keys keep queue order).
+ *   RX_POLICY_LPM: requests sorted by decreasing tree match.  A request
+ *     whose tree match is at most 32 tokens is also matched against a radix
+ *     tree over the waiting queue: sharing at least 32 tokens with a prompt
+ *     already in it sends the request to the back (its sibling runs first
+ *     and populates the tree), otherwise its prompt joins that queue tree.
+ *     With more than 128 waiting requests LPM falls back to arrival order.
+ *   RX_POLICY_DFS_WEIGHT: a request hangs off the deepest node whose whole
+ *     root path its prompt matches; each node weighs the requests hanging in
+ *     its subtree; the order is depth first from the root, a node's own
+ *     requests (in queue order) before its children, heavier children first,
+ *     ties by the queue position of the child subtree's earliest request.
+ * Errors: RX_ERR_INVALID (unknown policy, empty prompt). */
+rx_status rx_schedule(const rx_cache* cache, int32_t policy, int32_t R,
+                      const int32_t* tokens, const int64_t* indptr,
+                      int32_t* out_order);
+
+/* ------------------------------------------------------------------------
  * Decode plan (S7/S8 split; host)
  * ---------------------------------------------------------------------- */
 

@@ -993,3 +993,139 @@ extern "C" rx_status rx_extend_plan(const int32_t* qo_indptr, int32_t R, int32_t
 namespace rx_internal {
 rx_status set_error(rx_status s, const char* msg) { return fail(s, "%s", msg); }
 }  // namespace rx_internal
+
+// ---------------------------------------------------- cache-aware scheduling
+// "SGLang: the tree, and the language nobody remembers", section "The
+// scheduler is where the cache is won or lost".  A request's match (against
+// the tree and against the queue tree) is taken on its prompt without the
+// last token, in whole pages; sorts are stable.
+namespace {
+
+constexpr int64_t kInBatchCheck = 32;       // thin tree match: check the queue
+constexpr int64_t kInBatchDeprioritize = 32;  // shares this much with the queue: wait
+constexpr int32_t kLpmQueueLimit = 128;     // above: first come, first served
+
+// The deepest node whose whole root path t[0..n) matches (n in whole pages).
+const Node* hanging_node(const rx_cache* c, const int32_t* t, int64_t n) {
+  n = c->aligned(n);
+  const Node* node = c->root;
+  int64_t pos = 0;
+  while (pos < n) {
+    const Node* ch = c->child_of(node, t + pos);
+    if (!ch) break;
+    const int64_t len = int64_t(ch->key.size());
+    if (n - pos < len || common_prefix(ch->key.data(), t + pos, len) < len) break;
+    pos += len;
+    node = ch;
+  }
+  return node;
+}
+
+void lpm_order(const rx_cache* c, int32_t R, const int32_t* tokens, const int64_t* indptr,
+               int32_t* out) {
+  for (int32_t i = 0; i < R; ++i) out[i] = i;
+  if (R > kLpmQueueLimit) return;
+  // the simulated radix tree over the waiting queue (no slots of its own)
+  rx_config qc{c->ps, int32_t(c->ps), 0};
+  rx_cache* q = nullptr;
+  rx_cache_create(&qc, &q);
+  std::vector<int32_t> dummy;
+  std::vector<std::pair<int64_t, int32_t>> keys(static_cast<size_t>(R));
+  const int64_t kBack = INT64_MAX;
+  for (int32_t i = 0; i < R; ++i) {
+    const int32_t* p = tokens + indptr[i];
+    const int64_t n = indptr[i + 1] - indptr[i];
+    const int64_t m = c->match_length(p, n - 1);
+    bool back = false;
+    if (m <= kInBatchCheck) {
+      if (q->match_length(p, n - 1) >= kInBatchDeprioritize) {
+        back = true;
+      } else {
+        if (int64_t(dummy.size()) < n) dummy.resize(size_t(n), 0);
+        int64_t already = 0;
+        q->insert(p, dummy.data(), n, &already);
+      }
+    }
+    keys[size_t(i)] = {back ? kBack : -m, i};
+  }
+  rx_cache_destroy(q);
+  std::stable_sort(keys.begin(), keys.end(),
+                   [](const std::pair<int64_t, int32_t>& a, const std::pair<int64_t, int32_t>& b) {
+                     return a.first < b.first;
+                   });
+  for (int32_t i = 0; i < R; ++i) out[i] = keys[size_t(i)].second;
+}
+
+void dfs_weight_order(const rx_cache* c, int32_t R, const int32_t* tokens, const int64_t* indptr,
+                      int32_t* out) {
+  std::unordered_map<const Node*, std::vector<int32_t>> at;
+  for (int32_t i = 0; i < R; ++i) {
+    const int32_t* p = tokens + indptr[i];
+    const int64_t n = indptr[i + 1] - indptr[i];
+    at[hanging_node(c, p, n - 1)].push_back(i);
+  }
+  // subtree weights and earliest waiting request, children before parents
+  std::unordered_map<const Node*, std::pair<int64_t, int32_t>> wf;  // weight, first
+  std::vector<const Node*> order{c->root};
+  for (size_t k = 0; k < order.size(); ++k)
+    c->for_children(order[k], [&](const Node* ch) { order.push_back(ch); });
+  for (size_t k = order.size(); k-- > 0;) {
+    const Node* x = order[k];
+    auto it = at.find(x);
+    int64_t w = it == at.end() ? 0 : int64_t(it->second.size());
+    int32_t f = it == at.end() ? R : it->second.front();
+    c->for_children(x, [&](const Node* ch) {
+      const auto& cw = wf[ch];
+      w += cw.first;
+      f = std::min(f, cw.second);
+    });
+    wf[x] = {w, f};
+  }
+  // depth first: a node's own requests, then heavier children first
+  int32_t o = 0;
+  std::vector<const Node*> stack{c->root};
+  std::vector<const Node*> kids;
+  while (!stack.empty()) {
+    const Node* x = stack.back();
+    stack.pop_back();
+    auto it = at.find(x);
+    if (it != at.end())
+      for (int32_t i : it->second) out[o++] = i;
+    kids.clear();
+    c->for_children(x, [&](const Node* ch) {
+      if (wf[ch].first > 0) kids.push_back(ch);
+    });
+    std::sort(kids.begin(), kids.end(), [&](const Node* a, const Node* b) {
+      const auto& wa = wf[a];
+      const auto& wb = wf[b];
+      if (wa.first != wb.first) return wa.first > wb.first;
+      return wa.second < wb.second;
+    });
+    for (size_t k = kids.size(); k-- > 0;) stack.push_back(kids[k]);
+  }
+}
+
+}  // namespace
+
+extern "C" rx_status rx_schedule(const rx_cache* c, int32_t policy, int32_t R,
+                                 const int32_t* tokens, const int64_t* indptr,
+                                 int32_t* out_order) {
+  if (!c || R < 0 || (R && (!tokens || !indptr || !out_order)))
+    return fail(RX_ERR_INVALID, "rx_schedule: bad argument");
+  for (int32_t i = 0; i < R; ++i)
+    if (indptr[i + 1] - indptr[i] < 1)
+      return fail(RX_ERR_INVALID, "rx_schedule: empty prompt %d", i);
+  switch (policy) {
+    case RX_POLICY_FCFS:
+      for (int32_t i = 0; i < R; ++i) out_order[i] = i;
+      return RX_OK;
+    case RX_POLICY_LPM:
+      lpm_order(c, R, tokens, indptr, out_order);
+      return RX_OK;
+    case RX_POLICY_DFS_WEIGHT:
+      dfs_weight_order(c, R, tokens, indptr, out_order);
+      return RX_OK;
+    default:
+      return fail(RX_ERR_INVALID, "rx_schedule: unknown policy %d", policy);
+  }
+}

@@ -471,6 +471,8 @@ class Engine:
     wave (per layer) are allocated on the first run and written again by
     every later run: they stay valid until the next run starts, and whoever
     reads them on another stream must be done (e.g. synchronized) by then.
+    ``policy`` ("fcfs", "lpm" or "dfs-weight") orders each wave's waiting
+    requests before every extend batch (``rx_schedule``).
     With ``out_ring`` (an ``OutputRing``) every launch writes into the ring's
     next device buffer and the ring copies each buffer back to the host once
     the next launch takes a buffer (and at the end of a run); the tensors the
@@ -479,7 +481,7 @@ class Engine:
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
                  on_decode=None, stream=None, timing=False, on_decode_wave=None,
-                 reuse_outputs=False, out_ring=None):
+                 reuse_outputs=False, out_ring=None, policy="fcfs"):
         self.wl = wl
         self.device = device
         self.inputs = inputs
@@ -500,6 +502,7 @@ class Engine:
         self.timing = timing
         self.reuse_outputs = reuse_outputs
         self.out_ring = out_ring
+        self.policy = policy
         self._out_bufs = {}
         self.kernel_events = []   # (kind, start event, end event, algorithmic work)
         if device is not None:
@@ -574,6 +577,8 @@ class Engine:
         return h
 
     def _run_wave(self, wi, wave):
+        if self.policy != "fcfs":
+            return self._run_wave_scheduled(wi, wave)
         wl = self.wl
         lens, indptr, tokens, full, findptr, tokens_p, indptr_p = self._wave_host(wi, wave)
         self.h_table[:len(wave)] = 0
@@ -593,18 +598,60 @@ class Engine:
         for r, a in zip(wave, already):
             self.trace.finishes.append((r.rid, int(a)))
 
-    def _extend_batch(self, wave, j0, j1, indptr, ptrs):
+    def _run_wave_scheduled(self, wi, wave):
+        """A wave under a cache-aware policy: before every extend batch the
+        waiting requests are ordered by ``rx_schedule`` and the batch is taken
+        from the head of that order by the in-batch rule; requests take slot
+        table rows in the order they are served, and decode and finish run in
+        that order."""
+        wl = self.wl
+        lens, indptr, tokens, full, findptr, _, _ = self._wave_host(wi, wave)
+        R = len(wave)
+        self.h_table[:R] = 0
+        prompt_nodes = np.zeros(R, dtype=np.int64)
+        pending = list(range(R))
+        served = []
+
+        def gather(pos, tok, ind):
+            parts = [tok[ind[j]:ind[j + 1]] for j in pos]
+            out_ind = np.zeros(len(pos) + 1, dtype=np.int64)
+            np.cumsum([len(x) for x in parts], out=out_ind[1:])
+            return np.concatenate(parts).astype(np.int32, copy=False), out_ind
+
+        while pending:
+            ptok, pind = gather(pending, tokens, indptr)
+            ordered = [pending[k] for k in self.cache.schedule(self.policy, ptok, pind)]
+            otok, oind = gather(ordered, tokens, indptr)
+            end = self.cache.batch_end(otok, oind, 0)
+            ptrs = (otok.ctypes.data, oind.ctypes.data, prompt_nodes.ctypes.data)
+            self._extend_batch([wave[j] for j in ordered], 0, end, oind, ptrs,
+                               row0=len(served))
+            served += ordered[:end]
+            taken = set(ordered[:end])
+            pending = [j for j in pending if j not in taken]
+        swave = [wave[j] for j in served]
+        slens = lens[served]
+        if wl.decode_steps:
+            self._decode_phase(swave, slens.astype(np.int32), prompt_nodes)
+        sfull, sfind = gather(served, full, findptr)
+        already = self.cache.finish(sfull, sfind, self.h_table[:R], slens, prompt_nodes)
+        for r, a in zip(swave, already):
+            self.trace.finishes.append((r.rid, int(a)))
+
+    def _extend_batch(self, wave, j0, j1, indptr, ptrs, row0=0):
         """Requests j0 .. j1-1 of the wave as one extend batch.  ``indptr`` is
         the wave's token offsets (this batch's slice of it is passed as is:
         offsets are relative to the wave's tokens); ``ptrs`` = addresses of
-        the wave's tokens, its offsets and its prompt-node array."""
+        the wave's tokens, its offsets and its prompt-node array.  Request j
+        uses row row0 + j of the slot table (and of the prompt-node array)."""
         tokens_p, indptr_p, nodes_out_p = ptrs
         reqs = wave[j0:j1]
         R = j1 - j0
         ind = indptr[j0:j1 + 1]
         ind_p = indptr_p + 8 * j0
-        table = self.h_table[j0:j1]
-        table_p = self._h_table_p + 4 * self.max_ctx * j0
+        r0 = row0 + j0
+        table = self.h_table[r0:r0 + R]
+        table_p = self._h_table_p + 4 * self.max_ctx * r0
         prefix_p, mnodes_p, new_p = self._b_ptrs
         total = self.cache.extend_begin_p(R, tokens_p, ind_p, table_p, self.max_ctx, prefix_p,
                                           mnodes_p, new_p)
@@ -617,9 +664,9 @@ class Engine:
         self.trace.batches.append([(r.rid, pre[i], rows[i, :ln[i]]) for i, r in enumerate(reqs)])
         self.trace.prefilled += int(lens.sum()) - sum(pre)
         if self.device is not None:
-            self._extend_device(reqs, j0, j1, prefix, ind, new_slots)
+            self._extend_device(reqs, r0, r0 + R, prefix, ind, new_slots)
         self.cache.extend_end_p(R, tokens_p, ind_p, table_p, self.max_ctx, prefix_p, mnodes_p,
-                                nodes_out_p + 8 * j0)
+                                nodes_out_p + 8 * r0)
         self.batch_no += 1
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):

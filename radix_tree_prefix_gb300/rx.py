@@ -23,6 +23,7 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 RX_OK, RX_ERR_INVALID, RX_ERR_NO_SPACE, RX_ERR_STATE, RX_ERR_CUDA = range(5)
+POLICIES = {"fcfs": 0, "lpm": 1, "dfs-weight": 2}     # RX_POLICY_* of rx.h
 RX_WORK_WORDS = 8
 RX_DECODE_STATIC_SCRATCH_BYTES = 16 << 20   # fixed scratch of rx_decode_attention_static
 
@@ -108,6 +109,7 @@ _SIGS = {
     "rx_plan_decode_steps": [P, I32, I32, P, P, P, I32, I32, I32, P, I64, P],
     "rx_alloc_steps": [P, I64, I32, P],
     "rx_alloc_decode_steps": [P, I32, I32, P, P, P],
+    "rx_schedule": [P, I32, I32, P, P, P],
     "rx_kv_store": [P, I32, P, P, P, I64, P],
     "rx_req_to_token_write": [P, I64, I64, P, P, P, I64, P],
     "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
@@ -268,6 +270,15 @@ class RadixCache:
         out = np.empty((max(1, n_steps), max(1, B)), dtype=np.int32)
         _check(_lib.rx_alloc_decode_steps(self._h, B, int(n_steps), _p(p0), _p(ls), _p(out)))
         return out[:n_steps, :B]
+
+    def schedule(self, policy, tokens, indptr):
+        """Serving order of a waiting queue (rx_schedule): queue positions."""
+        pol = POLICIES[policy] if isinstance(policy, str) else int(policy)
+        t, ip = _i32(tokens), _i64(indptr)
+        R = len(ip) - 1
+        out = np.empty(max(1, R), dtype=np.int32)
+        _check(_lib.rx_schedule(self._h, pol, R, _p(t), _p(ip), _p(out)))
+        return out[:R]
 
     def evict(self, k):
         f = C.c_int64()

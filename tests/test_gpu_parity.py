@@ -282,3 +282,17 @@ def test_output_ring_reads_back_every_output():
     assert rx.device_check() == 0
     ring.close()
     host.close()
+
+
+@pytest.mark.parametrize("policy", ["lpm", "dfs-weight"])
+def test_scheduled_fork_tree_parity(policy):
+    """A fork tree whose leaves arrive shuffled, served in the policy's order
+    under a pool that holds 60% of the distinct tokens (eviction, slot
+    reuse): bookkeeping bit-exact, attention within tolerance."""
+    import random
+    wl = workloads.fork_tree(branching=3, depth=3, level_tokens=48, decode_steps=4)
+    rng = random.Random(9)
+    wl.waves = [rng.sample(w, len(w)) for w in wl.waves]
+    run = DeviceRun(wl, policy=policy)
+    run.assert_close()
+    assert len(run.trace.eviction_log) > 0

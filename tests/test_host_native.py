@@ -504,3 +504,57 @@ def test_alloc_decode_steps_follows_pages():
     # starts a page -> page 4 (16..19); request 1 takes 13.  Step 2: 17, 14.
     assert out[:, 0].tolist() == [11, 16, 17]
     assert out[:, 1].tolist() == [12, 13, 14]
+
+
+# -------------------------------------------------------------- scheduling
+def test_schedule_matches_oracle_on_random_queues():
+    """rx_schedule equals the oracle's order for every policy on random
+    queues over random trees (tiny alphabets, page sizes 1 and 4)."""
+    from oracle import scheduler as osched
+    rng = random.Random(41)
+    for trial in range(150):
+        ps = rng.choice([1, 1, 4])
+        o, n = ORadix(4000, ps), rx.RadixCache(4000, ps)
+        base = [rng.randrange(3) for _ in range(60)]
+        for _ in range(rng.randint(0, 6)):
+            cut = rng.randint(0, 60)
+            seq = base[:cut] + [rng.randrange(3) for _ in range(rng.randint(1, 40))]
+            os_, _ = o.match_prefix(seq)
+            ns_, _ = n.match_prefix(seq)
+            onew = o.alloc(len(seq) - len(os_))
+            nnew = n.alloc(len(seq) - len(ns_))
+            o.insert(seq, list(os_) + onew)
+            n.insert(seq, np.concatenate([ns_, nnew]))
+        R = rng.choice([1, 3, 9, 40, 129, 140])
+        prompts = []
+        for _ in range(R):
+            cut = rng.choice([0, 10, 33, 40, 60])
+            prompts.append(base[:cut] + [rng.randrange(3) for _ in range(rng.randint(1, 45))])
+        tok = np.concatenate([np.array(p, dtype=np.int32) for p in prompts])
+        ind = np.zeros(R + 1, dtype=np.int64)
+        np.cumsum([len(p) for p in prompts], out=ind[1:])
+        for pol in ("fcfs", "lpm", "dfs-weight"):
+            assert n.schedule(pol, tok, ind).tolist() == osched.order(o, prompts, pol), (trial, pol)
+
+
+@pytest.mark.parametrize("policy", ["lpm", "dfs-weight"])
+@pytest.mark.parametrize("page_size", [1, 4])
+def test_scheduled_request_flow_matches_oracle(policy, page_size):
+    """Waves of a fork tree in shuffled arrival order under a policy (the pool
+    holds 60% of the distinct tokens): batches, served order, slot tables,
+    decode slots, finishes and eviction order equal the oracle's."""
+    wl = workloads.fork_tree(branching=3, depth=3, level_tokens=24, decode_steps=4)
+    rng = random.Random(9)
+    wl.waves = [rng.sample(w, len(w)) for w in wl.waves]
+    if page_size > 1:
+        wl = workloads.with_pages(wl, page_size)
+    got = Engine(wl, policy=policy).run()
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                              page_size=page_size, policy=policy)
+    assert got.as_tuple() == want.as_tuple()
+    assert got.stats == want.stats
+    assert len(got.eviction_log) > 0
+    fcfs, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                              page_size=page_size)
+    # shuffled arrivals: the cache-aware order prefills no more than arrival order
+    assert got.prefilled <= fcfs.prefilled
