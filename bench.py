@@ -45,6 +45,8 @@ DEFAULT_WORKLOAD = "multi_turn_chat"
 # other workloads measured in the same run, each with its own object in the line
 SIDE_WORKLOADS = ("agent_loop", "long_shared", "fork_tree")
 SIDE_STEPS = 10                 # timed steps of each side workload (3 warm-up)
+E2E_RING_BYTES = 24 << 30       # device (and page-locked host) bytes of the e2e output ring
+E2E_INPUT_RING = 4              # e2e input buffers (positions in flight: 3)
 
 
 def parse(argv=None):
@@ -401,7 +403,7 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
            "launches": eng.gpu_launches - launches0, "wall": wall, "e2e": None}
     if e2e:
         # host copies of every recorded input, then the device copies go
-        host = PreparedInputs(source, host=True)
+        host = PreparedInputs(source, host=True, ring=E2E_INPUT_RING)
         host.adopt(prepared)
         host.freeze()
         prepared.ext.clear()
@@ -411,7 +413,10 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
         hq, d = wl.num_q_heads, wl.head_dim
         most = max([sum(len(row) - m for _, m, row in b) for b in trace.batches] +
                    [len(w) * wl.decode_steps for w in wl.waves])
-        ring = OutputRing(dev, most * hq * (d + 1), slots=4)
+        # as many output buffers as fit in E2E_RING_BYTES (at least 4), so the
+        # read-back of a batch's outputs can trail its kernels
+        per = most * hq * (d + 1)
+        ring = OutputRing(dev, per, slots=max(4, min(64, E2E_RING_BYTES // (4 * per))))
         eng2 = Engine(wl, device=dev, inputs=host, layers=layers, out_ring=ring)
         eng2.run()                                      # untimed first run
         torch.cuda.synchronize()
@@ -431,9 +436,10 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
                       "h2d_bytes_per_step": host.h2d_bytes // steps,
                       "d2h_bytes_per_step": ring.d2h_bytes // steps,
                       "ms_per_step": e2e_s * 1e3,
-                      "copies": "inputs from page-locked host memory one batch ahead on a side "
-                                "stream; every output (fp32 o and lse) read back through a "
-                                "ring of 4 device/host buffer pairs on another stream"}
+                      "copies": f"inputs from page-locked host memory up to {host.ring - 1} "
+                                f"batches ahead on a side stream; every output (fp32 o and lse) "
+                                f"read back through a ring of {ring.slots} device/host buffer "
+                                f"pairs on another stream"}
         del eng2
         ring.close()
         host.close()

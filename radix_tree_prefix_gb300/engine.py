@@ -170,7 +170,8 @@ class PreparedInputs:
     for one batch's inputs, the next batch's (in the recorded order) are
     already being copied on a side stream, so the copies overlap the kernels.
     The device side is a ring of ``ring`` flat buffers, each as large as the
-    largest position, filled in turn: a buffer is refilled once the work that
+    largest position, filled in turn, and the ``ring - 1`` positions after the
+    one handed out are kept in flight: a buffer is refilled once the work that
     read its previous occupant on the consumer's stream (everything the
     consumer had enqueued when it asked for the position after that one) has
     completed."""
@@ -185,7 +186,7 @@ class PreparedInputs:
         self.recording = True
         self.h2d_bytes = 0
         self._pos = 0
-        self._ahead = None     # (position, event: its copy landed, views, buffer)
+        self._ahead = []       # [(position, event: its copy landed, views, buffer)]
         self._copy_stream = None
         self._dev = {}         # ring slot -> flat device buffer
         self._last_use = {}    # ring slot -> event after its last reader
@@ -284,24 +285,27 @@ class PreparedInputs:
         pos = self._pos
         if self.order[pos] != (name, key):     # not the recorded order: start over
             pos = self.order.index((name, key))
-            self._ahead = None
-        if self._ahead is not None and self._ahead[0] == pos:
-            _, ready, out, slot = self._ahead
+            self._ahead = []
+        if self._ahead and self._ahead[0][0] == pos:
+            _, ready, out, slot = self._ahead.pop(0)
             cur.wait_event(ready)
         else:
+            self._ahead = []
             slot = self._next_slot()
             out = self._fill(pos, slot, cur)
         self._handed = slot
         self._pos = (pos + 1) % len(self.order)
-        self._ahead = None
-        if self._pos != pos:
-            if self._copy_stream is None:
-                self._copy_stream = torch.cuda.Stream(self.source.device)
+        # keep the next ring - 1 positions in flight on the copy stream
+        if self._copy_stream is None:
+            self._copy_stream = torch.cuda.Stream(self.source.device)
+        nxt = (self._ahead[-1][0] + 1) % len(self.order) if self._ahead else self._pos
+        while len(self._ahead) < self.ring - 1:
             nslot = self._next_slot()
-            views = self._fill(self._pos, nslot, self._copy_stream)
+            views = self._fill(nxt, nslot, self._copy_stream)
             ready = torch.cuda.Event()
             ready.record(self._copy_stream)
-            self._ahead = (self._pos, ready, views, nslot)
+            self._ahead.append((nxt, ready, views, nslot))
+            nxt = (nxt + 1) % len(self.order)
         return out
 
     def extend(self, batch_no, reqs, prefix):
