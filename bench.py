@@ -77,6 +77,10 @@ TRAFFIC = {
     ("long_shared", "rx_decode_attention"): 406.35e6 + 16.01e6,
     ("long_shared", "rx_extend_attention"): (2230.64e6 + 3158.90e6) / 2,
     ("fork_tree", "rx_extend_attention"): (5711.18e6 + 887.04e6) / 130,
+    # (69.465 MB read + 0.655 MB written) / 69.865 MB algorithmic on the
+    # multi_turn_chat_small launch, times the full workload's 1.0940 GB of
+    # algorithmic bytes per decode launch
+    ("multi_turn_chat", "rx_decode_attention"): (69.465e6 + 0.655e6) / 69.865e6 * 1.0940e9,
 }
 
 

@@ -145,6 +145,17 @@ MUTANTS = {
     "dfs_own_requests_last": ("scheduler.py", [
         ("        out.extend(at.get(node.id, []))\n        kids = [",
          "        kids = [")]),
+    "draft_mask_without_diagonal": ("speculative.py", [
+        ("        path.append(i)\n        i = parents[i]\n",
+         "        i = parents[i]\n        if i >= 0:\n            path.append(i)\n")]),
+    "draft_path_without_root": ("speculative.py", [
+        ("    while i >= 0:\n", "    while i >= 0 and parents[i] >= 0:\n")]),
+    "draft_depth_from_one": ("speculative.py", [
+        ("out.append(0 if p < 0 else out[p] + 1)", "out.append(1 if p < 0 else out[p] + 1)")]),
+    "move_writes_before_reads": ("speculative.py", [
+        ("    rows = [np.array(pool[:, :, int(s), :], copy=True) for s in src]\n"
+         "    for t, r in zip(tgt, rows):\n        out[:, :, int(t), :] = r\n",
+         "    for t, s in zip(tgt, src):\n        out[:, :, int(t), :] = out[:, :, int(s), :]\n")]),
     "dfs_weight_without_subtree": ("scheduler.py", [
         ("            w += cw\n", "")]),
     "match_whole_prompt": ("harness.py", [

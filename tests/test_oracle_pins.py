@@ -14,6 +14,7 @@ import pytest
 from conftest import read_golden
 from oracle import attention as oatt
 from oracle import scheduler as oscheduler
+from oracle import speculative as ospec
 from oracle.harness import run_bookkeeping
 from oracle.radix_cache import NoSpace, RadixCache, StateError
 from radix_tree_prefix_gb300 import workloads
@@ -897,3 +898,113 @@ def test_scheduled_flow_conserves_slots_and_serves_everyone(policy):
     assert sorted(served) == sorted(r[0] for w in waves for r in w)
     assert len(trace.eviction_log) > 0
     _assert_slots_conserved(cache)
+
+
+# ------------------------------------------------------- draft-tree verify
+def _draft_fixture():
+    g = {}
+    for ln in read_golden("draft_tree.txt"):
+        k, *v = ln.split()
+        g[k] = [int(x) for x in v]
+    return g
+
+
+def test_draft_positions_example():
+    g = _draft_fixture()
+    parents = [-1, 0, 0, 1]                      # depths 0, 1, 1, 2
+    assert ospec.depths(parents) == g["depths"]
+    assert ospec.positions(g["prompt_len"][0], parents) == g["positions"]
+
+
+def test_tree_mask_by_hand_and_size_formula():
+    """The example tree after 2 context tokens, by hand; the entry count of
+    materialised masks equals the page's formula, and at the page's sizes
+    the formula gives its 128 MiB."""
+    m = ospec.tree_mask(2, [-1, 0, 0, 1])
+    want = np.array([[1, 1, 1, 0, 0, 0],
+                     [1, 1, 1, 1, 0, 0],
+                     [1, 1, 1, 0, 1, 0],
+                     [1, 1, 1, 1, 0, 1]], dtype=bool)
+    assert np.array_equal(m, want)
+    rng = random.Random(4)
+    for trial in range(20):
+        bs, nv = rng.randint(1, 5), rng.randint(1, 9)
+        lens = [rng.randint(0, 30) for _ in range(bs)]
+        parents = [[rng.randrange(-1, i) for i in range(nv)] for _ in range(bs)]
+        total = sum(ospec.tree_mask(p, par).size for p, par in zip(lens, parents))
+        assert total == sum(lens) * nv + nv * nv * bs
+    g = _draft_fixture()
+    bs, ctx, nv = g["mask_requests"][0], g["mask_context"][0], g["mask_verify"][0]
+    entries = bs * ctx * nv + nv * nv * bs
+    assert round(entries / 2 ** 20) == g["mask_mib"][0]
+
+
+def _qkv(rng, n, p, hq=4, hkv=2, d=8):
+    return (rng.standard_normal((n, hq, d)), rng.standard_normal((p, hkv, d)),
+            rng.standard_normal((p, hkv, d)), rng.standard_normal((n, hkv, d)),
+            rng.standard_normal((n, hkv, d)))
+
+
+def test_chain_tree_equals_causal_extend():
+    """A chain of drafts (each continues the one before) sees exactly what a
+    causal extend of the same tokens after the prefix sees."""
+    rng = np.random.default_rng(5)
+    n, p = 7, 11
+    q, kp, vp, kd, vd = _qkv(rng, n, p)
+    o, lse = ospec.verify_attention(q, kp, vp, kd, vd, list(range(-1, n - 1)))
+    eo, el = oatt.extend_attention(q, np.concatenate([kp, kd]), np.concatenate([vp, vd]), p)
+    assert np.array_equal(o, eo) and np.array_equal(lse, el)
+
+
+def test_depth_zero_drafts_are_independent_decodes():
+    """Drafts that all continue the verified token see the prefix and
+    themselves only: each equals a decode of that token alone."""
+    rng = np.random.default_rng(6)
+    n, p = 5, 9
+    q, kp, vp, kd, vd = _qkv(rng, n, p)
+    o, lse = ospec.verify_attention(q, kp, vp, kd, vd, [-1] * n)
+    for i in range(n):
+        do, dl = oatt.decode_attention(q[i], np.concatenate([kp, kd[i:i + 1]]),
+                                       np.concatenate([vp, vd[i:i + 1]]))
+        assert np.array_equal(o[i], do) and np.array_equal(lse[i], dl)
+
+
+def test_branch_equals_its_own_chain():
+    """Any draft's result equals the chain made of its root path alone."""
+    rng = np.random.default_rng(7)
+    parents = [-1, 0, 0, 1, 1, 2, 5, -1, 7]
+    n, p = len(parents), 6
+    q, kp, vp, kd, vd = _qkv(rng, n, p)
+    o, _ = ospec.verify_attention(q, kp, vp, kd, vd, parents)
+    for i in range(n):
+        path = ospec.ancestors_and_self(parents, i)
+        co, _ = oatt.extend_attention(q[path], np.concatenate([kp, kd[path]]),
+                                      np.concatenate([vp, vd[path]]), p)
+        assert np.allclose(o[i], co[-1], atol=1e-14)
+
+
+def test_move_kv_reads_before_writes():
+    rng = np.random.default_rng(8)
+    pool = rng.standard_normal((2, 3, 12, 4))
+    out = ospec.move_kv(pool, [3, 5, 9], [5, 3, 1])      # 3 <-> 5 swap, 1 -> 9
+    assert np.array_equal(out[:, :, 3], pool[:, :, 5])
+    assert np.array_equal(out[:, :, 5], pool[:, :, 3])
+    assert np.array_equal(out[:, :, 9], pool[:, :, 1])
+    keep = [s for s in range(12) if s not in (3, 5, 9)]
+    assert np.array_equal(out[:, :, keep], pool[:, :, keep])
+
+
+def test_chunked_extend_equals_unchunked():
+    """An extend split into chunks (each chunk's queries after the prefix
+    plus the earlier chunks) gives the unchunked rows exactly."""
+    rng = np.random.default_rng(9)
+    n, p = 37, 14
+    q = rng.standard_normal((n - p, 4, 8))
+    k = rng.standard_normal((n, 2, 8))
+    v = rng.standard_normal((n, 2, 8))
+    full_o, full_l = oatt.extend_attention(q, k, v, p)
+    for chunk in (1, 5, 8, 23):
+        for a in range(0, n - p, chunk):
+            b = min(n - p, a + chunk)
+            o, l = oatt.extend_attention(q[a:b], k[:p + b], v[:p + b], p + a)
+            assert np.array_equal(o, full_o[a:b]) and np.array_equal(l, full_l[a:b])
