@@ -548,6 +548,62 @@ rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_t layer,
                                      float scale, float* d_out, float* d_lse,
                                      rx_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Draft-tree verification and KV moves ([T] "Speculative decoding puts a
+ * tree inside the tree")
+ * ---------------------------------------------------------------------- */
+
+/* Host: slot-table rows of the draft tokens of R requests.  Request r's
+ * context before its draft tree is prefix_len[r] tokens whose slots are
+ * prefix_rows[r*prefix_stride .. +prefix_len[r]); its drafts are
+ * i in [draft_indptr[r], draft_indptr[r+1]) with parents[i] the index, local
+ * to the request, of the draft that i continues (-1: i continues the last
+ * verified token; a parent precedes its child) and draft_slots[i] the slot
+ * its K/V is stored in.  Writes, per draft i: out_rows[i*out_stride ..] =
+ * context slots ++ the slots of i's root path, root first, ending with i's
+ * own; out_ctx_len[i] = prefix_len[r] + depth(i) + 1; out_positions[i] (may
+ * be NULL) = prefix_len[r] + depth(i), the draft's sequence position.
+ * Errors: RX_ERR_INVALID (a parent not before its child, a row longer than
+ * out_stride). */
+rx_status rx_verify_rows(int32_t R, const int32_t* prefix_len,
+                         const int32_t* prefix_rows, int64_t prefix_stride,
+                         const int64_t* draft_indptr, const int32_t* parents,
+                         const int32_t* draft_slots, int32_t* out_rows,
+                         int64_t out_stride, int32_t* out_ctx_len,
+                         int32_t* out_positions);
+
+/* Tree-masked attention of N draft tokens over the pool: draft i (query
+ * d_q[i], bf16 [N][Hq][head_dim]) attends, with softmax, to the keys of its
+ * row of d_req_to_token (its request's context, then its ancestors and
+ * itself: exactly the tree mask).  The plan is rx_plan_decode over the
+ * drafts with prompt_node = each draft's request's locked node, ctx_len =
+ * out_ctx_len of rx_verify_rows and req_rows = the drafts' rows: the
+ * context a request's drafts share is read once for all of them as a
+ * multi-query tile.  The drafts' K/V must be stored first (rx_kv_store).
+ * Arguments, outputs and errors as rx_decode_attention with B = N. */
+rx_status rx_verify_attention(const rx_pool_desc* pool, int32_t layer,
+                              const void* d_q, int32_t num_q_heads,
+                              const int32_t* d_req_to_token,
+                              int64_t row_stride, const int32_t* d_plan,
+                              const rx_decode_plan_info* info, int32_t N,
+                              float scale, float* d_out, float* d_lse,
+                              void* d_workspace, size_t workspace_bytes,
+                              rx_stream_t stream);
+
+/* dst->k/v_pool[l][h][d_dst_slots[i]] = src->k/v_pool[l][h][d_src_slots[i]]
+ * for i < n, every layer l and KV head h (device int32 slot lists).  With
+ * src == dst it moves KV within the pool (the accepted path of a draft tree
+ * to the slots the request's next positions use, move_kv_cache); with two
+ * pools of the same shape it copies between them (e.g. the device pool and
+ * a page-locked host pool the device reads and writes directly).  Within
+ * one pool no target slot may be another entry's source.  A slot outside
+ * [1, num_slots) of its pool skips the entry on the device and is reported
+ * by rx_device_check (bit 5).  Errors: RX_ERR_INVALID (pools of different
+ * shape, NULL or misaligned pools). */
+rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst,
+                     const int32_t* d_src_slots, const int32_t* d_dst_slots,
+                     int64_t n, rx_stream_t stream);
+
 /* Synchronise the current device and read the kernels' error words (then
  * clear them).  *out_flags (may be NULL): bit 0 = rx_kv_store met a slot
  * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel
@@ -558,7 +614,8 @@ rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_t layer,
  * tensor-core operations they had issued before they exit); bit 3 = a
  * tensor-core tile found its dynamic shared memory off a 1024-byte boundary
  * and returned without results; bit 4 = rx_req_to_token_write met a row or
- * position outside the table and skipped that entry.  Returns RX_ERR_CUDA
+ * position outside the table and skipped that entry; bit 5 = rx_kv_copy met
+ * a slot outside its pool and skipped that entry.  Returns RX_ERR_CUDA
  * if a flag was set or the device reported an error. */
 rx_status rx_device_check(int32_t* out_flags);
 

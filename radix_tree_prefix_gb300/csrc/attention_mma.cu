@@ -245,6 +245,20 @@ extern "C" rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer
                                reinterpret_cast<cudaStream_t>(stream), true, 0);
 }
 
+extern "C" rx_status rx_verify_attention(const rx_pool_desc* pool, int32_t layer,
+                                         const void* d_q, int32_t num_q_heads,
+                                         const int32_t* d_req_to_token, int64_t row_stride,
+                                         const int32_t* d_plan, const rx_decode_plan_info* info,
+                                         int32_t N, float scale, float* d_out, float* d_lse,
+                                         void* d_workspace, size_t workspace_bytes,
+                                         rx_stream_t stream) {
+  // every draft token is one query of the plan; its row holds the context
+  // and its root path, so the decode kernels apply the tree mask
+  return decode_attention_impl(pool, layer, d_q, num_q_heads, d_req_to_token, row_stride, d_plan,
+                               info, N, scale, d_out, d_lse, d_workspace, workspace_bytes,
+                               reinterpret_cast<cudaStream_t>(stream), true, 0);
+}
+
 extern "C" rx_status rx_decode_steps(const rx_pool_desc* pool, int32_t layer, int32_t num_q_heads,
                                      const int32_t* d_req_to_token, int64_t row_stride,
                                      const rx_decode_step* steps, int32_t n_steps, int32_t B,

@@ -19,8 +19,9 @@
 #include "rx_internal.h"
 
 // Bit 0: rx_kv_store met a slot outside [1, num_slots); bit 4:
-// rx_req_to_token_write met a row or position outside the table.  The
-// offending write is skipped either way.  Read by rx_device_check().
+// rx_req_to_token_write met a row or position outside the table; bit 5:
+// rx_kv_copy met a slot outside its pool.  The offending write is skipped.
+// Read by rx_device_check().
 static __device__ int32_t g_kv_store_error;
 
 namespace {
@@ -68,6 +69,41 @@ __global__ void r2t_write_kernel(int32_t* __restrict__ table, int64_t num_rows, 
     return;
   }
   table[int64_t(r) * stride + p] = slots[i];
+}
+
+// dst_pool[l][h][dst[i]][:] = src_pool[l][h][src[i]][:] for every layer and
+// head: one 16-byte chunk per thread and iteration, chunks of a row on
+// consecutive threads.  A slot outside [1, num_slots) of its pool skips the
+// entry and sets bit 5 of the error word.  The pools may be the same (a move
+// within the pool) or different (for example the device pool and a
+// page-locked host pool the device reads and writes directly).
+__global__ void __launch_bounds__(256) kv_copy_kernel(const uint4* __restrict__ src_k,
+                                                      const uint4* __restrict__ src_v,
+                                                      uint4* dst_k, uint4* dst_v,
+                                                      const int32_t* __restrict__ src_slots,
+                                                      const int32_t* __restrict__ dst_slots,
+                                                      int64_t n, int L, int hkv, int cpr,
+                                                      int64_t src_slots_n, int64_t dst_slots_n) {
+  const int64_t per_entry = int64_t(L) * hkv * cpr;
+  const int64_t total = n * per_entry;
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < total;
+       c += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t i = c / per_entry;
+    int64_t rem = c - i * per_entry;
+    const int64_t lh = rem / cpr;          // layer * hkv + head
+    const int j = int(rem - lh * cpr);
+    const int32_t s = __ldg(src_slots + i), t = __ldg(dst_slots + i);
+    if (s < 1 || s >= src_slots_n || t < 1 || t >= dst_slots_n) {
+      if (j == 0 && lh == 0) atomicOr(&g_kv_store_error, 32);
+      continue;
+    }
+    const int64_t so = (lh * src_slots_n + s) * cpr + j;
+    const int64_t to = (lh * dst_slots_n + t) * cpr + j;
+    const uint4 kv = src_k[so];
+    const uint4 vv = src_v[so];
+    dst_k[to] = kv;
+    dst_v[to] = vv;
+  }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -161,6 +197,53 @@ extern "C" rx_status rx_req_to_token_write(int32_t* d_table, int64_t num_rows,
   return rx_internal::launch_status("rx_req_to_token_write");
 }
 
+extern "C" rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst,
+                                const int32_t* d_src_slots, const int32_t* d_dst_slots, int64_t n,
+                                rx_stream_t stream) {
+  rx_status st = rx_internal::check_pool(src, 0);
+  if (st == RX_OK) st = rx_internal::check_pool(dst, 0);
+  if (st != RX_OK) return st;
+  if (src->num_layers != dst->num_layers || src->num_kv_heads != dst->num_kv_heads ||
+      src->head_dim != dst->head_dim)
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_copy: pools differ in shape");
+  if (n < 0) return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_copy: n < 0");
+  if (n == 0) return RX_OK;
+  if (!d_src_slots || !d_dst_slots)
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_copy: NULL slot list");
+  // Every pool pointer must be one the device can reach: device (or
+  // managed) memory as it is, page-locked host memory through its mapped
+  // device address; pageable host memory is refused before any launch.
+  void* ptr[4] = {src->k_pool, src->v_pool, dst->k_pool, dst->v_pool};
+  for (void*& q : ptr) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+      cudaGetLastError();
+      return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_copy: pool pointer unknown to CUDA");
+    }
+    if (at.type == cudaMemoryTypeHost) {
+      if (!at.devicePointer)
+        return rx_internal::set_error(RX_ERR_INVALID,
+                                      "rx_kv_copy: host pool not mapped for device access");
+      q = at.devicePointer;
+    } else if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) {
+      return rx_internal::set_error(RX_ERR_INVALID,
+                                    "rx_kv_copy: pool must be device or page-locked host memory");
+    }
+    if (reinterpret_cast<uintptr_t>(q) & 15)
+      return rx_internal::set_error(RX_ERR_INVALID, "rx_kv_copy: misaligned pool");
+  }
+  const int cpr = src->head_dim / 8;
+  const int64_t total = n * src->num_layers * src->num_kv_heads * cpr;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = int64_t(rx_internal::sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  kv_copy_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(ptr[0]), reinterpret_cast<const uint4*>(ptr[1]),
+      reinterpret_cast<uint4*>(ptr[2]), reinterpret_cast<uint4*>(ptr[3]), d_src_slots,
+      d_dst_slots, n, src->num_layers, src->num_kv_heads, cpr, src->num_slots, dst->num_slots);
+  return rx_internal::launch_status("rx_kv_copy");
+}
+
 extern "C" rx_status rx_device_check(int32_t* out_flags) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -179,6 +262,8 @@ extern "C" rx_status rx_device_check(int32_t* out_flags) {
                                                "waiting on a barrier"
                                   : (f & 16) ? "rx_device_check: a slot-table write met a row "
                                                "or position outside the table"
+                                  : (f & 32) ? "rx_device_check: a KV copy met a slot outside "
+                                               "its pool"
                                              : "rx_device_check: a kernel met a slot outside the pool");
   return RX_OK;
 }

@@ -1129,3 +1129,49 @@ extern "C" rx_status rx_schedule(const rx_cache* c, int32_t policy, int32_t R,
       return fail(RX_ERR_INVALID, "rx_schedule: unknown policy %d", policy);
   }
 }
+
+// --------------------------------------------------- draft-tree verification
+// "SGLang: the tree, and the language nobody remembers", section
+// "Speculative decoding puts a tree inside the tree": a draft token attends
+// to the request's context and to its own ancestors in the draft tree (and
+// itself).  Its slot-table row is the context's slots followed by the slots
+// of its root path, so the decode kernels compute exactly the tree-masked
+// attention over that row.
+extern "C" rx_status rx_verify_rows(int32_t R, const int32_t* prefix_len,
+                                    const int32_t* prefix_rows, int64_t prefix_stride,
+                                    const int64_t* draft_indptr, const int32_t* parents,
+                                    const int32_t* draft_slots, int32_t* out_rows,
+                                    int64_t out_stride, int32_t* out_ctx_len,
+                                    int32_t* out_positions) {
+  if (R < 0 || (R && (!prefix_len || !prefix_rows || !draft_indptr || !out_rows ||
+                      !out_ctx_len)) || prefix_stride < 0 || out_stride < 1)
+    return fail(RX_ERR_INVALID, "rx_verify_rows: bad argument");
+  std::vector<int32_t> depth, path;
+  for (int32_t r = 0; r < R; ++r) {
+    const int64_t b = draft_indptr[r], e = draft_indptr[r + 1];
+    const int64_t p = prefix_len[r];
+    if (e < b || p < 0 || p > prefix_stride)
+      return fail(RX_ERR_INVALID, "rx_verify_rows: request %d: bad draft range or prefix", r);
+    depth.assign(size_t(e - b), 0);
+    for (int64_t i = b; i < e; ++i) {
+      const int64_t li = i - b;
+      const int32_t par = parents[i];
+      if (par < -1 || par >= li)
+        return fail(RX_ERR_INVALID, "rx_verify_rows: draft %lld: parent %d must precede it",
+                    (long long)i, par);
+      depth[size_t(li)] = par < 0 ? 0 : depth[size_t(par)] + 1;
+      const int64_t ctx = p + depth[size_t(li)] + 1;
+      if (ctx > out_stride)
+        return fail(RX_ERR_INVALID, "rx_verify_rows: draft %lld needs %lld row entries, row has %lld",
+                    (long long)i, (long long)ctx, (long long)out_stride);
+      int32_t* row = out_rows + i * out_stride;
+      std::memcpy(row, prefix_rows + int64_t(r) * prefix_stride, size_t(p) * sizeof(int32_t));
+      path.clear();
+      for (int64_t j = li; j >= 0; j = parents[b + j]) path.push_back(draft_slots[b + j]);
+      for (size_t k = 0; k < path.size(); ++k) row[p + int64_t(k)] = path[path.size() - 1 - k];
+      out_ctx_len[i] = int32_t(ctx);
+      if (out_positions) out_positions[i] = int32_t(p + depth[size_t(li)]);
+    }
+  }
+  return RX_OK;
+}

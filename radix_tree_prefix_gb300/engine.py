@@ -476,7 +476,12 @@ class Engine:
     every later run: they stay valid until the next run starts, and whoever
     reads them on another stream must be done (e.g. synchronized) by then.
     ``policy`` ("fcfs", "lpm" or "dfs-weight") orders each wave's waiting
-    requests before every extend batch (``rx_schedule``).
+    requests before every extend batch (``rx_schedule``).  ``chunk_tokens``
+    (chunked prefill, "SGLang: Structured LLM Programs for Efficient
+    Inference", section "How the runtime and frontend work together") cuts an
+    extend batch's queries into launches of at most that many query tokens,
+    in query order: a request's suffix may span several chunks, and a chunk's
+    part of it attends over the prefix plus the suffix tokens before it.
     With ``out_ring`` (an ``OutputRing``) every launch writes into the ring's
     next device buffer and the ring copies each buffer back to the host once
     the next launch takes a buffer (and at the end of a run); the tensors the
@@ -485,7 +490,7 @@ class Engine:
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
                  on_decode=None, stream=None, timing=False, on_decode_wave=None,
-                 reuse_outputs=False, out_ring=None, policy="fcfs"):
+                 reuse_outputs=False, out_ring=None, policy="fcfs", chunk_tokens=None):
         self.wl = wl
         self.device = device
         self.inputs = inputs
@@ -507,6 +512,7 @@ class Engine:
         self.reuse_outputs = reuse_outputs
         self.out_ring = out_ring
         self.policy = policy
+        self.chunk_tokens = chunk_tokens
         self._out_bufs = {}
         self.kernel_events = []   # (kind, start event, end event, algorithmic work)
         if device is not None:
@@ -602,6 +608,35 @@ class Engine:
         for r, a in zip(wave, already):
             self.trace.finishes.append((r.rid, int(a)))
 
+    def _chunks(self, prefix, qo):
+        """The batch's query rows [0, total) cut into consecutive chunks of at
+        most chunk_tokens rows.  Per chunk: the first row q0, and for each
+        request it touches its batch row, prefix (its own prefix plus its
+        suffix rows before the chunk), query offsets relative to q0 and the
+        tile plan.  One chunk (the whole batch) without chunk_tokens."""
+        total = int(qo[-1])
+        C = self.chunk_tokens
+        if not C or total <= C:
+            return [None]
+        wl = self.wl
+        out = []
+        for a in range(0, total, C):
+            b = min(total, a + C)
+            rows, pre, offs = [], [], [0]
+            for r in range(len(prefix)):
+                lo, hi = max(a, int(qo[r])), min(b, int(qo[r + 1]))
+                if lo >= hi:
+                    continue
+                rows.append(r)
+                pre.append(int(prefix[r]) + lo - int(qo[r]))
+                offs.append(offs[-1] + hi - lo)
+            cq = np.array(offs, dtype=np.int32)
+            tiles, n_tiles = rx.extend_plan(cq, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+            out.append({"q0": a, "rows": np.array(rows, dtype=np.int32),
+                        "prefix": np.array(pre, dtype=np.int32), "qo": cq, "tiles": tiles,
+                        "n_tiles": n_tiles})
+        return out
+
     def _run_wave_scheduled(self, wi, wave):
         """A wave under a cache-aware policy: before every extend batch the
         waiting requests are ordered by ``rx_schedule`` and the batch is taken
@@ -684,9 +719,11 @@ class Engine:
         # copy (rows 0 .. R-1); the engine's device table gets the wave's rows
         # once, before its decode steps
         width = int(max(ind[1:] - ind[:-1]))
-        d_rows, d_prefix, d_qo, d_tiles, d_slots, d_tab = self.staging.upload([
+        chunks = self._chunks(prefix, qo)
+        d_rows, d_prefix, d_qo, d_tiles, d_slots, d_tab, *d_extra = self.staging.upload([
             np.arange(R, dtype=np.int32), prefix, qo, tiles, new_slots,
-            self.h_table[j0:j1, :width].ravel()])
+            self.h_table[j0:j1, :width].ravel()] + ([c for ch in chunks for c in (
+                ch["rows"], ch["prefix"], ch["qo"], ch["tiles"])] if len(chunks) > 1 else []))
         d_tab.shape = (R, width)
         inputs = self.inputs.extend(self.batch_no, reqs, prefix)
         total_q = int(qo[-1])
@@ -700,13 +737,24 @@ class Engine:
             self._event_end(ev, "kv_store", store_bytes)
             out, lse = self._outputs(("ext", self.batch_no, layer),
                                      (total_q, wl.num_q_heads, wl.head_dim))
-            call = rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, d_tab,
-                                            d_rows, d_prefix, d_qo, d_tiles, R, n_tiles,
-                                            self.scale, out, lse, self.stream)
+            if len(chunks) == 1:
+                calls = [rx.extend_attention_call(self.pool, layer, q, wl.num_q_heads, d_tab,
+                                                  d_rows, d_prefix, d_qo, d_tiles, R, n_tiles,
+                                                  self.scale, out, lse, self.stream)]
+            else:
+                calls = []
+                for k, ch in enumerate(chunks):
+                    cr, cp, cq, ct = d_extra[4 * k:4 * k + 4]
+                    a = ch["q0"]
+                    calls.append(rx.extend_attention_call(
+                        self.pool, layer, q[a:], wl.num_q_heads, d_tab, cr, cp, cq, ct,
+                        len(ch["rows"]), ch["n_tiles"], self.scale, out[a:], lse[a:],
+                        self.stream))
             ev = self._event_start()
-            call()
+            for call in calls:
+                call()
             self._event_end(ev, "extend", flops)
-            self.gpu_launches += 2
+            self.gpu_launches += 1 + len(calls)
             outs[layer] = (out, lse)
         if self.on_extend is not None:
             self.on_extend(self.batch_no, [r.rid for r in reqs], prefix.copy(), qo, outs)

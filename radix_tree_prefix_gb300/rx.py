@@ -110,6 +110,9 @@ _SIGS = {
     "rx_alloc_steps": [P, I64, I32, P],
     "rx_alloc_decode_steps": [P, I32, I32, P, P, P],
     "rx_schedule": [P, I32, I32, P, P, P],
+    "rx_verify_rows": [I32, P, P, I64, P, P, P, P, I64, P, P],
+    "rx_verify_attention": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P, SZ, P],
+    "rx_kv_copy": [P, P, P, P, I64, P],
     "rx_kv_store": [P, I32, P, P, P, I64, P],
     "rx_req_to_token_write": [P, I64, I64, P, P, P, I64, P],
     "rx_extend_plan": [P, I32, I32, I32, I32, P, P],
@@ -451,6 +454,34 @@ def decode_steps(pool, layer, hq, d_table, steps, B, scale, d_workspace, stream=
     _check(_lib.rx_decode_steps(C.byref(pool), layer, hq, d_table.data_ptr(), d_table.shape[1],
                                 ptr, len(steps), B, scale, d_workspace.data_ptr(),
                                 d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
+
+
+def verify_rows(prefix_len, prefix_rows, draft_indptr, parents, draft_slots, out_stride):
+    """rx_verify_rows: (rows int32 [N, out_stride], ctx_len [N], positions [N])."""
+    pl, pr = _i32(prefix_len), _i32(prefix_rows)
+    di, par, ds = _i64(draft_indptr), _i32(parents), _i32(draft_slots)
+    R, N = len(pl), len(par)
+    rows = np.zeros((max(1, N), out_stride), dtype=np.int32)
+    ctx = np.empty(max(1, N), dtype=np.int32)
+    pos = np.empty(max(1, N), dtype=np.int32)
+    _check(_lib.rx_verify_rows(R, _p(pl), _p(pr), pr.shape[1] if pr.ndim == 2 else 0, _p(di),
+                               _p(par), _p(ds), _p(rows), int(out_stride), _p(ctx), _p(pos)))
+    return rows[:N], ctx[:N], pos[:N]
+
+
+def verify_attention(pool, layer, d_q, hq, d_table, d_plan, info, N, scale, d_out, d_lse,
+                     d_workspace, stream=None):
+    _check(_lib.rx_verify_attention(C.byref(pool), layer, d_q.data_ptr(), hq, d_table.data_ptr(),
+                                    d_table.shape[1], d_plan.data_ptr(), C.byref(info), N, scale,
+                                    d_out.data_ptr(), d_lse.data_ptr(), d_workspace.data_ptr(),
+                                    d_workspace.numel() * d_workspace.element_size(),
+                                    _stream(stream)))
+
+
+def kv_copy(src_pool, dst_pool, d_src_slots, d_dst_slots, stream=None):
+    """rx_kv_copy between (or within) pools given as rx_pool_desc."""
+    _check(_lib.rx_kv_copy(C.byref(src_pool), C.byref(dst_pool), d_src_slots.data_ptr(),
+                           d_dst_slots.data_ptr(), d_src_slots.numel(), _stream(stream)))
 
 
 def decode_attention_static(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_out, d_lse,

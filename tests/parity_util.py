@@ -13,7 +13,7 @@ MEAN_ABS = 1e-3
 
 class DeviceRun:
     def __init__(self, wl, layers=None, sample=None, extend_tokens=None, decode_steps=None,
-                 check_bookkeeping=True, values_fn=None, policy="fcfs"):
+                 check_bookkeeping=True, values_fn=None, policy="fcfs", chunk_tokens=None):
         import torch
 
         from radix_tree_prefix_gb300 import rx, workloads
@@ -34,7 +34,7 @@ class DeviceRun:
         self.rng = np.random.default_rng(123)
         eng = Engine(wl, device=self.dev, inputs=GatherInputs(wl, self.vals, self.layers),
                      layers=self.layers, on_extend=self._on_extend, on_decode=self._on_decode,
-                     policy=policy)
+                     policy=policy, chunk_tokens=chunk_tokens)
         self.trace = eng.run()
         torch.cuda.synchronize()
         self.flags = rx.device_check()

@@ -296,3 +296,16 @@ def test_scheduled_fork_tree_parity(policy):
     run = DeviceRun(wl, policy=policy)
     run.assert_close()
     assert len(run.trace.eviction_log) > 0
+
+
+@pytest.mark.parametrize("name,chunk", [("agent_small", 37), ("chat_d256", 100),
+                                        ("long_shared_small", 256), ("nested_share", 1000)])
+def test_chunked_extend_parity(name, chunk):
+    """Chunked prefill: every extend batch's queries in launches of at most
+    `chunk` query tokens (suffixes split across launches, ragged last
+    chunk): outputs within tolerance of the fp64 oracle, bookkeeping
+    unchanged."""
+    wl = SMALL[name][0]()
+    run = DeviceRun(wl, chunk_tokens=chunk)
+    run.assert_close()
+    assert run.engine.gpu_launches > 0

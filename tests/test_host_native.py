@@ -558,3 +558,33 @@ def test_scheduled_request_flow_matches_oracle(policy, page_size):
                               page_size=page_size)
     # shuffled arrivals: the cache-aware order prefills no more than arrival order
     assert got.prefilled <= fcfs.prefilled
+
+
+# ------------------------------------------------------- draft-tree rows
+def test_verify_rows_follow_the_tree():
+    """Each draft's row is its request's context then its root path (root
+    first, itself last); context length and position follow its depth."""
+    from oracle import speculative as ospec
+    rng = random.Random(12)
+    prefix_len = [5, 0, 9]
+    stride = 12
+    prefix_rows = np.zeros((3, stride), dtype=np.int32)
+    for r, p in enumerate(prefix_len):
+        prefix_rows[r, :p] = rng.sample(range(100, 200), p)
+    trees = [[-1, 0, 0, 1, 3, -1], [-1], [-1, 0, 1, 2]]
+    indptr = np.cumsum([0] + [len(t) for t in trees]).astype(np.int64)
+    parents = np.concatenate([np.array(t, dtype=np.int32) for t in trees])
+    slots = np.arange(500, 500 + len(parents), dtype=np.int32)
+    rows, ctx, pos = rx.verify_rows(prefix_len, prefix_rows, indptr, parents, slots, 20)
+    for r, tree in enumerate(trees):
+        p = prefix_len[r]
+        for li in range(len(tree)):
+            i = indptr[r] + li
+            path = [slots[indptr[r] + j] for j in ospec.ancestors_and_self(tree, li)]
+            want = list(prefix_rows[r, :p]) + path
+            assert rows[i, :len(want)].tolist() == want
+            assert ctx[i] == len(want) and pos[i] == ospec.positions(p, tree)[li]
+    with pytest.raises(rx.RxError):
+        rx.verify_rows([2], prefix_rows[:1], [0, 2], [-1, 1], [1, 2], 20)   # parent not before
+    with pytest.raises(rx.RxError):
+        rx.verify_rows([9], prefix_rows[:1], [0, 4], [-1, 0, 1, 2], [1, 2, 3, 4], 12)  # too long
