@@ -33,7 +33,11 @@ Readings of the pages where they leave a step open:
   prompts in consecutive batches), the request's own slots for that part are
   freed and its row takes the tree's slots, which hold the same K/V;
 * finish is ``insert(prompt + outputs)`` then unlock of the prompt's node; slots
-  of any part that another request had already inserted are freed.
+  of any part that another request had already inserted are freed;
+* with a host tier (``oracle/hicache.py``): before a batch matches and locks,
+  each member in order matches across both tiers and brings a prefix that is
+  resident on the host only back to the device; after a wave's finishes,
+  each finished sequence's path is written through to the host.
 
 With pages of more than one slot (keys page-aligned, "SGLang: the tree, and
 the language nobody remembers", section "A tree, not a map"), the readings
@@ -58,7 +62,8 @@ counts of the nested example; 2,800 of 3,000 reused at agent step 5).
 """
 
 from . import scheduler
-from .radix_cache import RadixCache, common_prefix_length
+from .hicache import TwoTierRadixCache
+from .radix_cache import NoSpace, RadixCache, common_prefix_length
 
 
 class Trace:
@@ -71,6 +76,9 @@ class Trace:
         self.prefilled = 0
         self.eviction_log = []
         self.stats = {}
+        self.loads = []          # per load from the host tier: (rid, host slots, device slots)
+        self.backups = []        # per finish with a host tier: (rid, device slots, host slots)
+        self.host_eviction_log = []
 
     def as_tuple(self):
         return (
@@ -79,6 +87,9 @@ class Trace:
             list(self.finishes),
             self.prefilled,
             list(self.eviction_log),
+            [(rid, tuple(h), tuple(d)) for rid, h, d in self.loads],
+            [(rid, tuple(d), tuple(h)) for rid, d, h in self.backups],
+            list(self.host_eviction_log),
         )
 
 
@@ -114,7 +125,7 @@ def plan_batches(cache, wave_prompts, policy="fcfs"):
 
 
 def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
-                    on_decode=None, page_size=1, policy="fcfs"):
+                    on_decode=None, page_size=1, policy="fcfs", host_slots=0):
     """Run the request flow over a fresh oracle cache.
 
     waves: list of waves; a wave is a list of ``(rid, prompt, outputs)`` with
@@ -123,7 +134,9 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
     ``on_decode(step, rows)`` are optional callbacks for attention checks.
     Returns ``(trace, cache)``.
     """
-    cache = RadixCache(num_slots, page_size)
+    tiered = host_slots > 0
+    cache = (TwoTierRadixCache(num_slots, host_slots, page_size) if tiered
+             else RadixCache(num_slots, page_size))
     ps = page_size
     trace = Trace()
     for wave in waves:
@@ -134,6 +147,16 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
         for batch in plan_batches(cache, prompts, policy):
             served += batch
             matched = []
+            if tiered:
+                # a prefix resident on the host only comes back to the device
+                # instead of being prefilled: members in order, before the
+                # batch matches and locks
+                for j in batch:
+                    _, _, host_len, host_node = cache.match_prefix_tiers(
+                        prompts[j][:len(prompts[j]) - 1])
+                    if host_len:
+                        hs, ds = cache.load_onboard(host_node)
+                        trace.loads.append((wave[j][0], hs, ds))
             for j in batch:
                 rid, prompt, _ = wave[j]
                 slots, node = cache.match_prefix(prompts[j][:len(prompts[j]) - 1])
@@ -177,16 +200,33 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
             trace.decode_steps.append(step_rec)
             if on_decode is not None:
                 on_decode(step, {rid: list(rows[rid]) for rid, _, _ in wave})
+        finished = []
         for rid, prompt, outputs in wave:
             full = list(prompt) + list(outputs[:decode_steps])
-            already, _ = cache.insert(full, rows[rid])
+            already, full_node = cache.insert(full, rows[rid])
+            finished.append((rid, full_node))
             if already > cache.aligned(len(prompt)):
                 cache.free(rows[rid][cache.aligned(len(prompt)):already])
             if cache.aligned(len(full)) < len(full):      # the partly filled last page
                 cache.free(rows[rid][cache.aligned(len(full)):])
             trace.finishes.append((rid, already))
             cache.dec_lock_ref(prompt_nodes[rid])
+        if tiered:
+            # write-through: every finished sequence's path is backed up to
+            # the host tier, in order, each committed at once (the copy is
+            # stream-ordered before any later load of it); a backup the host
+            # tier cannot hold is skipped
+            for rid, full_node in finished:
+                try:
+                    ticket, ds, hs = cache.write_through(full_node)
+                except NoSpace:
+                    ticket, ds, hs = 0, [], []
+                if ticket:
+                    cache.commit_write_through(ticket, True)
+                trace.backups.append((rid, ds, hs))
     trace.eviction_log = list(cache.eviction_log)
+    if tiered:
+        trace.host_eviction_log = list(cache.host_eviction_log)
     trace.stats = {
         "cached": cache.cached_size(),
         "evictable": cache.evictable_size_,

@@ -89,8 +89,8 @@ MUTANTS = {
     "store_into_layer_0": ("pool.py", [
         ("out[layer, h, int(s), :] = kv[i, h, :]", "out[0, h, int(s), :] = kv[i, h, :]")]),
     "finish_drops_outputs": ("harness.py", [
-        ("already, _ = cache.insert(full, rows[rid])",
-         "already, _ = cache.insert(list(prompt), rows[rid][:len(prompt)])")]),
+        ("already, full_node = cache.insert(full, rows[rid])",
+         "already, full_node = cache.insert(list(prompt), rows[rid][:len(prompt)])")]),
     "decode_tokens_inserted_each_step": ("harness.py", [
         ("            for (rid, _, _), s in zip(wave, slots):\n"
          "                rows[rid].append(s)\n",
@@ -156,6 +156,24 @@ MUTANTS = {
         ("    rows = [np.array(pool[:, :, int(s), :], copy=True) for s in src]\n"
          "    for t, r in zip(tgt, rows):\n        out[:, :, int(t), :] = r\n",
          "    for t, s in zip(tgt, src):\n        out[:, :, int(t), :] = out[:, :, int(s), :]\n")]),
+    "tier_eviction_drops_host_copy": ("hicache.py", [
+        ("            if self.on_host(victim):\n                victim.value = None\n",
+         "            if False:\n                victim.value = None\n")]),
+    "tier_match_counts_host_as_device": ("hicache.py", [
+        ("            if self.on_gpu(n) and host_len == 0:", "            if host_len == 0:")]),
+    "tier_failed_commit_keeps_backup": ("hicache.py", [
+        ("                if success:\n                    x.host_value = x.pending[1]\n",
+         "                if True:\n                    x.host_value = x.pending[1]\n")]),
+    "tier_host_eviction_ignores_children": ("hicache.py", [
+        ("                if n is not self.root and not self.on_gpu(n) and self.on_host(n)\n"
+         "                and not n.children]",
+         "                if n is not self.root and not self.on_gpu(n) and self.on_host(n)]")]),
+    "tier_insert_skips_host_only_nodes": ("hicache.py", [
+        ("                x.value = slots[off:off + len(x.key)]\n",
+         "                pass\n")]),
+    "tier_device_leaf_ignores_host_children": ("hicache.py", [
+        ("        return [c for c in node.children.values() if self.on_gpu(c)]",
+         "        return list(node.children.values())")]),
     "dfs_weight_without_subtree": ("scheduler.py", [
         ("            w += cw\n", "")]),
     "match_whole_prompt": ("harness.py", [

@@ -16,6 +16,7 @@ from oracle import attention as oatt
 from oracle import scheduler as oscheduler
 from oracle import speculative as ospec
 from oracle.harness import run_bookkeeping
+from oracle.hicache import TwoTierRadixCache
 from oracle.radix_cache import NoSpace, RadixCache, StateError
 from radix_tree_prefix_gb300 import workloads
 
@@ -1008,3 +1009,240 @@ def test_chunked_extend_equals_unchunked():
             b = min(n - p, a + chunk)
             o, l = oatt.extend_attention(q[a:b], k[:p + b], v[:p + b], p + a)
             assert np.array_equal(o, full_o[a:b]) and np.array_equal(l, full_l[a:b])
+
+
+# ---------------------------------------------------------- two-tier cache
+def _tt_conservation(cache, private_pages=()):
+    """Device-resident and host-resident nodes each hang from the root; every
+    device page and every host page is held by one tree position, the free
+    list or a pending backup, exactly once."""
+    ps = cache.page_size
+    dev, host = [], []
+    for n in cache.nodes.values():
+        if n is cache.root:
+            continue
+        assert cache.on_gpu(n) or cache.on_host(n), "node on neither tier"
+        if cache.on_gpu(n):
+            assert cache.on_gpu(n.parent), "device residency not top-connected"
+            dev += [s // ps for s in n.value[::ps]]
+        if cache.on_host(n):
+            assert cache.on_host(n.parent), "host residency not top-connected"
+            host += [s // ps for s in n.host_value[::ps]]
+        if n.pending is not None:
+            host += [s // ps for s in n.pending[1][::ps]]
+    assert sorted(dev + list(cache.free_pages) + list(private_pages)) == \
+        list(range(1, cache.num_slots // ps))
+    assert sorted(host + list(cache.free_host_pages)) == list(range(1, cache.host_slots // ps))
+
+
+def test_two_tier_without_backups_equals_single_tier():
+    """While nothing is written through, the two-tier cache makes every
+    decision of the single-tier cache (random operations)."""
+    rng = random.Random(23)
+    for trial in range(40):
+        n_slots = rng.randint(16, 70)
+        a, b = RadixCache(n_slots), TwoTierRadixCache(n_slots, 64)
+        la, lb = [], []
+        for step in range(100):
+            seq = [rng.randrange(3) for _ in range(rng.randint(1, 12))]
+            r = rng.random()
+            if r < 0.55:
+                sa, na = a.match_prefix(seq[:-1])
+                sb, nb = b.match_prefix(seq[:-1])
+                assert sa == sb and na.id == nb.id
+                a.inc_lock_ref(na)
+                b.inc_lock_ref(nb)
+                try:
+                    xa = a.alloc(len(seq) - len(sa))
+                except NoSpace:
+                    xa = None
+                try:
+                    xb = b.alloc(len(seq) - len(sb))
+                except NoSpace:
+                    xb = None
+                assert xa == xb and a.eviction_log == b.eviction_log
+                if xa is None:
+                    a.dec_lock_ref(na)
+                    b.dec_lock_ref(nb)
+                    continue
+                ka, ma = a.insert(seq, sa + xa)
+                kb, mb = b.insert(seq, sb + xb)
+                assert ka == kb and ma.id == mb.id
+                a.free((sa + xa)[len(sa):ka])
+                b.free((sb + xb)[len(sb):kb])
+                a.inc_lock_ref(ma)
+                b.inc_lock_ref(mb)
+                a.dec_lock_ref(na)
+                b.dec_lock_ref(nb)
+                la.append(ma)
+                lb.append(mb)
+            elif r < 0.8 and la:
+                i = rng.randrange(len(la))
+                a.dec_lock_ref(la.pop(i))
+                b.dec_lock_ref(lb.pop(i))
+            else:
+                k = rng.randint(1, 9)
+                assert a.evict(k) == b.evict(k)
+            assert (a.evictable_size_, a.protected_size_) == (b.evictable_size_, b.protected_size_)
+            assert list(a.free_pages) == list(b.free_pages)
+
+
+def test_worked_example_with_a_host_tier():
+    """"Worked example, step by step": C locked, D arrives, A (used longest
+    ago) leaves the device.  With every branch written through to a host
+    tier, A stays on the host; when user A returns, A's 900 tokens come back
+    from the host (900 host-matched tokens, one load) instead of being
+    prefilled, and the unlocked B leaves the device to make room."""
+    g = _golden_kv("worked_eviction.txt")
+    cache = TwoTierRadixCache(g["capacity"] + 1, 8192)
+    rng = random.Random(7)
+    seq = lambda n: [rng.randrange(32000) for _ in range(n)]
+    s = seq(g["S"])
+    branch = {b: seq(g[b]) for b in "ABC"}
+    nodes = {}
+    for b in "ABC":
+        toks = s + branch[b]
+        slots, _ = cache.match_prefix(toks)
+        _, nodes[b] = cache.insert(toks, slots + cache.alloc(len(toks) - len(slots)))
+        t, dev, host = cache.write_through(nodes[b])
+        cache.commit_write_through(t, True)
+    assert cache.host_cached_size() == g["S"] + g["A"] + g["B"] + g["C"]
+    cache.inc_lock_ref(nodes["C"])
+    d = s + seq(g["D_new"])
+    slots, dnode = cache.match_prefix(d[:-1])
+    cache.inc_lock_ref(dnode)
+    new = cache.alloc(g["D_new"])
+    _, dn = cache.insert(d, slots + new)
+    cache.inc_lock_ref(dn)
+    cache.dec_lock_ref(dnode)
+    assert cache.eviction_log == [(nodes["A"].id, g["A"])]
+    assert cache.device_cached_size() == 3500 and not cache.on_gpu(nodes["A"])
+    assert cache.on_host(nodes["A"])
+    # user A comes back with 100 new tokens
+    a2 = s + branch["A"] + seq(100)
+    slots, dev_node, host_len, host_node = cache.match_prefix_tiers(a2[:-1])
+    assert len(slots) == g["S"] and host_len == g["A"] and host_node is nodes["A"]
+    host_slots, dev_slots = cache.load_onboard(host_node)
+    assert host_slots == nodes["A"].host_value and len(dev_slots) == g["A"]
+    assert cache.eviction_log[-1] == (nodes["B"].id, g["B"])
+    slots, node = cache.match_prefix(a2[:-1])
+    assert len(slots) == g["S"] + g["A"]          # only 100 - 1 + 1 tokens left to prefill
+    _tt_conservation(cache)
+
+
+def test_two_tier_random_operations_keep_invariants():
+    """Random matches, loads, inserts, write-throughs (committed with success
+    or failure, or left pending across other operations), locks and
+    evictions on a small device pool and a small host pool: residency stays
+    top-connected on each tier, pages are conserved on each tier, locked
+    nodes never leave the device."""
+    rng = random.Random(29)
+    for trial in range(60):
+        ps = rng.choice([1, 2])
+        cache = TwoTierRadixCache(ps * rng.randint(12, 30), ps * rng.randint(6, 24), ps)
+        locks, pending, private = [], [], []
+        for step in range(120):
+            seq = [rng.randrange(3) for _ in range(rng.randint(1, 10))]
+            r = rng.random()
+            if r < 0.45:
+                _, _, host_len, host_node = cache.match_prefix_tiers(seq[:-1])
+                if host_len:
+                    try:
+                        cache.load_onboard(host_node)
+                    except NoSpace:
+                        pass
+                slots, node = cache.match_prefix(seq[:-1])
+                cache.inc_lock_ref(node)
+                before = {n.id for n in cache.nodes.values() if n.lock_ref > 0}
+                try:
+                    new = cache.alloc(len(seq) - len(slots))
+                except NoSpace:
+                    cache.dec_lock_ref(node)
+                    continue
+                for nid, _ in cache.eviction_log[-10:]:
+                    if nid in before and nid in cache.nodes:
+                        assert cache.on_gpu(cache.nodes[nid]) or cache.nodes[nid].lock_ref == 0
+                already, node2 = cache.insert(seq, slots + new)
+                cache.free((slots + new)[len(slots):already] +
+                           (slots + new)[cache.aligned(len(seq)):])
+                cache.inc_lock_ref(node2)
+                cache.dec_lock_ref(node)
+                locks.append(node2)
+            elif r < 0.6 and locks:
+                node = locks.pop(rng.randrange(len(locks)))
+                cache.dec_lock_ref(node)
+                try:
+                    t, _, _ = cache.write_through(node)
+                except NoSpace:
+                    t = 0
+                if t:
+                    pending.append(t)
+            elif r < 0.75 and pending:
+                cache.commit_write_through(pending.pop(rng.randrange(len(pending))),
+                                           rng.random() < 0.8)
+            else:
+                cache.evict(rng.randint(1, 8))
+            for n in locks:
+                walk = n
+                while walk is not cache.root:
+                    assert cache.on_gpu(walk), "a locked node left the device"
+                    walk = walk.parent
+            _tt_conservation(cache)
+
+
+def _round_robin_chat():
+    wl = workloads.multi_turn_chat(sessions=6, turns=4, system=64, user=24, decode_steps=8,
+                                   layers=1)
+    # one request per wave, sessions taking turns: a session's history has
+    # to survive five other sessions' turns to be reused
+    return [[r] for w in wl.oracle_waves() for r in w]
+
+
+def test_host_tier_saves_prefill_under_a_small_device_pool():
+    """A multi-turn chat whose device pool holds about two sessions'
+    histories: without a host tier most returning sessions find their
+    history evicted and prefill it again; with one, it comes back from the
+    host.  Every page is conserved on both tiers at the end."""
+    waves = _round_robin_chat()
+    single, _ = run_bookkeeping(waves, 400, 8)
+    tiered, cache = run_bookkeeping(waves, 400, 8, host_slots=4096)
+    assert tiered.prefilled < single.prefilled
+    assert len(tiered.loads) > 0 and len(tiered.backups) == len(waves)
+    loaded = sum(len(h) for _, h, _ in tiered.loads)
+    assert tiered.prefilled + loaded <= single.prefilled
+    _tt_conservation(cache)
+    # a small host tier evicts host-only leaves and still conserves pages
+    small, cache = run_bookkeeping(waves, 400, 8, host_slots=700)
+    assert len(small.host_eviction_log) > 0
+    assert small.prefilled <= single.prefilled
+    _tt_conservation(cache)
+
+
+def test_write_through_commit_outcomes():
+    """A committed backup makes the path resident on both tiers; a failed one
+    leaves it on the device only and returns every host page; a second
+    backup of an already backed-up path copies nothing; a backup below one
+    still in flight is refused until that one commits."""
+    cache = TwoTierRadixCache(200, 100)
+    a = list(range(1, 21))
+    _, na = cache.insert(a, cache.alloc(20))
+    free0 = len(cache.free_host_pages)
+    t, dev, host = cache.write_through(na)
+    assert t and len(dev) == len(host) == 20 and len(cache.free_host_pages) == free0 - 20
+    b = a[:10] + list(range(50, 60))
+    slots, _ = cache.match_prefix(b)
+    _, nb = cache.insert(b, slots + cache.alloc(10))      # splits a's node while in flight
+    assert cache.write_through(nb) == (0, [], [])           # refused: an ancestor is in flight
+    cache.commit_write_through(t, False)
+    assert not cache.on_host(na) and not cache.on_host(na.parent)
+    assert len(cache.free_host_pages) == free0 and cache.host_cached_size() == 0
+    t, dev, host = cache.write_through(nb)
+    assert len(dev) == 20                                   # the shared 10 and b's own 10
+    cache.commit_write_through(t, True)
+    assert cache.on_host(nb) and cache.on_host(nb.parent) and not cache.on_host(na)
+    assert cache.host_cached_size() == 20
+    assert cache.write_through(nb) == (0, [], [])           # nothing left to copy
+    t, dev, host = cache.write_through(na)
+    assert len(dev) == 10                                   # only a's own 10
+    cache.commit_write_through(t, True)
+    _tt_conservation(cache)
