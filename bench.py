@@ -138,6 +138,7 @@ class Clocks:
             self.proc = None
         self.t0 = None
         self.t1 = None
+        self.result = None
 
     def begin(self):
         self.t0 = time.time()
@@ -396,6 +397,7 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
     wall = time.perf_counter() - wall0
     if clocks is not None:
         clocks.end()
+        clocks.result = clocks.stop()      # the sampler does not run during the e2e leg
     if world > 1:
         dist.barrier()
     assert t.as_tuple() == trace.as_tuple(), "timed steps made different cache decisions"
@@ -429,17 +431,24 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        host_s, step_s = [], []
         t0 = time.perf_counter()
         for _ in range(steps):
             flush.zero_()
+            h0 = time.perf_counter()
             eng2.run()
+            host_s.append(time.perf_counter() - h0)
             torch.cuda.synchronize()
+            step_s.append(time.perf_counter() - h0)
         e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
         rx.device_check()
         out["e2e"] = {"value": job_rate(n_ext + n_dec, e2e_s, world), "unit": "query-tok/s",
                       "h2d_bytes_per_step": host.h2d_bytes // steps,
                       "d2h_bytes_per_step": ring.d2h_bytes // steps,
                       "ms_per_step": e2e_s * 1e3,
+                      "host_enqueue_ms_per_step": 1e3 * statistics.mean(host_s),
+                      "step_ms_min_median_max": [1e3 * min(step_s), 1e3 * statistics.median(step_s),
+                                                 1e3 * max(step_s)],
                       "copies": f"inputs from page-locked host memory up to {host.ring - 1} "
                                 f"batches ahead on a side stream; every output (fp32 o and lse) "
                                 f"read back through a ring of {ring.slots} device/host buffer "
@@ -535,7 +544,7 @@ def main(argv=None):
     wl = workloads.WORKLOADS[args.workload]()
     clocks = Clocks(local)          # started before warm-up: its start-up is not timed
     res = measure(wl, dev, args.steps, args.warmup, world, e2e=not args.no_e2e, clocks=clocks)
-    clk = clocks.stop()
+    clk = clocks.result
     torch.cuda.empty_cache()
     n_ext, n_dec = res["n_ext"], res["n_dec"]
     q_per_step = n_ext + n_dec

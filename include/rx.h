@@ -89,6 +89,8 @@ typedef struct rx_config {
                         page_size                                        */
   int32_t page_size; /* slots per page, >= 1 (1 = token granularity)     */
   int32_t reserved;  /* must be 0                                         */
+  int64_t host_slots;/* slots of the host tier including its pad page; 0
+                        = one tier; else a multiple of page_size          */
 } rx_config;
 
 typedef struct rx_stats_t {
@@ -100,6 +102,9 @@ typedef struct rx_stats_t {
   int64_t evicted_nodes;    /* since creation                              */
   int64_t evicted_tokens;   /* since creation                              */
   int64_t clock;            /* logical access clock                        */
+  int64_t host_cached_tokens; /* tokens resident on the host tier          */
+  int64_t host_free_slots;    /* slots on the host free list               */
+  int64_t host_evicted_nodes; /* nodes evicted from the host tier          */
 } rx_stats_t;
 
 typedef struct rx_evict_rec {
@@ -258,11 +263,13 @@ rx_status rx_extend_end(rx_cache* cache, int32_t R, const int32_t* tokens,
  * tokens/tok_indptr hold prompt ++ outputs and the row holds their slots;
  * the request's pages past the prompt's whole pages that another request
  * had already inserted, and its partly filled last page, are freed; then
- * rx_unlock(prompt_node[r]).  out_already[r] may be NULL. */
+ * rx_unlock(prompt_node[r]).  out_already[r] and out_full_node[r] (the node
+ * ending at the inserted sequence's last whole page) may be NULL. */
 rx_status rx_finish(rx_cache* cache, int32_t R, const int32_t* tokens,
                     const int64_t* tok_indptr, const int32_t* req_to_token,
                     int64_t row_stride, const int64_t* prompt_len,
-                    const rx_node* prompt_node, int64_t* out_already);
+                    const rx_node* prompt_node, int64_t* out_already,
+                    rx_node* out_full_node);
 
 /* In-batch prefix rule ([T] "The scheduler is where the cache is won or
  * lost") at token granularity: *out_conflict = 1 if the common prefix of
@@ -286,6 +293,90 @@ rx_status rx_batch_conflict(const int32_t* tokens, int64_t n,
 rx_status rx_batch_end(const rx_cache* cache, const int32_t* tokens,
                        const int64_t* indptr, int32_t start, int32_t R,
                        int32_t* out_end);
+
+/* ------------------------------------------------------------------------
+ * Two tiers: device pool + host pool ([T] "What the C++ tree is actually
+ * for": match_prefix returns the device indices, the host-matched length
+ * and a node per tier; writing_through / commit_writing_through; loading
+ * onboard).  With rx_config.host_slots > 0 a node holds device slots, host
+ * slots or both; the device-resident nodes hang from the root as a subtree,
+ * and so do the host-resident ones.  Device eviction (rx_evict, and every
+ * allocation) takes unlocked device leaves (no child on the device), least
+ * recent first: a node backed up on the host gives up its device slots and
+ * stays, a device-only node leaves the tree; the parent joins the
+ * candidates once it has no child on the device.  A backup that needs host
+ * pages evicts host-only childless nodes, least recent first.  The calls
+ * only decide slots; the caller copies KV between the pools (rx_kv_copy)
+ * in stream order before anything reads the destination.  With one tier
+ * every call below finds nothing to move.
+ * ---------------------------------------------------------------------- */
+
+/* Walk every tier as rx_match_prefix does (split, touch).  Writes the slots
+ * of the leading device-resident part of the match to out_slots, its length
+ * to *out_device_len and its last node to *out_device_node; *out_host_len =
+ * the tokens matched past it on the host only, *out_host_node = the last
+ * node matched (== device node when *out_host_len is 0). */
+rx_status rx_match_prefix_tiers(rx_cache* cache, const int32_t* tokens,
+                                int64_t n, int32_t* out_slots,
+                                int64_t* out_device_len, int64_t* out_host_len,
+                                rx_node* out_device_node,
+                                rx_node* out_host_node);
+
+/* Bring the host-only nodes of node's root path to the device: device pages
+ * are allocated for them (evicting as rx_alloc does, with the path's device
+ * part locked meanwhile) and they become resident on both tiers.  Writes
+ * the copies to make, host slot -> device slot, to out_host_slots /
+ * out_device_slots (capacity cap), *out_n = their number (0: nothing to
+ * load).  RX_ERR_NO_SPACE (nothing loaded) if the device cannot hold them. */
+rx_status rx_load_onboard(rx_cache* cache, rx_node node,
+                          int32_t* out_host_slots, int32_t* out_device_slots,
+                          int64_t cap, int64_t* out_n);
+
+/* Back up the device-only nodes of node's root path (which must be on the
+ * device) to the host: host pages are allocated for them (evicting host-only
+ * leaves if needed), node is locked until the commit, and the copies to
+ * make, device slot -> host slot, are written (capacity cap); *out_n = their
+ * number, *out_ticket = the ticket to commit.  *out_ticket = 0 and *out_n =
+ * 0 when there is nothing to copy or a backup of a node on the path is
+ * still in flight (retry after its commit).  RX_ERR_NO_SPACE if the host
+ * tier cannot hold the path (nothing changes). */
+rx_status rx_write_through(rx_cache* cache, rx_node node,
+                           int32_t* out_device_slots, int32_t* out_host_slots,
+                           int64_t cap, int64_t* out_n, int64_t* out_ticket);
+
+/* Resolve a write-through: success != 0 makes the path resident on both
+ * tiers; 0 returns its host pages.  The node is unlocked either way. */
+rx_status rx_commit_write_through(rx_cache* cache, int64_t ticket,
+                                  int32_t success);
+
+/* Batch step before rx_extend_begin: for each request in order, match its
+ * prompt without the last token across tiers and load a host-only remainder
+ * (rx_load_onboard; a load the device cannot hold is skipped and that part
+ * is prefilled).  Prompts as in rx_extend_begin.  Copies host slot ->
+ * device slot of every load, request after request, to out_host_slots /
+ * out_device_slots (capacity cap); *out_n = their number, out_counts[r] =
+ * request r's share. */
+rx_status rx_load_batch(rx_cache* cache, int32_t R, const int32_t* tokens,
+                        const int64_t* indptr, int32_t* out_host_slots,
+                        int32_t* out_device_slots, int64_t cap, int64_t* out_n,
+                        int64_t* out_counts);
+
+/* Batch step after rx_finish: rx_write_through of every node (in order,
+ * e.g. rx_finish's out_full_node), each committed with success at once (the
+ * caller's copies are stream-ordered before any later load); a backup the
+ * host tier cannot hold is skipped.  Copies device slot -> host slot to
+ * the output arrays (capacity cap); *out_n = their number, out_counts[r] =
+ * node r's share. */
+rx_status rx_write_through_batch(rx_cache* cache, int32_t R,
+                                 const rx_node* nodes,
+                                 int32_t* out_device_slots,
+                                 int32_t* out_host_slots, int64_t cap,
+                                 int64_t* out_n, int64_t* out_counts);
+
+/* Host-tier eviction records [start, start+cap); *out_total = their count. */
+rx_status rx_host_eviction_log(const rx_cache* cache, int64_t start,
+                               rx_evict_rec* out, int64_t cap,
+                               int64_t* out_total);
 
 /* ------------------------------------------------------------------------
  * Cache-aware scheduling ([T] "The scheduler is where the cache is won or

@@ -155,7 +155,10 @@ def run_bookkeeping(waves, num_slots, decode_steps, on_extend=None,
                     _, _, host_len, host_node = cache.match_prefix_tiers(
                         prompts[j][:len(prompts[j]) - 1])
                     if host_len:
-                        hs, ds = cache.load_onboard(host_node)
+                        try:
+                            hs, ds = cache.load_onboard(host_node)
+                        except NoSpace:          # no device room: prefilled instead
+                            continue
                         trace.loads.append((wave[j][0], hs, ds))
             for j in batch:
                 rid, prompt, _ = wave[j]

@@ -66,6 +66,14 @@ struct Node {
   int64_t lock_ref = 0;
   int64_t last_access_time = 0;
   int32_t priority = 0;
+  // Two-tier residency: device slots in `value` while `gpu`, host slots in
+  // `host_value` while `host`; a backup in flight holds its host slots in
+  // `pending_host` under ticket `pending_ticket`.
+  bool gpu = true;
+  bool host = false;
+  std::vector<int32_t> host_value;
+  int64_t pending_ticket = 0;
+  std::vector<int32_t> pending_host;
 };
 
 // Length of the common prefix of a[0..n) and b[0..n): gallop over windows
@@ -108,6 +116,21 @@ struct rx_cache {
   int64_t cached = 0;
   int64_t evicted_tokens = 0;
   std::vector<rx_evict_rec> evict_log;
+  // host tier (empty when host_slots is 0)
+  int64_t host_slots = 0;
+  std::deque<int32_t> host_free;  // free host pages
+  int64_t host_cached = 0;
+  std::vector<rx_evict_rec> host_evict_log;
+  std::unordered_map<int64_t, int64_t> tickets;  // ticket -> end node of the backup
+  int64_t next_ticket = 1;
+
+  bool on_gpu(const Node* x) const { return x == root || x->gpu; }
+  bool on_host(const Node* x) const { return x == root || x->host; }
+  bool has_gpu_child(const Node* x) const {
+    bool any = false;
+    for_children(x, [&](const Node* c) { any = any || c->gpu; });
+    return any;
+  }
 
   // ------------------------------------------------------------- pages
   int64_t aligned(int64_t n) const { return n - n % ps; }
@@ -193,12 +216,24 @@ struct rx_cache {
   // Split `node` after its first k tokens; returns the new upper node.
   Node* split(Node* node, int64_t k) {
     Node* parent = node->parent;
-    Node* upper = new_node(node->key.data(), node->value.data(), k, parent);
+    Node* upper = new_node(node->key.data(), node->value.data(), node->gpu ? k : 0, parent);
+    upper->key.assign(node->key.begin(), node->key.begin() + k);
     upper->lock_ref = node->lock_ref;
     upper->last_access_time = node->last_access_time;
+    upper->gpu = node->gpu;
+    if (node->host) {
+      upper->host = true;
+      upper->host_value.assign(node->host_value.begin(), node->host_value.begin() + k);
+      node->host_value.erase(node->host_value.begin(), node->host_value.begin() + k);
+    }
+    if (node->pending_ticket) {
+      upper->pending_ticket = node->pending_ticket;
+      upper->pending_host.assign(node->pending_host.begin(), node->pending_host.begin() + k);
+      node->pending_host.erase(node->pending_host.begin(), node->pending_host.begin() + k);
+    }
     set_child(parent, node->key.data(), upper);
     node->key.erase(node->key.begin(), node->key.begin() + k);
-    node->value.erase(node->value.begin(), node->value.begin() + k);
+    if (node->gpu) node->value.erase(node->value.begin(), node->value.begin() + k);
     node->parent = upper;
     set_child(upper, node->key.data(), node);
     return upper;
@@ -228,7 +263,7 @@ struct rx_cache {
     int64_t pos = 0;
     while (pos < n) {
       const Node* c = child_of(node, t + pos);
-      if (!c) break;
+      if (!c || !c->gpu) break;
       int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
       int64_t k = aligned(common_prefix(c->key.data(), t + pos, lim));
       std::memcpy(out + pos, c->value.data(), size_t(k) * sizeof(int32_t));
@@ -239,35 +274,51 @@ struct rx_cache {
     return pos;
   }
 
-  // Walk (splitting at the end of the match); returns the deepest node and
-  // the matched length; appends matched slots to `slots` if non-null.
+  // Walk every tier (splitting at the end of the match); returns the
+  // deepest node and the matched length; *dev_len / *dev_node = the leading
+  // device-resident part of the walk and its last node, whose slots are
+  // written to `slots` if non-null.
   Node* walk(const int32_t* t, int64_t n, int64_t* matched,
-             std::vector<Node*>* path, int32_t* slots) {
+             std::vector<Node*>* path, int32_t* slots, int64_t* dev_len = nullptr,
+             Node** dev_node = nullptr) {
     n = aligned(n);
     Node* node = root;
-    int64_t pos = 0;
+    Node* dnode = root;
+    int64_t pos = 0, dlen = 0;
+    bool dev_run = true;
     while (pos < n) {
       Node* c = child_of(node, t + pos);
       if (!c) break;
       int64_t lim = std::min<int64_t>(int64_t(c->key.size()), n - pos);
       int64_t k = aligned(common_prefix(c->key.data(), t + pos, lim));
       if (k < int64_t(c->key.size())) c = split(c, k);
-      if (slots) std::memcpy(slots + pos, c->value.data(), size_t(k) * sizeof(int32_t));
+      if (dev_run && c->gpu) {
+        if (slots) std::memcpy(slots + pos, c->value.data(), size_t(k) * sizeof(int32_t));
+        dlen += k;
+        dnode = c;
+      } else {
+        dev_run = false;
+      }
       pos += k;
       path->push_back(c);
       node = c;
     }
     *matched = pos;
+    if (dev_len) *dev_len = dlen;
+    if (dev_node) *dev_node = dnode;
     return node;
   }
 
+  // The device part of a match across tiers.
   Node* match_prefix(const int32_t* t, int64_t n, int32_t* slots,
                      int64_t* len) {
     clock += 1;
     std::vector<Node*> path;
-    Node* node = walk(t, n, len, &path, slots);
+    int64_t all = 0;
+    Node* dnode = root;
+    walk(t, n, &all, &path, slots, len, &dnode);
     for (Node* x : path) x->last_access_time = clock;
-    return node;
+    return dnode;
   }
 
   // Inserts the whole pages of t[0..n) (the key truncated to a multiple of
@@ -278,8 +329,19 @@ struct rx_cache {
     clock += 1;
     std::vector<Node*> path;
     int64_t pos = 0;
-    Node* node = walk(t, n, &pos, &path, nullptr);
-    *already = pos;
+    Node* node = walk(t, n, &pos, &path, nullptr, already);
+    // host-only nodes of the path adopt the caller's device slots
+    int64_t off = 0;
+    for (Node* x : path) {
+      const int64_t len = int64_t(x->key.size());
+      if (!x->gpu) {
+        x->value.assign(s + off, s + off + len);
+        x->gpu = true;
+        (x->lock_ref > 0 ? protected_ : evictable) += len;
+        cached += len;
+      }
+      off += len;
+    }
     if (pos < n) {
       Node* leaf = new_node(t + pos, s + pos, n - pos, node);
       set_child(node, t + pos, leaf);
@@ -331,7 +393,7 @@ struct rx_cache {
     while (!stack.empty()) {
       Node* x = stack.back();
       stack.pop_back();
-      if (x != root && childless(x) && x->lock_ref == 0)
+      if (x != root && x->gpu && !has_gpu_child(x) && x->lock_ref == 0)
         heap.push({x->priority, x->last_access_time, x->id, x});
       for_children(x, [&](Node* c) { stack.push_back(c); });
     }
@@ -340,7 +402,6 @@ struct rx_cache {
       Node* v = heap.top().node;
       heap.pop();
       Node* parent = v->parent;
-      erase_child(parent, v->key.data());
       for (size_t i = 0; i < v->value.size(); i += size_t(ps))
         free_list.push_back(int32_t(v->value[i] / ps));
       int64_t len = int64_t(v->key.size());
@@ -349,12 +410,73 @@ struct rx_cache {
       cached -= len;
       evicted_tokens += len;
       evict_log.push_back({v->id, len});
-      nodes.erase(v->id);
-      if (parent != root && childless(parent) && parent->lock_ref == 0)
+      if (v->host) {  // the host copy stays: the node leaves the device only
+        v->gpu = false;
+        v->value.clear();
+      } else {
+        erase_child(parent, v->key.data());
+        nodes.erase(v->id);
+      }
+      if (parent != root && parent->gpu && !has_gpu_child(parent) && parent->lock_ref == 0)
         heap.push({parent->priority, parent->last_access_time, parent->id,
                    parent});
     }
     return freed;
+  }
+
+  // Host eviction: host-only childless nodes, least recent first; their
+  // parent joins once childless and host-only.
+  int64_t host_evict(int64_t k) {
+    struct Cand {
+      int32_t priority;
+      int64_t time, id;
+      Node* node;
+      bool operator>(const Cand& o) const {
+        if (priority != o.priority) return priority > o.priority;
+        if (time != o.time) return time > o.time;
+        return id > o.id;
+      }
+    };
+    std::priority_queue<Cand, std::vector<Cand>, std::greater<Cand>> heap;
+    for (auto& kv : nodes) {
+      Node* x = kv.second.get();
+      if (x != root && !x->gpu && x->host && childless(x))
+        heap.push({x->priority, x->last_access_time, x->id, x});
+    }
+    int64_t freed = 0;
+    while (freed < k && !heap.empty()) {
+      Node* v = heap.top().node;
+      heap.pop();
+      Node* parent = v->parent;
+      for (size_t i = 0; i < v->host_value.size(); i += size_t(ps))
+        host_free.push_back(int32_t(v->host_value[i] / ps));
+      const int64_t len = int64_t(v->key.size());
+      freed += len;
+      host_cached -= len;
+      host_evict_log.push_back({v->id, len});
+      erase_child(parent, v->key.data());
+      nodes.erase(v->id);
+      if (parent != root && !parent->gpu && parent->host && childless(parent))
+        heap.push({parent->priority, parent->last_access_time, parent->id, parent});
+    }
+    return freed;
+  }
+
+  bool host_alloc_pages(int64_t n, int32_t* out) {
+    if (int64_t(host_free.size()) < n) host_evict((n - int64_t(host_free.size())) * ps);
+    if (int64_t(host_free.size()) < n) return false;
+    for (int64_t i = 0; i < n; ++i) {
+      out[i] = host_free.front();
+      host_free.pop_front();
+    }
+    return true;
+  }
+
+  std::vector<Node*> root_path(Node* x) const {
+    std::vector<Node*> p;
+    for (; x != root; x = x->parent) p.push_back(x);
+    std::reverse(p.begin(), p.end());
+    return p;
   }
 
   // k slots: the first k slots of ceil(k / page size) pages (all of them at
@@ -410,9 +532,14 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache** out) {
     return fail(RX_ERR_INVALID,
                 "rx_cache_create: page_size %d must be >= 1 and divide num_slots %lld",
                 cfg->page_size, (long long)cfg->num_slots);
+  if (cfg->host_slots < 0 || cfg->host_slots % cfg->page_size != 0)
+    return fail(RX_ERR_INVALID, "rx_cache_create: host_slots %lld not a multiple of page_size",
+                (long long)cfg->host_slots);
   auto* c = new rx_cache();
   c->num_slots = cfg->num_slots;
   c->ps = cfg->page_size;
+  c->host_slots = cfg->host_slots;
+  for (int64_t p = 1; p < cfg->host_slots / cfg->page_size; ++p) c->host_free.push_back(int32_t(p));
   auto root = std::make_unique<Node>();
   root->id = 0;
   c->root = root.get();
@@ -449,6 +576,8 @@ rx_status rx_match_prefix(rx_cache* c, const int32_t* tokens, int64_t n,
 rx_status rx_lock(rx_cache* c, rx_node node) {
   Node* x = c ? c->find(node) : nullptr;
   if (!x) return fail(RX_ERR_INVALID, "rx_lock: unknown node %lld", (long long)node);
+  for (Node* w = x; w != c->root; w = w->parent)
+    if (!w->gpu) return fail(RX_ERR_STATE, "rx_lock: node %lld not on the device", (long long)node);
   c->lock(x);
   return RX_OK;
 }
@@ -506,6 +635,9 @@ rx_status rx_stats(const rx_cache* c, rx_stats_t* out) {
   out->evicted_nodes = int64_t(c->evict_log.size());
   out->evicted_tokens = c->evicted_tokens;
   out->clock = c->clock;
+  out->host_cached_tokens = c->host_cached;
+  out->host_free_slots = int64_t(c->host_free.size()) * c->ps;
+  out->host_evicted_nodes = int64_t(c->host_evict_log.size());
   return RX_OK;
 }
 
@@ -623,7 +755,8 @@ rx_status rx_extend_end(rx_cache* c, int32_t R, const int32_t* tokens,
 rx_status rx_finish(rx_cache* c, int32_t R, const int32_t* tokens,
                     const int64_t* tok_indptr, const int32_t* req_to_token,
                     int64_t row_stride, const int64_t* prompt_len,
-                    const rx_node* prompt_node, int64_t* out_already) {
+                    const rx_node* prompt_node, int64_t* out_already,
+                    rx_node* out_full_node) {
   if (!c || R < 0 || !tok_indptr || (R && (!tokens || !req_to_token || !prompt_len ||
                                           !prompt_node)))
     return fail(RX_ERR_INVALID, "rx_finish: bad argument");
@@ -638,7 +771,8 @@ rx_status rx_finish(rx_cache* c, int32_t R, const int32_t* tokens,
     int64_t n = tok_indptr[r + 1] - tok_indptr[r];
     const int32_t* row = req_to_token + r * row_stride;
     int64_t already = 0;
-    c->insert(t, row, n, &already);
+    Node* full = c->insert(t, row, n, &already);
+    if (out_full_node) out_full_node[r] = full->id;
     // the request's own pages another request had already inserted, and the
     // partly filled page past the last whole one
     const int64_t p_al = c->aligned(prompt_len[r]);
@@ -1173,5 +1307,228 @@ extern "C" rx_status rx_verify_rows(int32_t R, const int32_t* prefix_len,
       if (out_positions) out_positions[i] = int32_t(p + depth[size_t(li)]);
     }
   }
+  return RX_OK;
+}
+
+// ------------------------------------------------------ two-tier transfers
+// "SGLang: the tree, and the language nobody remembers", section "What the
+// C++ tree is actually for": match across tiers with a node for each tier,
+// write-through tickets committed later, load-onboard of host-resident nodes.
+namespace {
+
+// Host pages for the device-only nodes of node's root path; the path stays
+// locked until the commit.  *ticket = 0 (nothing to copy) when the path is
+// on the host already or a backup on it is in flight.
+rx_status write_through_impl(rx_cache* c, Node* node, int32_t* out_dev, int32_t* out_host,
+                             int64_t cap, int64_t* out_n, int64_t* out_ticket) {
+  *out_n = 0;
+  *out_ticket = 0;
+  const std::vector<Node*> path = c->root_path(node);
+  for (const Node* x : path)
+    if (x->pending_ticket) return RX_OK;
+  int64_t n = 0;
+  for (const Node* x : path)
+    if (!x->host) n += int64_t(x->key.size());
+  if (n == 0) return RX_OK;
+  if (n > cap)
+    return fail(RX_ERR_INVALID, "rx_write_through: %lld tokens to copy, capacity %lld",
+                (long long)n, (long long)cap);
+  if (c->host_slots == 0) return fail(RX_ERR_NO_SPACE, "rx_write_through: no host tier");
+  std::vector<int32_t> pages(static_cast<size_t>(n / c->ps));
+  if (!c->host_alloc_pages(int64_t(pages.size()), pages.data()))
+    return fail(RX_ERR_NO_SPACE, "rx_write_through: %lld host slots needed, %lld free",
+                (long long)n, (long long)(int64_t(c->host_free.size()) * c->ps));
+  const int64_t ticket = c->next_ticket++;
+  int64_t pos = 0;
+  for (Node* x : path) {
+    if (x->host) continue;
+    const int64_t len = int64_t(x->key.size());
+    x->pending_ticket = ticket;
+    x->pending_host.resize(size_t(len));
+    c->page_slots(pages.data() + pos / c->ps, len, x->pending_host.data());
+    std::memcpy(out_dev + pos, x->value.data(), size_t(len) * sizeof(int32_t));
+    std::memcpy(out_host + pos, x->pending_host.data(), size_t(len) * sizeof(int32_t));
+    pos += len;
+  }
+  c->lock(node);
+  c->tickets[ticket] = node->id;
+  *out_n = n;
+  *out_ticket = ticket;
+  return RX_OK;
+}
+
+rx_status commit_impl(rx_cache* c, int64_t ticket, bool success) {
+  auto it = c->tickets.find(ticket);
+  if (it == c->tickets.end())
+    return fail(RX_ERR_INVALID, "rx_commit_write_through: unknown ticket %lld", (long long)ticket);
+  Node* node = c->find(it->second);
+  c->tickets.erase(it);
+  for (Node* x = node; x != c->root; x = x->parent) {
+    if (x->pending_ticket != ticket) continue;
+    if (success) {
+      x->host_value = std::move(x->pending_host);
+      x->host = true;
+      c->host_cached += int64_t(x->key.size());
+    } else {
+      for (size_t i = 0; i < x->pending_host.size(); i += size_t(c->ps))
+        c->host_free.push_back(int32_t(x->pending_host[i] / c->ps));
+    }
+    x->pending_host.clear();
+    x->pending_ticket = 0;
+  }
+  c->unlock(node);
+  return RX_OK;
+}
+
+// Device pages for the host-only nodes of node's root path (the path's
+// device part locked while allocating); they become resident on both tiers.
+rx_status load_impl(rx_cache* c, Node* node, int32_t* out_host, int32_t* out_dev, int64_t cap,
+                    int64_t* out_n) {
+  *out_n = 0;
+  const std::vector<Node*> path = c->root_path(node);
+  int64_t n = 0;
+  Node* dev_node = c->root;
+  bool dev_run = true;
+  for (Node* x : path) {
+    if (x->gpu && dev_run) {
+      dev_node = x;
+    } else {
+      dev_run = false;
+      if (!x->gpu) n += int64_t(x->key.size());
+    }
+  }
+  if (n == 0) return RX_OK;
+  if (n > cap)
+    return fail(RX_ERR_INVALID, "rx_load_onboard: %lld tokens to load, capacity %lld",
+                (long long)n, (long long)cap);
+  std::vector<int32_t> pages(static_cast<size_t>(n / c->ps));
+  c->lock(dev_node);
+  const bool ok = c->alloc_pages(int64_t(pages.size()), pages.data());
+  c->unlock(dev_node);
+  if (!ok)
+    return fail(RX_ERR_NO_SPACE, "rx_load_onboard: %lld device slots needed, %lld free",
+                (long long)n, (long long)(int64_t(c->free_list.size()) * c->ps));
+  int64_t pos = 0;
+  for (Node* x : path) {
+    if (x->gpu) continue;
+    const int64_t len = int64_t(x->key.size());
+    x->value.resize(size_t(len));
+    c->page_slots(pages.data() + pos / c->ps, len, x->value.data());
+    x->gpu = true;
+    c->evictable += len;
+    c->cached += len;
+    std::memcpy(out_host + pos, x->host_value.data(), size_t(len) * sizeof(int32_t));
+    std::memcpy(out_dev + pos, x->value.data(), size_t(len) * sizeof(int32_t));
+    pos += len;
+  }
+  *out_n = n;
+  return RX_OK;
+}
+
+}  // namespace
+
+extern "C" rx_status rx_match_prefix_tiers(rx_cache* c, const int32_t* tokens, int64_t n,
+                                           int32_t* out_slots, int64_t* out_device_len,
+                                           int64_t* out_host_len, rx_node* out_device_node,
+                                           rx_node* out_host_node) {
+  if (!c || (!tokens && n) || n < 0 || (!out_slots && n) || !out_device_len || !out_host_len ||
+      !out_device_node || !out_host_node)
+    return fail(RX_ERR_INVALID, "rx_match_prefix_tiers: bad argument");
+  c->clock += 1;
+  std::vector<Node*> path;
+  int64_t all = 0;
+  Node* dnode = c->root;
+  Node* last = c->walk(tokens, n, &all, &path, out_slots, out_device_len, &dnode);
+  for (Node* x : path) x->last_access_time = c->clock;
+  *out_host_len = all - *out_device_len;
+  *out_device_node = dnode->id;
+  *out_host_node = last->id;
+  return RX_OK;
+}
+
+extern "C" rx_status rx_load_onboard(rx_cache* c, rx_node node, int32_t* out_host_slots,
+                                     int32_t* out_device_slots, int64_t cap, int64_t* out_n) {
+  Node* x = c ? c->find(node) : nullptr;
+  if (!x || !out_n || (cap && (!out_host_slots || !out_device_slots)))
+    return fail(RX_ERR_INVALID, "rx_load_onboard: bad argument or unknown node");
+  return load_impl(c, x, out_host_slots, out_device_slots, cap, out_n);
+}
+
+extern "C" rx_status rx_write_through(rx_cache* c, rx_node node, int32_t* out_device_slots,
+                                      int32_t* out_host_slots, int64_t cap, int64_t* out_n,
+                                      int64_t* out_ticket) {
+  Node* x = c ? c->find(node) : nullptr;
+  if (!x || !out_n || !out_ticket || (cap && (!out_device_slots || !out_host_slots)))
+    return fail(RX_ERR_INVALID, "rx_write_through: bad argument or unknown node");
+  for (Node* w = x; w != c->root; w = w->parent)
+    if (!w->gpu) return fail(RX_ERR_STATE, "rx_write_through: path not on the device");
+  return write_through_impl(c, x, out_device_slots, out_host_slots, cap, out_n, out_ticket);
+}
+
+extern "C" rx_status rx_commit_write_through(rx_cache* c, int64_t ticket, int32_t success) {
+  if (!c) return fail(RX_ERR_INVALID, "rx_commit_write_through: NULL cache");
+  return commit_impl(c, ticket, success != 0);
+}
+
+extern "C" rx_status rx_load_batch(rx_cache* c, int32_t R, const int32_t* tokens,
+                                   const int64_t* indptr, int32_t* out_host_slots,
+                                   int32_t* out_device_slots, int64_t cap, int64_t* out_n,
+                                   int64_t* out_counts) {
+  if (!c || R < 0 || !indptr || (R && (!tokens || !out_counts)) || !out_n)
+    return fail(RX_ERR_INVALID, "rx_load_batch: bad argument");
+  *out_n = 0;
+  std::vector<Node*> path;
+  for (int32_t r = 0; r < R; ++r) {
+    out_counts[r] = 0;
+    const int64_t n = indptr[r + 1] - indptr[r];
+    if (n < 1) return fail(RX_ERR_INVALID, "rx_load_batch: empty prompt %d", r);
+    c->clock += 1;
+    path.clear();
+    int64_t all = 0, dlen = 0;
+    Node* dnode = c->root;
+    Node* last = c->walk(tokens + indptr[r], n - 1, &all, &path, nullptr, &dlen, &dnode);
+    for (Node* x : path) x->last_access_time = c->clock;
+    if (all == dlen) continue;
+    int64_t got = 0;
+    const rx_status st = load_impl(c, last, out_host_slots + *out_n, out_device_slots + *out_n,
+                                   cap - *out_n, &got);
+    if (st == RX_ERR_NO_SPACE) continue;  // prefilled instead
+    if (st != RX_OK) return st;
+    out_counts[r] = got;
+    *out_n += got;
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_write_through_batch(rx_cache* c, int32_t R, const rx_node* nodes,
+                                            int32_t* out_device_slots, int32_t* out_host_slots,
+                                            int64_t cap, int64_t* out_n, int64_t* out_counts) {
+  if (!c || R < 0 || (R && (!nodes || !out_counts)) || !out_n)
+    return fail(RX_ERR_INVALID, "rx_write_through_batch: bad argument");
+  *out_n = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    out_counts[r] = 0;
+    Node* x = c->find(nodes[r]);
+    if (!x) return fail(RX_ERR_INVALID, "rx_write_through_batch: unknown node %lld",
+                        (long long)nodes[r]);
+    int64_t got = 0, ticket = 0;
+    const rx_status st = write_through_impl(c, x, out_device_slots + *out_n,
+                                            out_host_slots + *out_n, cap - *out_n, &got, &ticket);
+    if (st == RX_ERR_NO_SPACE) continue;  // the host tier cannot hold it: not backed up
+    if (st != RX_OK) return st;
+    if (ticket) commit_impl(c, ticket, true);
+    out_counts[r] = got;
+    *out_n += got;
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_host_eviction_log(const rx_cache* c, int64_t start, rx_evict_rec* out,
+                                          int64_t cap, int64_t* out_total) {
+  if (!c || start < 0 || cap < 0 || (cap && !out))
+    return fail(RX_ERR_INVALID, "rx_host_eviction_log: bad argument");
+  const int64_t total = int64_t(c->host_evict_log.size());
+  for (int64_t i = 0; i < cap && start + i < total; ++i) out[i] = c->host_evict_log[start + i];
+  if (out_total) *out_total = total;
   return RX_OK;
 }

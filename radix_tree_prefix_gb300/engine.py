@@ -41,17 +41,24 @@ class Trace:
         self.prefilled = 0
         self.eviction_log = []
         self.stats = {}
+        self.loads = []          # per load from the host tier: (rid, host slots, device slots)
+        self.backups = []        # per written-through sequence: (rid, device slots, host slots)
+        self.host_eviction_log = []
 
     def as_tuple(self):
         steps = []
         for rec in self.decode_steps:
             steps.extend(rec.steps())
+        t = lambda a: tuple(int(x) for x in a)
         return (
             [[(rid, m, tuple(int(x) for x in row)) for rid, m, row in b] for b in self.batches],
             steps,
             list(self.finishes),
             self.prefilled,
             list(self.eviction_log),
+            [(rid, t(h), t(d)) for rid, h, d in self.loads],
+            [(rid, t(d), t(h)) for rid, d, h in self.backups],
+            list(self.host_eviction_log),
         )
 
 
@@ -482,6 +489,14 @@ class Engine:
     extend batch's queries into launches of at most that many query tokens,
     in query order: a request's suffix may span several chunks, and a chunk's
     part of it attends over the prefix plus the suffix tokens before it.
+    ``host_slots`` > 0 adds a host tier ("SGLang: the tree, and the language
+    nobody remembers", section "What the C++ tree is actually for"): a
+    page-locked host pool of that many slots; before each extend batch the
+    members' prefixes resident on the host only are loaded back into the
+    device pool (``rx_load_batch`` + ``rx_kv_copy``) instead of being
+    prefilled, and after each wave's finish every finished sequence is
+    written through to the host pool (``rx_write_through_batch`` +
+    ``rx_kv_copy``).
     With ``out_ring`` (an ``OutputRing``) every launch writes into the ring's
     next device buffer and the ring copies each buffer back to the host once
     the next launch takes a buffer (and at the end of a run); the tensors the
@@ -490,7 +505,8 @@ class Engine:
 
     def __init__(self, wl, device=None, inputs=None, layers=None, on_extend=None,
                  on_decode=None, stream=None, timing=False, on_decode_wave=None,
-                 reuse_outputs=False, out_ring=None, policy="fcfs", chunk_tokens=None):
+                 reuse_outputs=False, out_ring=None, policy="fcfs", chunk_tokens=None,
+                 host_slots=0):
         self.wl = wl
         self.device = device
         self.inputs = inputs
@@ -513,6 +529,7 @@ class Engine:
         self.out_ring = out_ring
         self.policy = policy
         self.chunk_tokens = chunk_tokens
+        self.host_slots = int(host_slots)
         self._out_bufs = {}
         self.kernel_events = []   # (kind, start event, end event, algorithmic work)
         if device is not None:
@@ -525,6 +542,11 @@ class Engine:
                                       device=device)
             self.v_pool = torch.empty_like(self.k_pool)
             self.pool = rx.pool_desc(self.k_pool, self.v_pool)
+            if self.host_slots:
+                self.hk_pool = torch.empty((L, hkv, self.host_slots, d), dtype=torch.bfloat16,
+                                           pin_memory=True)
+                self.hv_pool = torch.empty_like(self.hk_pool).pin_memory()
+                self.host_pool = rx.pool_desc(self.hk_pool, self.hv_pool)
             self.d_table = torch.zeros((self.max_wave, self.max_ctx), dtype=torch.int32,
                                        device=device)
             self.d_ws = torch.empty(0, dtype=torch.uint8, device=device)
@@ -545,7 +567,7 @@ class Engine:
 
     # ------------------------------------------------------------------ run
     def run(self):
-        self.cache = rx.RadixCache(self.wl.num_slots, self.wl.page_size)
+        self.cache = rx.RadixCache(self.wl.num_slots, self.wl.page_size, self.host_slots)
         self.trace = Trace()
         self.batch_no = 0
         self.step_no = 0
@@ -554,6 +576,8 @@ class Engine:
         if self.out_ring is not None and self.device is not None:
             self.out_ring.flush(self.stream)
         self.trace.eviction_log = self.cache.eviction_log()
+        if self.host_slots:
+            self.trace.host_eviction_log = self.cache.host_eviction_log()
         st = self.cache.stats()
         self.trace.stats = {
             "cached": st["cached_tokens"], "evictable": st["evictable_tokens"],
@@ -604,9 +628,21 @@ class Engine:
         if wl.decode_steps:
             self._decode_phase(wave, lens.astype(np.int32), prompt_nodes)
         # finish: insert prompt ++ outputs, unlock
-        already = self.cache.finish(full, findptr, self.h_table[:len(wave)], lens, prompt_nodes)
-        for r, a in zip(wave, already):
-            self.trace.finishes.append((r.rid, int(a)))
+        self._finish(wave, full, findptr, lens, prompt_nodes)
+
+    def _load_from_host(self, reqs, R, tokens_p, ind_p, cap):
+        """rx_load_batch for a batch's members and the copy of the loaded KV
+        from the host pool into the device pool."""
+        h, d, cnt = self.cache.load_batch_p(R, tokens_p, ind_p, cap)
+        pos = 0
+        for r, c in zip(reqs, cnt.tolist()):
+            if c:
+                self.trace.loads.append((r.rid, h[pos:pos + c].copy(), d[pos:pos + c].copy()))
+            pos += c
+        if self.device is not None and len(h):
+            d_src, d_dst = self.staging.upload([h, d])
+            rx.kv_copy(self.host_pool, self.pool, d_src, d_dst, self.stream)
+            self.gpu_launches += 1
 
     def _chunks(self, prefix, qo):
         """The batch's query rows [0, total) cut into consecutive chunks of at
@@ -673,9 +709,28 @@ class Engine:
         if wl.decode_steps:
             self._decode_phase(swave, slens.astype(np.int32), prompt_nodes)
         sfull, sfind = gather(served, full, findptr)
-        already = self.cache.finish(sfull, sfind, self.h_table[:R], slens, prompt_nodes)
-        for r, a in zip(swave, already):
+        self._finish(swave, sfull, sfind, slens, prompt_nodes)
+
+    def _finish(self, wave, full, findptr, lens, prompt_nodes):
+        """rx_finish of a wave (rows 0 .. len(wave)-1), then with a host tier
+        the write-through of every finished sequence and its copy to the
+        host pool."""
+        R = len(wave)
+        nodes = np.zeros(R, dtype=np.int64)
+        already = self.cache.finish(full, findptr, self.h_table[:R], lens, prompt_nodes, nodes)
+        for r, a in zip(wave, already):
             self.trace.finishes.append((r.rid, int(a)))
+        if not self.host_slots:
+            return
+        d, h, cnt = self.cache.write_through_batch(nodes, int(findptr[-1] - findptr[0]))
+        pos = 0
+        for r, c in zip(wave, cnt.tolist()):
+            self.trace.backups.append((r.rid, d[pos:pos + c].copy(), h[pos:pos + c].copy()))
+            pos += c
+        if self.device is not None and len(d):
+            d_src, d_dst = self.staging.upload([d, h])
+            rx.kv_copy(self.pool, self.host_pool, d_src, d_dst, self.stream)
+            self.gpu_launches += 1
 
     def _extend_batch(self, wave, j0, j1, indptr, ptrs, row0=0):
         """Requests j0 .. j1-1 of the wave as one extend batch.  ``indptr`` is
@@ -692,6 +747,8 @@ class Engine:
         table = self.h_table[r0:r0 + R]
         table_p = self._h_table_p + 4 * self.max_ctx * r0
         prefix_p, mnodes_p, new_p = self._b_ptrs
+        if self.host_slots:
+            self._load_from_host(reqs, R, tokens_p, ind_p, int(ind[-1] - ind[0]))
         total = self.cache.extend_begin_p(R, tokens_p, ind_p, table_p, self.max_ctx, prefix_p,
                                           mnodes_p, new_p)
         prefix = self._b_prefix[:R]

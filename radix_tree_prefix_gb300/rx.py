@@ -43,13 +43,15 @@ class StateError(RxError):
 
 
 class rx_config(C.Structure):
-    _fields_ = [("num_slots", C.c_int64), ("page_size", C.c_int32), ("reserved", C.c_int32)]
+    _fields_ = [("num_slots", C.c_int64), ("page_size", C.c_int32), ("reserved", C.c_int32),
+                ("host_slots", C.c_int64)]
 
 
 class rx_stats_t(C.Structure):
     _fields_ = [(n, C.c_int64) for n in (
         "cached_tokens", "evictable_tokens", "protected_tokens", "free_slots",
-        "num_nodes", "evicted_nodes", "evicted_tokens", "clock")]
+        "num_nodes", "evicted_nodes", "evicted_tokens", "clock", "host_cached_tokens",
+        "host_free_slots", "host_evicted_nodes")]
 
 
 class rx_evict_rec(C.Structure):
@@ -102,7 +104,14 @@ _SIGS = {
     "rx_node_depth": [P, I64, P],
     "rx_extend_begin": [P, I32, P, P, P, I64, P, P, P, P],
     "rx_extend_end": [P, I32, P, P, P, I64, P, P, P, P],
-    "rx_finish": [P, I32, P, P, P, I64, P, P, P],
+    "rx_finish": [P, I32, P, P, P, I64, P, P, P, P],
+    "rx_match_prefix_tiers": [P, P, I64, P, P, P, P, P],
+    "rx_load_onboard": [P, I64, P, P, I64, P],
+    "rx_write_through": [P, I64, P, P, I64, P, P],
+    "rx_commit_write_through": [P, I64, I32],
+    "rx_load_batch": [P, I32, P, P, P, P, I64, P, P],
+    "rx_write_through_batch": [P, I32, P, P, P, I64, P, P],
+    "rx_host_eviction_log": [P, I64, P, I64, P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_batch_end": [P, P, P, I32, I32, P],
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
@@ -174,13 +183,14 @@ def build_info():
 class RadixCache:
     """Owner of one native rx_cache (pages of `page_size` slots)."""
 
-    def __init__(self, num_slots, page_size=1):
-        cfg = rx_config(int(num_slots), int(page_size), 0)
+    def __init__(self, num_slots, page_size=1, host_slots=0):
+        cfg = rx_config(int(num_slots), int(page_size), 0, int(host_slots))
         h = C.c_void_p()
         _check(_lib.rx_cache_create(C.byref(cfg), C.byref(h)))
         self._h = h
         self.num_slots = int(num_slots)
         self.page_size = int(page_size)
+        self.host_slots = int(host_slots)
         self._i32 = C.c_int32()
         self._i64 = C.c_int64()
 
@@ -341,13 +351,88 @@ class RadixCache:
                                   C.byref(rew)))
         return out[:R], rew.value
 
-    def finish(self, tokens, tok_indptr, req_to_token, prompt_len, prompt_nodes):
+    def finish(self, tokens, tok_indptr, req_to_token, prompt_len, prompt_nodes, nodes_out=None):
+        """rx_finish; returns `already` per request (the nodes of the inserted
+        sequences go to nodes_out, int64 [R], when given)."""
         R = len(tok_indptr) - 1
         already = np.empty(max(1, R), dtype=np.int64)
         _check(_lib.rx_finish(self._h, R, _p(tokens), _p(tok_indptr), _p(req_to_token),
                               req_to_token.shape[1], _p(prompt_len), _p(prompt_nodes),
-                              _p(already)))
+                              _p(already), _p(nodes_out)))
         return already[:R]
+
+    # two tiers
+    def match_prefix_tiers(self, tokens):
+        """(device slots, device node, host_len, host node)."""
+        t = _i32(tokens)
+        slots = np.empty(max(1, len(t)), dtype=np.int32)
+        dl, hl, dn, hn = C.c_int64(), C.c_int64(), C.c_int64(), C.c_int64()
+        _check(_lib.rx_match_prefix_tiers(self._h, _p(t), len(t), _p(slots), C.byref(dl),
+                                          C.byref(hl), C.byref(dn), C.byref(hn)))
+        return slots[:dl.value].copy(), dn.value, hl.value, hn.value
+
+    def load_onboard(self, node, cap):
+        """(host slots, device slots) of the copies to make."""
+        h = np.empty(max(1, cap), dtype=np.int32)
+        d = np.empty(max(1, cap), dtype=np.int32)
+        n = C.c_int64()
+        _check(_lib.rx_load_onboard(self._h, int(node), _p(h), _p(d), int(cap), C.byref(n)))
+        return h[:n.value], d[:n.value]
+
+    def write_through(self, node, cap):
+        """(ticket, device slots, host slots)."""
+        d = np.empty(max(1, cap), dtype=np.int32)
+        h = np.empty(max(1, cap), dtype=np.int32)
+        n, t = C.c_int64(), C.c_int64()
+        _check(_lib.rx_write_through(self._h, int(node), _p(d), _p(h), int(cap), C.byref(n),
+                                     C.byref(t)))
+        return t.value, d[:n.value], h[:n.value]
+
+    def commit_write_through(self, ticket, success):
+        _check(_lib.rx_commit_write_through(self._h, int(ticket), 1 if success else 0))
+
+    def load_batch(self, tokens, indptr, cap):
+        """(host slots, device slots, per-request counts) of a batch's loads."""
+        t, ip = _i32(tokens), _i64(indptr)
+        R = len(ip) - 1
+        h = np.empty(max(1, cap), dtype=np.int32)
+        d = np.empty(max(1, cap), dtype=np.int32)
+        cnt = np.empty(max(1, R), dtype=np.int64)
+        n = C.c_int64()
+        _check(_lib.rx_load_batch(self._h, R, _p(t), _p(ip), _p(h), _p(d), int(cap), C.byref(n),
+                                  _p(cnt)))
+        return h[:n.value], d[:n.value], cnt[:R]
+
+    def load_batch_p(self, R, tokens_p, indptr_p, cap):
+        """rx_load_batch with the prompts given by address (see the pointer
+        forms of the batch steps)."""
+        h = np.empty(max(1, cap), dtype=np.int32)
+        d = np.empty(max(1, cap), dtype=np.int32)
+        cnt = np.empty(max(1, R), dtype=np.int64)
+        _check(_lib.rx_load_batch(self._h, int(R), tokens_p, indptr_p, _p(h), _p(d), int(cap),
+                                  C.byref(self._i64), _p(cnt)))
+        n = self._i64.value
+        return h[:n], d[:n], cnt[:R]
+
+    def write_through_batch(self, nodes, cap):
+        """(device slots, host slots, per-node counts) of the backups."""
+        nd = _i64(nodes)
+        R = len(nd)
+        d = np.empty(max(1, cap), dtype=np.int32)
+        h = np.empty(max(1, cap), dtype=np.int32)
+        cnt = np.empty(max(1, R), dtype=np.int64)
+        n = C.c_int64()
+        _check(_lib.rx_write_through_batch(self._h, R, _p(nd), _p(d), _p(h), int(cap),
+                                           C.byref(n), _p(cnt)))
+        return d[:n.value], h[:n.value], cnt[:R]
+
+    def host_eviction_log(self):
+        total = C.c_int64()
+        _check(_lib.rx_host_eviction_log(self._h, 0, None, 0, C.byref(total)))
+        n = total.value
+        recs = (rx_evict_rec * max(1, n))()
+        _check(_lib.rx_host_eviction_log(self._h, 0, recs, n, C.byref(total)))
+        return [(recs[i].node_id, recs[i].num_tokens) for i in range(n)]
 
     def plan_decode(self, prompt_nodes, ctx_len, req_rows, hq, hkv, d, plan=None, n_steps=None):
         """rx_plan_decode, or rx_plan_decode_steps when n_steps is given."""

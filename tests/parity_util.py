@@ -13,7 +13,8 @@ MEAN_ABS = 1e-3
 
 class DeviceRun:
     def __init__(self, wl, layers=None, sample=None, extend_tokens=None, decode_steps=None,
-                 check_bookkeeping=True, values_fn=None, policy="fcfs", chunk_tokens=None):
+                 check_bookkeeping=True, values_fn=None, policy="fcfs", chunk_tokens=None,
+                 host_slots=0):
         import torch
 
         from radix_tree_prefix_gb300 import rx, workloads
@@ -34,14 +35,15 @@ class DeviceRun:
         self.rng = np.random.default_rng(123)
         eng = Engine(wl, device=self.dev, inputs=GatherInputs(wl, self.vals, self.layers),
                      layers=self.layers, on_extend=self._on_extend, on_decode=self._on_decode,
-                     policy=policy, chunk_tokens=chunk_tokens)
+                     policy=policy, chunk_tokens=chunk_tokens, host_slots=host_slots)
         self.trace = eng.run()
         torch.cuda.synchronize()
         self.flags = rx.device_check()
         self.engine = eng
         if check_bookkeeping:
             want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
-                                      page_size=wl.page_size, policy=policy)
+                                      page_size=wl.page_size, policy=policy,
+                                      host_slots=host_slots)
             assert self.trace.as_tuple() == want.as_tuple(), "bookkeeping differs from oracle"
 
     def _pick_tokens(self, s):

@@ -309,3 +309,22 @@ def test_chunked_extend_parity(name, chunk):
     run = DeviceRun(wl, chunk_tokens=chunk)
     run.assert_close()
     assert run.engine.gpu_launches > 0
+
+
+@pytest.mark.parametrize("host_slots,page_size", [(8192, 1), (1200, 1), (8192, 16)])
+def test_two_tier_chat_parity(host_slots, page_size):
+    """A round-robin multi-turn chat (head_dim 256, two layers) whose device
+    pool holds about two sessions' histories, with a host tier: evicted
+    histories come back from the page-locked host pool (written through at
+    every finish, copied back by rx_kv_copy before the extend that reads
+    them); bookkeeping bit-exact, every attention output within tolerance."""
+    wl = workloads.multi_turn_chat(sessions=6, turns=4, system=64, user=24, decode_steps=8,
+                                   layers=2)
+    wl.waves = [[r] for w in wl.waves for r in w]
+    wl.num_slots = 512
+    wl.page_size = page_size
+    run = DeviceRun(wl, host_slots=host_slots)
+    run.assert_close()
+    assert len(run.trace.loads) > 0
+    if host_slots == 1200:
+        assert len(run.trace.host_eviction_log) > 0

@@ -588,3 +588,126 @@ def test_verify_rows_follow_the_tree():
         rx.verify_rows([2], prefix_rows[:1], [0, 2], [-1, 1], [1, 2], 20)   # parent not before
     with pytest.raises(rx.RxError):
         rx.verify_rows([9], prefix_rows[:1], [0, 4], [-1, 0, 1, 2], [1, 2, 3, 4], 12)  # too long
+
+
+# --------------------------------------------------------------- two tiers
+def test_two_tier_random_ops_match_oracle():
+    """Random matches across tiers, loads, inserts, write-throughs (committed
+    later with success or failure), locks and evictions on both caches:
+    identical slots, nodes, tickets, copies, counts and eviction logs."""
+    from oracle.hicache import TwoTierRadixCache
+    rng = random.Random(43)
+    for trial in range(50):
+        ps = rng.choice([1, 2])
+        ns, hs_ = ps * rng.randint(12, 30), ps * rng.randint(6, 24)
+        o, n = TwoTierRadixCache(ns, hs_, ps), rx.RadixCache(ns, ps, hs_)
+        olocks, nlocks, pend = [], [], []
+        for step in range(100):
+            seq = [rng.randrange(3) for _ in range(rng.randint(1, 10))]
+            r = rng.random()
+            if r < 0.45:
+                os_, on, ohl, ohn = o.match_prefix_tiers(seq[:-1])
+                ns_, nn, nhl, nhn = n.match_prefix_tiers(seq[:-1])
+                assert (list(os_), on.id, ohl, ohn.id) == (ns_.tolist(), nn, nhl, nhn)
+                if ohl:
+                    try:
+                        oload = o.load_onboard(ohn)
+                    except ONoSpace:
+                        oload = None
+                    try:
+                        h, d = n.load_onboard(nhn, 64)
+                        nload = (h.tolist(), d.tolist())
+                    except rx.NoSpace:
+                        nload = None
+                    assert (None if oload is None else (list(oload[0]), list(oload[1]))) == nload
+                os_, on = o.match_prefix(seq[:-1])
+                ns_, nn = n.match_prefix(seq[:-1])
+                assert list(os_) == ns_.tolist() and on.id == nn
+                o.inc_lock_ref(on)
+                n.lock(nn)
+                k = len(seq) - len(os_)
+                try:
+                    onew = o.alloc(k)
+                except ONoSpace:
+                    onew = None
+                try:
+                    nnew = n.alloc(k).tolist()
+                except rx.NoSpace:
+                    nnew = None
+                assert onew == nnew
+                if onew is None:
+                    o.dec_lock_ref(on)
+                    n.unlock(nn)
+                    continue
+                orow = list(os_) + onew
+                oa, on2 = o.insert(seq, orow)
+                na, nn2 = n.insert(seq, np.array(orow, dtype=np.int32))
+                assert (oa, on2.id) == (na, nn2)
+                extra = orow[len(os_):oa] + orow[o.aligned(len(seq)):]
+                o.free(extra)
+                n.free(np.array(extra, dtype=np.int32))
+                o.inc_lock_ref(on2)
+                n.lock(nn2)
+                o.dec_lock_ref(on)
+                n.unlock(nn)
+                olocks.append(on2)
+                nlocks.append(nn2)
+            elif r < 0.6 and olocks:
+                i = rng.randrange(len(olocks))
+                on, nn = olocks.pop(i), nlocks.pop(i)
+                o.dec_lock_ref(on)
+                n.unlock(nn)
+                try:
+                    ot = o.write_through(on)
+                except ONoSpace:
+                    ot = None
+                try:
+                    t, d, h = n.write_through(nn, 64)
+                    nt = (t, d.tolist(), h.tolist())
+                except rx.NoSpace:
+                    nt = None
+                assert (None if ot is None else (ot[0], list(ot[1]), list(ot[2]))) == nt
+                if nt and nt[0]:
+                    pend.append(nt[0])
+            elif r < 0.75 and pend:
+                t = pend.pop(rng.randrange(len(pend)))
+                ok = rng.random() < 0.8
+                o.commit_write_through(t, ok)
+                n.commit_write_through(t, ok)
+            else:
+                k = rng.randint(1, 8)
+                assert o.evict(k) == n.evict(k)
+            st = n.stats()
+            assert st["cached_tokens"] == o.device_cached_size()
+            assert st["host_cached_tokens"] == o.host_cached_size()
+            assert st["evictable_tokens"] == o.evictable_size_
+            assert st["protected_tokens"] == o.protected_size_
+            assert st["free_slots"] == len(o.free_slots)
+            assert st["host_free_slots"] == len(o.free_host_pages) * ps
+            assert st["num_nodes"] == o.num_nodes()
+            assert n.eviction_log() == o.eviction_log
+            assert n.host_eviction_log() == o.host_eviction_log
+
+
+@pytest.mark.parametrize("host_slots,page_size", [(4096, 1), (700, 1), (4096, 4)])
+def test_tiered_request_flow_matches_oracle(host_slots, page_size):
+    """A round-robin multi-turn chat under a device pool that holds about two
+    sessions' histories, with a host tier (large, or small enough to evict):
+    loads, backups, slot tables, finishes and both eviction logs equal the
+    oracle's, and the host tier prefills less than one tier."""
+    wl = workloads.multi_turn_chat(sessions=6, turns=4, system=64, user=24, decode_steps=8,
+                                   layers=1)
+    wl.waves = [[r] for w in wl.waves for r in w]
+    wl.num_slots = 400
+    if page_size > 1:
+        wl.page_size = page_size
+    got = Engine(wl, host_slots=host_slots).run()
+    want, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                              page_size=page_size, host_slots=host_slots)
+    assert got.as_tuple() == want.as_tuple()
+    assert len(got.loads) > 0
+    single, _ = run_bookkeeping(wl.oracle_waves(), wl.num_slots, wl.decode_steps,
+                                page_size=page_size)
+    assert got.prefilled < single.prefilled
+    if host_slots == 700:
+        assert len(got.host_eviction_log) > 0
