@@ -89,7 +89,8 @@ def config_of(wl, world):
     return {"workload": wl.name, **{k: v for k, v in wl.describe().items() if k != "workload"},
             "l2": "inputs larger than L2, and L2 flushed between timed steps (256 MiB write, "
                   "outside the step events)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single"}
+            "parallelism": (f"{world} replicas, subtree-affine shards (no collective in the "
+                            "data path)") if world > 1 else "single"}
 
 
 def max_over_ranks(x, world, device):
@@ -104,10 +105,17 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
-def job_rate(units_per_rank, seconds, world):
-    """Whole-job throughput of `world` replicas that each process
-    units_per_rank units in the (max over ranks) time `seconds`."""
-    return world * units_per_rank / seconds
+def job_rate(units_per_rank, seconds, world, device=None):
+    """Whole-job throughput of `world` replicas: the units all ranks
+    processed (each rank its own share) in the (max over ranks) time
+    `seconds`."""
+    if world <= 1:
+        return units_per_rank / seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(units_per_rank)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item()) / seconds
 
 
 def peaks():
@@ -442,7 +450,7 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
             step_s.append(time.perf_counter() - h0)
         e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
         rx.device_check()
-        out["e2e"] = {"value": job_rate(n_ext + n_dec, e2e_s, world), "unit": "query-tok/s",
+        out["e2e"] = {"value": job_rate(n_ext + n_dec, e2e_s, world, dev), "unit": "query-tok/s",
                       "h2d_bytes_per_step": host.h2d_bytes // steps,
                       "d2h_bytes_per_step": ring.d2h_bytes // steps,
                       "ms_per_step": e2e_s * 1e3,
@@ -541,14 +549,16 @@ def main(argv=None):
         return
 
     hbm_peak, bf16_peak, peak_src = peaks()
-    wl = workloads.WORKLOADS[args.workload]()
+    # each replica takes its subtree-affine share (the whole workload on one GPU)
+    full_wl = workloads.WORKLOADS[args.workload]()
+    wl = workloads.shard(full_wl, rank, world)
     clocks = Clocks(local)          # started before warm-up: its start-up is not timed
     res = measure(wl, dev, args.steps, args.warmup, world, e2e=not args.no_e2e, clocks=clocks)
     clk = clocks.result
     torch.cuda.empty_cache()
     n_ext, n_dec = res["n_ext"], res["n_dec"]
     q_per_step = n_ext + n_dec
-    value = job_rate(q_per_step, res["ms"] / 1000.0, world)
+    value = job_rate(q_per_step, res["ms"] / 1000.0, world, dev)
     extend, decode, kv_store = _summary(res, args.steps, hbm_peak, bf16_peak)
     if extend["ms_per_step"] >= decode["ms_per_step"]:
         roof = {"kernel": "rx_extend_attention", "bound": "tensor", "achieved": extend["tflops"],
@@ -587,7 +597,7 @@ def main(argv=None):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": config_of(wl, world),
+            "config": config_of(full_wl, world),
             "detail": {"query_tokens_per_step": q_per_step, "extend_query_tokens": n_ext,
                        "decode_query_tokens": n_dec,
                        "wall_s_timed_region_incl_flush": res["wall"]},

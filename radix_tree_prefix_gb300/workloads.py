@@ -265,6 +265,26 @@ def with_pages(wl, page_size):
     return wl
 
 
+def shard(wl, rank, world):
+    """Rank `rank`'s share of the workload among `world` replicas, each with
+    its own cache and pool (no data exchange between them), routed so that
+    requests that share a subtree stay on one replica: fork_tree's waves (one
+    level-1 subtree each) go round-robin by wave; every other workload's
+    requests go round-robin by their position in the wave (a chat session, an
+    agent call, a long-context request keeps its replica from turn to turn).
+    The pool keeps its size; the segment tables are shared."""
+    if world <= 1:
+        return wl
+    if wl.name.startswith("fork_tree") and len(wl.waves) >= world:
+        waves = [w for i, w in enumerate(wl.waves) if i % world == rank]
+    else:
+        waves = [[r for i, r in enumerate(w) if i % world == rank] for w in wl.waves]
+        waves = [w for w in waves if w]
+    out = Workload(wl.name, wl.num_layers, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                   wl.num_slots, wl.decode_steps, wl.seg_tokens, waves, wl.seed, wl.page_size)
+    return out
+
+
 WORKLOADS = {
     "nested_share": nested_share,
     "agent_loop": agent_loop,
