@@ -710,6 +710,14 @@ rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst,
  * if a flag was set or the device reported an error. */
 rx_status rx_device_check(int32_t* out_flags);
 
+/* Test hook (host fault injection): the k-th page allocation from now, on
+ * the device or the host pool (counted together, k >= 1), fails with
+ * RX_ERR_NO_SPACE after the evictions it would do anyway, exactly as if the
+ * pool were still short; every call then takes its documented failure path
+ * (locks released, nothing allocated, evictions kept).  k = 0 turns the
+ * hook off.  Not for production use. */
+rx_status rx_debug_fail_alloc(rx_cache* cache, int64_t k);
+
 /* Library build information (kernel variant names, compiled arch). */
 const char* rx_build_info(void);
 

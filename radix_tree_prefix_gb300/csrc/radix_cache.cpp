@@ -123,6 +123,12 @@ struct rx_cache {
   std::vector<rx_evict_rec> host_evict_log;
   std::unordered_map<int64_t, int64_t> tickets;  // ticket -> end node of the backup
   int64_t next_ticket = 1;
+  // fault injection (tests): the fail_countdown-th page allocation from now
+  // fails as if the pool were short after eviction; 0 = off
+  int64_t fail_countdown = 0;
+  bool injected_failure() {
+    return fail_countdown > 0 && --fail_countdown == 0;
+  }
 
   bool on_gpu(const Node* x) const { return x == root || x->gpu; }
   bool on_host(const Node* x) const { return x == root || x->host; }
@@ -185,7 +191,7 @@ struct rx_cache {
   // first; false (nothing taken) if still short.
   bool alloc_pages(int64_t n, int32_t* out) {
     if (int64_t(free_list.size()) < n) evict((n - int64_t(free_list.size())) * ps);
-    if (int64_t(free_list.size()) < n) return false;
+    if (int64_t(free_list.size()) < n || injected_failure()) return false;
     for (int64_t i = 0; i < n; ++i) {
       out[i] = free_list.front();
       free_list.pop_front();
@@ -464,7 +470,7 @@ struct rx_cache {
 
   bool host_alloc_pages(int64_t n, int32_t* out) {
     if (int64_t(host_free.size()) < n) host_evict((n - int64_t(host_free.size())) * ps);
-    if (int64_t(host_free.size()) < n) return false;
+    if (int64_t(host_free.size()) < n || injected_failure()) return false;
     for (int64_t i = 0; i < n; ++i) {
       out[i] = host_free.front();
       host_free.pop_front();
@@ -1530,5 +1536,15 @@ extern "C" rx_status rx_host_eviction_log(const rx_cache* c, int64_t start, rx_e
   const int64_t total = int64_t(c->host_evict_log.size());
   for (int64_t i = 0; i < cap && start + i < total; ++i) out[i] = c->host_evict_log[start + i];
   if (out_total) *out_total = total;
+  return RX_OK;
+}
+
+// Fault injection for tests: the k-th page allocation from now (device or
+// host pool, counted together; k >= 1) fails with RX_ERR_NO_SPACE after the
+// evictions it would do anyway, as if the pool were still short.  k = 0
+// turns it off.
+extern "C" rx_status rx_debug_fail_alloc(rx_cache* c, int64_t k) {
+  if (!c || k < 0) return fail(RX_ERR_INVALID, "rx_debug_fail_alloc: bad argument");
+  c->fail_countdown = k;
   return RX_OK;
 }

@@ -112,6 +112,7 @@ _SIGS = {
     "rx_load_batch": [P, I32, P, P, P, P, I64, P, P],
     "rx_write_through_batch": [P, I32, P, P, P, I64, P, P],
     "rx_host_eviction_log": [P, I64, P, I64, P],
+    "rx_debug_fail_alloc": [P, I64],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_batch_end": [P, P, P, I32, I32, P],
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
@@ -425,6 +426,10 @@ class RadixCache:
         _check(_lib.rx_write_through_batch(self._h, R, _p(nd), _p(d), _p(h), int(cap),
                                            C.byref(n), _p(cnt)))
         return d[:n.value], h[:n.value], cnt[:R]
+
+    def debug_fail_alloc(self, k):
+        """Test hook: the k-th page allocation from now fails (0: off)."""
+        _check(_lib.rx_debug_fail_alloc(self._h, int(k)))
 
     def host_eviction_log(self):
         total = C.c_int64()

@@ -711,3 +711,94 @@ def test_tiered_request_flow_matches_oracle(host_slots, page_size):
     assert got.prefilled < single.prefilled
     if host_slots == 700:
         assert len(got.host_eviction_log) > 0
+
+
+# --------------------------------------------------------- fault injection
+def _snapshot(c, tokens_list):
+    """What a failed step must leave alone: stats, and the match (slots and
+    node) of every sequence inserted so far."""
+    st = c.stats()
+    matches = [(c.match_length(t), c.match_prefix_tiers(t)[0].tolist()) for t in tokens_list]
+    return st, matches
+
+
+def test_injected_allocation_failures_leave_the_tree_unchanged():
+    """A failing k-th allocation inside each batch step: the step reports
+    RX_ERR_NO_SPACE (or skips, where the step skips), releases the locks it
+    took, allocates nothing, and leaves every earlier sequence matched as
+    before; the next step runs normally."""
+    rng = np.random.default_rng(13)
+    c = rx.RadixCache(4000, 1, 2000)
+    seqs = [rng.integers(1, 50, size=int(rng.integers(20, 60))).astype(np.int32) for _ in range(6)]
+    # cache a few sequences and back them up
+    for sq in seqs[:4]:
+        slots, _ = c.match_prefix(sq)
+        _, node = c.insert(sq, np.concatenate([slots, c.alloc(len(sq) - len(slots))]))
+        t, d, h = c.write_through(node, 200)
+        if t:
+            c.commit_write_through(t, True)
+    before = c.stats()
+    # extend_begin: the batch's one allocation fails -> no locks, no slots
+    tok = np.concatenate(seqs[4:6])
+    ind = np.array([0, len(seqs[4]), len(tok)], dtype=np.int64)
+    table = np.zeros((2, 100), dtype=np.int32)
+    c.debug_fail_alloc(1)
+    with pytest.raises(rx.NoSpace):
+        c.extend_begin(tok, ind, table)
+    after = c.stats()
+    assert after["protected_tokens"] == 0 and after["free_slots"] == before["free_slots"]
+    assert after["cached_tokens"] == before["cached_tokens"]
+    # alloc_steps: the second step fails, the first stays allocated
+    c.debug_fail_alloc(2)
+    with pytest.raises(rx.NoSpace):
+        c.alloc_steps(3, 4)
+    assert c.stats()["free_slots"] == before["free_slots"] - 3
+    # write-through: the host allocation fails -> no ticket, nothing pending
+    slots, _ = c.match_prefix(seqs[4])
+    _, n4 = c.insert(seqs[4], np.concatenate([slots, c.alloc(len(seqs[4]) - len(slots))]))
+    st0 = c.stats()
+    c.debug_fail_alloc(1)
+    with pytest.raises(rx.NoSpace):
+        c.write_through(n4, 200)
+    st1 = c.stats()
+    assert st1["host_free_slots"] == st0["host_free_slots"] and st1["protected_tokens"] == 0
+    # write-through batch skips the failing backup and takes the next
+    d, h, cnt = c.write_through_batch(np.array([n4], dtype=np.int64), 200)
+    assert len(d) == len(h) == cnt[0] > 0
+    # evict seqs[0] from the device (it is backed up), then a failing load
+    # is skipped by the batch load: the prefix is prefilled instead
+    c.evict(4000)
+    assert c.stats()["cached_tokens"] == 0
+    c.debug_fail_alloc(1)
+    hs, ds, cnt = c.load_batch(seqs[0], np.array([0, len(seqs[0])], dtype=np.int64), 200)
+    assert len(hs) == 0 and cnt.tolist() == [0]
+    assert c.stats()["cached_tokens"] == 0
+    # off again: the load goes through
+    c.debug_fail_alloc(0)
+    hs, ds, cnt = c.load_batch(seqs[0], np.array([0, len(seqs[0])], dtype=np.int64), 200)
+    assert cnt[0] == len(hs) > 0
+
+
+def test_injected_failure_in_the_request_flow_is_reported_and_recoverable():
+    """A whole request flow with the k-th allocation failing: the flow stops
+    with NoSpace at that allocation; the cache's accounting stays
+    consistent (evictable + protected == cached) and every lock the failing
+    batch took is released."""
+    wl = workloads.fork_tree(branching=3, depth=3, level_tokens=24, decode_steps=3)
+    for k in (1, 2, 5, 9):
+        eng = Engine(wl)
+        orig = rx.RadixCache
+
+        class Failing(orig):
+            def __init__(self, *a, **kw):
+                super().__init__(*a, **kw)
+                self.debug_fail_alloc(k)
+
+        rx.RadixCache = Failing
+        try:
+            with pytest.raises(rx.NoSpace):
+                eng.run()
+        finally:
+            rx.RadixCache = orig
+        st = eng.cache.stats()
+        assert st["evictable_tokens"] + st["protected_tokens"] == st["cached_tokens"]
