@@ -695,6 +695,16 @@ rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst,
                      const int32_t* d_src_slots, const int32_t* d_dst_slots,
                      int64_t n, rx_stream_t stream);
 
+/* Page-locked host memory of exactly `bytes` bytes, mapped into the device
+ * address space and usable from every device (cudaHostAlloc, portable and
+ * mapped): for a host pool that rx_kv_copy reads and writes directly, and
+ * for host buffers that copies to and from the device run asynchronously
+ * with.  Released with rx_host_free.  This is host memory: the library still
+ * allocates no device memory.  Errors: RX_ERR_INVALID (bytes 0, out NULL),
+ * RX_ERR_CUDA (the allocation failed; *out = NULL). */
+rx_status rx_host_alloc(size_t bytes, void** out);
+rx_status rx_host_free(void* p);
+
 /* Synchronise the current device and read the kernels' error words (then
  * clear them).  *out_flags (may be NULL): bit 0 = rx_kv_store met a slot
  * outside [1, num_slots) and skipped that write; bit 1 = an attention kernel

@@ -13,7 +13,7 @@
 //           causal limit per row = prefix + token + 1;
 //   decode: rows = (member request, head in group) of a tree segment chunk
 //           shared by the members; writes partial (o, lse) per row.
-// The tile (tc_tile3, 352 threads) streams K and V tiles of 32 KB (128 keys
+// The tile (tc_tile3, 384 threads) streams K and V tiles of 32 KB (128 keys
 // at head_dim 128, 64 at head_dim 256):
 //   warps 0-7  softmax in two warpgroups that split every key tile's keys;
 //              thread (w, i) owns query row i = TMEM lane i; the two halves
@@ -21,10 +21,11 @@
 //              goes into TMEM over the S tile it came from; O is rescaled in
 //              TMEM when the max grows by more than 2^8 (rare after the
 //              first tile); then the output is written;
-//   warp 8     allocates TMEM and issues tcgen05.mma from one thread: S_j =
-//              Q K_j^T into a ring of three TMEM buffers, two tiles ahead of
-//              the softmax, and O += P_j V_j with P_j read from TMEM (O stays
-//              in TMEM for the whole key loop);
+//   warp 8     allocates TMEM and issues S_j = Q K_j^T (tcgen05.mma from
+//              one thread) into a ring of three TMEM buffers, ahead of the
+//              softmax;
+//   warp 11    issues O += P_j V_j with P_j read from TMEM (O stays in TMEM
+//              for the whole key loop);
 //   warps 9-10 load K and V into 128-byte swizzled shared memory (three and
 //              two stages): a tile whose slots form one contiguous run (the
 //              allocator hands out runs, so this is the common case) is one
@@ -178,22 +179,26 @@ __device__ __forceinline__ uint32_t sw128(uint32_t base, int rows, int r, int ch
 }
 
 // Tensor-core tile: 128 query rows, key tiles of BN = 128 keys at head_dim
-// 128 and 64 at head_dim 256 (a K or V tile is 32 KB either way), 352
-// threads.  The MMA warp keeps two S tiles ahead of the softmax: S_{j+2} =
+// 128 and 64 at head_dim 256 (a K or V tile is 32 KB either way), 384
+// threads.  The MMA warps keep S tiles ahead of the softmax: S_{j+2} =
 // Q K_{j+2}^T is issued before PV_j, into a ring of three S buffers in TMEM,
 // so the softmax of tile j+1 never waits for an MMA.  P_j (bf16, two keys per
 // column) overwrites the first BN/2 columns of S_j's buffer once the softmax
-// has read S_j, and PV_j reads it from TMEM as its A operand; tcgen05.mma
-// operations from one thread run in issue order, so S_{j+3} (issued after
-// PV_j) reuses that buffer only after PV_j read P_j.
+// has read S_j, and PV_j reads it from TMEM as its A operand; the S issuer
+// waits for PV_j's completion (barrier pf) before S_{j+3} reuses that
+// buffer.
 // TMEM: S ring [0, 3 BN), O from column O_COL (D columns).  Shared memory: Q
 // (128-byte swizzled, the A operand of S), K in three stages, V in two.
 // Warps 0-7 softmax in two warpgroups that split each key tile's columns
 // (thread (w, i) of warpgroup w: row i = TMEM lane i, keys [w BN/2, (w+1)
-// BN/2); it also gathers half of Q row i first), warp 8 issues the MMAs,
-// warp 9 loads K and warp 10 loads V (a V stage frees only when PV of its
-// previous tile completes, and K loads must not queue behind that).
-constexpr int kThreads3 = 352;
+// BN/2); it also gathers half of Q row i first), warp 8 issues the S MMAs
+// and warp 11 the PV MMAs (two instruction streams: one thread issuing all
+// of a key tile's MMAs set the tile's period), warp 9 loads K and warp 10
+// loads V (a V stage frees only when PV of its previous tile completes, and
+// K loads must not queue behind that).
+// 12 warps: 0-7 softmax (two warpgroups), 8 S = Q K^T issue, 9 K loader, 10 V
+// loader, 11 O += P V issue
+constexpr int kThreads3 = 384;
 
 template <int HEAD_DIM>
 struct Layout3 {
@@ -210,11 +215,12 @@ struct Layout3 {
   static constexpr int XCH = V0 + VSTAGES * KV_BYTES;
   static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
   // barriers: q, kfull, vfull (one per stage), s[3], p[3], o[2] (PV of even
-  // / odd tiles), final, max exchange[2], sum exchange.  A K stage is free
+  // / odd tiles), final, max exchange[2], sum exchange, pf[3] (PV of the P
+  // in S buffer b done, so S may overwrite it).  A K stage is free
   // again when the S product that read it completes (s[] of the same index:
   // both rings have three entries) and a V stage when its PV product does
   // (o[] of the same parity: two V stages).
-  static constexpr int NBAR = 1 + KSTAGES + VSTAGES + 2 * SBUF + 6;
+  static constexpr int NBAR = 1 + KSTAGES + VSTAGES + 2 * SBUF + 6 + SBUF;
   static_assert(KSTAGES == SBUF && VSTAGES == 2, "stage rings share the MMA barriers");
   static constexpr int MISC = BAR + NBAR * 8;  // tmem address, abort flag
   // At head_dim 128 the layout carries 1024 bytes of slack to align the
@@ -301,7 +307,10 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const uint32_t BAR_FIN = bar + 8u * (kAfterP + 2);
   auto XB = [&](int p) { return bar + 8u * (kAfterP + 3 + p); };
   const uint32_t XE = bar + 8u * (kAfterP + 5);
-  static_assert(kAfterP + 6 == Lo::NBAR, "barrier count");
+  // PV_j completes phase j / NB of BAR_PF(j % NB): S buffer j % NB is free
+  // for S_{j+NB}
+  auto BAR_PF = [&](int b) { return bar + 8u * (kAfterP + 6 + b); };
+  static_assert(kAfterP + 6 + NB == Lo::NBAR, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lo::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lo::MISC + 4);
 
@@ -324,7 +333,8 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     tc::mbar_init(XE, 8 * 32);
     tc::mbar_init(BAR_O(0), 1);
     tc::mbar_init(BAR_O(1), 1);
-    tc::mbar_init(BAR_FIN, 1);
+    tc::mbar_init(BAR_FIN, 2);  // one commit per issuing thread
+    for (int b = 0; b < NB; ++b) tc::mbar_init(BAR_PF(b), 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -337,7 +347,7 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 9) {
+  if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------- loaders
     const bool load_v = warp == 10;
     // keys written by earlier kernels on the stream are read from here on
@@ -460,10 +470,15 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       }
     }
     __syncwarp();
-  } else if (warp == 8) {
+  } else if (warp == 8 || warp == 11) {
     // ------------------------------------------------------------ MMA issue
-    // S_j = Q K_j^T into S buffer j % 3 (two tiles ahead of the softmax), then
-    // O += P_j V_j with P_j from TMEM.
+    // Two issuing threads, so neither instruction stream alone sets the key
+    // tile's period: warp 8 issues S_j = Q K_j^T into S buffer j % 3, warp 11
+    // issues O += P_j V_j with P_j from TMEM.  The two streams no longer
+    // complete in one order, so the S issuer waits, before S_j, until PV_{j-3}
+    // (which read P_{j-3} from the same buffer) has completed (barrier pf[j %
+    // 3]); hence S_j completing still implies PV_{j-3} completed, which the
+    // softmax's wait on o[] relies on.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
       constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
@@ -477,64 +492,68 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
       // start on 1024-byte boundaries
       constexpr uint32_t DHI = (1024u >> 4) | (1u << 14) | (2u << 29);
       constexpr uint32_t KV_STEP = uint32_t(Lo::KV_BYTES) >> 4;
-      const uint32_t q_lo = ((sQ & 0x3FFFFu) >> 4) | (1u << 16);
-      const uint32_t k_lo0 = (((base + Lo::K0) & 0x3FFFFu) >> 4) | (1u << 16);
-      const uint32_t v_lo0 = (((base + Lo::V0) & 0x3FFFFu) >> 4) | (uint32_t(BN * 128 / 16) << 16);
       static_assert(Lo::V0 + NV * Lo::KV_BYTES < (1 << 18), "descriptor address field");
-      bool ok = tc::mbar_wait(BAR_Q, 0, abort_flag, kWaitLimit, kSleepNs);
-      // running stage indices and barrier phases: S_j's K stage, S buffer
-      // of the next S to issue; PV's V stage and S buffer
-      int ks_stage = 0, s_buf = 0;
-      uint32_t k_phase = 0;
-      auto issue_s = [&](int j) -> bool {
-        if (!tc::mbar_wait(BAR_KF(ks_stage), k_phase, abort_flag, kWaitLimit, kSleepNs))
-          return false;
-        tc::tc_fence_after();
-        const uint32_t k_lo = k_lo0 + uint32_t(ks_stage) * KV_STEP;
-        const uint32_t d_s = tmem + uint32_t(s_buf * BN);
+      if (warp == 8) {
+        const uint32_t q_lo = ((sQ & 0x3FFFFu) >> 4) | (1u << 16);
+        const uint32_t k_lo0 = (((base + Lo::K0) & 0x3FFFFu) >> 4) | (1u << 16);
+        const bool ok = tc::mbar_wait(BAR_Q, 0, abort_flag, kWaitLimit, kSleepNs);
+        // S_j's K stage and S buffer (the same index: both rings have NB
+        // entries) and the phases of its waits
+        int sb = 0;
+        uint32_t k_phase = 0, pf_phase = 0;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          if (j >= NB && !tc::mbar_wait(BAR_PF(sb), pf_phase, abort_flag, kWaitLimit, kSleepNs))
+            break;
+          if (!tc::mbar_wait(BAR_KF(sb), k_phase, abort_flag, kWaitLimit, kSleepNs)) break;
+          tc::tc_fence_after();
+          const uint32_t k_lo = k_lo0 + uint32_t(sb) * KV_STEP;
+          const uint32_t d_s = tmem + uint32_t(sb * BN);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t a_off = uint32_t(((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4);
-          const uint32_t b_off = uint32_t(((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4);
-          mma_ss_split(d_s, q_lo + a_off, k_lo + b_off, DHI, IDESC_S, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t a_off = uint32_t(((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4);
+            const uint32_t b_off = uint32_t(((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4);
+            mma_ss_split(d_s, q_lo + a_off, k_lo + b_off, DHI, IDESC_S, ks > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(BAR_S(sb));  // also frees K stage sb
+          if (++sb == NB) {
+            sb = 0;
+            k_phase ^= 1u;
+            if (j >= NB) pf_phase ^= 1u;
+          }
         }
-        tc::mma_commit(BAR_S(s_buf));  // also frees K stage ks_stage (== s_buf)
-        if (++ks_stage == NK) {
-          ks_stage = 0;
-          k_phase ^= 1u;
-        }
-        if (++s_buf == NB) s_buf = 0;
-        return true;
-      };
-      for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_s(j);
-      int sv = 0, pb = 0;
-      uint32_t v_phase = 0, p_phase = 0;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 2 < n_tiles && !issue_s(j + 2)) break;
-        if (!tc::mbar_wait(BAR_P(pb), p_phase, abort_flag, kWaitLimit, kSleepNs)) break;
-        if (!tc::mbar_wait(BAR_VF(sv), v_phase, abort_flag, kWaitLimit, kSleepNs)) break;
-        tc::tc_fence_after();
-        const uint32_t v_lo = v_lo0 + uint32_t(sv) * KV_STEP;
-        const uint32_t p_t = tmem + uint32_t(pb * BN);
+      } else {
+        const uint32_t v_lo0 =
+            (((base + Lo::V0) & 0x3FFFFu) >> 4) | (uint32_t(BN * 128 / 16) << 16);
+        int sv = 0, pb = 0;
+        uint32_t v_phase = 0, p_phase = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+          if (!tc::mbar_wait(BAR_P(pb), p_phase, abort_flag, kWaitLimit, kSleepNs)) break;
+          if (!tc::mbar_wait(BAR_VF(sv), v_phase, abort_flag, kWaitLimit, kSleepNs)) break;
+          tc::tc_fence_after();
+          const uint32_t v_lo = v_lo0 + uint32_t(sv) * KV_STEP;
+          const uint32_t p_t = tmem + uint32_t(pb * BN);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ts_split(tmem + uint32_t(Lo::O_COL), p_t + uint32_t(ks * 8),
-                       v_lo + uint32_t(ks * 2048 / 16), DHI, IDESC_PV,
-                       (j > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(BAR_O(j & 1));  // also frees V stage sv (== j & 1)
-        if (++sv == NV) {
-          sv = 0;
-          v_phase ^= 1u;
-        }
-        if (++pb == NB) {
-          pb = 0;
-          p_phase ^= 1u;
+          for (int ks = 0; ks < BN / 16; ++ks)
+            mma_ts_split(tmem + uint32_t(Lo::O_COL), p_t + uint32_t(ks * 8),
+                         v_lo + uint32_t(ks * 2048 / 16), DHI, IDESC_PV,
+                         (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_commit(BAR_O(j & 1));  // also frees V stage sv (== j & 1)
+          tc::mma_commit(BAR_PF(pb));    // S buffer pb may take S_{j+3}
+          if (++sv == NV) {
+            sv = 0;
+            v_phase ^= 1u;
+          }
+          if (++pb == NB) {
+            pb = 0;
+            p_phase ^= 1u;
+          }
         }
       }
-      // drain: every MMA issued above has completed once this arrives.  The
-      // wait ignores the abort flag (bounded all the same): after another
-      // warp gave up, MMAs already issued must finish writing TMEM and
-      // reading shared memory before the CTA frees both.
+      // drain: every MMA this thread issued has completed once the final
+      // barrier (one arrival per issuing thread) completes.  The wait ignores
+      // the abort flag (bounded all the same): after another warp gave up,
+      // MMAs already issued must finish writing TMEM and reading shared
+      // memory before the CTA frees both.
       tc::mma_commit(BAR_FIN);
       int drain_abort = 0;
       tc::mbar_wait(BAR_FIN, 0, &drain_abort, kWaitLimit);

@@ -244,6 +244,33 @@ extern "C" rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst
   return rx_internal::launch_status("rx_kv_copy");
 }
 
+extern "C" rx_status rx_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return rx_internal::set_error(RX_ERR_INVALID, "rx_host_alloc: bad argument");
+  *out = nullptr;
+  // page-locked, mapped into the device address space (a host pool the
+  // kernels read and write directly), usable from every device
+  const cudaError_t e =
+      cudaHostAlloc(out, bytes, cudaHostAllocPortable | cudaHostAllocMapped);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    static thread_local char buf[256];
+    snprintf(buf, sizeof(buf), "rx_host_alloc: %zu bytes: %s", bytes, cudaGetErrorString(e));
+    return rx_internal::set_error(RX_ERR_CUDA, buf);
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_host_free(void* p) {
+  if (!p) return RX_OK;
+  const cudaError_t e = cudaFreeHost(p);
+  if (e != cudaSuccess) {
+    static thread_local char buf[256];
+    snprintf(buf, sizeof(buf), "rx_host_free: %s", cudaGetErrorString(e));
+    return rx_internal::set_error(RX_ERR_CUDA, buf);
+  }
+  return RX_OK;
+}
+
 extern "C" rx_status rx_device_check(int32_t* out_flags) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {

@@ -12,7 +12,7 @@ namespace rx_internal {
 // rows (members x group heads) go to the warp role of the fused decode
 // kernel (16 rows at head_dim 128; 8 at head_dim 256, where the O^T
 // accumulators of 16 rows would not fit in the registers a warp of the
-// 352-thread CTA has); larger ones are cut into member blocks of at most
+// 384-thread CTA has); larger ones are cut into member blocks of at most
 // kDecodeTcRows rows for its tensor-core tiles.
 inline int decode_small_rows(int head_dim) { return head_dim == 128 ? 16 : 8; }
 constexpr int kDecodeTcRows = 128;

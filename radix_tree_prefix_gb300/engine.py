@@ -112,34 +112,45 @@ class GatherInputs:
 
 
 class HostBuffer:
-    """Page-locked host memory of an exact size: a numpy array registered
-    with CUDA (cudaHostRegister), so copies from and to it run
-    asynchronously, without the power-of-two rounding of the framework's
-    pinned-memory cache.  ``tensor`` views it; ``close`` unregisters it."""
+    """Page-locked host memory of an exact size.  By default it comes from
+    the library (``rx_host_alloc``: cudaHostAlloc, mapped into the device
+    address space); with ``mode="register"`` it is a numpy array registered
+    with CUDA (cudaHostRegister).  Copies from and to it run asynchronously,
+    without the power-of-two rounding of the framework's pinned-memory
+    cache.  ``tensor`` views it as uint8; ``close`` releases it."""
 
-    def __init__(self, nbytes):
+    def __init__(self, nbytes, mode="alloc"):
         import torch
         self.torch = torch
-        self.array = np.empty(max(1, int(nbytes)), dtype=np.uint8)
-        self.registered = False
-        rt = getattr(torch._C, "_cudart", None)
-        if rt is not None and hasattr(rt, "cudaHostRegister"):
-            err = rt.cudaHostRegister(self.array.ctypes.data, self.array.nbytes, 0)
-            self.registered = int(getattr(err, "value", err)) == 0
-        if self.registered:
+        self.nbytes = max(1, int(nbytes))
+        self.mode = mode
+        self.ptr = None
+        self.array = None
+        if mode == "alloc":
+            self.ptr = rx.host_alloc(self.nbytes)
+            buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+            self.tensor = torch.frombuffer(buf, dtype=torch.uint8)
+        else:
+            self.array = np.empty(self.nbytes, dtype=np.uint8)
+            err = torch._C._cudart.cudaHostRegister(self.array.ctypes.data, self.nbytes, 0)
+            if int(getattr(err, "value", err)) != 0:
+                raise RuntimeError(f"cudaHostRegister failed: {err}")
             self.tensor = torch.from_numpy(self.array)
-        else:   # registration unavailable: the framework's pinned allocator
-            self.tensor = torch.empty(self.array.nbytes, dtype=torch.uint8, pin_memory=True)
-            self.array = None
 
     def view(self, offset, shape, dtype):
         n = int(np.prod(shape)) * _itemsize(dtype)
         return self.tensor[offset:offset + n].view(dtype).view(shape)
 
     def close(self):
-        if self.registered:
+        if self.tensor is None:
+            return
+        self.tensor = None
+        if self.ptr is not None:
+            rx.host_free(self.ptr)
+            self.ptr = None
+        elif self.array is not None:
             self.torch._C._cudart.cudaHostUnregister(self.array.ctypes.data)
-            self.registered = False
+            self.array = None
 
     def __del__(self):
         try:

@@ -113,6 +113,8 @@ _SIGS = {
     "rx_write_through_batch": [P, I32, P, P, P, I64, P, P],
     "rx_host_eviction_log": [P, I64, P, I64, P],
     "rx_debug_fail_alloc": [P, I64],
+    "rx_host_alloc": [SZ, P],
+    "rx_host_free": [P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_batch_end": [P, P, P, I32, I32, P],
     "rx_plan_decode": [P, I32, P, P, P, I32, I32, I32, P, I64, P],
@@ -581,6 +583,18 @@ def decode_attention_static(pool, layer, d_q, hq, d_table, d_plan, info, B, scal
                                            d_table.data_ptr(), d_table.shape[1], d_plan.data_ptr(),
                                            C.byref(info), B, scale, d_out.data_ptr(),
                                            d_lse.data_ptr(), _stream(stream)))
+
+
+def host_alloc(nbytes):
+    """rx_host_alloc: address of `nbytes` of page-locked, device-mapped host
+    memory (free with host_free)."""
+    out = C.c_void_p()
+    _check(_lib.rx_host_alloc(int(nbytes), C.byref(out)))
+    return out.value
+
+
+def host_free(ptr):
+    _check(_lib.rx_host_free(ptr))
 
 
 def device_check():
