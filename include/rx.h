@@ -728,13 +728,6 @@ rx_status rx_device_check(int32_t* out_flags);
  * hook off.  Not for production use. */
 rx_status rx_debug_fail_alloc(rx_cache* cache, int64_t k);
 
-/* Test hook: d_y[i] = 2^d_x[i] (device fp32 arrays of n) computed as the
- * attention tiles compute every second softmax weight, on the FMA and
- * integer pipes (range reduction to [-1/2, 1/2] and a minimax cubic;
- * relative error below 7.5e-5 for x >= -125, 0 below), so a test can hold it
- * against CUDA's exp2. */
-rx_status rx_debug_exp2(const float* d_x, float* d_y, int64_t n, rx_stream_t stream);
-
 /* Library build information (kernel variant names, compiled arch). */
 const char* rx_build_info(void);
 

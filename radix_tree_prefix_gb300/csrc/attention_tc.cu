@@ -681,18 +681,16 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          // p = 2^(scale*s - m) for two keys in fp32, then both rounded to
-          // nearest into one bf16x2 word (the precision P has in the PV
-          // product).  The first key's exp2 runs on the SFU, the second's on
-          // the FMA and integer pipes (rxk::poly_exp2), so neither unit alone
-          // sets the softmax's pace.  With the lazy max the dominant keys'
+          // p = 2^(scale*s - m) for two keys: exp2 in fp32 on the SFU, then
+          // both rounded to nearest into one bf16x2 word (the precision P has
+          // in the PV product).  With the lazy max the dominant keys'
           // exponents reach +8, where a bf16 exponent or a bf16 exp2 result
           // would cost up to 1% per weight on peaked rows.  The row sum adds
           // exactly the rounded values in fp32, in eight independent partial
           // sums.
           const float x0 = fmaf(__uint_as_float(sr[cc * 32 + e]), a.scale_log2, -m_use);
           const float x1 = fmaf(__uint_as_float(sr[cc * 32 + e + 1]), a.scale_log2, -m_use);
-          const uint32_t h = rxk::pack_bf16(rxk::fast_exp2(x0), rxk::poly_exp2(x1));
+          const uint32_t h = rxk::pack_bf16(rxk::fast_exp2(x0), rxk::fast_exp2(x1));
           l8[(e >> 1) & 7] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
           pk[e >> 1] = h;
         }

@@ -15,7 +15,6 @@
 #include <cuda_runtime.h>
 #include <stdio.h>
 
-#include "ptx_util.cuh"
 #include "rx.h"
 #include "rx_internal.h"
 
@@ -105,11 +104,6 @@ __global__ void __launch_bounds__(256) kv_copy_kernel(const uint4* __restrict__ 
     dst_k[to] = kv;
     dst_v[to] = vv;
   }
-}
-
-__global__ void poly_exp2_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < n) y[i] = rxk::poly_exp2(x[i]);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -248,15 +242,6 @@ extern "C" rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst
       reinterpret_cast<uint4*>(ptr[2]), reinterpret_cast<uint4*>(ptr[3]), d_src_slots,
       d_dst_slots, n, src->num_layers, src->num_kv_heads, cpr, src->num_slots, dst->num_slots);
   return rx_internal::launch_status("rx_kv_copy");
-}
-
-extern "C" rx_status rx_debug_exp2(const float* d_x, float* d_y, int64_t n, rx_stream_t stream) {
-  if (n < 0 || (n && (!d_x || !d_y)))
-    return rx_internal::set_error(RX_ERR_INVALID, "rx_debug_exp2: bad argument");
-  if (n == 0) return RX_OK;
-  poly_exp2_kernel<<<unsigned((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      d_x, d_y, n);
-  return rx_internal::launch_status("rx_debug_exp2");
 }
 
 extern "C" rx_status rx_host_alloc(size_t bytes, void** out) {

@@ -60,26 +60,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x on the FMA and integer pipes instead of the special-function unit
-// (Cody-Waite range reduction with a polynomial, the scheme FlashAttention-4
-// uses to relieve the SFU in softmax): x = n + f with n the nearest integer
-// (adding 1.5 * 2^23 leaves n in the low mantissa bits; subtracting it back
-// is exact) and f in [-1/2, 1/2]; 2^f by a cubic whose coefficients minimise
-// the maximum relative error on [-1/2, 1/2] (a Remez exchange, derived for
-// this library: 7.5e-5, far below the 2^-9 of the bf16 rounding P gets);
-// 2^n added to the exponent field.  x below -125 gives 0 (2^-125 would be
-// the smallest result), as the SFU's flushed result does.
-__device__ __forceinline__ float poly_exp2(float x) {
-  const float xc = fmaxf(x, -125.0f);
-  const float t = xc + 12582912.0f;  // 1.5 * 2^23
-  const float f = xc - (t - 12582912.0f);
-  const float p = fmaf(fmaf(fmaf(0.05517166905792616f, f, 0.2426111221932161f), f,
-                            0.6932609854606553f),
-                       f, 0.9999280735394012f);
-  const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-  return x < -125.0f ? 0.0f : r;
-}
-
 // Programmatic dependent launch: wait until the kernels this grid depends on
 // (the previous ones on its stream) have completed and their writes are
 // visible; a no-op in a grid launched without that attribute.

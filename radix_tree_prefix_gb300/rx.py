@@ -114,7 +114,6 @@ _SIGS = {
     "rx_host_eviction_log": [P, I64, P, I64, P],
     "rx_debug_fail_alloc": [P, I64],
     "rx_host_alloc": [SZ, P],
-    "rx_debug_exp2": [P, P, I64, P],
     "rx_host_free": [P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_batch_end": [P, P, P, I32, I32, P],
@@ -584,11 +583,6 @@ def decode_attention_static(pool, layer, d_q, hq, d_table, d_plan, info, B, scal
                                            d_table.data_ptr(), d_table.shape[1], d_plan.data_ptr(),
                                            C.byref(info), B, scale, d_out.data_ptr(),
                                            d_lse.data_ptr(), _stream(stream)))
-
-
-def debug_exp2(d_x, d_y, stream=None):
-    """rx_debug_exp2: the tiles' FMA-pipe 2^x on device fp32 tensors."""
-    _check(_lib.rx_debug_exp2(d_x.data_ptr(), d_y.data_ptr(), d_x.numel(), _stream(stream)))
 
 
 def host_alloc(nbytes):
