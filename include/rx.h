@@ -75,6 +75,7 @@ typedef enum rx_status {
 } rx_status;
 
 typedef struct CUstream_st* rx_stream_t; /* identical to cudaStream_t */
+typedef struct CUevent_st* rx_event_t;   /* identical to cudaEvent_t  */
 
 /* A node handle is the node's id: 0 is the root, every created node (new
  * leaf, or the upper half of a split) takes the next id.  A handle stays valid
@@ -408,6 +409,27 @@ rx_status rx_schedule(const rx_cache* cache, int32_t policy, int32_t R,
                       const int32_t* tokens, const int64_t* indptr,
                       int32_t* out_order);
 
+/* A whole wave's extend bookkeeping in one call: starting at request 0,
+ * each batch is found by rx_batch_end and run through rx_extend_begin and
+ * rx_extend_end, exactly as those calls made batch by batch would (so the
+ * slots, nodes and eviction order are the same).  tokens/indptr hold the
+ * wave's R prompts; req_to_token rows 0 .. R-1 (row_stride) receive the
+ * rows, as rx_extend_end leaves them.  Writes out_batch_end[b] (the request
+ * that ends batch b, exclusive) for b < *out_n_batches, out_prefix_len[r],
+ * out_prompt_node[r], out_new_slots (every batch's new slots, batch after
+ * batch, request order within a batch: request r's new tokens' slots) and
+ * out_batch_rewritten[b] (rows of batch b that rx_extend_end rewrote with
+ * tree slots: the row a batch's kernels use is then its matched slots
+ * followed by its new slots).  A failing batch returns its error with
+ * *out_n_batches = the batches done before it (their effects kept, the
+ * failing batch's locks released). */
+rx_status rx_extend_wave(rx_cache* cache, int32_t R, const int32_t* tokens,
+                         const int64_t* indptr, int32_t* req_to_token,
+                         int64_t row_stride, int32_t* out_batch_end,
+                         int32_t* out_n_batches, int32_t* out_prefix_len,
+                         rx_node* out_prompt_node, int32_t* out_new_slots,
+                         int64_t* out_batch_rewritten);
+
 /* ------------------------------------------------------------------------
  * Decode plan (S7/S8 split; host)
  * ---------------------------------------------------------------------- */
@@ -562,6 +584,47 @@ rx_status rx_extend_attention(const rx_pool_desc* pool, int32_t layer,
                               const int32_t* d_tile_indptr, int32_t R,
                               int64_t num_tiles, float scale, float* d_out,
                               float* d_lse, rx_stream_t stream);
+
+/* The extend batches of one wave for one layer, launched in order on one
+ * stream: for batch i, rx_kv_store of its new tokens' K/V, then
+ * rx_extend_attention of its requests (each with the arguments those calls
+ * document).  Batch i + 1 may read KV that batch i stored, which the single
+ * stream orders.  A batch's d_q, d_k, d_v hold its n_new suffix tokens
+ * (n_new = d_qo_indptr[R]) and d_new_slots their slots; d_req_to_token with
+ * row_stride holds the rows d_req_rows names.  events: NULL, or 4 events per
+ * batch (rx_events_create) recorded before and after the store and before
+ * and after the attention, for rx_event_elapsed_ms.  Stops at the first
+ * error, with the batches before it launched. */
+typedef struct rx_extend_batch {
+  const void* d_q;               /* bf16 [n_new][Hq][head_dim]              */
+  const void* d_k;               /* bf16 [n_new][Hkv][head_dim]             */
+  const void* d_v;               /* bf16 [n_new][Hkv][head_dim]             */
+  const int32_t* d_new_slots;    /* device int32 [n_new]                    */
+  const int32_t* d_req_to_token; /* device int32 rows, row_stride apart     */
+  const int32_t* d_req_rows;     /* device int32 [R]                        */
+  const int32_t* d_prefix_len;   /* device int32 [R]                        */
+  const int32_t* d_qo_indptr;    /* device int32 [R+1]                      */
+  const int32_t* d_tile_indptr;  /* device int32 [R+1], from rx_extend_plan */
+  float* d_out;                  /* fp32 [n_new][Hq][head_dim]              */
+  float* d_lse;                  /* fp32 [n_new][Hq]                        */
+  int64_t n_new;
+  int64_t num_tiles;
+  int64_t row_stride;
+  int32_t R;
+  int32_t reserved;
+} rx_extend_batch;
+
+rx_status rx_extend_batches(const rx_pool_desc* pool, int32_t layer,
+                            int32_t num_q_heads, const rx_extend_batch* batches,
+                            int32_t n, float scale, const rx_event_t* events,
+                            rx_stream_t stream);
+
+/* n timing events (cudaEventCreate) written to out[0 .. n); destroyed by
+ * rx_events_destroy.  rx_event_elapsed_ms: milliseconds between two
+ * recorded events (RX_ERR_CUDA while either is not complete). */
+rx_status rx_events_create(int32_t n, rx_event_t* out);
+rx_status rx_events_destroy(int32_t n, const rx_event_t* events);
+rx_status rx_event_elapsed_ms(rx_event_t start, rx_event_t end, float* out_ms);
 
 /* S7+S8+S9 decode attention ([L] "A quick recap": each new token attends
  * over the KV cache, its own K/V already stored).  For request b < B, query

@@ -381,3 +381,65 @@ extern "C" rx_status rx_decode_attention_static(const rx_pool_desc* pool, int32_
                                size_t(RX_DECODE_STATIC_SCRATCH_BYTES),
                                reinterpret_cast<cudaStream_t>(stream), true, 0);
 }
+
+extern "C" rx_status rx_extend_batches(const rx_pool_desc* pool, int32_t layer,
+                                       int32_t num_q_heads, const rx_extend_batch* batches,
+                                       int32_t n, float scale, const rx_event_t* events,
+                                       rx_stream_t stream) {
+  if (n < 0 || (n && !batches))
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_extend_batches: bad batch list");
+  rx_status r = rx_internal::check_pool(pool, layer);
+  if (r != RX_OK) return r;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto mark = [&](int32_t i, int k) -> rx_status {
+    if (!events) return RX_OK;
+    if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[4 * int64_t(i) + k]), s) !=
+        cudaSuccess)
+      return rx_internal::launch_status("rx_extend_batches: event record");
+    return RX_OK;
+  };
+  // batch i + 1 reads the KV that batch i stored (its prefix may end inside
+  // batch i's tokens): the launches stay in batch order on one stream
+  for (int32_t i = 0; i < n; ++i) {
+    const rx_extend_batch& b = batches[i];
+    if ((r = mark(i, 0)) != RX_OK) return r;
+    r = rx_kv_store(pool, layer, b.d_new_slots, b.d_k, b.d_v, b.n_new, stream);
+    if (r != RX_OK) return r;
+    if ((r = mark(i, 1)) != RX_OK || (r = mark(i, 2)) != RX_OK) return r;
+    r = rx_extend_attention(pool, layer, b.d_q, num_q_heads, b.d_req_to_token, b.row_stride,
+                            b.d_req_rows, b.d_prefix_len, b.d_qo_indptr, b.d_tile_indptr, b.R,
+                            b.num_tiles, scale, b.d_out, b.d_lse, stream);
+    if (r != RX_OK) return r;
+    if ((r = mark(i, 3)) != RX_OK) return r;
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_events_create(int32_t n, rx_event_t* out) {
+  if (n < 0 || (n && !out)) return rx_internal::set_error(RX_ERR_INVALID, "rx_events_create");
+  for (int32_t i = 0; i < n; ++i) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      for (int32_t j = 0; j < i; ++j) cudaEventDestroy(reinterpret_cast<cudaEvent_t>(out[j]));
+      return rx_internal::launch_status("rx_events_create");
+    }
+    out[i] = reinterpret_cast<rx_event_t>(e);
+  }
+  return RX_OK;
+}
+
+extern "C" rx_status rx_events_destroy(int32_t n, const rx_event_t* ev) {
+  if (n < 0 || (n && !ev)) return rx_internal::set_error(RX_ERR_INVALID, "rx_events_destroy");
+  for (int32_t i = 0; i < n; ++i)
+    if (ev[i]) cudaEventDestroy(reinterpret_cast<cudaEvent_t>(ev[i]));
+  return RX_OK;
+}
+
+extern "C" rx_status rx_event_elapsed_ms(rx_event_t start, rx_event_t end, float* out_ms) {
+  if (!start || !end || !out_ms)
+    return rx_internal::set_error(RX_ERR_INVALID, "rx_event_elapsed_ms: bad argument");
+  if (cudaEventElapsedTime(out_ms, reinterpret_cast<cudaEvent_t>(start),
+                           reinterpret_cast<cudaEvent_t>(end)) != cudaSuccess)
+    return rx_internal::launch_status("rx_event_elapsed_ms");
+  return RX_OK;
+}

@@ -1548,3 +1548,47 @@ extern "C" rx_status rx_debug_fail_alloc(rx_cache* c, int64_t k) {
   c->fail_countdown = k;
   return RX_OK;
 }
+
+// ------------------------------------------------------------- whole waves
+// The in-batch rule's batch loop over a whole wave in one call: for each
+// batch in turn rx_batch_end, rx_extend_begin, rx_extend_end, exactly as a
+// caller making those calls batch by batch would ("SGLang: the tree, and the
+// language nobody remembers", section "The overlap that pays for itself":
+// the host decides slots ahead of the GPU, which needs only slot numbers).
+extern "C" rx_status rx_extend_wave(rx_cache* c, int32_t R, const int32_t* tokens,
+                                    const int64_t* indptr, int32_t* req_to_token,
+                                    int64_t row_stride, int32_t* out_batch_end,
+                                    int32_t* out_n_batches, int32_t* out_prefix_len,
+                                    rx_node* out_prompt_node, int32_t* out_new_slots,
+                                    int64_t* out_batch_rewritten) {
+  if (!c || R < 0 || !indptr || !out_n_batches ||
+      (R && (!tokens || !req_to_token || !out_batch_end || !out_prefix_len ||
+             !out_prompt_node || !out_new_slots || !out_batch_rewritten)))
+    return fail(RX_ERR_INVALID, "rx_extend_wave: bad argument");
+  *out_n_batches = 0;
+  std::vector<rx_node> match(static_cast<size_t>(R));
+  int64_t new_off = 0;
+  int32_t start = 0;
+  while (start < R) {
+    int32_t end = R;
+    rx_status st = rx_batch_end(c, tokens, indptr, start, R, &end);
+    if (st != RX_OK) return st;
+    const int32_t n = end - start;
+    int64_t total = 0;
+    st = rx_extend_begin(c, n, tokens, indptr + start, req_to_token + int64_t(start) * row_stride,
+                         row_stride, out_prefix_len + start, match.data() + start,
+                         out_new_slots + new_off, &total);
+    if (st != RX_OK) return st;
+    new_off += total;
+    int64_t rew = 0;
+    st = rx_extend_end(c, n, tokens, indptr + start, req_to_token + int64_t(start) * row_stride,
+                       row_stride, out_prefix_len + start, match.data() + start,
+                       out_prompt_node + start, &rew);
+    if (st != RX_OK) return st;
+    out_batch_end[*out_n_batches] = end;
+    out_batch_rewritten[*out_n_batches] = rew;
+    *out_n_batches += 1;
+    start = end;
+  }
+  return RX_OK;
+}

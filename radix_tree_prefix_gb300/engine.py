@@ -574,6 +574,9 @@ class Engine:
         self._b_new = np.zeros(max(1, max_wave_tokens), dtype=np.int32)
         self._b_ptrs = (self._b_prefix.ctypes.data, self._b_nodes.ctypes.data,
                         self._b_new.ctypes.data)
+        self._w_ends = np.zeros(self.max_wave, dtype=np.int32)
+        self._w_rew = np.zeros(self.max_wave, dtype=np.int64)
+        self._events = rx.EventPool() if device is not None else None
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
 
     # ------------------------------------------------------------------ run
@@ -628,14 +631,17 @@ class Engine:
         lens, indptr, tokens, full, findptr, tokens_p, indptr_p = self._wave_host(wi, wave)
         self.h_table[:len(wave)] = 0
         prompt_nodes = np.zeros(len(wave), dtype=np.int64)
-        ptrs = (tokens_p, indptr_p, prompt_nodes.ctypes.data)
-        # in-batch prefix rule: each batch runs to the first request that would
-        # share more with an earlier member than the tree gives it
-        start = 0
-        while start < len(wave):
-            end = self.cache.batch_end_p(tokens_p, indptr_p, start, len(wave))
-            self._extend_batch(wave, start, end, indptr, ptrs)
-            start = end
+        if self.host_slots or self.chunk_tokens:
+            ptrs = (tokens_p, indptr_p, prompt_nodes.ctypes.data)
+            # in-batch prefix rule: each batch runs to the first request that
+            # would share more with an earlier member than the tree gives it
+            start = 0
+            while start < len(wave):
+                end = self.cache.batch_end_p(tokens_p, indptr_p, start, len(wave))
+                self._extend_batch(wave, start, end, indptr, ptrs)
+                start = end
+        else:
+            self._extend_wave(wave, lens, tokens_p, indptr_p, prompt_nodes)
         if wl.decode_steps:
             self._decode_phase(wave, lens.astype(np.int32), prompt_nodes)
         # finish: insert prompt ++ outputs, unlock
@@ -775,6 +781,121 @@ class Engine:
         self.cache.extend_end_p(R, tokens_p, ind_p, table_p, self.max_ctx, prefix_p, mnodes_p,
                                 nodes_out_p + 8 * r0)
         self.batch_no += 1
+
+    def _extend_wave(self, wave, lens, tokens_p, indptr_p, prompt_nodes):
+        """Every extend batch of a wave: the bookkeeping of all its batches in
+        one native call (``rx_extend_wave``: the in-batch rule, match, lock,
+        allocation, insert, batch after batch), then, with a device, one
+        upload of every batch's rows and plans and one native call per layer
+        that launches each batch's store and attention in batch order
+        (``rx_extend_batches``)."""
+        R = len(wave)
+        ends, prefix, new = self._w_ends, self._b_prefix, self._b_new
+        nb = self.cache.extend_wave_p(R, tokens_p, indptr_p, self._h_table_p, self.max_ctx, ends,
+                                      prefix, prompt_nodes, new, self._w_rew)
+        prefix = prefix[:R].copy()
+        sfx = lens - prefix
+        total = int(sfx.sum())
+        new_slots = new[:total].copy()
+        bounds = [0] + ends[:nb].tolist()
+        # each row as its batch's kernels read it: the matched slots, then the
+        # request's new slots (rx_extend_end may since have swapped the new
+        # slots of a prompt an earlier batch inserted whole for the tree's)
+        W = int(lens.max())
+        rows = self.h_table[:R, :W].copy()
+        rew = self._w_rew[:nb]
+        if rew.any():
+            col = np.arange(W)
+            rows[(col[None, :] >= prefix[:, None]) & (col[None, :] < lens[:, None])] = new_slots
+        pre, ln = prefix.tolist(), lens.tolist()
+        for b in range(nb):
+            self.trace.batches.append([(wave[j].rid, pre[j], rows[j, :ln[j]])
+                                       for j in range(bounds[b], bounds[b + 1])])
+        self.trace.prefilled += total
+        if self.device is not None:
+            self._extend_wave_device(wave, bounds, prefix, sfx, rows, new_slots)
+        self.batch_no += nb
+
+    def _extend_wave_device(self, wave, bounds, prefix, sfx, rows, new_slots):
+        wl = self.wl
+        R, nb = len(wave), len(bounds) - 1
+        # query offsets and tile plans of the whole wave (a request's tiles
+        # depend on its own suffix only), cut per batch: batch b's R_b + 1
+        # entries start at position bounds[b] + b of the concatenated arrays
+        qo_w = np.zeros(R + 1, dtype=np.int32)
+        np.cumsum(sfx, out=qo_w[1:])
+        tiles_w, _ = rx.extend_plan(qo_w, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
+        starts = np.asarray(bounds[:-1], dtype=np.int64)
+        cnt = np.diff(np.asarray(bounds, dtype=np.int64)) + 1
+        first = np.repeat(np.cumsum(cnt) - cnt, cnt)
+        idx = np.repeat(starts, cnt) + (np.arange(R + nb) - first)
+        qo_c = qo_w[idx] - np.repeat(qo_w[starts], cnt)
+        tiles_c = tiles_w[idx] - np.repeat(tiles_w[starts], cnt)
+        W = rows.shape[1]
+        d_rows, d_prefix, d_qo, d_tiles, d_slots, d_tab = self.staging.upload([
+            np.arange(R, dtype=np.int32), prefix, qo_c, tiles_c, new_slots, rows.ravel()])
+        rec = np.zeros(nb, dtype=rx.EXTEND_BATCH_DTYPE)
+        bo = np.asarray(bounds, dtype=np.int64)
+        qo_at = qo_w[bo].astype(np.int64)
+        rec["n_new"] = qo_at[1:] - qo_at[:-1]
+        rec["num_tiles"] = tiles_w[bo[1:]] - tiles_w[bo[:-1]]
+        rec["row_stride"] = W
+        rec["R"] = bo[1:] - bo[:-1]
+        rec["d_req_to_token"] = d_tab.ptr
+        rec["d_req_rows"] = d_rows.ptr + 4 * bo[:-1]
+        rec["d_prefix_len"] = d_prefix.ptr + 4 * bo[:-1]
+        off = 4 * (bo[:-1] + np.arange(nb))
+        rec["d_qo_indptr"] = d_qo.ptr + off
+        rec["d_tile_indptr"] = d_tiles.ptr + off
+        rec["d_new_slots"] = d_slots.ptr + 4 * qo_at[:-1]
+        b0 = self.batch_no
+        n_new = rec["n_new"].tolist()
+        flops = [self._extend_flops(prefix[bounds[b]:bounds[b + 1]],
+                                    qo_c[bounds[b] + b:bounds[b + 1] + b + 1])
+                 for b in range(nb)] if self.timing else None
+        outs = [dict() for _ in range(nb)]
+
+        def fill(b, inp, layer):
+            q, k, v = inp[layer]
+            o, l = self._outputs(("ext", b0 + b, layer), (n_new[b], wl.num_q_heads, wl.head_dim))
+            for f, t in (("d_q", q), ("d_k", k), ("d_v", v), ("d_out", o), ("d_lse", l)):
+                rec[f][b] = t.data_ptr()
+            outs[b][layer] = (o, l)
+
+        def launch(layer, lo, hi):
+            ev = self._events.take(4 * (hi - lo)) if self.timing else None
+            rx.extend_batches(self.pool, layer, wl.num_q_heads, rec[lo:hi], self.scale, ev,
+                              self.stream)
+            self.gpu_launches += 2 * (hi - lo)
+            if ev is not None:
+                for b in range(lo, hi):
+                    e = [rx.NativeEvent(x) for x in ev[4 * (b - lo):4 * (b - lo) + 4]]
+                    self.kernel_events.append(
+                        ("kv_store", e[0], e[1],
+                         float(4 * total_new_bytes(n_new[b], wl) + 4 * n_new[b])))
+                    self.kernel_events.append(("extend", e[2], e[3], flops[b]))
+
+        if self.out_ring is not None or getattr(self.inputs, "host", False):
+            # rings of inputs or outputs hand a buffer out on the understanding
+            # that the work on the one before it is enqueued: batch by batch
+            for b in range(nb):
+                inp = self.inputs.extend(b0 + b, wave[bounds[b]:bounds[b + 1]],
+                                         prefix[bounds[b]:bounds[b + 1]])
+                for layer in self.layers:
+                    fill(b, inp, layer)
+                    launch(layer, b, b + 1)
+        else:
+            inputs = [self.inputs.extend(b0 + b, wave[bounds[b]:bounds[b + 1]],
+                                         prefix[bounds[b]:bounds[b + 1]]) for b in range(nb)]
+            for layer in self.layers:
+                for b in range(nb):
+                    fill(b, inputs[b], layer)
+                launch(layer, 0, nb)
+        if self.on_extend is not None:
+            for b in range(nb):
+                j0, j1 = bounds[b], bounds[b + 1]
+                self.on_extend(b0 + b, [r.rid for r in wave[j0:j1]], prefix[j0:j1].copy(),
+                               qo_c[j0 + b:j1 + b + 1].copy(), outs[b])
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):
         torch = self.torch

@@ -79,6 +79,23 @@ DECODE_STEP_DTYPE = np.dtype([("d_q", np.uint64), ("d_k", np.uint64), ("d_v", np
                               ("step", np.int32), ("reserved", np.int32)])
 assert DECODE_STEP_DTYPE.itemsize == C.sizeof(rx_decode_step)
 
+# rx_extend_batch as a numpy record (pointers as uint64)
+_EXT_PTRS = ("d_q", "d_k", "d_v", "d_new_slots", "d_req_to_token", "d_req_rows",
+             "d_prefix_len", "d_qo_indptr", "d_tile_indptr", "d_out", "d_lse")
+EXTEND_BATCH_DTYPE = np.dtype([(n, np.uint64) for n in _EXT_PTRS] +
+                              [("n_new", np.int64), ("num_tiles", np.int64),
+                               ("row_stride", np.int64), ("R", np.int32),
+                               ("reserved", np.int32)])
+
+
+class rx_extend_batch(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in _EXT_PTRS] + [
+        ("n_new", C.c_int64), ("num_tiles", C.c_int64), ("row_stride", C.c_int64),
+        ("R", C.c_int32), ("reserved", C.c_int32)]
+
+
+assert EXTEND_BATCH_DTYPE.itemsize == C.sizeof(rx_extend_batch)
+
 
 class rx_pool_desc(C.Structure):
     _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("num_slots", C.c_int64),
@@ -114,6 +131,7 @@ _SIGS = {
     "rx_host_eviction_log": [P, I64, P, I64, P],
     "rx_debug_fail_alloc": [P, I64],
     "rx_host_alloc": [SZ, P],
+    "rx_extend_wave": [P, I32, P, P, P, I64, P, P, P, P, P, P],
     "rx_host_free": [P],
     "rx_batch_conflict": [P, I64, I64, I32, P, P, P],
     "rx_batch_end": [P, P, P, I32, I32, P],
@@ -132,6 +150,10 @@ _SIGS = {
     "rx_decode_attention": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P, SZ, P],
     "rx_decode_attention_static": [P, I32, P, I32, P, I64, P, P, I32, F32, P, P, P],
     "rx_decode_steps": [P, I32, I32, P, I64, P, I32, I32, F32, P, SZ, P],
+    "rx_extend_batches": [P, I32, I32, P, I32, F32, P, P],
+    "rx_events_create": [I32, P],
+    "rx_events_destroy": [I32, P],
+    "rx_event_elapsed_ms": [P, P, P],
     "rx_device_check": [P],
 }
 for _name, _args in _SIGS.items():
@@ -241,6 +263,17 @@ class RadixCache:
                                   int(row_stride), prefix_p, nodes_p, out_nodes_p,
                                   C.byref(self._i64)))
         return self._i64.value
+
+    def extend_wave_p(self, R, tokens_p, indptr_p, table_p, row_stride, ends, prefix, nodes,
+                      new_slots, rewritten):
+        """rx_extend_wave with the wave's arrays by address and caller-owned
+        output arrays (numpy: int32 ends [R], int32 prefix [R], int64 nodes
+        [R], int32 new_slots [total tokens], int64 rewritten [R]); returns
+        the number of batches."""
+        _check(_lib.rx_extend_wave(self._h, int(R), tokens_p, indptr_p, table_p, int(row_stride),
+                                   _p(ends), C.byref(self._i32), _p(prefix), _p(nodes),
+                                   _p(new_slots), _p(rewritten)))
+        return self._i32.value
 
     # S1
     def match_length(self, tokens):
@@ -533,6 +566,60 @@ def decode_attention(pool, layer, d_q, hq, d_table, d_plan, info, B, scale, d_ou
                                     d_out.data_ptr(), d_lse.data_ptr(), d_workspace.data_ptr(),
                                     d_workspace.numel() * d_workspace.element_size(),
                                     _stream(stream)))
+
+
+def extend_batches(pool, layer, hq, batches, scale, events=None, stream=None):
+    """rx_extend_batches over a numpy array of EXTEND_BATCH_DTYPE records;
+    ``events`` is None or a uint64 array of 4 event handles per batch."""
+    assert batches.dtype == EXTEND_BATCH_DTYPE and batches.flags.c_contiguous
+    ev = None
+    if events is not None:
+        assert events.dtype == np.uint64 and len(events) >= 4 * len(batches)
+        ev = events.ctypes.data
+    _check(_lib.rx_extend_batches(C.byref(pool), layer, hq, batches.ctypes.data, len(batches),
+                                  scale, ev, _stream(stream)))
+
+
+class EventPool:
+    """Timing events made by the library (``rx_events_create``), handed out
+    in blocks and never reused while the pool lives; ``close`` destroys
+    them."""
+
+    def __init__(self, block=1024):
+        self.block = block
+        self.blocks = []
+        self.cur = None
+        self.used = 0
+
+    def take(self, n):
+        """A uint64 array of n fresh event handles (consecutive)."""
+        if self.cur is None or self.used + n > len(self.cur):
+            blk = np.zeros(max(self.block, n), dtype=np.uint64)
+            _check(_lib.rx_events_create(len(blk), blk.ctypes.data))
+            self.blocks.append(blk)
+            self.cur, self.used = blk, 0
+        out = self.cur[self.used:self.used + n]
+        self.used += n
+        return out
+
+    def close(self):
+        for blk in self.blocks:
+            _lib.rx_events_destroy(len(blk), blk.ctypes.data)
+        self.blocks, self.cur, self.used = [], None, 0
+
+
+class NativeEvent:
+    """One library event; ``elapsed_time(end)`` in milliseconds, as a
+    torch.cuda.Event gives it."""
+    __slots__ = ("h",)
+
+    def __init__(self, h):
+        self.h = int(h)
+
+    def elapsed_time(self, end):
+        ms = C.c_float()
+        _check(_lib.rx_event_elapsed_ms(C.c_void_p(self.h), C.c_void_p(end.h), C.byref(ms)))
+        return ms.value
 
 
 def decode_steps(pool, layer, hq, d_table, steps, B, scale, d_workspace, stream=None):

@@ -1,8 +1,8 @@
 // Randomised stress of the host radix cache through its C ABI, built with
 // AddressSanitizer and UndefinedBehaviorSanitizer by tests/test_sanitizers.py.
 // Every call of the host cache is exercised (match, lock, alloc, insert,
-// evict, free, pages, batch steps, decode planning, scheduling, the two tiers,
-// draft rows, fault injection) on small pools so that eviction, splits and
+// evict, free, pages, batch steps, whole-wave extends, decode planning,
+// scheduling, the two tiers, draft rows, fault injection) on small pools so that eviction, splits and
 // page boundaries are frequent; after every operation the cache's counts must
 // agree: evictable + protected == cached.  Any memory error or undefined
 // behaviour aborts the run through the sanitizers.
@@ -60,7 +60,7 @@ int main(int argc, char** argv) {
       const int n = uni(1, 14);
       std::vector<int32_t> t(static_cast<size_t>(n));
       for (auto& x : t) x = uni(0, 2);
-      const int op = uni(0, 15);
+      const int op = uni(0, 16);
       int64_t len = 0, already = 0, hl = 0, got = 0, tk = 0;
       rx_node node = 0, node2 = 0, hn = 0;
       switch (op) {
@@ -173,6 +173,34 @@ int main(int argc, char** argv) {
           const int32_t ds[4] = {9, 10, 11, 12};
           std::vector<int32_t> rows(4 * 8), ctx(4), pos(4);
           rx_verify_rows(1, pl, pr, 4, di, par, ds, rows.data(), 8, ctx.data(), pos.data());
+          break;
+        }
+        case 12: {  // a whole wave's extend bookkeeping, then its locks released
+          std::vector<int32_t> toks;
+          std::vector<int64_t> ind{0};
+          const int R = uni(1, 5);
+          for (int r = 0; r < R; ++r) {
+            const int m = uni(1, 10);
+            for (int k = 0; k < m; ++k) toks.push_back(uni(0, 2));
+            ind.push_back(int64_t(toks.size()));
+          }
+          std::vector<int32_t> table(static_cast<size_t>(R) * 10), ends(static_cast<size_t>(R)),
+              pre(static_cast<size_t>(R)), fresh(toks.size());
+          std::vector<rx_node> nodes(static_cast<size_t>(R));
+          std::vector<int64_t> rew(static_cast<size_t>(R));
+          int32_t nb = 0;
+          if (rx_extend_wave(c, R, toks.data(), ind.data(), table.data(), 10, ends.data(), &nb,
+                             pre.data(), nodes.data(), fresh.data(), rew.data()) == RX_OK) {
+            for (int r = 0; r < R; ++r) {
+              // the partly filled last page stays with the request: free it
+              const int64_t n = ind[size_t(r) + 1] - ind[size_t(r)];
+              if (n % ps) rx_free(c, table.data() + size_t(r) * 10 + (n - n % ps), 1);
+              rx_unlock(c, nodes[size_t(r)]);
+            }
+          } else {
+            for (int32_t b = 0, r = 0; b < nb; ++b)
+              for (; r < ends[size_t(b)]; ++r) rx_unlock(c, nodes[size_t(r)]);
+          }
           break;
         }
         default: {

@@ -328,3 +328,42 @@ def test_two_tier_chat_parity(host_slots, page_size):
     assert len(run.trace.loads) > 0
     if host_slots == 704:
         assert len(run.trace.host_eviction_log) > 0
+
+
+@pytest.mark.parametrize("name", ["fork_evict", "chat_d256", "fork_evict_p4"])
+def test_wave_launches_equal_batch_launches(name):
+    """A wave's extend batches launched by one native call per layer
+    (rx_extend_batches over every batch of the wave) give bit for bit the
+    outputs of launching batch by batch (the per-batch path), and the timing
+    events it records bracket each batch's store and attention."""
+    from radix_tree_prefix_gb300.engine import Engine, GatherInputs, PreparedInputs
+
+    dev = torch.device("cuda:0")
+    wl = SMALL[name][0]()
+    layers = list(range(wl.num_layers))
+    vals = workloads.make_values(wl, dev, layers)
+
+    def run(**kw):
+        store = {}
+
+        def on_ext(b, rids, prefix, qo, outs):
+            store[b] = [tuple(x.clone() for x in outs[ly]) for ly in layers]
+        eng = Engine(wl, device=dev, inputs=PreparedInputs(GatherInputs(wl, vals, layers)),
+                     layers=layers, on_extend=on_ext, **kw)
+        trace = eng.run()
+        torch.cuda.synchronize()
+        return store, trace, eng
+
+    per_batch, t0, _ = run(chunk_tokens=1 << 30)
+    waved, t1, eng = run(timing=True)
+    assert t0.as_tuple() == t1.as_tuple()
+    assert len(t1.batches) > len(wl.waves)          # waves of several batches
+    assert per_batch.keys() == waved.keys()
+    for b in per_batch:
+        for x, y in zip(per_batch[b], waved[b]):
+            for a, c in zip(x, y):
+                assert torch.equal(a, c), b
+    kinds = [k for k, *_ in eng.kernel_events if k in ("kv_store", "extend")]
+    assert kinds.count("extend") == kinds.count("kv_store") == len(t1.batches) * len(layers)
+    assert all(a.elapsed_time(e) > 0 for k, a, e, _ in eng.kernel_events if k == "extend")
+    assert rx.device_check() == 0

@@ -802,3 +802,115 @@ def test_injected_failure_in_the_request_flow_is_reported_and_recoverable():
             rx.RadixCache = orig
         st = eng.cache.stats()
         assert st["evictable_tokens"] + st["protected_tokens"] == st["cached_tokens"]
+
+
+def _wave_prompts(rng, n, page_size):
+    """Prompts with shared heads, identical copies and one-token prompts."""
+    base = rng.integers(1, 40, size=400).astype(np.int32)
+    out = []
+    for i in range(n):
+        if out and rng.random() < 0.15:
+            out.append(out[int(rng.integers(0, len(out)))].copy())     # identical
+            continue
+        cut = int(rng.choice([0, page_size, 40, 120, 121, 300]))
+        tail = rng.integers(1, 40, size=int(rng.integers(1, 60))).astype(np.int32)
+        out.append(np.concatenate([base[:cut], tail]))
+    out.append(base[:1].copy())
+    tokens = np.concatenate(out).astype(np.int32)
+    indptr = np.zeros(len(out) + 1, dtype=np.int64)
+    np.cumsum([len(p) for p in out], out=indptr[1:])
+    return tokens, indptr
+
+
+def _by_batches(c, tokens, indptr, stride):
+    """The wave through rx_batch_end / rx_extend_begin / rx_extend_end."""
+    R = len(indptr) - 1
+    table = np.zeros((R, stride), dtype=np.int32)
+    ends, prefix, nodes, new, rew = [], np.zeros(R, np.int32), np.zeros(R, np.int64), [], []
+    start = 0
+    while start < R:
+        end = c.batch_end(tokens, indptr, start)
+        n = end - start
+        pre = np.zeros(n, np.int32)
+        mn = np.zeros(n, np.int64)
+        nw = np.zeros(int(indptr[end] - indptr[start]), np.int32)
+        ind = np.ascontiguousarray(indptr[start:end + 1])
+        tot = c.extend_begin_p(n, tokens.ctypes.data, ind.ctypes.data,
+                               table[start:].ctypes.data, stride, pre.ctypes.data,
+                               mn.ctypes.data, nw.ctypes.data)
+        new.append(nw[:tot])
+        rew.append(c.extend_end_p(n, tokens.ctypes.data, ind.ctypes.data,
+                                  table[start:].ctypes.data, stride, pre.ctypes.data,
+                                  mn.ctypes.data, nodes[start:].ctypes.data))
+        prefix[start:end] = pre
+        ends.append(end)
+        start = end
+    return ends, prefix, nodes, np.concatenate(new), rew, table
+
+
+@pytest.mark.parametrize("page_size", [1, 4])
+def test_extend_wave_equals_batch_by_batch_calls(page_size):
+    """rx_extend_wave makes exactly the decisions of the per-batch calls:
+    batch ends, prefixes, nodes, new slots, rewritten rows, final rows, the
+    eviction log and the cache's counts; identical prompts are rewritten to
+    the tree's slots in both."""
+    rng = np.random.default_rng(11 + page_size)
+    evicted = rewritten = 0
+    for trial in range(6):
+        tokens, indptr = _wave_prompts(rng, 24, page_size)
+        R, stride = len(indptr) - 1, int(np.max(np.diff(indptr)))
+        # what the wave holds at once (a generous pool, no history)
+        big = rx.RadixCache(1 << 16, page_size)
+        _by_batches(big, tokens, indptr, stride)
+        held = big.stats()["cached_tokens"] + R * page_size
+        # odd trials: the 88-token history must be partly evicted
+        slots = -(-(held + (40 if trial % 2 else 400)) // page_size) * page_size
+        a = rx.RadixCache(slots, page_size)
+        b = rx.RadixCache(slots, page_size)
+        hist = rng.integers(40, 80, size=88).astype(np.int32)
+        for c in (a, b):
+            c.insert(hist, c.alloc(88))
+        ends, prefix, nodes, new, rew, table = _by_batches(a, tokens, indptr, stride)
+        w_table = np.zeros((R, stride), dtype=np.int32)
+        w_ends = np.zeros(R, np.int32)
+        w_pre = np.zeros(R, np.int32)
+        w_nodes = np.zeros(R, np.int64)
+        w_new = np.zeros(int(indptr[-1]), np.int32)
+        w_rew = np.zeros(R, np.int64)
+        nb = b.extend_wave_p(R, tokens.ctypes.data, indptr.ctypes.data, w_table.ctypes.data,
+                             stride, w_ends, w_pre, w_nodes, w_new, w_rew)
+        assert w_ends[:nb].tolist() == ends
+        assert np.array_equal(w_pre, prefix) and np.array_equal(w_nodes, nodes)
+        assert np.array_equal(w_new[:len(new)], new)
+        assert w_rew[:nb].tolist() == rew
+        assert np.array_equal(w_table, table)
+        assert a.eviction_log() == b.eviction_log() and a.stats() == b.stats()
+        evicted += len(a.eviction_log()) > 0
+        rewritten += sum(rew)
+    assert evicted and rewritten      # both branches were taken
+
+
+def test_extend_wave_failure_keeps_earlier_batches():
+    """An allocation failing in a later batch: the call reports it, the
+    batches before it stay done (their nodes locked) and the failing batch
+    holds no lock."""
+    rng = np.random.default_rng(3)
+    tokens, indptr = _wave_prompts(rng, 12, 1)
+    R, stride = len(indptr) - 1, int(np.max(np.diff(indptr)))
+    c = rx.RadixCache(5000)
+    ref = rx.RadixCache(5000)
+    ends, *_ = _by_batches(ref, tokens, indptr, stride)
+    assert len(ends) >= 2
+    c.debug_fail_alloc(2)       # the second batch's allocation fails
+    out = [np.zeros(R, np.int32), np.zeros(R, np.int32), np.zeros(R, np.int64),
+           np.zeros(int(indptr[-1]), np.int32), np.zeros(R, np.int64)]
+    table = np.zeros((R, stride), dtype=np.int32)
+    with pytest.raises(rx.NoSpace):
+        c.extend_wave_p(R, tokens.ctypes.data, indptr.ctypes.data, table.ctypes.data, stride,
+                        *out)
+    st = c.stats()
+    first = int(indptr[ends[0]])
+    # the first batch's prompts are in the tree and protected; nothing else is
+    assert st["protected_tokens"] == st["cached_tokens"]
+    assert 0 < st["cached_tokens"] <= first
+    c.debug_fail_alloc(0)
