@@ -422,11 +422,10 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
         host.freeze()
         prepared.ext.clear()
         prepared.dec.clear()
+        most = max([eng.max_extend_rows] + [len(w) * wl.decode_steps for w in wl.waves])
         del eng
         torch.cuda.empty_cache()
         hq, d = wl.num_q_heads, wl.head_dim
-        most = max([sum(len(row) - m for _, m, row in b) for b in trace.batches] +
-                   [len(w) * wl.decode_steps for w in wl.waves])
         # as many output buffers as fit in E2E_RING_BYTES (at least 4), so the
         # read-back of a batch's outputs can trail its kernels
         per = most * hq * (d + 1)

@@ -577,6 +577,7 @@ class Engine:
         self._w_ends = np.zeros(self.max_wave, dtype=np.int32)
         self._w_rew = np.zeros(self.max_wave, dtype=np.int64)
         self._events = rx.EventPool() if device is not None else None
+        self.max_extend_rows = 0      # query rows of the largest extend launch so far
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
 
     # ------------------------------------------------------------------ run
@@ -817,50 +818,71 @@ class Engine:
         self.batch_no += nb
 
     def _extend_wave_device(self, wave, bounds, prefix, sfx, rows, new_slots):
+        """A wave's extend batches on the device, in launch groups: a group is
+        a run of consecutive batches in which only the last may have rows that
+        rx_extend_end rewrote.  Per group and layer one store of all its new
+        tokens' K/V, then one attention over all its requests.  That equals
+        launching batch by batch: a batch's prefix may end in tokens an
+        earlier batch of its group stored, which the group's store has
+        written before its attention runs; no slot is stored twice within a
+        group, since slots become free during a wave's bookkeeping only by
+        eviction (of nodes no batch of the wave reads, which are locked) or
+        by a rewrite, which ends the group; and a rewritten request's row as
+        its kernels read it holds its own new slots, which later groups
+        reuse only after its attention ran (one stream)."""
         wl = self.wl
         R, nb = len(wave), len(bounds) - 1
+        rew = self._w_rew[:nb]
+        gb = [0] + [b + 1 for b in range(nb - 1) if rew[b] > 0] + [nb]
+        gbounds = [bounds[g] for g in gb]
+        ng = len(gb) - 1
         # query offsets and tile plans of the whole wave (a request's tiles
-        # depend on its own suffix only), cut per batch: batch b's R_b + 1
-        # entries start at position bounds[b] + b of the concatenated arrays
+        # depend on its own suffix only), cut per group: group g's R_g + 1
+        # entries start at position gbounds[g] + g of the concatenated arrays
         qo_w = np.zeros(R + 1, dtype=np.int32)
         np.cumsum(sfx, out=qo_w[1:])
         tiles_w, _ = rx.extend_plan(qo_w, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
-        starts = np.asarray(bounds[:-1], dtype=np.int64)
-        cnt = np.diff(np.asarray(bounds, dtype=np.int64)) + 1
+        go = np.asarray(gbounds, dtype=np.int64)
+        cnt = np.diff(go) + 1
         first = np.repeat(np.cumsum(cnt) - cnt, cnt)
-        idx = np.repeat(starts, cnt) + (np.arange(R + nb) - first)
-        qo_c = qo_w[idx] - np.repeat(qo_w[starts], cnt)
-        tiles_c = tiles_w[idx] - np.repeat(tiles_w[starts], cnt)
+        idx = np.repeat(go[:-1], cnt) + (np.arange(R + ng) - first)
+        qo_c = qo_w[idx] - np.repeat(qo_w[go[:-1]], cnt)
+        tiles_c = tiles_w[idx] - np.repeat(tiles_w[go[:-1]], cnt)
         W = rows.shape[1]
         d_rows, d_prefix, d_qo, d_tiles, d_slots, d_tab = self.staging.upload([
             np.arange(R, dtype=np.int32), prefix, qo_c, tiles_c, new_slots, rows.ravel()])
-        rec = np.zeros(nb, dtype=rx.EXTEND_BATCH_DTYPE)
-        bo = np.asarray(bounds, dtype=np.int64)
-        qo_at = qo_w[bo].astype(np.int64)
+        rec = np.zeros(ng, dtype=rx.EXTEND_BATCH_DTYPE)
+        qo_at = qo_w[go].astype(np.int64)
         rec["n_new"] = qo_at[1:] - qo_at[:-1]
-        rec["num_tiles"] = tiles_w[bo[1:]] - tiles_w[bo[:-1]]
+        rec["num_tiles"] = tiles_w[go[1:]] - tiles_w[go[:-1]]
         rec["row_stride"] = W
-        rec["R"] = bo[1:] - bo[:-1]
+        rec["R"] = go[1:] - go[:-1]
         rec["d_req_to_token"] = d_tab.ptr
-        rec["d_req_rows"] = d_rows.ptr + 4 * bo[:-1]
-        rec["d_prefix_len"] = d_prefix.ptr + 4 * bo[:-1]
-        off = 4 * (bo[:-1] + np.arange(nb))
+        rec["d_req_rows"] = d_rows.ptr + 4 * go[:-1]
+        rec["d_prefix_len"] = d_prefix.ptr + 4 * go[:-1]
+        off = 4 * (go[:-1] + np.arange(ng))
         rec["d_qo_indptr"] = d_qo.ptr + off
         rec["d_tile_indptr"] = d_tiles.ptr + off
         rec["d_new_slots"] = d_slots.ptr + 4 * qo_at[:-1]
         b0 = self.batch_no
         n_new = rec["n_new"].tolist()
-        flops = [self._extend_flops(prefix[bounds[b]:bounds[b + 1]],
-                                    qo_c[bounds[b] + b:bounds[b + 1] + b + 1])
-                 for b in range(nb)] if self.timing else None
-        outs = [dict() for _ in range(nb)]
+        self.max_extend_rows = max([self.max_extend_rows] + n_new)
+        flops = [self._extend_flops(prefix[gbounds[g]:gbounds[g + 1]],
+                                    qo_c[gbounds[g] + g:gbounds[g + 1] + g + 1])
+                 for g in range(ng)] if self.timing else None
+        outs = [dict() for _ in range(ng)]
 
-        def fill(b, inp, layer):
+        def group_inputs(g):
+            j0, j1 = gbounds[g], gbounds[g + 1]
+            return self.inputs.extend(b0 + gb[g], wave[j0:j1], prefix[j0:j1])
+
+        def fill(g, inp, layer):
             q, k, v = inp[layer]
-            o, l = self._outputs(("ext", b0 + b, layer), (n_new[b], wl.num_q_heads, wl.head_dim))
+            o, l = self._outputs(("ext", b0 + gb[g], layer),
+                                 (n_new[g], wl.num_q_heads, wl.head_dim))
             for f, t in (("d_q", q), ("d_k", k), ("d_v", v), ("d_out", o), ("d_lse", l)):
-                rec[f][b] = t.data_ptr()
-            outs[b][layer] = (o, l)
+                rec[f][g] = t.data_ptr()
+            outs[g][layer] = (o, l)
 
         def launch(layer, lo, hi):
             ev = self._events.take(4 * (hi - lo)) if self.timing else None
@@ -868,34 +890,37 @@ class Engine:
                               self.stream)
             self.gpu_launches += 2 * (hi - lo)
             if ev is not None:
-                for b in range(lo, hi):
-                    e = [rx.NativeEvent(x) for x in ev[4 * (b - lo):4 * (b - lo) + 4]]
+                for g in range(lo, hi):
+                    e = [rx.NativeEvent(x) for x in ev[4 * (g - lo):4 * (g - lo) + 4]]
                     self.kernel_events.append(
                         ("kv_store", e[0], e[1],
-                         float(4 * total_new_bytes(n_new[b], wl) + 4 * n_new[b])))
-                    self.kernel_events.append(("extend", e[2], e[3], flops[b]))
+                         float(4 * total_new_bytes(n_new[g], wl) + 4 * n_new[g])))
+                    self.kernel_events.append(("extend", e[2], e[3], flops[g]))
 
         if self.out_ring is not None or getattr(self.inputs, "host", False):
             # rings of inputs or outputs hand a buffer out on the understanding
-            # that the work on the one before it is enqueued: batch by batch
-            for b in range(nb):
-                inp = self.inputs.extend(b0 + b, wave[bounds[b]:bounds[b + 1]],
-                                         prefix[bounds[b]:bounds[b + 1]])
+            # that the work on the one before it is enqueued: group by group
+            for g in range(ng):
+                inp = group_inputs(g)
                 for layer in self.layers:
-                    fill(b, inp, layer)
-                    launch(layer, b, b + 1)
+                    fill(g, inp, layer)
+                    launch(layer, g, g + 1)
         else:
-            inputs = [self.inputs.extend(b0 + b, wave[bounds[b]:bounds[b + 1]],
-                                         prefix[bounds[b]:bounds[b + 1]]) for b in range(nb)]
+            inputs = [group_inputs(g) for g in range(ng)]
             for layer in self.layers:
-                for b in range(nb):
-                    fill(b, inputs[b], layer)
-                launch(layer, 0, nb)
+                for g in range(ng):
+                    fill(g, inputs[g], layer)
+                launch(layer, 0, ng)
         if self.on_extend is not None:
-            for b in range(nb):
-                j0, j1 = bounds[b], bounds[b + 1]
-                self.on_extend(b0 + b, [r.rid for r in wave[j0:j1]], prefix[j0:j1].copy(),
-                               qo_c[j0 + b:j1 + b + 1].copy(), outs[b])
+            qo_l = qo_w.tolist()
+            for g in range(ng):
+                for b in range(gb[g], gb[g + 1]):
+                    j0, j1 = bounds[b], bounds[b + 1]
+                    q0, q1 = qo_l[j0] - qo_l[gbounds[g]], qo_l[j1] - qo_l[gbounds[g]]
+                    qo = qo_w[j0:j1 + 1] - qo_w[j0]
+                    self.on_extend(b0 + b, [r.rid for r in wave[j0:j1]], prefix[j0:j1].copy(),
+                                   qo, {ly: (o[q0:q1], l[q0:q1])
+                                        for ly, (o, l) in outs[g].items()})
 
     def _extend_device(self, reqs, j0, j1, prefix, ind, new_slots):
         torch = self.torch
@@ -916,6 +941,7 @@ class Engine:
         d_tab.shape = (R, width)
         inputs = self.inputs.extend(self.batch_no, reqs, prefix)
         total_q = int(qo[-1])
+        self.max_extend_rows = max(self.max_extend_rows, total_q)
         flops = self._extend_flops(prefix, qo) if self.timing else 0.0
         outs = {}
         store_bytes = float(4 * total_new_bytes(len(new_slots), wl) + 4 * len(new_slots))

@@ -330,16 +330,31 @@ def test_two_tier_chat_parity(host_slots, page_size):
         assert len(run.trace.host_eviction_log) > 0
 
 
-@pytest.mark.parametrize("name", ["fork_evict", "chat_d256", "fork_evict_p4"])
+def _dup_waves(pool=735):
+    """Identical prompts in one wave: the second's row is rewritten to the
+    tree's slots and its own new slot freed, and a later batch of the same
+    wave, short of free slots, takes that slot again (then evicts the first
+    wave's history for the rest)."""
+    s = workloads._Segments(91)
+    base, x, a, big, tail = s.new(300), s.new(200), s.new(40), s.new(150), s.new(60)
+    outs = [s.new(3) for _ in range(5)]
+    waves = [[Request(0, (base, x), outs[0])],
+             [Request(1, (base, a), outs[1]), Request(2, (base, a), outs[2]),
+              Request(3, (base, big), outs[3]), Request(4, (base, big, tail), outs[4])]]
+    return Workload("dups", 1, 16, 4, 128, pool, 3, s.tokens, waves, 91)
+
+
+@pytest.mark.parametrize("name", ["fork_evict", "chat_d256", "fork_evict_p4", "dups"])
 def test_wave_launches_equal_batch_launches(name):
-    """A wave's extend batches launched by one native call per layer
-    (rx_extend_batches over every batch of the wave) give bit for bit the
-    outputs of launching batch by batch (the per-batch path), and the timing
-    events it records bracket each batch's store and attention."""
+    """A wave's extend batches launched in groups (rx_extend_batches: per
+    group one store and one attention over all its batches' requests, a
+    group ending at a batch with rewritten rows) give bit for bit the outputs
+    of launching batch by batch (the per-batch path), and the timing events
+    bracket each group's store and attention."""
     from radix_tree_prefix_gb300.engine import Engine, GatherInputs, PreparedInputs
 
     dev = torch.device("cuda:0")
-    wl = SMALL[name][0]()
+    wl = _dup_waves() if name == "dups" else SMALL[name][0]()
     layers = list(range(wl.num_layers))
     vals = workloads.make_values(wl, dev, layers)
 
@@ -364,6 +379,13 @@ def test_wave_launches_equal_batch_launches(name):
             for a, c in zip(x, y):
                 assert torch.equal(a, c), b
     kinds = [k for k, *_ in eng.kernel_events if k in ("kv_store", "extend")]
-    assert kinds.count("extend") == kinds.count("kv_store") == len(t1.batches) * len(layers)
+    n = kinds.count("extend")
+    assert n == kinds.count("kv_store")
+    assert len(wl.waves) * len(layers) <= n < len(t1.batches) * len(layers)
+    if name == "dups":
+        # wave 2's last batch reuses the slot its second batch's rewrite freed
+        new = [int(x) for b in t1.batches[1:] for _, m, row in b for x in row[m:]]
+        assert len(new) > len(set(new)) and len(t1.eviction_log) > 0
+        assert n == 3       # wave 1; wave 2 split after the rewriting batch
     assert all(a.elapsed_time(e) > 0 for k, a, e, _ in eng.kernel_events if k == "extend")
     assert rx.device_check() == 0
