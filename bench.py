@@ -67,16 +67,19 @@ def parse(argv=None):
 # DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
 # captures summarised in profiles/ (cold L2, the current kernels):
 # decode_fused_kernel on one agent_loop and one long_shared decode step; the
-# extend kernel averaged over the launches of one step (long_shared: 2,
-# fork_tree: 130), as `achieved` averages over them; multi_turn_chat's decode
+# extend kernel per launch (one launch per wave and layer, as `achieved`
+# averages over launches); multi_turn_chat's decode
 # launch scaled from a capture of one multi_turn_chat_small decode launch by
 # the ratio of algorithmic bytes (the full workload's pool is beyond the
 # capture size rule).  None (absent) where no capture of that launch exists.
 TRAFFIC = {
     ("agent_loop", "rx_decode_attention"): 44.534e6 + 0.006e6,
     ("long_shared", "rx_decode_attention"): 406.35e6 + 16.01e6,
-    ("long_shared", "rx_extend_attention"): (2230.64e6 + 3158.90e6) / 2,
-    ("fork_tree", "rx_extend_attention"): (5711.18e6 + 887.04e6) / 130,
+    # one launch per wave: long_shared's two batches (captured as two
+    # launches before they were launched together), summed
+    ("long_shared", "rx_extend_attention"): 2230.64e6 + 3158.90e6,
+    # one wave's launch (26 batches), from its capture
+    ("fork_tree", "rx_extend_attention"): 1009.52e6 + 1283.28e6,
     # (69.465 MB read + 0.655 MB written) / 69.865 MB algorithmic on the
     # multi_turn_chat_small launch, times the full workload's 1.0940 GB of
     # algorithmic bytes per decode launch
