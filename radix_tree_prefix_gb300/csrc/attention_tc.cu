@@ -64,6 +64,10 @@ constexpr float kRescaleThreshold = 8.0f;       // log2 units
 constexpr uint32_t kSleepNs = 0;                // MMA / loader waits: plain try_wait polling
 constexpr float kMasked = -1.0e30f;             // raw score of a masked key
 constexpr int kExtendInterleaveWaves = 8;
+// Extend CTA order: heads interleaved also when one request's keys over all
+// KV heads (K and V, bf16) take at most this much: the row tiles in flight
+// then read a few requests' keys, which stay in L2 for every head at once.
+constexpr int64_t kExtendInterleaveKvBytes = 32ll << 20;
 constexpr int BM = 128;
 
 struct TcArgs {
@@ -775,11 +779,12 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   }
 }
 
-// Extend: one tile per CTA, heaviest row tile first.  With few waves of CTAs
-// (heads_interleaved) CTA c takes row tile c / Hkv of KV head c % Hkv, so the
-// heavy tiles of every head go out before the light ones and the last wave
-// is short; with many waves CTA c takes head c / tiles, so the CTAs resident
-// at one time read the keys of one head and those stay in L2.
+// Extend: one tile per CTA, heaviest row tile first.  With heads_interleaved
+// (few waves of CTAs, or short contexts) CTA c takes row tile c / Hkv of KV
+// head c % Hkv, so the heavy tiles of every head go out before the light
+// ones and the last wave is short; otherwise CTA c takes head c / tiles, so
+// the CTAs resident at one time read the keys of one head and those stay in
+// L2.
 template <int D>
 __global__ void __launch_bounds__(kThreads3, 1)
     attn_tc3_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -1441,10 +1446,15 @@ rx_status extend_attention_tc(const rx_pool_desc* pool, int32_t layer, const voi
   a.tile_indptr = d_tile_indptr;
   a.num_req = R;
   a.num_tiles = int(num_tiles);
-  // up to kExtendInterleaveWaves waves of CTAs: heads interleaved (short tail);
-  // more: head-major (L2 locality of long key ranges)
+  // heads interleaved (the heavy row tiles of every head first, a short
+  // tail) for up to kExtendInterleaveWaves waves of CTAs, or when a
+  // request's keys over all heads are small enough to stay in L2 while its
+  // row tiles run (row_stride bounds a request's keys); otherwise
+  // head-major, so the CTAs in flight read one head's long key ranges
+  const int64_t kv_row_bytes = row_stride * pool->num_kv_heads * int64_t(D) * 4;
   a.heads_interleaved =
-      num_tiles * pool->num_kv_heads <= int64_t(kExtendInterleaveWaves) * rx_internal::sm_count();
+      num_tiles * pool->num_kv_heads <= int64_t(kExtendInterleaveWaves) * rx_internal::sm_count() ||
+      kv_row_bytes <= kExtendInterleaveKvBytes;
   a.out = d_out;
   a.lse = d_lse;
   if (D == 128)
