@@ -418,6 +418,7 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
     out = {"wl": wl, "trace": trace, "n_ext": n_ext, "n_dec": n_dec, "ms": ms,
            "kinds": _kind_stats(eng.kernel_events, steps),
            "launches": eng.gpu_launches - launches0, "wall": wall, "e2e": None}
+    eng.close()                             # its timing events are read
     if e2e:
         # host copies of every recorded input, then the device copies go
         host = PreparedInputs(source, host=True, ring=E2E_INPUT_RING)
@@ -464,6 +465,7 @@ def measure(wl, dev, steps, warmup, world, e2e=False, clocks=None):
                                 f"lse) read back through a ring of {ring.slots} device/host "
                                 f"buffer pairs on another stream; steps back to back, one "
                                 f"synchronize after the last"}
+        eng2.close()
         del eng2
         ring.close()
         host.close()

@@ -580,6 +580,12 @@ class Engine:
         self.max_extend_rows = 0      # query rows of the largest extend launch so far
         self.plan_buf = np.empty(1 << 16, dtype=np.int32)
 
+    def close(self):
+        """Releases the library timing events this engine made (the kernel
+        events of earlier timed runs are invalid afterwards)."""
+        if self._events is not None:
+            self._events.close()
+
     # ------------------------------------------------------------------ run
     def run(self):
         self.cache = rx.RadixCache(self.wl.num_slots, self.wl.page_size, self.host_slots)
