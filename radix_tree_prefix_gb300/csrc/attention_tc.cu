@@ -484,8 +484,11 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // 3]); hence S_j completing still implies PV_{j-3} completed, which the
     // softmax's wait on o[] relies on.
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0);
-      constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 1);
+      // a tile of at most 64 rows runs M = 64 products (half the MMA work;
+      // its row r then sits in TMEM lane 32 (r / 16) + r % 16)
+      const bool m64 = t.n_rows <= 64;
+      const uint32_t IDESC_S = m64 ? tc::idesc_bf16(64, BN, 0) : tc::idesc_bf16(BM, BN, 0);
+      const uint32_t IDESC_PV = m64 ? tc::idesc_bf16(64, D, 1) : tc::idesc_bf16(BM, D, 1);
       // shared-memory descriptors (128-byte swizzle, 1024 bytes between
       // 8-row groups): common high half; low halves of Q, K stage 0 (K-major,
       // leading offset 16 B) and V stage 0 (MN-major, leading offset = one
@@ -571,12 +574,29 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // through shared memory (one bounded mbarrier round), so both write P
     // against the same reference and share one O accumulator.
     const int wg = warp >> 2;
-    const int i = (warp & 3) * 32 + lane;
+    const int i = (warp & 3) * 32 + lane;  // TMEM lane
     constexpr int HALF = BN / 2;
+    // the tile row in lane i: row i, or with M = 64 products (at most 64
+    // rows) row 16 (i / 32) + i % 16 in the first 16 lanes of each quadrant
+    const bool m64 = t.n_rows <= 64;
+    const int row = m64 ? (((i >> 5) << 4) | (i & 15)) : i;
     int64_t qi = 0, part = 0;
     int head = 0, lim = t.key_end;
-    const bool valid = i < t.n_rows;
-    if (valid) row_info<DECODE>(a, t, kvh, i, qi, head, part, lim);
+    const bool valid = (!m64 || (i & 16) == 0) && row < t.n_rows;
+    if (valid) row_info<DECODE>(a, t, kvh, row, qi, head, part, lim);
+    // the Q row this thread gathers: tile row i into shared-memory row i
+    // (the A operand's rows, whatever the TMEM layout of the products)
+    int64_t gqi = qi;
+    int ghead = head;
+    bool gvalid = valid;
+    if (m64) {
+      int64_t gpart = 0;
+      int glim = 0;
+      gqi = 0;
+      ghead = 0;
+      gvalid = i < t.n_rows;
+      if (gvalid) row_info<DECODE>(a, t, kvh, i, gqi, ghead, gpart, glim);
+    }
     const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
     float* xch = reinterpret_cast<float*>(gbase + Lo::XCH);  // [2][2 warpgroups][BM]
     // the queries and the outputs (decode: partial buffers the previous
@@ -587,11 +607,11 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     {
       // chunks [8 w, 8 w + 8) of Q row i (zeros past the tile's rows) while
       // the loader warp already streams the first K/V tiles
-      const bf16* src = a.q + (qi * a.hq + head) * D;
+      const bf16* src = a.q + (gqi * a.hq + ghead) * D;
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
         const int ch = wg * (D / 16) + c;
-        rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, valid);
+        rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, gvalid);
       }
       rxk::cp_async_commit();
       rxk::cp_async_wait<0>();

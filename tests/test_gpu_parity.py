@@ -396,3 +396,26 @@ def test_wave_launches_equal_batch_launches(name):
         assert n == 3       # wave 1; wave 2 split after the rewriting batch
     assert all(a.elapsed_time(e) > 0 for k, a, e, _ in eng.kernel_events if k == "extend")
     assert rx.device_check() == 0
+
+
+@pytest.mark.parametrize("head_dim,hq,hkv", [(128, 16, 4), (256, 16, 4), (128, 8, 8)])
+def test_row_tiles_at_the_64_row_boundary(head_dim, hq, hkv):
+    """Row tiles of at most 64 rows run M = 64 tensor-core products (rows in
+    the first 16 TMEM lanes of each quadrant), larger ones M = 128: suffixes
+    of 16 and 17 tokens at G = 4 (64 and 68 rows), 32 and 33 (128, 132),
+    and at G = 1 suffixes of 64 and 65 tokens, over a shared prefix; decode
+    member blocks of 8 and 17 requests take the same split."""
+    G = hq // hkv
+    s = workloads._Segments(404)
+    pre = s.new(300)
+    lens = [16, 17, 32, 33] if G > 1 else [64, 65, 7, 1]
+    outs = [s.new(2) for _ in range(25)]
+    first = [Request(99, (pre,), outs[24])]        # the prefix is cached first
+    wave = [Request(k, (pre, s.new(n)), outs[k]) for k, n in enumerate(lens)]
+    # decode: a shared prefix over 17 requests (G x 17 rows: member blocks
+    # of 128 / G requests and the rest)
+    big = [Request(10 + k, (pre, s.new(3)), outs[4 + k]) for k in range(17)]
+    wl = Workload("m64", 1, hq, hkv, head_dim, 8000, 2, s.tokens, [first, wave, big], 404)
+    run = DeviceRun(wl)
+    run.assert_close()
+    assert [m for _, m, _ in run.trace.batches[1]] == [300] * 4
