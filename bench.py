@@ -79,11 +79,11 @@ TRAFFIC = {
     # launches before they were launched together), summed
     ("long_shared", "rx_extend_attention"): 2230.64e6 + 3158.90e6,
     # one wave's launch (26 batches), from its capture
-    ("fork_tree", "rx_extend_attention"): 1009.52e6 + 1283.28e6,
-    # (69.465 MB read + 0.655 MB written) / 69.865 MB algorithmic on the
+    ("fork_tree", "rx_extend_attention"): 982.84e6 + 1269.86e6,
+    # (69.452 MB read + 0.609 MB written) / 69.865 MB algorithmic on the
     # multi_turn_chat_small launch, times the full workload's 1.0940 GB of
     # algorithmic bytes per decode launch
-    ("multi_turn_chat", "rx_decode_attention"): (69.465e6 + 0.655e6) / 69.865e6 * 1.0940e9,
+    ("multi_turn_chat", "rx_decode_attention"): (69.452e6 + 0.609e6) / 69.865e6 * 1.0940e9,
 }
 
 
