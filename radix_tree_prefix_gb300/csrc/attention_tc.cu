@@ -135,10 +135,24 @@ __device__ __forceinline__ TileDesc describe(const TcArgs& a, int bx) {
     t.gr0 = t.q_base = t.prefix = 0;
   } else {
     const int tile = a.num_tiles - 1 - bx;  // heaviest first
+    // the request of this tile: the last r with tile_indptr[r] <= tile, found
+    // by the warp in rounds of 32 samples (each round one load per lane and
+    // a ballot) instead of a binary search's chain of dependent loads, which
+    // held every CTA's start-up for several microseconds
+    const int ln = int(threadIdx.x & 31);
     int lo = 0, hi = a.num_req;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (a.tile_indptr[mid] <= tile) lo = mid; else hi = mid;
+    while (hi - lo > 32) {
+      const int step = (hi - lo + 31) >> 5;
+      const int p = lo + ln * step;
+      const bool le = p < hi && __ldg(a.tile_indptr + p) <= tile;
+      const int k = 31 - __clz(__ballot_sync(0xffffffffu, le));  // lane 0's sample is <= tile
+      lo = lo + k * step;
+      hi = min(hi, lo + step);
+    }
+    {
+      const int p = lo + ln;
+      const bool le = p < hi && __ldg(a.tile_indptr + p) <= tile;
+      lo += 31 - __clz(__ballot_sync(0xffffffffu, le));
     }
     const int G = a.group;
     t.q_base = a.qo_indptr[lo];
