@@ -338,6 +338,51 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
   const TileDesc t = describe<DECODE>(a, bx);
   const int n_tiles = (t.key_end - t.key_begin + BN - 1) / BN;
 
+  // Softmax threads: the query row of their TMEM lane, and the gather of
+  // half of Q row i, issued before the barriers and TMEM are set up so the
+  // copies overlap that start-up (nothing else uses the Q buffer yet; the
+  // arrival on the Q barrier follows the CTA-wide sync below).
+  const int wg = warp >> 2;
+  const int i = (warp & 3) * 32 + lane;  // TMEM lane
+  // the tile row in lane i: row i, or with M = 64 products (at most 64
+  // rows) row 16 (i / 32) + i % 16 in the first 16 lanes of each quadrant
+  const bool m64 = t.n_rows <= 64;
+  const int row = m64 ? (((i >> 5) << 4) | (i & 15)) : i;
+  int64_t qi = 0, part = 0;
+  int head = 0, lim = t.key_end;
+  bool valid = false;
+  if (warp < 8) {
+    valid = (!m64 || (i & 16) == 0) && row < t.n_rows;
+    if (valid) row_info<DECODE>(a, t, kvh, row, qi, head, part, lim);
+    // the Q row this thread gathers: tile row i into shared-memory row i
+    // (the A operand's rows, whatever the TMEM layout of the products)
+    int64_t gqi = qi;
+    int ghead = head;
+    bool gvalid = valid;
+    if (m64) {
+      int64_t gpart = 0;
+      int glim = 0;
+      gqi = 0;
+      ghead = 0;
+      gvalid = i < t.n_rows;
+      if (gvalid) row_info<DECODE>(a, t, kvh, i, gqi, ghead, gpart, glim);
+    }
+    // the queries (and, below, the outputs: decode's partial buffers the
+    // previous merge read) are touched only once earlier kernels on the
+    // stream are done; with early inputs the queries are complete already
+    // and only the partial writes wait
+    if (!DECODE || !a.early_inputs) rxk::griddep_wait();
+    // chunks [8 w, 8 w + 8) of Q row i (zeros past the tile's rows) while
+    // the loader warps already stream the first K/V tiles
+    const bf16* src = a.q + (gqi * a.hq + ghead) * D;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      const int ch = wg * (D / 16) + c;
+      rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, gvalid);
+    }
+    rxk::cp_async_commit();
+  }
+
   if (tid == 0) {
     tc::mbar_init(BAR_Q, 8 * 32);  // every softmax thread lands half a Q row
     for (int s = 0; s < NK; ++s) tc::mbar_init(BAR_KF(s), 1);
@@ -587,51 +632,13 @@ __device__ __forceinline__ void tc_tile3(const TcArgs& a, const CUtensorMap* tmk
     // lanes 32 q ..).  Per tile the two halves of a row agree on the row max
     // through shared memory (one bounded mbarrier round), so both write P
     // against the same reference and share one O accumulator.
-    const int wg = warp >> 2;
-    const int i = (warp & 3) * 32 + lane;  // TMEM lane
     constexpr int HALF = BN / 2;
-    // the tile row in lane i: row i, or with M = 64 products (at most 64
-    // rows) row 16 (i / 32) + i % 16 in the first 16 lanes of each quadrant
-    const bool m64 = t.n_rows <= 64;
-    const int row = m64 ? (((i >> 5) << 4) | (i & 15)) : i;
-    int64_t qi = 0, part = 0;
-    int head = 0, lim = t.key_end;
-    const bool valid = (!m64 || (i & 16) == 0) && row < t.n_rows;
-    if (valid) row_info<DECODE>(a, t, kvh, row, qi, head, part, lim);
-    // the Q row this thread gathers: tile row i into shared-memory row i
-    // (the A operand's rows, whatever the TMEM layout of the products)
-    int64_t gqi = qi;
-    int ghead = head;
-    bool gvalid = valid;
-    if (m64) {
-      int64_t gpart = 0;
-      int glim = 0;
-      gqi = 0;
-      ghead = 0;
-      gvalid = i < t.n_rows;
-      if (gvalid) row_info<DECODE>(a, t, kvh, i, gqi, ghead, gpart, glim);
-    }
     const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
     float* xch = reinterpret_cast<float*>(gbase + Lo::XCH);  // [2][2 warpgroups][BM]
-    // the queries and the outputs (decode: partial buffers the previous
-    // merge read) are touched only once earlier kernels on the stream are
-    // done; with early inputs the queries are complete already and only the
-    // partial writes wait (below)
-    if (!DECODE || !a.early_inputs) rxk::griddep_wait();
-    {
-      // chunks [8 w, 8 w + 8) of Q row i (zeros past the tile's rows) while
-      // the loader warp already streams the first K/V tiles
-      const bf16* src = a.q + (gqi * a.hq + ghead) * D;
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        const int ch = wg * (D / 16) + c;
-        rxk::cp_async_16(sw128(sQ, BM, i, ch), src + ch * 8, gvalid);
-      }
-      rxk::cp_async_commit();
-      rxk::cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(BAR_Q);
-    }
+    // the Q gather issued at the start has landed
+    rxk::cp_async_wait<0>();
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive(BAR_Q);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
