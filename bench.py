@@ -79,7 +79,7 @@ TRAFFIC = {
     # launches before they were launched together), summed
     ("long_shared", "rx_extend_attention"): 2230.64e6 + 3158.90e6,
     # one wave's launch (26 batches), from its capture
-    ("fork_tree", "rx_extend_attention"): 982.84e6 + 1269.86e6,
+    ("fork_tree", "rx_extend_attention"): 983.37e6 + 1269.09e6,
     # (69.452 MB read + 0.609 MB written) / 69.865 MB algorithmic on the
     # multi_turn_chat_small launch, times the full workload's 1.0940 GB of
     # algorithmic bytes per decode launch
