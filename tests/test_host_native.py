@@ -914,3 +914,31 @@ def test_extend_wave_failure_keeps_earlier_batches():
     assert st["protected_tokens"] == st["cached_tokens"]
     assert 0 < st["cached_tokens"] <= first
     c.debug_fail_alloc(0)
+
+
+def test_wave_entry_points_validate_before_cuda():
+    """rx_extend_batches, rx_extend_wave and the event calls reject bad
+    arguments before any CUDA call (no GPU needed)."""
+    import ctypes as C
+    pool = rx.rx_pool_desc(16, 16, 8, 1, 2, 128, 0)
+    assert rx._lib.rx_extend_batches(C.byref(pool), 0, 4, None, -1, 1.0, None, None) == rx.RX_ERR_INVALID
+    assert rx._lib.rx_extend_batches(C.byref(pool), 0, 4, None, 2, 1.0, None, None) == rx.RX_ERR_INVALID
+    bad = rx.rx_pool_desc(16, 16, 8, 1, 2, 64, 0)     # head_dim 64 unsupported
+    recs = np.zeros(1, dtype=rx.EXTEND_BATCH_DTYPE)
+    assert rx._lib.rx_extend_batches(C.byref(bad), 0, 4, recs.ctypes.data, 1, 1.0, None,
+                                     None) == rx.RX_ERR_INVALID
+    assert rx._lib.rx_extend_batches(C.byref(pool), 0, 4, recs.ctypes.data, 0, 1.0, None,
+                                     None) == rx.RX_OK
+    assert rx._lib.rx_events_create(-1, None) == rx.RX_ERR_INVALID
+    assert rx._lib.rx_events_create(0, None) == rx.RX_OK
+    assert rx._lib.rx_events_destroy(-1, None) == rx.RX_ERR_INVALID
+    assert rx._lib.rx_event_elapsed_ms(None, None, None) == rx.RX_ERR_INVALID
+    c = rx.RadixCache(64)
+    n = C.c_int32()
+    # a negative wave size, and a wave with no arrays
+    assert rx._lib.rx_extend_wave(c._h, -1, None, None, None, 8, None, C.byref(n), None, None,
+                                  None, None) == rx.RX_ERR_INVALID
+    ind = np.zeros(1, dtype=np.int64)
+    assert rx._lib.rx_extend_wave(c._h, 0, None, ind.ctypes.data, None, 8, None, C.byref(n),
+                                  None, None, None, None) == rx.RX_OK
+    assert n.value == 0
