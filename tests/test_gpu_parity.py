@@ -419,3 +419,51 @@ def test_row_tiles_at_the_64_row_boundary(head_dim, hq, hkv):
     run = DeviceRun(wl)
     run.assert_close()
     assert [m for _, m, _ in run.trace.batches[1]] == [300] * 4
+
+
+def test_rings_with_several_launch_groups_per_wave():
+    """The end-to-end path (inputs replayed from page-locked host memory
+    through the input ring, outputs read back through the output ring)
+    hands its rings over group by group; on a wave split into several launch
+    groups (identical prompts) every output read back equals the output of
+    a run fed from device tensors, on each of two runs."""
+    from radix_tree_prefix_gb300.engine import Engine, GatherInputs, OutputRing, PreparedInputs
+
+    dev = torch.device("cuda:0")
+    wl = _dup_waves()
+    vals = workloads.make_values(wl, dev, [0])
+    want, seen = [], []
+
+    def on_ext(b, rids, prefix, qo, outs):
+        o, lse = (x if x._base is None else x._base for x in outs[0])
+        if seen and seen[-1] == (o.data_ptr(), o.numel()):
+            return
+        seen.append((o.data_ptr(), o.numel()))
+        want.append(torch.cat([o.reshape(-1), lse.reshape(-1)]).clone())
+
+    def on_wave(s, rids, ctx, outs, info):
+        seen.clear()
+        want.append(torch.cat([x.reshape(-1) for x in outs[0]]).clone())
+
+    prepared = PreparedInputs(GatherInputs(wl, vals, [0]))
+    first = Engine(wl, device=dev, inputs=prepared, layers=[0], on_extend=on_ext,
+                   on_decode_wave=on_wave)
+    first.run()
+    prepared.freeze()
+    torch.cuda.synchronize()
+    assert len(want) > 2 * len(wl.waves)          # some wave has several groups
+    host = PreparedInputs(prepared.source, host=True, ring=2)
+    host.adopt(prepared)
+    host.freeze()
+    n = max(w.numel() for w in want)
+    ring = OutputRing(dev, n, slots=len(want))
+    eng = Engine(wl, device=dev, inputs=host, layers=[0], out_ring=ring)
+    for _ in range(2):
+        eng.run()
+        torch.cuda.synchronize()
+        for k, w in enumerate(want):
+            got = ring.host[k].view(0, (w.numel(),), torch.float32)
+            assert torch.equal(got, w.cpu()), k
+    assert rx.device_check() == 0
+    ring.close()
+    host.close()
