@@ -15,6 +15,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # collected on CPU machines, skipped there
     pytest.skip("no CUDA device", allow_module_level=True)
 
+from oracle import attention as oatt  # noqa: E402
 from oracle import pool as opool  # noqa: E402
 from parity_util import DeviceRun  # noqa: E402
 from radix_tree_prefix_gb300 import rx, workloads  # noqa: E402
@@ -467,3 +468,92 @@ def test_rings_with_several_launch_groups_per_wave():
     assert rx.device_check() == 0
     ring.close()
     host.close()
+
+
+def _tile_kinds(rows, prefix, sfx, BM, BN, G):
+    """The kinds of key tiles in the slot rows: 'run' (one run of BN
+    slots), 'mixed' (not one run, but some of its 16-row groups are runs of
+    valid slots: a tile that straddles runs of the pool) or 'gather' (no
+    group is a run)."""
+    kinds = set()
+    for row, p, s in zip(rows, prefix, sfx):
+        per = max(1, BM // G)
+        for r0 in range(0, s, per):
+            kend = p + min(s, r0 + per)
+            for k0 in range(0, kend, BN):
+                sl = np.full(BN, -1)
+                seg = row[k0:min(kend, k0 + BN)]
+                sl[:len(seg)] = seg
+                groups = [sl[g:g + 16] for g in range(0, BN, 16)]
+                ok = [x[0] >= 0 and np.all(np.diff(x) == 1) for x in groups]
+                if len(seg) == BN and np.all(np.diff(sl) == 1):
+                    kinds.add("run")
+                else:
+                    kinds.add("mixed" if any(ok) else "gather")
+    return kinds
+
+
+@pytest.mark.parametrize("head_dim,hq,hkv", [(128, 16, 4), (256, 16, 4), (128, 8, 8)])
+def test_extend_over_slot_rows_of_mixed_runs(head_dim, hq, hkv):
+    """Slot rows made of runs of the pool of mixed lengths (whole 16-row
+    groups, runs of 17 and 100, single slots) give key tiles of one run
+    (box loads), tiles that straddle runs and scattered tiles (gathered slot
+    by slot).  Extend attention over them equals fp64 attention over the
+    same slots."""
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(1700 + head_dim + hkv)
+    N, L, layer = 9000, 2, 1
+    G = hq // hkv
+    BN = 128 if head_dim == 128 else 64
+    kp = (torch.randn(L, hkv, N, head_dim, generator=torch.Generator().manual_seed(5)) * 0.7)
+    vp = torch.randn(L, hkv, N, head_dim, generator=torch.Generator().manual_seed(6))
+    kp, vp = kp.to(torch.bfloat16), vp.to(torch.bfloat16)
+
+    def slot_row(n):
+        out = []
+        while len(out) < n:
+            m = int(rng.choice([16, 32, 48, 128, 17, 100, 1, 3]))
+            a = int(rng.integers(0, N - m))
+            out.extend(range(a, a + m))
+        return np.asarray(out[:n], dtype=np.int32)
+
+    prefix = [0, 300, 517, 64, 1000]
+    sfx = [70, 1, 130, 200, 33]
+    R = len(prefix)
+    W = max(p + s for p, s in zip(prefix, sfx))
+    rows = [slot_row(p + s) for p, s in zip(prefix, sfx)]
+    rows[4][:256] = np.arange(4000, 4256)          # whole tiles of one run
+    assert _tile_kinds(rows, prefix, sfx, 128, BN, G) == {"run", "mixed", "gather"}
+    table = np.zeros((R + 2, W + 5), dtype=np.int32)
+    req_rows = np.array([2, 0, 4, 1, 3], dtype=np.int32)
+    for r in range(R):
+        table[req_rows[r], :len(rows[r])] = rows[r]
+    qo = np.zeros(R + 1, dtype=np.int32)
+    np.cumsum(sfx, out=qo[1:])
+    q = torch.randn(int(qo[-1]), hq, head_dim, generator=torch.Generator().manual_seed(7))
+    q = q.to(torch.bfloat16)
+    tiles, n_tiles = rx.extend_plan(qo, hq, hkv, head_dim)
+
+    kd, vd, qd = kp.to(dev), vp.to(dev), q.to(dev)
+    out = torch.full((int(qo[-1]), hq, head_dim), float("nan"), device=dev)
+    lse = torch.full((int(qo[-1]), hq), float("nan"), device=dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+    pool = rx.pool_desc(kd, vd)
+    rx.extend_attention(pool, layer, qd, hq, i32(table), i32(req_rows), i32(prefix), i32(qo),
+                        i32(tiles), R, n_tiles, head_dim ** -0.5, out, lse)
+    torch.cuda.synchronize()
+    assert rx.device_check() == 0
+    o, ls = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    k64 = kp[layer].double().numpy()
+    v64 = vp[layer].double().numpy()
+    q64 = q.double().numpy()
+    errs = []
+    for r in range(R):
+        sl = rows[r]
+        k = k64[:, sl, :].transpose(1, 0, 2)
+        v = v64[:, sl, :].transpose(1, 0, 2)
+        want_o, want_l = oatt.extend_attention(q64[qo[r]:qo[r + 1]], k, v, prefix[r])
+        errs.append(np.abs(o[qo[r]:qo[r + 1]] - want_o).ravel())
+        errs.append(np.abs(ls[qo[r]:qo[r + 1]] - want_l).ravel())
+    e = np.concatenate(errs)
+    assert e.max() <= 1e-2 and e.mean() <= 1e-3, (e.max(), e.mean())
