@@ -524,6 +524,11 @@ rx_status rx_alloc_decode_steps(rx_cache* cache, int32_t B, int32_t n_steps,
  * Device calls
  * ---------------------------------------------------------------------- */
 
+/* A KV pool, owned by the caller.  Every device call checks it first:
+ * both pointers non-NULL and 16-byte aligned, head_dim 128 or 256,
+ * num_slots >= 2, L and Hkv > 0, and L * Hkv * num_slots < 2^31 (the
+ * kernels address pool rows with 32-bit TMA coordinates); RX_ERR_INVALID
+ * otherwise. */
 typedef struct rx_pool_desc {
   void* k_pool;          /* device bf16 [L][Hkv][num_slots][head_dim]      */
   void* v_pool;          /* same layout                                    */

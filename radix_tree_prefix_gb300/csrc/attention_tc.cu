@@ -1288,10 +1288,13 @@ EncodeTiled encode_fn() {
 }
 
 // Tensor map over a whole pool [L * Hkv * num_slots rows][D] of bf16, box of
-// 64 columns x BN rows, 128-byte swizzle (the shared-memory tile layout).
+// 64 columns x BN rows, 128-byte swizzle (the shared-memory tile layout);
+// false if it cannot be encoded or the pool has 2^31 rows or more.
 bool make_pool_map(CUtensorMap* m, const void* pool, const rx_pool_desc* d, int BN) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
+  // TMA row coordinates are 32-bit signed
+  if (int64_t(d->num_layers) * d->num_kv_heads * d->num_slots > INT32_MAX) return false;
   const cuuint64_t dims[2] = {cuuint64_t(d->head_dim),
                               cuuint64_t(d->num_layers) * d->num_kv_heads * d->num_slots};
   const cuuint64_t strides[1] = {cuuint64_t(d->head_dim) * 2};

@@ -119,6 +119,9 @@ rx_status check_pool(const rx_pool_desc* pool, int32_t layer) {
     return set_error(RX_ERR_INVALID, "head_dim must be 128 or 256");
   if (pool->num_kv_heads <= 0 || pool->num_layers <= 0 || pool->num_slots < 2)
     return set_error(RX_ERR_INVALID, "pool shape invalid");
+  // the attention kernels address pool rows with 32-bit TMA coordinates
+  if (int64_t(pool->num_layers) * pool->num_kv_heads * pool->num_slots > INT32_MAX)
+    return set_error(RX_ERR_INVALID, "pool has 2^31 rows (layers x KV heads x slots) or more");
   if (layer < 0 || layer >= pool->num_layers)
     return set_error(RX_ERR_INVALID, "layer out of range");
   if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool))

@@ -54,6 +54,17 @@ def test_argument_errors_need_no_gpu():
     st = rx._lib.rx_extend_attention(C.byref(bad), 3, None, 4, None, 0, None, None, None,
                                      None, 1, 1, 1.0, None, None, None)
     assert st == rx.RX_ERR_INVALID and "layer" in rx.last_error()
+    # pool rows (layers x KV heads x slots) must stay below 2^31, the range
+    # of the kernels' TMA row coordinates
+    big = rx.rx_pool_desc(16, 16, 2 ** 28, 4, 2, 128, 0)     # 2^31 rows
+    st = rx._lib.rx_extend_attention(C.byref(big), 0, None, 4, None, 0, None, None, None,
+                                     None, 0, 0, 1.0, None, None, None)
+    assert st == rx.RX_ERR_INVALID and "2^31" in rx.last_error()
+    st = rx._lib.rx_kv_store(C.byref(big), 0, None, None, None, 0, None)
+    assert st == rx.RX_ERR_INVALID
+    under = rx.rx_pool_desc(16, 16, 2 ** 28 - 1, 4, 2, 128, 0)
+    assert rx._lib.rx_extend_attention(C.byref(under), 0, None, 4, None, 0, None, None, None,
+                                       None, 0, 0, 1.0, None, None, None) == rx.RX_OK
     h = C.c_void_p()
     for slots, ps in ((9, 2), (8, 0), (3, 4)):    # page size must divide the slot count
         cfg = rx.rx_config(slots, ps, 0)
