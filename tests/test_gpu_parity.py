@@ -557,3 +557,69 @@ def test_extend_over_slot_rows_of_mixed_runs(head_dim, hq, hkv):
         errs.append(np.abs(ls[qo[r]:qo[r + 1]] - want_l).ravel())
     e = np.concatenate(errs)
     assert e.max() <= 1e-2 and e.mean() <= 1e-3, (e.max(), e.mean())
+
+
+@pytest.mark.parametrize("head_dim,hq,hkv", [(128, 16, 4), (256, 16, 4)])
+def test_pool_rows_outside_the_slots_are_never_read(head_dim, hq, hkv):
+    """No kernel reads a pool row that the slot rows do not name: with every
+    other row NaN, extend attention over slot rows with ragged runs (partial
+    last key tiles inside one run, tiles that straddle runs) equals fp64
+    attention, and equals bit for bit the same call on a pool whose other
+    rows are zero."""
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(2900 + head_dim)
+    N = 6000
+    prefix = [200, 0, 333, 90]
+    sfx = [57, 300, 41, 129]
+    rows = [np.arange(1000, 1257, dtype=np.int32),              # one ragged run
+            np.arange(2000, 2300, dtype=np.int32)]
+    for p, s in zip(prefix[2:], sfx[2:]):
+        out = []
+        while len(out) < p + s:
+            m = int(rng.choice([16, 64, 100, 7]))
+            a = int(rng.integers(3000, N - m))
+            out.extend(range(a, a + m))
+        rows.append(np.asarray(out[:p + s], dtype=np.int32))
+    used = np.unique(np.concatenate(rows))
+    gen = torch.Generator().manual_seed(11)
+    kp = torch.full((1, hkv, N, head_dim), float("nan"))
+    vp = torch.full((1, hkv, N, head_dim), float("nan"))
+    kp[:, :, used] = torch.randn(1, hkv, len(used), head_dim, generator=gen) * 0.7
+    vp[:, :, used] = torch.randn(1, hkv, len(used), head_dim, generator=gen)
+    kp, vp = kp.to(torch.bfloat16), vp.to(torch.bfloat16)
+    R = len(rows)
+    W = max(len(r) for r in rows)
+    table = np.zeros((R, W), dtype=np.int32)
+    for r in range(R):
+        table[r, :len(rows[r])] = rows[r]
+    qo = np.zeros(R + 1, dtype=np.int32)
+    np.cumsum(sfx, out=qo[1:])
+    q = (torch.randn(int(qo[-1]), hq, head_dim, generator=gen)).to(torch.bfloat16)
+    tiles, n_tiles = rx.extend_plan(qo, hq, hkv, head_dim)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+    args = (i32(table), i32(np.arange(R)), i32(prefix), i32(qo), i32(tiles))
+
+    def run(kd, vd):
+        out = torch.empty((int(qo[-1]), hq, head_dim), device=dev)
+        lse = torch.empty((int(qo[-1]), hq), device=dev)
+        rx.extend_attention(rx.pool_desc(kd, vd), 0, q.to(dev), hq,
+                            args[0], args[1], args[2], args[3], args[4], R, n_tiles,
+                            head_dim ** -0.5, out, lse)
+        torch.cuda.synchronize()
+        assert rx.device_check() == 0
+        return out, lse
+
+    o, ls = run(kp.to(dev), vp.to(dev))
+    assert torch.isfinite(o).all() and torch.isfinite(ls).all()
+    k64, v64 = kp[0].double().numpy(), vp[0].double().numpy()
+    q64 = q.double().numpy()
+    on, lsn = o.double().cpu().numpy(), ls.double().cpu().numpy()
+    for r in range(R):
+        k = k64[:, rows[r], :].transpose(1, 0, 2)
+        v = v64[:, rows[r], :].transpose(1, 0, 2)
+        want_o, want_l = oatt.extend_attention(q64[qo[r]:qo[r + 1]], k, v, prefix[r])
+        assert np.abs(on[qo[r]:qo[r + 1]] - want_o).max() <= 1e-2
+        assert np.abs(lsn[qo[r]:qo[r + 1]] - want_l).max() <= 1e-2
+    kz, vz = kp.nan_to_num(0.0).to(dev), vp.nan_to_num(0.0).to(dev)
+    o0, l0 = run(kz, vz)
+    assert torch.equal(o0, o) and torch.equal(l0, ls)
