@@ -42,6 +42,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "ptx_util.cuh"
 #include "rx.h"
@@ -1344,16 +1345,37 @@ bool pool_maps(const rx_pool_desc* d, int BN, const CUtensorMap** mk, const CUte
   return true;
 }
 
+// A kernel's dynamic shared-memory limit is an attribute of the kernel in
+// the current device's context: it is raised once per device (any thread
+// may do it first; setting it twice is harmless).
+constexpr int kMaxDevices = 64;
+
+template <typename K>
+rx_status ensure_smem(std::atomic<bool> (&done)[kMaxDevices], K* kernel, int bytes) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return rx_internal::set_error(RX_ERR_CUDA, "no usable current device");
+  if (done[dev].load(std::memory_order_acquire)) return RX_OK;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // not left for a later launch check to report
+    static thread_local char buf[160];
+    snprintf(buf, sizeof(buf), "raising a kernel's shared-memory limit: %s",
+             cudaGetErrorString(e));
+    return rx_internal::set_error(RX_ERR_CUDA, buf);
+  }
+  done[dev].store(true, std::memory_order_release);
+  return RX_OK;
+}
+
 template <int D>
 rx_status launch_extend(TcArgs a, const rx_pool_desc* pool, int32_t layer, unsigned gx,
                         unsigned gy, cudaStream_t s) {
   using Lo = Layout3<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(attn_tc3_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Lo::BYTES);
-    configured = true;
-  }
+  static std::atomic<bool> configured[kMaxDevices];
+  const rx_status cs = ensure_smem(configured, attn_tc3_kernel<D>, Lo::BYTES);
+  if (cs != RX_OK) return cs;
   const CUtensorMap *tmk, *tmv;
   if (!pool_maps(pool, Lo::BN, &tmk, &tmv))
     return rx_internal::set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
@@ -1435,16 +1457,11 @@ rx_status decode_fused(const rx_pool_desc* pool, int32_t layer, const void* d_q,
   a.slots_new = slots_new;
   a.tma_row_base = int64_t(layer) * hkv * pool->num_slots;
   a.tma_head_rows = pool->num_slots;
-  static bool configured[2] = {false, false};
-  if (!configured[D == 256]) {
-    if (D == 128)
-      cudaFuncSetAttribute(decode_fused_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Fused<128>::SMEM);
-    else
-      cudaFuncSetAttribute(decode_fused_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Fused<256>::SMEM);
-    configured[D == 256] = true;
-  }
+  static std::atomic<bool> configured128[kMaxDevices], configured256[kMaxDevices];
+  const rx_status cs =
+      D == 128 ? ensure_smem(configured128, decode_fused_kernel<128>, Fused<128>::SMEM)
+               : ensure_smem(configured256, decode_fused_kernel<256>, Fused<256>::SMEM);
+  if (cs != RX_OK) return cs;
   const CUtensorMap *tmk, *tmv;
   if (!pool_maps(pool, D == 128 ? 128 : 64, &tmk, &tmv))
     return set_error(RX_ERR_CUDA, "could not encode the pool's TMA tensor maps");
