@@ -953,3 +953,40 @@ def test_wave_entry_points_validate_before_cuda():
     assert rx._lib.rx_extend_wave(c._h, 0, None, ind.ctypes.data, None, 8, None, C.byref(n),
                                   None, None, None, None) == rx.RX_OK
     assert n.value == 0
+
+
+def test_extend_plan_counts_row_tiles():
+    """rx_extend_plan: request r has s_r x G rows per KV head (its suffix
+    tokens times the query heads sharing a KV head), cut into tiles of 128
+    rows; an empty suffix has no tile.  Counts checked against that formula
+    on ragged suffixes, and bad arguments rejected."""
+    import ctypes as C
+    rng = np.random.default_rng(5)
+    for hq, hkv in ((32, 8), (16, 4), (8, 8), (64, 8)):
+        G = hq // hkv
+        s = rng.integers(0, 700, size=40)
+        s[[3, 17]] = 0
+        s[5], s[6], s[7] = 128 // G, 128 // G + 1, 1
+        qo = np.zeros(len(s) + 1, dtype=np.int32)
+        np.cumsum(s, out=qo[1:])
+        for d in (128, 256):
+            tiles, n = rx.extend_plan(qo, hq, hkv, d)
+            want = np.zeros(len(s) + 1, dtype=np.int64)
+            np.cumsum(-(-s * G // 128), out=want[1:])
+            assert tiles.tolist() == want.tolist() and n == want[-1]
+    tiles, n = rx.extend_plan(np.zeros(1, dtype=np.int32), 32, 8, 128)
+    assert tiles.tolist() == [0] and n == 0
+    for qo, hq, hkv, d in (([0, 5, 3], 32, 8, 128),     # not monotone
+                           ([0, 5], 30, 8, 128),        # Hq % Hkv != 0
+                           ([0, 5], 32, 8, 64)):        # head_dim
+        with pytest.raises(rx.RxError) as e:
+            rx.extend_plan(np.asarray(qo, dtype=np.int32), hq, hkv, d)
+        assert e.value.status == rx.RX_ERR_INVALID
+    out = np.zeros(3, dtype=np.int32)
+    # at G = 256 two tiles per suffix token: 2^32 tiles overflow the int32 plan
+    big = np.array([0, 2 ** 30 - 64, 2 ** 31 - 1], dtype=np.int32)
+    n = C.c_int64()
+    assert rx._lib.rx_extend_plan(big.ctypes.data, 1, 2048, 8, 128, out.ctypes.data,
+                                  C.byref(n)) == rx.RX_OK and n.value == 2 ** 31 - 128
+    assert rx._lib.rx_extend_plan(big.ctypes.data, 2, 2048, 8, 128, out.ctypes.data,
+                                  C.byref(n)) == rx.RX_ERR_INVALID
