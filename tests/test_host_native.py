@@ -990,3 +990,66 @@ def test_extend_plan_counts_row_tiles():
                                   C.byref(n)) == rx.RX_OK and n.value == 2 ** 31 - 128
     assert rx._lib.rx_extend_plan(big.ctypes.data, 2, 2048, 8, 128, out.ctypes.data,
                                   C.byref(n)) == rx.RX_ERR_INVALID
+
+
+def test_device_entry_points_reject_bad_arguments_without_a_gpu():
+    """Each remaining device call rejects bad arguments (and returns at once
+    on empty work) before any CUDA call, so none of this needs a GPU: slot
+    table writes, decode (plain, static scratch, multi-step), verification,
+    KV copies and page-locked allocations."""
+    import ctypes as C
+    L = rx._lib
+    INV, OK = rx.RX_ERR_INVALID, rx.RX_OK
+    pool = rx.rx_pool_desc(16, 16, 64, 2, 2, 128, 0)
+    bad = rx.rx_pool_desc(16, 16, 64, 2, 2, 64, 0)            # head_dim 64
+    other = rx.rx_pool_desc(32, 32, 64, 2, 4, 128, 0)         # other head count
+    fake = 16                                                  # never dereferenced
+    # req_to_token writes
+    assert L.rx_req_to_token_write(fake, 4, 8, fake, fake, fake, -1, None) == INV
+    assert L.rx_req_to_token_write(fake, 4, 0, fake, fake, fake, 1, None) == INV
+    assert L.rx_req_to_token_write(fake, -1, 8, fake, fake, fake, 1, None) == INV
+    assert L.rx_req_to_token_write(None, 4, 8, fake, fake, fake, 1, None) == INV
+    assert L.rx_req_to_token_write(None, 4, 8, None, None, None, 0, None) == OK
+    # decode and verification (the same checks)
+    info = rx.rx_decode_plan_info()
+    info.workspace_bytes = 4096
+    for fn in (L.rx_decode_attention, L.rx_verify_attention):
+        def call(p, hq=8, i=C.byref(info), B=1, q=fake, ws=fake, wsb=4096):
+            return fn(C.byref(p), 0, q, hq, fake, 8, fake, i, B, 1.0, fake, fake, ws, wsb, None)
+        assert call(bad) == INV and "head_dim" in rx.last_error()
+        assert call(pool, hq=7) == INV                      # Hq % Hkv != 0
+        assert call(pool, i=None) == INV                    # no plan info
+        assert call(pool, B=-1) == INV
+        assert call(pool, B=0) == OK                        # nothing to do
+        assert call(pool, wsb=4095) == INV and "workspace" in rx.last_error()
+        assert call(pool, ws=None) == INV
+        assert call(pool, ws=fake + 8) == INV               # misaligned workspace
+        assert call(pool, q=None) == INV
+    # decode with the library's static scratch: a plan larger than it
+    assert L.rx_decode_attention_static(C.byref(pool), 0, fake, 8, fake, 8, fake, None, 1, 1.0,
+                                        fake, fake, None) == INV
+    info.workspace_bytes = 16 * 2 ** 20 + 1
+    assert L.rx_decode_attention_static(C.byref(pool), 0, fake, 8, fake, 8, fake,
+                                        C.byref(info), 1, 1.0, fake, fake, None) == INV
+    assert "static" in rx.last_error()
+    # multi-step decode
+    assert L.rx_decode_steps(C.byref(pool), 0, 8, fake, 8, None, -1, 1, 1.0, fake, 0,
+                             None) == INV
+    assert L.rx_decode_steps(C.byref(pool), 0, 8, fake, 8, None, 2, 1, 1.0, fake, 0,
+                             None) == INV
+    steps = (rx.rx_decode_step * 1)()
+    assert L.rx_decode_steps(C.byref(bad), 0, 8, fake, 8, steps, 1, 1, 1.0, fake, 0,
+                             None) == INV
+    assert L.rx_decode_steps(C.byref(pool), 0, 6, fake, 8, steps, 1, 1, 1.0, fake, 0,
+                             None) == INV                   # Hq % Hkv != 0
+    # KV copies between pools
+    assert L.rx_kv_copy(C.byref(pool), C.byref(bad), fake, fake, 1, None) == INV
+    assert L.rx_kv_copy(C.byref(pool), C.byref(other), fake, fake, 1, None) == INV
+    assert "shape" in rx.last_error()
+    assert L.rx_kv_copy(C.byref(pool), C.byref(pool), fake, fake, -1, None) == INV
+    assert L.rx_kv_copy(C.byref(pool), C.byref(pool), None, None, 0, None) == OK
+    assert L.rx_kv_copy(C.byref(pool), C.byref(pool), None, fake, 1, None) == INV
+    # page-locked host allocations
+    out = C.c_void_p()
+    assert L.rx_host_alloc(0, C.byref(out)) == INV
+    assert L.rx_host_alloc(64, None) == INV
