@@ -543,7 +543,8 @@ typedef struct rx_pool_desc {
  * cache): K_pool[layer][h][d_slots[i]][:] = d_k[i][h][:], same for V, for
  * i < T.  d_k, d_v: device bf16 [T][Hkv][head_dim], 16-byte aligned.
  * Slots must be distinct.  A slot outside [1, num_slots) is skipped on the
- * device and reported by rx_device_check (bit 0). */
+ * device and reported by rx_device_check (bit 0).  Errors: RX_ERR_INVALID
+ * (the pool, T < 0, NULL or misaligned inputs); T = 0 launches nothing. */
 rx_status rx_kv_store(const rx_pool_desc* pool, int32_t layer,
                       const int32_t* d_slots, const void* d_k,
                       const void* d_v, int64_t T, rx_stream_t stream);
@@ -553,7 +554,8 @@ rx_status rx_kv_store(const rx_pool_desc* pool, int32_t layer,
  * is device int32 [num_rows][row_stride]; d_rows, d_pos, d_slots device
  * int32 [n].  An entry whose row is outside [0, num_rows) or whose position
  * is outside [0, row_stride) is skipped on the device and reported by
- * rx_device_check (bit 4). */
+ * rx_device_check (bit 4).  Errors: RX_ERR_INVALID (n < 0, num_rows < 0,
+ * row_stride <= 0, a NULL array when n > 0); n = 0 launches nothing. */
 rx_status rx_req_to_token_write(int32_t* d_table, int64_t num_rows,
                                 int64_t row_stride, const int32_t* d_rows,
                                 const int32_t* d_pos, const int32_t* d_slots,
@@ -561,7 +563,10 @@ rx_status rx_req_to_token_write(int32_t* d_table, int64_t num_rows,
 
 /* Host tile schedule for rx_extend_attention: tile_indptr[R+1] = prefix sums
  * of the query-row tiles of each request (request r has
- * (qo_indptr[r+1]-qo_indptr[r]) * Hq/Hkv rows per KV head). */
+ * (qo_indptr[r+1]-qo_indptr[r]) * Hq/Hkv rows per KV head, in tiles of 128
+ * rows; an empty suffix has none).  Errors: RX_ERR_INVALID (NULL arrays,
+ * R < 0, Hq % Hkv != 0, head_dim not 128 or 256, qo_indptr decreasing, 2^31
+ * tiles or more). */
 rx_status rx_extend_plan(const int32_t* qo_indptr, int32_t R,
                          int32_t num_q_heads, int32_t num_kv_heads,
                          int32_t head_dim, int32_t* tile_indptr,
@@ -661,7 +666,9 @@ rx_status rx_decode_attention(const rx_pool_desc* pool, int32_t layer,
  * steps[s].d_slots[b], then reads the chunk; the result is the same.  The
  * req_to_token rows must already hold every step's slots (a token's position
  * beyond a step's context is never read by that step).  d_workspace must hold
- * the largest steps[s].info->workspace_bytes.  Stops at the first error. */
+ * the largest steps[s].info->workspace_bytes.  Stops at the first error.
+ * Errors: RX_ERR_INVALID (n_steps < 0, steps NULL, the pool, Hq % Hkv != 0,
+ * and each step's as in rx_decode_attention). */
 typedef struct rx_decode_step {
   const void* d_q;          /* bf16 [B][Hq][head_dim]                     */
   const void* d_k;          /* bf16 [B][Hkv][head_dim] new tokens' K      */
@@ -769,7 +776,9 @@ rx_status rx_kv_copy(const rx_pool_desc* src, const rx_pool_desc* dst,
  * for host buffers that copies to and from the device run asynchronously
  * with.  Released with rx_host_free.  This is host memory: the library still
  * allocates no device memory.  Errors: RX_ERR_INVALID (bytes 0, out NULL),
- * RX_ERR_CUDA (the allocation failed; *out = NULL). */
+ * RX_ERR_CUDA (the allocation failed; *out = NULL).  rx_host_free(NULL)
+ * does nothing; freeing anything but a pointer from rx_host_alloc is
+ * RX_ERR_CUDA. */
 rx_status rx_host_alloc(size_t bytes, void** out);
 rx_status rx_host_free(void* p);
 
