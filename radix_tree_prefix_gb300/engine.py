@@ -12,14 +12,23 @@ Every cache decision is taken by the C++ library and every tensor operation
 of the method by the CUDA kernels; this module only moves arrays between
 them.  Per wave of requests:
 
-* extend batches: consecutive requests join the open batch until one shares
-  more with a member than its own tree match; ``rx_extend_begin`` (match +
-  lock + one allocation) -> upload of the batch's req_to_token rows ->
-  ``rx_kv_store`` + ``rx_extend_attention`` per layer -> ``rx_extend_end``
-  (insert the prompt, move the lock to the prompt's node);
-* ``decode_steps`` decode steps over the whole wave: ``rx_alloc`` one slot per
-  request -> device row append -> ``rx_kv_store`` -> ``rx_plan_decode`` ->
-  ``rx_decode_attention`` per layer;
+* extend: ``rx_extend_wave`` makes the bookkeeping of every extend batch of
+  the wave in one native call (consecutive requests join the open batch
+  until one shares more with a member than its own tree match; per batch:
+  match, lock, one allocation, then insert of the prompt and the lock moved
+  to the prompt's node); one staged upload carries every batch's
+  req_to_token rows and tile plans; then per layer ``rx_extend_batches``
+  launches, batch group by batch group, ``rx_kv_store`` and
+  ``rx_extend_attention`` on one stream (with a host tier or chunked
+  prefill the per-batch calls ``rx_batch_end`` / ``rx_extend_begin`` /
+  ``rx_extend_end`` are used instead);
+* decode: the wave's ``decode_steps`` steps are allocated at once
+  (``rx_alloc_steps``; ``rx_alloc_decode_steps`` with pages), appended to
+  the device rows (``rx_req_to_token_write``) and planned once
+  (``rx_plan_decode_steps``: the tree does not change while the wave
+  decodes); per layer ``rx_decode_steps`` runs every step (new token's K/V
+  stored, attention over shared segments and private tails, log-sum-exp
+  merge);
 * finish: ``rx_finish`` (insert prompt + outputs, unlock).
 """
 
