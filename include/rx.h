@@ -35,12 +35,16 @@
  *   - The library owns the tree (opaque rx_cache).  The caller owns every host
  *     array and every device buffer (raw pointers, e.g. from torch tensors)
  *     and the CUDA stream.  The library never allocates device memory and
- *     creates no streams or events: every kernel runs on the caller's
- *     stream, in call order.
+ *     creates no streams; it creates events only when asked to
+ *     (rx_events_create).  Every kernel runs on the caller's stream, in call
+ *     order.
  *   - Host calls are synchronous and not thread-safe for one cache.  Device
  *     calls only enqueue work on the given stream (cudaStream_t passed as
  *     rx_stream_t; NULL is the legacy default stream) and return RX_ERR_CUDA
- *     if the launch itself fails.
+ *     if the launch itself fails.  They may be made from several threads and
+ *     on several devices at once (the library's per-device and per-thread
+ *     state is set up safely); rx_decode_attention_static is the exception
+ *     (one scratch array per device).
  *   - Token ids and slots are int32.  Slot 0 is a pad slot that the allocator
  *     never hands out; kernels read it for out-of-range keys only as a
  *     harmless address and mask the value.
