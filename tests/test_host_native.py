@@ -1053,3 +1053,82 @@ def test_device_entry_points_reject_bad_arguments_without_a_gpu():
     out = C.c_void_p()
     assert L.rx_host_alloc(0, C.byref(out)) == INV
     assert L.rx_host_alloc(64, None) == INV
+
+
+def _planned_wave(wl, wave_index, n_steps):
+    """The wave's prompts inserted and locked in a fresh cache (earlier waves
+    first, so later turns share their history), then one multi-step plan."""
+    c = rx.RadixCache(sum(len(wl.prompt_tokens(r)) for w in wl.waves for r in w) + 4096)
+    for w in wl.waves[:wave_index]:
+        for r in w:
+            toks = wl.prompt_tokens(r)
+            slots, _ = c.match_prefix(toks)
+            c.insert(toks, np.concatenate([slots, c.alloc(len(toks) - len(slots))]))
+    nodes, lens = [], []
+    for r in wl.waves[wave_index]:
+        toks = wl.prompt_tokens(r)
+        slots, _ = c.match_prefix(toks)
+        _, node = c.insert(toks, np.concatenate([slots, c.alloc(len(toks) - len(slots))]))
+        c.lock(node)
+        nodes.append(node)
+        lens.append(len(toks) + 1)
+    B = len(nodes)
+    plan, info = c.plan_decode(nodes, lens, list(range(B)), wl.num_q_heads, wl.num_kv_heads,
+                               wl.head_dim, n_steps=n_steps)
+    W = rx.RX_WORK_WORDS
+    work = plan[info.off_work:info.off_work + info.n_work * W].reshape(-1, W).astype(np.int64)
+    members = plan[info.off_members:info.off_members + info.n_member_entries]
+    return work, members, info, lens
+
+
+@pytest.mark.parametrize("name", ["long_shared", "chat_turn_3"])
+def test_decode_plan_sizes_its_work_items(name):
+    """The decode planner's sizing rules: warp-role items (listed first) hold
+    at most 16 query rows (8 at head_dim 256), tensor-core items at most 128
+    and key chunks of whole key tiles (128 keys, 64 at head_dim 256) except
+    at a segment's end; tile CTAs (items x KV heads) stay within 128; each
+    group runs heaviest first; every request's context over all steps is
+    covered once.  On long_shared the 32,768-token prefix of 64 requests
+    (512 rows per KV head: four blocks of 128) is cut into chunks of 8 keys
+    per row doubled until 128 tile CTAs remain: 8,192 keys."""
+    T = 4
+    if name == "long_shared":
+        wl = workloads.long_shared(decode_steps=T)
+        work, members, info, lens = _planned_wave(wl, 0, T)
+    else:
+        wl = workloads.multi_turn_chat(sessions=64, turns=3, decode_steps=T, layers=1)
+        work, members, info, lens = _planned_wave(wl, 2, T)
+    G = wl.num_q_heads // wl.num_kv_heads
+    small_rows = 16 if wl.head_dim == 128 else 8
+    step = 128 if wl.head_dim == 128 else 64
+    n_tc = int(info.n_work_tc)
+    warp, tile = work[:len(work) - n_tc], work[len(work) - n_tc:]
+    assert n_tc > 0 and len(warp) > 0
+    assert (warp[:, 6] <= small_rows).all() and (warp[:, 6] == warp[:, 4] * G).all()
+    assert (tile[:, 6] <= 128).all() and (tile[:, 6] > 32).all()
+    assert n_tc * wl.num_kv_heads <= 128
+    for grp in (warp, tile):
+        weight = (grp[:, 2] - grp[:, 1]) * grp[:, 4]
+        assert (np.diff(weight) <= 0).all()
+    # tile chunks: whole key tiles except the last chunk of a segment
+    seg_end = {}
+    for row, kb, ke, *_ in tile:
+        seg_end[row] = max(seg_end.get(row, 0), ke)
+    for row, kb, ke, *_ in tile:
+        assert (ke - kb) % step == 0 or ke == seg_end[row]
+    # coverage: each request's keys 0 .. ctx + T - 1 once (the private tail
+    # of the last step included)
+    covered = {b: [] for b in range(len(lens))}
+    for row, kb, ke, moff, nm, *_ in work:
+        for i in range(nm):
+            covered[int(members[moff + i])].append((kb, ke))
+    for b, rng_ in covered.items():
+        pos = 0
+        for kb, ke in sorted(rng_):
+            assert kb == pos
+            pos = ke
+        assert pos == lens[b] + T - 1
+    if name == "long_shared":
+        assert info.n_shared_segments == 1
+        assert len(tile) == 16 and n_tc * wl.num_kv_heads == 128
+        assert sorted(set((tile[:, 2] - tile[:, 1]).tolist())) == [8192]
