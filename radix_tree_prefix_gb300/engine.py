@@ -40,6 +40,24 @@ import numpy as np
 from . import rx
 
 
+def launch_groups(rewritten):
+    """Launch groups of a wave's nb extend batches, as batch boundaries
+    [0, .., nb]: a group ends after a batch whose rows rx_extend_end
+    rewrote (``rewritten[b] > 0``), and at the wave's last batch."""
+    nb = len(rewritten)
+    return [0] + [b + 1 for b in range(nb - 1) if rewritten[b] > 0] + [nb]
+
+
+def cut_per_group(x, go):
+    """``x``: R + 1 prefix sums over a wave's requests; ``go``: the groups'
+    request boundaries [0, .., R].  Returns every group's R_g + 1 entries,
+    rebased to start at 0, concatenated (group g's at position go[g] + g)."""
+    cnt = np.diff(go) + 1
+    first = np.repeat(np.cumsum(cnt) - cnt, cnt)
+    idx = np.repeat(go[:-1], cnt) + (np.arange(int(cnt.sum())) - first)
+    return x[idx] - np.repeat(x[go[:-1]], cnt)
+
+
 class Trace:
     """The bookkeeping decisions, in the same form as the oracle's trace."""
 
@@ -847,8 +865,7 @@ class Engine:
         reuse only after its attention ran (one stream)."""
         wl = self.wl
         R, nb = len(wave), len(bounds) - 1
-        rew = self._w_rew[:nb]
-        gb = [0] + [b + 1 for b in range(nb - 1) if rew[b] > 0] + [nb]
+        gb = launch_groups(self._w_rew[:nb])
         gbounds = [bounds[g] for g in gb]
         ng = len(gb) - 1
         # query offsets and tile plans of the whole wave (a request's tiles
@@ -858,11 +875,8 @@ class Engine:
         np.cumsum(sfx, out=qo_w[1:])
         tiles_w, _ = rx.extend_plan(qo_w, wl.num_q_heads, wl.num_kv_heads, wl.head_dim)
         go = np.asarray(gbounds, dtype=np.int64)
-        cnt = np.diff(go) + 1
-        first = np.repeat(np.cumsum(cnt) - cnt, cnt)
-        idx = np.repeat(go[:-1], cnt) + (np.arange(R + ng) - first)
-        qo_c = qo_w[idx] - np.repeat(qo_w[go[:-1]], cnt)
-        tiles_c = tiles_w[idx] - np.repeat(tiles_w[go[:-1]], cnt)
+        qo_c = cut_per_group(qo_w, go)
+        tiles_c = cut_per_group(tiles_w, go)
         W = rows.shape[1]
         d_rows, d_prefix, d_qo, d_tiles, d_slots, d_tab = self.staging.upload([
             np.arange(R, dtype=np.int32), prefix, qo_c, tiles_c, new_slots, rows.ravel()])

@@ -1132,3 +1132,41 @@ def test_decode_plan_sizes_its_work_items(name):
         assert info.n_shared_segments == 1
         assert len(tile) == 16 and n_tc * wl.num_kv_heads == 128
         assert sorted(set((tile[:, 2] - tile[:, 1]).tolist())) == [8192]
+
+
+def test_launch_groups_and_their_plans():
+    """A wave's extend batches merge into launch groups that end after each
+    batch whose rows were rewritten (and at the wave's end); each group's
+    query offsets and tile plan, cut from the whole wave's, equal those of
+    the group's requests planned alone."""
+    from radix_tree_prefix_gb300.engine import cut_per_group, launch_groups
+    assert launch_groups(np.array([0, 0, 0])) == [0, 3]
+    assert launch_groups(np.array([0, 2, 0, 1])) == [0, 2, 4]   # the last batch ends anyway
+    assert launch_groups(np.array([1])) == [0, 1]
+    assert launch_groups(np.array([1, 1, 1])) == [0, 1, 2, 3]
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        R = int(rng.integers(1, 40))
+        sfx = rng.integers(0, 300, size=R)
+        sfx[rng.random(R) < 0.1] = 0
+        cuts = np.sort(rng.choice(np.arange(1, R), size=min(R - 1, int(rng.integers(0, 8))),
+                                  replace=False)) if R > 1 else np.array([], dtype=np.int64)
+        bounds = [0] + cuts.tolist() + [R]
+        rew = (rng.random(len(bounds) - 1) < 0.3).astype(np.int64)
+        gb = launch_groups(rew)
+        assert gb[0] == 0 and gb[-1] == len(bounds) - 1 and gb == sorted(set(gb))
+        go = np.asarray([bounds[g] for g in gb], dtype=np.int64)
+        qo_w = np.zeros(R + 1, dtype=np.int32)
+        np.cumsum(sfx, out=qo_w[1:])
+        hq, hkv = [(32, 8), (16, 4), (8, 8)][trial % 3]
+        tiles_w, _ = rx.extend_plan(qo_w, hq, hkv, 128)
+        qo_c, tiles_c = cut_per_group(qo_w, go), cut_per_group(tiles_w, go)
+        assert len(qo_c) == R + len(go) - 1
+        for g in range(len(go) - 1):
+            j0, j1 = int(go[g]), int(go[g + 1])
+            want_qo = np.zeros(j1 - j0 + 1, dtype=np.int64)
+            np.cumsum(sfx[j0:j1], out=want_qo[1:])
+            want_tiles, _ = rx.extend_plan(want_qo.astype(np.int32), hq, hkv, 128)
+            at = j0 + g
+            assert qo_c[at:at + j1 - j0 + 1].tolist() == want_qo.tolist()
+            assert tiles_c[at:at + j1 - j0 + 1].tolist() == want_tiles.tolist()
