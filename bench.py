@@ -277,6 +277,8 @@ def oracle_rate(wl, budget_s=12.0, seed=0, booked=None, n_requests=8):
         "value": total_q / est,
         "unit": "query-tok/s",
         "cores": 1,
+        "host_cpus": os.cpu_count(),
+        "blas_threads": int(os.environ.get("OPENBLAS_NUM_THREADS", "1")),
         "kind": "oracle",
         "sample": (f"bookkeeping of the whole workload ({t_book:.2f} s) + fp64 attention, layer "
                    f"0, all {wl.num_q_heads} heads, of {done} queries drawn from {len(pick)} "
@@ -312,8 +314,9 @@ def run_reference(args, rank, world):
         "ms_per_step": 1000.0 * wall / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl, world),
-        "cpu_baseline": {"value": value, "unit": "query-tok/s", "cores": 1, "kind": "oracle",
-                         "sample": r["sample"] + f"; mean of {args.steps} steps"},
+        "cpu_baseline": {"value": value, "unit": "query-tok/s", "cores": 1,
+                         "host_cpus": r["host_cpus"], "blas_threads": r["blas_threads"],
+                         "kind": "oracle", "sample": r["sample"] + f"; mean of {args.steps} steps"},
         "e2e": {"value": value, "unit": "query-tok/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -39,6 +39,8 @@ def test_reference_arm_prints_the_contract_line(monkeypatch):
     from radix_tree_prefix_gb300 import workloads
     assert d["config"] == bench.config_of(workloads.nested_share(), 1)
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["host_cpus"] == os.cpu_count()
+    assert d["cpu_baseline"]["blas_threads"] == 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
